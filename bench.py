@@ -1,0 +1,337 @@
+"""Benchmark: Falcon-1 chunked forward on GB300 (tokens/s and roofline).
+
+Workload (one step = one chunked forward over one batch of synthetic
+inputs): Falcon-1, B=8, T=2048, H=12, d_k=d_v=64, bf16 q/k/v/o, fp32 state,
+chunk 64 — the layer shape of the pages' 124-130M-parameter models.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one replica per GPU (weak scaling: each rank
+processes its own batch; the path has no exchange step, so there is no
+data-path collective).  Timing: W untimed steps, then K steps between a
+barrier + synchronize on both sides, CUDA events on the launching stream,
+max over ranks.  The inputs of one step (~102 MB) fit in L2 (129 MB), so the
+steps rotate through 4 input sets (~410 MB) and each step reads inputs that
+the previous steps evicted.  Rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+N_SETS = 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="lm124m_f1_8x2048x12_d64")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+def get_workload(name):
+    from workloads import WORKLOADS
+    for w in WORKLOADS:
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}")
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes the method must move per forward: q, k, v in and o out in the
+    input dtype, beta and lambda in fp32, the final state once in fp32."""
+    es = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.T * w.H
+    beta = th * (w.dv if w.per_channel else 1) * 4
+    return th * (2 * w.dk + w.dv + w.dv) * es + beta + th * 4 + w.B * w.H * w.dk * w.dv * 4
+
+
+def algorithmic_flops(w) -> int:
+    th = w.B * w.T * w.H
+    if w.variant in (1, 3, 5):
+        per = w.chunk * (w.dk + w.dv) + 4 * w.dk * w.dv
+    elif w.variant == 4:
+        per = (4 * w.window + 2) * w.dk * w.dv
+    else:
+        per = w.chunk * (2 * w.dk + 2 * w.dv) + 6 * w.dk * w.dv
+    return th * per
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_baseline(w, budget_s=20.0) -> dict:
+    """The oracle as it stands (fp64 token-by-token recurrence) on a bounded
+    sample of the workload: the first sequences, all heads, all tokens."""
+    import numpy as np
+
+    import oracle
+    from workloads import make_inputs
+    nb = 1
+    x = {k: v.double().numpy() for k, v in make_inputs(w.with_(B=nb)).items()}
+    t0 = time.perf_counter()
+    oracle.recurrent(**x, variant=w.variant, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma)
+    dt = time.perf_counter() - t0
+    reps = 1
+    while time.perf_counter() - t0 < min(budget_s, 5 * dt) and reps < 3:
+        oracle.recurrent(**x, variant=w.variant, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    del np
+    return {"value": nb * w.T / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{nb} of {w.B} sequences x {w.T} tokens x {w.H} heads, fp64 numpy "
+                      f"recurrence, {reps} run(s), single thread"}
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path)).get(kernel)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "chunked_delta_rule_gb300", "csrc", rec["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return rec["bytes_per_launch"] if h == rec["source_sha"] else None
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    import oracle
+    from workloads import make_inputs
+    nb, T = 1, min(w.T, 512)
+    x = {k: v.double().numpy() for k, v in make_inputs(w.with_(B=nb, T=T)).items()}
+    for _ in range(args.warmup):
+        oracle.recurrent(**x, variant=w.variant, window=w.window)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.recurrent(**x, variant=w.variant, window=w.window)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = nb * T / dt
+    line = {"impl": "reference", "metric": "Falcon-1 chunked fwd tokens/s", "value": value,
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk, "variant": "falcon1", "reference_sample": f"{nb}x{T}x{w.H}"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{nb} sequence x {T} tokens x {w.H} heads per step, fp64 "
+                                       "numpy recurrence, single thread"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = get_workload(args.workload)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    base = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        base = cpu_baseline(w)      # host work first: nothing forked after CUDA init
+
+    import torch
+    import torch.distributed as dist
+
+    import chunked_delta_rule_gb300 as F
+    from workloads import make_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    p = F.Params(B=w.B, T=w.T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk, window=w.window,
+                 eps=w.eps, eps_gamma=w.eps_gamma, variant=w.variant,
+                 dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32)
+    sets = [make_inputs(w, seed=w.seed + 100 * rank + i, device=dev) for i in range(N_SETS)]
+    o = torch.empty((w.B, w.T, w.H, w.dv), dtype=sets[0]["q"].dtype, device=dev)
+    carry = F.empty_carry(p, dev)
+    ws_n = F.falcon_workspace_size(p)
+    ws = F.alloc_workspace(ws_n, dev) if ws_n else None
+    impl_used, launches = F.falcon_chunk_fwd_plan(p)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        x = sets[i % N_SETS]
+        F.falcon_chunk_fwd(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o, carry, ws,
+                           ws_n, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and vis.split(",")[local].strip().isdigit():
+        gpu_index = int(vis.split(",")[local])
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    time.sleep(0.3)
+    # per-launch events for the kernel timing, one pair per step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    per_call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_step = ms / args.steps
+    tokens = w.B * w.T * world
+    value = tokens / (ms_step / 1e3)
+
+    # end to end through the C ABI with host buffers: pinned host -> device
+    # copies of the step's inputs, the call, and the output read back
+    host = {k: v.cpu().pin_memory() for k, v in sets[0].items()}
+    dev_in = {k: torch.empty_like(v) for k, v in sets[0].items()}
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o.numel() * o.element_size()
+    for _ in range(3):
+        for k2 in host:
+            dev_in[k2].copy_(host[k2], non_blocking=True)
+        F.falcon_chunk_fwd(p, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["beta"], dev_in["lam"],
+                           None, o, carry, ws, ws_n, stream)
+        o_host.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        for k2 in host:
+            dev_in[k2].copy_(host[k2], non_blocking=True)
+        F.falcon_chunk_fwd(p, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["beta"], dev_in["lam"],
+                           None, o, carry, ws, ws_n, stream)
+        o_host.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank == 0:
+        peaks = {}
+        try:
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        except Exception:
+            pass
+        hbm_peak = peaks.get("hbm_gbs", 6800.0)
+        abytes = algorithmic_bytes(w)
+        kernel = "tc_chunk_fused" if impl_used == F.FALCON_IMPL_TC else "generic_chunk_kernel"
+        achieved = abytes / (per_call_ms / 1e3) / 1e9
+        line = {
+            "metric": "Falcon-1 chunked fwd tokens/s and % of roofline (GB300, T=2048, H=12, d=64)",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk, "variant": "falcon1", "global_batch": w.B * world,
+                       "seq_len": w.T, "parallelism": f"replicas x{world}",
+                       "l2": f"rotating {N_SETS} input sets ({N_SETS * abytes / 1e6:.0f} MB > 2 x L2)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic_for(kernel),
+                         "kernel": kernel, "algorithmic_bytes": abytes,
+                         "algorithmic_flops": algorithmic_flops(w),
+                         "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+            "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * args.steps,
+            "clocks": clk,
+        }
+        if base is not None:
+            line["cpu_baseline"] = base
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+// C ABI of libfalcon.so: argument checks on the host, workspace sizing and
+// dispatch to the kernels.  Nothing here allocates device memory.
+
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+
+using namespace falcon;
+
+namespace {
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+int check_params(const falcon_params_t* p, bool need_T_pos) {
+  if (!p) return FALCON_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->T < 0 || (need_T_pos && p->T < 1)) return FALCON_ERR_INVALID_ARG;
+  if (p->variant < FALCON_1 || p->variant > FALCON_3A) return FALCON_ERR_INVALID_ARG;
+  if (p->dtype != FALCON_BF16 && p->dtype != FALCON_F32) return FALCON_ERR_INVALID_ARG;
+  if (p->impl < FALCON_IMPL_AUTO || p->impl > FALCON_IMPL_TC) return FALCON_ERR_INVALID_ARG;
+  if (!(p->eps > 0.f) || !(p->eps_gamma > 0.f) || !(p->eps_gamma <= 1.f)) return FALCON_ERR_INVALID_ARG;
+  if (!dim_ok(p->dk) || !dim_ok(p->dv)) return FALCON_ERR_UNSUPPORTED;
+  if (p->chunk != 16 && p->chunk != 32 && p->chunk != 64) return FALCON_ERR_UNSUPPORTED;
+  if (variant_windowed(p->variant) && (p->window < 1 || p->window > 64)) return FALCON_ERR_UNSUPPORTED;
+  return FALCON_OK;
+}
+
+size_t elem_size(int dtype) { return dtype == FALCON_BF16 ? 2 : 4; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  auto pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+FwdArgs make_args(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                  const float* beta, const float* lambda, void* o, void* stream) {
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = p->B; a.T = p->T; a.H = p->H; a.dk = p->dk; a.dv = p->dv; a.chunk = p->chunk;
+  a.W = effective_window(p->variant, p->window);
+  a.eps = p->eps; a.eps_gamma = p->eps_gamma; a.variant = p->variant; a.dtype = p->dtype;
+  a.q = q; a.k = k; a.v = v; a.beta = beta; a.lam = lambda; a.o = o;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* falcon_strerror(int code) {
+  switch (code) {
+    case FALCON_OK: return "ok";
+    case FALCON_ERR_INVALID_ARG: return "invalid argument";
+    case FALCON_ERR_UNSUPPORTED: return "unsupported shape or combination";
+    case FALCON_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case FALCON_ERR_CUDA: return "CUDA error";
+    case FALCON_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown error";
+  }
+}
+
+const char* falcon_version(void) { return "falcon-gb300 0.1 sm_103a"; }
+
+size_t falcon_workspace_size(const falcon_params_t* p) {
+  if (check_params(p, false) != FALCON_OK) return 0;
+  FwdArgs a = make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  if (p->impl != FALCON_IMPL_GENERIC && tc_chunk_supported(a))
+    return tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant);
+  return 0;
+}
+
+int falcon_chunk_fwd(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                     const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                     void* o, falcon_carry_t* carry_out, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  int st = check_params(p, false);
+  if (st != FALCON_OK) return st;
+  if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !o)) return FALCON_ERR_INVALID_ARG;
+  FwdArgs a = make_args(p, q, k, v, beta, lambda, o, stream);
+  const size_t es = elem_size(p->dtype);
+  const size_t BH = (size_t)p->B * p->H;
+  const int Wr = a.W - 1;
+  if (carry_in) {
+    a.S_in = carry_in->S; a.kprev_in = carry_in->k_prev; a.pos_in = carry_in->pos;
+    if (Wr > 0) { a.winx_in = carry_in->win_x; a.winv_in = carry_in->win_v; }
+  }
+  if (carry_out) {
+    a.S_out = carry_out->S; a.kprev_out = carry_out->k_prev; a.pos_out = carry_out->pos;
+    if (Wr > 0) { a.winx_out = carry_out->win_x; a.winv_out = carry_out->win_v; }
+  }
+  if (carry_in && carry_out) {
+    const size_t nS = BH * p->dk * p->dv * 4, nK = BH * p->dk * es, nP = BH * 8;
+    const size_t nWX = BH * (size_t)(Wr > 0 ? Wr : 0) * p->dk * es;
+    const size_t nWV = BH * (size_t)(Wr > 0 ? Wr : 0) * p->dv * es;
+    const void* ins[5] = {a.S_in, a.kprev_in, a.pos_in, a.winx_in, a.winv_in};
+    const size_t nin[5] = {nS, nK, nP, nWX, nWV};
+    const void* outs[5] = {a.S_out, a.kprev_out, a.pos_out, a.winx_out, a.winv_out};
+    for (int i = 0; i < 5; ++i)
+      for (int j = 0; j < 5; ++j)
+        if (overlaps(ins[i], nin[i], outs[j], nin[j])) return FALCON_ERR_INVALID_ARG;
+  }
+  a.ws = workspace; a.ws_bytes = workspace_bytes;
+  const bool tc_ok = tc_chunk_supported(a);
+  if (p->impl == FALCON_IMPL_TC && !tc_ok) return FALCON_ERR_UNSUPPORTED;
+  if (p->impl != FALCON_IMPL_GENERIC && tc_ok) {
+    const size_t need = tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant);
+    if (need > 0 && (!workspace || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255) != 0))
+      return FALCON_ERR_WORKSPACE;
+    return launch_tc_chunk(a);
+  }
+  return launch_generic_chunk(a);
+}
+
+int falcon_chunk_fwd_plan(const falcon_params_t* p, int32_t* impl_out, int32_t* launches_out) {
+  int st = check_params(p, false);
+  if (st != FALCON_OK) return st;
+  FwdArgs a = make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  const bool tc_ok = tc_chunk_supported(a);
+  if (p->impl == FALCON_IMPL_TC && !tc_ok) return FALCON_ERR_UNSUPPORTED;
+  const bool tc = p->impl != FALCON_IMPL_GENERIC && tc_ok;
+  if (impl_out) *impl_out = tc ? FALCON_IMPL_TC : FALCON_IMPL_GENERIC;
+  if (launches_out) *launches_out = tc ? tc_chunk_launches(a) : 1;
+  return FALCON_OK;
+}
+
+int falcon_recurrent_step(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                          const float* beta, const float* lambda, falcon_carry_t* carry, void* o,
+                          void* stream) {
+  int st = check_params(p, true);
+  if (st != FALCON_OK) return st;
+  if (p->T != 1) return FALCON_ERR_INVALID_ARG;
+  if (!q || !k || !v || !beta || !lambda || !o || !carry || !carry->S || !carry->k_prev || !carry->pos)
+    return FALCON_ERR_INVALID_ARG;
+  FwdArgs a = make_args(p, q, k, v, beta, lambda, o, stream);
+  if (a.W > 1 && (!carry->win_x || !carry->win_v)) return FALCON_ERR_INVALID_ARG;
+  a.S_in = a.S_out = carry->S;
+  a.kprev_in = a.kprev_out = carry->k_prev;
+  a.pos_in = a.pos_out = carry->pos;
+  if (a.W > 1) { a.winx_in = a.winx_out = carry->win_x; a.winv_in = a.winv_out = carry->win_v; }
+  return launch_recurrent_step(a);
+}
+
+size_t falcon_masked_parallel_workspace_size(const falcon_params_t* p) {
+  if (check_params(p, true) != FALCON_OK) return 0;
+  const int W = effective_window(p->variant, p->window);
+  return masked_parallel_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, W);
+}
+
+int falcon_masked_parallel_ref_gpu(const falcon_params_t* p, const void* q, const void* k,
+                                   const void* v, const float* beta, const float* lambda, void* o,
+                                   float* S_final, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  int st = check_params(p, true);
+  if (st != FALCON_OK) return st;
+  if (!q || !k || !v || !beta || !lambda || !o || !S_final) return FALCON_ERR_INVALID_ARG;
+  const int W = effective_window(p->variant, p->window);
+  if (p->T > 1024 || (size_t)p->T * W > 2048) return FALCON_ERR_UNSUPPORTED;
+  const size_t need = masked_parallel_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, W);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return FALCON_ERR_WORKSPACE;
+  FwdArgs a = make_args(p, q, k, v, beta, lambda, o, stream);
+  a.S_out = S_final;
+  a.ws = workspace; a.ws_bytes = workspace_bytes;
+  return launch_masked_parallel(a);
+}
+
+}  // extern "C"

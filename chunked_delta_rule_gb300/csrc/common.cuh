@@ -1,0 +1,77 @@
+// Shared device/host helpers of the Falcon GB300 library (internal).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "falcon.h"
+
+namespace falcon {
+
+// ---------------------------------------------------------------- dtypes
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__host__ __device__ inline bool variant_additive(int v) {
+  return v == FALCON_1A || v == FALCON_2A || v == FALCON_3A;
+}
+__host__ __device__ inline bool variant_per_channel(int v) { return v == FALCON_2 || v == FALCON_2A; }
+__host__ __device__ inline bool variant_windowed(int v) { return v == FALCON_3 || v == FALCON_3A; }
+__host__ __device__ inline int effective_window(int v, int w) { return variant_windowed(v) ? w : 1; }
+
+// Decay with the positive-decay floor: gamma = clamp(1 - lambda, eps_gamma, 1);
+// its log is then >= log(eps_gamma) > -inf.
+__device__ __forceinline__ float clamped_log_decay(float lam, float eps_gamma) {
+  float g = fminf(fmaxf(1.0f - lam, eps_gamma), 1.0f);
+  return logf(g);
+}
+
+// Ring slot of the pair with global index p (p >= 1) in a ring of Wr slots.
+__host__ __device__ inline int ring_slot(int64_t p, int Wr) { return (int)(p % (int64_t)Wr); }
+
+// Everything one chunk-forward call needs, resolved on the host.
+struct FwdArgs {
+  int B, T, H, dk, dv, chunk, W;  // W: effective window (1 outside Falcon-3/3A)
+  float eps, eps_gamma;
+  int variant, dtype;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* lam;
+  const float* S_in;        // may be NULL (zero state)
+  const void* kprev_in;     // may be NULL (zero key)
+  const void* winx_in;      // may be NULL
+  const void* winv_in;      // may be NULL
+  const int64_t* pos_in;    // may be NULL (pos = 0)
+  void* o;
+  float* S_out;             // may be NULL
+  void* kprev_out;          // may be NULL
+  void* winx_out;           // may be NULL
+  void* winv_out;           // may be NULL
+  int64_t* pos_out;         // may be NULL
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+};
+
+// Launchers (each returns a FALCON_* code; host-side checks only).
+int launch_generic_chunk(const FwdArgs& a);
+size_t generic_chunk_smem_bytes(int dk, int dvs, int c, int W);
+int launch_recurrent_step(const FwdArgs& a);
+int launch_masked_parallel(const FwdArgs& a);
+size_t masked_parallel_ws_bytes(int B, int T, int H, int dk, int dv, int W);
+int launch_tc_chunk(const FwdArgs& a);
+bool tc_chunk_supported(const FwdArgs& a);
+int tc_chunk_launches(const FwdArgs& a);
+size_t tc_chunk_ws_bytes(int B, int T, int H, int dk, int dv, int chunk, int variant);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace falcon

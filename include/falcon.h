@@ -1,0 +1,187 @@
+/*
+ * falcon.h — C ABI of the GB300 Falcon fast-weight forward library
+ * (libfalcon.so, built for sm_103a).
+ *
+ * The method: a fixed-size fast-weight state S (d_k x d_v, fp32) is written
+ * once per token by one normalised online gradient step on the
+ * prefix-aligned pair (x_t, v_t) = (phi(k_{t-1}), v_t), with a shrinkage
+ * decay gamma_t = 1 - lambda_t kept >= eps_gamma, and read after the write,
+ * o_t = S_t^T q_t.  Sources, cited by page title and section:
+ *   [FW]  "Falcon 家族重新对齐 fast-weight 记忆" (zhouql-dev explainer):
+ *         本质 (pair alignment), Falcon 家族 (variants, knobs),
+ *         三种等价形式 (recurrent / masked-parallel / chunked forms).
+ *   [JC]  "给记忆装一个“及时纠错”的开关" (long write-up):
+ *         把记忆更新变成一次梯度下降 (gradient step, NLMS step),
+ *         Falcon家族六个变体各管一段 (1/2/3 and A variants, batched solve),
+ *         数学上的稳定阀门:正衰减钳制 (decay floor eps_gamma),
+ *         三种视角看同一个更新 (the three forms, WY representation).
+ *
+ * Update of one step t (window W(t) = existing pairs among the last W;
+ * W = 1 except for Falcon-3/3A; n_t = |W(t)|; e_t = mean ||x_j||^2 over W(t)):
+ *   gamma_t = clamp(1 - lambda_t, eps_gamma, 1)
+ *   eta_t   = beta_t / (eps + e_t)          (scalar, or per value channel)
+ *   Z       = gamma_t S_{t-1}
+ *   regression (1, 2, 3):  S_t = Z + (1/n_t) sum_j x_j (eta_t * (v_j - Z^T x_j))^T
+ *   additive  (1A, 2A, 3A): S_t = Z + (1/n_t) sum_j x_j (eta_t * v_j)^T
+ *   o_t = S_t^T q_t
+ * The pair of a token whose global index (carry pos + local index) is < 1
+ * does not exist (it would need the key before the sequence) and writes
+ * nothing; a step with no existing pair only decays.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates device memory.  Scratch memory, where needed,
+ *     is the caller's `workspace` of at least the size the matching
+ *     *_workspace_size() call returns, 256-byte aligned.
+ *   - Layouts are dense row-major: q, k [B, T, H, dk]; v, o [B, T, H, dv];
+ *     beta [B, T, H] (Falcon-2/2A: [B, T, H, dv]); lambda [B, T, H].
+ *     q, k, v, o, carry k_prev / win_x / win_v use the params' dtype
+ *     (bf16 or fp32); beta, lambda and the state S are fp32; pos is int64.
+ *     q and k are the features phi(q), phi(k): the caller applies phi.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  Errors found on the host
+ *     (arguments, shapes) return before anything is enqueued.
+ *   - Return value: FALCON_OK (0) or a negative FALCON_ERR_* code; no
+ *     exception crosses the ABI.  FALCON_ERR_CUDA reports a launch error
+ *     (cudaGetLastError after the launches).
+ *   - Inputs must not overlap outputs.  The chunk forward reads carry_in
+ *     and writes carry_out; the two must not overlap (use two carries).
+ *     The recurrent step updates its carry in place.
+ */
+#ifndef FALCON_H
+#define FALCON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Variants [FW Falcon 家族; JC Falcon家族六个变体各管一段]:
+ * 1 scalar step, 2 per-value-channel step, 3 sliding-window mini-batch of the
+ * last `window` pairs (window-averaged); "A" = inner-product objective,
+ * additive write. */
+typedef enum {
+  FALCON_1 = 0,
+  FALCON_1A = 1,
+  FALCON_2 = 2,
+  FALCON_2A = 3,
+  FALCON_3 = 4,
+  FALCON_3A = 5
+} falcon_variant_t;
+
+typedef enum { FALCON_BF16 = 0, FALCON_F32 = 1 } falcon_dtype_t;
+
+/* Kernel family for the chunk forward.  AUTO picks the tensor-core path
+ * (tcgen05 + TMEM + TMA) when it supports the shape, else the portable
+ * CUDA-core path.  GENERIC/TC force one (TC returns FALCON_ERR_UNSUPPORTED
+ * for shapes it does not cover). */
+typedef enum { FALCON_IMPL_AUTO = 0, FALCON_IMPL_GENERIC = 1, FALCON_IMPL_TC = 2 } falcon_impl_t;
+
+enum {
+  FALCON_OK = 0,
+  FALCON_ERR_INVALID_ARG = -1,   /* null pointer, bad enum, bad size */
+  FALCON_ERR_UNSUPPORTED = -2,   /* shape or combination not supported */
+  FALCON_ERR_WORKSPACE = -3,     /* workspace missing, too small or misaligned */
+  FALCON_ERR_CUDA = -4,          /* a CUDA call or launch failed */
+  FALCON_ERR_TIMEOUT = -5        /* a bounded device-side wait expired */
+};
+
+typedef struct {
+  int32_t B, T, H;      /* batch, tokens in this call, heads (all >= 1; T >= 0 for chunk fwd) */
+  int32_t dk, dv;       /* key / value head dims: 16, 32, 64 or 128 */
+  int32_t chunk;        /* chunk length of the chunked form: 16, 32 or 64 */
+  int32_t window;       /* Falcon-3/3A window W in [1, 64]; ignored otherwise */
+  float eps;            /* NLMS regulariser, > 0 (e.g. 1e-6) */
+  float eps_gamma;      /* positive-decay floor, in (0, 1] (e.g. 1e-3) */
+  int32_t variant;      /* falcon_variant_t */
+  int32_t dtype;        /* falcon_dtype_t of q, k, v, o and the carried keys/values */
+  int32_t impl;         /* falcon_impl_t (chunk forward only) */
+} falcon_params_t;
+
+/* Decode carry: everything the next call needs to continue a sequence.
+ * All pointers are device pointers owned by the caller.
+ *   S      [B, H, dk, dv] fp32   fast-weight state
+ *   k_prev [B, H, dk]     dtype  last key consumed (x of the next pair)
+ *   win_x  [B, H, W-1, dk] dtype  window ring of previous pairs' keys  (3/3A, W > 1)
+ *   win_v  [B, H, W-1, dv] dtype  window ring of previous pairs' values (3/3A, W > 1)
+ *   pos    [B, H]         int64  tokens consumed so far
+ * The pair with global index p lives in ring slot p mod (W-1); slots whose
+ * pair index is < 1 hold zeros.  As an input, a NULL carry (or NULL fields)
+ * means a fresh sequence: S = 0, k_prev = 0, pos = 0; win_* may be NULL only
+ * when pos <= 1 for every (b, h) (no earlier pair exists). */
+typedef struct {
+  float* S;
+  void* k_prev;
+  void* win_x;
+  void* win_v;
+  int64_t* pos;
+} falcon_carry_t;
+
+/* Bytes of workspace falcon_chunk_fwd needs for these params (0 if none). */
+size_t falcon_workspace_size(const falcon_params_t* p);
+
+/* Chunk-parallel (SSD-style) forward [FW 三种等价形式; JC 三种视角看同一个更新]:
+ * the sequence is cut into chunks of `chunk` tokens; inside a chunk the
+ * rank-one updates are gathered in the WY representation (Gram matrix of
+ * the shifted keys, unit lower-triangular solve), and the state S is carried
+ * across chunks with the cumulative log-decay.  Computes o [B, T, H, dv] for
+ * the T tokens and, when carry_out is non-NULL, the carry after them
+ * (carry_out->S holds the final state S_T; every non-NULL carry_out field
+ * is written).  carry_in == NULL starts a fresh sequence.
+ * Errors: FALCON_ERR_INVALID_ARG (null q/k/v/beta/lambda/o with T > 0, bad
+ * params, carry_in/carry_out overlap), FALCON_ERR_UNSUPPORTED (dims outside
+ * {16,32,64,128}, window outside [1,64], forced TC on an unsupported shape),
+ * FALCON_ERR_WORKSPACE, FALCON_ERR_CUDA. */
+int falcon_chunk_fwd(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                     const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                     void* o, falcon_carry_t* carry_out, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Which kernel family falcon_chunk_fwd uses for these params
+ * (FALCON_IMPL_GENERIC or FALCON_IMPL_TC, written to *impl_out) and how many
+ * kernels one call enqueues (*launches_out).  Host-only; either output
+ * pointer may be NULL.  Returns FALCON_OK or the error the call would give
+ * for these params. */
+int falcon_chunk_fwd_plan(const falcon_params_t* p, int32_t* impl_out, int32_t* launches_out);
+
+/* Recurrent form, one token per sequence [FW 三种等价形式 (inference form,
+ * O(1) state per step); JC 三种视角看同一个更新]: p->T must be 1.  q, k, v
+ * are [B, 1, H, d], beta / lambda [B, 1, H] (or [B, 1, H, dv]).  Updates the
+ * carry in place (S, k_prev <- k, window ring push, pos += 1) and writes
+ * o [B, 1, H, dv].  carry, carry->S, carry->k_prev and carry->pos are
+ * required; win_x / win_v are required for Falcon-3/3A with window > 1.
+ * Errors: FALCON_ERR_INVALID_ARG, FALCON_ERR_UNSUPPORTED, FALCON_ERR_CUDA. */
+int falcon_recurrent_step(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                          const float* beta, const float* lambda, falcon_carry_t* carry, void* o,
+                          void* stream);
+
+/* Bytes of workspace falcon_masked_parallel_ref_gpu needs. */
+size_t falcon_masked_parallel_workspace_size(const falcon_params_t* p);
+
+/* Masked-parallel form of a fresh sequence [FW 三种等价形式 (linear attention
+ * (phi(Q) phi(K)^T (.) M) V without denominator); JC 三种视角看同一个更新]:
+ * the whole T x T decay mask from the global cumulative log-decay and, for
+ * the regression variants, one unit lower-triangular solve over all T
+ * steps (T*W unknowns for Falcon-3).  fp32 arithmetic, quadratic cost: a
+ * reference for tests, limited to T <= 1024 (T*window <= 2048).  Writes
+ * o [B, T, H, dv] and S_final [B, H, dk, dv] (fp32).
+ * Errors: FALCON_ERR_INVALID_ARG, FALCON_ERR_UNSUPPORTED (T too large),
+ * FALCON_ERR_WORKSPACE, FALCON_ERR_CUDA. */
+int falcon_masked_parallel_ref_gpu(const falcon_params_t* p, const void* q, const void* k,
+                                   const void* v, const float* beta, const float* lambda, void* o,
+                                   float* S_final, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* Static description of an error code (never NULL). */
+const char* falcon_strerror(int code);
+
+/* Library version string, e.g. "falcon-gb300 0.1 sm_103a". */
+const char* falcon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FALCON_H */

@@ -1,0 +1,110 @@
+"""Host-side checks that need no GPU: the C-ABI library builds, loads and
+exports every symbol include/falcon.h declares; argument errors are caught
+on the host before anything is enqueued; workspace sizing."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__
+    __graft_entry__.build()
+    import chunked_delta_rule_gb300 as F
+    return F
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "falcon.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(falcon_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(F):
+    syms = declared_symbols()
+    assert "falcon_chunk_fwd" in syms and "falcon_recurrent_step" in syms
+    assert "falcon_masked_parallel_ref_gpu" in syms
+    lib = ctypes.CDLL(F.LIB_PATH)
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert sorted(F.EXPORTED) == sorted(syms)
+
+
+def test_version_and_strerror(F):
+    assert "sm_103a" in F.falcon_version()
+    for code in (0, -1, -2, -3, -4, -5):
+        assert F.strerror(code)
+    assert F.strerror(-99) == "unknown error"
+
+
+def _p(F, **kw):
+    base = dict(B=2, T=100, H=3, dk=64, dv=64, chunk=64, window=1, variant=F.FALCON_1,
+                dtype=F.FALCON_BF16)
+    base.update(kw)
+    return F.Params(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=48), -2), (dict(dv=256), -2), (dict(chunk=48), -2),
+    (dict(variant=9), -1), (dict(dtype=7), -1), (dict(B=0), -1), (dict(T=-1), -1),
+    (dict(eps=0.0), -1), (dict(eps_gamma=0.0), -1), (dict(eps_gamma=1.5), -1),
+    (dict(variant=4, window=0), -2), (dict(variant=4, window=65), -2), (dict(impl=3), -1),
+])
+def test_chunk_fwd_rejects_bad_params_on_host(F, kw, code):
+    p = _p(F, **kw)
+    fake = 1 << 20  # never dereferenced: the call must return before enqueueing
+    with pytest.raises(F.FalconError) as e:
+        F.falcon_chunk_fwd(p, fake, fake, fake, fake, fake, None, fake, None, None, 0, 0)
+    assert e.value.code == code
+
+
+def test_null_pointers_rejected(F):
+    p = _p(F)
+    fake = 1 << 20
+    with pytest.raises(F.FalconError) as e:
+        F.falcon_chunk_fwd(p, None, fake, fake, fake, fake, None, fake, None, None, 0, 0)
+    assert e.value.code == -1
+    with pytest.raises(F.FalconError) as e:  # recurrent step needs T == 1 and a carry
+        F.falcon_recurrent_step(_p(F, T=1), fake, fake, fake, fake, fake, None, fake, 0)
+    assert e.value.code == -1
+    with pytest.raises(F.FalconError) as e:
+        F.falcon_recurrent_step(_p(F, T=2), fake, fake, fake, fake, fake,
+                                {"S": fake, "k_prev": fake, "pos": fake}, fake, 0)
+    assert e.value.code == -1
+
+
+def test_overlapping_carries_rejected(F):
+    p = _p(F)
+    fake = 1 << 20
+    c = {"S": 1 << 24, "k_prev": 1 << 25, "pos": 1 << 26}
+    with pytest.raises(F.FalconError) as e:
+        F.falcon_chunk_fwd(p, fake, fake, fake, fake, fake, c, fake, c, None, 0, 0)
+    assert e.value.code == -1
+
+
+def test_masked_parallel_limits(F):
+    fake = 1 << 20
+    with pytest.raises(F.FalconError) as e:
+        F.falcon_masked_parallel_ref_gpu(_p(F, T=2048), fake, fake, fake, fake, fake, fake, fake,
+                                         fake, 1 << 30, 0)
+    assert e.value.code == -2
+    with pytest.raises(F.FalconError) as e:  # workspace too small
+        F.falcon_masked_parallel_ref_gpu(_p(F, T=100), fake, fake, fake, fake, fake, fake, fake,
+                                         1 << 12, 16, 0)
+    assert e.value.code == -3
+    assert F.falcon_masked_parallel_workspace_size(_p(F, T=100)) > 0
+
+
+def test_workspace_size_is_deterministic(F):
+    p = _p(F, B=8, T=2048, H=12)
+    n1 = F.falcon_workspace_size(p)
+    n2 = F.falcon_workspace_size(p)
+    assert n1 == n2 and n1 % 256 == 0
+    assert F.falcon_workspace_size(_p(F, dk=48)) == 0
