@@ -41,9 +41,9 @@ __host__ __device__ inline GenLayout gen_layout(int dk, int dvs, int c, int W) {
   L.NP = c + W - 1;
   size_t off = 0;
   auto take = [&](size_t n) { size_t o = off; off += (n + 3) & ~size_t(3); return o; };
-  L.Xw = take((size_t)L.NP * dk);
+  L.Xw = take((size_t)L.NP * (dk + 1));  // rows padded to dk + 1: no bank conflicts
   L.Vw = take((size_t)L.NP * dvs);
-  L.Qb = take((size_t)c * dk);
+  L.Qb = take((size_t)c * (dk + 1));
   L.S = take((size_t)dk * dvs);
   L.XS = take((size_t)L.NP * dvs);
   L.QS = take((size_t)c * dvs);
@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) generic_chunk_kernel(FwdArgs a, int 
   const bool perch = variant_per_channel(a.variant);
   const GenLayout L = gen_layout(dk, dvs, c, W);
   const int NP = L.NP;
+  const int LX = dk + 1;  // padded row stride of Xw and Qb
   float* Xw = sm + L.Xw;
   float* Vw = sm + L.Vw;
   float* Qb = sm + L.Qb;
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) generic_chunk_kernel(FwdArgs a, int 
       int kk = i / dk, col = i % dk;
       int j = s0 - W + 1 + kk;
       bool ok = (pos + j >= 1) && (j < T);
-      Xw[i] = ok ? pair_key<Tin>(a, b, h, j, col, pos) : 0.f;
+      Xw[kk * LX + col] = ok ? pair_key<Tin>(a, b, h, j, col, pos) : 0.f;
     }
     for (int i = tid; i < NP * dvs; i += kThreads) {
       int kk = i / dvs, col = i % dvs;
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) generic_chunk_kernel(FwdArgs a, int 
     for (int i = tid; i < c * dk; i += kThreads) {
       int sg = i / dk, col = i % dk;
       int s = s0 + sg;
-      Qb[i] = (s < T) ? ld<Tin>(a.q, (((size_t)b * T + s) * a.H + h) * dk + col) : 0.f;
+      Qb[sg * LX + col] = (s < T) ? ld<Tin>(a.q, (((size_t)b * T + s) * a.H + h) * dk + col) : 0.f;
     }
     for (int sg = tid; sg < c; sg += kThreads) {
       int s = s0 + sg;
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) generic_chunk_kernel(FwdArgs a, int 
     }
     for (int kk = tid; kk < NP; kk += kThreads) {
       float acc = 0.f;
-      for (int d = 0; d < dk; ++d) acc += Xw[kk * dk + d] * Xw[kk * dk + d];
+      for (int d = 0; d < dk; ++d) acc += Xw[kk * LX + d] * Xw[kk * LX + d];
       xn[kk] = acc;
     }
     __syncthreads();
@@ -191,26 +192,26 @@ __global__ void __launch_bounds__(kThreads) generic_chunk_kernel(FwdArgs a, int 
       for (int i = tid; i < NP * NP; i += kThreads) {
         int r = i / NP, q = i % NP;
         float acc = 0.f;
-        for (int d = 0; d < dk; ++d) acc += Xw[r * dk + d] * Xw[q * dk + d];
+        for (int d = 0; d < dk; ++d) acc += Xw[r * LX + d] * Xw[q * LX + d];
         Gk[i] = acc;
       }
       for (int i = tid; i < NP * dvs; i += kThreads) {
         int kk = i / dvs, col = i % dvs;
         float acc = 0.f;
-        for (int d = 0; d < dk; ++d) acc += Xw[kk * dk + d] * S[d * dvs + col];
+        for (int d = 0; d < dk; ++d) acc += Xw[kk * LX + d] * S[d * dvs + col];
         XS[i] = acc;
       }
     }
     for (int i = tid; i < c * NP; i += kThreads) {
       int r = i / NP, q = i % NP;
       float acc = 0.f;
-      for (int d = 0; d < dk; ++d) acc += Qb[r * dk + d] * Xw[q * dk + d];
+      for (int d = 0; d < dk; ++d) acc += Qb[r * LX + d] * Xw[q * LX + d];
       PQ[i] = acc;
     }
     for (int i = tid; i < c * dvs; i += kThreads) {
       int sg = i / dvs, col = i % dvs;
       float acc = 0.f;
-      for (int d = 0; d < dk; ++d) acc += Qb[sg * dk + d] * S[d * dvs + col];
+      for (int d = 0; d < dk; ++d) acc += Qb[sg * LX + d] * S[d * dvs + col];
       QS[i] = acc;
     }
     __syncthreads();
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) generic_chunk_kernel(FwdArgs a, int 
       float acc = 0.f;
       for (int sp = 0; sp < c; ++sp) {
         float inner = 0.f;
-        for (int bb = 0; bb < W; ++bb) inner += Xw[(sp + bb) * dk + d] * Dl[(sp * W + bb) * dvs + col];
+        for (int bb = 0; bb < W; ++bb) inner += Xw[(sp + bb) * LX + d] * Dl[(sp * W + bb) * dvs + col];
         acc += Dm[(c - 1) * c + sp] * inner;
       }
       S[i] = gend * S[i] + acc;

@@ -1,11 +1,826 @@
-// Tensor-core chunk forward (placeholder until the tcgen05 kernels land).
+// Tensor-core chunk forward for sm_103a (Falcon-1 / Falcon-1A, bf16 inputs,
+// fp32 state, chunk 64, d_k = d_v in {64, 128}).
+//
+// Chunked form [FW 三种等价形式, 图4C; JC 三种视角看同一个更新]: per chunk
+// of C = 64 steps with state S0 at its start, in-chunk cumulative log-decay
+// g_r (clamped decay [JC 数学上的稳定阀门:正衰减钳制]) and Gamma_r = exp(g_r),
+//   A_ri = eta_r exp(g_r - g_i) x_r.x_i (i < r),     T = (I + A)^{-1}
+//   [W | U] = T [diag(eta Gamma) X | diag(eta) V]            (WY representation)
+//   Delta   = U - W S0                  (Falcon-1A: Delta = diag(eta) V)
+//   O       = diag(Gamma) Q S0 + (Q X^T (.) [exp(g_r - g_i)]_{i<=r}) Delta
+//   S1      = Gamma_last S0 + (diag(exp(g_last - g)) X)^T Delta
+//
+// Two kernels:
+//  (a) tc_wy_kernel — one CTA per pair of chunks, fully parallel: TMA loads
+//      the 128 shifted keys, one tcgen05 MMA forms the Gram matrix in TMEM,
+//      the gates (clamped log-decay, its in-chunk prefix sum, NLMS step) are
+//      formed from lambda, beta and the Gram diagonal, and T = (I + A)^{-1}
+//      is found by blocked forward substitution: 16x16 diagonal blocks in
+//      registers, off-diagonal blocks merged with warp-level tf32 MMAs in
+//      shared memory.  T is written as bf16 in the exact image of a 128B-
+//      swizzled K-major shared-memory tile, plus eta and g per row.
+//  (b) tc_fwd_kernel — one CTA per (b, h, value slice), sequential over the
+//      chunks with the fp32 state held in registers: TMA brings q, shifted k,
+//      v (and T, gates by bulk copy) for chunk c+1 while chunk c computes;
+//      every contraction (P = Q X^T, [W|U], W S0, Q S0, X~^T Delta,
+//      P~ Delta) is a tcgen05 MMA with the accumulator in TMEM; the output
+//      tile leaves by TMA store.
+// Every mbarrier wait is bounded; on timeout a kernel records an error in the
+// workspace status word and leaves its chunk loop.
+
+#include <cuda.h>
+
+#include <mutex>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace falcon {
 
-bool tc_chunk_supported(const FwdArgs&) { return false; }
-int tc_chunk_launches(const FwdArgs&) { return 0; }
-size_t tc_chunk_ws_bytes(int, int, int, int, int, int, int) { return 0; }
-int launch_tc_chunk(const FwdArgs&) { return FALCON_ERR_UNSUPPORTED; }
+using namespace tc;
+
+namespace {
+
+constexpr int kC = 64;           // chunk length of this path
+constexpr int kLD = 68;          // fp32 row stride of the solve buffers (bank spread)
+constexpr int kYL = 24;          // row stride of the 16x16 scratch blocks
+constexpr uint32_t kStatusTimeout = 1;
+
+struct TcArgs {
+  int B, T, H, NC, NV;
+  float eps, eps_gamma;
+  const float* beta;
+  const float* lam;
+  const int64_t* pos_in;
+  const __nv_bfloat16* kprev_in;
+  const float* S_in;
+  const __nv_bfloat16* k;
+  float* S_out;
+  __nv_bfloat16* kprev_out;
+  int64_t* pos_out;
+  uint8_t* ws_T;      // [B*H*NC][8192] bf16 swizzled images of T
+  float* ws_g;        // [B*H*NC][128]: eta[64], g[64]
+  uint32_t* status;   // workspace status word
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Issue a chain of K/16 MMAs: D = A (M rows, K) * B (N rows, K)^T, both K-major
+// 128B-swizzled; K beyond 64 continues in the next 64-column slab.
+__device__ __forceinline__ void mma_chain(uint32_t d_tmem, const uint8_t* A, int a_rows,
+                                          const uint8_t* Bm, int b_rows, int K, uint32_t idesc,
+                                          bool accumulate) {
+  const uint32_t a0 = smem_u32(A), b0 = smem_u32(Bm);
+  for (int ks = 0; ks < K / 16; ++ks) {
+    const uint32_t off = (ks & 3) * 32;
+    const uint32_t slab = ks >> 2;
+    const uint64_t ad = sdesc_k128(a0 + slab * a_rows * 128 + off);
+    const uint64_t bd = sdesc_k128(b0 + slab * b_rows * 128 + off);
+    umma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
+  }
+}
+
+// Load 64 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  tmem_ld32(taddr + 32, r);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
+}
+
+// ======================================================================
+// (a) per-chunk gates, Gram matrix and T = (I + A)^{-1}
+// ======================================================================
+template <int DK>
+struct WySmem {
+  static constexpr int kSlabs = DK / 64;
+  static constexpr size_t X = 0;                                  // kSlabs x 128 rows x 128 B
+  static constexpr size_t A = X + kSlabs * 16384;                 // [2][64][kLD] fp32
+  static constexpr size_t Tm = A + 2 * 64 * kLD * 4;              // [2][64][kLD] fp32
+  static constexpr size_t Y = Tm + 2 * 64 * kLD * 4;              // [2 chunks][2][2][16*kYL]
+  static constexpr size_t Ysc = Y + 2 * 4 * 16 * kYL * 4;         // [4 warps][16*kYL]
+  static constexpr size_t G = Ysc + 4 * 16 * kYL * 4;             // g[128]
+  static constexpr size_t E = G + 128 * 4;                        // eta[128]
+  static constexpr size_t WS = E + 128 * 4;                       // warp sums [4]
+  static constexpr size_t BAR = WS + 8 * 4;                       // 2 mbarriers
+  static constexpr size_t MISC = BAR + 16;                        // tmem addr, abort flag
+  static constexpr size_t TOTAL = MISC + 16 + 1024;               // + alignment slack
+};
+
+template <int DK, bool SOLVE>
+__global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUtensorMap tm_k128,
+                                                    TcArgs a) {
+  using L = WySmem<DK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* Xs = sm + L::X;
+  float* Am = reinterpret_cast<float*>(sm + L::A);
+  float* Tf = reinterpret_cast<float*>(sm + L::Tm);
+  float* Yb = reinterpret_cast<float*>(sm + L::Y);
+  float* Ysc = reinterpret_cast<float*>(sm + L::Ysc);
+  float* gs = reinterpret_cast<float*>(sm + L::G);
+  float* es = reinterpret_cast<float*>(sm + L::E);
+  float* wsum = reinterpret_cast<float*>(sm + L::WS);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pair = blockIdx.x, bh = blockIdx.y;
+  const int b = bh / a.H, h = bh % a.H;
+  const int t_base = pair * 128;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  if (SOLVE && warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar[0], L::kSlabs * 128 * 128);
+    for (int s = 0; s < L::kSlabs; ++s)
+      tma_load_4d(Xs + s * 16384, &tm_k128, &bar[0], 64 * s, h, t_base - 1, b);
+  }
+  // gates while the keys are in flight: row tid <-> step t_base + tid
+  const int t = t_base + tid;
+  const bool step_ok = t < a.T;
+  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+  const bool exists = step_ok && (pos + t >= 1);
+  const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
+  const float ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
+  const float beta = step_ok ? a.beta[gi] : 0.f;
+  float g = ell;  // inclusive prefix sum inside each 64-step chunk
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, g, o);
+    if (lane >= o) g += n;
+  }
+  if (lane == 31) wsum[warp] = g;
+  __syncthreads();
+  if (warp & 1) g += wsum[warp - 1];
+  gs[tid] = g;
+
+  if (!mbar_wait(&bar[0], 0)) {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  }
+  if (pair == 0 && a.kprev_in) {  // x_0 = carried key (row 0 of the first chunk)
+    for (int i = tid; i < DK; i += 128)
+      *reinterpret_cast<__nv_bfloat16*>(Xs + (i >> 6) * 16384 + sw128(0, i & 63)) =
+          a.kprev_in[(size_t)bh * DK + i];
+  }
+  fence_proxy_async();
+  __syncthreads();
+  const int cidx = tid >> 6, rl = tid & 63;
+  const int chunk = 2 * pair + cidx;
+  const bool aborted = *abort_flag != 0;
+
+  if (!SOLVE) {
+    // additive variants need only the gates: eta from the key energy
+    float n = 0.f;
+    if (!aborted) {
+      for (int i = 0; i < DK; ++i) {
+        const float x = __bfloat162float(
+            *reinterpret_cast<const __nv_bfloat16*>(Xs + (i >> 6) * 16384 + sw128(tid, i & 63)));
+        n += x * x;
+      }
+    }
+    const float eta = exists ? beta / (a.eps + n) : 0.f;
+    if (chunk < a.NC && !aborted) {
+      float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * 128;
+      go[rl] = eta;
+      go[64 + rl] = g;
+    }
+    return;
+  }
+
+  const uint32_t tmem = *tmem_slot;
+  if (!aborted && tid == 0) {
+    tc_fence_after();
+    mma_chain(tmem, Xs, 128, Xs, 128, DK, idesc_bf16(128, 128), false);
+    umma_commit(&bar[1]);
+  }
+  bool ok = aborted ? false : mbar_wait(&bar[1], 0);
+  if (!ok && !aborted) atomicExch(a.status, kStatusTimeout);
+  tc_fence_after();
+  float grow[64];
+  tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + 64 * cidx, grow);
+  tmem_wait_ld();
+  float n = 0.f;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) n = (j == rl) ? grow[j] : n;
+  const float eta = exists ? beta / (a.eps + n) : 0.f;
+  es[tid] = eta;
+  tc_fence_before();
+  __syncthreads();
+  {
+    float* Arow = Am + cidx * 64 * kLD + rl * kLD;
+    const float* gc = gs + cidx * 64;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) Arow[i] = (i < rl) ? eta * __expf(g - gc[i]) * grow[i] : 0.f;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+
+  // ---- T = (I + A)^{-1}: two warps per chunk
+  const int w2 = warp & 1;
+  const int nb_id = 1 + cidx;
+  float* A = Am + cidx * 64 * kLD;
+  float* Tm = Tf + cidx * 64 * kLD;
+  {  // 16x16 diagonal blocks, one column per lane, forward substitution
+    const int I = 2 * w2 + (lane >> 4), l = lane & 15;
+    float tv[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float s = (r == l) ? 1.f : 0.f;
+#pragma unroll
+      for (int i = 0; i < r; ++i) s -= A[(16 * I + r) * kLD + 16 * I + i] * tv[i];
+      tv[r] = s;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Tm[(16 * I + r) * kLD + 16 * I + l] = tv[r];
+  }
+  named_bar(nb_id, 64);
+  {  // T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22
+    const int I = w2 == 0 ? 1 : 3, J = I - 1;
+    float acc[2][4] = {};
+    warp_mm16(acc, A + 16 * I * kLD + 16 * J, kLD, Tm + 16 * J * kLD + 16 * J, kLD, lane);
+    float* ys = Ysc + warp * 16 * kYL;
+    warp_store16(ys, kYL, acc, 1.f, lane);
+    __syncwarp();
+    float acc2[2][4] = {};
+    warp_mm16(acc2, Tm + 16 * I * kLD + 16 * I, kLD, ys, kYL, lane);
+    warp_store16(Tm + 16 * I * kLD + 16 * J, kLD, acc2, -1.f, lane);
+  }
+  named_bar(nb_id, 64);
+  float* Yc = Yb + cidx * 4 * 16 * kYL;  // [I-2][J] blocks
+  {  // Y = A[32:64, 0:32] T[0:32, 0:32], row block I = 2 + w2
+    const int I = 2 + w2;
+    float acc[2][4] = {};
+    warp_mm16(acc, A + 16 * I * kLD, kLD, Tm, kLD, lane);
+    warp_mm16(acc, A + 16 * I * kLD + 16, kLD, Tm + 16 * kLD, kLD, lane);
+    warp_store16(Yc + (2 * w2 + 0) * 16 * kYL, kYL, acc, 1.f, lane);
+    float acc1[2][4] = {};
+    warp_mm16(acc1, A + 16 * I * kLD + 16, kLD, Tm + 16 * kLD + 16, kLD, lane);
+    warp_store16(Yc + (2 * w2 + 1) * 16 * kYL, kYL, acc1, 1.f, lane);
+  }
+  named_bar(nb_id, 64);
+  {  // T[32:64, 0:32] = -T[32:64, 32:64] Y
+    const int I = 2 + w2;
+#pragma unroll
+    for (int J = 0; J < 2; ++J) {
+      float acc[2][4] = {};
+      for (int K = 2; K <= I; ++K)
+        warp_mm16(acc, Tm + 16 * I * kLD + 16 * K, kLD, Yc + (2 * (K - 2) + J) * 16 * kYL, kYL,
+                  lane);
+      warp_store16(Tm + 16 * I * kLD + 16 * J, kLD, acc, -1.f, lane);
+    }
+  }
+  named_bar(nb_id, 64);
+  if (chunk < a.NC && !aborted) {
+    // bf16 image of T as a 128B-swizzled K-major tile, upper triangle zero
+    uint8_t* To = a.ws_T + ((size_t)bh * a.NC + chunk) * 8192;
+    for (int idx = rl; idx < 512; idx += 64) {
+      const int R = idx >> 3, j = idx & 7;
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c0 = 8 * j + 2 * e;
+        const float v0 = (c0 <= R) ? Tm[R * kLD + c0] : 0.f;
+        const float v1 = (c0 + 1 <= R) ? Tm[R * kLD + c0 + 1] : 0.f;
+        pk[e] = pack_bf16(v0, v1);
+      }
+      *reinterpret_cast<uint4*>(To + R * 128 + 16 * (j ^ (R & 7))) =
+          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * 128;
+    go[rl] = eta;
+    go[64 + rl] = g;
+  }
+}
+
+// ======================================================================
+// (b) sequential state propagation and chunk outputs
+// ======================================================================
+template <int DK, int NV, bool SOLVE>
+struct FwdSmem {
+  static constexpr int kKS = DK / 64;                 // K slabs of the d_k contractions
+  static constexpr size_t XSZ = DK * 128, QSZ = DK * 128, VSZ = NV * 128;
+  static constexpr size_t TSZ = SOLVE ? 8192 : 0, GSZ = 512;
+  static constexpr size_t STAGE = XSZ + QSZ + VSZ + TSZ + 1024;  // gates padded to 1 KB
+  static constexpr size_t ST0 = 0;
+  static constexpr size_t XVH = 2 * STAGE;            // [(DK+NV) rows][64] K-major
+  static constexpr size_t QH = XVH + (SOLVE ? (DK + NV) * 128 : 0);
+  static constexpr size_t XTT = QH + QSZ;             // [DK rows][64]
+  static constexpr size_t PM = XTT + DK * 128;        // [64][64]
+  static constexpr size_t WB = PM + 8192;             // [64][DK]
+  static constexpr size_t STT = WB + (SOLVE ? DK * 128 : 0);   // S^T: [NV rows][DK]
+  static constexpr size_t DT = STT + NV * DK * 2;     // Delta^T: [NV rows][64]
+  static constexpr size_t OST = DT + NV * 128;        // O staging [64][NV]
+  static constexpr size_t SMALL = OST + NV * 128;     // gamma, dec, g, eta (4 x 64 fp32)
+  static constexpr size_t BAR = SMALL + 4 * 64 * 4;   // full[2], mma
+  static constexpr size_t MISC = BAR + 32;
+  static constexpr size_t TOTAL = MISC + 16 + 1024;
+  static constexpr uint32_t COL_P = 0, COL_WU = 64, COL_D1 = 64 + DK + NV, COL_D2 = COL_D1 + NV,
+                            COL_O = COL_D2 + NV;
+  static_assert(COL_O + NV <= 512, "TMEM budget");
+};
+
+template <int DK, int NV, bool SOLVE>
+__global__ void __launch_bounds__(256, 1)
+    tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  TcArgs a) {
+  using L = FwdSmem<DK, NV, SOLVE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* XVh = sm + L::XVH;
+  uint8_t* Qh = sm + L::QH;
+  uint8_t* XtT = sm + L::XTT;
+  uint8_t* Pm = sm + L::PM;
+  uint8_t* Wb = sm + L::WB;
+  uint8_t* STt = sm + L::STT;
+  uint8_t* DTt = sm + L::DT;
+  uint8_t* Ost = sm + L::OST;
+  float* Gam = reinterpret_cast<float*>(sm + L::SMALL);
+  float* dec = Gam + 64;
+  float* gl = dec + 64;
+  float* et = gl + 64;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint64_t* mbar = full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x, split = blockIdx.y;
+  const int b = bh / a.H, h = bh % a.H;
+  const int c0 = split * NV;  // first value channel of this CTA
+  const int NC = a.NC;
+  auto stage = [&](int s) { return sm + L::ST0 + s * L::STAGE; };
+  auto Xst = [&](int s) { return stage(s); };
+  auto Qst = [&](int s) { return stage(s) + L::XSZ; };
+  auto Vst = [&](int s) { return stage(s) + L::XSZ + L::QSZ; };
+  auto Tst = [&](int s) { return stage(s) + L::XSZ + L::QSZ + L::VSZ; };
+  auto Gst = [&](int s) {
+    return reinterpret_cast<float*>(stage(s) + L::XSZ + L::QSZ + L::VSZ + L::TSZ);
+  };
+
+  auto issue_stage = [&](int c, int s) {
+    const uint32_t bytes = (uint32_t)(L::XSZ + L::QSZ + L::VSZ + L::TSZ + L::GSZ);
+    mbar_arrive_expect_tx(&full[s], bytes);
+    for (int k = 0; k < L::kKS; ++k) {
+      tma_load_4d(Xst(s) + k * 8192, &tm_k, &full[s], 64 * k, h, c * kC - 1, b);
+      tma_load_4d(Qst(s) + k * 8192, &tm_q, &full[s], 64 * k, h, c * kC, b);
+    }
+    tma_load_4d(Vst(s), &tm_v, &full[s], c0, h, c * kC, b);
+    const size_t ci = (size_t)bh * NC + c;
+    if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 8192, 8192, &full[s]);
+    bulk_load(Gst(s), a.ws_g + ci * 128, 512, &full[s]);
+  };
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(mbar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  int issued[2] = {0, 0};  // loads issued per stage (thread 0's bookkeeping)
+  if (tid == 0 && NC > 0) { issue_stage(0, 0); issued[0] = 1; }
+
+  // thread roles on the M = 64 accumulators: row r = 16 * quadrant + lane
+  const int quad = warp & 3;
+  const bool row64 = lane < 16;
+  const int r64 = 16 * quad + lane;
+  const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+  const bool p_role = warp < 4 && row64;             // P, then S rows (d_k = 64)
+  const bool u_role = warp >= 4 && row64;            // W/U, Delta, O rows
+  // S rows: d_k = 64 -> M = 64 layout; d_k = 128 -> M = 128 (lane = row)
+  const bool s_role = (DK == 64) ? p_role : (warp < 4);
+  const int s_row = (DK == 64) ? r64 : 32 * quad + lane;
+
+  // initial state: fp32 rows in registers, bf16 S^T operand in shared memory
+  float sreg[NV];
+#pragma unroll
+  for (int n = 0; n < NV; ++n) sreg[n] = 0.f;
+  if (s_role && a.S_in) {
+    const size_t dv = (size_t)gridDim.y * NV;
+    const float* src = a.S_in + ((size_t)bh * DK + s_row) * dv + c0;
+#pragma unroll
+    for (int n = 0; n < NV; ++n) sreg[n] = src[n];
+  }
+  if (s_role) {
+    uint8_t* base = STt + (s_row >> 6) * (NV * 128);
+#pragma unroll
+    for (int n = 0; n < NV; ++n)
+      *reinterpret_cast<__nv_bfloat16*>(base + sw128(n, s_row & 63)) = __float2bfloat16_rn(sreg[n]);
+  }
+  fence_proxy_async();
+  __syncthreads();
+
+  float ureg[NV];
+  uint32_t mph = 0;
+  for (int c = 0; c < NC; ++c) {
+    const int s = c & 1;
+    const int t0 = c * kC;
+    if (tid == 0 && c + 1 < NC) { issue_stage(c + 1, s ^ 1); ++issued[s ^ 1]; }
+    if (!mbar_wait(&full[s], (c >> 1) & 1)) {
+      *abort_flag = 1;
+      atomicExch(a.status, kStatusTimeout);
+    }
+    if (c == 0 && a.kprev_in) {
+      for (int i = tid; i < DK; i += 256)
+        *reinterpret_cast<__nv_bfloat16*>(Xst(0) + (i >> 6) * 8192 + sw128(0, i & 63)) =
+            a.kprev_in[(size_t)bh * DK + i];
+    }
+    if (tid < 64) {
+      const float* G = Gst(s);
+      const float g = G[64 + tid], glast = G[64 + 63];
+      Gam[tid] = __expf(g);
+      dec[tid] = __expf(glast - g);
+      gl[tid] = g;
+      et[tid] = G[tid];
+    }
+    __syncthreads();
+    if (*abort_flag) break;
+    const float gam_last = Gam[63];
+
+    // ---- operands built from the stage tiles
+    if (SOLVE) {  // [diag(eta Gamma) X | diag(eta) V]^T, rows n, K = chunk rows
+      constexpr int NR = DK + NV;
+      for (int idx = tid; idx < NR * 8; idx += 256) {
+        const int n = idx % NR, j = idx / NR;
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k0 = 8 * j + 2 * e;
+          float v0, v1;
+          if (n < DK) {
+            const uint8_t* xb = Xst(s) + (n >> 6) * 8192;
+            v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xb + sw128(k0, n & 63))) *
+                 et[k0] * Gam[k0];
+            v1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xb + sw128(k0 + 1, n & 63))) *
+                 et[k0 + 1] * Gam[k0 + 1];
+          } else {
+            const int nv = n - DK;
+            v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Vst(s) + sw128(k0, nv))) * et[k0];
+            v1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Vst(s) + sw128(k0 + 1, nv))) *
+                 et[k0 + 1];
+          }
+          pk[e] = pack_bf16(v0, v1);
+        }
+        *reinterpret_cast<uint4*>(XVh + sw128(n, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    } else {  // additive write: Delta = diag(eta) V, stored transposed
+      for (int idx = tid; idx < NV * 8; idx += 256) {
+        const int n = idx % NV, j = idx / NV;
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k0 = 8 * j + 2 * e;
+          const float v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Vst(s) + sw128(k0, n))) * et[k0];
+          const float v1 =
+              __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Vst(s) + sw128(k0 + 1, n))) * et[k0 + 1];
+          pk[e] = pack_bf16(v0, v1);
+        }
+        *reinterpret_cast<uint4*>(DTt + sw128(n, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    // Q~ = diag(Gamma) Q (same layout as the Q tile, row scale)
+    for (int idx = tid; idx < L::kKS * 64 * 8; idx += 256) {
+      const int slab = idx / 512, rem = idx % 512, R = rem >> 3, jj = rem & 7;
+      const size_t off = slab * 8192 + R * 128 + jj * 16;
+      const uint4 in = *reinterpret_cast<const uint4*>(Qst(s) + off);
+      const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
+      const float gr = Gam[R];
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(pin[e]);
+        pk[e] = pack_bf16(f.x * gr, f.y * gr);
+      }
+      *reinterpret_cast<uint4*>(Qh + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    // X~^T = (diag(exp(g_last - g)) X)^T: rows i (key dims), K = chunk rows
+    for (int idx = tid; idx < DK * 8; idx += 256) {
+      const int i = idx % DK, j = idx / DK;
+      const uint8_t* xb = Xst(s) + (i >> 6) * 8192;
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k0 = 8 * j + 2 * e;
+        const float v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xb + sw128(k0, i & 63))) * dec[k0];
+        const float v1 =
+            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xb + sw128(k0 + 1, i & 63))) * dec[k0 + 1];
+        pk[e] = pack_bf16(v0, v1);
+      }
+      *reinterpret_cast<uint4*>(XtT + sw128(i, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- P = Q X^T, [W|U] = T [X^|V^], O = Q~ S0
+    if (tid == 0) {
+      mma_chain(tmem + L::COL_P, Qst(s), 64, Xst(s), 64, DK, idesc_bf16(64, 64), false);
+      if (SOLVE) mma_chain(tmem + L::COL_WU, Tst(s), 64, XVh, DK + NV, 64, idesc_bf16(64, DK + NV), false);
+      mma_chain(tmem + L::COL_O, Qh, 64, STt, NV, DK, idesc_bf16(64, NV), false);
+      umma_commit(mbar);
+    }
+    if (!mbar_wait(mbar, mph)) { *abort_flag = 1; atomicExch(a.status, kStatusTimeout); }
+    mph ^= 1;
+    tc_fence_after();
+    if (warp < 4) {  // P~ = decay-masked P, bf16 K-major rows (lanes 0..15 hold rows)
+      float pv[64];
+      tmem_ld64(tmem + lane_off + L::COL_P, pv);
+      tmem_wait_ld();
+      if (row64) {
+        const float gr = gl[r64];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i0 = 8 * j + 2 * e;
+            const float v0 = (i0 <= r64) ? __expf(gr - gl[i0]) * pv[i0] : 0.f;
+            const float v1 = (i0 + 1 <= r64) ? __expf(gr - gl[i0 + 1]) * pv[i0 + 1] : 0.f;
+            pk[e] = pack_bf16(v0, v1);
+          }
+          *reinterpret_cast<uint4*>(Pm + sw128(r64, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    }
+    if (SOLVE && warp >= 4) {  // W rows -> bf16 operand; U rows kept in registers
+#pragma unroll
+      for (int kk = 0; kk < DK / 64; ++kk) {
+        float wv[64];
+        tmem_ld64(tmem + lane_off + L::COL_WU + 64 * kk, wv);
+        tmem_wait_ld();
+        if (row64) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(wv[8 * j + 2 * e], wv[8 * j + 2 * e + 1]);
+            *reinterpret_cast<uint4*>(Wb + kk * 8192 + sw128(r64, 8 * j)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      }
+      float uv[64];
+      tmem_ld64(tmem + lane_off + L::COL_WU + DK, uv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int n = 0; n < NV; ++n) ureg[n] = uv[n];
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    if (tid == 0) bulk_wait_read0();  // the previous output tile has left O staging
+    __syncthreads();
+    tc_fence_after();
+    if (*abort_flag) break;
+
+    if (SOLVE) {  // Delta = U - W S0
+      if (tid == 0) {
+        mma_chain(tmem + L::COL_D1, Wb, 64, STt, NV, DK, idesc_bf16(64, NV), false);
+        umma_commit(mbar);
+      }
+      if (!mbar_wait(mbar, mph)) { *abort_flag = 1; atomicExch(a.status, kStatusTimeout); }
+      mph ^= 1;
+      tc_fence_after();
+      if (warp >= 4) {
+        float dv1[64];
+        tmem_ld64(tmem + lane_off + L::COL_D1, dv1);
+        tmem_wait_ld();
+        if (row64) {
+#pragma unroll
+          for (int n = 0; n < NV; ++n)
+            *reinterpret_cast<__nv_bfloat16*>(DTt + sw128(n, r64)) = __float2bfloat16_rn(ureg[n] - dv1[n]);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (*abort_flag) break;
+    }
+
+    // ---- state and output: D2 = X~^T Delta, O += P~ Delta
+    if (tid == 0) {
+      mma_chain(tmem + L::COL_D2, XtT, DK, DTt, NV, 64, idesc_bf16(DK, NV), false);
+      mma_chain(tmem + L::COL_O, Pm, 64, DTt, NV, 64, idesc_bf16(64, NV), true);
+      umma_commit(mbar);
+    }
+    if (!mbar_wait(mbar, mph)) { *abort_flag = 1; atomicExch(a.status, kStatusTimeout); }
+    mph ^= 1;
+    tc_fence_after();
+    if (warp < 4) {  // S1 = Gamma_last S0 + D2, then the bf16 S^T operand
+      float d2[64];
+      tmem_ld64(tmem + lane_off + L::COL_D2, d2);
+      tmem_wait_ld();
+      if (s_role) {
+        uint8_t* base = STt + (s_row >> 6) * (NV * 128);
+#pragma unroll
+        for (int n = 0; n < NV; ++n) {
+          sreg[n] = gam_last * sreg[n] + d2[n];
+          *reinterpret_cast<__nv_bfloat16*>(base + sw128(n, s_row & 63)) = __float2bfloat16_rn(sreg[n]);
+        }
+      }
+    } else {  // output rows -> bf16 staging tile
+      float ov[64];
+      tmem_ld64(tmem + lane_off + L::COL_O, ov);
+      tmem_wait_ld();
+      if (row64) {
+#pragma unroll
+        for (int j = 0; j < NV / 8; ++j) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(ov[8 * j + 2 * e], ov[8 * j + 2 * e + 1]);
+          *reinterpret_cast<uint4*>(Ost + sw128(r64, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      tma_store_4d(&tm_o, Ost, c0, h, t0, b);
+      bulk_commit();
+    }
+    if (*abort_flag) break;
+  }
+  if (tid == 0) bulk_wait0();
+  // ---- carry out
+  if (!*abort_flag) {
+    if (s_role && a.S_out) {
+      const size_t dv = (size_t)gridDim.y * NV;
+      float* dst = a.S_out + ((size_t)bh * DK + s_row) * dv + c0;
+#pragma unroll
+      for (int n = 0; n < NV; ++n) dst[n] = sreg[n];
+    }
+    if (split == 0) {
+      if (a.kprev_out)
+        for (int i = tid; i < DK; i += 256)
+          a.kprev_out[(size_t)bh * DK + i] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * DK + i];
+      if (a.pos_out && tid == 0) a.pos_out[bh] = (a.pos_in ? a.pos_in[bh] : 0) + a.T;
+    }
+  } else if (tid == 0) {
+    // drain the loads still in flight before the shared memory goes away
+    // (stage s has completed issued[s] - 1 phases at least; wait for the last one)
+    for (int s = 0; s < 2; ++s)
+      if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1));
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// [B, T, H, D] bf16 tensor, box of 64 columns x `rows` time steps.
+bool make_map(CUtensorMap* m, const void* base, int B, int T, int H, int D, int rows) {
+  EncodeFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct WsLayout {
+  size_t status, T, g, total;
+};
+WsLayout ws_layout(int B, int T, int H, int chunk) {
+  const size_t NC = (size_t)(T + chunk - 1) / chunk;
+  WsLayout w;
+  w.status = 0;
+  w.T = 256;
+  w.g = w.T + (size_t)B * H * NC * 8192;
+  w.total = align_up(w.g + (size_t)B * H * NC * 512, 256);
+  return w;
+}
+
+template <int DK, int NV, bool SOLVE>
+int launch_t(const FwdArgs& fa, const TcArgs& ta) {
+  const int BH = fa.B * fa.H;
+  const int nsplit = fa.dv / NV;
+  CUtensorMap mq, mk, mk128, mv, mo;
+  if (!make_map(&mq, fa.q, fa.B, fa.T, fa.H, DK, 64) || !make_map(&mk, fa.k, fa.B, fa.T, fa.H, DK, 64) ||
+      !make_map(&mk128, fa.k, fa.B, fa.T, fa.H, DK, 128) ||
+      !make_map(&mv, fa.v, fa.B, fa.T, fa.H, fa.dv, 64) || !make_map(&mo, fa.o, fa.B, fa.T, fa.H, fa.dv, 64))
+    return FALCON_ERR_CUDA;
+  {
+    auto k = tc_wy_kernel<DK, SOLVE>;
+    const size_t smem = WySmem<DK>::TOTAL;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return FALCON_ERR_CUDA;
+    dim3 grid((ta.NC + 1) / 2, BH);
+    k<<<grid, 128, smem, fa.stream>>>(mk128, ta);
+  }
+  {
+    auto k = tc_fwd_kernel<DK, NV, SOLVE>;
+    const size_t smem = FwdSmem<DK, NV, SOLVE>::TOTAL;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return FALCON_ERR_CUDA;
+    dim3 grid(BH, nsplit);
+    k<<<grid, 256, smem, fa.stream>>>(mq, mk, mv, mo, ta);
+  }
+  return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
+}
+
+}  // namespace
+
+bool tc_chunk_supported(const FwdArgs& a) {
+  if (a.variant != FALCON_1 && a.variant != FALCON_1A) return false;
+  if (a.dtype != FALCON_BF16 || a.chunk != 64 || a.T < 1) return false;
+  if (a.dk != a.dv || (a.dk != 64 && a.dk != 128)) return false;
+  return true;
+}
+
+int tc_chunk_launches(const FwdArgs&) { return 2; }
+
+size_t tc_chunk_ws_bytes(int B, int T, int H, int, int, int chunk, int) {
+  return ws_layout(B, T, H, chunk).total;
+}
+
+int launch_tc_chunk(const FwdArgs& fa) {
+  const WsLayout w = ws_layout(fa.B, fa.T, fa.H, 64);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(fa.ws);
+  TcArgs ta;
+  ta.B = fa.B; ta.T = fa.T; ta.H = fa.H; ta.NC = (fa.T + kC - 1) / kC;
+  ta.eps = fa.eps; ta.eps_gamma = fa.eps_gamma;
+  ta.beta = fa.beta; ta.lam = fa.lam; ta.pos_in = fa.pos_in;
+  ta.kprev_in = reinterpret_cast<const __nv_bfloat16*>(fa.kprev_in);
+  ta.S_in = fa.S_in;
+  ta.k = reinterpret_cast<const __nv_bfloat16*>(fa.k);
+  ta.S_out = fa.S_out;
+  ta.kprev_out = reinterpret_cast<__nv_bfloat16*>(fa.kprev_out);
+  ta.pos_out = fa.pos_out;
+  ta.ws_T = ws + w.T;
+  ta.ws_g = reinterpret_cast<float*>(ws + w.g);
+  ta.status = reinterpret_cast<uint32_t*>(ws + w.status);
+  ta.NV = 64;
+  const bool solve = fa.variant == FALCON_1;
+  if (fa.dk == 64) return solve ? launch_t<64, 64, true>(fa, ta) : launch_t<64, 64, false>(fa, ta);
+  return solve ? launch_t<128, 64, true>(fa, ta) : launch_t<128, 64, false>(fa, ta);
+}
 
 }  // namespace falcon

@@ -1,0 +1,144 @@
+"""Tensor-core chunk path (tcgen05 / TMEM / TMA): parity with the oracle when
+forced, agreement with the portable path, and a white-box check of the
+per-chunk WY stage (the bf16 T = (I + A)^{-1} images and the gates it leaves
+in the workspace)."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL, oracle_full, params_for, rel_err
+from workloads import FALCON_1, FALCON_1A, LM_F1, Workload, make_carry, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F():
+    import chunked_delta_rule_gb300 as F
+    return F
+
+
+def w_tc(variant, d=64, T=300, B=2, H=2, seed=31):
+    return Workload(f"tc_v{variant}_d{d}", variant, B, T, H, d, d, chunk=64, seed=seed + variant)
+
+
+def decode_T(img: np.ndarray) -> np.ndarray:
+    """bf16 image of a 64x64 K-major tile with the 128-byte swizzle -> matrix."""
+    raw = img.view(np.uint16).reshape(-1)
+    out = np.zeros((64, 64), dtype=np.float32)
+    for R in range(64):
+        for j in range(8):
+            base = (R * 128 + 16 * (j ^ (R & 7))) // 2
+            vals = raw[base:base + 8].astype(np.uint32) << 16
+            out[R, 8 * j:8 * j + 8] = vals.view(np.float32)
+    return out
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_wy_stage_workspace(F, d):
+    w = w_tc(FALCON_1, d=d, T=150, B=1, H=2)
+    x = make_inputs(w, device="cuda")
+    p = params_for(F, w, impl=F.FALCON_IMPL_TC)
+    o = torch.empty((w.B, w.T, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+    n = F.falcon_workspace_size(p)
+    ws = F.alloc_workspace(n)
+    ws.zero_()
+    F.falcon_chunk_fwd(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o, None, ws, n)
+    torch.cuda.synchronize()
+    NC = (w.T + 63) // 64
+    wsn = ws.cpu().numpy()
+    assert int(wsn[:4].view(np.uint32)[0]) == 0, "status word set"
+    t_off = 256
+    g_off = t_off + w.B * w.H * NC * 8192
+    k = x["k"].float().cpu().numpy().astype(np.float64)
+    lam = x["lam"].cpu().numpy().astype(np.float64)
+    beta = x["beta"].cpu().numpy().astype(np.float64)
+    for bh in range(w.B * w.H):
+        b, h = divmod(bh, w.H)
+        for c in range(NC):
+            rows = np.arange(c * 64, c * 64 + 64)
+            X = np.zeros((64, d))
+            for r, t in enumerate(rows):
+                if 1 <= t < w.T:
+                    X[r] = k[b, t - 1, h]
+            ok = rows < w.T
+            ell = np.where(ok, np.log(np.clip(1 - lam[b, np.minimum(rows, w.T - 1), h], 1e-3, 1)), 0)
+            g = np.cumsum(ell)
+            G = X @ X.T
+            eta = np.where(ok & (rows >= 1), beta[b, np.minimum(rows, w.T - 1), h] / (1e-6 + np.diag(G)), 0)
+            A = eta[:, None] * np.exp(np.minimum(g[:, None] - g[None, :], 0)) * G * np.tril(np.ones((64, 64)), -1)
+            Tref = np.linalg.inv(np.eye(64) + A)
+            ci = bh * NC + c
+            Tg = decode_T(wsn[t_off + ci * 8192: t_off + (ci + 1) * 8192])
+            assert np.abs(Tg - Tref).max() <= 2e-2 * np.abs(Tref).max(), (bh, c)
+            gates = wsn[g_off + ci * 512: g_off + (ci + 1) * 512].view(np.float32)
+            assert np.allclose(gates[:64], eta, rtol=2e-3, atol=1e-6), (bh, c)
+            assert np.allclose(gates[64:], g, rtol=1e-4, atol=1e-5), (bh, c)
+
+
+@pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])
+@pytest.mark.parametrize("d", [64, 128])
+def test_tc_forced_matches_oracle(F, variant, d):
+    w = w_tc(variant, d=d)
+    x = make_inputs(w, device="cuda")
+    p = params_for(F, w, impl=F.FALCON_IMPL_TC)
+    assert F.falcon_chunk_fwd_plan(p)[0] == F.FALCON_IMPL_TC
+    o, co = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"])
+    torch.cuda.synchronize()
+    o_ref, c_ref = oracle_full(w, x)
+    e_o = rel_err(o.float().cpu().numpy(), o_ref)
+    e_s = rel_err(co["S"].cpu().numpy(), c_ref["S"])
+    assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"], (e_o, e_s)
+    assert torch.equal(co["k_prev"].cpu(), x["k"][:, -1].cpu())
+    assert torch.all(co["pos"].cpu() == w.T)
+
+
+@pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])
+def test_tc_with_carry(F, variant):
+    w = w_tc(variant, T=200, B=2, H=3)
+    x = make_inputs(w, device="cuda")
+    carry = make_carry(w, 77, torch.tensor([[0, 3, 64], [1, 2, 500]]), device="cuda")
+    p = params_for(F, w, impl=F.FALCON_IMPL_TC)
+    o, co = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], carry)
+    torch.cuda.synchronize()
+    o_ref, c_ref = oracle_full(w, x, carry)
+    assert rel_err(o.float().cpu().numpy(), o_ref) <= TOL["bf16"]
+    assert rel_err(co["S"].cpu().numpy(), c_ref["S"]) <= TOL["bf16"]
+    assert np.array_equal(co["pos"].cpu().numpy(), c_ref["pos"])
+
+
+@pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])
+def test_tc_agrees_with_generic(F, variant):
+    w = w_tc(variant, T=513, B=1, H=4)
+    x = make_inputs(w, device="cuda")
+    outs = {}
+    for impl in (F.FALCON_IMPL_TC, F.FALCON_IMPL_GENERIC):
+        p = params_for(F, w, impl=impl)
+        outs[impl] = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"])
+    torch.cuda.synchronize()
+    (o1, c1), (o2, c2) = outs[F.FALCON_IMPL_TC], outs[F.FALCON_IMPL_GENERIC]
+    assert rel_err(o1.float().cpu().numpy(), o2.float().cpu().numpy()) <= TOL["bf16"]
+    assert rel_err(c1["S"].cpu().numpy(), c2["S"].cpu().numpy()) <= TOL["bf16"]
+
+
+def test_tc_full_size_sampled_heads(F):
+    """Falcon-1, 8 x 2048 x 12 heads, d = 64, bf16, in the launch
+    configuration the benchmark times; sampled heads against the oracle."""
+    import oracle
+    w = LM_F1
+    x = make_inputs(w, device="cuda")
+    p = params_for(F, w)
+    assert F.falcon_chunk_fwd_plan(p)[0] == F.FALCON_IMPL_TC
+    o, co = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"])
+    torch.cuda.synchronize()
+    heads = [(0, 0), (3, 7), (7, 11)]
+    xn = {k: v.cpu().double().numpy() for k, v in x.items()}
+    o_ref, S_ref = oracle.recurrent_heads(xn["q"], xn["k"], xn["v"], xn["beta"], xn["lam"],
+                                          w.variant, heads)
+    for i, (b, h) in enumerate(heads):
+        assert rel_err(o[b, :, h].float().cpu().numpy(), o_ref[i]) <= TOL["bf16"]
+        assert rel_err(co["S"][b, h].cpu().numpy(), S_ref[i]) <= TOL["bf16"]
+    assert torch.isfinite(o.float()).all()
