@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--workload", default="lm124m_f1_8x2048x12_d64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--sets", type=int, default=N_SETS,
+                    help="rotating input sets (fewer only for profiler captures)")
     return ap.parse_args()
 
 
@@ -58,6 +60,20 @@ def algorithmic_bytes(w) -> int:
     th = w.B * w.T * w.H
     beta = th * (w.dv if w.per_channel else 1) * 4
     return th * (2 * w.dk + w.dv + w.dv) * es + beta + th * 4 + w.B * w.H * w.dk * w.dv * 4
+
+
+def kernel_bytes(w, names) -> list:
+    """Algorithmic bytes each kernel of the path must move: the per-chunk WY
+    kernel reads the keys and the gate inputs; the sequential kernel reads
+    q, k, v, writes o and the final state.  Intermediates are not counted."""
+    es = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.T * w.H
+    beta = th * (w.dv if w.per_channel else 1) * 4
+    if names == ["generic_chunk_kernel"]:
+        return [algorithmic_bytes(w)]
+    wy = th * w.dk * es + beta + th * 4
+    fwd = th * (2 * w.dk + 2 * w.dv) * es + w.B * w.H * w.dk * w.dv * 4
+    return [wy, fwd]
 
 
 def algorithmic_flops(w) -> int:
@@ -212,7 +228,7 @@ def main():
     p = F.Params(B=w.B, T=w.T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk, window=w.window,
                  eps=w.eps, eps_gamma=w.eps_gamma, variant=w.variant,
                  dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32)
-    sets = [make_inputs(w, seed=w.seed + 100 * rank + i, device=dev) for i in range(N_SETS)]
+    sets = [make_inputs(w, seed=w.seed + 100 * rank + i, device=dev) for i in range(args.sets)]
     o = torch.empty((w.B, w.T, w.H, w.dv), dtype=sets[0]["q"].dtype, device=dev)
     carry = F.empty_carry(p, dev)
     ws_n = F.falcon_workspace_size(p)
@@ -221,7 +237,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step(i):
-        x = sets[i % N_SETS]
+        x = sets[i % len(sets)]
         F.falcon_chunk_fwd(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o, carry, ws,
                            ws_n, stream)
 
@@ -235,9 +251,13 @@ def main():
     clocks = ClockSampler(gpu_index)
     clocks.start()
     time.sleep(0.3)
-    # per-launch events for the kernel timing, one pair per step
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # per-kernel events: the library records them around each kernel it launches
+    nev = launches + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    for evs in ev:
+        for e in evs:
+            e.record(stream)   # creates the event handles before they are handed over
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -245,9 +265,9 @@ def main():
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
-        step(i)
-        ev[i][1].record(stream)
+        x = sets[i % len(sets)]
+        F.falcon_chunk_fwd_timed(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o, carry,
+                                 ws, ws_n, stream, ev[i])
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -258,7 +278,9 @@ def main():
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    per_call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    kern_ms = [statistics.mean(evs[j].elapsed_time(evs[j + 1]) for evs in ev)
+               for j in range(launches)]
+    per_call_ms = statistics.mean(evs[0].elapsed_time(evs[-1]) for evs in ev)
     ms_step = ms / args.steps
     tokens = w.B * w.T * world
     value = tokens / (ms_step / 1e3)
@@ -304,8 +326,13 @@ def main():
             pass
         hbm_peak = peaks.get("hbm_gbs", 6800.0)
         abytes = algorithmic_bytes(w)
-        kernel = "tc_chunk_fused" if impl_used == F.FALCON_IMPL_TC else "generic_chunk_kernel"
-        achieved = abytes / (per_call_ms / 1e3) / 1e9
+        names = (["tc_wy_kernel", "tc_fwd_kernel"] if impl_used == F.FALCON_IMPL_TC
+                 else ["generic_chunk_kernel"])
+        kbytes = kernel_bytes(w, names)
+        dom = max(range(launches), key=lambda j: kern_ms[j])
+        kernel = names[dom]
+        achieved = kbytes[dom] / (kern_ms[dom] / 1e3) / 1e9
+        step_achieved = abytes / (per_call_ms / 1e3) / 1e9
         line = {
             "metric": "Falcon-1 chunked fwd tokens/s and % of roofline (GB300, T=2048, H=12, d=64)",
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -315,12 +342,16 @@ def main():
             "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                        "chunk": w.chunk, "variant": "falcon1", "global_batch": w.B * world,
                        "seq_len": w.T, "parallelism": f"replicas x{world}",
-                       "l2": f"rotating {N_SETS} input sets ({N_SETS * abytes / 1e6:.0f} MB > 2 x L2)"},
+                       "l2": f"rotating {len(sets)} input sets ({len(sets) * abytes / 1e6:.0f} MB)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": traffic_for(kernel),
                          "kernel": kernel, "algorithmic_bytes": abytes,
                          "algorithmic_flops": algorithmic_flops(w),
-                         "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+                         "kernel_algorithmic_bytes": kbytes[dom],
+                         "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+                         "step_achieved": step_achieved, "step_frac": step_achieved / hbm_peak},
+            "kernels": [{"name": n, "ms": kern_ms[j], "share": kern_ms[j] / sum(kern_ms)}
+                        for j, n in enumerate(names)],
             "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches * args.steps,

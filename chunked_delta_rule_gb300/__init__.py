@@ -24,7 +24,7 @@ FALCON_OK = 0
 EXPORTED = [
     "falcon_workspace_size", "falcon_chunk_fwd", "falcon_recurrent_step",
     "falcon_masked_parallel_workspace_size", "falcon_masked_parallel_ref_gpu",
-    "falcon_strerror", "falcon_version", "falcon_chunk_fwd_plan",
+    "falcon_strerror", "falcon_version", "falcon_chunk_fwd_plan", "falcon_chunk_fwd_timed",
 ]
 
 
@@ -69,6 +69,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.falcon_masked_parallel_workspace_size.restype = S
     lib.falcon_masked_parallel_ref_gpu.argtypes = [P, V, V, V, V, V, V, V, V, S, V]
     lib.falcon_masked_parallel_ref_gpu.restype = ctypes.c_int
+    lib.falcon_chunk_fwd_timed.argtypes = [P, V, V, V, V, V, C, V, C, V, S, V,
+                                           ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
+    lib.falcon_chunk_fwd_timed.restype = ctypes.c_int
     lib.falcon_chunk_fwd_plan.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.falcon_chunk_fwd_plan.restype = ctypes.c_int
     lib.falcon_strerror.argtypes = [ctypes.c_int]
@@ -169,6 +172,22 @@ def falcon_chunk_fwd(p: Params, q, k, v, beta, lam, carry_in: dict | None, o,
                                 ctypes.byref(co) if co is not None else None, _ptr(workspace),
                                 workspace_bytes, _stream(stream))
     _check(code, "falcon_chunk_fwd")
+
+
+def falcon_chunk_fwd_timed(p: Params, q, k, v, beta, lam, carry_in: dict | None, o,
+                           carry_out: dict | None, workspace, workspace_bytes: int, stream,
+                           events: list):
+    """falcon_chunk_fwd recording torch.cuda.Event objects around each kernel."""
+    lib = load_library()
+    ci = make_carry(carry_in)
+    co = make_carry(carry_out)
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    code = lib.falcon_chunk_fwd_timed(ctypes.byref(p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                      _ptr(lam), ctypes.byref(ci) if ci is not None else None,
+                                      _ptr(o), ctypes.byref(co) if co is not None else None,
+                                      _ptr(workspace), workspace_bytes, _stream(stream), arr,
+                                      len(events))
+    _check(code, "falcon_chunk_fwd_timed")
 
 
 def falcon_recurrent_step(p: Params, q, k, v, beta, lam, carry: dict, o, stream=None):

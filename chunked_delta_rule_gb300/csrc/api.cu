@@ -71,10 +71,10 @@ size_t falcon_workspace_size(const falcon_params_t* p) {
   return 0;
 }
 
-int falcon_chunk_fwd(const falcon_params_t* p, const void* q, const void* k, const void* v,
-                     const float* beta, const float* lambda, const falcon_carry_t* carry_in,
-                     void* o, falcon_carry_t* carry_out, void* workspace, size_t workspace_bytes,
-                     void* stream) {
+static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                          const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                          void* o, falcon_carry_t* carry_out, void* workspace,
+                          size_t workspace_bytes, void* stream, void* const* events, int n_events) {
   int st = check_params(p, false);
   if (st != FALCON_OK) return st;
   if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !o)) return FALCON_ERR_INVALID_ARG;
@@ -102,6 +102,8 @@ int falcon_chunk_fwd(const falcon_params_t* p, const void* q, const void* k, con
         if (overlaps(ins[i], nin[i], outs[j], nin[j])) return FALCON_ERR_INVALID_ARG;
   }
   a.ws = workspace; a.ws_bytes = workspace_bytes;
+  a.events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
+  a.n_events = n_events;
   const bool tc_ok = tc_chunk_supported(a);
   if (p->impl == FALCON_IMPL_TC && !tc_ok) return FALCON_ERR_UNSUPPORTED;
   if (p->impl != FALCON_IMPL_GENERIC && tc_ok) {
@@ -112,6 +114,29 @@ int falcon_chunk_fwd(const falcon_params_t* p, const void* q, const void* k, con
     return launch_tc_chunk(a);
   }
   return launch_generic_chunk(a);
+}
+
+int falcon_chunk_fwd(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                     const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                     void* o, falcon_carry_t* carry_out, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  return chunk_fwd_impl(p, q, k, v, beta, lambda, carry_in, o, carry_out, workspace,
+                        workspace_bytes, stream, nullptr, 0);
+}
+
+int falcon_chunk_fwd_timed(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                           const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                           void* o, falcon_carry_t* carry_out, void* workspace,
+                           size_t workspace_bytes, void* stream, void* const* events,
+                           int32_t n_events) {
+  int32_t launches = 0;
+  const int st = falcon_chunk_fwd_plan(p, nullptr, &launches);
+  if (st != FALCON_OK) return st;
+  if (!events || n_events != launches + 1) return FALCON_ERR_INVALID_ARG;
+  for (int i = 0; i < n_events; ++i)
+    if (!events[i]) return FALCON_ERR_INVALID_ARG;
+  return chunk_fwd_impl(p, q, k, v, beta, lambda, carry_in, o, carry_out, workspace,
+                        workspace_bytes, stream, events, n_events);
 }
 
 int falcon_chunk_fwd_plan(const falcon_params_t* p, int32_t* impl_out, int32_t* launches_out) {

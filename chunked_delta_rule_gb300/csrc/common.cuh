@@ -59,7 +59,14 @@ struct FwdArgs {
   void* ws;
   size_t ws_bytes;
   cudaStream_t stream;
+  cudaEvent_t* events;      // optional: recorded before the first and after every kernel
+  int n_events;
 };
+
+// Record the caller's event i on the stream (no-op without events).
+inline void record_event(const FwdArgs& a, int i) {
+  if (a.events && i < a.n_events) cudaEventRecord(a.events[i], a.stream);
+}
 
 // Launchers (each returns a FALCON_* code; host-side checks only).
 int launch_generic_chunk(const FwdArgs& a);

@@ -336,6 +336,7 @@ int launch_generic_chunk(const FwdArgs& a) {
   const size_t smem = generic_chunk_smem_bytes(a.dk, dvs, c, a.W);
   if (smem > 227 * 1024) return FALCON_ERR_UNSUPPORTED;
   dim3 grid(a.B * a.H, (a.dv + dvs - 1) / dvs);
+  record_event(a, 0);
   if (a.dtype == FALCON_BF16) {
     auto k = generic_chunk_kernel<__nv_bfloat16>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -347,6 +348,7 @@ int launch_generic_chunk(const FwdArgs& a) {
       return FALCON_ERR_CUDA;
     k<<<grid, kThreads, smem, a.stream>>>(a, c, dvs);
   }
+  record_event(a, 1);
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
 

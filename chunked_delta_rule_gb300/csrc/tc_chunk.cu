@@ -773,7 +773,9 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return FALCON_ERR_CUDA;
     dim3 grid((ta.NC + 1) / 2, BH);
+    record_event(fa, 0);
     k<<<grid, 128, smem, fa.stream>>>(mk128, ta);
+    record_event(fa, 1);
   }
   {
     auto k = tc_fwd_kernel<DK, NV, SOLVE>;
@@ -782,6 +784,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       return FALCON_ERR_CUDA;
     dim3 grid(BH, nsplit);
     k<<<grid, 256, smem, fa.stream>>>(mq, mk, mv, mo, ta);
+    record_event(fa, 2);
   }
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }

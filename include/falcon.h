@@ -139,6 +139,18 @@ int falcon_chunk_fwd(const falcon_params_t* p, const void* q, const void* k, con
                      void* o, falcon_carry_t* carry_out, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* falcon_chunk_fwd, plus timing hooks: records the caller's CUDA events
+ * (cudaEvent_t handles passed as void*) on `stream`, events[0] before the
+ * first kernel of the call and events[i] right after kernel i.  n_events must
+ * equal the launch count falcon_chunk_fwd_plan reports plus one.  The work
+ * done is exactly that of falcon_chunk_fwd.  Errors: those of
+ * falcon_chunk_fwd, and FALCON_ERR_INVALID_ARG for a bad event list. */
+int falcon_chunk_fwd_timed(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                           const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                           void* o, falcon_carry_t* carry_out, void* workspace,
+                           size_t workspace_bytes, void* stream, void* const* events,
+                           int32_t n_events);
+
 /* Which kernel family falcon_chunk_fwd uses for these params
  * (FALCON_IMPL_GENERIC or FALCON_IMPL_TC, written to *impl_out) and how many
  * kernels one call enqueues (*launches_out).  Host-only; either output
