@@ -328,27 +328,77 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
 // ======================================================================
 template <int DK, int NV, bool SOLVE>
 struct FwdSmem {
-  static constexpr int kKS = DK / 64;                 // K slabs of the d_k contractions
+  static constexpr int kKS = DK / 64;                 // 64-column slabs of the d_k contractions
   static constexpr size_t XSZ = DK * 128, QSZ = DK * 128, VSZ = NV * 128;
   static constexpr size_t TSZ = SOLVE ? 8192 : 0, GSZ = 512;
   static constexpr size_t STAGE = XSZ + QSZ + VSZ + TSZ + 1024;  // gates padded to 1 KB
   static constexpr size_t ST0 = 0;
-  static constexpr size_t XVH = 2 * STAGE;            // [(DK+NV) rows][64] K-major
-  static constexpr size_t QH = XVH + (SOLVE ? (DK + NV) * 128 : 0);
-  static constexpr size_t XTT = QH + QSZ;             // [DK rows][64]
-  static constexpr size_t PM = XTT + DK * 128;        // [64][64]
-  static constexpr size_t WB = PM + 8192;             // [64][DK]
-  static constexpr size_t STT = WB + (SOLVE ? DK * 128 : 0);   // S^T: [NV rows][DK]
-  static constexpr size_t DT = STT + NV * DK * 2;     // Delta^T: [NV rows][64]
-  static constexpr size_t OST = DT + NV * 128;        // O staging [64][NV]
-  static constexpr size_t SMALL = OST + NV * 128;     // gamma, dec, g, eta (4 x 64 fp32)
-  static constexpr size_t BAR = SMALL + 4 * 64 * 4;   // full[2], mma
+  static constexpr size_t XH = 2 * STAGE;              // diag(eta Gamma) X, rows (MN-major B)
+  static constexpr size_t VH = XH + (SOLVE ? XSZ : 0); // diag(eta) V, rows (MN-major B)
+  static constexpr size_t PM = VH + VSZ;               // decay-masked Q X^T, K-major rows
+  static constexpr size_t WB = PM + 8192;              // W rows, K-major [64][DK]
+  static constexpr size_t SB = WB + (SOLVE ? DK * 128 : 0);   // S rows, MN-major [DK][NV]
+  static constexpr size_t DL = SB + DK * 128;          // Delta rows (MN-major B)
+  static constexpr size_t DD = DL + (SOLVE ? VSZ : 0); // diag(exp(g_last - g)) Delta rows
+  static constexpr size_t OST = DD + VSZ;              // output staging [64][NV]
+  static constexpr size_t SMALL = OST + NV * 128;      // gamma, dec, g, eta (4 x 64 fp32)
+  static constexpr size_t BAR = SMALL + 4 * 64 * 4;    // full[2], mma
   static constexpr size_t MISC = BAR + 32;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
-  static constexpr uint32_t COL_P = 0, COL_WU = 64, COL_D1 = 64 + DK + NV, COL_D2 = COL_D1 + NV,
-                            COL_O = COL_D2 + NV;
-  static_assert(COL_O + NV <= 512, "TMEM budget");
+  // TMEM columns: P and later P~ Delta share one block, W and later X~^T Delta another
+  static constexpr uint32_t COL_P = 0, COL_W = 64, COL_U = 64 + DK, COL_D1 = COL_U + NV,
+                            COL_OA = COL_D1 + NV, NCOL = COL_OA + NV;
+  static_assert(NCOL <= 512, "TMEM budget");
+  static_assert(NV == 64, "value slice of 64 channels");
 };
+
+// MN-major operand chain: D = A^T-or-B with 64 elements along M/N, K rows of
+// 128 B in the swizzled layout; K steps of 16 rows = 2048 B.
+__device__ __forceinline__ void mma_chain_mn(uint32_t d_tmem, uint64_t (*adesc)(uint32_t, int),
+                                             uint32_t a0, uint64_t (*bdesc)(uint32_t, int),
+                                             uint32_t b0, int K, uint32_t idesc, bool accumulate) {
+  for (int ks = 0; ks < K / 16; ++ks)
+    umma_bf16(d_tmem, adesc(a0, ks), bdesc(b0, ks), idesc, (ks > 0 || accumulate) ? 1u : 0u);
+}
+// descriptor of K step ks for a K-major operand (64-col slabs of `rows` rows)
+template <int ROWS>
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int ks) {
+  return sdesc_k128(base + (ks >> 2) * ROWS * 128 + (ks & 3) * 32);
+}
+// descriptor of K step ks for an MN-major operand (16 K rows per step)
+__device__ __forceinline__ uint64_t mndesc(uint32_t base, int ks) {
+  return sdesc_mn128(base + ks * 2048);
+}
+
+// Row r (K-major or MN-major rows of 64 bf16 are the same swizzled image):
+// write 64 fp32 values as bf16 with 16-byte stores.
+__device__ __forceinline__ void store_row64(uint8_t* tile, int r, const float* v) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+    *reinterpret_cast<uint4*>(tile + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+// Scale every row of a [64 x 64] bf16 swizzled tile by f[row] into dst (16-byte chunks).
+__device__ __forceinline__ void scale_rows(uint8_t* dst, const uint8_t* src, const float* f,
+                                           int tid, int nthreads) {
+  for (int idx = tid; idx < 512; idx += nthreads) {
+    const int R = idx >> 3;
+    const uint4 in = *reinterpret_cast<const uint4*>(src + idx * 16);
+    const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
+    const float fr = f[R];
+    uint32_t pk[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(pin[e]);
+      pk[e] = pack_bf16(x.x * fr, x.y * fr);
+    }
+    *reinterpret_cast<uint4*>(dst + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
 
 template <int DK, int NV, bool SOLVE>
 __global__ void __launch_bounds__(256, 1)
@@ -358,13 +408,13 @@ __global__ void __launch_bounds__(256, 1)
   using L = FwdSmem<DK, NV, SOLVE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* XVh = sm + L::XVH;
-  uint8_t* Qh = sm + L::QH;
-  uint8_t* XtT = sm + L::XTT;
+  uint8_t* XH = sm + L::XH;
+  uint8_t* VH = sm + L::VH;
   uint8_t* Pm = sm + L::PM;
   uint8_t* Wb = sm + L::WB;
-  uint8_t* STt = sm + L::STT;
-  uint8_t* DTt = sm + L::DT;
+  uint8_t* SB = sm + L::SB;
+  uint8_t* DL = SOLVE ? sm + L::DL : sm + L::VH;  // additive write: Delta = diag(eta) V
+  uint8_t* DD = sm + L::DD;
   uint8_t* Ost = sm + L::OST;
   float* Gam = reinterpret_cast<float*>(sm + L::SMALL);
   float* dec = Gam + 64;
@@ -418,217 +468,185 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   int issued[2] = {0, 0};  // loads issued per stage (thread 0's bookkeeping)
-  if (tid == 0 && NC > 0) { issue_stage(0, 0); issued[0] = 1; }
+  if (tid == 0 && NC > 0) {
+    issue_stage(0, 0);
+    issued[0] = 1;
+  }
 
-  // thread roles on the M = 64 accumulators: row r = 16 * quadrant + lane
+  // Thread roles on the M = 64 accumulators: rows r = 16 * quadrant + lane
+  // live in lanes 0..15 of each TMEM quadrant.  Warps 0..3 keep S rows 0..63
+  // in registers; for d_k = 128, warps 4..7 keep rows 64..127.  The output
+  // epilogue runs on the warps that hold no second S half.
   const int quad = warp & 3;
   const bool row64 = lane < 16;
   const int r64 = 16 * quad + lane;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-  const bool p_role = warp < 4 && row64;             // P, then S rows (d_k = 64)
-  const bool u_role = warp >= 4 && row64;            // W/U, Delta, O rows
-  // S rows: d_k = 64 -> M = 64 layout; d_k = 128 -> M = 128 (lane = row)
-  const bool s_role = (DK == 64) ? p_role : (warp < 4);
-  const int s_row = (DK == 64) ? r64 : 32 * quad + lane;
+  const bool lo = warp < 4;
+  const bool s_warp = lo || DK == 128;
+  const int s_row = lo ? r64 : 64 + r64;
+  const bool o_warp = (DK == 64) ? !lo : lo;
+  const uint32_t col_d2 = L::COL_W + (lo ? 0 : 64);
 
-  // initial state: fp32 rows in registers, bf16 S^T operand in shared memory
   float sreg[NV];
 #pragma unroll
   for (int n = 0; n < NV; ++n) sreg[n] = 0.f;
-  if (s_role && a.S_in) {
+  if (s_warp && row64 && a.S_in) {
     const size_t dv = (size_t)gridDim.y * NV;
     const float* src = a.S_in + ((size_t)bh * DK + s_row) * dv + c0;
 #pragma unroll
     for (int n = 0; n < NV; ++n) sreg[n] = src[n];
   }
-  if (s_role) {
-    uint8_t* base = STt + (s_row >> 6) * (NV * 128);
-#pragma unroll
-    for (int n = 0; n < NV; ++n)
-      *reinterpret_cast<__nv_bfloat16*>(base + sw128(n, s_row & 63)) = __float2bfloat16_rn(sreg[n]);
-  }
+  if (s_warp && row64) store_row64(SB, s_row, sreg);
   fence_proxy_async();
   __syncthreads();
 
+  const uint32_t sP = smem_u32(Pm), sW = smem_u32(Wb), sS = smem_u32(SB), sDL = smem_u32(DL),
+                 sDD = smem_u32(DD), sXH = smem_u32(XH), sVH = smem_u32(VH);
   float ureg[NV];
   uint32_t mph = 0;
   for (int c = 0; c < NC; ++c) {
     const int s = c & 1;
     const int t0 = c * kC;
-    if (tid == 0 && c + 1 < NC) { issue_stage(c + 1, s ^ 1); ++issued[s ^ 1]; }
+    if (tid == 0 && c + 1 < NC) {
+      issue_stage(c + 1, s ^ 1);
+      ++issued[s ^ 1];
+    }
     if (!mbar_wait(&full[s], (c >> 1) & 1)) {
       *abort_flag = 1;
       atomicExch(a.status, kStatusTimeout);
     }
-    if (c == 0 && a.kprev_in) {
+    if (c == 0 && a.kprev_in) {  // x_0 = carried key
       for (int i = tid; i < DK; i += 256)
         *reinterpret_cast<__nv_bfloat16*>(Xst(0) + (i >> 6) * 8192 + sw128(0, i & 63)) =
             a.kprev_in[(size_t)bh * DK + i];
     }
     if (tid < 64) {
       const float* G = Gst(s);
-      const float g = G[64 + tid], glast = G[64 + 63];
-      Gam[tid] = __expf(g);
+      const float g = G[64 + tid], glast = G[64 + 63], e = G[tid];
+      const float gm = __expf(g);
+      Gam[tid] = gm;
       dec[tid] = __expf(glast - g);
       gl[tid] = g;
-      et[tid] = G[tid];
+      et[tid] = SOLVE ? e * gm : e;  // row scale of X (Falcon-1) or of V (Falcon-1A)
     }
     __syncthreads();
     if (*abort_flag) break;
     const float gam_last = Gam[63];
 
-    // ---- operands built from the stage tiles
-    if (SOLVE) {  // [diag(eta Gamma) X | diag(eta) V]^T, rows n, K = chunk rows
-      constexpr int NR = DK + NV;
-      for (int idx = tid; idx < NR * 8; idx += 256) {
-        const int n = idx % NR, j = idx / NR;
+    // ---- row-scaled operands (16-byte chunks)
+    if (SOLVE) {
+      for (int k = 0; k < L::kKS; ++k) scale_rows(XH + k * 8192, Xst(s) + k * 8192, et, tid, 256);
+      // diag(eta) V: eta = et / Gamma
+      for (int idx = tid; idx < 512; idx += 256) {
+        const int R = idx >> 3;
+        const uint4 in = *reinterpret_cast<const uint4*>(Vst(s) + idx * 16);
+        const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
+        const float fr = Gst(s)[R];
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int k0 = 8 * j + 2 * e;
-          float v0, v1;
-          if (n < DK) {
-            const uint8_t* xb = Xst(s) + (n >> 6) * 8192;
-            v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xb + sw128(k0, n & 63))) *
-                 et[k0] * Gam[k0];
-            v1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xb + sw128(k0 + 1, n & 63))) *
-                 et[k0 + 1] * Gam[k0 + 1];
-          } else {
-            const int nv = n - DK;
-            v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Vst(s) + sw128(k0, nv))) * et[k0];
-            v1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Vst(s) + sw128(k0 + 1, nv))) *
-                 et[k0 + 1];
-          }
-          pk[e] = pack_bf16(v0, v1);
+          const float2 x = __bfloat1622float2(pin[e]);
+          pk[e] = pack_bf16(x.x * fr, x.y * fr);
         }
-        *reinterpret_cast<uint4*>(XVh + sw128(n, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(VH + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-    } else {  // additive write: Delta = diag(eta) V, stored transposed
-      for (int idx = tid; idx < NV * 8; idx += 256) {
-        const int n = idx % NV, j = idx / NV;
+    } else {
+      scale_rows(VH, Vst(s), et, tid, 256);  // Delta = diag(eta) V
+      for (int idx = tid; idx < 512; idx += 256) {  // diag(exp(g_last - g) eta) V
+        const int R = idx >> 3;
+        const uint4 in = *reinterpret_cast<const uint4*>(Vst(s) + idx * 16);
+        const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
+        const float fr = et[R] * dec[R];
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int k0 = 8 * j + 2 * e;
-          const float v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Vst(s) + sw128(k0, n))) * et[k0];
-          const float v1 =
-              __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Vst(s) + sw128(k0 + 1, n))) * et[k0 + 1];
-          pk[e] = pack_bf16(v0, v1);
+          const float2 x = __bfloat1622float2(pin[e]);
+          pk[e] = pack_bf16(x.x * fr, x.y * fr);
         }
-        *reinterpret_cast<uint4*>(DTt + sw128(n, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(DD + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-    }
-    // Q~ = diag(Gamma) Q (same layout as the Q tile, row scale)
-    for (int idx = tid; idx < L::kKS * 64 * 8; idx += 256) {
-      const int slab = idx / 512, rem = idx % 512, R = rem >> 3, jj = rem & 7;
-      const size_t off = slab * 8192 + R * 128 + jj * 16;
-      const uint4 in = *reinterpret_cast<const uint4*>(Qst(s) + off);
-      const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-      const float gr = Gam[R];
-      uint32_t pk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(pin[e]);
-        pk[e] = pack_bf16(f.x * gr, f.y * gr);
-      }
-      *reinterpret_cast<uint4*>(Qh + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-    // X~^T = (diag(exp(g_last - g)) X)^T: rows i (key dims), K = chunk rows
-    for (int idx = tid; idx < DK * 8; idx += 256) {
-      const int i = idx % DK, j = idx / DK;
-      const uint8_t* xb = Xst(s) + (i >> 6) * 8192;
-      uint32_t pk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int k0 = 8 * j + 2 * e;
-        const float v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xb + sw128(k0, i & 63))) * dec[k0];
-        const float v1 =
-            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xb + sw128(k0 + 1, i & 63))) * dec[k0 + 1];
-        pk[e] = pack_bf16(v0, v1);
-      }
-      *reinterpret_cast<uint4*>(XtT + sw128(i, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- P = Q X^T, [W|U] = T [X^|V^], O = Q~ S0
+    // ---- P = Q X^T, W = T X^, U = T V^, Oa = Q S0
     if (tid == 0) {
-      mma_chain(tmem + L::COL_P, Qst(s), 64, Xst(s), 64, DK, idesc_bf16(64, 64), false);
-      if (SOLVE) mma_chain(tmem + L::COL_WU, Tst(s), 64, XVh, DK + NV, 64, idesc_bf16(64, DK + NV), false);
-      mma_chain(tmem + L::COL_O, Qh, 64, STt, NV, DK, idesc_bf16(64, NV), false);
+      const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s)), sT = smem_u32(Tst(s));
+      mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, DK, idesc_bf16(64, 64), false);
+      if (SOLVE) {
+        for (int k = 0; k < L::kKS; ++k)
+          mma_chain_mn(tmem + L::COL_W + 64 * k, kdesc<64>, sT, mndesc, sXH + k * 8192, 64,
+                       idesc_bf16(64, 64, false, true), false);
+        mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT, mndesc, sVH, 64, idesc_bf16(64, NV, false, true),
+                     false);
+      }
+      mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
+                   false);
       umma_commit(mbar);
     }
-    if (!mbar_wait(mbar, mph)) { *abort_flag = 1; atomicExch(a.status, kStatusTimeout); }
+    if (!mbar_wait(mbar, mph)) {
+      *abort_flag = 1;
+      atomicExch(a.status, kStatusTimeout);
+    }
     mph ^= 1;
     tc_fence_after();
-    if (warp < 4) {  // P~ = decay-masked P, bf16 K-major rows (lanes 0..15 hold rows)
+    if (lo) {  // P~ = decay-masked P
       float pv[64];
       tmem_ld64(tmem + lane_off + L::COL_P, pv);
       tmem_wait_ld();
       if (row64) {
         const float gr = gl[r64];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = 8 * j + 2 * e;
-            const float v0 = (i0 <= r64) ? __expf(gr - gl[i0]) * pv[i0] : 0.f;
-            const float v1 = (i0 + 1 <= r64) ? __expf(gr - gl[i0 + 1]) * pv[i0 + 1] : 0.f;
-            pk[e] = pack_bf16(v0, v1);
-          }
-          *reinterpret_cast<uint4*>(Pm + sw128(r64, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
+        for (int i = 0; i < 64; ++i) pv[i] = (i <= r64) ? __expf(gr - gl[i]) * pv[i] : 0.f;
+        store_row64(Pm, r64, pv);
       }
-    }
-    if (SOLVE && warp >= 4) {  // W rows -> bf16 operand; U rows kept in registers
+    } else if (SOLVE) {  // W rows -> K-major operand, U rows -> registers
 #pragma unroll
-      for (int kk = 0; kk < DK / 64; ++kk) {
+      for (int k = 0; k < L::kKS; ++k) {
         float wv[64];
-        tmem_ld64(tmem + lane_off + L::COL_WU + 64 * kk, wv);
+        tmem_ld64(tmem + lane_off + L::COL_W + 64 * k, wv);
         tmem_wait_ld();
-        if (row64) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(wv[8 * j + 2 * e], wv[8 * j + 2 * e + 1]);
-            *reinterpret_cast<uint4*>(Wb + kk * 8192 + sw128(r64, 8 * j)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-        }
+        if (row64) store_row64(Wb + k * 8192, r64, wv);
       }
       float uv[64];
-      tmem_ld64(tmem + lane_off + L::COL_WU + DK, uv);
+      tmem_ld64(tmem + lane_off + L::COL_U, uv);
       tmem_wait_ld();
 #pragma unroll
       for (int n = 0; n < NV; ++n) ureg[n] = uv[n];
     }
     fence_proxy_async();
     tc_fence_before();
-    if (tid == 0) bulk_wait_read0();  // the previous output tile has left O staging
+    if (tid == 0) bulk_wait_read0();  // the previous output tile has left the staging buffer
     __syncthreads();
     tc_fence_after();
     if (*abort_flag) break;
 
     if (SOLVE) {  // Delta = U - W S0
       if (tid == 0) {
-        mma_chain(tmem + L::COL_D1, Wb, 64, STt, NV, DK, idesc_bf16(64, NV), false);
+        mma_chain_mn(tmem + L::COL_D1, kdesc<64>, sW, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
+                     false);
         umma_commit(mbar);
       }
-      if (!mbar_wait(mbar, mph)) { *abort_flag = 1; atomicExch(a.status, kStatusTimeout); }
+      if (!mbar_wait(mbar, mph)) {
+        *abort_flag = 1;
+        atomicExch(a.status, kStatusTimeout);
+      }
       mph ^= 1;
       tc_fence_after();
-      if (warp >= 4) {
+      if (!lo) {
         float dv1[64];
         tmem_ld64(tmem + lane_off + L::COL_D1, dv1);
         tmem_wait_ld();
         if (row64) {
 #pragma unroll
-          for (int n = 0; n < NV; ++n)
-            *reinterpret_cast<__nv_bfloat16*>(DTt + sw128(n, r64)) = __float2bfloat16_rn(ureg[n] - dv1[n]);
+          for (int n = 0; n < NV; ++n) dv1[n] = ureg[n] - dv1[n];
+          store_row64(DL, r64, dv1);
+          const float dr = dec[r64];
+#pragma unroll
+          for (int n = 0; n < NV; ++n) dv1[n] *= dr;
+          store_row64(DD, r64, dv1);
         }
       }
       fence_proxy_async();
@@ -638,38 +656,53 @@ __global__ void __launch_bounds__(256, 1)
       if (*abort_flag) break;
     }
 
-    // ---- state and output: D2 = X~^T Delta, O += P~ Delta
+    // ---- D2 = X^T diag(exp(g_last - g)) Delta, Ob = P~ Delta
     if (tid == 0) {
-      mma_chain(tmem + L::COL_D2, XtT, DK, DTt, NV, 64, idesc_bf16(DK, NV), false);
-      mma_chain(tmem + L::COL_O, Pm, 64, DTt, NV, 64, idesc_bf16(64, NV), true);
+      const uint32_t sX = smem_u32(Xst(s));
+      for (int k = 0; k < L::kKS; ++k)
+        mma_chain_mn(tmem + L::COL_W + 64 * k, mndesc, sX + k * 8192, mndesc, sDD, 64,
+                     idesc_bf16(64, NV, true, true), false);
+      mma_chain_mn(tmem + L::COL_P, kdesc<64>, sP, mndesc, sDL, 64, idesc_bf16(64, NV, false, true),
+                   false);
       umma_commit(mbar);
     }
-    if (!mbar_wait(mbar, mph)) { *abort_flag = 1; atomicExch(a.status, kStatusTimeout); }
+    if (!mbar_wait(mbar, mph)) {
+      *abort_flag = 1;
+      atomicExch(a.status, kStatusTimeout);
+    }
     mph ^= 1;
     tc_fence_after();
-    if (warp < 4) {  // S1 = Gamma_last S0 + D2, then the bf16 S^T operand
+    if (s_warp) {  // S1 = Gamma_last S0 + D2
       float d2[64];
-      tmem_ld64(tmem + lane_off + L::COL_D2, d2);
-      tmem_wait_ld();
-      if (s_role) {
-        uint8_t* base = STt + (s_row >> 6) * (NV * 128);
-#pragma unroll
-        for (int n = 0; n < NV; ++n) {
-          sreg[n] = gam_last * sreg[n] + d2[n];
-          *reinterpret_cast<__nv_bfloat16*>(base + sw128(n, s_row & 63)) = __float2bfloat16_rn(sreg[n]);
-        }
-      }
-    } else {  // output rows -> bf16 staging tile
-      float ov[64];
-      tmem_ld64(tmem + lane_off + L::COL_O, ov);
+      tmem_ld64(tmem + lane_off + col_d2, d2);
       tmem_wait_ld();
       if (row64) {
 #pragma unroll
-        for (int j = 0; j < NV / 8; ++j) {
-          uint32_t pk[4];
+        for (int n = 0; n < NV; ++n) sreg[n] = gam_last * sreg[n] + d2[n];
+        store_row64(SB, s_row, sreg);
+      }
+    }
+    if (o_warp) {  // O = diag(Gamma) Oa + Ob, in two 32-column halves
+      const float gr = Gam[r64];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(ov[8 * j + 2 * e], ov[8 * j + 2 * e + 1]);
-          *reinterpret_cast<uint4*>(Ost + sw128(r64, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t oa[32], ob[32];
+        tmem_ld32(tmem + lane_off + L::COL_OA + 32 * hf, oa);
+        tmem_ld32(tmem + lane_off + L::COL_P + 32 * hf, ob);
+        tmem_wait_ld();
+        if (row64) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int n = 8 * j + 2 * e;
+              pk[e] = pack_bf16(gr * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
+                                gr * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
+            }
+            *reinterpret_cast<uint4*>(Ost + sw128(r64, 32 * hf + 8 * j)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
         }
       }
     }
@@ -686,7 +719,7 @@ __global__ void __launch_bounds__(256, 1)
   if (tid == 0) bulk_wait0();
   // ---- carry out
   if (!*abort_flag) {
-    if (s_role && a.S_out) {
+    if (s_warp && row64 && a.S_out) {
       const size_t dv = (size_t)gridDim.y * NV;
       float* dst = a.S_out + ((size_t)bh * DK + s_row) * dv + c0;
 #pragma unroll
@@ -700,7 +733,6 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (tid == 0) {
     // drain the loads still in flight before the shared memory goes away
-    // (stage s has completed issued[s] - 1 phases at least; wait for the last one)
     for (int s = 0; s < 2; ++s)
       if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1));
   }

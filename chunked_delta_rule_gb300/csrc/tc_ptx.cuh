@@ -165,10 +165,26 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// Shared-memory matrix descriptor, MN-major operand with the 128-byte swizzle
+// and exactly 64 elements along M (or N): rows of 64 bf16 along M/N, one row
+// per K index, 8-row atoms of 1024 B stacked along K.  Both byte offsets are
+// 1024: the K-direction atom stride; the M/N-direction one is never used
+// with a single 64-wide atom.  A K step of 16 advances the start by 2048 B.
+__device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1024 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> fp32; a_mn / b_mn select MN-major
+// (transposed) A / B operands, otherwise K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = false, bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Byte offset of element (row, col) of a K-major 128B-swizzled bf16 tile
