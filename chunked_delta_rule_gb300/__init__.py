@@ -25,6 +25,7 @@ EXPORTED = [
     "falcon_workspace_size", "falcon_chunk_fwd", "falcon_recurrent_step",
     "falcon_masked_parallel_workspace_size", "falcon_masked_parallel_ref_gpu",
     "falcon_strerror", "falcon_version", "falcon_chunk_fwd_plan", "falcon_chunk_fwd_timed",
+    "falcon_chunk_fwd_noalloc",
 ]
 
 
@@ -72,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.falcon_chunk_fwd_timed.argtypes = [P, V, V, V, V, V, C, V, C, V, S, V,
                                            ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
     lib.falcon_chunk_fwd_timed.restype = ctypes.c_int
+    lib.falcon_chunk_fwd_noalloc.argtypes = [P, V, V, V, V, V, C, V, C, V]
+    lib.falcon_chunk_fwd_noalloc.restype = ctypes.c_int
     lib.falcon_chunk_fwd_plan.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.falcon_chunk_fwd_plan.restype = ctypes.c_int
     lib.falcon_strerror.argtypes = [ctypes.c_int]
@@ -188,6 +191,20 @@ def falcon_chunk_fwd_timed(p: Params, q, k, v, beta, lam, carry_in: dict | None,
                                       _ptr(workspace), workspace_bytes, _stream(stream), arr,
                                       len(events))
     _check(code, "falcon_chunk_fwd_timed")
+
+
+def falcon_chunk_fwd_noalloc(p: Params, q, k, v, beta, lam, carry_in: dict | None, o,
+                             carry_out: dict | None, stream=None):
+    """falcon_chunk_fwd without a workspace argument, for callers that cannot
+    allocate device memory: the library uses its own fixed scratch array."""
+    lib = load_library()
+    ci = make_carry(carry_in)
+    co = make_carry(carry_out)
+    code = lib.falcon_chunk_fwd_noalloc(ctypes.byref(p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                        _ptr(lam), ctypes.byref(ci) if ci is not None else None,
+                                        _ptr(o), ctypes.byref(co) if co is not None else None,
+                                        _stream(stream))
+    _check(code, "falcon_chunk_fwd_noalloc")
 
 
 def falcon_recurrent_step(p: Params, q, k, v, beta, lam, carry: dict, o, stream=None):

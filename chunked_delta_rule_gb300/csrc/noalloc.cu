@@ -1,0 +1,63 @@
+// Chunk forward for callers that cannot allocate device memory.
+//
+// Some hosts hand a kernel library nothing but input/output pointers and a
+// stream: plugin interfaces of inference runtimes that expose no allocator,
+// or services that fix their memory budget at start-up and forbid any
+// allocation while serving.  Such callers cannot provide the scratch buffer
+// falcon_chunk_fwd asks for.  This entry point runs the same tensor-core
+// kernels with their scratch in a fixed array that lives in the library's
+// own device image instead.
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+// 32 MiB: enough for B * H * ceil(T / 64) <= 3855 chunks of the tensor-core
+// path (8 KB of T image + 512 B of gates per chunk, plus a 256-byte status
+// word).  Every device that loads the library holds this array until exit.
+constexpr size_t kScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the array on the current device (looked up once per
+// device).  In host code the array's name is only a host-side stand-in, so
+// the address must come from the runtime.
+int scratch_on_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FALCON_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FALCON_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FALCON_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return FALCON_OK;
+}
+
+}  // namespace
+
+extern "C" int falcon_chunk_fwd_noalloc(const falcon_params_t* p, const void* q, const void* k,
+                                        const void* v, const float* beta, const float* lambda,
+                                        const falcon_carry_t* carry_in, void* o,
+                                        falcon_carry_t* carry_out, void* stream) {
+  int32_t impl = 0;
+  int st = falcon_chunk_fwd_plan(p, &impl, nullptr);
+  if (st != FALCON_OK) return st;
+  if (impl != FALCON_IMPL_TC) return FALCON_ERR_UNSUPPORTED;
+  if (falcon_workspace_size(p) > kScratchBytes) return FALCON_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = scratch_on_current_device(&scratch);
+  if (st != FALCON_OK) return st;
+  // the status word is the one part of the scratch that must start at zero
+  if (cudaMemsetAsync(scratch, 0, 256, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FALCON_ERR_CUDA;
+  return falcon_chunk_fwd(p, q, k, v, beta, lambda, carry_in, o, carry_out, scratch, kScratchBytes,
+                          stream);
+}

@@ -151,6 +151,30 @@ int falcon_chunk_fwd_timed(const falcon_params_t* p, const void* q, const void* 
                            size_t workspace_bytes, void* stream, void* const* events,
                            int32_t n_events);
 
+/* falcon_chunk_fwd for callers that cannot allocate device memory.  The
+ * pages have no counterpart to this entry point; it exists for hosts that
+ * pass a kernel library only tensors and a stream (plugin interfaces without
+ * an allocator, services whose memory budget is fixed once they start
+ * serving), which therefore cannot supply falcon_chunk_fwd's workspace.
+ *
+ * The scratch lives in a fixed 32 MiB array inside the library's device
+ * image, held by every device that loads the library until the process
+ * exits.  The call itself allocates nothing (no cudaMalloc/cudaFree).
+ * Covered: the shapes the tensor-core path takes (see falcon_chunk_fwd_plan;
+ * Falcon-1/1A, bf16, d_k = d_v in {64, 128}, chunk 64) needing at most
+ * 32 MiB of scratch, i.e. B * H * ceil(T / 64) <= 3855.  Larger problems
+ * return FALCON_ERR_WORKSPACE, other shapes FALCON_ERR_UNSUPPORTED (they
+ * need no workspace: call falcon_chunk_fwd with workspace = NULL).
+ * The first call on a device looks up the array's device address (which may
+ * also load the library's device code there); make that first call before
+ * any stream capture.  All calls share the one array: calls that overlap on
+ * the GPU (other streams, other host threads) race and must be serialised
+ * by the caller.  Arguments, outputs and other errors as falcon_chunk_fwd. */
+int falcon_chunk_fwd_noalloc(const falcon_params_t* p, const void* q, const void* k,
+                             const void* v, const float* beta, const float* lambda,
+                             const falcon_carry_t* carry_in, void* o, falcon_carry_t* carry_out,
+                             void* stream);
+
 /* Which kernel family falcon_chunk_fwd uses for these params
  * (FALCON_IMPL_GENERIC or FALCON_IMPL_TC, written to *impl_out) and how many
  * kernels one call enqueues (*launches_out).  Host-only; either output
