@@ -114,8 +114,8 @@ struct WySmem {
   static constexpr size_t Y = Tm + 2 * 64 * kLD * 4;              // [2 chunks][2][2][16*kYL]
   static constexpr size_t Ysc = Y + 2 * 4 * 16 * kYL * 4;         // [4 warps][16*kYL]
   static constexpr size_t G = Ysc + 4 * 16 * kYL * 4;             // g[128]
-  static constexpr size_t E = G + 128 * 4;                        // eta[128]
-  static constexpr size_t WS = E + 128 * 4;                       // warp sums [4]
+  static constexpr size_t E = G + 128 * 4;                        // eta[128], column factors[128]
+  static constexpr size_t WS = E + 256 * 4;                       // warp sums [4]
   static constexpr size_t BAR = WS + 8 * 4;                       // 2 mbarriers
   static constexpr size_t MISC = BAR + 16;                        // tmem addr, abort flag
   static constexpr size_t TOTAL = MISC + 16 + 1024;               // + alignment slack
@@ -232,13 +232,41 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
   for (int j = 0; j < 64; ++j) n = (j == rl) ? grow[j] : n;
   const float eta = exists ? beta / (a.eps + n) : 0.f;
   es[tid] = eta;
+  // column factor exp(g_end(J) - g_i) of this row as a column, J = its 16-block
+  float* cfs = es + 128;
+  cfs[tid] = __expf(gs[cidx * 64 + (rl | 15)] - g);
   tc_fence_before();
   __syncthreads();
-  {
+  {  // A_ri = eta_r exp(g_r - g_i) G_ri (i < r), the decay factored per 16-block
     float* Arow = Am + cidx * 64 * kLD + rl * kLD;
     const float* gc = gs + cidx * 64;
+    const float* cf = cfs + cidx * 64;
+    const int I = rl >> 4;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) Arow[i] = (i < rl) ? eta * __expf(g - gc[i]) * grow[i] : 0.f;
+    for (int J = 0; J < 4; ++J) {
+      float av[16];
+      if (J < I) {
+        const float rf = eta * __expf(g - gc[16 * J + 15]);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(cf + 16 * J + i);
+          av[i] = rf * c4.x * grow[16 * J + i];
+          av[i + 1] = rf * c4.y * grow[16 * J + i + 1];
+          av[i + 2] = rf * c4.z * grow[16 * J + i + 2];
+          av[i + 3] = rf * c4.w * grow[16 * J + i + 3];
+        }
+      } else if (J == I) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          av[i] = (16 * J + i < rl) ? eta * __expf(g - gc[16 * J + i]) * grow[16 * J + i] : 0.f;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) av[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(Arow + 16 * J + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
+    }
   }
   __syncthreads();
   if (warp == 0) {
@@ -306,13 +334,14 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
     uint8_t* To = a.ws_T + ((size_t)bh * a.NC + chunk) * 8192;
     for (int idx = rl; idx < 512; idx += 64) {
       const int R = idx >> 3, j = idx & 7;
+      const float4 lo4 = *reinterpret_cast<const float4*>(Tm + R * kLD + 8 * j);
+      const float4 hi4 = *reinterpret_cast<const float4*>(Tm + R * kLD + 8 * j + 4);
+      const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
       uint32_t pk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c0 = 8 * j + 2 * e;
-        const float v0 = (c0 <= R) ? Tm[R * kLD + c0] : 0.f;
-        const float v1 = (c0 + 1 <= R) ? Tm[R * kLD + c0 + 1] : 0.f;
-        pk[e] = pack_bf16(v0, v1);
+        pk[e] = pack_bf16((c0 <= R) ? v[2 * e] : 0.f, (c0 + 1 <= R) ? v[2 * e + 1] : 0.f);
       }
       *reinterpret_cast<uint4*>(To + R * 128 + 16 * (j ^ (R & 7))) =
           make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -744,6 +773,389 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
+// ----------------------------------------------------------------------
+// (b') pipelined sequential kernel, d_k = d_v = 64.  Three roles:
+//   warp 8      producer: TMA of chunk c into one of three stages
+//   warps 4..7  front: the state-independent part of chunk c (gates, row
+//               scaling, P = Q X^T, W = T X^, U = T V^, the decay-masked
+//               P~) into a double-buffered slot
+//   warps 0..3  back: the state chain of chunk c (W S0, Q S0, Delta,
+//               X^T Delta~, P~ Delta, state update, output tile)
+// so the front of chunk c+1 overlaps the back of chunk c.  Hand-offs are
+// mbarriers: full/empty per stage, fdone/bdone per slot.
+// ----------------------------------------------------------------------
+template <bool SOLVE>
+struct PipeSmem {
+  static constexpr int NST = 3;
+  static constexpr size_t XSZ = 8192, QSZ = 8192, VSZ = 8192, TSZ = SOLVE ? 8192 : 0, GSZ = 512;
+  static constexpr size_t STAGE = XSZ + QSZ + VSZ + TSZ + 1024;
+  static constexpr size_t XH = NST * STAGE;               // diag(eta Gamma) X (front scratch)
+  static constexpr size_t VH = XH + (SOLVE ? 8192 : 0);    // diag(eta) V (front scratch)
+  static constexpr size_t SLOT0 = VH + (SOLVE ? 8192 : 0);
+  // slot: P~ rows | W rows | U rows fp32 (stride 68) | Delta, Delta~ (additive) | gates
+  static constexpr size_t S_PM = 0, S_WB = 8192, S_U = S_WB + (SOLVE ? 8192 : 0);
+  static constexpr size_t S_DLA = S_U + (SOLVE ? 64 * 68 * 4 : 0);
+  static constexpr size_t S_DDA = S_DLA + (SOLVE ? 0 : 8192);
+  static constexpr size_t S_GATE = S_DDA + (SOLVE ? 0 : 8192);
+  static constexpr size_t SLOT = (S_GATE + 2048 + 1023) / 1024 * 1024;
+  static constexpr size_t SB = SLOT0 + 2 * SLOT;          // S rows (MN-major B)
+  static constexpr size_t DL = SB + 8192;                 // Delta rows
+  static constexpr size_t DD = DL + (SOLVE ? 8192 : 0);   // Delta~ rows
+  static constexpr size_t OST = DD + (SOLVE ? 8192 : 0);  // two output staging tiles
+  static constexpr size_t BAR = OST + 2 * 8192;
+  static constexpr size_t MISC = BAR + 128;
+  static constexpr size_t TOTAL = MISC + 16 + 1024;
+  static constexpr uint32_t COL_P = 0, COL_W = 64, COL_U = 128, COL_D1 = 192, COL_OA = 256,
+                            COL_D2 = 320, COL_OB = 384;
+  static_assert(TOTAL <= 232448, "shared memory budget");
+  // gate arrays inside a slot (fp32 x 64 each)
+  static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192, G_EX = 256, G_ET = 320;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+template <bool SOLVE>
+__global__ void __launch_bounds__(288, 1)
+    tc_fwd_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       TcArgs a) {
+  using L = PipeSmem<SOLVE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint64_t* full = bars;        // [3]
+  uint64_t* empty = bars + 3;   // [3]
+  uint64_t* fdone = bars + 6;   // [2]
+  uint64_t* bdone = bars + 8;   // [2]
+  uint64_t* fmma = bars + 10;
+  uint64_t* bmma = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / a.H, h = bh % a.H;
+  const int NC = a.NC;
+  auto stage = [&](int s) { return sm + s * L::STAGE; };
+  auto Xst = [&](int s) { return stage(s); };
+  auto Qst = [&](int s) { return stage(s) + L::XSZ; };
+  auto Vst = [&](int s) { return stage(s) + L::XSZ + L::QSZ; };
+  auto Tst = [&](int s) { return stage(s) + L::XSZ + L::QSZ + L::VSZ; };
+  auto Gst = [&](int s) {
+    return reinterpret_cast<const float*>(stage(s) + L::XSZ + L::QSZ + L::VSZ + L::TSZ);
+  };
+  auto slot = [&](int p) { return sm + L::SLOT0 + p * L::SLOT; };
+  auto gates = [&](int p) { return reinterpret_cast<float*>(slot(p) + L::S_GATE); };
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  };
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < 3; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&fdone[i], 128); mbar_init(&bdone[i], 128); }
+    mbar_init(fmma, 1);
+    mbar_init(bmma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int quad = warp & 3;
+  const bool row64 = lane < 16;
+  const int r64 = 16 * quad + lane;
+  const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int c = 0;
+      for (; c < NC; ++c) {
+        const int s = c % 3;
+        if (c >= 3 && !mbar_wait(&empty[s], (uint32_t)(((c - 3) / 3) & 1))) { fail(); break; }
+        if (*abort_flag) break;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(L::XSZ + L::QSZ + L::VSZ + L::TSZ + L::GSZ));
+        tma_load_4d(Xst(s), &tm_k, &full[s], 0, h, c * kC - 1, b);
+        tma_load_4d(Qst(s), &tm_q, &full[s], 0, h, c * kC, b);
+        tma_load_4d(Vst(s), &tm_v, &full[s], 0, h, c * kC, b);
+        const size_t ci = (size_t)bh * NC + c;
+        if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 8192, 8192, &full[s]);
+        bulk_load(const_cast<float*>(Gst(s)), a.ws_g + ci * 128, 512, &full[s]);
+      }
+      if (*abort_flag) {  // drain the loads still in flight
+        for (int cc = (c > 3 ? c - 3 : 0); cc < c; ++cc) mbar_wait(&full[cc % 3], (uint32_t)((cc / 3) & 1));
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ front
+    const int ftid = tid - 128;
+    uint8_t* XH = sm + L::XH;
+    uint8_t* VH = sm + L::VH;
+    const uint32_t sXH = smem_u32(XH), sVH = smem_u32(VH);
+    uint32_t fph = 0;
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % 3, p = c & 1;
+      bool ok = mbar_wait(&full[s], (uint32_t)((c / 3) & 1));
+      if (c >= 2) ok = ok && mbar_wait(&bdone[p], (uint32_t)(((c - 2) >> 1) & 1));
+      if (!ok) fail();
+      if (c == 0 && a.kprev_in && ftid < 64)  // x_0 = carried key
+        *reinterpret_cast<__nv_bfloat16*>(Xst(0) + sw128(0, ftid)) = a.kprev_in[(size_t)bh * 64 + ftid];
+      float* gt = gates(p);
+      if (ftid < 64) {
+        const float* G = Gst(s);
+        const float g = G[64 + ftid], glast = G[127], e = G[ftid];
+        const float gend = G[64 + (ftid | 15)];
+        const float gm = __expf(g);
+        gt[L::G_GAM + ftid] = gm;
+        gt[L::G_DEC + ftid] = __expf(glast - g);
+        gt[L::G_GL + ftid] = g;
+        gt[L::G_CF + ftid] = __expf(gend - g);
+        gt[L::G_EX + ftid] = e * gm;   // row scale of X: eta Gamma
+        gt[L::G_ET + ftid] = e;        // row scale of V: eta
+      }
+      named_bar(1, 128);
+      if (*abort_flag) break;
+      uint8_t* sl = slot(p);
+      if (SOLVE) {
+        scale_rows(XH, Xst(s), gt + L::G_EX, ftid, 128);
+        scale_rows(VH, Vst(s), gt + L::G_ET, ftid, 128);
+      } else {
+        scale_rows(sl + L::S_DLA, Vst(s), gt + L::G_ET, ftid, 128);  // Delta = diag(eta) V
+        for (int idx = ftid; idx < 512; idx += 128) {                  // Delta~ rows
+          const int R = idx >> 3;
+          const uint4 in = *reinterpret_cast<const uint4*>(Vst(s) + idx * 16);
+          const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
+          const float fr = gt[L::G_ET + R] * gt[L::G_DEC + R];
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(pin[e]);
+            pk[e] = pack_bf16(x.x * fr, x.y * fr);
+          }
+          *reinterpret_cast<uint4*>(sl + L::S_DDA + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      named_bar(1, 128);
+      tc_fence_after();
+      if (ftid == 0) {
+        const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s)), sT = smem_u32(Tst(s));
+        mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, 64, idesc_bf16(64, 64), false);
+        if (SOLVE) {
+          mma_chain_mn(tmem + L::COL_W, kdesc<64>, sT, mndesc, sXH, 64, idesc_bf16(64, 64, false, true),
+                       false);
+          mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT, mndesc, sVH, 64, idesc_bf16(64, 64, false, true),
+                       false);
+        }
+        umma_commit(fmma);
+      }
+      if (!mbar_wait(fmma, fph)) fail();
+      fph ^= 1;
+      tc_fence_after();
+      {  // P~ rows: decay exp(g_r - g_i) for i <= r, factored per 16-block
+        float pv[64];
+        tmem_ld64(tmem + lane_off + L::COL_P, pv);
+        tmem_wait_ld();
+        if (row64) {
+          const float* gl = gt + L::G_GL;
+          const float* cf = gt + L::G_CF;
+          const float gr = gl[r64];
+#pragma unroll
+          for (int J = 0; J < 4; ++J) {
+            if (J < quad) {
+              const float rf = __expf(gr - gl[16 * J + 15]);
+#pragma unroll
+              for (int i = 16 * J; i < 16 * J + 16; i += 4) {
+                const float4 c4 = *reinterpret_cast<const float4*>(cf + i);
+                pv[i] *= rf * c4.x;
+                pv[i + 1] *= rf * c4.y;
+                pv[i + 2] *= rf * c4.z;
+                pv[i + 3] *= rf * c4.w;
+              }
+            } else if (J == quad) {
+#pragma unroll
+              for (int i = 16 * J; i < 16 * J + 16; ++i)
+                pv[i] = (i <= r64) ? __expf(gr - gl[i]) * pv[i] : 0.f;
+            } else {
+#pragma unroll
+              for (int i = 16 * J; i < 16 * J + 16; ++i) pv[i] = 0.f;
+            }
+          }
+          store_row64(sl + L::S_PM, r64, pv);
+        }
+      }
+      if (SOLVE) {  // W rows (bf16 K-major operand) and U rows (fp32)
+        float wv[64];
+        tmem_ld64(tmem + lane_off + L::COL_W, wv);
+        tmem_wait_ld();
+        if (row64) store_row64(sl + L::S_WB, r64, wv);
+        tmem_ld64(tmem + lane_off + L::COL_U, wv);
+        tmem_wait_ld();
+        if (row64) {
+          float* urow = reinterpret_cast<float*>(sl + L::S_U) + r64 * 68;
+#pragma unroll
+          for (int n = 0; n < 64; n += 4)
+            *reinterpret_cast<float4*>(urow + n) = make_float4(wv[n], wv[n + 1], wv[n + 2], wv[n + 3]);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(&fdone[p]);
+    }
+    if (a.kprev_out && !*abort_flag && ftid < 64)
+      a.kprev_out[(size_t)bh * 64 + ftid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + ftid];
+    if (a.pos_out && !*abort_flag && ftid == 0) a.pos_out[bh] = (a.pos_in ? a.pos_in[bh] : 0) + a.T;
+  } else {
+    // ------------------------------------------------------------ back
+    uint8_t* SB = sm + L::SB;
+    const uint32_t sS = smem_u32(SB);
+    float sreg[64];
+#pragma unroll
+    for (int n = 0; n < 64; ++n) sreg[n] = 0.f;
+    if (row64 && a.S_in) {
+      const float* src = a.S_in + ((size_t)bh * 64 + r64) * 64;
+#pragma unroll
+      for (int n = 0; n < 64; n += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + n);
+        sreg[n] = v.x; sreg[n + 1] = v.y; sreg[n + 2] = v.z; sreg[n + 3] = v.w;
+      }
+    }
+    if (row64) store_row64(SB, r64, sreg);
+    fence_proxy_async();
+    named_bar(2, 128);
+    uint32_t bph = 0;
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % 3, p = c & 1;
+      if (!mbar_wait(&fdone[p], (uint32_t)((c >> 1) & 1))) fail();
+      tc_fence_after();
+      named_bar(2, 128);
+      if (*abort_flag) break;
+      uint8_t* sl = slot(p);
+      const float* gt = gates(p);
+      const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s));
+      const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(sl + L::S_DLA);
+      const uint32_t sDD = SOLVE ? smem_u32(sm + L::DD) : smem_u32(sl + L::S_DDA);
+      if (tid == 0) {
+        if (SOLVE)
+          mma_chain_mn(tmem + L::COL_D1, kdesc<64>, smem_u32(sl + L::S_WB), mndesc, sS, 64,
+                       idesc_bf16(64, 64, false, true), false);
+        mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, 64, idesc_bf16(64, 64, false, true),
+                     false);
+        umma_commit(bmma);
+      }
+      if (!mbar_wait(bmma, bph)) fail();
+      bph ^= 1;
+      tc_fence_after();
+      if (SOLVE) {  // Delta = U - W S0, and diag(exp(g_last - g)) Delta
+        float dv1[64];
+        tmem_ld64(tmem + lane_off + L::COL_D1, dv1);
+        tmem_wait_ld();
+        if (row64) {
+          const float* urow = reinterpret_cast<const float*>(sl + L::S_U) + r64 * 68;
+#pragma unroll
+          for (int n = 0; n < 64; n += 4) {
+            const float4 u = *reinterpret_cast<const float4*>(urow + n);
+            dv1[n] = u.x - dv1[n];
+            dv1[n + 1] = u.y - dv1[n + 1];
+            dv1[n + 2] = u.z - dv1[n + 2];
+            dv1[n + 3] = u.w - dv1[n + 3];
+          }
+          store_row64(sm + L::DL, r64, dv1);
+          const float dr = gt[L::G_DEC + r64];
+#pragma unroll
+          for (int n = 0; n < 64; ++n) dv1[n] *= dr;
+          store_row64(sm + L::DD, r64, dv1);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_bar(2, 128);
+        tc_fence_after();
+      }
+      if (tid == 0) {
+        mma_chain_mn(tmem + L::COL_D2, mndesc, sX, mndesc, sDD, 64, idesc_bf16(64, 64, true, true), false);
+        mma_chain_mn(tmem + L::COL_OB, kdesc<64>, smem_u32(sl + L::S_PM), mndesc, sDL, 64,
+                     idesc_bf16(64, 64, false, true), false);
+        umma_commit(bmma);
+      }
+      if (!mbar_wait(bmma, bph)) fail();
+      bph ^= 1;
+      tc_fence_after();
+      if (tid == 0) mbar_arrive(&empty[s]);  // the stage's tiles are no longer read
+      uint8_t* Ost = sm + L::OST + (c & 1) * 8192;
+      {  // S1 = Gamma_last S0 + D2
+        float d2[64];
+        tmem_ld64(tmem + lane_off + L::COL_D2, d2);
+        tmem_wait_ld();
+        if (row64) {
+          const float gl_ = gt[L::G_GAM + 63];
+#pragma unroll
+          for (int n = 0; n < 64; ++n) sreg[n] = gl_ * sreg[n] + d2[n];
+          store_row64(SB, r64, sreg);
+        }
+      }
+      {  // O = diag(Gamma) Oa + Ob
+        const float gr = gt[L::G_GAM + r64];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t oa[32], ob[32];
+          tmem_ld32(tmem + lane_off + L::COL_OA + 32 * hf, oa);
+          tmem_ld32(tmem + lane_off + L::COL_OB + 32 * hf, ob);
+          tmem_wait_ld();
+          if (row64) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int n = 8 * j + 2 * e;
+                pk[e] = pack_bf16(gr * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
+                                  gr * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
+              }
+              *reinterpret_cast<uint4*>(Ost + sw128(r64, 32 * hf + 8 * j)) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      named_bar(2, 128);
+      tc_fence_after();
+      mbar_arrive(&bdone[p]);
+      if (tid == 0) {
+        tma_store_4d(&tm_o, Ost, 0, h, c * kC, b);
+        bulk_commit();
+        bulk_wait_read1();  // the tile stored one chunk ago has left its buffer
+      }
+    }
+    if (tid == 0) bulk_wait0();
+    if (!*abort_flag && row64 && a.S_out) {
+      float* dst = a.S_out + ((size_t)bh * 64 + r64) * 64;
+#pragma unroll
+      for (int n = 0; n < 64; n += 4)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(sreg[n], sreg[n + 1], sreg[n + 2], sreg[n + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
@@ -809,7 +1221,14 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
     k<<<grid, 128, smem, fa.stream>>>(mk128, ta);
     record_event(fa, 1);
   }
-  {
+  if (DK == 64) {  // pipelined: producer warp, front and back warpgroups
+    auto k = tc_fwd_pipe_kernel<SOLVE>;
+    const size_t smem = PipeSmem<SOLVE>::TOTAL;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return FALCON_ERR_CUDA;
+    k<<<BH, 288, smem, fa.stream>>>(mq, mk, mv, mo, ta);
+    record_event(fa, 2);
+  } else {
     auto k = tc_fwd_kernel<DK, NV, SOLVE>;
     const size_t smem = FwdSmem<DK, NV, SOLVE>::TOTAL;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
