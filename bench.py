@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--workload", default="lm124m_f1_8x2048x12_d64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--mode", choices=["chunk", "decode"], default="chunk",
+                    help="decode: the recurrent one-token step (256 sequences x 12 heads)")
+    ap.add_argument("--decode-variant", type=int, default=0)
     ap.add_argument("--sets", type=int, default=N_SETS,
                     help="rotating input sets (fewer only for profiler captures)")
     return ap.parse_args()
@@ -201,8 +204,65 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_decode(args):
+    """Recurrent decode step: one token for 256 sequences x 12 heads, d = 64,
+    fp32 state in HBM.  4 state sets (4 x 50 MB) rotate so every step reads
+    a state that is not in L2."""
+    import torch
+
+    import chunked_delta_rule_gb300 as F
+    from workloads import make_decode_inputs
+    torch.cuda.set_device(0)
+    sets = []
+    for i in range(args.sets):
+        x, carry, w = make_decode_inputs(args.decode_variant, window=8, seed=5 + 10 * i,
+                                         device="cuda")
+        sets.append((x, carry))
+    p = F.Params(B=w.B, T=1, H=w.H, dk=w.dk, dv=w.dv, window=w.window, variant=w.variant,
+                 dtype=F.FALCON_BF16)
+    o = torch.empty((w.B, 1, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        x, c = sets[i % len(sets)]
+        F.falcon_recurrent_step(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], c, o, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    bh = w.B * w.H
+    Wp = w.window if w.variant in (4, 5) else 1
+    nbytes = bh * (2 * w.dk * w.dv * 4 + (w.dk + 2 * w.dk + 2 * w.dv) * 2 + 8 + 8
+                   + (Wp - 1) * (w.dk + w.dv) * 2 + (w.dk + w.dv) * 2 * (Wp > 1))
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"metric": "Falcon recurrent decode step tokens/s", "value": w.B / (ms / 1e3),
+                      "unit": "tokens/s", "ms_per_step": ms, "steps": args.steps,
+                      "config": {"workload": f"decode_{w.B}x{w.H}_d{w.dk}", "variant": w.variant,
+                                 "window": Wp, "state_sets": len(sets)},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                   "frac": gbs / peak, "algorithmic_bytes": nbytes,
+                                   "kernel": "recurrent_step_kernel"}}), flush=True)
+
+
 def main():
     args = parse()
+    if args.mode == "decode":
+        run_decode(args)
+        return
     w = get_workload(args.workload)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

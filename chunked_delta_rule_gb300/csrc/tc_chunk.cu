@@ -58,7 +58,7 @@ struct TcArgs {
   float* S_out;
   __nv_bfloat16* kprev_out;
   int64_t* pos_out;
-  uint8_t* ws_T;      // [B*H*NC][8192] bf16 swizzled images of T
+  uint8_t* ws_T;      // [B*H*NC][16384]: bf16 swizzled images of T diag(eta Gamma), T diag(eta)
   float* ws_g;        // [B*H*NC][128]: eta[64], g[64]
   uint32_t* status;   // workspace status word
 };
@@ -114,8 +114,8 @@ struct WySmem {
   static constexpr size_t Y = Tm + 2 * 64 * kLD * 4;              // [2 chunks][2][2][16*kYL]
   static constexpr size_t Ysc = Y + 2 * 4 * 16 * kYL * 4;         // [4 warps][16*kYL]
   static constexpr size_t G = Ysc + 4 * 16 * kYL * 4;             // g[128]
-  static constexpr size_t E = G + 128 * 4;                        // eta[128], column factors[128]
-  static constexpr size_t WS = E + 256 * 4;                       // warp sums [4]
+  static constexpr size_t E = G + 128 * 4;                        // eta, column factors, Gamma [128] each
+  static constexpr size_t WS = E + 384 * 4;                       // warp sums [4]
   static constexpr size_t BAR = WS + 8 * 4;                       // 2 mbarriers
   static constexpr size_t MISC = BAR + 16;                        // tmem addr, abort flag
   static constexpr size_t TOTAL = MISC + 16 + 1024;               // + alignment slack
@@ -235,6 +235,8 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
   // column factor exp(g_end(J) - g_i) of this row as a column, J = its 16-block
   float* cfs = es + 128;
   cfs[tid] = __expf(gs[cidx * 64 + (rl | 15)] - g);
+  float* gms = es + 256;
+  gms[tid] = __expf(g);
   tc_fence_before();
   __syncthreads();
   {  // A_ri = eta_r exp(g_r - g_i) G_ri (i < r), the decay factored per 16-block
@@ -330,21 +332,27 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
   }
   named_bar(nb_id, 64);
   if (chunk < a.NC && !aborted) {
-    // bf16 image of T as a 128B-swizzled K-major tile, upper triangle zero
-    uint8_t* To = a.ws_T + ((size_t)bh * a.NC + chunk) * 8192;
+    // bf16 images of T diag(eta Gamma) (for W) and T diag(eta) (for U) as
+    // 128B-swizzled K-major tiles; the upper triangle is zero
+    uint8_t* To = a.ws_T + ((size_t)bh * a.NC + chunk) * 16384;
+    const float* ec = es + cidx * 64;
+    const float* gc = gms + cidx * 64;
     for (int idx = rl; idx < 512; idx += 64) {
       const int R = idx >> 3, j = idx & 7;
       const float4 lo4 = *reinterpret_cast<const float4*>(Tm + R * kLD + 8 * j);
       const float4 hi4 = *reinterpret_cast<const float4*>(Tm + R * kLD + 8 * j + 4);
       const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-      uint32_t pk[4];
+      uint32_t pw[4], pu[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c0 = 8 * j + 2 * e;
-        pk[e] = pack_bf16((c0 <= R) ? v[2 * e] : 0.f, (c0 + 1 <= R) ? v[2 * e + 1] : 0.f);
+        const float t0 = (c0 <= R) ? v[2 * e] : 0.f, t1 = (c0 + 1 <= R) ? v[2 * e + 1] : 0.f;
+        pw[e] = pack_bf16(t0 * ec[c0] * gc[c0], t1 * ec[c0 + 1] * gc[c0 + 1]);
+        pu[e] = pack_bf16(t0 * ec[c0], t1 * ec[c0 + 1]);
       }
-      *reinterpret_cast<uint4*>(To + R * 128 + 16 * (j ^ (R & 7))) =
-          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      const int off = R * 128 + 16 * (j ^ (R & 7));
+      *reinterpret_cast<uint4*>(To + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      *reinterpret_cast<uint4*>(To + 8192 + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
     }
     float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * 128;
     go[rl] = eta;
@@ -359,12 +367,11 @@ template <int DK, int NV, bool SOLVE>
 struct FwdSmem {
   static constexpr int kKS = DK / 64;                 // 64-column slabs of the d_k contractions
   static constexpr size_t XSZ = DK * 128, QSZ = DK * 128, VSZ = NV * 128;
-  static constexpr size_t TSZ = SOLVE ? 8192 : 0, GSZ = 512;
+  static constexpr size_t TSZ = SOLVE ? 16384 : 0, GSZ = 512;   // T diag(eta Gamma) | T diag(eta)
   static constexpr size_t STAGE = XSZ + QSZ + VSZ + TSZ + 1024;  // gates padded to 1 KB
   static constexpr size_t ST0 = 0;
-  static constexpr size_t XH = 2 * STAGE;              // diag(eta Gamma) X, rows (MN-major B)
-  static constexpr size_t VH = XH + (SOLVE ? XSZ : 0); // diag(eta) V, rows (MN-major B)
-  static constexpr size_t PM = VH + VSZ;               // decay-masked Q X^T, K-major rows
+  static constexpr size_t VH = 2 * STAGE;              // additive: diag(eta) V rows (MN-major B)
+  static constexpr size_t PM = VH + (SOLVE ? 0 : VSZ); // decay-masked Q X^T, K-major rows
   static constexpr size_t WB = PM + 8192;              // W rows, K-major [64][DK]
   static constexpr size_t SB = WB + (SOLVE ? DK * 128 : 0);   // S rows, MN-major [DK][NV]
   static constexpr size_t DL = SB + DK * 128;          // Delta rows (MN-major B)
@@ -437,7 +444,6 @@ __global__ void __launch_bounds__(256, 1)
   using L = FwdSmem<DK, NV, SOLVE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* XH = sm + L::XH;
   uint8_t* VH = sm + L::VH;
   uint8_t* Pm = sm + L::PM;
   uint8_t* Wb = sm + L::WB;
@@ -477,7 +483,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     tma_load_4d(Vst(s), &tm_v, &full[s], c0, h, c * kC, b);
     const size_t ci = (size_t)bh * NC + c;
-    if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 8192, 8192, &full[s]);
+    if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 16384, 16384, &full[s]);
     bulk_load(Gst(s), a.ws_g + ci * 128, 512, &full[s]);
   };
 
@@ -530,7 +536,7 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
 
   const uint32_t sP = smem_u32(Pm), sW = smem_u32(Wb), sS = smem_u32(SB), sDL = smem_u32(DL),
-                 sDD = smem_u32(DD), sXH = smem_u32(XH), sVH = smem_u32(VH);
+                 sDD = smem_u32(DD);
   float ureg[NV];
   uint32_t mph = 0;
   for (int c = 0; c < NC; ++c) {
@@ -562,23 +568,8 @@ __global__ void __launch_bounds__(256, 1)
     if (*abort_flag) break;
     const float gam_last = Gam[63];
 
-    // ---- row-scaled operands (16-byte chunks)
+    // ---- row-scaled operands of the additive write (16-byte chunks)
     if (SOLVE) {
-      for (int k = 0; k < L::kKS; ++k) scale_rows(XH + k * 8192, Xst(s) + k * 8192, et, tid, 256);
-      // diag(eta) V: eta = et / Gamma
-      for (int idx = tid; idx < 512; idx += 256) {
-        const int R = idx >> 3;
-        const uint4 in = *reinterpret_cast<const uint4*>(Vst(s) + idx * 16);
-        const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-        const float fr = Gst(s)[R];
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 x = __bfloat1622float2(pin[e]);
-          pk[e] = pack_bf16(x.x * fr, x.y * fr);
-        }
-        *reinterpret_cast<uint4*>(VH + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
     } else {
       scale_rows(VH, Vst(s), et, tid, 256);  // Delta = diag(eta) V
       for (int idx = tid; idx < 512; idx += 256) {  // diag(exp(g_last - g) eta) V
@@ -605,11 +596,11 @@ __global__ void __launch_bounds__(256, 1)
       const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s)), sT = smem_u32(Tst(s));
       mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, DK, idesc_bf16(64, 64), false);
       if (SOLVE) {
-        for (int k = 0; k < L::kKS; ++k)
-          mma_chain_mn(tmem + L::COL_W + 64 * k, kdesc<64>, sT, mndesc, sXH + k * 8192, 64,
+        for (int k = 0; k < L::kKS; ++k)  // W = T diag(eta Gamma) X, U = T diag(eta) V
+          mma_chain_mn(tmem + L::COL_W + 64 * k, kdesc<64>, sT, mndesc, sX + k * 8192, 64,
                        idesc_bf16(64, 64, false, true), false);
-        mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT, mndesc, sVH, 64, idesc_bf16(64, NV, false, true),
-                     false);
+        mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT + 8192, mndesc, smem_u32(Vst(s)), 64,
+                     idesc_bf16(64, NV, false, true), false);
       }
       mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
                    false);
@@ -786,12 +777,10 @@ __global__ void __launch_bounds__(256, 1)
 // ----------------------------------------------------------------------
 template <bool SOLVE>
 struct PipeSmem {
-  static constexpr int NST = 3;
-  static constexpr size_t XSZ = 8192, QSZ = 8192, VSZ = 8192, TSZ = SOLVE ? 8192 : 0, GSZ = 512;
+  static constexpr int NST = SOLVE ? 2 : 3;               // TMA stages
+  static constexpr size_t XSZ = 8192, QSZ = 8192, VSZ = 8192, TSZ = SOLVE ? 16384 : 0, GSZ = 512;
   static constexpr size_t STAGE = XSZ + QSZ + VSZ + TSZ + 1024;
-  static constexpr size_t XH = NST * STAGE;               // diag(eta Gamma) X (front scratch)
-  static constexpr size_t VH = XH + (SOLVE ? 8192 : 0);    // diag(eta) V (front scratch)
-  static constexpr size_t SLOT0 = VH + (SOLVE ? 8192 : 0);
+  static constexpr size_t SLOT0 = NST * STAGE;
   // slot: P~ rows | W rows | U rows fp32 (stride 68) | Delta, Delta~ (additive) | gates
   static constexpr size_t S_PM = 0, S_WB = 8192, S_U = S_WB + (SOLVE ? 8192 : 0);
   static constexpr size_t S_DLA = S_U + (SOLVE ? 64 * 68 * 4 : 0);
@@ -828,8 +817,9 @@ __global__ void __launch_bounds__(288, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  uint64_t* full = bars;        // [3]
-  uint64_t* empty = bars + 3;   // [3]
+  constexpr int NST = L::NST;
+  uint64_t* full = bars;        // [NST]
+  uint64_t* empty = bars + 3;   // [NST]
   uint64_t* fdone = bars + 6;   // [2]
   uint64_t* bdone = bars + 8;   // [2]
   uint64_t* fmma = bars + 10;
@@ -858,7 +848,7 @@ __global__ void __launch_bounds__(288, 1)
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < 3; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&fdone[i], 128); mbar_init(&bdone[i], 128); }
     mbar_init(fmma, 1);
     mbar_init(bmma, 1);
@@ -882,31 +872,29 @@ __global__ void __launch_bounds__(288, 1)
     if (lane == 0) {
       int c = 0;
       for (; c < NC; ++c) {
-        const int s = c % 3;
-        if (c >= 3 && !mbar_wait(&empty[s], (uint32_t)(((c - 3) / 3) & 1))) { fail(); break; }
+        const int s = c % NST;
+        if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1))) { fail(); break; }
         if (*abort_flag) break;
         mbar_arrive_expect_tx(&full[s], (uint32_t)(L::XSZ + L::QSZ + L::VSZ + L::TSZ + L::GSZ));
         tma_load_4d(Xst(s), &tm_k, &full[s], 0, h, c * kC - 1, b);
         tma_load_4d(Qst(s), &tm_q, &full[s], 0, h, c * kC, b);
         tma_load_4d(Vst(s), &tm_v, &full[s], 0, h, c * kC, b);
         const size_t ci = (size_t)bh * NC + c;
-        if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 8192, 8192, &full[s]);
+        if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 16384, 16384, &full[s]);
         bulk_load(const_cast<float*>(Gst(s)), a.ws_g + ci * 128, 512, &full[s]);
       }
       if (*abort_flag) {  // drain the loads still in flight
-        for (int cc = (c > 3 ? c - 3 : 0); cc < c; ++cc) mbar_wait(&full[cc % 3], (uint32_t)((cc / 3) & 1));
+        for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
+          mbar_wait(&full[cc % NST], (uint32_t)((cc / NST) & 1));
       }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ front
     const int ftid = tid - 128;
-    uint8_t* XH = sm + L::XH;
-    uint8_t* VH = sm + L::VH;
-    const uint32_t sXH = smem_u32(XH), sVH = smem_u32(VH);
     uint32_t fph = 0;
     for (int c = 0; c < NC; ++c) {
-      const int s = c % 3, p = c & 1;
-      bool ok = mbar_wait(&full[s], (uint32_t)((c / 3) & 1));
+      const int s = c % NST, p = c & 1;
+      bool ok = mbar_wait(&full[s], (uint32_t)((c / NST) & 1));
       if (c >= 2) ok = ok && mbar_wait(&bdone[p], (uint32_t)(((c - 2) >> 1) & 1));
       if (!ok) fail();
       if (c == 0 && a.kprev_in && ftid < 64)  // x_0 = carried key
@@ -927,10 +915,7 @@ __global__ void __launch_bounds__(288, 1)
       named_bar(1, 128);
       if (*abort_flag) break;
       uint8_t* sl = slot(p);
-      if (SOLVE) {
-        scale_rows(XH, Xst(s), gt + L::G_EX, ftid, 128);
-        scale_rows(VH, Vst(s), gt + L::G_ET, ftid, 128);
-      } else {
+      if (!SOLVE) {
         scale_rows(sl + L::S_DLA, Vst(s), gt + L::G_ET, ftid, 128);  // Delta = diag(eta) V
         for (int idx = ftid; idx < 512; idx += 128) {                  // Delta~ rows
           const int R = idx >> 3;
@@ -954,10 +939,11 @@ __global__ void __launch_bounds__(288, 1)
         const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s)), sT = smem_u32(Tst(s));
         mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, 64, idesc_bf16(64, 64), false);
         if (SOLVE) {
-          mma_chain_mn(tmem + L::COL_W, kdesc<64>, sT, mndesc, sXH, 64, idesc_bf16(64, 64, false, true),
+          // W = T diag(eta Gamma) X, U = T diag(eta) V, straight from the TMA tiles
+          mma_chain_mn(tmem + L::COL_W, kdesc<64>, sT, mndesc, sX, 64, idesc_bf16(64, 64, false, true),
                        false);
-          mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT, mndesc, sVH, 64, idesc_bf16(64, 64, false, true),
-                       false);
+          mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT + 8192, mndesc, smem_u32(Vst(s)), 64,
+                       idesc_bf16(64, 64, false, true), false);
         }
         umma_commit(fmma);
       }
@@ -1037,7 +1023,7 @@ __global__ void __launch_bounds__(288, 1)
     named_bar(2, 128);
     uint32_t bph = 0;
     for (int c = 0; c < NC; ++c) {
-      const int s = c % 3, p = c & 1;
+      const int s = c % NST, p = c & 1;
       if (!mbar_wait(&fdone[p], (uint32_t)((c >> 1) & 1))) fail();
       tc_fence_after();
       named_bar(2, 128);
@@ -1197,7 +1183,7 @@ WsLayout ws_layout(int B, int T, int H, int chunk) {
   WsLayout w;
   w.status = 0;
   w.T = 256;
-  w.g = w.T + (size_t)B * H * NC * 8192;
+  w.g = w.T + (size_t)B * H * NC * 16384;
   w.total = align_up(w.g + (size_t)B * H * NC * 512, 256);
   return w;
 }

@@ -1,7 +1,7 @@
 """Tensor-core chunk path (tcgen05 / TMEM / TMA): parity with the oracle when
 forced, agreement with the portable path, and a white-box check of the
-per-chunk WY stage (the bf16 T = (I + A)^{-1} images and the gates it leaves
-in the workspace)."""
+per-chunk WY stage (the bf16 images of T diag(eta Gamma) and T diag(eta),
+T = (I + A)^{-1}, and the gates it leaves in the workspace)."""
 
 from __future__ import annotations
 
@@ -52,7 +52,7 @@ def test_wy_stage_workspace(F, d):
     wsn = ws.cpu().numpy()
     assert int(wsn[:4].view(np.uint32)[0]) == 0, "status word set"
     t_off = 256
-    g_off = t_off + w.B * w.H * NC * 8192
+    g_off = t_off + w.B * w.H * NC * 16384
     k = x["k"].float().cpu().numpy().astype(np.float64)
     lam = x["lam"].cpu().numpy().astype(np.float64)
     beta = x["beta"].cpu().numpy().astype(np.float64)
@@ -72,8 +72,13 @@ def test_wy_stage_workspace(F, d):
             A = eta[:, None] * np.exp(np.minimum(g[:, None] - g[None, :], 0)) * G * np.tril(np.ones((64, 64)), -1)
             Tref = np.linalg.inv(np.eye(64) + A)
             ci = bh * NC + c
-            Tg = decode_T(wsn[t_off + ci * 8192: t_off + (ci + 1) * 8192])
-            assert np.abs(Tg - Tref).max() <= 2e-2 * np.abs(Tref).max(), (bh, c)
+            img = wsn[t_off + ci * 16384: t_off + (ci + 1) * 16384]
+            Tw_ref = Tref * (eta * np.exp(g))[None, :]
+            Tu_ref = Tref * eta[None, :]
+            Tw = decode_T(img[:8192])
+            Tu = decode_T(img[8192:])
+            assert np.abs(Tw - Tw_ref).max() <= 2e-2 * np.abs(Tw_ref).max(), (bh, c)
+            assert np.abs(Tu - Tu_ref).max() <= 2e-2 * np.abs(Tu_ref).max(), (bh, c)
             gates = wsn[g_off + ci * 512: g_off + (ci + 1) * 512].view(np.float32)
             assert np.allclose(gates[:64], eta, rtol=2e-3, atol=1e-6), (bh, c)
             assert np.allclose(gates[64:], g, rtol=1e-4, atol=1e-5), (bh, c)
