@@ -5,6 +5,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "falcon.h"
 
 namespace falcon {
@@ -80,5 +84,23 @@ int tc_chunk_launches(const FwdArgs& a);
 size_t tc_chunk_ws_bytes(int B, int T, int H, int dk, int dv, int chunk, int variant);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Raise a kernel's dynamic shared-memory limit, once per kernel and device
+// (the attribute call costs host time on every launch otherwise).
+inline bool set_smem_limit(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_pair(kernel, dev);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return false;
+  done[key] = bytes;
+  return true;
+}
 
 }  // namespace falcon

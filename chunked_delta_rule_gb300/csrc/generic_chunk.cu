@@ -339,12 +339,12 @@ int launch_generic_chunk(const FwdArgs& a) {
   record_event(a, 0);
   if (a.dtype == FALCON_BF16) {
     auto k = generic_chunk_kernel<__nv_bfloat16>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
       return FALCON_ERR_CUDA;
     k<<<grid, kThreads, smem, a.stream>>>(a, c, dvs);
   } else {
     auto k = generic_chunk_kernel<float>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
       return FALCON_ERR_CUDA;
     k<<<grid, kThreads, smem, a.stream>>>(a, c, dvs);
   }

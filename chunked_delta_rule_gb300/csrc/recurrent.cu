@@ -175,6 +175,162 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
   if (tid == 0) a.pos_out[bhi] = pos + 1;
 }
 
+// Bandwidth-shaped variant for d_k = d_v in {64, 128}: float4 state
+// accesses (every warp moves whole 256/512-byte rows), partial predictions
+// reduced with shuffles and one shared-memory pass, two CTA barriers.
+// Thread t owns 4 value columns (quad t % NQ) of the rows rg + RGS * i.
+template <typename Tin, int D, int NT, int MAXW>
+__global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
+  constexpr int NQ = D / 4;          // column quads
+  constexpr int RGS = NT / NQ;       // row groups
+  constexpr int RPT = D / RGS;       // rows per thread
+  constexpr int GPW = 32 / NQ;       // row groups inside one warp
+  constexpr int NW = NT / 32;
+  __shared__ float xw[MAXW][D];      // window keys (oldest first; last = current pair)
+  __shared__ float vw[MAXW][D];
+  __shared__ float qv[D];
+  __shared__ float pv[MAXW], xq[MAXW], xn[MAXW];
+  __shared__ float4 red[NW][MAXW + 1][NQ];
+  const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cq = tid % NQ, rg = tid / NQ;
+  const int W = a.W, Wr = W - 1;
+  const size_t bhi = (size_t)bh;
+  float4* Sg = reinterpret_cast<float4*>(a.S_out + bhi * D * D);
+  float4 s[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) s[i] = Sg[(size_t)(rg + RGS * i) * NQ + cq];
+
+  const int64_t pos = a.pos_out[bhi];
+  for (int i = tid; i < W * D; i += NT) {
+    const int w = i / D, d = i % D;
+    const int64_t p = pos - Wr + w;
+    float x = 0.f, v = 0.f;
+    if (p >= 1) {
+      if (w == Wr) {
+        x = to_f32(reinterpret_cast<const Tin*>(a.kprev_out)[bhi * D + d]);
+        v = to_f32(reinterpret_cast<const Tin*>(a.v)[bhi * D + d]);
+      } else {
+        const size_t o = (bhi * Wr + ring_slot(p, Wr)) * D + d;
+        x = to_f32(reinterpret_cast<const Tin*>(a.winx_out)[o]);
+        v = to_f32(reinterpret_cast<const Tin*>(a.winv_out)[o]);
+      }
+    }
+    xw[w][d] = x;
+    vw[w][d] = v;
+  }
+  for (int d = tid; d < D; d += NT) qv[d] = to_f32(reinterpret_cast<const Tin*>(a.q)[bhi * D + d]);
+  __syncthreads();
+  for (int w = warp; w < W; w += NW) {  // x_j . q and ||x_j||^2
+    float aq = 0.f, an = 0.f;
+    for (int d = lane; d < D; d += 32) {
+      const float x = xw[w][d];
+      aq += x * qv[d];
+      an += x * x;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      aq += __shfl_xor_sync(0xffffffffu, aq, o);
+      an += __shfl_xor_sync(0xffffffffu, an, o);
+    }
+    if (lane == 0) {
+      xq[w] = aq;
+      xn[w] = an;
+      pv[w] = (pos - Wr + w >= 1) ? 1.f : 0.f;
+    }
+  }
+  // partial predictions S^T x_j (j < W) and S^T q over this thread's rows
+  const bool additive = variant_additive(a.variant);
+  for (int w = 0; w <= W; ++w) {
+    if (additive && w < W) continue;
+    const float* xv = (w < W) ? xw[w] : qv;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float x = xv[rg + RGS * i];
+      acc.x += s[i].x * x; acc.y += s[i].y * x; acc.z += s[i].z * x; acc.w += s[i].w * x;
+    }
+#pragma unroll
+    for (int o = NQ; o < 32; o <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+    }
+    if (lane < NQ) red[warp][w][cq] = acc;
+  }
+  __syncthreads();
+  // every thread forms the writes of its own 4 columns
+  const float gamma = fminf(fmaxf(1.0f - a.lam[bhi], a.eps_gamma), 1.0f);
+  const bool perch = variant_per_channel(a.variant);
+  float n = 0.f, e = 0.f;
+  for (int w = 0; w < W; ++w) { n += pv[w]; e += pv[w] * xn[w]; }
+  float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n > 0.f) {
+    const float den = a.eps + e / n;
+    if (perch) {
+      const float4 bt = reinterpret_cast<const float4*>(a.beta + bhi * D)[cq];
+      cf = make_float4(bt.x / den / n, bt.y / den / n, bt.z / den / n, bt.w / den / n);
+    } else {
+      const float c = a.beta[bhi] / den / n;
+      cf = make_float4(c, c, c, c);
+    }
+  }
+  auto total = [&](int w) {
+    float4 t = red[0][w][cq];
+#pragma unroll
+    for (int g = 1; g < NW; ++g) {
+      const float4 u = red[g][w][cq];
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+    }
+    return t;
+  };
+  float4 dl[MAXW];
+  const float4 cqs = total(W);
+  float4 o = make_float4(gamma * cqs.x, gamma * cqs.y, gamma * cqs.z, gamma * cqs.w);
+#pragma unroll
+  for (int w = 0; w < MAXW; ++w) {
+    if (w >= W) break;
+    const float4 v4 = *reinterpret_cast<const float4*>(&vw[w][4 * cq]);
+    float4 r = v4;
+    if (!additive) {
+      const float4 pr = total(w);
+      r = make_float4(v4.x - gamma * pr.x, v4.y - gamma * pr.y, v4.z - gamma * pr.z, v4.w - gamma * pr.w);
+    }
+    const float m = pv[w];
+    dl[w] = make_float4(m * cf.x * r.x, m * cf.y * r.y, m * cf.z * r.z, m * cf.w * r.w);
+    const float xqw = xq[w];
+    o.x += xqw * dl[w].x; o.y += xqw * dl[w].y; o.z += xqw * dl[w].z; o.w += xqw * dl[w].w;
+  }
+  if (rg == 0) {
+    Tin* op = reinterpret_cast<Tin*>(a.o) + bhi * D + 4 * cq;
+    op[0] = from_f32<Tin>(o.x); op[1] = from_f32<Tin>(o.y);
+    op[2] = from_f32<Tin>(o.z); op[3] = from_f32<Tin>(o.w);
+  }
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = rg + RGS * i;
+    float4 acc = make_float4(gamma * s[i].x, gamma * s[i].y, gamma * s[i].z, gamma * s[i].w);
+#pragma unroll
+    for (int w = 0; w < MAXW; ++w) {
+      if (w >= W) break;
+      const float x = xw[w][r];
+      acc.x += x * dl[w].x; acc.y += x * dl[w].y; acc.z += x * dl[w].z; acc.w += x * dl[w].w;
+    }
+    Sg[(size_t)r * NQ + cq] = acc;
+  }
+  if (Wr > 0) {  // ring push of the current pair
+    const int slot = ring_slot(pos, Wr);
+    const bool ok = pos >= 1;
+    for (int d = tid; d < D; d += NT) {
+      reinterpret_cast<Tin*>(a.winx_out)[(bhi * Wr + slot) * D + d] = from_f32<Tin>(ok ? xw[Wr][d] : 0.f);
+      reinterpret_cast<Tin*>(a.winv_out)[(bhi * Wr + slot) * D + d] = from_f32<Tin>(ok ? vw[Wr][d] : 0.f);
+    }
+  }
+  for (int d = tid; d < D; d += NT)
+    reinterpret_cast<Tin*>(a.kprev_out)[bhi * D + d] = reinterpret_cast<const Tin*>(a.k)[bhi * D + d];
+  if (tid == 0) a.pos_out[bhi] = pos + 1;
+}
+
 template <typename Tin, int EPT>
 int launch_rec(const FwdArgs& a) {
   const int RG = kRecThreads / a.dv;
@@ -182,7 +338,7 @@ int launch_rec(const FwdArgs& a) {
                                        a.dv + (size_t)RG * (a.W + 1) * a.dv + (size_t)a.W * a.dv + 4);
   if (smem > 227 * 1024) return FALCON_ERR_UNSUPPORTED;
   auto k = recurrent_step_kernel<Tin, EPT>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
     return FALCON_ERR_CUDA;
   k<<<a.B * a.H, kRecThreads, smem, a.stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
@@ -205,7 +361,27 @@ int launch_rec_t(const FwdArgs& a) {
 
 }  // namespace
 
+template <typename Tin, int D, int NT>
+int launch_rec_vec(const FwdArgs& a) {
+  if (a.W <= 1) {
+    recurrent_step_vec_kernel<Tin, D, NT, 1><<<a.B * a.H, NT, 0, a.stream>>>(a);
+  } else if (a.W <= 8) {
+    recurrent_step_vec_kernel<Tin, D, NT, 8><<<a.B * a.H, NT, 0, a.stream>>>(a);
+  } else {
+    return -100;  // not covered: the generic kernel takes it
+  }
+  return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
+}
+
 int launch_recurrent_step(const FwdArgs& a) {
+  if (a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.W <= 8) {
+    int st;
+    if (a.dk == 64)
+      st = a.dtype == FALCON_BF16 ? launch_rec_vec<__nv_bfloat16, 64, 128>(a) : launch_rec_vec<float, 64, 128>(a);
+    else
+      st = a.dtype == FALCON_BF16 ? launch_rec_vec<__nv_bfloat16, 128, 256>(a) : launch_rec_vec<float, 128, 256>(a);
+    if (st != -100) return st;
+  }
   // the thread layout needs dv | 256 and dk*dv >= 256
   if (kRecThreads % a.dv != 0 || a.dk * a.dv < kRecThreads) return FALCON_ERR_UNSUPPORTED;
   return a.dtype == FALCON_BF16 ? launch_rec_t<__nv_bfloat16>(a) : launch_rec_t<float>(a);

@@ -777,13 +777,13 @@ __global__ void __launch_bounds__(256, 1)
 // ----------------------------------------------------------------------
 template <bool SOLVE>
 struct PipeSmem {
-  static constexpr int NST = SOLVE ? 2 : 3;               // TMA stages
+  static constexpr int NST = 3;                           // TMA stages
   static constexpr size_t XSZ = 8192, QSZ = 8192, VSZ = 8192, TSZ = SOLVE ? 16384 : 0, GSZ = 512;
   static constexpr size_t STAGE = XSZ + QSZ + VSZ + TSZ + 1024;
   static constexpr size_t SLOT0 = NST * STAGE;
-  // slot: P~ rows | W rows | U rows fp32 (stride 68) | Delta, Delta~ (additive) | gates
-  static constexpr size_t S_PM = 0, S_WB = 8192, S_U = S_WB + (SOLVE ? 8192 : 0);
-  static constexpr size_t S_DLA = S_U + (SOLVE ? 64 * 68 * 4 : 0);
+  // slot: P~ rows | W rows | Delta, Delta~ (additive) | gates  (U stays in TMEM)
+  static constexpr size_t S_PM = 0, S_WB = 8192;
+  static constexpr size_t S_DLA = S_WB + (SOLVE ? 8192 : 0);
   static constexpr size_t S_DDA = S_DLA + (SOLVE ? 0 : 8192);
   static constexpr size_t S_GATE = S_DDA + (SOLVE ? 0 : 8192);
   static constexpr size_t SLOT = (S_GATE + 2048 + 1023) / 1024 * 1024;
@@ -794,8 +794,9 @@ struct PipeSmem {
   static constexpr size_t BAR = OST + 2 * 8192;
   static constexpr size_t MISC = BAR + 128;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
-  static constexpr uint32_t COL_P = 0, COL_W = 64, COL_U = 128, COL_D1 = 192, COL_OA = 256,
-                            COL_D2 = 320, COL_OB = 384;
+  // TMEM: front P, W, U (U double-buffered: the back reads it), back D1, OA, D2, OB
+  static constexpr uint32_t COL_P = 0, COL_W = 64, COL_U = 128, COL_D1 = 256, COL_OA = 320,
+                            COL_D2 = 384, COL_OB = 448;
   static_assert(TOTAL <= 232448, "shared memory budget");
   // gate arrays inside a slot (fp32 x 64 each)
   static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192, G_EX = 256, G_ET = 320;
@@ -822,8 +823,8 @@ __global__ void __launch_bounds__(288, 1)
   uint64_t* empty = bars + 3;   // [NST]
   uint64_t* fdone = bars + 6;   // [2]
   uint64_t* bdone = bars + 8;   // [2]
-  uint64_t* fmma = bars + 10;
-  uint64_t* bmma = bars + 11;
+  uint64_t* fmma = bars + 10;   // [2]: P done, W/U done
+  uint64_t* bmma = bars + 12;   // [4]: D1, OA, D2, OB done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -850,8 +851,8 @@ __global__ void __launch_bounds__(288, 1)
     *abort_flag = 0;
     for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&fdone[i], 128); mbar_init(&bdone[i], 128); }
-    mbar_init(fmma, 1);
-    mbar_init(bmma, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&fmma[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bmma[i], 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -938,17 +939,17 @@ __global__ void __launch_bounds__(288, 1)
       if (ftid == 0) {
         const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s)), sT = smem_u32(Tst(s));
         mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, 64, idesc_bf16(64, 64), false);
+        umma_commit(&fmma[0]);
         if (SOLVE) {
           // W = T diag(eta Gamma) X, U = T diag(eta) V, straight from the TMA tiles
           mma_chain_mn(tmem + L::COL_W, kdesc<64>, sT, mndesc, sX, 64, idesc_bf16(64, 64, false, true),
                        false);
-          mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT + 8192, mndesc, smem_u32(Vst(s)), 64,
+          mma_chain_mn(tmem + L::COL_U + 64 * p, kdesc<64>, sT + 8192, mndesc, smem_u32(Vst(s)), 64,
                        idesc_bf16(64, 64, false, true), false);
+          umma_commit(&fmma[1]);
         }
-        umma_commit(fmma);
       }
-      if (!mbar_wait(fmma, fph)) fail();
-      fph ^= 1;
+      if (!mbar_wait(&fmma[0], fph)) fail();
       tc_fence_after();
       {  // P~ rows: decay exp(g_r - g_i) for i <= r, factored per 16-block
         float pv[64];
@@ -982,20 +983,15 @@ __global__ void __launch_bounds__(288, 1)
           store_row64(sl + L::S_PM, r64, pv);
         }
       }
-      if (SOLVE) {  // W rows (bf16 K-major operand) and U rows (fp32)
+      if (SOLVE) {  // W rows -> bf16 K-major operand (U stays in TMEM for the back)
+        if (!mbar_wait(&fmma[1], fph)) fail();
+        tc_fence_after();
         float wv[64];
         tmem_ld64(tmem + lane_off + L::COL_W, wv);
         tmem_wait_ld();
         if (row64) store_row64(sl + L::S_WB, r64, wv);
-        tmem_ld64(tmem + lane_off + L::COL_U, wv);
-        tmem_wait_ld();
-        if (row64) {
-          float* urow = reinterpret_cast<float*>(sl + L::S_U) + r64 * 68;
-#pragma unroll
-          for (int n = 0; n < 64; n += 4)
-            *reinterpret_cast<float4*>(urow + n) = make_float4(wv[n], wv[n + 1], wv[n + 2], wv[n + 3]);
-        }
       }
+      fph ^= 1;
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&fdone[p]);
@@ -1034,35 +1030,42 @@ __global__ void __launch_bounds__(288, 1)
       const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(sl + L::S_DLA);
       const uint32_t sDD = SOLVE ? smem_u32(sm + L::DD) : smem_u32(sl + L::S_DDA);
       if (tid == 0) {
-        if (SOLVE)
+        if (SOLVE) {
           mma_chain_mn(tmem + L::COL_D1, kdesc<64>, smem_u32(sl + L::S_WB), mndesc, sS, 64,
                        idesc_bf16(64, 64, false, true), false);
+          umma_commit(&bmma[0]);
+        }
         mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, 64, idesc_bf16(64, 64, false, true),
                      false);
-        umma_commit(bmma);
+        umma_commit(&bmma[1]);
       }
-      if (!mbar_wait(bmma, bph)) fail();
-      bph ^= 1;
-      tc_fence_after();
       if (SOLVE) {  // Delta = U - W S0, and diag(exp(g_last - g)) Delta
-        float dv1[64];
-        tmem_ld64(tmem + lane_off + L::COL_D1, dv1);
-        tmem_wait_ld();
-        if (row64) {
-          const float* urow = reinterpret_cast<const float*>(sl + L::S_U) + r64 * 68;
+        if (!mbar_wait(&bmma[0], bph)) fail();
+        tc_fence_after();
+        const float dr = gt[L::G_DEC + r64];
 #pragma unroll
-          for (int n = 0; n < 64; n += 4) {
-            const float4 u = *reinterpret_cast<const float4*>(urow + n);
-            dv1[n] = u.x - dv1[n];
-            dv1[n + 1] = u.y - dv1[n + 1];
-            dv1[n + 2] = u.z - dv1[n + 2];
-            dv1[n + 3] = u.w - dv1[n + 3];
+        for (int hf = 0; hf < 2; ++hf) {  // two 32-column halves keep registers low
+          uint32_t d1[32], uu[32];
+          tmem_ld32(tmem + lane_off + L::COL_D1 + 32 * hf, d1);
+          tmem_ld32(tmem + lane_off + L::COL_U + 64 * p + 32 * hf, uu);
+          tmem_wait_ld();
+          if (row64) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t pd[4], ps[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int n = 8 * j + 2 * e;
+                const float x0 = __uint_as_float(uu[n]) - __uint_as_float(d1[n]);
+                const float x1 = __uint_as_float(uu[n + 1]) - __uint_as_float(d1[n + 1]);
+                pd[e] = pack_bf16(x0, x1);
+                ps[e] = pack_bf16(x0 * dr, x1 * dr);
+              }
+              const uint32_t off = sw128(r64, 32 * hf + 8 * j);
+              *reinterpret_cast<uint4*>(sm + L::DL + off) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
+              *reinterpret_cast<uint4*>(sm + L::DD + off) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
+            }
           }
-          store_row64(sm + L::DL, r64, dv1);
-          const float dr = gt[L::G_DEC + r64];
-#pragma unroll
-          for (int n = 0; n < 64; ++n) dv1[n] *= dr;
-          store_row64(sm + L::DD, r64, dv1);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -1071,26 +1074,32 @@ __global__ void __launch_bounds__(288, 1)
       }
       if (tid == 0) {
         mma_chain_mn(tmem + L::COL_D2, mndesc, sX, mndesc, sDD, 64, idesc_bf16(64, 64, true, true), false);
+        umma_commit(&bmma[2]);
         mma_chain_mn(tmem + L::COL_OB, kdesc<64>, smem_u32(sl + L::S_PM), mndesc, sDL, 64,
                      idesc_bf16(64, 64, false, true), false);
-        umma_commit(bmma);
+        umma_commit(&bmma[3]);
       }
-      if (!mbar_wait(bmma, bph)) fail();
+      uint8_t* Ost = sm + L::OST + (c & 1) * 8192;
+      if (!mbar_wait(&bmma[2], bph)) fail();
+      tc_fence_after();
+      {  // S1 = Gamma_last S0 + D2
+        const float gl_ = gt[L::G_GAM + 63];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t d2[32];
+          tmem_ld32(tmem + lane_off + L::COL_D2 + 32 * hf, d2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int n = 0; n < 32; ++n) sreg[32 * hf + n] = gl_ * sreg[32 * hf + n] + __uint_as_float(d2[n]);
+        }
+        if (row64) store_row64(SB, r64, sreg);
+      }
+      bool okb = mbar_wait(&bmma[1], bph);
+      okb = mbar_wait(&bmma[3], bph) && okb;
+      if (!okb) fail();
       bph ^= 1;
       tc_fence_after();
       if (tid == 0) mbar_arrive(&empty[s]);  // the stage's tiles are no longer read
-      uint8_t* Ost = sm + L::OST + (c & 1) * 8192;
-      {  // S1 = Gamma_last S0 + D2
-        float d2[64];
-        tmem_ld64(tmem + lane_off + L::COL_D2, d2);
-        tmem_wait_ld();
-        if (row64) {
-          const float gl_ = gt[L::G_GAM + 63];
-#pragma unroll
-          for (int n = 0; n < 64; ++n) sreg[n] = gl_ * sreg[n] + d2[n];
-          store_row64(SB, r64, sreg);
-        }
-      }
       {  // O = diag(Gamma) Oa + Ob
         const float gr = gt[L::G_GAM + r64];
 #pragma unroll
@@ -1200,7 +1209,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
   {
     auto k = tc_wy_kernel<DK, SOLVE>;
     const size_t smem = WySmem<DK>::TOTAL;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
       return FALCON_ERR_CUDA;
     dim3 grid((ta.NC + 1) / 2, BH);
     record_event(fa, 0);
@@ -1210,14 +1219,14 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
   if (DK == 64) {  // pipelined: producer warp, front and back warpgroups
     auto k = tc_fwd_pipe_kernel<SOLVE>;
     const size_t smem = PipeSmem<SOLVE>::TOTAL;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
       return FALCON_ERR_CUDA;
     k<<<BH, 288, smem, fa.stream>>>(mq, mk, mv, mo, ta);
     record_event(fa, 2);
   } else {
     auto k = tc_fwd_kernel<DK, NV, SOLVE>;
     const size_t smem = FwdSmem<DK, NV, SOLVE>::TOTAL;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
       return FALCON_ERR_CUDA;
     dim3 grid(BH, nsplit);
     k<<<grid, 256, smem, fa.stream>>>(mq, mk, mv, mo, ta);
