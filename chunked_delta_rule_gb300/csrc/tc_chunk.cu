@@ -58,7 +58,7 @@ struct TcArgs {
   float* S_out;
   __nv_bfloat16* kprev_out;
   int64_t* pos_out;
-  uint8_t* ws_T;      // [B*H*NC][16384]: bf16 swizzled images of T diag(eta Gamma), T diag(eta)
+  uint8_t* ws_T;      // [B*H*NC][16384]: bf16 swizzled images of T diag(eta), T diag(eta Gamma)
   float* ws_g;        // [B*H*NC][128]: eta[64], g[64]
   uint32_t* status;   // workspace status word
 };
@@ -332,8 +332,8 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
   }
   named_bar(nb_id, 64);
   if (chunk < a.NC && !aborted) {
-    // bf16 images of T diag(eta Gamma) (for W) and T diag(eta) (for U) as
-    // 128B-swizzled K-major tiles; the upper triangle is zero
+    // bf16 images of T diag(eta) (for U) and T diag(eta Gamma) (for W) as
+    // 128B-swizzled K-major tiles, in that order; the upper triangle is zero
     uint8_t* To = a.ws_T + ((size_t)bh * a.NC + chunk) * 16384;
     const float* ec = es + cidx * 64;
     const float* gc = gms + cidx * 64;
@@ -351,8 +351,8 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
         pu[e] = pack_bf16(t0 * ec[c0], t1 * ec[c0 + 1]);
       }
       const int off = R * 128 + 16 * (j ^ (R & 7));
-      *reinterpret_cast<uint4*>(To + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-      *reinterpret_cast<uint4*>(To + 8192 + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+      *reinterpret_cast<uint4*>(To + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+      *reinterpret_cast<uint4*>(To + 8192 + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
     }
     float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * 128;
     go[rl] = eta;
@@ -597,9 +597,9 @@ __global__ void __launch_bounds__(256, 1)
       mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, DK, idesc_bf16(64, 64), false);
       if (SOLVE) {
         for (int k = 0; k < L::kKS; ++k)  // W = T diag(eta Gamma) X, U = T diag(eta) V
-          mma_chain_mn(tmem + L::COL_W + 64 * k, kdesc<64>, sT, mndesc, sX + k * 8192, 64,
+          mma_chain_mn(tmem + L::COL_W + 64 * k, kdesc<64>, sT + 8192, mndesc, sX + k * 8192, 64,
                        idesc_bf16(64, 64, false, true), false);
-        mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT + 8192, mndesc, smem_u32(Vst(s)), 64,
+        mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT, mndesc, smem_u32(Vst(s)), 64,
                      idesc_bf16(64, NV, false, true), false);
       }
       mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
@@ -767,39 +767,46 @@ __global__ void __launch_bounds__(256, 1)
 // ----------------------------------------------------------------------
 // (b') pipelined sequential kernel, d_k = d_v = 64.  Three roles:
 //   warp 8      producer: TMA of chunk c into one of three stages
-//   warps 4..7  front: the state-independent part of chunk c (gates, row
-//               scaling, P = Q X^T, W = T X^, U = T V^, the decay-masked
-//               P~) into a double-buffered slot
-//   warps 0..3  back: the state chain of chunk c (W S0, Q S0, Delta,
-//               X^T Delta~, P~ Delta, state update, output tile)
-// so the front of chunk c+1 overlaps the back of chunk c.  Hand-offs are
-// mbarriers: full/empty per stage, fdone/bdone per slot.
+//   warps 4..7  front: the state-independent part of chunk c into a
+//               double-buffered slot
+//   warps 0..3  back: the state chain of chunk c
+// so the front of chunk c+1 overlaps the back of chunk c.  Products that
+// share an operand are stacked into one 128-row or 128-column MMA:
+//   front  P^T = X Q^T                                   (M 64,  N 64)
+//          [U  . ; .  W] = [T diag(eta) ; T diag(eta Gamma)] [V | X]   (M 128, N 128)
+//   back   [D1 ; Oa] = [W ; Q] S0                        (M 128, N 64)
+//          [D2 ; Ob] = [X~ | P~^T]^T-as-MN-major Delta   (M 128, N 64)
+// with Delta = U - D1 (Falcon-1A: diag(eta) V), X~ = diag(exp(g_last - g)) X,
+// P~ = (Q X^T) (.) [exp(g_r - g_i)]_{i<=r}, S1 = Gamma_last S0 + D2 and
+// O = diag(Gamma) Oa + Ob.  Hand-offs are mbarriers: full/empty per stage,
+// fdone/bdone per slot.
 // ----------------------------------------------------------------------
 template <bool SOLVE>
 struct PipeSmem {
-  static constexpr int NST = 3;                           // TMA stages
-  static constexpr size_t XSZ = 8192, QSZ = 8192, VSZ = 8192, TSZ = SOLVE ? 16384 : 0, GSZ = 512;
-  static constexpr size_t STAGE = XSZ + QSZ + VSZ + TSZ + 1024;
+  static constexpr int NST = 3;  // TMA stages
+  // stage: V | X (adjacent: [V | X] is one MN-major operand) | Q | T diag(eta), T diag(eta Gamma) | gates
+  static constexpr size_t VO = 0, XO = 8192, QO = 16384, TO = 24576;
+  static constexpr size_t TSZ = SOLVE ? 16384 : 0, GSZ = 512;
+  static constexpr size_t GO = TO + TSZ;
+  static constexpr size_t STAGE = GO + 1024;
   static constexpr size_t SLOT0 = NST * STAGE;
-  // slot: P~ rows | W rows | Delta, Delta~ (additive) | gates  (U stays in TMEM)
-  static constexpr size_t S_PM = 0, S_WB = 8192;
-  static constexpr size_t S_DLA = S_WB + (SOLVE ? 8192 : 0);
-  static constexpr size_t S_DDA = S_DLA + (SOLVE ? 0 : 8192);
-  static constexpr size_t S_GATE = S_DDA + (SOLVE ? 0 : 8192);
-  static constexpr size_t SLOT = (S_GATE + 2048 + 1023) / 1024 * 1024;
+  // slot: A1 = [W ; Q] (K-major, 128 rows) | A2 = [X~ | P~^T] (MN-major, two atoms) |
+  //       Delta rows (additive write) | gates
+  static constexpr size_t S_A1 = 0, S_A2 = 16384, S_DLA = 32768;
+  static constexpr size_t S_GATE = S_DLA + (SOLVE ? 0 : 8192);
+  static constexpr size_t SLOT = S_GATE + 2048;
   static constexpr size_t SB = SLOT0 + 2 * SLOT;          // S rows (MN-major B)
-  static constexpr size_t DL = SB + 8192;                 // Delta rows
-  static constexpr size_t DD = DL + (SOLVE ? 8192 : 0);   // Delta~ rows
-  static constexpr size_t OST = DD + (SOLVE ? 8192 : 0);  // two output staging tiles
+  static constexpr size_t DL = SB + 8192;                 // Delta rows (MN-major B)
+  static constexpr size_t OST = DL + (SOLVE ? 8192 : 0);  // two output staging tiles
   static constexpr size_t BAR = OST + 2 * 8192;
   static constexpr size_t MISC = BAR + 128;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
-  // TMEM: front P, W, U (U double-buffered: the back reads it), back D1, OA, D2, OB
-  static constexpr uint32_t COL_P = 0, COL_W = 64, COL_U = 128, COL_D1 = 256, COL_OA = 320,
-                            COL_D2 = 384, COL_OB = 448;
   static_assert(TOTAL <= 232448, "shared memory budget");
+  static_assert(STAGE % 1024 == 0 && SLOT % 1024 == 0, "1 KB aligned tiles");
+  // TMEM: P^T (M=64 layout) | [U . ; . W] x 2 slots (M=128) | [D1 ; Oa] | [D2 ; Ob]
+  static constexpr uint32_t COL_PT = 0, COL_UW = 64, COL_B1 = 320, COL_B2 = 384;
   // gate arrays inside a slot (fp32 x 64 each)
-  static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192, G_EX = 256, G_ET = 320;
+  static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192, G_ET = 256;
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -817,14 +824,14 @@ __global__ void __launch_bounds__(288, 1)
   using L = PipeSmem<SOLVE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
   constexpr int NST = L::NST;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* full = bars;        // [NST]
   uint64_t* empty = bars + 3;   // [NST]
   uint64_t* fdone = bars + 6;   // [2]
   uint64_t* bdone = bars + 8;   // [2]
-  uint64_t* fmma = bars + 10;   // [2]: P done, W/U done
-  uint64_t* bmma = bars + 12;   // [4]: D1, OA, D2, OB done
+  uint64_t* fmma = bars + 10;   // [2]: P^T done, [U ; W] done
+  uint64_t* bmma = bars + 12;   // [2]: [D1 ; Oa] done, [D2 ; Ob] done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -833,13 +840,7 @@ __global__ void __launch_bounds__(288, 1)
   const int b = bh / a.H, h = bh % a.H;
   const int NC = a.NC;
   auto stage = [&](int s) { return sm + s * L::STAGE; };
-  auto Xst = [&](int s) { return stage(s); };
-  auto Qst = [&](int s) { return stage(s) + L::XSZ; };
-  auto Vst = [&](int s) { return stage(s) + L::XSZ + L::QSZ; };
-  auto Tst = [&](int s) { return stage(s) + L::XSZ + L::QSZ + L::VSZ; };
-  auto Gst = [&](int s) {
-    return reinterpret_cast<const float*>(stage(s) + L::XSZ + L::QSZ + L::VSZ + L::TSZ);
-  };
+  auto Gst = [&](int s) { return reinterpret_cast<const float*>(stage(s) + L::GO); };
   auto slot = [&](int p) { return sm + L::SLOT0 + p * L::SLOT; };
   auto gates = [&](int p) { return reinterpret_cast<float*>(slot(p) + L::S_GATE); };
   auto fail = [&]() {
@@ -851,21 +852,23 @@ __global__ void __launch_bounds__(288, 1)
     *abort_flag = 0;
     for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&fdone[i], 128); mbar_init(&bdone[i], 128); }
-    for (int i = 0; i < 2; ++i) mbar_init(&fmma[i], 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&bmma[i], 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&fmma[i], 1); mbar_init(&bmma[i], 1); }
     fence_mbar_init();
+  }
+  if (!SOLVE) {  // additive write: the W rows of [W ; Q] stay zero
+    for (int i = tid; i < 2 * 512; i += 288)
+      *reinterpret_cast<uint4*>(slot(i >> 9) + L::S_A1 + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
     tc_fence_before();
   }
+  fence_proxy_async();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int quad = warp & 3;
-  const bool row64 = lane < 16;
-  const int r64 = 16 * quad + lane;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
 
   if (warp == 8) {
@@ -876,13 +879,14 @@ __global__ void __launch_bounds__(288, 1)
         const int s = c % NST;
         if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1))) { fail(); break; }
         if (*abort_flag) break;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(L::XSZ + L::QSZ + L::VSZ + L::TSZ + L::GSZ));
-        tma_load_4d(Xst(s), &tm_k, &full[s], 0, h, c * kC - 1, b);
-        tma_load_4d(Qst(s), &tm_q, &full[s], 0, h, c * kC, b);
-        tma_load_4d(Vst(s), &tm_v, &full[s], 0, h, c * kC, b);
+        uint8_t* st = stage(s);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(3 * 8192 + L::TSZ + L::GSZ));
+        tma_load_4d(st + L::VO, &tm_v, &full[s], 0, h, c * kC, b);
+        tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - 1, b);
+        tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
         const size_t ci = (size_t)bh * NC + c;
-        if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 16384, 16384, &full[s]);
-        bulk_load(const_cast<float*>(Gst(s)), a.ws_g + ci * 128, 512, &full[s]);
+        if (SOLVE) bulk_load(st + L::TO, a.ws_T + ci * 16384, 16384, &full[s]);
+        bulk_load(st + L::GO, a.ws_g + ci * 128, 512, &full[s]);
       }
       if (*abort_flag) {  // drain the loads still in flight
         for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
@@ -892,106 +896,99 @@ __global__ void __launch_bounds__(288, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ front
     const int ftid = tid - 128;
+    const bool row64 = lane < 16;
+    const int i64 = 16 * quad + lane;  // P^T row (key index) in the M = 64 layout
     uint32_t fph = 0;
     for (int c = 0; c < NC; ++c) {
       const int s = c % NST, p = c & 1;
       bool ok = mbar_wait(&full[s], (uint32_t)((c / NST) & 1));
       if (c >= 2) ok = ok && mbar_wait(&bdone[p], (uint32_t)(((c - 2) >> 1) & 1));
       if (!ok) fail();
+      uint8_t* st = stage(s);
       if (c == 0 && a.kprev_in && ftid < 64)  // x_0 = carried key
-        *reinterpret_cast<__nv_bfloat16*>(Xst(0) + sw128(0, ftid)) = a.kprev_in[(size_t)bh * 64 + ftid];
+        *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = a.kprev_in[(size_t)bh * 64 + ftid];
       float* gt = gates(p);
       if (ftid < 64) {
         const float* G = Gst(s);
-        const float g = G[64 + ftid], glast = G[127], e = G[ftid];
-        const float gend = G[64 + (ftid | 15)];
-        const float gm = __expf(g);
-        gt[L::G_GAM + ftid] = gm;
+        const float g = G[64 + ftid], glast = G[127];
+        gt[L::G_GAM + ftid] = __expf(g);
         gt[L::G_DEC + ftid] = __expf(glast - g);
         gt[L::G_GL + ftid] = g;
-        gt[L::G_CF + ftid] = __expf(gend - g);
-        gt[L::G_EX + ftid] = e * gm;   // row scale of X: eta Gamma
-        gt[L::G_ET + ftid] = e;        // row scale of V: eta
+        gt[L::G_CF + ftid] = __expf(g - G[64 + (ftid & ~15)]);  // decay from the 16-block start
+        gt[L::G_ET + ftid] = G[ftid];
       }
       named_bar(1, 128);
       if (*abort_flag) break;
       uint8_t* sl = slot(p);
-      if (!SOLVE) {
-        scale_rows(sl + L::S_DLA, Vst(s), gt + L::G_ET, ftid, 128);  // Delta = diag(eta) V
-        for (int idx = ftid; idx < 512; idx += 128) {                  // Delta~ rows
-          const int R = idx >> 3;
-          const uint4 in = *reinterpret_cast<const uint4*>(Vst(s) + idx * 16);
-          const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-          const float fr = gt[L::G_ET + R] * gt[L::G_DEC + R];
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 x = __bfloat1622float2(pin[e]);
-            pk[e] = pack_bf16(x.x * fr, x.y * fr);
-          }
-          *reinterpret_cast<uint4*>(sl + L::S_DDA + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-      }
+      // X~ rows (atom 0 of A2), the Q rows of [W ; Q], additive Delta rows
+      scale_rows(sl + L::S_A2, st + L::XO, gt + L::G_DEC, ftid, 128);
+      for (int idx = ftid; idx < 512; idx += 128)
+        *reinterpret_cast<uint4*>(sl + L::S_A1 + 8192 + idx * 16) =
+            *reinterpret_cast<const uint4*>(st + L::QO + idx * 16);
+      if (!SOLVE) scale_rows(sl + L::S_DLA, st + L::VO, gt + L::G_ET, ftid, 128);
       fence_proxy_async();
       tc_fence_before();
       named_bar(1, 128);
       tc_fence_after();
       if (ftid == 0) {
-        const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s)), sT = smem_u32(Tst(s));
-        mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, 64, idesc_bf16(64, 64), false);
+        const uint32_t sV = smem_u32(st + L::VO), sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
+        // P^T = X Q^T
+        mma_chain_mn(tmem + L::COL_PT, kdesc<64>, sX, kdesc<64>, sQ, 64, idesc_bf16(64, 64), false);
         umma_commit(&fmma[0]);
-        if (SOLVE) {
-          // W = T diag(eta Gamma) X, U = T diag(eta) V, straight from the TMA tiles
-          mma_chain_mn(tmem + L::COL_W, kdesc<64>, sT, mndesc, sX, 64, idesc_bf16(64, 64, false, true),
-                       false);
-          mma_chain_mn(tmem + L::COL_U + 64 * p, kdesc<64>, sT + 8192, mndesc, smem_u32(Vst(s)), 64,
-                       idesc_bf16(64, 64, false, true), false);
+        if (SOLVE) {  // [T diag(eta) ; T diag(eta Gamma)] [V | X]
+          const uint32_t sT = smem_u32(st + L::TO);
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + L::COL_UW + 128 * p, kdesc<128>(sT, ks), sdesc_mn128_wide(sV + ks * 2048, 8192),
+                      idesc_bf16(128, 128, false, true), ks > 0 ? 1u : 0u);
           umma_commit(&fmma[1]);
         }
       }
       if (!mbar_wait(&fmma[0], fph)) fail();
       tc_fence_after();
-      {  // P~ rows: decay exp(g_r - g_i) for i <= r, factored per 16-block
+      {  // P~^T rows: P[r][i] exp(g_r - g_i) for r >= i, the decay factored per 16-block of r
         float pv[64];
-        tmem_ld64(tmem + lane_off + L::COL_P, pv);
+        tmem_ld64(tmem + lane_off + L::COL_PT, pv);
         tmem_wait_ld();
         if (row64) {
           const float* gl = gt + L::G_GL;
           const float* cf = gt + L::G_CF;
-          const float gr = gl[r64];
+          const float gi = gl[i64];
 #pragma unroll
           for (int J = 0; J < 4; ++J) {
-            if (J < quad) {
-              const float rf = __expf(gr - gl[16 * J + 15]);
+            if (J > quad) {
+              const float f = __expf(gl[16 * J] - gi);
 #pragma unroll
-              for (int i = 16 * J; i < 16 * J + 16; i += 4) {
-                const float4 c4 = *reinterpret_cast<const float4*>(cf + i);
-                pv[i] *= rf * c4.x;
-                pv[i + 1] *= rf * c4.y;
-                pv[i + 2] *= rf * c4.z;
-                pv[i + 3] *= rf * c4.w;
+              for (int r = 16 * J; r < 16 * J + 16; r += 4) {
+                const float4 c4 = *reinterpret_cast<const float4*>(cf + r);
+                pv[r] *= f * c4.x;
+                pv[r + 1] *= f * c4.y;
+                pv[r + 2] *= f * c4.z;
+                pv[r + 3] *= f * c4.w;
               }
             } else if (J == quad) {
 #pragma unroll
-              for (int i = 16 * J; i < 16 * J + 16; ++i)
-                pv[i] = (i <= r64) ? __expf(gr - gl[i]) * pv[i] : 0.f;
+              for (int r = 16 * J; r < 16 * J + 16; ++r)
+                pv[r] = (r >= i64) ? __expf(gl[r] - gi) * pv[r] : 0.f;
             } else {
 #pragma unroll
-              for (int i = 16 * J; i < 16 * J + 16; ++i) pv[i] = 0.f;
+              for (int r = 16 * J; r < 16 * J + 16; ++r) pv[r] = 0.f;
             }
           }
-          store_row64(sl + L::S_PM, r64, pv);
+          store_row64(sl + L::S_A2 + 8192, i64, pv);
         }
       }
-      if (SOLVE) {  // W rows -> bf16 K-major operand (U stays in TMEM for the back)
+      if (SOLVE) {  // W rows (lanes 64..127 of the stacked product) -> rows 0..63 of [W ; Q]
         if (!mbar_wait(&fmma[1], fph)) fail();
         tc_fence_after();
-        float wv[64];
-        tmem_ld64(tmem + lane_off + L::COL_W, wv);
-        tmem_wait_ld();
-        if (row64) store_row64(sl + L::S_WB, r64, wv);
+        if (quad >= 2) {
+          float wv[64];
+          tmem_ld64(tmem + lane_off + L::COL_UW + 128 * p + 64, wv);
+          tmem_wait_ld();
+          store_row64(sl + L::S_A1, 32 * (quad - 2) + lane, wv);
+        }
       }
       fph ^= 1;
+      if (ftid == 0) mbar_arrive(&empty[s]);  // the stage's tiles are no longer read
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&fdone[p]);
@@ -1001,69 +998,64 @@ __global__ void __launch_bounds__(288, 1)
     if (a.pos_out && !*abort_flag && ftid == 0) a.pos_out[bh] = (a.pos_in ? a.pos_in[bh] : 0) + a.T;
   } else {
     // ------------------------------------------------------------ back
+    // warps 0, 1: S rows 32 w + lane (lanes 0..63 of the stacked products);
+    // warps 2, 3: output rows 32 (w - 2) + lane (lanes 64..127)
     uint8_t* SB = sm + L::SB;
     const uint32_t sS = smem_u32(SB);
+    const bool srow = warp < 2;
+    const int r = 32 * (warp & 1) + lane;
     float sreg[64];
 #pragma unroll
     for (int n = 0; n < 64; ++n) sreg[n] = 0.f;
-    if (row64 && a.S_in) {
-      const float* src = a.S_in + ((size_t)bh * 64 + r64) * 64;
+    if (srow && a.S_in) {
+      const float* src = a.S_in + ((size_t)bh * 64 + r) * 64;
 #pragma unroll
       for (int n = 0; n < 64; n += 4) {
         const float4 v = *reinterpret_cast<const float4*>(src + n);
         sreg[n] = v.x; sreg[n + 1] = v.y; sreg[n + 2] = v.z; sreg[n + 3] = v.w;
       }
     }
-    if (row64) store_row64(SB, r64, sreg);
+    if (srow) store_row64(SB, r, sreg);
     fence_proxy_async();
     named_bar(2, 128);
     uint32_t bph = 0;
     for (int c = 0; c < NC; ++c) {
-      const int s = c % NST, p = c & 1;
+      const int p = c & 1;
       if (!mbar_wait(&fdone[p], (uint32_t)((c >> 1) & 1))) fail();
       tc_fence_after();
       named_bar(2, 128);
       if (*abort_flag) break;
       uint8_t* sl = slot(p);
       const float* gt = gates(p);
-      const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s));
       const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(sl + L::S_DLA);
-      const uint32_t sDD = SOLVE ? smem_u32(sm + L::DD) : smem_u32(sl + L::S_DDA);
-      if (tid == 0) {
-        if (SOLVE) {
-          mma_chain_mn(tmem + L::COL_D1, kdesc<64>, smem_u32(sl + L::S_WB), mndesc, sS, 64,
-                       idesc_bf16(64, 64, false, true), false);
-          umma_commit(&bmma[0]);
-        }
-        mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, 64, idesc_bf16(64, 64, false, true),
-                     false);
-        umma_commit(&bmma[1]);
+      if (tid == 0) {  // [D1 ; Oa] = [W ; Q] S0
+        const uint32_t sA1 = smem_u32(sl + L::S_A1);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + L::COL_B1, kdesc<128>(sA1, ks), mndesc(sS, ks), idesc_bf16(128, 64, false, true),
+                    ks > 0 ? 1u : 0u);
+        umma_commit(&bmma[0]);
       }
-      if (SOLVE) {  // Delta = U - W S0, and diag(exp(g_last - g)) Delta
+      if (SOLVE) {  // Delta = U - W S0 (rows 0..63: warps 0, 1)
         if (!mbar_wait(&bmma[0], bph)) fail();
         tc_fence_after();
-        const float dr = gt[L::G_DEC + r64];
+        if (srow) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {  // two 32-column halves keep registers low
-          uint32_t d1[32], uu[32];
-          tmem_ld32(tmem + lane_off + L::COL_D1 + 32 * hf, d1);
-          tmem_ld32(tmem + lane_off + L::COL_U + 64 * p + 32 * hf, uu);
-          tmem_wait_ld();
-          if (row64) {
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t d1[32], uu[32];
+            tmem_ld32(tmem + lane_off + L::COL_B1 + 32 * hf, d1);
+            tmem_ld32(tmem + lane_off + L::COL_UW + 128 * p + 32 * hf, uu);
+            tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              uint32_t pd[4], ps[4];
+              uint32_t pd[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int n = 8 * j + 2 * e;
-                const float x0 = __uint_as_float(uu[n]) - __uint_as_float(d1[n]);
-                const float x1 = __uint_as_float(uu[n + 1]) - __uint_as_float(d1[n + 1]);
-                pd[e] = pack_bf16(x0, x1);
-                ps[e] = pack_bf16(x0 * dr, x1 * dr);
+                pd[e] = pack_bf16(__uint_as_float(uu[n]) - __uint_as_float(d1[n]),
+                                  __uint_as_float(uu[n + 1]) - __uint_as_float(d1[n + 1]));
               }
-              const uint32_t off = sw128(r64, 32 * hf + 8 * j);
-              *reinterpret_cast<uint4*>(sm + L::DL + off) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
-              *reinterpret_cast<uint4*>(sm + L::DD + off) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
+              *reinterpret_cast<uint4*>(sm + L::DL + sw128(r, 32 * hf + 8 * j)) =
+                  make_uint4(pd[0], pd[1], pd[2], pd[3]);
             }
           }
         }
@@ -1072,55 +1064,48 @@ __global__ void __launch_bounds__(288, 1)
         named_bar(2, 128);
         tc_fence_after();
       }
-      if (tid == 0) {
-        mma_chain_mn(tmem + L::COL_D2, mndesc, sX, mndesc, sDD, 64, idesc_bf16(64, 64, true, true), false);
-        umma_commit(&bmma[2]);
-        mma_chain_mn(tmem + L::COL_OB, kdesc<64>, smem_u32(sl + L::S_PM), mndesc, sDL, 64,
-                     idesc_bf16(64, 64, false, true), false);
-        umma_commit(&bmma[3]);
+      if (tid == 0) {  // [D2 ; Ob] = [X~ | P~^T] Delta, A MN-major over two atoms
+        const uint32_t sA2 = smem_u32(sl + L::S_A2);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + L::COL_B2, sdesc_mn128_wide(sA2 + ks * 2048, 8192), mndesc(sDL, ks),
+                    idesc_bf16(128, 64, true, true), ks > 0 ? 1u : 0u);
+        umma_commit(&bmma[1]);
       }
       uint8_t* Ost = sm + L::OST + (c & 1) * 8192;
-      if (!mbar_wait(&bmma[2], bph)) fail();
+      bool okb = mbar_wait(&bmma[1], bph);
+      if (!SOLVE) okb = mbar_wait(&bmma[0], bph) && okb;
+      if (!okb) fail();
+      bph ^= 1;
       tc_fence_after();
-      {  // S1 = Gamma_last S0 + D2
+      if (srow) {  // S1 = Gamma_last S0 + D2
         const float gl_ = gt[L::G_GAM + 63];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t d2[32];
-          tmem_ld32(tmem + lane_off + L::COL_D2 + 32 * hf, d2);
+          tmem_ld32(tmem + lane_off + L::COL_B2 + 32 * hf, d2);
           tmem_wait_ld();
 #pragma unroll
           for (int n = 0; n < 32; ++n) sreg[32 * hf + n] = gl_ * sreg[32 * hf + n] + __uint_as_float(d2[n]);
         }
-        if (row64) store_row64(SB, r64, sreg);
-      }
-      bool okb = mbar_wait(&bmma[1], bph);
-      okb = mbar_wait(&bmma[3], bph) && okb;
-      if (!okb) fail();
-      bph ^= 1;
-      tc_fence_after();
-      if (tid == 0) mbar_arrive(&empty[s]);  // the stage's tiles are no longer read
-      {  // O = diag(Gamma) Oa + Ob
-        const float gr = gt[L::G_GAM + r64];
+        store_row64(SB, r, sreg);
+      } else {  // O = diag(Gamma) Oa + Ob
+        const float gr = gt[L::G_GAM + r];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t oa[32], ob[32];
-          tmem_ld32(tmem + lane_off + L::COL_OA + 32 * hf, oa);
-          tmem_ld32(tmem + lane_off + L::COL_OB + 32 * hf, ob);
+          tmem_ld32(tmem + lane_off + L::COL_B1 + 32 * hf, oa);
+          tmem_ld32(tmem + lane_off + L::COL_B2 + 32 * hf, ob);
           tmem_wait_ld();
-          if (row64) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t pk[4];
+          for (int j = 0; j < 4; ++j) {
+            uint32_t pk[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int n = 8 * j + 2 * e;
-                pk[e] = pack_bf16(gr * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
-                                  gr * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
-              }
-              *reinterpret_cast<uint4*>(Ost + sw128(r64, 32 * hf + 8 * j)) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int e = 0; e < 4; ++e) {
+              const int n = 8 * j + 2 * e;
+              pk[e] = pack_bf16(gr * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
+                                gr * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
             }
+            *reinterpret_cast<uint4*>(Ost + sw128(r, 32 * hf + 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
       }
@@ -1136,8 +1121,8 @@ __global__ void __launch_bounds__(288, 1)
       }
     }
     if (tid == 0) bulk_wait0();
-    if (!*abort_flag && row64 && a.S_out) {
-      float* dst = a.S_out + ((size_t)bh * 64 + r64) * 64;
+    if (!*abort_flag && srow && a.S_out) {
+      float* dst = a.S_out + ((size_t)bh * 64 + r) * 64;
 #pragma unroll
       for (int n = 0; n < 64; n += 4)
         *reinterpret_cast<float4*>(dst + n) = make_float4(sreg[n], sreg[n + 1], sreg[n + 2], sreg[n + 3]);

@@ -180,6 +180,19 @@ __device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr) {
   return d;
 }
 
+// MN-major operand spanning several 64-element atoms along M (or N): the
+// leading byte offset is the stride between those atoms, the stride byte
+// offset the one between 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc_mn128_wide(uint32_t saddr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((atom_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor: bf16 x bf16 -> fp32; a_mn / b_mn select MN-major
 // (transposed) A / B operands, otherwise K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = false, bool b_mn = false) {

@@ -1,6 +1,6 @@
 """Tensor-core chunk path (tcgen05 / TMEM / TMA): parity with the oracle when
 forced, agreement with the portable path, and a white-box check of the
-per-chunk WY stage (the bf16 images of T diag(eta Gamma) and T diag(eta),
+per-chunk WY stage (the bf16 images of T diag(eta) and T diag(eta Gamma),
 T = (I + A)^{-1}, and the gates it leaves in the workspace)."""
 
 from __future__ import annotations
@@ -75,8 +75,8 @@ def test_wy_stage_workspace(F, d):
             img = wsn[t_off + ci * 16384: t_off + (ci + 1) * 16384]
             Tw_ref = Tref * (eta * np.exp(g))[None, :]
             Tu_ref = Tref * eta[None, :]
-            Tw = decode_T(img[:8192])
-            Tu = decode_T(img[8192:])
+            Tu = decode_T(img[:8192])
+            Tw = decode_T(img[8192:])
             assert np.abs(Tw - Tw_ref).max() <= 2e-2 * np.abs(Tw_ref).max(), (bh, c)
             assert np.abs(Tu - Tu_ref).max() <= 2e-2 * np.abs(Tu_ref).max(), (bh, c)
             gates = wsn[g_off + ci * 512: g_off + (ci + 1) * 512].view(np.float32)
