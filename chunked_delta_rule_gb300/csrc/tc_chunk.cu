@@ -767,46 +767,40 @@ __global__ void __launch_bounds__(256, 1)
 // ----------------------------------------------------------------------
 // (b') pipelined sequential kernel, d_k = d_v = 64.  Three roles:
 //   warp 8      producer: TMA of chunk c into one of three stages
-//   warps 4..7  front: the state-independent part of chunk c into a
-//               double-buffered slot
-//   warps 0..3  back: the state chain of chunk c
-// so the front of chunk c+1 overlaps the back of chunk c.  Products that
-// share an operand are stacked into one 128-row or 128-column MMA:
-//   front  P^T = X Q^T                                   (M 64,  N 64)
-//          [U  . ; .  W] = [T diag(eta) ; T diag(eta Gamma)] [V | X]   (M 128, N 128)
-//   back   [D1 ; Oa] = [W ; Q] S0                        (M 128, N 64)
-//          [D2 ; Ob] = [X~ | P~^T]^T-as-MN-major Delta   (M 128, N 64)
-// with Delta = U - D1 (Falcon-1A: diag(eta) V), X~ = diag(exp(g_last - g)) X,
-// P~ = (Q X^T) (.) [exp(g_r - g_i)]_{i<=r}, S1 = Gamma_last S0 + D2 and
-// O = diag(Gamma) Oa + Ob.  Hand-offs are mbarriers: full/empty per stage,
-// fdone/bdone per slot.
+//   warps 4..7  front: gates of chunk c, the products P^T = X Q^T and
+//               [U . ; . W] = [T diag(eta) ; T diag(eta Gamma)] [V | X],
+//               and the decay-masked P~^T rows
+//   warps 0..3  back: W rows and X~ = diag(exp(g_last - g)) X, then the
+//               state chain [D1 ; Oa] = [W ; Q] S0, Delta = U - D1,
+//               [D2 ; Ob] = [X~ | P~^T]^T Delta, S1 = Gamma_last S0 + D2,
+//               O = diag(Gamma) Oa + Ob
+// so the front of chunk c+1 overlaps the back of chunk c.  Every buffer of a
+// chunk lives in its stage, laid out so that the stacked operands are
+// adjacent: V | X (then X~) | P~^T | W | Q | T | gates, i.e. [V | X] and
+// [X~ | P~^T] are two-atom MN-major operands and [W ; Q] one 128-row K-major
+// operand.  Hand-offs are mbarriers: full/empty per stage, fdone/bdone per
+// TMEM slot.
 // ----------------------------------------------------------------------
 template <bool SOLVE>
 struct PipeSmem {
-  static constexpr int NST = 3;  // TMA stages
-  // stage: V | X (adjacent: [V | X] is one MN-major operand) | Q | T diag(eta), T diag(eta Gamma) | gates
-  static constexpr size_t VO = 0, XO = 8192, QO = 16384, TO = 24576;
-  static constexpr size_t TSZ = SOLVE ? 16384 : 0, GSZ = 512;
-  static constexpr size_t GO = TO + TSZ;
-  static constexpr size_t STAGE = GO + 1024;
-  static constexpr size_t SLOT0 = NST * STAGE;
-  // slot: A1 = [W ; Q] (K-major, 128 rows) | A2 = [X~ | P~^T] (MN-major, two atoms) |
-  //       Delta rows (additive write) | gates
-  static constexpr size_t S_A1 = 0, S_A2 = 16384, S_DLA = 32768;
-  static constexpr size_t S_GATE = S_DLA + (SOLVE ? 0 : 8192);
-  static constexpr size_t SLOT = S_GATE + 2048;
-  static constexpr size_t SB = SLOT0 + 2 * SLOT;          // S rows (MN-major B)
-  static constexpr size_t DL = SB + 8192;                 // Delta rows (MN-major B)
-  static constexpr size_t OST = DL + (SOLVE ? 8192 : 0);  // two output staging tiles
+  static constexpr int NST = 3;  // TMA stages (each also holds its chunk's buffers)
+  static constexpr size_t VO = 0, XO = 8192, PO = 16384, WO = 24576, QO = 32768, TO = 40960;
+  // T region: T diag(eta) | T diag(eta Gamma) (regression) or the Delta rows (additive)
+  static constexpr size_t TSZ = SOLVE ? 16384 : 8192, TLOAD = SOLVE ? 16384 : 0, GSZ = 512;
+  static constexpr size_t GO = TO + TSZ;            // gates from the WY kernel (eta, g)
+  static constexpr size_t DO = GO + 512;            // derived gates (gamma, dec, g, cf)
+  static constexpr size_t STAGE = (DO + 1024 + 1023) / 1024 * 1024;
+  static constexpr size_t SB = NST * STAGE;         // S rows (MN-major B)
+  static constexpr size_t DL = SB + 8192;           // Delta rows (MN-major B)
+  static constexpr size_t OST = DL + 8192;          // two output staging tiles
   static constexpr size_t BAR = OST + 2 * 8192;
   static constexpr size_t MISC = BAR + 128;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
   static_assert(TOTAL <= 232448, "shared memory budget");
-  static_assert(STAGE % 1024 == 0 && SLOT % 1024 == 0, "1 KB aligned tiles");
-  // TMEM: P^T (M=64 layout) | [U . ; . W] x 2 slots (M=128) | [D1 ; Oa] | [D2 ; Ob]
+  static_assert(STAGE % 1024 == 0, "1 KB aligned stages");
+  // TMEM: P^T (M=64 layout) | [U . ; . W] x 2 (M=128) | [D1 ; Oa] | [D2 ; Ob]
   static constexpr uint32_t COL_PT = 0, COL_UW = 64, COL_B1 = 320, COL_B2 = 384;
-  // gate arrays inside a slot (fp32 x 64 each)
-  static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192, G_ET = 256;
+  static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192;
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -840,9 +834,6 @@ __global__ void __launch_bounds__(288, 1)
   const int b = bh / a.H, h = bh % a.H;
   const int NC = a.NC;
   auto stage = [&](int s) { return sm + s * L::STAGE; };
-  auto Gst = [&](int s) { return reinterpret_cast<const float*>(stage(s) + L::GO); };
-  auto slot = [&](int p) { return sm + L::SLOT0 + p * L::SLOT; };
-  auto gates = [&](int p) { return reinterpret_cast<float*>(slot(p) + L::S_GATE); };
   auto fail = [&]() {
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
@@ -856,8 +847,8 @@ __global__ void __launch_bounds__(288, 1)
     fence_mbar_init();
   }
   if (!SOLVE) {  // additive write: the W rows of [W ; Q] stay zero
-    for (int i = tid; i < 2 * 512; i += 288)
-      *reinterpret_cast<uint4*>(slot(i >> 9) + L::S_A1 + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < NST * 512; i += 288)
+      *reinterpret_cast<uint4*>(stage(i >> 9) + L::WO + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, 512);
@@ -880,7 +871,7 @@ __global__ void __launch_bounds__(288, 1)
         if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1))) { fail(); break; }
         if (*abort_flag) break;
         uint8_t* st = stage(s);
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(3 * 8192 + L::TSZ + L::GSZ));
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(3 * 8192 + L::TLOAD + L::GSZ));
         tma_load_4d(st + L::VO, &tm_v, &full[s], 0, h, c * kC, b);
         tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - 1, b);
         tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
@@ -907,43 +898,49 @@ __global__ void __launch_bounds__(288, 1)
       uint8_t* st = stage(s);
       if (c == 0 && a.kprev_in && ftid < 64)  // x_0 = carried key
         *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = a.kprev_in[(size_t)bh * 64 + ftid];
-      float* gt = gates(p);
+      float* gt = reinterpret_cast<float*>(st + L::DO);
       if (ftid < 64) {
-        const float* G = Gst(s);
+        const float* G = reinterpret_cast<const float*>(st + L::GO);
         const float g = G[64 + ftid], glast = G[127];
         gt[L::G_GAM + ftid] = __expf(g);
         gt[L::G_DEC + ftid] = __expf(glast - g);
         gt[L::G_GL + ftid] = g;
         gt[L::G_CF + ftid] = __expf(g - G[64 + (ftid & ~15)]);  // decay from the 16-block start
-        gt[L::G_ET + ftid] = G[ftid];
       }
-      named_bar(1, 128);
-      if (*abort_flag) break;
-      uint8_t* sl = slot(p);
-      // X~ rows (atom 0 of A2), the Q rows of [W ; Q], additive Delta rows
-      scale_rows(sl + L::S_A2, st + L::XO, gt + L::G_DEC, ftid, 128);
-      for (int idx = ftid; idx < 512; idx += 128)
-        *reinterpret_cast<uint4*>(sl + L::S_A1 + 8192 + idx * 16) =
-            *reinterpret_cast<const uint4*>(st + L::QO + idx * 16);
-      if (!SOLVE) scale_rows(sl + L::S_DLA, st + L::VO, gt + L::G_ET, ftid, 128);
+      if (!SOLVE) {  // additive write: Delta = diag(eta) V rows in the stage's T region
+        const float* G = reinterpret_cast<const float*>(st + L::GO);
+        for (int idx = ftid; idx < 512; idx += 128) {
+          const uint4 in = *reinterpret_cast<const uint4*>(st + L::VO + idx * 16);
+          const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
+          const float fr = G[idx >> 3];
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(pin[e]);
+            pk[e] = pack_bf16(x.x * fr, x.y * fr);
+          }
+          *reinterpret_cast<uint4*>(st + L::TO + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
       fence_proxy_async();
       tc_fence_before();
       named_bar(1, 128);
       tc_fence_after();
+      if (*abort_flag) break;
       if (ftid == 0) {
         const uint32_t sV = smem_u32(st + L::VO), sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
-        // P^T = X Q^T
-        mma_chain_mn(tmem + L::COL_PT, kdesc<64>, sX, kdesc<64>, sQ, 64, idesc_bf16(64, 64), false);
-        umma_commit(&fmma[0]);
         if (SOLVE) {  // [T diag(eta) ; T diag(eta Gamma)] [V | X]
           const uint32_t sT = smem_u32(st + L::TO);
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16(tmem + L::COL_UW + 128 * p, kdesc<128>(sT, ks), sdesc_mn128_wide(sV + ks * 2048, 8192),
                       idesc_bf16(128, 128, false, true), ks > 0 ? 1u : 0u);
-          umma_commit(&fmma[1]);
         }
+        // P^T = X Q^T
+        mma_chain_mn(tmem + L::COL_PT, kdesc<64>, sX, kdesc<64>, sQ, 64, idesc_bf16(64, 64), false);
+        umma_commit(&fmma[0]);
       }
       if (!mbar_wait(&fmma[0], fph)) fail();
+      fph ^= 1;
       tc_fence_after();
       {  // P~^T rows: P[r][i] exp(g_r - g_i) for r >= i, the decay factored per 16-block of r
         float pv[64];
@@ -974,21 +971,9 @@ __global__ void __launch_bounds__(288, 1)
               for (int r = 16 * J; r < 16 * J + 16; ++r) pv[r] = 0.f;
             }
           }
-          store_row64(sl + L::S_A2 + 8192, i64, pv);
+          store_row64(st + L::PO, i64, pv);
         }
       }
-      if (SOLVE) {  // W rows (lanes 64..127 of the stacked product) -> rows 0..63 of [W ; Q]
-        if (!mbar_wait(&fmma[1], fph)) fail();
-        tc_fence_after();
-        if (quad >= 2) {
-          float wv[64];
-          tmem_ld64(tmem + lane_off + L::COL_UW + 128 * p + 64, wv);
-          tmem_wait_ld();
-          store_row64(sl + L::S_A1, 32 * (quad - 2) + lane, wv);
-        }
-      }
-      fph ^= 1;
-      if (ftid == 0) mbar_arrive(&empty[s]);  // the stage's tiles are no longer read
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&fdone[p]);
@@ -999,7 +984,7 @@ __global__ void __launch_bounds__(288, 1)
   } else {
     // ------------------------------------------------------------ back
     // warps 0, 1: S rows 32 w + lane (lanes 0..63 of the stacked products);
-    // warps 2, 3: output rows 32 (w - 2) + lane (lanes 64..127)
+    // warps 2, 3: W rows and output rows 32 (w - 2) + lane (lanes 64..127)
     uint8_t* SB = sm + L::SB;
     const uint32_t sS = smem_u32(SB);
     const bool srow = warp < 2;
@@ -1020,16 +1005,41 @@ __global__ void __launch_bounds__(288, 1)
     named_bar(2, 128);
     uint32_t bph = 0;
     for (int c = 0; c < NC; ++c) {
-      const int p = c & 1;
+      const int s = c % NST, p = c & 1;
       if (!mbar_wait(&fdone[p], (uint32_t)((c >> 1) & 1))) fail();
       tc_fence_after();
+      uint8_t* st = stage(s);
+      const float* gt = reinterpret_cast<const float*>(st + L::DO);
+      if (srow) {
+        // X~ rows in place of X (the front's products that read X are done)
+        for (int idx = tid; idx < 512; idx += 64) {
+          const int R = idx >> 3;
+          uint4* ptr = reinterpret_cast<uint4*>(st + L::XO + idx * 16);
+          const uint4 in = *ptr;
+          const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
+          const float fr = gt[L::G_DEC + R];
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(pin[e]);
+            pk[e] = pack_bf16(x.x * fr, x.y * fr);
+          }
+          *ptr = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      } else if (SOLVE) {  // W rows (lanes 64..127 of [U . ; . W], columns 64..127)
+        float wv[64];
+        tmem_ld64(tmem + lane_off + L::COL_UW + 128 * p + 64, wv);
+        tmem_wait_ld();
+        store_row64(st + L::WO, r, wv);
+      }
+      fence_proxy_async();
+      tc_fence_before();
       named_bar(2, 128);
+      tc_fence_after();
       if (*abort_flag) break;
-      uint8_t* sl = slot(p);
-      const float* gt = gates(p);
-      const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(sl + L::S_DLA);
+      const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(st + L::TO);
       if (tid == 0) {  // [D1 ; Oa] = [W ; Q] S0
-        const uint32_t sA1 = smem_u32(sl + L::S_A1);
+        const uint32_t sA1 = smem_u32(st + L::WO);
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tmem + L::COL_B1, kdesc<128>(sA1, ks), mndesc(sS, ks), idesc_bf16(128, 64, false, true),
                     ks > 0 ? 1u : 0u);
@@ -1065,7 +1075,7 @@ __global__ void __launch_bounds__(288, 1)
         tc_fence_after();
       }
       if (tid == 0) {  // [D2 ; Ob] = [X~ | P~^T] Delta, A MN-major over two atoms
-        const uint32_t sA2 = smem_u32(sl + L::S_A2);
+        const uint32_t sA2 = smem_u32(st + L::XO);
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tmem + L::COL_B2, sdesc_mn128_wide(sA2 + ks * 2048, 8192), mndesc(sDL, ks),
                     idesc_bf16(128, 64, true, true), ks > 0 ? 1u : 0u);
@@ -1077,6 +1087,7 @@ __global__ void __launch_bounds__(288, 1)
       if (!okb) fail();
       bph ^= 1;
       tc_fence_after();
+      if (tid == 0) mbar_arrive(&empty[s]);  // nothing reads this stage any more
       if (srow) {  // S1 = Gamma_last S0 + D2
         const float gl_ = gt[L::G_GAM + 63];
 #pragma unroll
