@@ -66,16 +66,22 @@ def algorithmic_bytes(w) -> int:
 
 
 def kernel_bytes(w, names) -> list:
-    """Algorithmic bytes each kernel of the path must move: the per-chunk WY
-    kernel reads the keys and the gate inputs; the sequential kernel reads
-    q, k, v, writes o and the final state.  Intermediates are not counted."""
+    """Algorithmic bytes each kernel of the path must move (the method's own
+    inputs and outputs that the kernel touches; intermediates are not
+    counted).  d = 64: the per-chunk kernel reads k, v and the gate inputs,
+    the sequential one q and k and writes o and the final state.  d = 128:
+    the per-chunk kernel reads k and the gate inputs, the sequential one q,
+    k, v and writes o and the final state."""
     es = 2 if w.dtype == "bf16" else 4
     th = w.B * w.T * w.H
     beta = th * (w.dv if w.per_channel else 1) * 4
     if names == ["generic_chunk_kernel"]:
         return [algorithmic_bytes(w)]
+    state = w.B * w.H * w.dk * w.dv * 4
+    if names[0] == "tc_wyu_kernel":
+        return [th * (w.dk + w.dv) * es + beta + th * 4, th * (2 * w.dk + w.dv) * es + state]
     wy = th * w.dk * es + beta + th * 4
-    fwd = th * (2 * w.dk + 2 * w.dv) * es + w.B * w.H * w.dk * w.dv * 4
+    fwd = th * (2 * w.dk + 2 * w.dv) * es + state
     return [wy, fwd]
 
 
@@ -402,8 +408,12 @@ def main():
             pass
         hbm_peak = peaks.get("hbm_gbs", 6800.0)
         abytes = algorithmic_bytes(w)
-        names = (["tc_wy_kernel", "tc_fwd_kernel"] if impl_used == F.FALCON_IMPL_TC
-                 else ["generic_chunk_kernel"])
+        if impl_used != F.FALCON_IMPL_TC:
+            names = ["generic_chunk_kernel"]
+        elif w.dk == 64:
+            names = ["tc_wyu_kernel", "tc_fwd_pipe_kernel"]
+        else:
+            names = ["tc_wy_kernel", "tc_fwd_kernel"]
         kbytes = kernel_bytes(w, names)
         dom = max(range(launches), key=lambda j: kern_ms[j])
         kernel = names[dom]

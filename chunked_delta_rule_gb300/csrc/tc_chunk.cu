@@ -10,21 +10,23 @@
 //   O       = diag(Gamma) Q S0 + (Q X^T (.) [exp(g_r - g_i)]_{i<=r}) Delta
 //   S1      = Gamma_last S0 + (diag(exp(g_last - g)) X)^T Delta
 //
-// Two kernels:
-//  (a) tc_wy_kernel — one CTA per pair of chunks, fully parallel: TMA loads
-//      the 128 shifted keys, one tcgen05 MMA forms the Gram matrix in TMEM,
+// Two kernels per call:
+//  (a) per-chunk kernel, fully parallel: TMA loads the shifted keys (and, for
+//      d = 64, the values), one tcgen05 MMA forms the Gram matrix in TMEM,
 //      the gates (clamped log-decay, its in-chunk prefix sum, NLMS step) are
 //      formed from lambda, beta and the Gram diagonal, and T = (I + A)^{-1}
 //      is found by blocked forward substitution: 16x16 diagonal blocks in
 //      registers, off-diagonal blocks merged with warp-level tf32 MMAs in
-//      shared memory.  T is written as bf16 in the exact image of a 128B-
-//      swizzled K-major shared-memory tile, plus eta and g per row.
-//  (b) tc_fwd_kernel — one CTA per (b, h, value slice), sequential over the
-//      chunks with the fp32 state held in registers: TMA brings q, shifted k,
-//      v (and T, gates by bulk copy) for chunk c+1 while chunk c computes;
-//      every contraction (P = Q X^T, [W|U], W S0, Q S0, X~^T Delta,
-//      P~ Delta) is a tcgen05 MMA with the accumulator in TMEM; the output
-//      tile leaves by TMA store.
+//      shared memory.  d = 64 (tc_wyu_kernel, one chunk per CTA): a second
+//      MMA forms [U ; W] = [T diag(eta) ; T diag(eta Gamma)] [V | X] and
+//      both leave as bf16 images of 128B-swizzled tiles.  d = 128
+//      (tc_wy_kernel, two chunks per CTA): T diag(eta) and T diag(eta Gamma)
+//      leave as such images.  Gates eta and g per row go along.
+//  (b) sequential kernel, one CTA per (b, h) (per value slice for d = 128),
+//      the fp32 state in registers: TMA and bulk copies bring the chunk's
+//      operands while earlier chunks compute; every contraction is a
+//      tcgen05 MMA with the accumulator in TMEM; the output tile leaves by
+//      TMA store.  d = 64 is warp-specialised (tc_fwd_pipe_kernel).
 // Every mbarrier wait is bounded; on timeout a kernel records an error in the
 // workspace status word and leaves its chunk loop.
 
@@ -58,7 +60,7 @@ struct TcArgs {
   float* S_out;
   __nv_bfloat16* kprev_out;
   int64_t* pos_out;
-  uint8_t* ws_T;      // [B*H*NC][16384]: bf16 swizzled images of T diag(eta), T diag(eta Gamma)
+  uint8_t* ws_T;      // [B*H*NC][16384]: bf16 swizzled images, d = 64: W | U; d = 128: T diag(eta) | T diag(eta Gamma)
   float* ws_g;        // [B*H*NC][128]: eta[64], g[64]
   uint32_t* status;   // workspace status word
 };
@@ -357,6 +359,336 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
     float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * 128;
     go[rl] = eta;
     go[64 + rl] = g;
+  }
+}
+
+// ======================================================================
+// (a') per-chunk WY products for the pipelined d = 64 path: one CTA per
+// chunk.  Besides the gates it leaves W = T diag(eta Gamma) X and
+// U = T diag(eta) V (Falcon-1) or U = diag(eta) V (Falcon-1A) in the
+// workspace as bf16 images of 128B-swizzled 64 x 64 tiles, so that the
+// sequential kernel needs no per-chunk products of its own beyond P.
+// ======================================================================
+struct WyuSmem {
+  static constexpr size_t VX = 0;                  // V tile | X tile: [V | X] as a two-atom MN-major B
+  static constexpr size_t TI = 16384;              // [T diag(eta) ; T diag(eta Gamma)], 128 K-major rows;
+                                                   // the solve's 16x16 scratch blocks before that
+  static constexpr size_t AT = TI + 16384;         // A, then T in place: [64][kLD] fp32
+  static constexpr size_t E = AT + 64 * kLD * 4;   // g, eta, column factors, Gamma, beta (64 each)
+  static constexpr size_t WS = E + 5 * 64 * 4;     // warp sums
+  static constexpr size_t BAR = WS + 16;           // 2 mbarriers
+  static constexpr size_t MISC = BAR + 16;         // tmem addr, abort flag
+  static constexpr size_t TOTAL = MISC + 16 + 1024;
+};
+
+template <bool SOLVE>
+__global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                     const __grid_constant__ CUtensorMap tm_v,
+                                                     TcArgs a) {
+  using L = WyuSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* Vs = sm + L::VX;
+  uint8_t* Xs = sm + L::VX + 8192;
+  uint8_t* TI = sm + L::TI;
+  float* T = reinterpret_cast<float*>(sm + L::AT);  // A, overwritten by T block by block
+  float* gs = reinterpret_cast<float*>(sm + L::E);
+  float* es = gs + 64;
+  float* cfs = gs + 128;
+  float* gms = gs + 192;
+  float* bs = gs + 256;
+  float* wsum = reinterpret_cast<float*>(sm + L::WS);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = blockIdx.x, bh = blockIdx.y;
+  const int b = bh / a.H, h = bh % a.H;
+  const int t0 = chunk * kC;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  if (SOLVE && warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar[0], 16384);
+    tma_load_4d(Vs, &tm_v, &bar[0], 0, h, t0, b);
+    tma_load_4d(Xs, &tm_k, &bar[0], 0, h, t0 - 1, b);
+  }
+  // gates while the tiles are in flight: row tid <-> step t0 + tid
+  {
+    const int t = t0 + tid;
+    const bool step_ok = tid < 64 && t < a.T;
+    const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+    const bool exists = step_ok && (pos + t >= 1);
+    const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
+    const float ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
+    float g = ell;  // inclusive prefix sum over the chunk
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, g, o);
+      if (lane >= o) g += n;
+    }
+    if (lane == 31) wsum[warp] = g;
+    const float beta = exists ? a.beta[gi] : 0.f;
+    __syncthreads();
+    if (warp == 1) g += wsum[0];
+    if (tid < 64) {
+      gs[tid] = g;
+      bs[tid] = beta;
+    }
+  }
+  if (!mbar_wait(&bar[0], 0)) {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  }
+  if (chunk == 0 && a.kprev_in && tid < 64)  // x_0 = carried key (row 0 of the first chunk)
+    *reinterpret_cast<__nv_bfloat16*>(Xs + sw128(0, tid)) = a.kprev_in[(size_t)bh * 64 + tid];
+  fence_proxy_async();
+  __syncthreads();
+  const bool aborted = *abort_flag != 0;
+  const size_t ci = (size_t)bh * a.NC + chunk;
+  uint8_t* Wo = a.ws_T + ci * 16384;  // W image, then the U image 8 KB further
+  float* go = a.ws_g + ci * 128;
+  const uint32_t tmem = SOLVE ? *tmem_slot : 0u;
+  if (SOLVE && !aborted && tid == 0) {  // Gram matrix X X^T (M = 64: row r in lane 32 (r / 16) + r % 16)
+    tc_fence_after();
+    mma_chain(tmem, Xs, 64, Xs, 64, 64, idesc_bf16(64, 64), false);
+    umma_commit(&bar[1]);
+  }
+  // NLMS step from the key energy, and the decay factors of each row
+  if (tid < 64) {
+    float n = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(Xs + sw128(tid, 8 * j));
+      const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(px[e]);
+        n = fmaf(x.x, x.x, n);
+        n = fmaf(x.y, x.y, n);
+      }
+    }
+    const float eta = bs[tid] != 0.f ? bs[tid] / (a.eps + n) : 0.f;
+    const float g = gs[tid];
+    es[tid] = eta;
+    cfs[tid] = __expf(gs[tid | 15] - g);  // exp(g_end(J) - g_r), J the row's 16-block
+    gms[tid] = __expf(g);
+    if (!SOLVE && !aborted) {
+      go[tid] = eta;
+      go[64 + tid] = g;
+    }
+  }
+  __syncthreads();
+
+  if (!SOLVE) {  // additive write: U = diag(eta) V
+    if (!aborted) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int idx = tid + 128 * k;
+        const uint4 in = *reinterpret_cast<const uint4*>(Vs + idx * 16);
+        const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
+        const float fr = es[idx >> 3];
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(pin[e]);
+          pk[e] = pack_bf16(x.x * fr, x.y * fr);
+        }
+        *reinterpret_cast<uint4*>(Wo + 8192 + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    return;
+  }
+
+  if (!aborted && !mbar_wait(&bar[1], 0)) {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  }
+  tc_fence_after();
+  const bool rowlane = lane < 16;
+  const int rl = 16 * warp + (lane & 15);  // this lane's Gram row (lanes 0..15)
+  float grow[64];
+  tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16), grow);
+  tmem_wait_ld();
+  tc_fence_before();
+  if (rowlane) {  // A_ri = eta_r exp(g_r - g_i) G_ri (i < r), the decay factored per 16-block
+    const float eta = es[rl], g = gs[rl], cfr = cfs[rl];
+    const bool ratio_ok = cfr > 1e-30f;  // inside the row's block exp(g_r - g_i) = cf_i / cf_r
+    const float inv = ratio_ok ? __fdividef(eta, cfr) : 0.f;
+    float* Arow = T + rl * kLD;
+    const int I = rl >> 4;
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+      float av[16];
+      if (J < I) {
+        const float rf = eta * __expf(g - gs[16 * J + 15]);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(cfs + 16 * J + i);
+          av[i] = rf * c4.x * grow[16 * J + i];
+          av[i + 1] = rf * c4.y * grow[16 * J + i + 1];
+          av[i + 2] = rf * c4.z * grow[16 * J + i + 2];
+          av[i + 3] = rf * c4.w * grow[16 * J + i + 3];
+        }
+      } else if (J == I) {
+        if (ratio_ok) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(cfs + 16 * J + i);
+            const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              av[i + e] = (16 * J + i + e < rl) ? inv * cc[e] * grow[16 * J + i + e] : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            av[i] = (16 * J + i < rl) ? eta * __expf(g - gs[16 * J + i]) * grow[16 * J + i] : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) av[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(Arow + 16 * J + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
+    }
+  }
+  __syncthreads();
+
+  // ---- T = (I + A)^{-1} in place; the 16x16 scratch blocks live in the
+  // (not yet written) T image region
+  float* Ysc = reinterpret_cast<float*>(TI);             // [2 warps][16 * kYL]
+  float* Yc = reinterpret_cast<float*>(TI + 4096);       // [I-2][J] blocks, 4 x 16 * kYL
+  const int w2 = warp & 1;
+  if (warp < 2) {  // 16x16 diagonal blocks, one column per lane, forward substitution
+    const int I = 2 * w2 + (lane >> 4), l = lane & 15;
+    float tv[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float s = (r == l) ? 1.f : 0.f;
+#pragma unroll
+      for (int i = 0; i < r; ++i) s -= T[(16 * I + r) * kLD + 16 * I + i] * tv[i];
+      tv[r] = s;
+    }
+    __syncwarp();  // every lane of the block has read its A rows
+#pragma unroll
+    for (int r = 0; r < 16; ++r) T[(16 * I + r) * kLD + 16 * I + l] = tv[r];
+  }
+  __syncthreads();
+  if (warp < 2) {  // T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (A_IJ replaced by T_IJ)
+    const int I = w2 == 0 ? 1 : 3, J = I - 1;
+    float acc[2][4] = {};
+    warp_mm16(acc, T + 16 * I * kLD + 16 * J, kLD, T + 16 * J * kLD + 16 * J, kLD, lane);
+    float* ys = Ysc + warp * 16 * kYL;
+    warp_store16(ys, kYL, acc, 1.f, lane);
+    __syncwarp();
+    float acc2[2][4] = {};
+    warp_mm16(acc2, T + 16 * I * kLD + 16 * I, kLD, ys, kYL, lane);
+    warp_store16(T + 16 * I * kLD + 16 * J, kLD, acc2, -1.f, lane);
+  }
+  __syncthreads();
+  {  // Y = A[32:64, 0:32] T[0:32, 0:32]: block (I, J) = (2 + warp / 2, warp % 2)
+    const int I = 2 + (warp >> 1), J = warp & 1;
+    float acc[2][4] = {};
+    if (J == 0) {
+      warp_mm16(acc, T + 16 * I * kLD, kLD, T, kLD, lane);
+      warp_mm16(acc, T + 16 * I * kLD + 16, kLD, T + 16 * kLD, kLD, lane);
+    } else {
+      warp_mm16(acc, T + 16 * I * kLD + 16, kLD, T + 16 * kLD + 16, kLD, lane);
+    }
+    warp_store16(Yc + (2 * (I - 2) + J) * 16 * kYL, kYL, acc, 1.f, lane);
+  }
+  __syncthreads();
+  {  // T[I][J] = -sum_{K=2..I} T[I][K] Y[K-2][J], block (I, J) = (2 + warp / 2, warp % 2)
+    const int I = 2 + (warp >> 1), J = warp & 1;
+    float acc[2][4] = {};
+    for (int K = 2; K <= I; ++K)
+      warp_mm16(acc, T + 16 * I * kLD + 16 * K, kLD, Yc + (2 * (K - 2) + J) * 16 * kYL, kYL, lane);
+    warp_store16(T + 16 * I * kLD + 16 * J, kLD, acc, -1.f, lane);
+  }
+  __syncthreads();
+  // ---- [T diag(eta) ; T diag(eta Gamma)] as one 128-row K-major bf16 operand
+  {
+    const int j = tid & 7;  // this thread's 8 columns are the same in every pass
+    float eu[8], ew[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      eu[e] = es[8 * j + e];
+      ew[e] = eu[e] * gms[8 * j + e];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int R = (tid >> 3) + 16 * k;
+      const float4 lo4 = *reinterpret_cast<const float4*>(T + R * kLD + 8 * j);
+      const float4 hi4 = *reinterpret_cast<const float4*>(T + R * kLD + 8 * j + 4);
+      const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+      uint32_t pw[4], pu[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c0 = 8 * j + 2 * e;
+        const float q0 = (c0 <= R) ? v[2 * e] : 0.f, q1 = (c0 + 1 <= R) ? v[2 * e + 1] : 0.f;
+        pu[e] = pack_bf16(q0 * eu[2 * e], q1 * eu[2 * e + 1]);
+        pw[e] = pack_bf16(q0 * ew[2 * e], q1 * ew[2 * e + 1]);
+      }
+      const int off = R * 128 + 16 * (j ^ (R & 7));
+      *reinterpret_cast<uint4*>(TI + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+      *reinterpret_cast<uint4*>(TI + 8192 + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  if (!aborted && tid == 0) {  // [U . ; . W] = [T diag(eta) ; T diag(eta Gamma)] [V | X]
+    tc_fence_after();
+    const uint32_t sT = smem_u32(TI), sV = smem_u32(Vs);
+    for (int ks = 0; ks < 4; ++ks)
+      umma_bf16(tmem, sdesc_k128(sT + ks * 32), sdesc_mn128_wide(sV + ks * 2048, 8192),
+                idesc_bf16(128, 128, false, true), ks > 0 ? 1u : 0u);
+    umma_commit(&bar[1]);
+  }
+  if (!aborted && !mbar_wait(&bar[1], 1)) {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  }
+  tc_fence_after();
+  {  // rows 0..63: U (columns 0..63); rows 64..127: W (columns 64..127)
+    float rv[64];
+    tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + (warp < 2 ? 0 : 64), rv);
+    tmem_wait_ld();
+    if (!*abort_flag) {
+      const int r = (32 * warp + lane) & 63;
+      uint8_t* dst = warp < 2 ? Wo + 8192 : Wo;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(rv[8 * j + 2 * e], rv[8 * j + 2 * e + 1]);
+        *reinterpret_cast<uint4*>(dst + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      if (tid < 64) {
+        go[tid] = es[tid];
+        go[64 + tid] = gs[tid];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
   }
 }
 
@@ -765,29 +1097,24 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 // ----------------------------------------------------------------------
-// (b') pipelined sequential kernel, d_k = d_v = 64.  Three roles:
-//   warp 8      producer: TMA of chunk c into one of three stages
-//   warps 4..7  front: gates of chunk c, the products P^T = X Q^T and
-//               [U . ; . W] = [T diag(eta) ; T diag(eta Gamma)] [V | X],
-//               and the decay-masked P~^T rows
-//   warps 0..3  back: W rows and X~ = diag(exp(g_last - g)) X, then the
-//               state chain [D1 ; Oa] = [W ; Q] S0, Delta = U - D1,
-//               [D2 ; Ob] = [X~ | P~^T]^T Delta, S1 = Gamma_last S0 + D2,
-//               O = diag(Gamma) Oa + Ob
-// so the front of chunk c+1 overlaps the back of chunk c.  Every buffer of a
-// chunk lives in its stage, laid out so that the stacked operands are
-// adjacent: V | X (then X~) | P~^T | W | Q | T | gates, i.e. [V | X] and
-// [X~ | P~^T] are two-atom MN-major operands and [W ; Q] one 128-row K-major
-// operand.  Hand-offs are mbarriers: full/empty per stage, fdone/bdone per
-// TMEM slot.
+// (b') pipelined sequential kernel, d_k = d_v = 64.  W, U and the gates of
+// every chunk come from the per-chunk kernel; three roles:
+//   warp 8      producer: TMA of chunk c into one of NST stages
+//   warps 4..7  front: derived gates, P^T = [X ; X] Q^T (one 128-row product,
+//               each half of it read by two warps) -> decay-masked P~^T, and
+//               X~ = diag(exp(g_last - g)) X in place of X
+//   warps 0..3  back: the state chain [D1 ; Oa] = [W ; Q] S0,
+//               Delta = U - D1, [D2 ; Ob] = [X~ | P~^T]^T Delta,
+//               S1 = Gamma_last S0 + D2, O = diag(Gamma) Oa + Ob
+// The front works up to NST chunks ahead of the back.  Stage layout: X (then
+// X~) | X copy (then P~^T) | W | Q | U | gates, so that [X ; X], [W ; Q]
+// and [X~ | P~^T] are single operands.  Hand-offs are mbarriers: full/empty
+// and front-done per stage, MMA completions per role.
 // ----------------------------------------------------------------------
 template <bool SOLVE>
 struct PipeSmem {
-  static constexpr int NST = 3;  // TMA stages (each also holds its chunk's buffers)
-  static constexpr size_t VO = 0, XO = 8192, PO = 16384, WO = 24576, QO = 32768, TO = 40960;
-  // T region: T diag(eta) | T diag(eta Gamma) (regression) or the Delta rows (additive)
-  static constexpr size_t TSZ = SOLVE ? 16384 : 8192, TLOAD = SOLVE ? 16384 : 0, GSZ = 512;
-  static constexpr size_t GO = TO + TSZ;            // gates from the WY kernel (eta, g)
+  static constexpr int NST = 4;
+  static constexpr size_t XO = 0, PO = 8192, WO = 16384, QO = 24576, UO = 32768, GO = 40960;
   static constexpr size_t DO = GO + 512;            // derived gates (gamma, dec, g, cf)
   static constexpr size_t STAGE = (DO + 1024 + 1023) / 1024 * 1024;
   static constexpr size_t SB = NST * STAGE;         // S rows (MN-major B)
@@ -796,10 +1123,11 @@ struct PipeSmem {
   static constexpr size_t BAR = OST + 2 * 8192;
   static constexpr size_t MISC = BAR + 128;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
+  static constexpr uint32_t TX = 3 * 8192 + (SOLVE ? 8192 : 0) + 8192 + 512;
   static_assert(TOTAL <= 232448, "shared memory budget");
   static_assert(STAGE % 1024 == 0, "1 KB aligned stages");
-  // TMEM: P^T (M=64 layout) | [U . ; . W] x 2 (M=128) | [D1 ; Oa] | [D2 ; Ob]
-  static constexpr uint32_t COL_PT = 0, COL_UW = 64, COL_B1 = 320, COL_B2 = 384;
+  // TMEM: P^T (M = 128 layout) | [D1 ; Oa] | [D2 ; Ob]
+  static constexpr uint32_t COL_PT = 0, COL_B1 = 64, COL_B2 = 128, NCOLS = 256;
   static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192;
 };
 
@@ -813,19 +1141,17 @@ __device__ __forceinline__ void bulk_wait_read1() {
 template <bool SOLVE>
 __global__ void __launch_bounds__(288, 1)
     tc_fwd_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                       TcArgs a) {
+                       const __grid_constant__ CUtensorMap tm_o, TcArgs a) {
   using L = PipeSmem<SOLVE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   constexpr int NST = L::NST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  uint64_t* full = bars;        // [NST]
-  uint64_t* empty = bars + 3;   // [NST]
-  uint64_t* fdone = bars + 6;   // [2]
-  uint64_t* bdone = bars + 8;   // [2]
-  uint64_t* fmma = bars + 10;   // [2]: P^T done, [U ; W] done
-  uint64_t* bmma = bars + 12;   // [2]: [D1 ; Oa] done, [D2 ; Ob] done
+  uint64_t* full = bars;              // [NST]
+  uint64_t* empty = bars + NST;       // [NST]
+  uint64_t* fdone = bars + 2 * NST;   // [NST]
+  uint64_t* fmma = bars + 3 * NST;    // P^T done
+  uint64_t* bmma = fmma + 1;          // [2]: [D1 ; Oa] done, [D2 ; Ob] done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -841,9 +1167,14 @@ __global__ void __launch_bounds__(288, 1)
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&fdone[i], 128); mbar_init(&bdone[i], 128); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&fmma[i], 1); mbar_init(&bmma[i], 1); }
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&fdone[i], 128);
+    }
+    mbar_init(fmma, 1);
+    mbar_init(&bmma[0], 1);
+    mbar_init(&bmma[1], 1);
     fence_mbar_init();
   }
   if (!SOLVE) {  // additive write: the W rows of [W ; Q] stay zero
@@ -851,7 +1182,7 @@ __global__ void __launch_bounds__(288, 1)
       *reinterpret_cast<uint4*>(stage(i >> 9) + L::WO + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, L::NCOLS);
     tmem_relinquish();
     tc_fence_before();
   }
@@ -871,12 +1202,13 @@ __global__ void __launch_bounds__(288, 1)
         if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1))) { fail(); break; }
         if (*abort_flag) break;
         uint8_t* st = stage(s);
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(3 * 8192 + L::TLOAD + L::GSZ));
-        tma_load_4d(st + L::VO, &tm_v, &full[s], 0, h, c * kC, b);
-        tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - 1, b);
-        tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
         const size_t ci = (size_t)bh * NC + c;
-        if (SOLVE) bulk_load(st + L::TO, a.ws_T + ci * 16384, 16384, &full[s]);
+        mbar_arrive_expect_tx(&full[s], L::TX);
+        tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - 1, b);
+        tma_load_4d(st + L::PO, &tm_k, &full[s], 0, h, c * kC - 1, b);
+        tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
+        if (SOLVE) bulk_load(st + L::WO, a.ws_T + ci * 16384, 8192, &full[s]);
+        bulk_load(st + L::UO, a.ws_T + ci * 16384 + 8192, 8192, &full[s]);
         bulk_load(st + L::GO, a.ws_g + ci * 128, 512, &full[s]);
       }
       if (*abort_flag) {  // drain the loads still in flight
@@ -887,17 +1219,18 @@ __global__ void __launch_bounds__(288, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ front
     const int ftid = tid - 128;
-    const bool row64 = lane < 16;
-    const int i64 = 16 * quad + lane;  // P^T row (key index) in the M = 64 layout
+    const int r = (32 * quad + lane) & 63;  // P^T row (key index) of this lane
+    const int half = quad >> 1;             // P^T columns 32 half .. 32 half + 31
     uint32_t fph = 0;
     for (int c = 0; c < NC; ++c) {
-      const int s = c % NST, p = c & 1;
-      bool ok = mbar_wait(&full[s], (uint32_t)((c / NST) & 1));
-      if (c >= 2) ok = ok && mbar_wait(&bdone[p], (uint32_t)(((c - 2) >> 1) & 1));
-      if (!ok) fail();
+      const int s = c % NST;
+      if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
       uint8_t* st = stage(s);
-      if (c == 0 && a.kprev_in && ftid < 64)  // x_0 = carried key
-        *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = a.kprev_in[(size_t)bh * 64 + ftid];
+      if (c == 0 && a.kprev_in && ftid < 64) {  // x_0 = carried key, in both copies of X
+        const __nv_bfloat16 kv = a.kprev_in[(size_t)bh * 64 + ftid];
+        *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = kv;
+        *reinterpret_cast<__nv_bfloat16*>(st + L::PO + sw128(0, ftid)) = kv;
+      }
       float* gt = reinterpret_cast<float*>(st + L::DO);
       if (ftid < 64) {
         const float* G = reinterpret_cast<const float*>(st + L::GO);
@@ -907,76 +1240,92 @@ __global__ void __launch_bounds__(288, 1)
         gt[L::G_GL + ftid] = g;
         gt[L::G_CF + ftid] = __expf(g - G[64 + (ftid & ~15)]);  // decay from the 16-block start
       }
-      if (!SOLVE) {  // additive write: Delta = diag(eta) V rows in the stage's T region
-        const float* G = reinterpret_cast<const float*>(st + L::GO);
-        for (int idx = ftid; idx < 512; idx += 128) {
-          const uint4 in = *reinterpret_cast<const uint4*>(st + L::VO + idx * 16);
-          const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-          const float fr = G[idx >> 3];
+      fence_proxy_async();
+      tc_fence_before();
+      named_bar(1, 128);
+      tc_fence_after();
+      if (*abort_flag) break;
+      if (ftid == 0) {  // P^T = [X ; X] Q^T
+        const uint32_t sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + L::COL_PT, kdesc<128>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(128, 64),
+                    ks > 0 ? 1u : 0u);
+        umma_commit(fmma);
+      }
+      if (!mbar_wait(fmma, fph)) fail();
+      fph ^= 1;
+      tc_fence_after();
+      {  // P~^T[r][t] = P[t][r] exp(g_t - g_r) for t >= r.  With cf_t = exp(g_t - g_{16 J(t)}):
+         // exp(g_t - g_r) = cf_t exp(g_{16 J} - g_r) across blocks and cf_t / cf_r inside one
+        uint32_t pr[32];
+        tmem_ld32(tmem + lane_off + L::COL_PT + 32 * half, pr);
+        const float* gl = gt + L::G_GL;
+        const float* cf = gt + L::G_CF;
+        const float gi = gl[r], cfr = cf[r];
+        const int I = r >> 4;
+        const bool ratio_ok = cfr > 1e-30f;
+        float cfv[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(cf + 32 * half + i);
+          cfv[i] = c4.x; cfv[i + 1] = c4.y; cfv[i + 2] = c4.z; cfv[i + 3] = c4.w;
+        }
+        float f[2];
+#pragma unroll
+        for (int J2 = 0; J2 < 2; ++J2) {
+          const int J = 2 * half + J2;
+          f[J2] = J > I ? __expf(gl[16 * J] - gi) : (J == I && ratio_ok ? __fdividef(1.f, cfr) : 0.f);
+        }
+        tmem_wait_ld();
+        float pv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int t = 32 * half + i;
+          const float v = __uint_as_float(pr[i]) * cfv[i] * f[i >> 4];
+          pv[i] = (t >= r) ? v : 0.f;
+        }
+        if (!ratio_ok) {  // exact decays in the row's own block
+#pragma unroll
+          for (int J2 = 0; J2 < 2; ++J2) {
+            if (2 * half + J2 == I) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int t = 16 * I + i;
+                pv[16 * J2 + i] = (t >= r) ? __expf(gl[t] - gi) * __uint_as_float(pr[16 * J2 + i]) : 0.f;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(pv[8 * j + 2 * e], pv[8 * j + 2 * e + 1]);
+          *reinterpret_cast<uint4*>(st + L::PO + sw128(r, 32 * half + 8 * j)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      {  // X~ rows in place of X (the product that read X is complete)
+        uint4 in[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) in[k] = *reinterpret_cast<const uint4*>(st + L::XO + (ftid + 128 * k) * 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int idx = ftid + 128 * k;
+          const float fr = gt[L::G_DEC + (idx >> 3)];
+          const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in[k]);
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 x = __bfloat1622float2(pin[e]);
             pk[e] = pack_bf16(x.x * fr, x.y * fr);
           }
-          *reinterpret_cast<uint4*>(st + L::TO + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(st + L::XO + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
       fence_proxy_async();
       tc_fence_before();
-      named_bar(1, 128);
-      tc_fence_after();
-      if (*abort_flag) break;
-      if (ftid == 0) {
-        const uint32_t sV = smem_u32(st + L::VO), sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
-        if (SOLVE) {  // [T diag(eta) ; T diag(eta Gamma)] [V | X]
-          const uint32_t sT = smem_u32(st + L::TO);
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + L::COL_UW + 128 * p, kdesc<128>(sT, ks), sdesc_mn128_wide(sV + ks * 2048, 8192),
-                      idesc_bf16(128, 128, false, true), ks > 0 ? 1u : 0u);
-        }
-        // P^T = X Q^T
-        mma_chain_mn(tmem + L::COL_PT, kdesc<64>, sX, kdesc<64>, sQ, 64, idesc_bf16(64, 64), false);
-        umma_commit(&fmma[0]);
-      }
-      if (!mbar_wait(&fmma[0], fph)) fail();
-      fph ^= 1;
-      tc_fence_after();
-      {  // P~^T rows: P[r][i] exp(g_r - g_i) for r >= i, the decay factored per 16-block of r
-        float pv[64];
-        tmem_ld64(tmem + lane_off + L::COL_PT, pv);
-        tmem_wait_ld();
-        if (row64) {
-          const float* gl = gt + L::G_GL;
-          const float* cf = gt + L::G_CF;
-          const float gi = gl[i64];
-#pragma unroll
-          for (int J = 0; J < 4; ++J) {
-            if (J > quad) {
-              const float f = __expf(gl[16 * J] - gi);
-#pragma unroll
-              for (int r = 16 * J; r < 16 * J + 16; r += 4) {
-                const float4 c4 = *reinterpret_cast<const float4*>(cf + r);
-                pv[r] *= f * c4.x;
-                pv[r + 1] *= f * c4.y;
-                pv[r + 2] *= f * c4.z;
-                pv[r + 3] *= f * c4.w;
-              }
-            } else if (J == quad) {
-#pragma unroll
-              for (int r = 16 * J; r < 16 * J + 16; ++r)
-                pv[r] = (r >= i64) ? __expf(gl[r] - gi) * pv[r] : 0.f;
-            } else {
-#pragma unroll
-              for (int r = 16 * J; r < 16 * J + 16; ++r) pv[r] = 0.f;
-            }
-          }
-          store_row64(st + L::PO, i64, pv);
-        }
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(&fdone[p]);
+      mbar_arrive(&fdone[s]);
     }
     if (a.kprev_out && !*abort_flag && ftid < 64)
       a.kprev_out[(size_t)bh * 64 + ftid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + ftid];
@@ -984,7 +1333,7 @@ __global__ void __launch_bounds__(288, 1)
   } else {
     // ------------------------------------------------------------ back
     // warps 0, 1: S rows 32 w + lane (lanes 0..63 of the stacked products);
-    // warps 2, 3: W rows and output rows 32 (w - 2) + lane (lanes 64..127)
+    // warps 2, 3: output rows 32 (w - 2) + lane (lanes 64..127)
     uint8_t* SB = sm + L::SB;
     const uint32_t sS = smem_u32(SB);
     const bool srow = warp < 2;
@@ -1005,39 +1354,14 @@ __global__ void __launch_bounds__(288, 1)
     named_bar(2, 128);
     uint32_t bph = 0;
     for (int c = 0; c < NC; ++c) {
-      const int s = c % NST, p = c & 1;
-      if (!mbar_wait(&fdone[p], (uint32_t)((c >> 1) & 1))) fail();
+      const int s = c % NST;
+      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1))) fail();
       tc_fence_after();
       uint8_t* st = stage(s);
-      const float* gt = reinterpret_cast<const float*>(st + L::DO);
-      if (srow) {
-        // X~ rows in place of X (the front's products that read X are done)
-        for (int idx = tid; idx < 512; idx += 64) {
-          const int R = idx >> 3;
-          uint4* ptr = reinterpret_cast<uint4*>(st + L::XO + idx * 16);
-          const uint4 in = *ptr;
-          const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-          const float fr = gt[L::G_DEC + R];
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 x = __bfloat1622float2(pin[e]);
-            pk[e] = pack_bf16(x.x * fr, x.y * fr);
-          }
-          *ptr = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-      } else if (SOLVE) {  // W rows (lanes 64..127 of [U . ; . W], columns 64..127)
-        float wv[64];
-        tmem_ld64(tmem + lane_off + L::COL_UW + 128 * p + 64, wv);
-        tmem_wait_ld();
-        store_row64(st + L::WO, r, wv);
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      named_bar(2, 128);
-      tc_fence_after();
       if (*abort_flag) break;
-      const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(st + L::TO);
+      const float* gt = reinterpret_cast<const float*>(st + L::DO);
+      // the stage is handed back before the epilogues: keep their gates
+      const float gfac = srow ? gt[L::G_GAM + 63] : gt[L::G_GAM + r];
       if (tid == 0) {  // [D1 ; Oa] = [W ; Q] S0
         const uint32_t sA1 = smem_u32(st + L::WO);
         for (int ks = 0; ks < 4; ++ks)
@@ -1045,24 +1369,31 @@ __global__ void __launch_bounds__(288, 1)
                     ks > 0 ? 1u : 0u);
         umma_commit(&bmma[0]);
       }
-      if (SOLVE) {  // Delta = U - W S0 (rows 0..63: warps 0, 1)
+      // Delta = U - W S0 (rows 0..63: warps 0, 1); the additive write has W = 0
+      // and feeds U to the second product directly
+      const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(st + L::UO);
+      if (SOLVE) {
         if (!mbar_wait(&bmma[0], bph)) fail();
         tc_fence_after();
         if (srow) {
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            uint32_t d1[32], uu[32];
+            uint32_t d1[32];
             tmem_ld32(tmem + lane_off + L::COL_B1 + 32 * hf, d1);
-            tmem_ld32(tmem + lane_off + L::COL_UW + 128 * p + 32 * hf, uu);
+            uint4 uu[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              uu[j] = *reinterpret_cast<const uint4*>(st + L::UO + sw128(r, 32 * hf + 8 * j));
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+              const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&uu[j]);
               uint32_t pd[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int n = 8 * j + 2 * e;
-                pd[e] = pack_bf16(__uint_as_float(uu[n]) - __uint_as_float(d1[n]),
-                                  __uint_as_float(uu[n + 1]) - __uint_as_float(d1[n + 1]));
+                const float2 u2 = __bfloat1622float2(pu[e]);
+                pd[e] = pack_bf16(u2.x - __uint_as_float(d1[n]), u2.y - __uint_as_float(d1[n + 1]));
               }
               *reinterpret_cast<uint4*>(sm + L::DL + sw128(r, 32 * hf + 8 * j)) =
                   make_uint4(pd[0], pd[1], pd[2], pd[3]);
@@ -1089,18 +1420,16 @@ __global__ void __launch_bounds__(288, 1)
       tc_fence_after();
       if (tid == 0) mbar_arrive(&empty[s]);  // nothing reads this stage any more
       if (srow) {  // S1 = Gamma_last S0 + D2
-        const float gl_ = gt[L::G_GAM + 63];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t d2[32];
           tmem_ld32(tmem + lane_off + L::COL_B2 + 32 * hf, d2);
           tmem_wait_ld();
 #pragma unroll
-          for (int n = 0; n < 32; ++n) sreg[32 * hf + n] = gl_ * sreg[32 * hf + n] + __uint_as_float(d2[n]);
+          for (int n = 0; n < 32; ++n) sreg[32 * hf + n] = gfac * sreg[32 * hf + n] + __uint_as_float(d2[n]);
         }
         store_row64(SB, r, sreg);
       } else {  // O = diag(Gamma) Oa + Ob
-        const float gr = gt[L::G_GAM + r];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t oa[32], ob[32];
@@ -1113,8 +1442,8 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int n = 8 * j + 2 * e;
-              pk[e] = pack_bf16(gr * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
-                                gr * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
+              pk[e] = pack_bf16(gfac * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
+                                gfac * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
             }
             *reinterpret_cast<uint4*>(Ost + sw128(r, 32 * hf + 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
@@ -1124,7 +1453,6 @@ __global__ void __launch_bounds__(288, 1)
       tc_fence_before();
       named_bar(2, 128);
       tc_fence_after();
-      mbar_arrive(&bdone[p]);
       if (tid == 0) {
         tma_store_4d(&tm_o, Ost, 0, h, c * kC, b);
         bulk_commit();
@@ -1143,7 +1471,7 @@ __global__ void __launch_bounds__(288, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, L::NCOLS);
   }
 }
 
@@ -1177,7 +1505,7 @@ bool make_map(CUtensorMap* m, const void* base, int B, int T, int H, int D, int 
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct WsLayout {
@@ -1196,37 +1524,51 @@ WsLayout ws_layout(int B, int T, int H, int chunk) {
 template <int DK, int NV, bool SOLVE>
 int launch_t(const FwdArgs& fa, const TcArgs& ta) {
   const int BH = fa.B * fa.H;
-  const int nsplit = fa.dv / NV;
-  CUtensorMap mq, mk, mk128, mv, mo;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, fa.q, fa.B, fa.T, fa.H, DK, 64) || !make_map(&mk, fa.k, fa.B, fa.T, fa.H, DK, 64) ||
-      !make_map(&mk128, fa.k, fa.B, fa.T, fa.H, DK, 128) ||
       !make_map(&mv, fa.v, fa.B, fa.T, fa.H, fa.dv, 64) || !make_map(&mo, fa.o, fa.B, fa.T, fa.H, fa.dv, 64))
     return FALCON_ERR_CUDA;
-  {
-    auto k = tc_wy_kernel<DK, SOLVE>;
-    const size_t smem = WySmem<DK>::TOTAL;
-    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
-      return FALCON_ERR_CUDA;
-    dim3 grid((ta.NC + 1) / 2, BH);
-    record_event(fa, 0);
-    k<<<grid, 128, smem, fa.stream>>>(mk128, ta);
-    record_event(fa, 1);
-  }
-  if (DK == 64) {  // pipelined: producer warp, front and back warpgroups
-    auto k = tc_fwd_pipe_kernel<SOLVE>;
-    const size_t smem = PipeSmem<SOLVE>::TOTAL;
-    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
-      return FALCON_ERR_CUDA;
-    k<<<BH, 288, smem, fa.stream>>>(mq, mk, mv, mo, ta);
-    record_event(fa, 2);
+  if constexpr (DK == 64) {
+    {  // per-chunk gates, W and U
+      auto k = tc_wyu_kernel<SOLVE>;
+      const size_t smem = WyuSmem::TOTAL;
+      if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
+        return FALCON_ERR_CUDA;
+      dim3 grid(ta.NC, BH);
+      record_event(fa, 0);
+      k<<<grid, 128, smem, fa.stream>>>(mk, mv, ta);
+      record_event(fa, 1);
+    }
+    {  // pipelined: producer warp, front and back warpgroups
+      auto k = tc_fwd_pipe_kernel<SOLVE>;
+      const size_t smem = PipeSmem<SOLVE>::TOTAL;
+      if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
+        return FALCON_ERR_CUDA;
+      k<<<BH, 288, smem, fa.stream>>>(mq, mk, mo, ta);
+      record_event(fa, 2);
+    }
   } else {
-    auto k = tc_fwd_kernel<DK, NV, SOLVE>;
-    const size_t smem = FwdSmem<DK, NV, SOLVE>::TOTAL;
-    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
-      return FALCON_ERR_CUDA;
-    dim3 grid(BH, nsplit);
-    k<<<grid, 256, smem, fa.stream>>>(mq, mk, mv, mo, ta);
-    record_event(fa, 2);
+    CUtensorMap mk128;
+    if (!make_map(&mk128, fa.k, fa.B, fa.T, fa.H, DK, 128)) return FALCON_ERR_CUDA;
+    {
+      auto k = tc_wy_kernel<DK, SOLVE>;
+      const size_t smem = WySmem<DK>::TOTAL;
+      if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
+        return FALCON_ERR_CUDA;
+      dim3 grid((ta.NC + 1) / 2, BH);
+      record_event(fa, 0);
+      k<<<grid, 128, smem, fa.stream>>>(mk128, ta);
+      record_event(fa, 1);
+    }
+    {
+      auto k = tc_fwd_kernel<DK, NV, SOLVE>;
+      const size_t smem = FwdSmem<DK, NV, SOLVE>::TOTAL;
+      if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
+        return FALCON_ERR_CUDA;
+      dim3 grid(BH, fa.dv / NV);
+      k<<<grid, 256, smem, fa.stream>>>(mq, mk, mv, mo, ta);
+      record_event(fa, 2);
+    }
   }
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
