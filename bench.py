@@ -75,7 +75,7 @@ def kernel_bytes(w, names) -> list:
     es = 2 if w.dtype == "bf16" else 4
     th = w.B * w.T * w.H
     beta = th * (w.dv if w.per_channel else 1) * 4
-    if names == ["generic_chunk_kernel"]:
+    if len(names) == 1:  # one kernel does the whole forward
         return [algorithmic_bytes(w)]
     state = w.B * w.H * w.dk * w.dv * 4
     if names[0] == "tc_wyu_kernel":
@@ -410,6 +410,8 @@ def main():
         abytes = algorithmic_bytes(w)
         if impl_used != F.FALCON_IMPL_TC:
             names = ["generic_chunk_kernel"]
+        elif w.per_channel:
+            names = ["tc_f2_kernel"]
         elif w.dk == 64:
             names = ["tc_wyu_kernel", "tc_fwd_pipe_kernel"]
         else:

@@ -82,6 +82,8 @@ int launch_tc_chunk(const FwdArgs& a);
 bool tc_chunk_supported(const FwdArgs& a);
 int tc_chunk_launches(const FwdArgs& a);
 size_t tc_chunk_ws_bytes(int B, int T, int H, int dk, int dv, int chunk, int variant);
+bool tc_f2_supported(const FwdArgs& a);
+int launch_tc_f2(const FwdArgs& a);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -36,17 +36,17 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tc_util.cuh"
 
 namespace falcon {
 
 using namespace tc;
+using namespace tcu;
 
 namespace {
 
-constexpr int kC = 64;           // chunk length of this path
 constexpr int kLD = 68;          // fp32 row stride of the solve buffers (bank spread)
 constexpr int kYL = 24;          // row stride of the 16x16 scratch blocks
-constexpr uint32_t kStatusTimeout = 1;
 
 struct TcArgs {
   int B, T, H, NC, NV;
@@ -64,45 +64,6 @@ struct TcArgs {
   float* ws_g;        // [B*H*NC][128]: eta[64], g[64]
   uint32_t* status;   // workspace status word
 };
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Issue a chain of K/16 MMAs: D = A (M rows, K) * B (N rows, K)^T, both K-major
-// 128B-swizzled; K beyond 64 continues in the next 64-column slab.
-__device__ __forceinline__ void mma_chain(uint32_t d_tmem, const uint8_t* A, int a_rows,
-                                          const uint8_t* Bm, int b_rows, int K, uint32_t idesc,
-                                          bool accumulate) {
-  const uint32_t a0 = smem_u32(A), b0 = smem_u32(Bm);
-  for (int ks = 0; ks < K / 16; ++ks) {
-    const uint32_t off = (ks & 3) * 32;
-    const uint32_t slab = ks >> 2;
-    const uint64_t ad = sdesc_k128(a0 + slab * a_rows * 128 + off);
-    const uint64_t bd = sdesc_k128(b0 + slab * b_rows * 128 + off);
-    umma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
-  }
-}
-
-// Load 64 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-  tmem_ld32(taddr + 32, r);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
-}
 
 // ======================================================================
 // (a) per-chunk gates, Gram matrix and T = (I + A)^{-1}
@@ -720,54 +681,6 @@ struct FwdSmem {
   static_assert(NV == 64, "value slice of 64 channels");
 };
 
-// MN-major operand chain: D = A^T-or-B with 64 elements along M/N, K rows of
-// 128 B in the swizzled layout; K steps of 16 rows = 2048 B.
-__device__ __forceinline__ void mma_chain_mn(uint32_t d_tmem, uint64_t (*adesc)(uint32_t, int),
-                                             uint32_t a0, uint64_t (*bdesc)(uint32_t, int),
-                                             uint32_t b0, int K, uint32_t idesc, bool accumulate) {
-  for (int ks = 0; ks < K / 16; ++ks)
-    umma_bf16(d_tmem, adesc(a0, ks), bdesc(b0, ks), idesc, (ks > 0 || accumulate) ? 1u : 0u);
-}
-// descriptor of K step ks for a K-major operand (64-col slabs of `rows` rows)
-template <int ROWS>
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int ks) {
-  return sdesc_k128(base + (ks >> 2) * ROWS * 128 + (ks & 3) * 32);
-}
-// descriptor of K step ks for an MN-major operand (16 K rows per step)
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int ks) {
-  return sdesc_mn128(base + ks * 2048);
-}
-
-// Row r (K-major or MN-major rows of 64 bf16 are the same swizzled image):
-// write 64 fp32 values as bf16 with 16-byte stores.
-__device__ __forceinline__ void store_row64(uint8_t* tile, int r, const float* v) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t pk[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
-    *reinterpret_cast<uint4*>(tile + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  }
-}
-
-// Scale every row of a [64 x 64] bf16 swizzled tile by f[row] into dst (16-byte chunks).
-__device__ __forceinline__ void scale_rows(uint8_t* dst, const uint8_t* src, const float* f,
-                                           int tid, int nthreads) {
-  for (int idx = tid; idx < 512; idx += nthreads) {
-    const int R = idx >> 3;
-    const uint4 in = *reinterpret_cast<const uint4*>(src + idx * 16);
-    const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-    const float fr = f[R];
-    uint32_t pk[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 x = __bfloat1622float2(pin[e]);
-      pk[e] = pack_bf16(x.x * fr, x.y * fr);
-    }
-    *reinterpret_cast<uint4*>(dst + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  }
-}
-
 template <int DK, int NV, bool SOLVE>
 __global__ void __launch_bounds__(256, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -896,8 +809,7 @@ __global__ void __launch_bounds__(256, 1)
       gl[tid] = g;
       et[tid] = SOLVE ? e * gm : e;  // row scale of X (Falcon-1) or of V (Falcon-1A)
     }
-    __syncthreads();
-    if (*abort_flag) break;
+    if (__syncthreads_or(*abort_flag)) break;
     const float gam_last = Gam[63];
 
     // ---- row-scaled operands of the additive write (16-byte chunks)
@@ -971,9 +883,9 @@ __global__ void __launch_bounds__(256, 1)
     fence_proxy_async();
     tc_fence_before();
     if (tid == 0) bulk_wait_read0();  // the previous output tile has left the staging buffer
-    __syncthreads();
+    const bool ab2 = __syncthreads_or(*abort_flag);
     tc_fence_after();
-    if (*abort_flag) break;
+    if (ab2) break;
 
     if (SOLVE) {  // Delta = U - W S0
       if (tid == 0) {
@@ -1003,9 +915,9 @@ __global__ void __launch_bounds__(256, 1)
       }
       fence_proxy_async();
       tc_fence_before();
-      __syncthreads();
+      const bool ab3 = __syncthreads_or(*abort_flag);
       tc_fence_after();
-      if (*abort_flag) break;
+      if (ab3) break;
     }
 
     // ---- D2 = X^T diag(exp(g_last - g)) Delta, Ob = P~ Delta
@@ -1066,7 +978,6 @@ __global__ void __launch_bounds__(256, 1)
       tma_store_4d(&tm_o, Ost, c0, h, t0, b);
       bulk_commit();
     }
-    if (*abort_flag) break;
   }
   if (tid == 0) bulk_wait0();
   // ---- carry out
@@ -1130,13 +1041,6 @@ struct PipeSmem {
   static constexpr uint32_t COL_PT = 0, COL_B1 = 64, COL_B2 = 128, NCOLS = 256;
   static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192;
 };
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_read1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
 
 template <bool SOLVE>
 __global__ void __launch_bounds__(288, 1)
@@ -1242,9 +1146,8 @@ __global__ void __launch_bounds__(288, 1)
       }
       fence_proxy_async();
       tc_fence_before();
-      named_bar(1, 128);
+      if (named_bar_any(1, 128, *abort_flag != 0)) break;
       tc_fence_after();
-      if (*abort_flag) break;
       if (ftid == 0) {  // P^T = [X ; X] Q^T
         const uint32_t sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
         for (int ks = 0; ks < 4; ++ks)
@@ -1358,7 +1261,7 @@ __global__ void __launch_bounds__(288, 1)
       if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1))) fail();
       tc_fence_after();
       uint8_t* st = stage(s);
-      if (*abort_flag) break;
+      if (named_bar_any(2, 128, *abort_flag != 0)) break;
       const float* gt = reinterpret_cast<const float*>(st + L::DO);
       // the stage is handed back before the epilogues: keep their gates
       const float gfac = srow ? gt[L::G_GAM + 63] : gt[L::G_GAM + r];
@@ -1476,38 +1379,6 @@ __global__ void __launch_bounds__(288, 1)
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                              CUtensorMapFloatOOBfill);
-
-EncodeFn get_encode() {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  });
-  return fn;
-}
-
-// [B, T, H, D] bf16 tensor, box of 64 columns x `rows` time steps.
-bool make_map(CUtensorMap* m, const void* base, int B, int T, int H, int D, int rows) {
-  EncodeFn enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct WsLayout {
   size_t status, T, g, total;
 };
@@ -1576,19 +1447,22 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
 }  // namespace
 
 bool tc_chunk_supported(const FwdArgs& a) {
+  if (tc_f2_supported(a)) return true;
   if (a.variant != FALCON_1 && a.variant != FALCON_1A) return false;
   if (a.dtype != FALCON_BF16 || a.chunk != 64 || a.T < 1) return false;
   if (a.dk != a.dv || (a.dk != 64 && a.dk != 128)) return false;
   return true;
 }
 
-int tc_chunk_launches(const FwdArgs&) { return 2; }
+int tc_chunk_launches(const FwdArgs& a) { return tc_f2_supported(a) ? 1 : 2; }
 
-size_t tc_chunk_ws_bytes(int B, int T, int H, int, int, int chunk, int) {
+size_t tc_chunk_ws_bytes(int B, int T, int H, int, int, int chunk, int variant) {
+  if (variant == FALCON_2 || variant == FALCON_2A) return 256;  // status word only
   return ws_layout(B, T, H, chunk).total;
 }
 
 int launch_tc_chunk(const FwdArgs& fa) {
+  if (tc_f2_supported(fa)) return launch_tc_f2(fa);
   const WsLayout w = ws_layout(fa.B, fa.T, fa.H, 64);
   uint8_t* ws = reinterpret_cast<uint8_t*>(fa.ws);
   TcArgs ta;

@@ -49,8 +49,11 @@ def test_noalloc_rejects_what_it_cannot_cover(F):
         F.falcon_chunk_fwd_noalloc(p, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, None, 1 << 20,
                                    None)
     assert e.value.code == -3
-    w2 = Workload("noalloc_f2", 2, 1, 64, 1, 64, 64)
-    with pytest.raises(F.FalconError) as e:
-        F.falcon_chunk_fwd_noalloc(params_for(F, w2), 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20,
-                                   None, 1 << 20, None)
-    assert e.value.code == -2
+    for variant in (2, 3, 4, 5):  # outside the Falcon-1 / 1A tensor-core path
+        w2 = Workload("noalloc_other", variant, 1, 64, 1, 64, 64, window=4 if variant >= 4 else 1)
+        x = make_inputs(w2, device="cuda")
+        o = torch.empty_like(x["v"])
+        with pytest.raises(F.FalconError) as e:
+            F.falcon_chunk_fwd_noalloc(params_for(F, w2), x["q"], x["k"], x["v"], x["beta"], x["lam"],
+                                       None, o, None)
+        assert e.value.code == -2
