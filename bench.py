@@ -412,6 +412,8 @@ def main():
             names = ["generic_chunk_kernel"]
         elif w.per_channel:
             names = ["tc_f2_kernel"]
+        elif w.variant == 5:  # Falcon-3A
+            names = ["tc_f3a_kernel"]
         elif w.dk == 64:
             names = ["tc_wyu_kernel", "tc_fwd_pipe_kernel"]
         else:

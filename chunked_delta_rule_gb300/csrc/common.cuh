@@ -84,6 +84,8 @@ int tc_chunk_launches(const FwdArgs& a);
 size_t tc_chunk_ws_bytes(int B, int T, int H, int dk, int dv, int chunk, int variant);
 bool tc_f2_supported(const FwdArgs& a);
 int launch_tc_f2(const FwdArgs& a);
+bool tc_f3a_supported(const FwdArgs& a);
+int launch_tc_f3a(const FwdArgs& a);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -76,7 +76,8 @@ typedef enum { FALCON_BF16 = 0, FALCON_F32 = 1 } falcon_dtype_t;
 /* Kernel family for the chunk forward.  AUTO picks the tensor-core path
  * (tcgen05 + TMEM + TMA) when it supports the shape, else the portable
  * CUDA-core path.  GENERIC/TC force one (TC returns FALCON_ERR_UNSUPPORTED
- * for shapes it does not cover). */
+ * for shapes it does not cover).  The tensor-core path covers Falcon-1, 1A,
+ * 2 and 2A with bf16 inputs, chunk 64 and d_k = d_v in {64, 128}. */
 typedef enum { FALCON_IMPL_AUTO = 0, FALCON_IMPL_GENERIC = 1, FALCON_IMPL_TC = 2 } falcon_impl_t;
 
 enum {
@@ -160,8 +161,8 @@ int falcon_chunk_fwd_timed(const falcon_params_t* p, const void* q, const void* 
  * The scratch lives in a fixed 32 MiB array inside the library's device
  * image, held by every device that loads the library until the process
  * exits.  The call itself allocates nothing (no cudaMalloc/cudaFree).
- * Covered: the shapes the tensor-core path takes (see falcon_chunk_fwd_plan;
- * Falcon-1/1A, bf16, d_k = d_v in {64, 128}, chunk 64) needing at most
+ * Covered: Falcon-1 and Falcon-1A on the tensor-core path (bf16,
+ * d_k = d_v in {64, 128}, chunk 64; see falcon_chunk_fwd_plan) needing at most
  * 32 MiB of scratch, i.e. B * H * ceil(T / 64) <= 3855.  Larger problems
  * return FALCON_ERR_WORKSPACE, other shapes FALCON_ERR_UNSUPPORTED (they
  * need no workspace: call falcon_chunk_fwd with workspace = NULL).
