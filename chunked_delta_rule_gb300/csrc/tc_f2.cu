@@ -61,7 +61,8 @@ struct F2Smem {
   static constexpr size_t XQ = 0;
   static constexpr size_t VS = XQ + kSl * 16384;    // V slice, bf16 swizzled rows
   static constexpr size_t BS = VS + 8192;           // beta slice, fp32 [64][64]
-  static constexpr size_t LT = BS + 16384;          // L^T, fp32 [64][64] (row i = column i of L)
+  static constexpr size_t LT = BS + 16384;          // L: diagonal 16x16 blocks fp32 [4][16][16] at +0,
+                                                    // all of L as bf16 K-major rows at +8192
   static constexpr size_t PT = LT + 16384;          // P~, bf16 K-major rows t
   static constexpr size_t GT = PT + 8192;           // gates
   static constexpr size_t STAGE = GT + 2048;
@@ -77,9 +78,9 @@ struct F2Smem {
   static_assert(TOTAL <= 232448, "shared memory budget");
   // gates (fp32 offsets in GT)
   static constexpr int G_INV = 0, G_GAM = 64, G_DEC = 128, G_G = 192, G_CFE = 256, G_WS = 320;
-  // TMEM: S^T | [(X S0)^T | O^T] x 2 | [G ; P] (front)
-  static constexpr uint32_t COL_S = 0, COL_YO = DK, COL_F = DK + 256, NCOLS = 512;
-  static_assert(COL_F + 64 <= NCOLS, "TMEM budget");
+  // TMEM: S^T | [(X S0)^T | O^T] x 2 | [G ; P] (front) | E: sum_{i in earlier blocks} L_ri Delta_i
+  static constexpr uint32_t COL_S = 0, COL_YO = DK, COL_F = DK + 256, COL_E = DK + 320, NCOLS = 512;
+  static_assert(COL_E + 64 <= NCOLS, "TMEM budget");
 };
 
 template <int DK, bool SOLVE>
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* fdone = bars + NST;      // [NST]
   uint64_t* fmma = bars + 2 * NST;
   uint64_t* bmma = fmma + 1;         // [2]
+  uint64_t* tmma = bmma + 2;         // trailing update of the solve done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(fmma, 1);
     mbar_init(&bmma[0], 1);
     mbar_init(&bmma[1], 1);
+    mbar_init(tmma, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -241,10 +244,20 @@ __global__ void __launch_bounds__(256, 1)
           const int t = c * kC + x;
           const bool exists = t < a.T && pos + t >= 1;
           gt[L::G_INV + x] = exists ? 1.f / (a.eps + n) : 0.f;
-          if (SOLVE) {
-            float* lt = reinterpret_cast<float*>(st + L::LT);
+          if (SOLVE) {  // row x of L: its diagonal block in fp32, the whole row in bf16
 #pragma unroll
-            for (int i = 0; i < 64; ++i) lt[i * 64 + x] = (i < x) ? w[i] : 0.f;
+            for (int i = 0; i < 64; ++i) w[i] = (i < x) ? w[i] : 0.f;
+            float* ld = reinterpret_cast<float*>(st + L::LT) + (I * 16 + (x & 15)) * 16;
+#pragma unroll
+            for (int J = 0; J < 4; ++J) {
+              if (J == I) {
+#pragma unroll
+                for (int i = 0; i < 16; i += 4)
+                  *reinterpret_cast<float4*>(ld + i) = make_float4(w[16 * J + i], w[16 * J + i + 1],
+                                                                   w[16 * J + i + 2], w[16 * J + i + 3]);
+              }
+            }
+            store_row64(st + L::LT + 8192, x, w);
           }
         } else {  // P row t = x: P~[t][r] = exp(g_t - g_r) q_t . x_r for r <= t
 #pragma unroll
@@ -298,7 +311,7 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_before();
     named_bar(2, 128);
     tc_fence_after();
-    uint32_t bph = 0;
+    uint32_t bph = 0, tph = 0;
     int c = 0;
     for (; c < NC; ++c) {
       const int s = c % NST, p = c & 1;
@@ -360,19 +373,53 @@ __global__ void __launch_bounds__(256, 1)
               acc[r] = vr - gam[r] * __uint_as_float(y[n]);
             }
           }
-          // forward substitution for this channel, L^T rows broadcast from shared memory
-          const float* lt = reinterpret_cast<const float*>(st + L::LT);
+          // forward substitution for this channel in 16-row blocks: inside a block
+          // in registers with the fp32 diagonal block of L; the contributions of
+          // finished blocks to all later rows accumulate in TMEM (E) by one MMA
+          // [Delta^T ; Delta^T]_(block) L_(:, block)^T per block
+          const float* ldiag = reinterpret_cast<const float*>(st + L::LT);
+          const uint32_t sDA = smem_u32(DA), sLb = smem_u32(st + L::LT + 8192);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const float d = bsl[i * 64 + j] * inv[i] * acc[i];
-            acc[i] = d;
+          for (int I = 0; I < 4; ++I) {
+            if (I > 0) {  // E holds sum over the finished blocks
+              if (!mbar_wait(tmma, tph)) fail();
+              tph ^= 1;
+              tc_fence_after();
+              uint32_t e[16];
+              tmem_ld16(tmem + lane_off + L::COL_E + 16 * I, e);
+              tmem_wait_ld();
 #pragma unroll
-            for (int m = (i + 1) >> 2; m < 16; ++m) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lt + i * 64 + 4 * m);
-              if (4 * m > i) acc[4 * m] = fmaf(-l4.x, d, acc[4 * m]);
-              if (4 * m + 1 > i) acc[4 * m + 1] = fmaf(-l4.y, d, acc[4 * m + 1]);
-              if (4 * m + 2 > i) acc[4 * m + 2] = fmaf(-l4.z, d, acc[4 * m + 2]);
-              acc[4 * m + 3] = fmaf(-l4.w, d, acc[4 * m + 3]);
+              for (int r = 0; r < 16; ++r) acc[16 * I + r] -= __uint_as_float(e[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+              const int R = 16 * I + r;
+              float sacc = acc[R];
+#pragma unroll
+              for (int i = 0; i < r; ++i) sacc = fmaf(-ldiag[(I * 16 + r) * 16 + i], acc[16 * I + i], sacc);
+              acc[R] = bsl[R * 64 + j] * inv[R] * sacc;
+            }
+            {  // this block of Delta^T (bf16) in both halves of the operand
+              uint32_t pk[8];
+#pragma unroll
+              for (int e2 = 0; e2 < 8; ++e2) pk[e2] = pack_bf16(acc[16 * I + 2 * e2], acc[16 * I + 2 * e2 + 1]);
+#pragma unroll
+              for (int hlf = 0; hlf < 2; ++hlf) {
+                const uint4 u = make_uint4(pk[4 * hlf], pk[4 * hlf + 1], pk[4 * hlf + 2], pk[4 * hlf + 3]);
+                *reinterpret_cast<uint4*>(DA + sw128(L_, 16 * I + 8 * hlf)) = u;
+                *reinterpret_cast<uint4*>(DA + sw128(L_ + 64, 16 * I + 8 * hlf)) = u;
+              }
+            }
+            if (I < 3) {
+              fence_proxy_async();
+              tc_fence_before();
+              named_bar(4, 64);
+              tc_fence_after();
+              if (tid == 0) {
+                umma_bf16(tmem + L::COL_E, kdesc<128>(sDA, I), kdesc<64>(sLb, I), idesc_bf16(128, 64),
+                          I > 0 ? 1u : 0u);
+                umma_commit(tmma);
+              }
             }
           }
         } else {  // additive write: Delta = eta (.) V
@@ -382,14 +429,16 @@ __global__ void __launch_bounds__(256, 1)
             acc[r] = bsl[r * 64 + j] * inv[r] * vr;
           }
         }
+        if (!SOLVE) {
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          uint32_t pk[4];
+          for (int m = 0; m < 8; ++m) {
+            uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(acc[8 * m + 2 * e], acc[8 * m + 2 * e + 1]);
-          const uint4 u = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(DA + sw128(L_, 8 * m)) = u;
-          *reinterpret_cast<uint4*>(DA + sw128(L_ + 64, 8 * m)) = u;
+            for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(acc[8 * m + 2 * e], acc[8 * m + 2 * e + 1]);
+            const uint4 u = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(DA + sw128(L_, 8 * m)) = u;
+            *reinterpret_cast<uint4*>(DA + sw128(L_ + 64, 8 * m)) = u;
+          }
         }
       } else {  // X~ rows in place of X (the product that read X is complete)
         const float* dec = gt + L::G_DEC;
