@@ -24,6 +24,10 @@ with the functions that rely on them:
   (x_t, v_t) = (phi(k_{t-1}), v_t) [FW 本质; JC 一个被忽略的时间差].  phi is
   applied by the caller; x_0 is the carried previous key (zero when fresh).
   A pair whose global index is < 1 does not exist and writes nothing.
+  The same-step pairing (x_t, v_t) = (phi(k_t), v_t), which the pages set
+  against the prefix alignment as the usual delta-rule pairing
+  [FW 本质; JC 一个被忽略的时间差], is available as an ablation
+  (``pairing="same"``): every pair with global index >= 0 exists.
 * shrink-then-correct: S_t = gamma_t S_{t-1} + eta_t x_t (v_t - gamma_t S_{t-1}^T x_t)^T,
   one online gradient step on the squared error at the shrunk state
   [JC 把记忆更新变成一次梯度下降], with the NLMS step
@@ -91,14 +95,22 @@ def _f64(a):
     return None if a is None else np.asarray(a, dtype=np.float64)
 
 
-def build_pairs(k, v, window, carry=None):
-    """Prefix-aligned training pairs (x_j, v_j) = (k_{j-1}, v_j) [FW 本质].
+PAIRINGS = ("prefix", "same")
+
+
+def build_pairs(k, v, window, carry=None, pairing="prefix"):
+    """Training pairs: prefix-aligned (x_j, v_j) = (k_{j-1}, v_j) [FW 本质], or
+    same-step (k_j, v_j) for the ablation.
 
     Returns X [B, H, T+W-1, dk], V [B, H, T+W-1, dv] and valid [B, H, T+W-1]
-    indexed by j + W - 1 for local pair index j in [-(W-1), T-1].  Pair 0 uses
-    the carried k_prev (zero when fresh); pairs j < 0 come from the carry's
-    window ring.  A pair exists iff its global index pos + j is >= 1.
+    indexed by j + W - 1 for local pair index j in [-(W-1), T-1].  Prefix
+    alignment: pair 0 uses the carried k_prev (zero when fresh) and a pair
+    exists iff its global index pos + j is >= 1.  Same-step: pair j >= 0 uses
+    k_j and exists iff pos + j >= 0.  Pairs j < 0 come from the carry's window
+    ring in both.
     """
+    assert pairing in PAIRINGS
+    same = pairing == "same"
     k = _f64(k)
     v = _f64(v)
     B, T, H, dk = k.shape
@@ -112,9 +124,11 @@ def build_pairs(k, v, window, carry=None):
     pos = np.zeros((B, H), dtype=np.int64)
     if carry is not None:
         pos = np.asarray(carry["pos"], dtype=np.int64).reshape(B, H)
-        if carry.get("k_prev") is not None:
+        if carry.get("k_prev") is not None and not same:
             X[:, :, W - 1, :] = _f64(carry["k_prev"])
-    if T > 1:
+    if same:
+        X[:, :, W - 1:, :] = kt
+    elif T > 1:
         X[:, :, W:, :] = kt[:, :, : T - 1, :]
     V[:, :, W - 1:, :] = vt
     if W > 1 and carry is not None and carry.get("win_x") is not None:
@@ -127,7 +141,7 @@ def build_pairs(k, v, window, carry=None):
                     X[b, h, j + W - 1] = wx[b, h, slot]
                     V[b, h, j + W - 1] = wv[b, h, slot]
     j = np.arange(-(W - 1), T)
-    valid = (pos[:, :, None] + j[None, None, :]) >= 1
+    valid = (pos[:, :, None] + j[None, None, :]) >= (0 if same else 1)
     X = X * valid[..., None]
     V = V * valid[..., None]
     return X, V, valid, pos
@@ -156,7 +170,7 @@ def step_coefficients(beta_t, x_win, valid_win, eps, per_channel):
 
 
 def recurrent(q, k, v, beta, lam, variant, window=1, eps=1e-6, eps_gamma=1e-3,
-              carry=None, return_trace=False):
+              carry=None, return_trace=False, pairing="prefix"):
     """Token-by-token recurrence: the definition of every variant.
 
     The recurrent form is the inference form with an O(1) state per step
@@ -185,7 +199,7 @@ def recurrent(q, k, v, beta, lam, variant, window=1, eps=1e-6, eps_gamma=1e-3,
     dv = v.shape[-1]
     W = effective_window(variant, window)
     per_ch = is_per_channel(variant)
-    X, V, valid, pos = build_pairs(k, v, W, carry)
+    X, V, valid, pos = build_pairs(k, v, W, carry, pairing)
     S = np.zeros((B, H, dk, dv))
     if carry is not None and carry.get("S") is not None:
         S = _f64(carry["S"]).copy()
@@ -252,7 +266,8 @@ def make_carry_out(k, V, valid, X, S, pos, W, carry, T):
 # Masked-parallel form
 # --------------------------------------------------------------------------
 
-def masked_parallel(q, k, v, beta, lam, variant, window=1, eps=1e-6, eps_gamma=1e-3):
+def masked_parallel(q, k, v, beta, lam, variant, window=1, eps=1e-6, eps_gamma=1e-3,
+                    pairing="prefix"):
     """Masked-parallel form of a fresh sequence [FW 三种等价形式; JC 三种视角看同一个更新].
 
     The whole sequence is laid out at once, as in denominator-free linear
@@ -280,7 +295,7 @@ def masked_parallel(q, k, v, beta, lam, variant, window=1, eps=1e-6, eps_gamma=1
     dv = v.shape[-1]
     W = effective_window(variant, window)
     per_ch = is_per_channel(variant)
-    X, V, valid, _ = build_pairs(k, v, W, None)
+    X, V, valid, _ = build_pairs(k, v, W, None, pairing)
     gamma = decay_factor(lam, eps_gamma)
     o = np.zeros((B, T, H, dv))
     S_final = np.zeros((B, H, dk, dv))
@@ -330,7 +345,7 @@ def masked_parallel(q, k, v, beta, lam, variant, window=1, eps=1e-6, eps_gamma=1
 # --------------------------------------------------------------------------
 
 def chunked(q, k, v, beta, lam, variant, window=1, chunk=16, eps=1e-6, eps_gamma=1e-3,
-            carry=None):
+            carry=None, pairing="prefix"):
     """Chunk-parallel form: cross-chunk state recurrence plus intra-chunk
     parallel work [FW 三种等价形式; JC 三种视角看同一个更新], with the per-chunk
     WY representation of the rank-one updates [FW 图4C; JC 三种视角看同一个更新].
@@ -362,7 +377,7 @@ def chunked(q, k, v, beta, lam, variant, window=1, chunk=16, eps=1e-6, eps_gamma
     dv = v.shape[-1]
     Wn = effective_window(variant, window)
     per_ch = is_per_channel(variant)
-    X, V, valid, pos = build_pairs(k, v, Wn, carry)
+    X, V, valid, pos = build_pairs(k, v, Wn, carry, pairing)
     gamma = decay_factor(lam, eps_gamma)
     S = np.zeros((B, H, dk, dv))
     if carry is not None and carry.get("S") is not None:
@@ -473,7 +488,7 @@ def _chunk_window(Q, Xk, Vk, coef, g, Gam, decay, S0, variant, Wn):
 # --------------------------------------------------------------------------
 
 def recurrent_heads(q, k, v, beta, lam, variant, heads, window=1, eps=1e-6, eps_gamma=1e-3,
-                    carry=None):
+                    carry=None, pairing="prefix"):
     """Run :func:`recurrent` on a subset of (b, h) pairs only.
 
     heads: list of (b, h).  Returns o [len(heads), T, dv] and S_final
@@ -488,7 +503,7 @@ def recurrent_heads(q, k, v, beta, lam, variant, heads, window=1, eps=1e-6, eps_
             c = {key: (None if val is None else np.asarray(val)[b:b + 1, h:h + 1])
                  for key, val in carry.items()}
         o, co = recurrent(sub(q), sub(k), sub(v), sub(beta), sub(lam), variant, window,
-                          eps, eps_gamma, c)
+                          eps, eps_gamma, c, pairing=pairing)
         outs.append(o[0, :, 0, :])
         states.append(co["S"][0, 0])
     return np.stack(outs), np.stack(states)

@@ -17,6 +17,11 @@ P4  Falcon-3 window averaging: W = 1 is Falcon-1, identical pairs give the
 P5  positive-decay clamp keeps every log-decay finite [same page, 正衰减钳制]
 P6  closed forms: hand-derived scalar sequences, exact orthonormal retrieval
 P7  variant reductions: Falcon-2 with equal channels is Falcon-1 (and 2A is 1A)
+P8  same-step pairing (the ablation of the prefix alignment): the three forms
+    agree; it equals the prefix alignment fed the next key; with unit step it
+    is the classical delta rule, which reads back the value just written
+    [Falcon 家族重新对齐 fast-weight 记忆, 本质; 给记忆装一个“及时纠错”的开关,
+    一个被忽略的时间差]
 """
 
 import json
@@ -372,3 +377,56 @@ def test_p7_per_channel_channels_are_independent_scalar_runs():
         o1, c1 = O.recurrent(**xc, variant=O.FALCON_1)
         assert np.abs(o1[..., 0] - o2[..., ch]).max() <= 1e-14
         assert np.abs(c1["S"][..., 0] - c2["S"][..., ch]).max() <= 1e-14
+
+
+# ---------------------------------------------------------------- P8
+@pytest.mark.parametrize("variant", ALL)
+def test_p8_same_step_three_forms_agree(variant):
+    rng = np.random.default_rng(300 + variant)
+    W = 3 if O.is_windowed(variant) else 1
+    x = rand_inputs(rng, 2, 45, 2, 8, 6, O.is_per_channel(variant))
+    o_r, c_r = O.recurrent(**x, variant=variant, window=W, pairing="same")
+    o_m, S_m = O.masked_parallel(**x, variant=variant, window=W, pairing="same")
+    o_c, c_c = O.chunked(**x, variant=variant, window=W, chunk=16, pairing="same")
+    assert rel(o_m, o_r) <= 1e-10 and rel(S_m, c_r["S"]) <= 1e-10
+    assert rel(o_c, o_r) <= 1e-10 and rel(c_c["S"], c_r["S"]) <= 1e-10
+    o_p, _ = O.recurrent(**x, variant=variant, window=W)
+    assert rel(o_p, o_r) > 1e-3  # the two alignments are different methods
+
+
+@pytest.mark.parametrize("variant", ALL)
+def test_p8_same_step_is_prefix_alignment_of_the_next_key(variant):
+    """Same-step pairs (k_t, v_t) are the prefix pairs of the key sequence
+    shifted by one, with k_0 as the carried key of a sequence that already
+    consumed one token."""
+    rng = np.random.default_rng(310 + variant)
+    W = 4 if O.is_windowed(variant) else 1
+    B, T, H, dk, dv = 2, 37, 2, 8, 6
+    x = rand_inputs(rng, B, T, H, dk, dv, O.is_per_channel(variant))
+    o_s, c_s = O.recurrent(**x, variant=variant, window=W, pairing="same")
+    k_next = np.zeros_like(x["k"])
+    k_next[:, :-1] = x["k"][:, 1:]
+    carry = {"S": np.zeros((B, H, dk, dv)), "k_prev": x["k"][:, 0].copy(),
+             "pos": np.ones((B, H), dtype=np.int64)}
+    if W > 1:
+        carry["win_x"] = np.zeros((B, H, W - 1, dk))
+        carry["win_v"] = np.zeros((B, H, W - 1, dv))
+    xp = dict(x, k=k_next)
+    o_p, c_p = O.recurrent(**xp, variant=variant, window=W, carry=carry)
+    assert rel(o_s, o_p) <= 1e-12 and rel(c_s["S"], c_p["S"]) <= 1e-12
+
+
+def test_p8_same_step_unit_step_reads_back_the_written_value():
+    """Classical delta rule: gamma = 1, beta = 1, eps = 0, unit keys and
+    q_t = k_t: after the write of (k_t, v_t) the state returns v_t for k_t,
+    for any (non-orthogonal) key sequence."""
+    rng = np.random.default_rng(320)
+    T, dk, dv = 25, 6, 4
+    k = rng.standard_normal((1, T, 1, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((1, T, 1, dv))
+    x = dict(q=k.copy(), k=k, v=v, beta=np.ones((1, T, 1)), lam=np.zeros((1, T, 1)))
+    o, _ = O.recurrent(**x, variant=O.FALCON_1, eps=0.0, pairing="same")
+    assert np.abs(o - v).max() <= 1e-12
+    o_p, _ = O.recurrent(**x, variant=O.FALCON_1, eps=0.0)
+    assert np.abs(o_p - v).max() > 1e-2  # prefix-aligned pairs do not do this
