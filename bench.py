@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--mode", choices=["chunk", "decode"], default="chunk",
                     help="decode: the recurrent one-token step (256 sequences x 12 heads)")
     ap.add_argument("--decode-variant", type=int, default=0)
+    ap.add_argument("--pairing", choices=["prefix", "same"], default="prefix",
+                    help="same: the same-step pairing ablation (x_t = k_t)")
     ap.add_argument("--sets", type=int, default=N_SETS,
                     help="rotating input sets (fewer only for profiler captures)")
     return ap.parse_args()
@@ -150,11 +152,13 @@ def cpu_baseline(w, budget_s=20.0) -> dict:
     nb = 1
     x = {k: v.double().numpy() for k, v in make_inputs(w.with_(B=nb)).items()}
     t0 = time.perf_counter()
-    oracle.recurrent(**x, variant=w.variant, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma)
+    oracle.recurrent(**x, variant=w.variant, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma,
+                     pairing=w.pairing)
     dt = time.perf_counter() - t0
     reps = 1
     while time.perf_counter() - t0 < min(budget_s, 5 * dt) and reps < 3:
-        oracle.recurrent(**x, variant=w.variant, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma)
+        oracle.recurrent(**x, variant=w.variant, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma,
+                     pairing=w.pairing)
         reps += 1
     dt = (time.perf_counter() - t0) / reps
     del np
@@ -190,10 +194,10 @@ def run_reference(args, w, rank):
     nb, T = 1, min(w.T, 512)
     x = {k: v.double().numpy() for k, v in make_inputs(w.with_(B=nb, T=T)).items()}
     for _ in range(args.warmup):
-        oracle.recurrent(**x, variant=w.variant, window=w.window)
+        oracle.recurrent(**x, variant=w.variant, window=w.window, pairing=w.pairing)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.recurrent(**x, variant=w.variant, window=w.window)
+        oracle.recurrent(**x, variant=w.variant, window=w.window, pairing=w.pairing)
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
     value = nb * T / dt
     line = {"impl": "reference", "metric": "Falcon-1 chunked fwd tokens/s", "value": value,
@@ -286,6 +290,8 @@ def main():
         run_decode(args)
         return
     w = get_workload(args.workload)
+    if args.pairing == "same":
+        w = w.with_(name=w.name + "_same_step", pairing="same")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -309,7 +315,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     p = F.Params(B=w.B, T=w.T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk, window=w.window,
                  eps=w.eps, eps_gamma=w.eps_gamma, variant=w.variant,
-                 dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32)
+                 dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32,
+                 pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX)
     sets = [make_inputs(w, seed=w.seed + 100 * rank + i, device=dev) for i in range(args.sets)]
     o = torch.empty((w.B, w.T, w.H, w.dv), dtype=sets[0]["q"].dtype, device=dev)
     carry = F.empty_carry(p, dev)

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(PKG, "libfalcon.so")
 FALCON_1, FALCON_1A, FALCON_2, FALCON_2A, FALCON_3, FALCON_3A = range(6)
 FALCON_BF16, FALCON_F32 = 0, 1
 FALCON_IMPL_AUTO, FALCON_IMPL_GENERIC, FALCON_IMPL_TC = 0, 1, 2
+FALCON_PAIR_PREFIX, FALCON_PAIR_SAME_STEP = 0, 1
 FALCON_OK = 0
 
 EXPORTED = [
@@ -39,7 +40,8 @@ class falcon_params_t(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
                 ("window", ctypes.c_int32), ("eps", ctypes.c_float), ("eps_gamma", ctypes.c_float),
-                ("variant", ctypes.c_int32), ("dtype", ctypes.c_int32), ("impl", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("dtype", ctypes.c_int32), ("impl", ctypes.c_int32),
+                ("pairing", ctypes.c_int32)]
 
 
 class falcon_carry_t(ctypes.Structure):
@@ -100,10 +102,12 @@ class Params:
     variant: int = FALCON_1
     dtype: int = FALCON_BF16
     impl: int = FALCON_IMPL_AUTO
+    pairing: int = FALCON_PAIR_PREFIX
 
     def c(self) -> falcon_params_t:
         return falcon_params_t(self.B, self.T, self.H, self.dk, self.dv, self.chunk, self.window,
-                               self.eps, self.eps_gamma, self.variant, self.dtype, self.impl)
+                               self.eps, self.eps_gamma, self.variant, self.dtype, self.impl,
+                               self.pairing)
 
 
 def _ptr(x) -> int | None:

@@ -18,6 +18,7 @@ int check_params(const falcon_params_t* p, bool need_T_pos) {
   if (p->variant < FALCON_1 || p->variant > FALCON_3A) return FALCON_ERR_INVALID_ARG;
   if (p->dtype != FALCON_BF16 && p->dtype != FALCON_F32) return FALCON_ERR_INVALID_ARG;
   if (p->impl < FALCON_IMPL_AUTO || p->impl > FALCON_IMPL_TC) return FALCON_ERR_INVALID_ARG;
+  if (p->pairing != FALCON_PAIR_PREFIX && p->pairing != FALCON_PAIR_SAME_STEP) return FALCON_ERR_INVALID_ARG;
   if (!(p->eps > 0.f) || !(p->eps_gamma > 0.f) || !(p->eps_gamma <= 1.f)) return FALCON_ERR_INVALID_ARG;
   if (!dim_ok(p->dk) || !dim_ok(p->dv)) return FALCON_ERR_UNSUPPORTED;
   if (p->chunk != 16 && p->chunk != 32 && p->chunk != 64) return FALCON_ERR_UNSUPPORTED;
@@ -40,6 +41,7 @@ FwdArgs make_args(const falcon_params_t* p, const void* q, const void* k, const 
   a.B = p->B; a.T = p->T; a.H = p->H; a.dk = p->dk; a.dv = p->dv; a.chunk = p->chunk;
   a.W = effective_window(p->variant, p->window);
   a.eps = p->eps; a.eps_gamma = p->eps_gamma; a.variant = p->variant; a.dtype = p->dtype;
+  a.shift = p->pairing == FALCON_PAIR_PREFIX ? 1 : 0;
   a.q = q; a.k = k; a.v = v; a.beta = beta; a.lam = lambda; a.o = o;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   return a;

@@ -44,6 +44,7 @@ struct FwdArgs {
   int B, T, H, dk, dv, chunk, W;  // W: effective window (1 outside Falcon-3/3A)
   float eps, eps_gamma;
   int variant, dtype;
+  int shift;                // pair t uses key t - shift: 1 prefix alignment, 0 same-step
   const void* q;
   const void* k;
   const void* v;

@@ -69,7 +69,7 @@ __device__ __forceinline__ float ld(const void* p, size_t i) {
 template <typename Tin>
 __device__ __forceinline__ float pair_key(const FwdArgs& a, int b, int h, int j, int col,
                                           int64_t pos) {
-  if (j >= 1) return ld<Tin>(a.k, (((size_t)b * a.T + (j - 1)) * a.H + h) * a.dk + col);
+  if (j >= a.shift) return ld<Tin>(a.k, (((size_t)b * a.T + (j - a.shift)) * a.H + h) * a.dk + col);
   if (j == 0) return a.kprev_in ? ld<Tin>(a.kprev_in, ((size_t)b * a.H + h) * a.dk + col) : 0.f;
   if (a.W > 1 && a.winx_in) {
     int slot = ring_slot(pos + j, a.W - 1);
@@ -133,18 +133,18 @@ __global__ void __launch_bounds__(kThreads) generic_chunk_kernel(FwdArgs a, int 
     // ---- pairs of the block (slot a of step s0+sigma is pair s0+sigma-W+1+a)
     for (int i = tid; i < NP; i += kThreads) {
       int j = s0 - W + 1 + i;
-      pval[i] = (pos + j >= 1 && j < T) ? 1.f : 0.f;
+      pval[i] = (pos + j >= a.shift && j < T) ? 1.f : 0.f;
     }
     for (int i = tid; i < NP * dk; i += kThreads) {
       int kk = i / dk, col = i % dk;
       int j = s0 - W + 1 + kk;
-      bool ok = (pos + j >= 1) && (j < T);
+      bool ok = (pos + j >= a.shift) && (j < T);
       Xw[kk * LX + col] = ok ? pair_key<Tin>(a, b, h, j, col, pos) : 0.f;
     }
     for (int i = tid; i < NP * dvs; i += kThreads) {
       int kk = i / dvs, col = i % dvs;
       int j = s0 - W + 1 + kk;
-      bool ok = (pos + j >= 1) && (j < T) && col < ncol;
+      bool ok = (pos + j >= a.shift) && (j < T) && col < ncol;
       Vw[i] = ok ? pair_value<Tin>(a, b, h, j, c0 + col, pos) : 0.f;
     }
     for (int i = tid; i < c * dk; i += kThreads) {
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) generic_chunk_kernel(FwdArgs a, int 
     for (int64_t p = pos + T - Wr; p <= pos + T - 1; ++p) {
       const int j = (int)(p - pos);
       const int slot = (int)(((p % Wr) + Wr) % Wr);
-      const bool ok = p >= 1;
+      const bool ok = p >= a.shift;
       if (slice == 0 && wxo)
         for (int col = tid; col < dk; col += kThreads)
           wxo[(((size_t)b * a.H + h) * Wr + slot) * dk + col] =

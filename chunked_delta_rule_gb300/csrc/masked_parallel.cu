@@ -57,11 +57,12 @@ __global__ void mp_prep_kernel(FwdArgs a, float* ws) {
   float* coef = base + L.coef;
   float* Xw = base + L.Xw;
   const int NP = T + W - 1;
-  // pair j = i - (W-1): (k_{j-1}, v_j); only j >= 1 exists in a fresh sequence
+  // pair j = i - (W-1): (k_{j-shift}, v_j); in a fresh sequence only j >= shift
+  // exists (shift 1: prefix alignment, 0: same-step pairing)
   for (int i = threadIdx.x; i < NP * dk; i += blockDim.x) {
     int p = i / dk, d = i % dk;
     int j = p - (W - 1);
-    Xw[i] = (j >= 1) ? ldm<Tin>(a.k, (((size_t)b * T + (j - 1)) * a.H + h) * dk + d) : 0.f;
+    Xw[i] = (j >= a.shift) ? ldm<Tin>(a.k, (((size_t)b * T + (j - a.shift)) * a.H + h) * dk + d) : 0.f;
   }
   if (threadIdx.x == 0) {
     float acc = 0.f;
@@ -77,7 +78,7 @@ __global__ void mp_prep_kernel(FwdArgs a, float* ws) {
     float n = 0.f, e = 0.f;
     for (int s = 0; s < W; ++s) {
       int j = t - (W - 1) + s;
-      if (j >= 1) {
+      if (j >= a.shift) {
         n += 1.f;
         float nn = 0.f;
         for (int d = 0; d < dk; ++d) { float x = Xw[(size_t)(t + s) * dk + d]; nn += x * x; }
@@ -91,7 +92,7 @@ __global__ void mp_prep_kernel(FwdArgs a, float* ws) {
     }
     for (int s = 0; s < W; ++s) {
       int j = t - (W - 1) + s;
-      coef[((size_t)t * W + s) * dv + cc] = (j >= 1) ? eta : 0.f;
+      coef[((size_t)t * W + s) * dv + cc] = (j >= a.shift) ? eta : 0.f;
     }
   }
 }

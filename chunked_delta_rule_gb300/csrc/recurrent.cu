@@ -63,8 +63,8 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
     int w = i / dk, d = i % dk;
     int64_t p = pos - Wr + w;
     float x = 0.f;
-    if (p >= 1) {
-      if (w == Wr) x = ldv<Tin>(a.kprev_out, bhi * dk + d);
+    if (p >= a.shift) {
+      if (w == Wr) x = a.shift ? ldv<Tin>(a.kprev_out, bhi * dk + d) : ldv<Tin>(a.k, bhi * dk + d);
       else x = ldv<Tin>(a.winx_out, (bhi * Wr + ring_slot(p, Wr)) * dk + d);
     }
     xw[i] = x;
@@ -73,14 +73,14 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
     int w = i / dv, d = i % dv;
     int64_t p = pos - Wr + w;
     float x = 0.f;
-    if (p >= 1) {
+    if (p >= a.shift) {
       if (w == Wr) x = ldv<Tin>(a.v, bhi * dv + d);
       else x = ldv<Tin>(a.winv_out, (bhi * Wr + ring_slot(p, Wr)) * dv + d);
     }
     vw[i] = x;
   }
   for (int d = tid; d < dk; d += kRecThreads) qv[d] = ldv<Tin>(a.q, bhi * dk + d);
-  for (int w = tid; w < W; w += kRecThreads) pv[w] = (pos - Wr + w >= 1) ? 1.f : 0.f;
+  for (int w = tid; w < W; w += kRecThreads) pv[w] = (pos - Wr + w >= a.shift) ? 1.f : 0.f;
   __syncthreads();
   // dot products x_j . q and ||x_j||^2: one warp per window slot
   {
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
   // carry: ring push of the current pair, new k_prev, position
   if (Wr > 0) {
     const int slot = ring_slot(pos, Wr);
-    const bool ok = pos >= 1;
+    const bool ok = pos >= a.shift;
     for (int d = tid; d < dk; d += kRecThreads)
       reinterpret_cast<Tin*>(a.winx_out)[(bhi * Wr + slot) * dk + d] =
           from_f32<Tin>(ok ? xw[Wr * dk + d] : 0.f);
@@ -205,9 +205,9 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
     const int w = i / D, d = i % D;
     const int64_t p = pos - Wr + w;
     float x = 0.f, v = 0.f;
-    if (p >= 1) {
+    if (p >= a.shift) {
       if (w == Wr) {
-        x = to_f32(reinterpret_cast<const Tin*>(a.kprev_out)[bhi * D + d]);
+        x = to_f32(reinterpret_cast<const Tin*>(a.shift ? a.kprev_out : a.k)[bhi * D + d]);
         v = to_f32(reinterpret_cast<const Tin*>(a.v)[bhi * D + d]);
       } else {
         const size_t o = (bhi * Wr + ring_slot(p, Wr)) * D + d;
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
     if (lane == 0) {
       xq[w] = aq;
       xn[w] = an;
-      pv[w] = (pos - Wr + w >= 1) ? 1.f : 0.f;
+      pv[w] = (pos - Wr + w >= a.shift) ? 1.f : 0.f;
     }
   }
   // partial predictions S^T x_j (j < W) and S^T q over this thread's rows
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
   }
   if (Wr > 0) {  // ring push of the current pair
     const int slot = ring_slot(pos, Wr);
-    const bool ok = pos >= 1;
+    const bool ok = pos >= a.shift;
     for (int d = tid; d < D; d += NT) {
       reinterpret_cast<Tin*>(a.winx_out)[(bhi * Wr + slot) * D + d] = from_f32<Tin>(ok ? xw[Wr][d] : 0.f);
       reinterpret_cast<Tin*>(a.winv_out)[(bhi * Wr + slot) * D + d] = from_f32<Tin>(ok ? vw[Wr][d] : 0.f);

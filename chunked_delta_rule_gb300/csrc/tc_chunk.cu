@@ -50,6 +50,7 @@ constexpr int kYL = 24;          // row stride of the 16x16 scratch blocks
 
 struct TcArgs {
   int B, T, H, NC, NV;
+  int shift;          // pair t uses key t - shift (1 prefix alignment, 0 same-step)
   float eps, eps_gamma;
   const float* beta;
   const float* lam;
@@ -123,13 +124,13 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar[0], L::kSlabs * 128 * 128);
     for (int s = 0; s < L::kSlabs; ++s)
-      tma_load_4d(Xs + s * 16384, &tm_k128, &bar[0], 64 * s, h, t_base - 1, b);
+      tma_load_4d(Xs + s * 16384, &tm_k128, &bar[0], 64 * s, h, t_base - a.shift, b);
   }
   // gates while the keys are in flight: row tid <-> step t_base + tid
   const int t = t_base + tid;
   const bool step_ok = t < a.T;
   const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
-  const bool exists = step_ok && (pos + t >= 1);
+  const bool exists = step_ok && (pos + t >= a.shift);
   const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
   const float ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
   const float beta = step_ok ? a.beta[gi] : 0.f;
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
   }
-  if (pair == 0 && a.kprev_in) {  // x_0 = carried key (row 0 of the first chunk)
+  if (pair == 0 && a.kprev_in && a.shift) {  // x_0 = carried key (row 0 of the first chunk)
     for (int i = tid; i < DK; i += 128)
       *reinterpret_cast<__nv_bfloat16*>(Xs + (i >> 6) * 16384 + sw128(0, i & 63)) =
           a.kprev_in[(size_t)bh * DK + i];
@@ -384,14 +385,14 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar[0], 16384);
     tma_load_4d(Vs, &tm_v, &bar[0], 0, h, t0, b);
-    tma_load_4d(Xs, &tm_k, &bar[0], 0, h, t0 - 1, b);
+    tma_load_4d(Xs, &tm_k, &bar[0], 0, h, t0 - a.shift, b);
   }
   // gates while the tiles are in flight: row tid <-> step t0 + tid
   {
     const int t = t0 + tid;
     const bool step_ok = tid < 64 && t < a.T;
     const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
-    const bool exists = step_ok && (pos + t >= 1);
+    const bool exists = step_ok && (pos + t >= a.shift);
     const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
     const float ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
     float g = ell;  // inclusive prefix sum over the chunk
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
   }
-  if (chunk == 0 && a.kprev_in && tid < 64)  // x_0 = carried key (row 0 of the first chunk)
+  if (chunk == 0 && a.kprev_in && a.shift && tid < 64)  // x_0 = carried key (row 0 of the first chunk)
     *reinterpret_cast<__nv_bfloat16*>(Xs + sw128(0, tid)) = a.kprev_in[(size_t)bh * 64 + tid];
   fence_proxy_async();
   __syncthreads();
@@ -723,7 +724,7 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t bytes = (uint32_t)(L::XSZ + L::QSZ + L::VSZ + L::TSZ + L::GSZ);
     mbar_arrive_expect_tx(&full[s], bytes);
     for (int k = 0; k < L::kKS; ++k) {
-      tma_load_4d(Xst(s) + k * 8192, &tm_k, &full[s], 64 * k, h, c * kC - 1, b);
+      tma_load_4d(Xst(s) + k * 8192, &tm_k, &full[s], 64 * k, h, c * kC - a.shift, b);
       tma_load_4d(Qst(s) + k * 8192, &tm_q, &full[s], 64 * k, h, c * kC, b);
     }
     tma_load_4d(Vst(s), &tm_v, &full[s], c0, h, c * kC, b);
@@ -795,7 +796,7 @@ __global__ void __launch_bounds__(256, 1)
       *abort_flag = 1;
       atomicExch(a.status, kStatusTimeout);
     }
-    if (c == 0 && a.kprev_in) {  // x_0 = carried key
+    if (c == 0 && a.kprev_in && a.shift) {  // x_0 = carried key
       for (int i = tid; i < DK; i += 256)
         *reinterpret_cast<__nv_bfloat16*>(Xst(0) + (i >> 6) * 8192 + sw128(0, i & 63)) =
             a.kprev_in[(size_t)bh * DK + i];
@@ -1108,8 +1109,8 @@ __global__ void __launch_bounds__(288, 1)
         uint8_t* st = stage(s);
         const size_t ci = (size_t)bh * NC + c;
         mbar_arrive_expect_tx(&full[s], L::TX);
-        tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - 1, b);
-        tma_load_4d(st + L::PO, &tm_k, &full[s], 0, h, c * kC - 1, b);
+        tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - a.shift, b);
+        tma_load_4d(st + L::PO, &tm_k, &full[s], 0, h, c * kC - a.shift, b);
         tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
         if (SOLVE) bulk_load(st + L::WO, a.ws_T + ci * 16384, 8192, &full[s]);
         bulk_load(st + L::UO, a.ws_T + ci * 16384 + 8192, 8192, &full[s]);
@@ -1130,7 +1131,7 @@ __global__ void __launch_bounds__(288, 1)
       const int s = c % NST;
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
       uint8_t* st = stage(s);
-      if (c == 0 && a.kprev_in && ftid < 64) {  // x_0 = carried key, in both copies of X
+      if (c == 0 && a.kprev_in && a.shift && ftid < 64) {  // x_0 = carried key, in both copies of X
         const __nv_bfloat16 kv = a.kprev_in[(size_t)bh * 64 + ftid];
         *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = kv;
         *reinterpret_cast<__nv_bfloat16*>(st + L::PO + sw128(0, ftid)) = kv;
@@ -1468,6 +1469,7 @@ int launch_tc_chunk(const FwdArgs& fa) {
   uint8_t* ws = reinterpret_cast<uint8_t*>(fa.ws);
   TcArgs ta;
   ta.B = fa.B; ta.T = fa.T; ta.H = fa.H; ta.NC = (fa.T + kC - 1) / kC;
+  ta.shift = fa.shift;
   ta.eps = fa.eps; ta.eps_gamma = fa.eps_gamma;
   ta.beta = fa.beta; ta.lam = fa.lam; ta.pos_in = fa.pos_in;
   ta.kprev_in = reinterpret_cast<const __nv_bfloat16*>(fa.kprev_in);

@@ -42,6 +42,7 @@ namespace {
 
 struct F2Args {
   int B, T, H, dv, NC;
+  int shift;  // pair t uses key t - shift (1 prefix alignment, 0 same-step)
   float eps, eps_gamma;
   const float* lam;
   const int64_t* pos_in;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(256, 1)
     mbar_arrive_expect_tx(&full[s], L::TX);
 #pragma unroll
     for (int s2 = 0; s2 < kSl; ++s2) {
-      tma_load_4d(st + L::XQ + s2 * 16384, &tm_k, &full[s], 64 * s2, h, c * kC - 1, b);
+      tma_load_4d(st + L::XQ + s2 * 16384, &tm_k, &full[s], 64 * s2, h, c * kC - a.shift, b);
       tma_load_4d(st + L::XQ + s2 * 16384 + 8192, &tm_q, &full[s], 64 * s2, h, c * kC, b);
     }
     tma_load_4d(st + L::VS, &tm_v, &full[s], c0, h, c * kC, b);
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(256, 1)
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
       uint8_t* st = stage(s);
       float* gt = reinterpret_cast<float*>(st + L::GT);
-      if (c == 0 && a.kprev_in && ftid < DK)  // x_0 = carried key
+      if (c == 0 && a.kprev_in && a.shift && ftid < DK)  // x_0 = carried key
         *reinterpret_cast<__nv_bfloat16*>(st + L::XQ + (ftid >> 6) * 16384 + sw128(0, ftid & 63)) =
             a.kprev_in[(size_t)bh * DK + ftid];
       // gates: inclusive prefix sum of the clamped log-decay over the chunk
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int j = 0; j < 64; ++j) n = (j == x) ? v[j] : n;
           const int t = c * kC + x;
-          const bool exists = t < a.T && pos + t >= 1;
+          const bool exists = t < a.T && pos + t >= a.shift;
           gt[L::G_INV + x] = exists ? 1.f / (a.eps + n) : 0.f;
           if (SOLVE) {  // row x of L: its diagonal block in fp32, the whole row in bf16
 #pragma unroll
@@ -556,6 +557,7 @@ bool tc_f2_supported(const FwdArgs& a) {
 int launch_tc_f2(const FwdArgs& fa) {
   F2Args ta;
   ta.B = fa.B; ta.T = fa.T; ta.H = fa.H; ta.dv = fa.dv; ta.NC = (fa.T + kC - 1) / kC;
+  ta.shift = fa.shift;
   ta.eps = fa.eps; ta.eps_gamma = fa.eps_gamma;
   ta.lam = fa.lam; ta.pos_in = fa.pos_in;
   ta.kprev_in = reinterpret_cast<const __nv_bfloat16*>(fa.kprev_in);

@@ -42,6 +42,7 @@ constexpr int kKeys = 80;  // key / value rows per chunk (C + W - 1 <= 79, padde
 
 struct F3aArgs {
   int B, T, H, W, NC;
+  int shift;  // pair t uses key t - shift (1 prefix alignment, 0 same-step)
   float eps, eps_gamma;
   const float* beta;
   const float* lam;
@@ -82,15 +83,15 @@ struct F3aSmem {
 // Key (x) and value of local pair j of (b, h): j >= 1 from the sequence,
 // j = 0 the carried key with the first value, j < 0 the carried window ring.
 __device__ __forceinline__ __nv_bfloat16 pair_x(const F3aArgs& a, int b, int h, int j, int col, int64_t pos) {
-  if (j >= 1) return a.k[(((size_t)b * a.T + (j - 1)) * a.H + h) * 64 + col];
+  if (j >= a.shift) return a.k[(((size_t)b * a.T + (j - a.shift)) * a.H + h) * 64 + col];
   if (j == 0) return a.kprev_in ? a.kprev_in[((size_t)b * a.H + h) * 64 + col] : __float2bfloat16_rn(0.f);
-  if (!a.winx_in || pos + j < 1) return __float2bfloat16_rn(0.f);
+  if (!a.winx_in || pos + j < a.shift) return __float2bfloat16_rn(0.f);
   const int Wr = a.W - 1;
   return a.winx_in[(((size_t)b * a.H + h) * Wr + ring_slot(pos + j, Wr)) * 64 + col];
 }
 __device__ __forceinline__ __nv_bfloat16 pair_v(const F3aArgs& a, int b, int h, int j, int col, int64_t pos) {
   if (j >= 0) return a.v[(((size_t)b * a.T + j) * a.H + h) * 64 + col];
-  if (!a.winv_in || pos + j < 1) return __float2bfloat16_rn(0.f);
+  if (!a.winv_in || pos + j < a.shift) return __float2bfloat16_rn(0.f);
   const int Wr = a.W - 1;
   return a.winv_in[(((size_t)b * a.H + h) * Wr + ring_slot(pos + j, Wr)) * 64 + col];
 }
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(288, 1)
         uint8_t* st = stage(s);
         const int j0 = c * kC - W + 1;  // first pair of the chunk's keys
         mbar_arrive_expect_tx(&full[s], L::TX);
-        tma_load_4d(st + L::XO, &tm_k80, &full[s], 0, h, j0 - 1, b);
+        tma_load_4d(st + L::XO, &tm_k80, &full[s], 0, h, j0 - a.shift, b);
         tma_load_4d(st + L::VO, &tm_v80, &full[s], 0, h, j0, b);
         tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
       }
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(288, 1)
       if (j0 < 1) {  // keys before the sequence: carried key and window ring
         for (int idx = ftid; idx < W * 64; idx += 128) {
           const int kap = idx >> 6, col = idx & 63, j = j0 + kap;
-          if (j <= 0) {
+          if (j < a.shift) {
             *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(kap, col)) = pair_x(a, b, h, j, col, pos);
             if (j < 0)
               *reinterpret_cast<__nv_bfloat16*>(st + L::VO + sw128(kap, col)) = pair_v(a, b, h, j, col, pos);
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(288, 1)
           }
         }
         gt[L::G_NRM + ftid] = n;
-        gt[L::G_EX + ftid] = (pos + j >= 1 && j < a.T) ? 1.f : 0.f;
+        gt[L::G_EX + ftid] = (pos + j >= a.shift && j < a.T) ? 1.f : 0.f;
       }
       float g = ell;  // inclusive prefix sum of the log-decay over the chunk
       if (ftid < 64) {
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(288, 1)
         const int64_t p = pos + a.T - Wr + i;  // global pair index
         const int j = (int)(p - pos);
         const int slot = (int)(((p % Wr) + Wr) % Wr);
-        const bool ok = p >= 1;  // slots of pairs before the sequence hold zeros
+        const bool ok = p >= a.shift;  // slots of pairs that do not exist hold zeros
         const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
         if (a.winx_out)
           a.winx_out[((size_t)bh * Wr + slot) * 64 + col] = ok ? pair_x(a, b, h, j, col, pos) : z;
@@ -420,6 +421,7 @@ bool tc_f3a_supported(const FwdArgs& a) {
 int launch_tc_f3a(const FwdArgs& fa) {
   F3aArgs ta;
   ta.B = fa.B; ta.T = fa.T; ta.H = fa.H; ta.W = fa.W; ta.NC = (fa.T + kC - 1) / kC;
+  ta.shift = fa.shift;
   ta.eps = fa.eps; ta.eps_gamma = fa.eps_gamma;
   ta.beta = fa.beta; ta.lam = fa.lam; ta.pos_in = fa.pos_in;
   ta.kprev_in = reinterpret_cast<const __nv_bfloat16*>(fa.kprev_in);

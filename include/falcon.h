@@ -73,6 +73,15 @@ typedef enum {
 
 typedef enum { FALCON_BF16 = 0, FALCON_F32 = 1 } falcon_dtype_t;
 
+/* Which key a value is paired with.  PREFIX (the method): pair t is
+ * (phi(k_{t-1}), v_t) [FW 本质; JC 一个被忽略的时间差], x_0 the carried k_prev,
+ * and a pair with global index < 1 does not exist.  SAME_STEP (the ablation
+ * the pages set against it, the usual delta-rule pairing): pair t is
+ * (phi(k_t), v_t), every pair with global index >= 0 exists and k_prev is
+ * not read (it is still written to a carry).  Window rings hold zeros for
+ * pairs that do not exist. */
+typedef enum { FALCON_PAIR_PREFIX = 0, FALCON_PAIR_SAME_STEP = 1 } falcon_pairing_t;
+
 /* Kernel family for the chunk forward.  AUTO picks the tensor-core path
  * (tcgen05 + TMEM + TMA) when it supports the shape, else the portable
  * CUDA-core path.  GENERIC/TC force one (TC returns FALCON_ERR_UNSUPPORTED
@@ -99,6 +108,7 @@ typedef struct {
   int32_t variant;      /* falcon_variant_t */
   int32_t dtype;        /* falcon_dtype_t of q, k, v, o and the carried keys/values */
   int32_t impl;         /* falcon_impl_t (chunk forward only) */
+  int32_t pairing;      /* falcon_pairing_t (0 = prefix alignment) */
 } falcon_params_t;
 
 /* Decode carry: everything the next call needs to continue a sequence.
@@ -109,9 +119,10 @@ typedef struct {
  *   win_v  [B, H, W-1, dv] dtype  window ring of previous pairs' values (3/3A, W > 1)
  *   pos    [B, H]         int64  tokens consumed so far
  * The pair with global index p lives in ring slot p mod (W-1); slots whose
- * pair index is < 1 hold zeros.  As an input, a NULL carry (or NULL fields)
- * means a fresh sequence: S = 0, k_prev = 0, pos = 0; win_* may be NULL only
- * when pos <= 1 for every (b, h) (no earlier pair exists). */
+ * pair does not exist (p < 1; with same-step pairing p < 0) hold zeros.  As
+ * an input, a NULL carry (or NULL fields) means a fresh sequence: S = 0,
+ * k_prev = 0, pos = 0; win_* may be NULL only when no earlier pair exists
+ * (pos <= 1, with same-step pairing pos == 0) for every (b, h). */
 typedef struct {
   float* S;
   void* k_prev;

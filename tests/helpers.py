@@ -35,10 +35,11 @@ def params_for(F, w, T=None, impl=None):
     return F.Params(B=w.B, T=w.T if T is None else T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk,
                     window=w.window, eps=w.eps, eps_gamma=w.eps_gamma, variant=w.variant,
                     dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32,
-                    impl=F.FALCON_IMPL_AUTO if impl is None else impl)
+                    impl=F.FALCON_IMPL_AUTO if impl is None else impl,
+                    pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX)
 
 
 def oracle_full(w, x: dict, carry=None):
     xn = to_np(x)
     return oracle.recurrent(xn["q"], xn["k"], xn["v"], xn["beta"], xn["lam"], w.variant,
-                            w.window, w.eps, w.eps_gamma, carry=to_np(carry))
+                            w.window, w.eps, w.eps_gamma, carry=to_np(carry), pairing=w.pairing)

@@ -49,6 +49,7 @@ class Workload:
     force_zero_gamma: float = 0.0  # fraction of positions with gamma forced to 0
     eps: float = 1e-6
     eps_gamma: float = 1e-3
+    pairing: str = "prefix"       # "prefix" (x_t = k_{t-1}) or "same" (x_t = k_t, the ablation)
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -109,7 +110,8 @@ def make_carry(w: Workload, seed: int, pos: int | torch.Tensor, device="cpu",
     """A synthetic carry as if ``pos`` tokens were already consumed.
 
     S ~ N(0, 1/dk) (fp32), k_prev a unit feature, ring entries unit keys and
-    N(0,1) values in the dtype.  Ring slots whose pair index is < 1 are zero.
+    N(0,1) values in the dtype.  Ring slots whose pair does not exist (global
+    index < 1 with prefix alignment, < 0 with same-step pairing) are zero.
     """
     g = torch.Generator().manual_seed(seed)
     dt = torch_dtype(w.dtype)
@@ -126,12 +128,13 @@ def make_carry(w: Workload, seed: int, pos: int | torch.Tensor, device="cpu",
         wx = _unit_rows(torch.randn((w.B, w.H, Wr, w.dk), generator=g)).to(dt)
         wv = torch.randn((w.B, w.H, Wr, w.dv), generator=g).to(dt)
         # zero slots that hold no pair: slot s holds the pair p in
-        # [pos - Wr, pos - 1] with p mod Wr == s; it exists iff p >= 1
+        # [pos - Wr, pos - 1] with p mod Wr == s; it exists iff p >= first
+        first = 0 if w.pairing == "same" else 1
         for b in range(w.B):
             for h in range(w.H):
                 p0 = int(pos_t[b, h])
                 for p in range(p0 - Wr, p0):
-                    if p < 1:
+                    if p < first:
                         s = p % Wr
                         wx[b, h, s] = 0
                         wv[b, h, s] = 0
