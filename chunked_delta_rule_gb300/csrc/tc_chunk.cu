@@ -32,6 +32,7 @@
 
 #include <cuda.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -344,7 +345,7 @@ struct WyuSmem {
 };
 
 template <bool SOLVE>
-__global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUtensorMap tm_k,
+__global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                      const __grid_constant__ CUtensorMap tm_v,
                                                      TcArgs a) {
   using L = WyuSmem;
@@ -365,9 +366,7 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chunk = blockIdx.x, bh = blockIdx.y;
-  const int b = bh / a.H, h = bh % a.H;
-  const int t0 = chunk * kC;
+  const int n_items = a.NC * a.B * a.H;  // work item = (b, h, chunk), chunk fastest
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -382,19 +381,35 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
   }
   __syncthreads();
   tc_fence_after();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar[0], 16384);
-    tma_load_4d(Vs, &tm_v, &bar[0], 0, h, t0, b);
-    tma_load_4d(Xs, &tm_k, &bar[0], 0, h, t0 - a.shift, b);
-  }
-  // gates while the tiles are in flight: row tid <-> step t0 + tid
-  {
+  const uint32_t tmem = SOLVE ? *tmem_slot : 0u;
+  // the tiles and gate inputs of an item are fetched while the previous item
+  // finishes: TMA into the tile buffers once the products that read them are
+  // done, lambda and beta into registers
+  int issued = 0;  // tile loads issued (thread 0); item `it` waits for the it-th
+  auto fetch = [&](int item, float& ell, float& beta) {
+    const int chunk = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
+    if (tid == 0) {
+      ++issued;
+      mbar_arrive_expect_tx(&bar[0], 16384);
+      tma_load_4d(Vs, &tm_v, &bar[0], 0, h, t0, b);
+      tma_load_4d(Xs, &tm_k, &bar[0], 0, h, t0 - a.shift, b);
+    }
     const int t = t0 + tid;
     const bool step_ok = tid < 64 && t < a.T;
     const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
     const bool exists = step_ok && (pos + t >= a.shift);
     const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
-    const float ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
+    ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
+    beta = exists ? a.beta[gi] : 0.f;
+  };
+  float ell_n = 0.f, beta_n = 0.f;
+  if (blockIdx.x < n_items) fetch(blockIdx.x, ell_n, beta_n);
+  int it = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+  const int chunk = item % a.NC, bh = item / a.NC;
+  const int next = item + gridDim.x;
+  const float ell = ell_n, beta = beta_n;
+  {  // gates: row tid <-> step chunk * 64 + tid
     float g = ell;  // inclusive prefix sum over the chunk
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -402,7 +417,6 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
       if (lane >= o) g += n;
     }
     if (lane == 31) wsum[warp] = g;
-    const float beta = exists ? a.beta[gi] : 0.f;
     __syncthreads();
     if (warp == 1) g += wsum[0];
     if (tid < 64) {
@@ -410,7 +424,7 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
       bs[tid] = beta;
     }
   }
-  if (!mbar_wait(&bar[0], 0)) {
+  if (!mbar_wait(&bar[0], (uint32_t)(it & 1))) {
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
   }
@@ -422,7 +436,6 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
   const size_t ci = (size_t)bh * a.NC + chunk;
   uint8_t* Wo = a.ws_T + ci * 16384;  // W image, then the U image 8 KB further
   float* go = a.ws_g + ci * 128;
-  const uint32_t tmem = SOLVE ? *tmem_slot : 0u;
   if (SOLVE && !aborted && tid == 0) {  // Gram matrix X X^T (M = 64: row r in lane 32 (r / 16) + r % 16)
     tc_fence_after();
     mma_chain(tmem, Xs, 64, Xs, 64, 64, idesc_bf16(64, 64), false);
@@ -471,7 +484,10 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
         *reinterpret_cast<uint4*>(Wo + 8192 + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
-    return;
+    __syncthreads();  // the tiles are read
+    if (__syncthreads_or(*abort_flag)) break;
+    if (next < n_items) fetch(next, ell_n, beta_n);
+    continue;
   }
 
   if (!aborted && !mbar_wait(&bar[1], 0)) {
@@ -626,6 +642,7 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
     atomicExch(a.status, kStatusTimeout);
   }
   tc_fence_after();
+  if (next < n_items && !*abort_flag) fetch(next, ell_n, beta_n);  // the tiles are read
   {  // rows 0..63: U (columns 0..63); rows 64..127: W (columns 64..127)
     float rv[64];
     tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + (warp < 2 ? 0 : 64), rv);
@@ -647,8 +664,12 @@ __global__ void __launch_bounds__(128) tc_wyu_kernel(const __grid_constant__ CUt
     }
   }
   tc_fence_before();
+  if (__syncthreads_or(*abort_flag)) break;
+  }  // items
+  if (tid == 0 && issued > it) mbar_wait(&bar[0], (uint32_t)(it & 1));  // a load still in flight
+  tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (SOLVE && warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 128);
   }
@@ -1393,6 +1414,21 @@ WsLayout ws_layout(int B, int T, int H, int chunk) {
   return w;
 }
 
+// Streaming multiprocessors of the current device (looked up once per device).
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <int DK, int NV, bool SOLVE>
 int launch_t(const FwdArgs& fa, const TcArgs& ta) {
   const int BH = fa.B * fa.H;
@@ -1406,7 +1442,9 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       const size_t smem = WyuSmem::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
-      dim3 grid(ta.NC, BH);
+      // persistent: four CTAs per SM (shared memory and TMEM both allow four)
+      const long items = (long)ta.NC * BH;
+      dim3 grid((unsigned)std::min<long>(items, 4L * sm_count()));
       record_event(fa, 0);
       k<<<grid, 128, smem, fa.stream>>>(mk, mv, ta);
       record_event(fa, 1);
