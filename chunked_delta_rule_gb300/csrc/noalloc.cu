@@ -14,8 +14,8 @@
 
 namespace {
 
-// 32 MiB: enough for B * H * ceil(T / 64) <= 3855 chunks of the tensor-core
-// path (8 KB of T image + 512 B of gates per chunk, plus a 256-byte status
+// 32 MiB: enough for B * H * ceil(T / 64) <= 1927 chunks of the tensor-core
+// path (16 KB of bf16 images + 1 KB of gates per chunk, plus a 256-byte status
 // word).  Every device that loads the library holds this array until exit.
 constexpr size_t kScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];

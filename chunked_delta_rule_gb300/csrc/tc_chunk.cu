@@ -46,6 +46,7 @@ using namespace tcu;
 
 namespace {
 
+constexpr int kGateF = 256;      // fp32 gate slot per chunk in the workspace
 constexpr int kLD = 68;          // fp32 row stride of the solve buffers (bank spread)
 constexpr int kYL = 24;          // row stride of the 16x16 scratch blocks
 
@@ -63,7 +64,7 @@ struct TcArgs {
   __nv_bfloat16* kprev_out;
   int64_t* pos_out;
   uint8_t* ws_T;      // [B*H*NC][16384]: bf16 swizzled images, d = 64: W | U; d = 128: T diag(eta) | T diag(eta Gamma)
-  float* ws_g;        // [B*H*NC][128]: eta[64], g[64]
+  float* ws_g;        // [B*H*NC][kGateF]: d = 64: Gamma, exp(g_last - g), g, exp(g - g_block); d = 128: eta, g
   uint32_t* status;   // workspace status word
 };
 
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
     }
     const float eta = exists ? beta / (a.eps + n) : 0.f;
     if (chunk < a.NC && !aborted) {
-      float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * 128;
+      float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * kGateF;
       go[rl] = eta;
       go[64 + rl] = g;
     }
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
       *reinterpret_cast<uint4*>(To + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
       *reinterpret_cast<uint4*>(To + 8192 + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
     }
-    float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * 128;
+    float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * kGateF;
     go[rl] = eta;
     go[64 + rl] = g;
   }
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
   const bool aborted = *abort_flag != 0;
   const size_t ci = (size_t)bh * a.NC + chunk;
   uint8_t* Wo = a.ws_T + ci * 16384;  // W image, then the U image 8 KB further
-  float* go = a.ws_g + ci * 128;
+  float* go = a.ws_g + ci * kGateF;
   if (SOLVE && !aborted && tid == 0) {  // Gram matrix X X^T (M = 64: row r in lane 32 (r / 16) + r % 16)
     tc_fence_after();
     mma_chain(tmem, Xs, 64, Xs, 64, 64, idesc_bf16(64, 64), false);
@@ -460,9 +461,11 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     es[tid] = eta;
     cfs[tid] = __expf(gs[tid | 15] - g);  // exp(g_end(J) - g_r), J the row's 16-block
     gms[tid] = __expf(g);
-    if (!SOLVE && !aborted) {
-      go[tid] = eta;
-      go[64 + tid] = g;
+    if (!aborted) {  // gates of the sequential kernel
+      go[tid] = gms[tid];
+      go[64 + tid] = __expf(gs[63] - g);
+      go[128 + tid] = g;
+      go[192 + tid] = __expf(g - gs[tid & ~15]);  // decay from the 16-block start
     }
   }
   __syncthreads();
@@ -657,10 +660,7 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
         for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(rv[8 * j + 2 * e], rv[8 * j + 2 * e + 1]);
         *reinterpret_cast<uint4*>(dst + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      if (tid < 64) {
-        go[tid] = es[tid];
-        go[64 + tid] = gs[tid];
-      }
+
     }
   }
   tc_fence_before();
@@ -751,7 +751,7 @@ __global__ void __launch_bounds__(256, 1)
     tma_load_4d(Vst(s), &tm_v, &full[s], c0, h, c * kC, b);
     const size_t ci = (size_t)bh * NC + c;
     if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 16384, 16384, &full[s]);
-    bulk_load(Gst(s), a.ws_g + ci * 128, 512, &full[s]);
+    bulk_load(Gst(s), a.ws_g + ci * kGateF, 512, &full[s]);
   };
 
   if (tid == 0) {
@@ -1031,36 +1031,39 @@ __global__ void __launch_bounds__(256, 1)
 
 // ----------------------------------------------------------------------
 // (b') pipelined sequential kernel, d_k = d_v = 64.  W, U and the gates of
-// every chunk come from the per-chunk kernel; three roles:
+// every chunk come from the per-chunk kernel; four roles:
 //   warp 8      producer: TMA of chunk c into one of NST stages
-//   warps 4..7  front: derived gates, P^T = [X ; X] Q^T (one 128-row product,
-//               each half of it read by two warps) -> decay-masked P~^T, and
+//   warps 4..7  front: P^T = [X ; X] Q^T (one 128-row product, each half of
+//               it read by two warps) -> decay-masked P~^T, and
 //               X~ = diag(exp(g_last - g)) X in place of X
-//   warps 0..3  back: the state chain [D1 ; Oa] = [W ; Q] S0,
-//               Delta = U - D1, [D2 ; Ob] = [X~ | P~^T]^T Delta,
-//               S1 = Gamma_last S0 + D2, O = diag(Gamma) Oa + Ob
-// The front works up to NST chunks ahead of the back.  Stage layout: X (then
-// X~) | X copy (then P~^T) | W | Q | U | gates, so that [X ; X], [W ; Q]
-// and [X~ | P~^T] are single operands.  Hand-offs are mbarriers: full/empty
-// and front-done per stage, MMA completions per role.
+//   warps 0, 1  state chain: [D1 ; Oa] = [W ; Q] S0, Delta = U - D1,
+//               [D2 ; Ob] = [X~ | P~^T]^T Delta, S1 = Gamma_last S0 + D2
+//   warps 2, 3  outputs: O = diag(Gamma) Oa + Ob from the TMEM of the chunk
+//               the chain has just finished (two TMEM buffers), TMA store
+// The front works up to NST chunks ahead of the chain; the output warps run
+// one chunk behind it, off the chain's critical path.  Stage layout: X (then
+// X~) | X copy (then P~^T) | W | Q | U | gates, so that [X ; X], [W ; Q] and
+// [X~ | P~^T] are single operands.  Hand-offs are mbarriers: full/empty and
+// front-done per stage, product completions, output-done per TMEM buffer.
 // ----------------------------------------------------------------------
 template <bool SOLVE>
 struct PipeSmem {
   static constexpr int NST = 4;
   static constexpr size_t XO = 0, PO = 8192, WO = 16384, QO = 24576, UO = 32768, GO = 40960;
-  static constexpr size_t DO = GO + 512;            // derived gates (gamma, dec, g, cf)
-  static constexpr size_t STAGE = (DO + 1024 + 1023) / 1024 * 1024;
-  static constexpr size_t SB = NST * STAGE;         // S rows (MN-major B)
-  static constexpr size_t DL = SB + 8192;           // Delta rows (MN-major B)
-  static constexpr size_t OST = DL + 8192;          // two output staging tiles
+  static constexpr size_t STAGE = GO + 1024;         // gates: Gamma, exp(g_last - g), g, exp(g - g_block)
+  static constexpr size_t SB = NST * STAGE;          // S rows (MN-major B)
+  static constexpr size_t DL = SB + 8192;            // Delta rows (MN-major B)
+  static constexpr size_t OST = DL + 8192;           // two output staging tiles
   static constexpr size_t BAR = OST + 2 * 8192;
-  static constexpr size_t MISC = BAR + 128;
+  static constexpr size_t MISC = BAR + 160;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
-  static constexpr uint32_t TX = 3 * 8192 + (SOLVE ? 8192 : 0) + 8192 + 512;
+  static constexpr uint32_t TX = 3 * 8192 + (SOLVE ? 8192 : 0) + 8192 + 1024;
   static_assert(TOTAL <= 232448, "shared memory budget");
   static_assert(STAGE % 1024 == 0, "1 KB aligned stages");
-  // TMEM: P^T (M = 128 layout) | [D1 ; Oa] | [D2 ; Ob]
-  static constexpr uint32_t COL_PT = 0, COL_B1 = 64, COL_B2 = 128, NCOLS = 256;
+  // TMEM: P^T (M = 128 layout) | per buffer p: [D1 ; Oa] at 64 + 128 p, [D2 ; Ob] at 128 + 128 p
+  static constexpr uint32_t COL_PT = 0, NCOLS = 512;
+  __host__ __device__ static constexpr uint32_t col_b1(int p) { return 64 + 128 * p; }
+  __host__ __device__ static constexpr uint32_t col_b2(int p) { return 128 + 128 * p; }
   static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192;
 };
 
@@ -1074,10 +1077,12 @@ __global__ void __launch_bounds__(288, 1)
   constexpr int NST = L::NST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* full = bars;              // [NST]
-  uint64_t* empty = bars + NST;       // [NST]
+  uint64_t* empty = bars + NST;       // [NST]: the chain's thread 0 and the 64 output threads
   uint64_t* fdone = bars + 2 * NST;   // [NST]
   uint64_t* fmma = bars + 3 * NST;    // P^T done
-  uint64_t* bmma = fmma + 1;          // [2]: [D1 ; Oa] done, [D2 ; Ob] done
+  uint64_t* b1mma = fmma + 1;         // [D1 ; Oa] done
+  uint64_t* b2mma = fmma + 2;         // [2]: [D2 ; Ob] of buffer p done
+  uint64_t* odone = fmma + 4;         // [2]: output warps finished buffer p
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -1095,12 +1100,15 @@ __global__ void __launch_bounds__(288, 1)
     *abort_flag = 0;
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], 1 + 64);
       mbar_init(&fdone[i], 128);
     }
     mbar_init(fmma, 1);
-    mbar_init(&bmma[0], 1);
-    mbar_init(&bmma[1], 1);
+    mbar_init(b1mma, 1);
+    mbar_init(&b2mma[0], 1);
+    mbar_init(&b2mma[1], 1);
+    mbar_init(&odone[0], 64);
+    mbar_init(&odone[1], 64);
     fence_mbar_init();
   }
   if (!SOLVE) {  // additive write: the W rows of [W ; Q] stay zero
@@ -1135,7 +1143,7 @@ __global__ void __launch_bounds__(288, 1)
         tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
         if (SOLVE) bulk_load(st + L::WO, a.ws_T + ci * 16384, 8192, &full[s]);
         bulk_load(st + L::UO, a.ws_T + ci * 16384 + 8192, 8192, &full[s]);
-        bulk_load(st + L::GO, a.ws_g + ci * 128, 512, &full[s]);
+        bulk_load(st + L::GO, a.ws_g + ci * kGateF, 1024, &full[s]);
       }
       if (*abort_flag) {  // drain the loads still in flight
         for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
@@ -1152,19 +1160,11 @@ __global__ void __launch_bounds__(288, 1)
       const int s = c % NST;
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
       uint8_t* st = stage(s);
+      const float* gt = reinterpret_cast<const float*>(st + L::GO);
       if (c == 0 && a.kprev_in && a.shift && ftid < 64) {  // x_0 = carried key, in both copies of X
         const __nv_bfloat16 kv = a.kprev_in[(size_t)bh * 64 + ftid];
         *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = kv;
         *reinterpret_cast<__nv_bfloat16*>(st + L::PO + sw128(0, ftid)) = kv;
-      }
-      float* gt = reinterpret_cast<float*>(st + L::DO);
-      if (ftid < 64) {
-        const float* G = reinterpret_cast<const float*>(st + L::GO);
-        const float g = G[64 + ftid], glast = G[127];
-        gt[L::G_GAM + ftid] = __expf(g);
-        gt[L::G_DEC + ftid] = __expf(glast - g);
-        gt[L::G_GL + ftid] = g;
-        gt[L::G_CF + ftid] = __expf(g - G[64 + (ftid & ~15)]);  // decay from the 16-block start
       }
       fence_proxy_async();
       tc_fence_before();
@@ -1177,6 +1177,24 @@ __global__ void __launch_bounds__(288, 1)
                     ks > 0 ? 1u : 0u);
         umma_commit(fmma);
       }
+      // the factors of this thread's 32 columns, gathered while the product runs
+      const float* gl = gt + L::G_GL;
+      const float* cf = gt + L::G_CF;
+      const float gi = gl[r], cfr = cf[r];
+      const int I = r >> 4;
+      const bool ratio_ok = cfr > 1e-30f;
+      float cfv[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(cf + 32 * half + i);
+        cfv[i] = c4.x; cfv[i + 1] = c4.y; cfv[i + 2] = c4.z; cfv[i + 3] = c4.w;
+      }
+      float f[2];
+#pragma unroll
+      for (int J2 = 0; J2 < 2; ++J2) {
+        const int J = 2 * half + J2;
+        f[J2] = J > I ? __expf(gl[16 * J] - gi) : (J == I && ratio_ok ? __fdividef(1.f, cfr) : 0.f);
+      }
       if (!mbar_wait(fmma, fph)) fail();
       fph ^= 1;
       tc_fence_after();
@@ -1184,23 +1202,6 @@ __global__ void __launch_bounds__(288, 1)
          // exp(g_t - g_r) = cf_t exp(g_{16 J} - g_r) across blocks and cf_t / cf_r inside one
         uint32_t pr[32];
         tmem_ld32(tmem + lane_off + L::COL_PT + 32 * half, pr);
-        const float* gl = gt + L::G_GL;
-        const float* cf = gt + L::G_CF;
-        const float gi = gl[r], cfr = cf[r];
-        const int I = r >> 4;
-        const bool ratio_ok = cfr > 1e-30f;
-        float cfv[32];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 c4 = *reinterpret_cast<const float4*>(cf + 32 * half + i);
-          cfv[i] = c4.x; cfv[i + 1] = c4.y; cfv[i + 2] = c4.z; cfv[i + 3] = c4.w;
-        }
-        float f[2];
-#pragma unroll
-        for (int J2 = 0; J2 < 2; ++J2) {
-          const int J = 2 * half + J2;
-          f[J2] = J > I ? __expf(gl[16 * J] - gi) : (J == I && ratio_ok ? __fdividef(1.f, cfr) : 0.f);
-        }
         tmem_wait_ld();
         float pv[32];
 #pragma unroll
@@ -1255,18 +1256,16 @@ __global__ void __launch_bounds__(288, 1)
     if (a.kprev_out && !*abort_flag && ftid < 64)
       a.kprev_out[(size_t)bh * 64 + ftid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + ftid];
     if (a.pos_out && !*abort_flag && ftid == 0) a.pos_out[bh] = (a.pos_in ? a.pos_in[bh] : 0) + a.T;
-  } else {
-    // ------------------------------------------------------------ back
-    // warps 0, 1: S rows 32 w + lane (lanes 0..63 of the stacked products);
-    // warps 2, 3: output rows 32 (w - 2) + lane (lanes 64..127)
+  } else if (warp < 2) {
+    // ------------------------------------------------------------ state chain
+    // S rows 32 w + lane (lanes 0..63 of the stacked products)
     uint8_t* SB = sm + L::SB;
     const uint32_t sS = smem_u32(SB);
-    const bool srow = warp < 2;
-    const int r = 32 * (warp & 1) + lane;
+    const int r = 32 * warp + lane;
     float sreg[64];
 #pragma unroll
     for (int n = 0; n < 64; ++n) sreg[n] = 0.f;
-    if (srow && a.S_in) {
+    if (a.S_in) {
       const float* src = a.S_in + ((size_t)bh * 64 + r) * 64;
 #pragma unroll
       for (int n = 0; n < 64; n += 4) {
@@ -1274,123 +1273,137 @@ __global__ void __launch_bounds__(288, 1)
         sreg[n] = v.x; sreg[n + 1] = v.y; sreg[n + 2] = v.z; sreg[n + 3] = v.w;
       }
     }
-    if (srow) store_row64(SB, r, sreg);
+    store_row64(SB, r, sreg);
     fence_proxy_async();
-    named_bar(2, 128);
-    uint32_t bph = 0;
+    named_bar(3, 64);
+    uint32_t b1ph = 0;
     for (int c = 0; c < NC; ++c) {
-      const int s = c % NST;
+      const int s = c % NST, p = c & 1;
       if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1))) fail();
       tc_fence_after();
       uint8_t* st = stage(s);
-      if (named_bar_any(2, 128, *abort_flag != 0)) break;
-      const float* gt = reinterpret_cast<const float*>(st + L::DO);
-      // the stage is handed back before the epilogues: keep their gates
-      const float gfac = srow ? gt[L::G_GAM + 63] : gt[L::G_GAM + r];
-      if (tid == 0) {  // [D1 ; Oa] = [W ; Q] S0
+      if (named_bar_any(3, 64, *abort_flag != 0)) break;
+      const float gl_ = reinterpret_cast<const float*>(st + L::GO)[L::G_GAM + 63];
+      if (tid == 0) {
+        // the output warps are done with this TMEM buffer (chunk c - 2)
+        if (c >= 2 && !mbar_wait(&odone[p], (uint32_t)(((c - 2) >> 1) & 1))) fail();
+        tc_fence_after();
+        // [D1 ; Oa] = [W ; Q] S0
         const uint32_t sA1 = smem_u32(st + L::WO);
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + L::COL_B1, kdesc<128>(sA1, ks), mndesc(sS, ks), idesc_bf16(128, 64, false, true),
+          umma_bf16(tmem + L::col_b1(p), kdesc<128>(sA1, ks), mndesc(sS, ks), idesc_bf16(128, 64, false, true),
                     ks > 0 ? 1u : 0u);
-        umma_commit(&bmma[0]);
+        umma_commit(b1mma);
       }
-      // Delta = U - W S0 (rows 0..63: warps 0, 1); the additive write has W = 0
-      // and feeds U to the second product directly
+      // Delta = U - W S0; the additive write has W = 0 and feeds U to the
+      // second product directly
       const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(st + L::UO);
       if (SOLVE) {
-        if (!mbar_wait(&bmma[0], bph)) fail();
+        uint4 uu[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) uu[j] = *reinterpret_cast<const uint4*>(st + L::UO + sw128(r, 8 * j));
+        if (!mbar_wait(b1mma, b1ph)) fail();
         tc_fence_after();
-        if (srow) {
+        uint32_t d1[2][32];
+        tmem_ld32(tmem + lane_off + L::col_b1(p), d1[0]);
+        tmem_ld32(tmem + lane_off + L::col_b1(p) + 32, d1[1]);
+        tmem_wait_ld();
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t d1[32];
-            tmem_ld32(tmem + lane_off + L::COL_B1 + 32 * hf, d1);
-            uint4 uu[4];
+        for (int j = 0; j < 8; ++j) {
+          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&uu[j]);
+          uint32_t pd[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              uu[j] = *reinterpret_cast<const uint4*>(st + L::UO + sw128(r, 32 * hf + 8 * j));
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&uu[j]);
-              uint32_t pd[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int n = 8 * j + 2 * e;
-                const float2 u2 = __bfloat1622float2(pu[e]);
-                pd[e] = pack_bf16(u2.x - __uint_as_float(d1[n]), u2.y - __uint_as_float(d1[n + 1]));
-              }
-              *reinterpret_cast<uint4*>(sm + L::DL + sw128(r, 32 * hf + 8 * j)) =
-                  make_uint4(pd[0], pd[1], pd[2], pd[3]);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int n = 8 * j + 2 * e;
+            const float2 u2 = __bfloat1622float2(pu[e]);
+            pd[e] = pack_bf16(u2.x - __uint_as_float(d1[n >> 5][n & 31]),
+                              u2.y - __uint_as_float(d1[(n + 1) >> 5][(n + 1) & 31]));
           }
+          *reinterpret_cast<uint4*>(sm + L::DL + sw128(r, 8 * j)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
         }
         fence_proxy_async();
         tc_fence_before();
-        named_bar(2, 128);
+        named_bar(3, 64);
         tc_fence_after();
       }
+      b1ph ^= 1;
       if (tid == 0) {  // [D2 ; Ob] = [X~ | P~^T] Delta, A MN-major over two atoms
         const uint32_t sA2 = smem_u32(st + L::XO);
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + L::COL_B2, sdesc_mn128_wide(sA2 + ks * 2048, 8192), mndesc(sDL, ks),
+          umma_bf16(tmem + L::col_b2(p), sdesc_mn128_wide(sA2 + ks * 2048, 8192), mndesc(sDL, ks),
                     idesc_bf16(128, 64, true, true), ks > 0 ? 1u : 0u);
-        umma_commit(&bmma[1]);
+        umma_commit(&b2mma[p]);
       }
-      uint8_t* Ost = sm + L::OST + (c & 1) * 8192;
-      bool okb = mbar_wait(&bmma[1], bph);
-      if (!SOLVE) okb = mbar_wait(&bmma[0], bph) && okb;
+      bool okb = mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1));
+      if (!SOLVE) okb = mbar_wait(b1mma, b1ph ^ 1) && okb;
       if (!okb) fail();
-      bph ^= 1;
       tc_fence_after();
-      if (tid == 0) mbar_arrive(&empty[s]);  // nothing reads this stage any more
-      if (srow) {  // S1 = Gamma_last S0 + D2
+      if (tid == 0) mbar_arrive(&empty[s]);  // the chain reads nothing more of this stage
+      {  // S1 = Gamma_last S0 + D2
+        uint32_t d2[2][32];
+        tmem_ld32(tmem + lane_off + L::col_b2(p), d2[0]);
+        tmem_ld32(tmem + lane_off + L::col_b2(p) + 32, d2[1]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t d2[32];
-          tmem_ld32(tmem + lane_off + L::COL_B2 + 32 * hf, d2);
-          tmem_wait_ld();
-#pragma unroll
-          for (int n = 0; n < 32; ++n) sreg[32 * hf + n] = gfac * sreg[32 * hf + n] + __uint_as_float(d2[n]);
-        }
+        for (int n = 0; n < 64; ++n) sreg[n] = gl_ * sreg[n] + __uint_as_float(d2[n >> 5][n & 31]);
         store_row64(SB, r, sreg);
-      } else {  // O = diag(Gamma) Oa + Ob
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t oa[32], ob[32];
-          tmem_ld32(tmem + lane_off + L::COL_B1 + 32 * hf, oa);
-          tmem_ld32(tmem + lane_off + L::COL_B2 + 32 * hf, ob);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int n = 8 * j + 2 * e;
-              pk[e] = pack_bf16(gfac * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
-                                gfac * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
-            }
-            *reinterpret_cast<uint4*>(Ost + sw128(r, 32 * hf + 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-        }
       }
       fence_proxy_async();
       tc_fence_before();
-      named_bar(2, 128);
+      named_bar(3, 64);
       tc_fence_after();
-      if (tid == 0) {
-        tma_store_4d(&tm_o, Ost, 0, h, c * kC, b);
-        bulk_commit();
-        bulk_wait_read1();  // the tile stored one chunk ago has left its buffer
-      }
     }
-    if (tid == 0) bulk_wait0();
-    if (!*abort_flag && srow && a.S_out) {
+    if (!*abort_flag && a.S_out) {
       float* dst = a.S_out + ((size_t)bh * 64 + r) * 64;
 #pragma unroll
       for (int n = 0; n < 64; n += 4)
         *reinterpret_cast<float4*>(dst + n) = make_float4(sreg[n], sreg[n + 1], sreg[n + 2], sreg[n + 3]);
     }
+  } else {
+    // ------------------------------------------------------------ outputs
+    // rows 32 (w - 2) + lane (lanes 64..127 of the stacked products)
+    const int r = 32 * (warp - 2) + lane;
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % NST, p = c & 1;
+      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1))) fail();
+      if (named_bar_any(4, 64, *abort_flag != 0)) break;
+      const float gr = reinterpret_cast<const float*>(stage(s) + L::GO)[L::G_GAM + r];
+      mbar_arrive(&empty[s]);  // this thread reads nothing more of the stage
+      if (!mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1))) fail();  // both products of the chunk
+      tc_fence_after();
+      uint8_t* Ost = sm + L::OST + p * 8192;
+      if (tid == 64) bulk_wait_read1();  // the tile stored from this buffer two chunks ago is out
+      named_bar(4, 64);
+      {  // O = diag(Gamma) Oa + Ob
+        uint32_t oa[2][32], ob[2][32];
+        tmem_ld32(tmem + lane_off + L::col_b1(p), oa[0]);
+        tmem_ld32(tmem + lane_off + L::col_b1(p) + 32, oa[1]);
+        tmem_ld32(tmem + lane_off + L::col_b2(p), ob[0]);
+        tmem_ld32(tmem + lane_off + L::col_b2(p) + 32, ob[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&odone[p]);  // the TMEM buffer is free
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int n = 8 * j + 2 * e;
+            pk[e] = pack_bf16(gr * __uint_as_float(oa[n >> 5][n & 31]) + __uint_as_float(ob[n >> 5][n & 31]),
+                              gr * __uint_as_float(oa[(n + 1) >> 5][(n + 1) & 31]) +
+                                  __uint_as_float(ob[(n + 1) >> 5][(n + 1) & 31]));
+          }
+          *reinterpret_cast<uint4*>(Ost + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      fence_proxy_async();
+      named_bar(4, 64);
+      if (tid == 64) {
+        tma_store_4d(&tm_o, Ost, 0, h, c * kC, b);
+        bulk_commit();
+      }
+    }
+    if (tid == 64) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -1410,7 +1423,7 @@ WsLayout ws_layout(int B, int T, int H, int chunk) {
   w.status = 0;
   w.T = 256;
   w.g = w.T + (size_t)B * H * NC * 16384;
-  w.total = align_up(w.g + (size_t)B * H * NC * 512, 256);
+  w.total = align_up(w.g + (size_t)B * H * NC * kGateF * 4, 256);
   return w;
 }
 

@@ -174,7 +174,7 @@ int falcon_chunk_fwd_timed(const falcon_params_t* p, const void* q, const void* 
  * exits.  The call itself allocates nothing (no cudaMalloc/cudaFree).
  * Covered: Falcon-1 and Falcon-1A on the tensor-core path (bf16,
  * d_k = d_v in {64, 128}, chunk 64; see falcon_chunk_fwd_plan) needing at most
- * 32 MiB of scratch, i.e. B * H * ceil(T / 64) <= 3855.  Larger problems
+ * 32 MiB of scratch, i.e. B * H * ceil(T / 64) <= 1927.  Larger problems
  * return FALCON_ERR_WORKSPACE, other shapes FALCON_ERR_UNSUPPORTED (they
  * need no workspace: call falcon_chunk_fwd with workspace = NULL).
  * The first call on a device looks up the array's device address (which may

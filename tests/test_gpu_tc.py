@@ -1,8 +1,9 @@
 """Tensor-core chunk path (tcgen05 / TMEM / TMA): parity with the oracle when
 forced, agreement with the portable path, and a white-box check of the
 per-chunk WY stage and what it leaves in the workspace, with T = (I + A)^{-1}:
-d = 64, the bf16 images of W = T diag(eta Gamma) X and U = T diag(eta) V;
-d = 128, those of T diag(eta) and T diag(eta Gamma); the gates in both."""
+d = 64, the bf16 images of W = T diag(eta Gamma) X and U = T diag(eta) V and
+the decay gates of the sequential kernel; d = 128, the images of T diag(eta)
+and T diag(eta Gamma), eta and the in-chunk log-decay."""
 
 from __future__ import annotations
 
@@ -85,9 +86,16 @@ def test_wy_stage_workspace(F, d):
                 pairs = [(decode_T(img[:8192]), Tu_ref), (decode_T(img[8192:]), Tw_ref)]
             for got, ref in pairs:
                 assert np.abs(got - ref).max() <= 2e-2 * max(np.abs(ref).max(), 1e-30), (bh, c)
-            gates = wsn[g_off + ci * 512: g_off + (ci + 1) * 512].view(np.float32)
-            assert np.allclose(gates[:64], eta, rtol=2e-3, atol=1e-6), (bh, c)
-            assert np.allclose(gates[64:], g, rtol=1e-4, atol=1e-5), (bh, c)
+            gates = wsn[g_off + ci * 1024: g_off + (ci + 1) * 1024].view(np.float32)
+            if d == 64:  # Gamma, exp(g_last - g), g, exp(g - g at the start of the 16-row block)
+                assert np.allclose(gates[:64], np.exp(g), rtol=1e-4, atol=1e-6), (bh, c)
+                assert np.allclose(gates[64:128], np.exp(g[-1] - g), rtol=1e-4, atol=1e-6), (bh, c)
+                assert np.allclose(gates[128:192], g, rtol=1e-4, atol=1e-5), (bh, c)
+                assert np.allclose(gates[192:256], np.exp(g - g[np.arange(64) & ~15]), rtol=1e-4,
+                                   atol=1e-6), (bh, c)
+            else:  # eta, g
+                assert np.allclose(gates[:64], eta, rtol=2e-3, atol=1e-6), (bh, c)
+                assert np.allclose(gates[64:128], g, rtol=1e-4, atol=1e-5), (bh, c)
 
 
 @pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])

@@ -43,7 +43,7 @@ def test_noalloc_matches_workspace_entry_point_twice(F):
 
 
 def test_noalloc_rejects_what_it_cannot_cover(F):
-    w = Workload("noalloc_big", FALCON_1, 64, 4096, 16, 64, 64)   # 64*16*64 chunks > 3855
+    w = Workload("noalloc_big", FALCON_1, 64, 4096, 16, 64, 64)   # 64*16*64 chunks > 1927
     p = params_for(F, w)
     with pytest.raises(F.FalconError) as e:
         F.falcon_chunk_fwd_noalloc(p, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, None, 1 << 20,
