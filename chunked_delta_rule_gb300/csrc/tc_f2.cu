@@ -62,7 +62,7 @@ struct F2Smem {
   static constexpr size_t XQ = 0;
   static constexpr size_t VS = XQ + kSl * 16384;    // V slice, bf16 swizzled rows
   static constexpr size_t BS = VS + 8192;           // beta slice, fp32 [64][64]
-  static constexpr size_t LT = BS + 16384;          // L: diagonal 16x16 blocks fp32 [4][16][16] at +0,
+  static constexpr size_t LT = BS + 16384;          // L: diagonal 16x16 blocks fp32 [4][col][row] at +0,
                                                     // all of L as bf16 K-major rows at +8192
   static constexpr size_t PT = LT + 16384;          // P~, bf16 K-major rows t
   static constexpr size_t GT = PT + 8192;           // gates
@@ -222,20 +222,28 @@ __global__ void __launch_bounds__(256, 1)
         const bool ratio_ok = cfx > 1e-30f;
         const float inv = ratio_ok ? __fdividef(1.f, cfx) : 0.f;
         float w[64];
+        const float4* cf4 = reinterpret_cast<const float4*>(cfe);
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
-          if (J < I) {
-            const float rf = __expf(gx - gg[16 * J + 15]);
+          // row factor of block J: exp(g_x - g_end(J)) before the row's block, 1 / cf_x in it, 0 after
+          const float f = J < I ? __expf(gx - gg[16 * J + 15]) : (J == I ? inv : 0.f);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[16 * J + i] = rf * cfe[16 * J + i] * v[16 * J + i];
-          } else if (J == I) {
+          for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 c4 = cf4[4 * J + i4];
+            const int i = 16 * J + 4 * i4;
+            w[i] = f * c4.x * v[i];
+            w[i + 1] = f * c4.y * v[i + 1];
+            w[i + 2] = f * c4.z * v[i + 2];
+            w[i + 3] = f * c4.w * v[i + 3];
+          }
+        }
+        if (!ratio_ok) {  // exact exponentials inside the row's own block
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              w[16 * J + i] = ratio_ok ? inv * cfe[16 * J + i] * v[16 * J + i]
-                                       : __expf(gx - gg[16 * J + i]) * v[16 * J + i];
-          } else {
+          for (int J = 0; J < 4; ++J) {
+            if (J == I) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[16 * J + i] = 0.f;
+              for (int i = 0; i < 16; ++i) w[16 * J + i] = __expf(gx - gg[16 * J + i]) * v[16 * J + i];
+            }
           }
         }
         if (quad < 2) {  // Gram row r = x: 1 / (eps + |x_r|^2) and column r of L^T
@@ -248,14 +256,13 @@ __global__ void __launch_bounds__(256, 1)
           if (SOLVE) {  // row x of L: its diagonal block in fp32, the whole row in bf16
 #pragma unroll
             for (int i = 0; i < 64; ++i) w[i] = (i < x) ? w[i] : 0.f;
-            float* ld = reinterpret_cast<float*>(st + L::LT) + (I * 16 + (x & 15)) * 16;
+            // diagonal block transposed: [block][column i][row], so a column is contiguous
+            float* ld = reinterpret_cast<float*>(st + L::LT) + I * 256 + (x & 15);
 #pragma unroll
             for (int J = 0; J < 4; ++J) {
               if (J == I) {
 #pragma unroll
-                for (int i = 0; i < 16; i += 4)
-                  *reinterpret_cast<float4*>(ld + i) = make_float4(w[16 * J + i], w[16 * J + i + 1],
-                                                                   w[16 * J + i + 2], w[16 * J + i + 3]);
+                for (int i = 0; i < 16; ++i) ld[16 * i] = w[16 * J + i];
               }
             }
             store_row64(st + L::LT + 8192, x, w);
@@ -393,12 +400,22 @@ __global__ void __launch_bounds__(256, 1)
               for (int r = 0; r < 16; ++r) acc[16 * I + r] -= __uint_as_float(e[r]);
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-              const int R = 16 * I + r;
-              float sacc = acc[R];
+            float eb[16];  // eta of the block's rows for this channel
 #pragma unroll
-              for (int i = 0; i < r; ++i) sacc = fmaf(-ldiag[(I * 16 + r) * 16 + i], acc[16 * I + i], sacc);
-              acc[R] = bsl[R * 64 + j] * inv[R] * sacc;
+            for (int r = 0; r < 16; ++r) eb[r] = bsl[(16 * I + r) * 64 + j] * inv[16 * I + r];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {  // right-looking: Delta_i, then its share of the later rows
+              const float d = eb[i] * acc[16 * I + i];
+              acc[16 * I + i] = d;
+              const float* col = ldiag + I * 256 + 16 * i;  // L[16 I + r][16 I + i], r = 0..15
+#pragma unroll
+              for (int r4 = (i + 1) >> 2; r4 < 4; ++r4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(col + 4 * r4);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  if (4 * r4 + e > i) acc[16 * I + 4 * r4 + e] = fmaf(-lv[e], d, acc[16 * I + 4 * r4 + e]);
+              }
             }
             {  // this block of Delta^T (bf16) in both halves of the operand
               uint32_t pk[8];

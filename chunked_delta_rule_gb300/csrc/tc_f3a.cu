@@ -173,15 +173,23 @@ __global__ void __launch_bounds__(288, 1)
     // ------------------------------------------------------------ front
     const int ftid = tid - 128;
     uint32_t fph = 0;
+    // gate inputs of step c * 64 + ftid, loaded one chunk ahead
+    auto gate_in = [&](int c, float& lam, float& beta) {
+      const int tg = c * kC + ftid;
+      const bool ok = ftid < 64 && c < NC && tg < a.T;
+      const size_t gi = ((size_t)b * a.T + (ok ? tg : 0)) * a.H + h;
+      lam = ok ? a.lam[gi] : 0.f;
+      beta = ok ? a.beta[gi] : 0.f;
+    };
+    float lam_n, beta_n;
+    gate_in(0, lam_n, beta_n);
     for (int c = 0; c < NC; ++c) {
       const int s = c % NST;
       const int t0 = c * kC, j0 = t0 - W + 1;
-      // gate inputs of step t0 + ftid, loaded while the tiles arrive
-      const int tg = t0 + ftid;
-      const bool step_ok = ftid < 64 && tg < a.T;
-      const size_t gi = ((size_t)b * a.T + (step_ok ? tg : 0)) * a.H + h;
-      const float ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
-      const float beta = step_ok ? a.beta[gi] : 0.f;
+      const bool step_ok = ftid < 64 && t0 + ftid < a.T;
+      const float lam_c = lam_n, beta = beta_n;
+      gate_in(c + 1, lam_n, beta_n);
+      const float ell = step_ok ? clamped_log_decay(lam_c, a.eps_gamma) : 0.f;
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
       uint8_t* st = stage(s);
       float* gt = reinterpret_cast<float*>(st + L::GO);
