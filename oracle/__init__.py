@@ -10,3 +10,4 @@ from .falcon import (  # noqa: F401
     is_per_channel, is_windowed, masked_parallel, recurrent, recurrent_heads,
     step_coefficients,
 )
+from .falcon_grad import ONE_PAIR, recurrent_torch, recurrent_vjp  # noqa: F401,E402
