@@ -40,8 +40,9 @@ def parse():
     ap.add_argument("--workload", default="lm124m_f1_8x2048x12_d64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--mode", choices=["chunk", "decode"], default="chunk",
-                    help="decode: the recurrent one-token step (256 sequences x 12 heads)")
+    ap.add_argument("--mode", choices=["chunk", "decode", "backward"], default="chunk",
+                    help="decode: the recurrent one-token step (256 sequences x 12 heads); "
+                         "backward: the gradient of the chunk forward for the workload")
     ap.add_argument("--decode-variant", type=int, default=0)
     ap.add_argument("--pairing", choices=["prefix", "same"], default="prefix",
                     help="same: the same-step pairing ablation (x_t = k_t)")
@@ -284,6 +285,77 @@ def run_decode(args):
                                    "kernel": "recurrent_step_kernel"}}), flush=True)
 
 
+def run_backward(args, w):
+    """Backward of the chunk forward (dq, dk, dv, dbeta, dlambda from dO)
+    for the workload, 4 rotating input sets; one kernel per call."""
+    import torch
+
+    import chunked_delta_rule_gb300 as F
+    from workloads import make_cotangents, make_inputs
+    torch.cuda.set_device(0)
+    p = F.Params(B=w.B, T=w.T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk, eps=w.eps,
+                 eps_gamma=w.eps_gamma, variant=w.variant,
+                 dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32,
+                 pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX)
+    sets = []
+    for i in range(args.sets):
+        x = make_inputs(w, seed=w.seed + i, device="cuda")
+        x.update(make_cotangents(w, 50 + i, device="cuda", with_dS=False))
+        sets.append(x)
+    g = {n: torch.empty_like(sets[0][m]) for n, m in
+         (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dbeta", "beta"), ("dlam", "lam"))}
+    ws_n = F.falcon_backward_workspace_size(p)
+    ws = F.alloc_workspace(ws_n)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        x = sets[i % len(sets)]
+        F.falcon_backward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, x["dO"], None,
+                          g["dq"], g["dk"], g["dv"], g["dbeta"], g["dlam"], None, None, ws, ws_n,
+                          stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    es = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.T * w.H
+    beta = th * (w.dv if w.per_channel else 1) * 4
+    # q, k, v, dO in and dq, dk, dv out in the dtype; beta, lambda in and
+    # their gradients out in fp32
+    nbytes = th * (2 * w.dk + w.dv + w.dv) * es + th * (2 * w.dk + w.dv) * es + 2 * (beta + th * 4)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"metric": "Falcon chunked backward tokens/s", "value": w.B * w.T / (ms / 1e3),
+                      "unit": "tokens/s", "ms_per_step": ms, "steps": args.steps,
+                      "warmup": args.warmup, "higher_is_better": True,
+                      "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                      "config": {"workload": w.name + "_backward", "B": w.B, "T": w.T, "H": w.H,
+                                 "dk": w.dk, "dv": w.dv, "variant": w.variant,
+                                 "pairing": w.pairing, "l2": f"rotating {len(sets)} input sets"},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                   "frac": gbs / peak, "algorithmic_bytes": nbytes,
+                                   "kernel": "falcon_bwd_kernel",
+                                   "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+                      "gpu_launches": args.steps, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse()
     if args.mode == "decode":
@@ -292,6 +364,9 @@ def main():
     w = get_workload(args.workload)
     if args.pairing == "same":
         w = w.with_(name=w.name + "_same_step", pairing="same")
+    if args.mode == "backward":
+        run_backward(args, w)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

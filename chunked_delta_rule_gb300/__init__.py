@@ -26,7 +26,7 @@ EXPORTED = [
     "falcon_workspace_size", "falcon_chunk_fwd", "falcon_recurrent_step",
     "falcon_masked_parallel_workspace_size", "falcon_masked_parallel_ref_gpu",
     "falcon_strerror", "falcon_version", "falcon_chunk_fwd_plan", "falcon_chunk_fwd_timed",
-    "falcon_chunk_fwd_noalloc",
+    "falcon_chunk_fwd_noalloc", "falcon_backward_workspace_size", "falcon_backward",
 ]
 
 
@@ -79,6 +79,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.falcon_chunk_fwd_noalloc.restype = ctypes.c_int
     lib.falcon_chunk_fwd_plan.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.falcon_chunk_fwd_plan.restype = ctypes.c_int
+    lib.falcon_backward_workspace_size.argtypes = [P]
+    lib.falcon_backward_workspace_size.restype = S
+    lib.falcon_backward.argtypes = [P, V, V, V, V, V, C, V, V, V, V, V, V, V, V, V, V, S, V]
+    lib.falcon_backward.restype = ctypes.c_int
     lib.falcon_strerror.argtypes = [ctypes.c_int]
     lib.falcon_strerror.restype = ctypes.c_char_p
     lib.falcon_version.argtypes = []
@@ -231,6 +235,23 @@ def falcon_masked_parallel_ref_gpu(p: Params, q, k, v, beta, lam, o, S_final, wo
     _check(code, "falcon_masked_parallel_ref_gpu")
 
 
+def falcon_backward_workspace_size(p: Params) -> int:
+    return int(load_library().falcon_backward_workspace_size(ctypes.byref(p.c())))
+
+
+def falcon_backward(p: Params, q, k, v, beta, lam, carry_in: dict | None, dO, dS_final, dq, dk, dv,
+                    dbeta, dlam, dS_in, dk_prev, workspace, workspace_bytes: int = 0, stream=None):
+    lib = load_library()
+    ci = make_carry(carry_in)
+    if workspace is not None and not workspace_bytes and not isinstance(workspace, int):
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    code = lib.falcon_backward(ctypes.byref(p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam),
+                               ctypes.byref(ci) if ci is not None else None, _ptr(dO), _ptr(dS_final),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dlam), _ptr(dS_in),
+                               _ptr(dk_prev), _ptr(workspace), workspace_bytes, _stream(stream))
+    _check(code, "falcon_backward")
+
+
 # ---------------------------------------------------------------- tensor helpers
 def alloc_workspace(nbytes: int, device="cuda"):
     """A 256-byte aligned byte buffer (torch's caching allocator aligns to 512)."""
@@ -271,6 +292,26 @@ def masked_parallel(p: Params, q, k, v, beta, lam, stream=None):
     ws = alloc_workspace(ws_n, q.device)
     falcon_masked_parallel_ref_gpu(p, q, k, v, beta, lam, o, S, ws, ws_n, stream)
     return o, S
+
+
+
+def backward(p: Params, q, k, v, beta, lam, dO, dS_final=None, carry_in: dict | None = None,
+             stream=None) -> dict:
+    """Allocate the gradients / workspace with torch and call falcon_backward.
+
+    Returns dq, dk, dv, dbeta, dlam, and dS_in / dk_prev (gradients of the
+    carried state and key)."""
+    import torch
+    dev = q.device
+    g = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+         "dbeta": torch.empty_like(beta), "dlam": torch.empty_like(lam),
+         "dS_in": torch.empty((p.B, p.H, p.dk, p.dv), dtype=torch.float32, device=dev),
+         "dk_prev": torch.empty((p.B, p.H, p.dk), dtype=q.dtype, device=dev)}
+    ws_n = falcon_backward_workspace_size(p)
+    ws = alloc_workspace(ws_n, dev) if ws_n else None
+    falcon_backward(p, q, k, v, beta, lam, carry_in, dO, dS_final, g["dq"], g["dk"], g["dv"],
+                    g["dbeta"], g["dlam"], g["dS_in"], g["dk_prev"], ws, ws_n, stream)
+    return g
 
 
 load_library()

@@ -87,6 +87,10 @@ bool tc_f2_supported(const FwdArgs& a);
 int launch_tc_f2(const FwdArgs& a);
 bool tc_f3a_supported(const FwdArgs& a);
 int launch_tc_f3a(const FwdArgs& a);
+size_t backward_ws_bytes(int B, int T, int H, int d);
+bool backward_supported(int variant, int dk, int dv);
+int launch_backward(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk,
+                    void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

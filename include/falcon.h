@@ -222,6 +222,35 @@ int falcon_masked_parallel_ref_gpu(const falcon_params_t* p, const void* q, cons
                                    float* S_final, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* Bytes of workspace falcon_backward needs for these params (0 when the
+ * params are invalid or not covered). */
+size_t falcon_backward_workspace_size(const falcon_params_t* p);
+
+/* Gradient of the chunk forward, for training in the chunked framework
+ * [FW 三种等价形式; JC 三种视角看同一个更新] (the pages give the forward
+ * only; the backward is the chain rule through the update written at the
+ * top of this header).  For the loss L = <o, dO> + <S_T, dS_final> of
+ * falcon_chunk_fwd(p, q, k, v, beta, lambda, carry_in) it writes
+ *   dq, dk [B, T, H, dk], dv [B, T, H, dv] (the params' dtype),
+ *   dbeta (the shape of beta), dlambda [B, T, H] (fp32),
+ *   dS_in [B, H, dk, dv] fp32 (gradient of carry_in->S; may be NULL),
+ *   dk_prev [B, H, dk] dtype (gradient of carry_in->k_prev; may be NULL).
+ * dO has the shape and dtype of o; dS_final (fp32 [B, H, dk, dv]) may be NULL
+ * (zero).  carry_in supplies S, k_prev and pos as for the forward (NULL =
+ * fresh sequence); a key that no pair reads gets a zero gradient.  The decay
+ * clamp passes the gradient where eps_gamma <= 1 - lambda <= 1.  The
+ * forward is recomputed inside (states kept at every 64th step in the
+ * workspace), so o need not be saved.  Covered: Falcon-1, 1A, 2, 2A, both
+ * pairings, bf16 or fp32, d_k = d_v in {32, 64}, any T >= 0 (chunk and impl
+ * are ignored).  Gradients must not overlap inputs or one another.
+ * Errors: FALCON_ERR_INVALID_ARG, FALCON_ERR_UNSUPPORTED (Falcon-3/3A,
+ * other dims), FALCON_ERR_WORKSPACE, FALCON_ERR_CUDA. */
+int falcon_backward(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                    const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                    const void* dO, const float* dS_final, void* dq, void* dk, void* dv,
+                    float* dbeta, float* dlambda, float* dS_in, void* dk_prev, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
 /* Static description of an error code (never NULL). */
 const char* falcon_strerror(int code);
 

@@ -108,3 +108,43 @@ def test_workspace_size_is_deterministic(F):
     n2 = F.falcon_workspace_size(p)
     assert n1 == n2 and n1 % 256 == 0
     assert F.falcon_workspace_size(_p(F, dk=48)) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(variant=4, window=4), -2), (dict(variant=5, window=1), -2), (dict(dk=128, dv=128), -2),
+    (dict(dk=32, dv=64), -2), (dict(dk=16, dv=16), -2), (dict(variant=9), -1), (dict(T=-1), -1),
+])
+def test_backward_rejects_bad_params_on_host(F, kw, code):
+    p = _p(F, **kw)
+    fake = 1 << 20
+    with pytest.raises(F.FalconError) as e:
+        F.falcon_backward(p, fake, fake, fake, fake, fake, None, fake, None, 1 << 22, 1 << 23,
+                          1 << 24, 1 << 25, 1 << 26, None, None, 1 << 30, 1 << 30, 0)
+    assert e.value.code == code
+    assert F.falcon_backward_workspace_size(p) == 0
+
+
+def test_backward_workspace_and_overlap_checks(F):
+    p = _p(F, B=2, T=100, H=3)
+    n = F.falcon_backward_workspace_size(p)
+    # two 64-step blocks of start states + one block of recomputed states, per head
+    assert n == 2 * 3 * (2 + 64) * 64 * 64 * 4
+    assert F.falcon_backward_workspace_size(_p(F, T=0)) == 2 * 3 * 64 * 64 * 64 * 4
+    fake = 1 << 20
+    outs = [1 << 22, 1 << 23, 1 << 24, 1 << 25, 1 << 26]
+    with pytest.raises(F.FalconError) as e:  # workspace too small
+        F.falcon_backward(p, fake, fake, fake, fake, fake, None, fake, None, *outs, None, None,
+                          1 << 30, n - 1, 0)
+    assert e.value.code == -3
+    with pytest.raises(F.FalconError) as e:  # dq on top of q
+        F.falcon_backward(p, fake, 1 << 27, 1 << 28, 1 << 29, 1 << 21, None, 1 << 31, None, fake,
+                          *outs[1:], None, None, 1 << 32, n, 0)
+    assert e.value.code == -1
+    with pytest.raises(F.FalconError) as e:  # two gradients overlap
+        F.falcon_backward(p, fake, 1 << 27, 1 << 28, 1 << 29, 1 << 21, None, 1 << 31, None,
+                          1 << 22, 1 << 22, *outs[2:], None, None, 1 << 32, n, 0)
+    assert e.value.code == -1
+    with pytest.raises(F.FalconError) as e:  # null gradient with T > 0
+        F.falcon_backward(p, fake, fake, fake, fake, fake, None, fake, None, None, *outs[1:], None,
+                          None, 1 << 30, n, 0)
+    assert e.value.code == -1

@@ -146,6 +146,16 @@ def make_carry(w: Workload, seed: int, pos: int | torch.Tensor, device="cpu",
     return {n: t.contiguous().to(device) for n, t in out.items()}
 
 
+def make_cotangents(w: Workload, seed: int, device="cpu", with_dS: bool = True) -> dict:
+    """Cotangents for a backward pass: dO ~ N(0, 1) in the dtype (the shape
+    of o) and dS_final ~ N(0, 1/dk) fp32 (or None)."""
+    g = torch.Generator().manual_seed(seed)
+    dO = torch.randn((w.B, w.T, w.H, w.dv), generator=g).to(torch_dtype(w.dtype))
+    dS = torch.randn((w.B, w.H, w.dk, w.dv), generator=g) * (1.0 / w.dk) ** 0.5 if with_dS else None
+    out = {"dO": dO, "dS_final": dS}
+    return {n: (t.contiguous().to(device) if t is not None else None) for n, t in out.items()}
+
+
 def make_decode_inputs(variant: int, window: int = 8, B: int = DECODE_B, H: int = DECODE_H,
                        d: int = DECODE_D, seed: int = 5, pos: int = 64, dtype: str = "bf16",
                        device="cpu") -> tuple[dict, dict, Workload]:
