@@ -490,7 +490,9 @@ def main():
             pass
         hbm_peak = peaks.get("hbm_gbs", 6800.0)
         abytes = algorithmic_bytes(w)
-        if impl_used != F.FALCON_IMPL_TC:
+        if impl_used == F.FALCON_IMPL_SCAN:
+            names = ["window_scan_kernel"]
+        elif impl_used != F.FALCON_IMPL_TC:
             names = ["generic_chunk_kernel"]
         elif w.per_channel:
             names = ["tc_f2_kernel"]
@@ -505,6 +507,18 @@ def main():
         kernel = names[dom]
         achieved = kbytes[dom] / (kern_ms[dom] / 1e3) / 1e9
         step_achieved = abytes / (per_call_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak,
+                "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
+        if impl_used == F.FALCON_IMPL_SCAN:
+            # fp32 FMA pipes: 152 SMs x 128 lanes x 2 flop per clock at the
+            # sampled SM clock (CUDA cores; no tensor-core work on this path)
+            mhz = clk.get("sm_mhz") or 2070.0
+            alu_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
+            fl = algorithmic_flops(w) / (kern_ms[dom] / 1e3) / 1e12
+            roof = {"bound": "alu", "achieved": fl, "peak": alu_peak, "unit": "TFLOP/s",
+                    "frac": fl / alu_peak, "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 "
+                    "flop x SM clock", "hbm_achieved_gbs": achieved, "hbm_frac": achieved / hbm_peak}
         line = {
             "metric": "Falcon-1 chunked fwd tokens/s and % of roofline (GB300, T=2048, H=12, d=64)",
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -515,13 +529,10 @@ def main():
                        "chunk": w.chunk, "variant": "falcon1", "global_batch": w.B * world,
                        "seq_len": w.T, "parallelism": f"replicas x{world}",
                        "l2": f"rotating {len(sets)} input sets ({len(sets) * abytes / 1e6:.0f} MB)"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic_for(kernel),
-                         "kernel": kernel, "algorithmic_bytes": abytes,
-                         "algorithmic_flops": algorithmic_flops(w),
-                         "kernel_algorithmic_bytes": kbytes[dom],
-                         "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
-                         "step_achieved": step_achieved, "step_frac": step_achieved / hbm_peak},
+            "roofline": dict(roof, traffic=traffic_for(kernel), kernel=kernel,
+                             algorithmic_bytes=abytes, algorithmic_flops=algorithmic_flops(w),
+                             kernel_algorithmic_bytes=kbytes[dom], step_achieved=step_achieved,
+                             step_frac=step_achieved / hbm_peak),
             "kernels": [{"name": n, "ms": kern_ms[j], "share": kern_ms[j] / sum(kern_ms)}
                         for j, n in enumerate(names)],
             "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",

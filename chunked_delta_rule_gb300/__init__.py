@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "libfalcon.so")
 
 FALCON_1, FALCON_1A, FALCON_2, FALCON_2A, FALCON_3, FALCON_3A = range(6)
 FALCON_BF16, FALCON_F32 = 0, 1
-FALCON_IMPL_AUTO, FALCON_IMPL_GENERIC, FALCON_IMPL_TC = 0, 1, 2
+FALCON_IMPL_AUTO, FALCON_IMPL_GENERIC, FALCON_IMPL_TC, FALCON_IMPL_SCAN = 0, 1, 2, 3
 FALCON_PAIR_PREFIX, FALCON_PAIR_SAME_STEP = 0, 1
 FALCON_OK = 0
 

@@ -17,7 +17,7 @@ int check_params(const falcon_params_t* p, bool need_T_pos) {
   if (p->B < 1 || p->H < 1 || p->T < 0 || (need_T_pos && p->T < 1)) return FALCON_ERR_INVALID_ARG;
   if (p->variant < FALCON_1 || p->variant > FALCON_3A) return FALCON_ERR_INVALID_ARG;
   if (p->dtype != FALCON_BF16 && p->dtype != FALCON_F32) return FALCON_ERR_INVALID_ARG;
-  if (p->impl < FALCON_IMPL_AUTO || p->impl > FALCON_IMPL_TC) return FALCON_ERR_INVALID_ARG;
+  if (p->impl < FALCON_IMPL_AUTO || p->impl > FALCON_IMPL_SCAN) return FALCON_ERR_INVALID_ARG;
   if (p->pairing != FALCON_PAIR_PREFIX && p->pairing != FALCON_PAIR_SAME_STEP) return FALCON_ERR_INVALID_ARG;
   if (!(p->eps > 0.f) || !(p->eps_gamma > 0.f) || !(p->eps_gamma <= 1.f)) return FALCON_ERR_INVALID_ARG;
   if (!dim_ok(p->dk) || !dim_ok(p->dv)) return FALCON_ERR_UNSUPPORTED;
@@ -47,6 +47,19 @@ FwdArgs make_args(const falcon_params_t* p, const void* q, const void* k, const 
   return a;
 }
 
+// Kernel family for the chunk forward: the forced one, or for AUTO the
+// tensor-core path, then the window recurrence (Falcon-3), then the portable
+// chunk kernel.  -1: the forced family does not cover the params.
+int pick_impl(const falcon_params_t* p, const FwdArgs& a) {
+  const bool tc_ok = tc_chunk_supported(a), scan_ok = window_scan_supported(a);
+  switch (p->impl) {
+    case FALCON_IMPL_GENERIC: return FALCON_IMPL_GENERIC;
+    case FALCON_IMPL_TC: return tc_ok ? FALCON_IMPL_TC : -1;
+    case FALCON_IMPL_SCAN: return scan_ok ? FALCON_IMPL_SCAN : -1;
+    default: return tc_ok ? FALCON_IMPL_TC : scan_ok ? FALCON_IMPL_SCAN : FALCON_IMPL_GENERIC;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -68,7 +81,7 @@ const char* falcon_version(void) { return "falcon-gb300 0.1 sm_103a"; }
 size_t falcon_workspace_size(const falcon_params_t* p) {
   if (check_params(p, false) != FALCON_OK) return 0;
   FwdArgs a = make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
-  if (p->impl != FALCON_IMPL_GENERIC && tc_chunk_supported(a))
+  if (pick_impl(p, a) == FALCON_IMPL_TC)
     return tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant);
   return 0;
 }
@@ -106,9 +119,10 @@ static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k
   a.ws = workspace; a.ws_bytes = workspace_bytes;
   a.events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
   a.n_events = n_events;
-  const bool tc_ok = tc_chunk_supported(a);
-  if (p->impl == FALCON_IMPL_TC && !tc_ok) return FALCON_ERR_UNSUPPORTED;
-  if (p->impl != FALCON_IMPL_GENERIC && tc_ok) {
+  const int impl = pick_impl(p, a);
+  if (impl < 0) return FALCON_ERR_UNSUPPORTED;
+  if (impl == FALCON_IMPL_SCAN) return launch_window_scan(a);
+  if (impl == FALCON_IMPL_TC) {
     const size_t need = tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant);
     if (need > 0 && (!workspace || workspace_bytes < need ||
                      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0))
@@ -145,11 +159,10 @@ int falcon_chunk_fwd_plan(const falcon_params_t* p, int32_t* impl_out, int32_t* 
   int st = check_params(p, false);
   if (st != FALCON_OK) return st;
   FwdArgs a = make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
-  const bool tc_ok = tc_chunk_supported(a);
-  if (p->impl == FALCON_IMPL_TC && !tc_ok) return FALCON_ERR_UNSUPPORTED;
-  const bool tc = p->impl != FALCON_IMPL_GENERIC && tc_ok;
-  if (impl_out) *impl_out = tc ? FALCON_IMPL_TC : FALCON_IMPL_GENERIC;
-  if (launches_out) *launches_out = tc ? tc_chunk_launches(a) : 1;
+  const int impl = pick_impl(p, a);
+  if (impl < 0) return FALCON_ERR_UNSUPPORTED;
+  if (impl_out) *impl_out = impl;
+  if (launches_out) *launches_out = impl == FALCON_IMPL_TC ? tc_chunk_launches(a) : 1;
   return FALCON_OK;
 }
 

@@ -83,11 +83,21 @@ typedef enum { FALCON_BF16 = 0, FALCON_F32 = 1 } falcon_dtype_t;
 typedef enum { FALCON_PAIR_PREFIX = 0, FALCON_PAIR_SAME_STEP = 1 } falcon_pairing_t;
 
 /* Kernel family for the chunk forward.  AUTO picks the tensor-core path
- * (tcgen05 + TMEM + TMA) when it supports the shape, else the portable
- * CUDA-core path.  GENERIC/TC force one (TC returns FALCON_ERR_UNSUPPORTED
- * for shapes it does not cover).  The tensor-core path covers Falcon-1, 1A,
- * 2 and 2A with bf16 inputs, chunk 64 and d_k = d_v in {64, 128}. */
-typedef enum { FALCON_IMPL_AUTO = 0, FALCON_IMPL_GENERIC = 1, FALCON_IMPL_TC = 2 } falcon_impl_t;
+ * (tcgen05 + TMEM + TMA) when it supports the shape, else the window
+ * recurrence for Falcon-3 when it does, else the portable CUDA-core chunk
+ * path.  GENERIC, TC and SCAN force one (TC and SCAN return
+ * FALCON_ERR_UNSUPPORTED for shapes they do not cover).  The tensor-core
+ * path covers Falcon-1, 1A, 2 and 2A with bf16 inputs, chunk 64 and
+ * d_k = d_v in {64, 128}, and Falcon-3A with bf16, chunk 64, d = 64 and
+ * 2 <= window <= 16.  SCAN (Falcon-3, 2 <= window <= 8, d_k in {32, 64},
+ * d_v a multiple of 16, bf16 or fp32) walks the steps with the state's
+ * value columns spread over threads and ignores `chunk`. */
+typedef enum {
+  FALCON_IMPL_AUTO = 0,
+  FALCON_IMPL_GENERIC = 1,
+  FALCON_IMPL_TC = 2,
+  FALCON_IMPL_SCAN = 3
+} falcon_impl_t;
 
 enum {
   FALCON_OK = 0,
@@ -188,7 +198,7 @@ int falcon_chunk_fwd_noalloc(const falcon_params_t* p, const void* q, const void
                              void* stream);
 
 /* Which kernel family falcon_chunk_fwd uses for these params
- * (FALCON_IMPL_GENERIC or FALCON_IMPL_TC, written to *impl_out) and how many
+ * (FALCON_IMPL_GENERIC, FALCON_IMPL_TC or FALCON_IMPL_SCAN, written to *impl_out) and how many
  * kernels one call enqueues (*launches_out).  Host-only; either output
  * pointer may be NULL.  Returns FALCON_OK or the error the call would give
  * for these params. */

@@ -55,7 +55,8 @@ def _p(F, **kw):
     (dict(dk=48), -2), (dict(dv=256), -2), (dict(chunk=48), -2),
     (dict(variant=9), -1), (dict(dtype=7), -1), (dict(B=0), -1), (dict(T=-1), -1),
     (dict(eps=0.0), -1), (dict(eps_gamma=0.0), -1), (dict(eps_gamma=1.5), -1),
-    (dict(variant=4, window=0), -2), (dict(variant=4, window=65), -2), (dict(impl=3), -1),
+    (dict(variant=4, window=0), -2), (dict(variant=4, window=65), -2), (dict(impl=4), -1),
+    (dict(impl=3), -2),
 ])
 def test_chunk_fwd_rejects_bad_params_on_host(F, kw, code):
     p = _p(F, **kw)
