@@ -81,6 +81,8 @@ def kernel_bytes(w, names) -> list:
     if len(names) == 1:  # one kernel does the whole forward
         return [algorithmic_bytes(w)]
     state = w.B * w.H * w.dk * w.dv * 4
+    if names[0] == "window_prep_kernel":  # keys and gate inputs; then the whole forward
+        return [th * w.dk * es + beta + th * 4, algorithmic_bytes(w)]
     if names[0] == "tc_wyu_kernel":
         return [th * (w.dk + w.dv) * es + beta + th * 4, th * (2 * w.dk + w.dv) * es + state]
     wy = th * w.dk * es + beta + th * 4
@@ -491,7 +493,7 @@ def main():
         hbm_peak = peaks.get("hbm_gbs", 6800.0)
         abytes = algorithmic_bytes(w)
         if impl_used == F.FALCON_IMPL_SCAN:
-            names = ["window_scan_kernel"]
+            names = ["window_prep_kernel", "window_scan_kernel"]
         elif impl_used != F.FALCON_IMPL_TC:
             names = ["generic_chunk_kernel"]
         elif w.per_channel:

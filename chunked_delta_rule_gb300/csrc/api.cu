@@ -47,6 +47,13 @@ FwdArgs make_args(const falcon_params_t* p, const void* q, const void* k, const 
   return a;
 }
 
+bool aligned16(const FwdArgs& a) {
+  const void* ps[6] = {a.q, a.k, a.v, a.kprev_in, a.winx_in, a.winv_in};
+  for (const void* x : ps)
+    if (reinterpret_cast<uintptr_t>(x) & 15) return false;
+  return true;
+}
+
 // Kernel family for the chunk forward: the forced one, or for AUTO the
 // tensor-core path, then the window recurrence (Falcon-3), then the portable
 // chunk kernel.  -1: the forced family does not cover the params.
@@ -81,8 +88,9 @@ const char* falcon_version(void) { return "falcon-gb300 0.1 sm_103a"; }
 size_t falcon_workspace_size(const falcon_params_t* p) {
   if (check_params(p, false) != FALCON_OK) return 0;
   FwdArgs a = make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
-  if (pick_impl(p, a) == FALCON_IMPL_TC)
-    return tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant);
+  const int impl = pick_impl(p, a);
+  if (impl == FALCON_IMPL_TC) return tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant);
+  if (impl == FALCON_IMPL_SCAN) return window_scan_ws_bytes(p->B, p->T, p->H, a.W);
   return 0;
 }
 
@@ -119,9 +127,19 @@ static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k
   a.ws = workspace; a.ws_bytes = workspace_bytes;
   a.events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
   a.n_events = n_events;
-  const int impl = pick_impl(p, a);
+  int impl = pick_impl(p, a);
   if (impl < 0) return FALCON_ERR_UNSUPPORTED;
-  if (impl == FALCON_IMPL_SCAN) return launch_window_scan(a);
+  if (impl == FALCON_IMPL_SCAN && !aligned16(a)) {  // its 16-byte async copies need aligned rows
+    if (p->impl == FALCON_IMPL_SCAN) return FALCON_ERR_INVALID_ARG;
+    impl = FALCON_IMPL_GENERIC;
+  }
+  if (impl == FALCON_IMPL_SCAN) {
+    const size_t need = window_scan_ws_bytes(p->B, p->T, p->H, a.W);
+    if (need > 0 && (!workspace || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255) != 0))
+      return FALCON_ERR_WORKSPACE;
+    return launch_window_scan(a);
+  }
   if (impl == FALCON_IMPL_TC) {
     const size_t need = tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant);
     if (need > 0 && (!workspace || workspace_bytes < need ||
@@ -162,7 +180,8 @@ int falcon_chunk_fwd_plan(const falcon_params_t* p, int32_t* impl_out, int32_t* 
   const int impl = pick_impl(p, a);
   if (impl < 0) return FALCON_ERR_UNSUPPORTED;
   if (impl_out) *impl_out = impl;
-  if (launches_out) *launches_out = impl == FALCON_IMPL_TC ? tc_chunk_launches(a) : 1;
+  if (launches_out)
+    *launches_out = impl == FALCON_IMPL_TC ? tc_chunk_launches(a) : impl == FALCON_IMPL_SCAN ? 2 : 1;
   return FALCON_OK;
 }
 

@@ -88,6 +88,7 @@ int launch_tc_f2(const FwdArgs& a);
 bool tc_f3a_supported(const FwdArgs& a);
 int launch_tc_f3a(const FwdArgs& a);
 bool window_scan_supported(const FwdArgs& a);
+size_t window_scan_ws_bytes(int B, int T, int H, int W);
 int launch_window_scan(const FwdArgs& a);
 size_t backward_ws_bytes(int B, int T, int H, int d);
 bool backward_supported(int variant, int dk, int dv);

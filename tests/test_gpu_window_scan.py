@@ -144,3 +144,20 @@ def test_scan_full_size_sampled_heads(F):
         e_o = rel_err(o[b:b + 1, :, h:h + 1].float().cpu().numpy(), o_ref)
         e_s = rel_err(co["S"][b:b + 1, h:h + 1].cpu().numpy(), c_ref["S"])
         assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"], (b, h, e_o, e_s)
+
+
+def test_scan_misaligned_tensors(F):
+    """Rows not on a 16-byte boundary: AUTO takes the portable kernel (same
+    result), a forced SCAN is refused."""
+    w = wl(W=4, T=90, B=1, H=2, seed=951)
+    x = make_inputs(w, device="cuda")
+    q2 = torch.empty(x["q"].numel() + 1, dtype=x["q"].dtype, device="cuda")
+    q2[1:].copy_(x["q"].reshape(-1))
+    xq = dict(x, q=q2[1:].view(x["q"].shape))
+    assert xq["q"].data_ptr() % 16 != 0
+    o, co = run(F, w, xq, impl=F.FALCON_IMPL_AUTO)
+    o_ref, c_ref = oracle_full(w, x)
+    check(w, o, co, o_ref, c_ref)
+    with pytest.raises(F.FalconError) as e:
+        run(F, w, xq)
+    assert e.value.code == -1
