@@ -20,6 +20,7 @@ FALCON_1, FALCON_1A, FALCON_2, FALCON_2A, FALCON_3, FALCON_3A = range(6)
 FALCON_BF16, FALCON_F32 = 0, 1
 FALCON_IMPL_AUTO, FALCON_IMPL_GENERIC, FALCON_IMPL_TC, FALCON_IMPL_SCAN = 0, 1, 2, 3
 FALCON_PAIR_PREFIX, FALCON_PAIR_SAME_STEP = 0, 1
+FALCON_PROLOGUE_L2NORM_QK, FALCON_PROLOGUE_GATE_LOGITS = 1, 2
 FALCON_OK = 0
 
 EXPORTED = [
@@ -27,6 +28,7 @@ EXPORTED = [
     "falcon_masked_parallel_workspace_size", "falcon_masked_parallel_ref_gpu",
     "falcon_strerror", "falcon_version", "falcon_chunk_fwd_plan", "falcon_chunk_fwd_timed",
     "falcon_chunk_fwd_noalloc", "falcon_backward_workspace_size", "falcon_backward",
+    "falcon_varlen_workspace_size", "falcon_chunk_fwd_varlen",
 ]
 
 
@@ -41,7 +43,7 @@ class falcon_params_t(ctypes.Structure):
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
                 ("window", ctypes.c_int32), ("eps", ctypes.c_float), ("eps_gamma", ctypes.c_float),
                 ("variant", ctypes.c_int32), ("dtype", ctypes.c_int32), ("impl", ctypes.c_int32),
-                ("pairing", ctypes.c_int32)]
+                ("pairing", ctypes.c_int32), ("prologue", ctypes.c_int32)]
 
 
 class falcon_carry_t(ctypes.Structure):
@@ -79,6 +81,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.falcon_chunk_fwd_noalloc.restype = ctypes.c_int
     lib.falcon_chunk_fwd_plan.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.falcon_chunk_fwd_plan.restype = ctypes.c_int
+    lib.falcon_varlen_workspace_size.argtypes = [P]
+    lib.falcon_varlen_workspace_size.restype = S
+    lib.falcon_chunk_fwd_varlen.argtypes = [P, V, ctypes.c_int64, V, V, V, V, V, C, V, C, V, S, V]
+    lib.falcon_chunk_fwd_varlen.restype = ctypes.c_int
     lib.falcon_backward_workspace_size.argtypes = [P]
     lib.falcon_backward_workspace_size.restype = S
     lib.falcon_backward.argtypes = [P, V, V, V, V, V, C, V, V, V, V, V, V, V, V, V, V, S, V]
@@ -107,11 +113,12 @@ class Params:
     dtype: int = FALCON_BF16
     impl: int = FALCON_IMPL_AUTO
     pairing: int = FALCON_PAIR_PREFIX
+    prologue: int = 0
 
     def c(self) -> falcon_params_t:
         return falcon_params_t(self.B, self.T, self.H, self.dk, self.dv, self.chunk, self.window,
                                self.eps, self.eps_gamma, self.variant, self.dtype, self.impl,
-                               self.pairing)
+                               self.pairing, self.prologue)
 
 
 def _ptr(x) -> int | None:
@@ -235,6 +242,26 @@ def falcon_masked_parallel_ref_gpu(p: Params, q, k, v, beta, lam, o, S_final, wo
     _check(code, "falcon_masked_parallel_ref_gpu")
 
 
+def falcon_varlen_workspace_size(p: Params) -> int:
+    return int(load_library().falcon_varlen_workspace_size(ctypes.byref(p.c())))
+
+
+def falcon_chunk_fwd_varlen(p: Params, cu_seqlens, total_tokens: int, q, k, v, beta, lam,
+                            carry_in: dict | None, o, carry_out: dict | None, workspace,
+                            workspace_bytes: int = 0, stream=None):
+    lib = load_library()
+    ci = make_carry(carry_in)
+    co = make_carry(carry_out)
+    if workspace is not None and not workspace_bytes and not isinstance(workspace, int):
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    code = lib.falcon_chunk_fwd_varlen(ctypes.byref(p.c()), _ptr(cu_seqlens), int(total_tokens), _ptr(q),
+                                       _ptr(k), _ptr(v), _ptr(beta), _ptr(lam),
+                                       ctypes.byref(ci) if ci is not None else None, _ptr(o),
+                                       ctypes.byref(co) if co is not None else None, _ptr(workspace),
+                                       workspace_bytes, _stream(stream))
+    _check(code, "falcon_chunk_fwd_varlen")
+
+
 def falcon_backward_workspace_size(p: Params) -> int:
     return int(load_library().falcon_backward_workspace_size(ctypes.byref(p.c())))
 
@@ -281,6 +308,20 @@ def chunk_forward(p: Params, q, k, v, beta, lam, carry_in: dict | None = None, w
     ws_n = falcon_workspace_size(p)
     ws = alloc_workspace(ws_n, q.device) if ws_n else None
     falcon_chunk_fwd(p, q, k, v, beta, lam, carry_in, o, co, ws, ws_n, stream)
+    return o, co
+
+
+def chunk_forward_varlen(p: Params, cu_seqlens, q, k, v, beta, lam, carry_in: dict | None = None,
+                        want_carry=True, stream=None):
+    """Packed sequences: q, k [total, H, dk], v [total, H, dv], cu_seqlens int32
+    [B + 1] on the device; p.B = number of sequences, p.T >= the longest."""
+    import torch
+    total = q.shape[0]
+    o = torch.empty((total, p.H, p.dv), dtype=q.dtype, device=q.device)
+    co = empty_carry(p, q.device) if want_carry else None
+    ws_n = falcon_varlen_workspace_size(p)
+    ws = alloc_workspace(ws_n, q.device)
+    falcon_chunk_fwd_varlen(p, cu_seqlens, total, q, k, v, beta, lam, carry_in, o, co, ws, ws_n, stream)
     return o, co
 
 

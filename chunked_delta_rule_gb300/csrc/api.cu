@@ -23,6 +23,7 @@ int check_params(const falcon_params_t* p, bool need_T_pos) {
   if (!dim_ok(p->dk) || !dim_ok(p->dv)) return FALCON_ERR_UNSUPPORTED;
   if (p->chunk != 16 && p->chunk != 32 && p->chunk != 64) return FALCON_ERR_UNSUPPORTED;
   if (variant_windowed(p->variant) && (p->window < 1 || p->window > 64)) return FALCON_ERR_UNSUPPORTED;
+  if (p->prologue & ~(FALCON_PROLOGUE_L2NORM_QK | FALCON_PROLOGUE_GATE_LOGITS)) return FALCON_ERR_INVALID_ARG;
   return FALCON_OK;
 }
 
@@ -85,13 +86,43 @@ const char* falcon_strerror(int code) {
 
 const char* falcon_version(void) { return "falcon-gb300 0.1 sm_103a"; }
 
-size_t falcon_workspace_size(const falcon_params_t* p) {
-  if (check_params(p, false) != FALCON_OK) return 0;
+// workspace of the kernel family alone (no prologue buffers), 256-byte multiple
+static size_t kernel_ws_bytes(const falcon_params_t* p) {
   FwdArgs a = make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
   const int impl = pick_impl(p, a);
-  if (impl == FALCON_IMPL_TC) return tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant);
+  if (impl == FALCON_IMPL_TC) return align_up(tc_chunk_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->chunk, p->variant), 256);
   if (impl == FALCON_IMPL_SCAN) return window_scan_ws_bytes(p->B, p->T, p->H, a.W);
   return 0;
+}
+
+static size_t prologue_bytes(const falcon_params_t* p, bool with_o) {
+  return prologue_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, p->dtype, variant_per_channel(p->variant), with_o);
+}
+
+static bool ws_ok(const void* ws, size_t have, size_t need) {
+  return need == 0 || (ws && have >= need && (reinterpret_cast<uintptr_t>(ws) & 255) == 0);
+}
+
+static ProArgs pro_args(const falcon_params_t* p, const int32_t* cu, const void* q, const void* k,
+                        const void* v, const float* beta, const float* lambda) {
+  ProArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = p->B; a.T = p->T; a.H = p->H; a.dk = p->dk; a.dv = p->dv; a.dtype = p->dtype;
+  a.flags = p->prologue; a.perch = variant_per_channel(p->variant) ? 1 : 0;
+  a.cu = cu; a.q = q; a.k = k; a.v = v; a.beta = beta; a.lam = lambda;
+  return a;
+}
+
+size_t falcon_workspace_size(const falcon_params_t* p) {
+  if (check_params(p, false) != FALCON_OK) return 0;
+  if (pick_impl(p, make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr)) < 0) return 0;
+  return kernel_ws_bytes(p) + (p->prologue ? prologue_bytes(p, false) : 0);
+}
+
+size_t falcon_varlen_workspace_size(const falcon_params_t* p) {
+  if (check_params(p, false) != FALCON_OK) return 0;
+  if (pick_impl(p, make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr)) < 0) return 0;
+  return kernel_ws_bytes(p) + prologue_bytes(p, true);
 }
 
 static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k, const void* v,
@@ -101,6 +132,24 @@ static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k
   int st = check_params(p, false);
   if (st != FALCON_OK) return st;
   if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !o)) return FALCON_ERR_INVALID_ARG;
+  if (p->prologue) {  // phi / gate logits: one pass into the workspace, then the features path
+    if (pick_impl(p, make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr)) < 0)
+      return FALCON_ERR_UNSUPPORTED;
+    const size_t kws = kernel_ws_bytes(p);
+    if (!ws_ok(workspace, workspace_bytes, kws + prologue_bytes(p, false))) return FALCON_ERR_WORKSPACE;
+    ProArgs pa = pro_args(p, nullptr, q, k, v, beta, lambda);
+    prologue_carve(pa, reinterpret_cast<uint8_t*>(workspace) + kws, false, nullptr);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
+    if (ev && n_events > 0) cudaEventRecord(ev[0], s);
+    st = launch_prologue(pa, s);
+    if (st != FALCON_OK) return st;
+    falcon_params_t p0 = *p;
+    p0.prologue = 0;
+    return chunk_fwd_impl(&p0, pa.qo, pa.ko, pa.vo, pa.bo, pa.lo, carry_in, o, carry_out,
+                          kws ? workspace : nullptr, kws, stream, events ? events + 1 : nullptr,
+                          events ? n_events - 1 : 0);
+  }
   FwdArgs a = make_args(p, q, k, v, beta, lambda, o, stream);
   const size_t es = elem_size(p->dtype);
   const size_t BH = (size_t)p->B * p->H;
@@ -181,8 +230,40 @@ int falcon_chunk_fwd_plan(const falcon_params_t* p, int32_t* impl_out, int32_t* 
   if (impl < 0) return FALCON_ERR_UNSUPPORTED;
   if (impl_out) *impl_out = impl;
   if (launches_out)
-    *launches_out = impl == FALCON_IMPL_TC ? tc_chunk_launches(a) : impl == FALCON_IMPL_SCAN ? 2 : 1;
+    *launches_out = (impl == FALCON_IMPL_TC ? tc_chunk_launches(a) : impl == FALCON_IMPL_SCAN ? 2 : 1) +
+                    (p->prologue ? 1 : 0);
   return FALCON_OK;
+}
+
+int falcon_chunk_fwd_varlen(const falcon_params_t* p, const int32_t* cu_seqlens, int64_t total_tokens,
+                            const void* q, const void* k, const void* v, const float* beta,
+                            const float* lambda, const falcon_carry_t* carry_in, void* o,
+                            falcon_carry_t* carry_out, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  int st = check_params(p, false);
+  if (st != FALCON_OK) return st;
+  if (!cu_seqlens || total_tokens < 0 || total_tokens > (int64_t)p->B * p->T) return FALCON_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!q || !k || !v || !beta || !lambda || !o)) return FALCON_ERR_INVALID_ARG;
+  if (pick_impl(p, make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr)) < 0)
+    return FALCON_ERR_UNSUPPORTED;
+  const size_t kws = kernel_ws_bytes(p);
+  if (!ws_ok(workspace, workspace_bytes, kws + prologue_bytes(p, true))) return FALCON_ERR_WORKSPACE;
+  ProArgs pa = pro_args(p, cu_seqlens, q, k, v, beta, lambda);
+  void* o_pad = nullptr;
+  prologue_carve(pa, reinterpret_cast<uint8_t*>(workspace) + kws, true, &o_pad);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = launch_prologue(pa, s);
+  if (st != FALCON_OK) return st;
+  falcon_params_t p0 = *p;
+  p0.prologue = 0;
+  falcon_carry_t co_state;  // the dense pass gives the state; the rest depends on each length
+  std::memset(&co_state, 0, sizeof(co_state));
+  if (carry_out) co_state.S = carry_out->S;
+  st = chunk_fwd_impl(&p0, pa.qo, pa.ko, pa.vo, pa.bo, pa.lo, carry_in, o_pad, &co_state,
+                      kws ? workspace : nullptr, kws, stream, nullptr, 0);
+  if (st != FALCON_OK) return st;
+  return launch_varlen_finish(pa, o_pad, o, effective_window(p->variant, p->window),
+                              p->pairing == FALCON_PAIR_PREFIX ? 1 : 0, carry_in, carry_out, s);
 }
 
 int falcon_recurrent_step(const falcon_params_t* p, const void* q, const void* k, const void* v,
@@ -194,6 +275,7 @@ int falcon_recurrent_step(const falcon_params_t* p, const void* q, const void* k
   if (!q || !k || !v || !beta || !lambda || !o || !carry || !carry->S || !carry->k_prev || !carry->pos)
     return FALCON_ERR_INVALID_ARG;
   FwdArgs a = make_args(p, q, k, v, beta, lambda, o, stream);
+  a.prologue = p->prologue;
   if (a.W > 1 && (!carry->win_x || !carry->win_v)) return FALCON_ERR_INVALID_ARG;
   a.S_in = a.S_out = carry->S;
   a.kprev_in = a.kprev_out = carry->k_prev;
@@ -215,6 +297,7 @@ int falcon_masked_parallel_ref_gpu(const falcon_params_t* p, const void* q, cons
   int st = check_params(p, true);
   if (st != FALCON_OK) return st;
   if (!q || !k || !v || !beta || !lambda || !o || !S_final) return FALCON_ERR_INVALID_ARG;
+  if (p->prologue) return FALCON_ERR_UNSUPPORTED;  // takes features and gates
   const int W = effective_window(p->variant, p->window);
   if (p->T > 1024 || (size_t)p->T * W > 2048) return FALCON_ERR_UNSUPPORTED;
   const size_t need = masked_parallel_ws_bytes(p->B, p->T, p->H, p->dk, p->dv, W);
@@ -227,7 +310,8 @@ int falcon_masked_parallel_ref_gpu(const falcon_params_t* p, const void* q, cons
 }
 
 size_t falcon_backward_workspace_size(const falcon_params_t* p) {
-  if (check_params(p, false) != FALCON_OK || !backward_supported(p->variant, p->dk, p->dv)) return 0;
+  if (check_params(p, false) != FALCON_OK || !backward_supported(p->variant, p->dk, p->dv) || p->prologue)
+    return 0;
   return backward_ws_bytes(p->B, p->T, p->H, p->dk);
 }
 
@@ -238,7 +322,7 @@ int falcon_backward(const falcon_params_t* p, const void* q, const void* k, cons
                     size_t workspace_bytes, void* stream) {
   int st = check_params(p, false);
   if (st != FALCON_OK) return st;
-  if (!backward_supported(p->variant, p->dk, p->dv)) return FALCON_ERR_UNSUPPORTED;
+  if (!backward_supported(p->variant, p->dk, p->dv) || p->prologue) return FALCON_ERR_UNSUPPORTED;
   if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !dO || !dq || !dk || !dv || !dbeta || !dlambda))
     return FALCON_ERR_INVALID_ARG;
   const size_t need = backward_ws_bytes(p->B, p->T, p->H, p->dk);

@@ -66,7 +66,39 @@ struct FwdArgs {
   cudaStream_t stream;
   cudaEvent_t* events;      // optional: recorded before the first and after every kernel
   int n_events;
+  int prologue;             // falcon_prologue_t flags applied inside the kernel (recurrent step)
 };
+
+// Gates with the optional logit prologue: gamma = clamp(1 - lambda) or
+// clamp(sigmoid(-a)); beta or sigmoid(b).
+__device__ __forceinline__ float gate_gamma(float lam, float eps_gamma, int prologue) {
+  const float g = (prologue & FALCON_PROLOGUE_GATE_LOGITS) ? 1.f / (1.f + __expf(lam)) : 1.0f - lam;
+  return fminf(fmaxf(g, eps_gamma), 1.0f);
+}
+__device__ __forceinline__ float gate_beta(float b, int prologue) {
+  return (prologue & FALCON_PROLOGUE_GATE_LOGITS) ? 1.f / (1.f + __expf(-b)) : b;
+}
+
+// Inputs of the prologue / varlen gather and its dense outputs.
+struct ProArgs {
+  int B, T, H, dk, dv, dtype, flags, perch;
+  const int32_t* cu;        // NULL: dense rows (b, t) at b * T + t; else packed sequences
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* lam;
+  void* qo;
+  void* ko;
+  void* vo;
+  float* bo;
+  float* lo;
+};
+size_t prologue_ws_bytes(int B, int T, int H, int dk, int dv, int dtype, bool perch, bool with_o);
+void prologue_carve(ProArgs& a, void* base, bool with_o, void** o_pad);
+int launch_prologue(const ProArgs& a, cudaStream_t s);
+int launch_varlen_finish(const ProArgs& a, const void* o_pad, void* o, int W, int shift,
+                         const falcon_carry_t* ci, falcon_carry_t* co, cudaStream_t s);
 
 // Record the caller's event i on the stream (no-op without events).
 inline void record_event(const FwdArgs& a, int i) {

@@ -49,7 +49,7 @@ extern "C" int falcon_chunk_fwd_noalloc(const falcon_params_t* p, const void* q,
                                         falcon_carry_t* carry_out, void* stream) {
   // covered: the Falcon-1 / Falcon-1A tensor-core path (the kernels that keep
   // per-chunk images in the scratch)
-  if (p && p->variant != FALCON_1 && p->variant != FALCON_1A) return FALCON_ERR_UNSUPPORTED;
+  if (p && ((p->variant != FALCON_1 && p->variant != FALCON_1A) || p->prologue)) return FALCON_ERR_UNSUPPORTED;
   int32_t impl = 0;
   int st = falcon_chunk_fwd_plan(p, &impl, nullptr);
   if (st != FALCON_OK) return st;

@@ -25,6 +25,33 @@ __device__ __forceinline__ float ldv(const void* p, size_t i) {
   return to_f32(reinterpret_cast<const Tin*>(p)[i]);
 }
 
+// Scales of phi (per-token L2 normalisation) of q and k, by the first warp;
+// 1 without the prologue flag.
+template <typename Tin>
+__device__ __forceinline__ void phi_scales(const FwdArgs& a, size_t bhi, int tid, float* out2) {
+  if (!(a.prologue & FALCON_PROLOGUE_L2NORM_QK)) {
+    if (tid == 0) { out2[0] = 1.f; out2[1] = 1.f; }
+    return;
+  }
+  if (tid < 32) {
+    float sq = 0.f, sk = 0.f;
+    for (int d = tid; d < a.dk; d += 32) {
+      const float q = ldv<Tin>(a.q, bhi * a.dk + d), k = ldv<Tin>(a.k, bhi * a.dk + d);
+      sq = fmaf(q, q, sq);
+      sk = fmaf(k, k, sk);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    if (tid == 0) {
+      out2[0] = 1.f / fmaxf(sqrtf(sq), 1e-12f);
+      out2[1] = 1.f / fmaxf(sqrtf(sk), 1e-12f);
+    }
+  }
+}
+
 template <typename Tin, int EPT>
 __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) {
   extern __shared__ float4 smem_f4[];
@@ -57,6 +84,9 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
 
   const int64_t pos = a.pos_out[bhi];
   const int Wr = W - 1;
+  phi_scales<Tin>(a, bhi, tid, misc + 1);
+  __syncthreads();
+  const float sq = misc[1], sk = misc[2];
   // window slot w (oldest first): pair p = pos - (W-1) + w; the newest slot
   // is the current pair (x = k_prev, v = v_t)
   for (int i = tid; i < W * dk; i += kRecThreads) {
@@ -64,7 +94,7 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
     int64_t p = pos - Wr + w;
     float x = 0.f;
     if (p >= a.shift) {
-      if (w == Wr) x = a.shift ? ldv<Tin>(a.kprev_out, bhi * dk + d) : ldv<Tin>(a.k, bhi * dk + d);
+      if (w == Wr) x = a.shift ? ldv<Tin>(a.kprev_out, bhi * dk + d) : sk * ldv<Tin>(a.k, bhi * dk + d);
       else x = ldv<Tin>(a.winx_out, (bhi * Wr + ring_slot(p, Wr)) * dk + d);
     }
     xw[i] = x;
@@ -79,7 +109,7 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
     }
     vw[i] = x;
   }
-  for (int d = tid; d < dk; d += kRecThreads) qv[d] = ldv<Tin>(a.q, bhi * dk + d);
+  for (int d = tid; d < dk; d += kRecThreads) qv[d] = sq * ldv<Tin>(a.q, bhi * dk + d);
   for (int w = tid; w < W; w += kRecThreads) pv[w] = (pos - Wr + w >= a.shift) ? 1.f : 0.f;
   __syncthreads();
   // dot products x_j . q and ||x_j||^2: one warp per window slot
@@ -101,13 +131,13 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
   }
   __syncthreads();
   const bool perch = variant_per_channel(a.variant);
-  if (tid == 0) misc[0] = fminf(fmaxf(1.0f - a.lam[bhi], a.eps_gamma), 1.0f);
+  if (tid == 0) misc[0] = gate_gamma(a.lam[bhi], a.eps_gamma, a.prologue);
   for (int i = tid; i < (perch ? dv : 1); i += kRecThreads) {
     float n = 0.f, e = 0.f;
     for (int w = 0; w < W; ++w) { n += pv[w]; e += pv[w] * xn[w]; }
     float c = 0.f;
     if (n > 0.f) {
-      float bt = perch ? a.beta[bhi * dv + i] : a.beta[bhi];
+      float bt = gate_beta(perch ? a.beta[bhi * dv + i] : a.beta[bhi], a.prologue);
       c = bt / (a.eps + e / n) / n;
     }
     cf[i] = c;
@@ -171,7 +201,8 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
   }
   for (int d = tid; d < dk; d += kRecThreads)
     reinterpret_cast<Tin*>(a.kprev_out)[bhi * dk + d] =
-        reinterpret_cast<const Tin*>(a.k)[bhi * dk + d];
+        (a.prologue & FALCON_PROLOGUE_L2NORM_QK) ? from_f32<Tin>(sk * ldv<Tin>(a.k, bhi * dk + d))
+                                                  : reinterpret_cast<const Tin*>(a.k)[bhi * dk + d];
   if (tid == 0) a.pos_out[bhi] = pos + 1;
 }
 
@@ -191,6 +222,7 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
   __shared__ float qv[D];
   __shared__ float pv[MAXW], xq[MAXW], xn[MAXW];
   __shared__ float4 red[NW][MAXW + 1][NQ];
+  __shared__ float scl[2];
   const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cq = tid % NQ, rg = tid / NQ;
   const int W = a.W, Wr = W - 1;
@@ -201,13 +233,17 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
   for (int i = 0; i < RPT; ++i) s[i] = Sg[(size_t)(rg + RGS * i) * NQ + cq];
 
   const int64_t pos = a.pos_out[bhi];
+  phi_scales<Tin>(a, bhi, tid, scl);
+  __syncthreads();
+  const float sq = scl[0], sk = scl[1];
   for (int i = tid; i < W * D; i += NT) {
     const int w = i / D, d = i % D;
     const int64_t p = pos - Wr + w;
     float x = 0.f, v = 0.f;
     if (p >= a.shift) {
       if (w == Wr) {
-        x = to_f32(reinterpret_cast<const Tin*>(a.shift ? a.kprev_out : a.k)[bhi * D + d]);
+        x = a.shift ? to_f32(reinterpret_cast<const Tin*>(a.kprev_out)[bhi * D + d])
+                    : sk * to_f32(reinterpret_cast<const Tin*>(a.k)[bhi * D + d]);
         v = to_f32(reinterpret_cast<const Tin*>(a.v)[bhi * D + d]);
       } else {
         const size_t o = (bhi * Wr + ring_slot(p, Wr)) * D + d;
@@ -218,7 +254,7 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
     xw[w][d] = x;
     vw[w][d] = v;
   }
-  for (int d = tid; d < D; d += NT) qv[d] = to_f32(reinterpret_cast<const Tin*>(a.q)[bhi * D + d]);
+  for (int d = tid; d < D; d += NT) qv[d] = sq * to_f32(reinterpret_cast<const Tin*>(a.q)[bhi * D + d]);
   __syncthreads();
   for (int w = warp; w < W; w += NW) {  // x_j . q and ||x_j||^2
     float aq = 0.f, an = 0.f;
@@ -260,7 +296,7 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
   }
   __syncthreads();
   // every thread forms the writes of its own 4 columns
-  const float gamma = fminf(fmaxf(1.0f - a.lam[bhi], a.eps_gamma), 1.0f);
+  const float gamma = gate_gamma(a.lam[bhi], a.eps_gamma, a.prologue);
   const bool perch = variant_per_channel(a.variant);
   float n = 0.f, e = 0.f;
   for (int w = 0; w < W; ++w) { n += pv[w]; e += pv[w] * xn[w]; }
@@ -268,10 +304,12 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
   if (n > 0.f) {
     const float den = a.eps + e / n;
     if (perch) {
-      const float4 bt = reinterpret_cast<const float4*>(a.beta + bhi * D)[cq];
+      float4 bt = reinterpret_cast<const float4*>(a.beta + bhi * D)[cq];
+      bt = make_float4(gate_beta(bt.x, a.prologue), gate_beta(bt.y, a.prologue), gate_beta(bt.z, a.prologue),
+                       gate_beta(bt.w, a.prologue));
       cf = make_float4(bt.x / den / n, bt.y / den / n, bt.z / den / n, bt.w / den / n);
     } else {
-      const float c = a.beta[bhi] / den / n;
+      const float c = gate_beta(a.beta[bhi], a.prologue) / den / n;
       cf = make_float4(c, c, c, c);
     }
   }
@@ -327,7 +365,10 @@ __global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
     }
   }
   for (int d = tid; d < D; d += NT)
-    reinterpret_cast<Tin*>(a.kprev_out)[bhi * D + d] = reinterpret_cast<const Tin*>(a.k)[bhi * D + d];
+    reinterpret_cast<Tin*>(a.kprev_out)[bhi * D + d] =
+        (a.prologue & FALCON_PROLOGUE_L2NORM_QK)
+            ? from_f32<Tin>(sk * to_f32(reinterpret_cast<const Tin*>(a.k)[bhi * D + d]))
+            : reinterpret_cast<const Tin*>(a.k)[bhi * D + d];
   if (tid == 0) a.pos_out[bhi] = pos + 1;
 }
 

@@ -82,6 +82,23 @@ typedef enum { FALCON_BF16 = 0, FALCON_F32 = 1 } falcon_dtype_t;
  * pairs that do not exist. */
 typedef enum { FALCON_PAIR_PREFIX = 0, FALCON_PAIR_SAME_STEP = 1 } falcon_pairing_t;
 
+/* Steps either side of the path, done by the library when asked
+ * [FW 三种等价形式 (phi(Q), phi(K)); JC 把记忆更新变成一次梯度下降]:
+ * L2NORM_QK: q and k are raw projections; the feature map phi is the
+ *   per-token L2 normalisation x / max(|x|, 1e-12) (fp32, then the dtype).
+ *   Carried keys (k_prev, win_x) hold features phi(k).
+ * GATE_LOGITS: beta and lambda hold logits: beta = sigmoid(b) and
+ *   lambda = sigmoid(a), i.e. gamma = 1 - lambda = sigmoid(-a) before the
+ *   eps_gamma floor.
+ * The chunk forward applies them in one pass over the inputs into its
+ * workspace (falcon_workspace_size counts it), the varlen forward in its
+ * gather pass, the recurrent step inside its kernel.  The backward and the
+ * masked-parallel reference take features and gates (prologue must be 0). */
+typedef enum {
+  FALCON_PROLOGUE_L2NORM_QK = 1,
+  FALCON_PROLOGUE_GATE_LOGITS = 2
+} falcon_prologue_t;
+
 /* Kernel family for the chunk forward.  AUTO picks the tensor-core path
  * (tcgen05 + TMEM + TMA) when it supports the shape, else the window
  * recurrence for Falcon-3 when it does, else the portable CUDA-core chunk
@@ -121,6 +138,7 @@ typedef struct {
   int32_t dtype;        /* falcon_dtype_t of q, k, v, o and the carried keys/values */
   int32_t impl;         /* falcon_impl_t (chunk forward only) */
   int32_t pairing;      /* falcon_pairing_t (0 = prefix alignment) */
+  int32_t prologue;     /* falcon_prologue_t flags (0 = inputs are features and gates) */
 } falcon_params_t;
 
 /* Decode carry: everything the next call needs to continue a sequence.
@@ -184,7 +202,7 @@ int falcon_chunk_fwd_timed(const falcon_params_t* p, const void* q, const void* 
  * The scratch lives in a fixed 32 MiB array inside the library's device
  * image, held by every device that loads the library until the process
  * exits.  The call itself allocates nothing (no cudaMalloc/cudaFree).
- * Covered: Falcon-1 and Falcon-1A on the tensor-core path (bf16,
+ * Covered: Falcon-1 and Falcon-1A with prologue 0 on the tensor-core path (bf16,
  * d_k = d_v in {64, 128}, chunk 64; see falcon_chunk_fwd_plan) needing at most
  * 32 MiB of scratch, i.e. B * H * ceil(T / 64) <= 1927.  Larger problems
  * return FALCON_ERR_WORKSPACE, other shapes FALCON_ERR_UNSUPPORTED (they
@@ -198,6 +216,32 @@ int falcon_chunk_fwd_noalloc(const falcon_params_t* p, const void* q, const void
                              const void* v, const float* beta, const float* lambda,
                              const falcon_carry_t* carry_in, void* o, falcon_carry_t* carry_out,
                              void* stream);
+
+/* Bytes of workspace falcon_chunk_fwd_varlen needs for these params
+ * (p->B = number of sequences, p->T = their maximum length). */
+size_t falcon_varlen_workspace_size(const falcon_params_t* p);
+
+/* Chunk forward over packed sequences of different lengths (varlen), as
+ * the chunked framework is used for training [FW 三种等价形式; JC
+ * 三种视角看同一个更新].  cu_seqlens (device int32 [B + 1], non-decreasing,
+ * cu_seqlens[0] = 0, cu_seqlens[B] = total_tokens) delimits sequence b's
+ * tokens [cu_seqlens[b], cu_seqlens[b+1]); every length must be <= p->T.
+ * q, k [total_tokens, H, dk], v, o [total_tokens, H, dv], beta
+ * [total_tokens, H] (or [total_tokens, H, dv]), lambda [total_tokens, H];
+ * carry_in / carry_out are per sequence ([B, H, ...], as for
+ * falcon_chunk_fwd; NULL carry_in = every sequence fresh).  The tokens are
+ * laid out as a [B, p->T] batch in the workspace (applying p->prologue on
+ * the way); positions past a sequence's end get beta = 0 and lambda = 0,
+ * steps that neither write nor decay, so each sequence's state after p->T
+ * steps is its state after its own length; the same kernel family as
+ * falcon_chunk_fwd then runs, and the outputs go back to the packed layout.
+ * carry_out's k_prev, pos and window ring are those after each sequence's
+ * own last token.  Errors as falcon_chunk_fwd. */
+int falcon_chunk_fwd_varlen(const falcon_params_t* p, const int32_t* cu_seqlens, int64_t total_tokens,
+                            const void* q, const void* k, const void* v, const float* beta,
+                            const float* lambda, const falcon_carry_t* carry_in, void* o,
+                            falcon_carry_t* carry_out, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
 /* Which kernel family falcon_chunk_fwd uses for these params
  * (FALCON_IMPL_GENERIC, FALCON_IMPL_TC or FALCON_IMPL_SCAN, written to *impl_out) and how many

@@ -11,3 +11,4 @@ from .falcon import (  # noqa: F401
     step_coefficients,
 )
 from .falcon_grad import ONE_PAIR, recurrent_torch, recurrent_vjp  # noqa: F401,E402
+from .prologue import GATE_LOGITS, L2NORM_QK, apply_prologue, phi, recurrent_varlen, sigmoid  # noqa: F401,E402

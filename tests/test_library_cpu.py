@@ -149,3 +149,33 @@ def test_backward_workspace_and_overlap_checks(F):
         F.falcon_backward(p, fake, fake, fake, fake, fake, None, fake, None, None, *outs[1:], None,
                           None, 1 << 30, n, 0)
     assert e.value.code == -1
+
+
+def test_prologue_and_varlen_sizes_and_flags(F):
+    p = _p(F, B=3, T=200, H=2)
+    base = F.falcon_workspace_size(p)
+    p.prologue = 3
+    with_pro = F.falcon_workspace_size(p)
+    assert with_pro > base and with_pro % 256 == 0
+    v = F.falcon_varlen_workspace_size(p)
+    assert v > with_pro  # the padded outputs on top
+    impl, n = F.falcon_chunk_fwd_plan(p)
+    p.prologue = 0
+    assert n == F.falcon_chunk_fwd_plan(p)[1] + 1
+    p.prologue = 8
+    assert F.falcon_workspace_size(p) == 0 and F.falcon_varlen_workspace_size(p) == 0
+    fake = 1 << 20
+    with pytest.raises(F.FalconError) as e:
+        F.falcon_chunk_fwd(p, fake, fake, fake, fake, fake, None, fake, None, None, 0, 0)
+    assert e.value.code == -1
+    p.prologue = 1
+    with pytest.raises(F.FalconError) as e:  # no cu_seqlens
+        F.falcon_chunk_fwd_varlen(p, None, 10, fake, fake, fake, fake, fake, None, fake, None, fake, 1 << 30, 0)
+    assert e.value.code == -1
+    with pytest.raises(F.FalconError) as e:  # more tokens than B x T
+        F.falcon_chunk_fwd_varlen(p, fake, 3 * 200 + 1, fake, fake, fake, fake, fake, None, fake, None, fake,
+                                  1 << 30, 0)
+    assert e.value.code == -1
+    with pytest.raises(F.FalconError) as e:  # workspace too small
+        F.falcon_chunk_fwd_varlen(p, fake, 10, fake, fake, fake, fake, fake, None, fake, None, 1 << 24, 16, 0)
+    assert e.value.code == -3

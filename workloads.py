@@ -146,6 +146,34 @@ def make_carry(w: Workload, seed: int, pos: int | torch.Tensor, device="cpu",
     return {n: t.contiguous().to(device) for n, t in out.items()}
 
 
+def make_raw_inputs(w: Workload, seed: int | None = None, device="cpu") -> dict:
+    """Raw projections and gate logits (for the library's prologue): q, k
+    ~ N(0, s^2) with a per-token scale s ~ U(0.2, 5) (not normalised), v ~
+    N(0, 1), beta logits ~ N(0, 1), lambda logits ~ N(-3, 1)."""
+    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    dt = torch_dtype(w.dtype)
+    shp_k = (w.B, w.T, w.H, w.dk)
+    sq = 0.2 + 4.8 * torch.rand((w.B, w.T, w.H, 1), generator=g)
+    sk = 0.2 + 4.8 * torch.rand((w.B, w.T, w.H, 1), generator=g)
+    q = (torch.randn(shp_k, generator=g) * sq).to(dt)
+    k = (torch.randn(shp_k, generator=g) * sk).to(dt)
+    v = torch.randn((w.B, w.T, w.H, w.dv), generator=g).to(dt)
+    bshape = (w.B, w.T, w.H, w.dv) if w.per_channel else (w.B, w.T, w.H)
+    beta = torch.randn(bshape, generator=g)
+    lam = -3.0 + torch.randn((w.B, w.T, w.H), generator=g)
+    out = {"q": q, "k": k, "v": v, "beta": beta.float(), "lam": lam.float()}
+    return {n: t.contiguous().to(device) for n, t in out.items()}
+
+
+def pack_varlen(x: dict, lengths, device="cpu") -> tuple[dict, torch.Tensor]:
+    """Pack batch rows b[:lengths[b]] of a [B, T, H, ...] input dict into
+    [sum(lengths), H, ...] tensors; returns them and cu_seqlens (int32)."""
+    packed = {n: torch.cat([t[b, :L] for b, L in enumerate(lengths)], dim=0).contiguous().to(device)
+              for n, t in x.items()}
+    cu = torch.tensor([0] + list(torch.cumsum(torch.tensor(lengths), 0).tolist()), dtype=torch.int32)
+    return packed, cu.to(device)
+
+
 def make_cotangents(w: Workload, seed: int, device="cpu", with_dS: bool = True) -> dict:
     """Cotangents for a backward pass: dO ~ N(0, 1) in the dtype (the shape
     of o) and dS_final ~ N(0, 1/dk) fp32 (or None)."""
