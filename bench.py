@@ -29,6 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 N_SETS = 4
+VARIANT_NAMES = ("falcon1", "falcon1a", "falcon2", "falcon2a", "falcon3", "falcon3a")
 
 
 def parse():
@@ -40,9 +41,12 @@ def parse():
     ap.add_argument("--workload", default="lm124m_f1_8x2048x12_d64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--mode", choices=["chunk", "decode", "backward"], default="chunk",
+    ap.add_argument("--mode", choices=["chunk", "decode", "backward", "varlen"], default="chunk",
                     help="decode: the recurrent one-token step (256 sequences x 12 heads); "
-                         "backward: the gradient of the chunk forward for the workload")
+                         "backward: the gradient of the chunk forward for the workload; "
+                         "varlen: the workload's B sequences packed with a mix of lengths")
+    ap.add_argument("--prologue", action="store_true",
+                    help="raw q, k and gate logits: the library applies phi and the sigmoids")
     ap.add_argument("--decode-variant", type=int, default=0)
     ap.add_argument("--pairing", choices=["prefix", "same"], default="prefix",
                     help="same: the same-step pairing ablation (x_t = k_t)")
@@ -358,6 +362,77 @@ def run_backward(args, w):
                       "gpu_launches": args.steps, "clocks": clk}), flush=True)
 
 
+VARLEN_FRACTIONS = (1.0, 0.75, 0.5, 0.25, 1.0, 0.125, 0.875, 0.375)
+
+
+def run_varlen(args, w):
+    """Packed sequences: the workload's B sequences with lengths T x (1, 3/4,
+    1/2, 1/4, 1, 1/8, 7/8, 3/8) (cycled), one falcon_chunk_fwd_varlen call per
+    step; tokens/s counts the real tokens."""
+    import torch
+
+    import chunked_delta_rule_gb300 as F
+    from workloads import make_inputs, make_raw_inputs, pack_varlen
+    torch.cuda.set_device(0)
+    lengths = [max(1, int(w.T * VARLEN_FRACTIONS[b % len(VARLEN_FRACTIONS)])) for b in range(w.B)]
+    p = F.Params(B=w.B, T=w.T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk, window=w.window, eps=w.eps,
+                 eps_gamma=w.eps_gamma, variant=w.variant,
+                 dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32,
+                 pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX,
+                 prologue=3 if args.prologue else 0)
+    gen = make_raw_inputs if args.prologue else make_inputs
+    sets = []
+    for i in range(args.sets):
+        packed, cu = pack_varlen(gen(w, seed=w.seed + i), lengths, device="cuda")
+        sets.append((packed, cu))
+    total = sum(lengths)
+    o = torch.empty((total, w.H, w.dv), dtype=sets[0][0]["q"].dtype, device="cuda")
+    carry = F.empty_carry(p)
+    ws_n = F.falcon_varlen_workspace_size(p)
+    ws = F.alloc_workspace(ws_n)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        x, cu = sets[i % len(sets)]
+        F.falcon_chunk_fwd_varlen(p, cu, total, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o,
+                                  carry, ws, ws_n, stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    wr = w.with_(B=1, T=total)
+    abytes = algorithmic_bytes(wr) + (w.B - 1) * w.H * w.dk * w.dv * 4
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    gbs = abytes / (ms / 1e3) / 1e9
+    print(json.dumps({"metric": "Falcon chunked fwd over packed sequences, tokens/s", "value": total / (ms / 1e3),
+                      "unit": "tokens/s", "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup,
+                      "higher_is_better": True, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                      "config": {"workload": w.name + "_varlen" + ("_prologue" if args.prologue else ""),
+                                 "lengths": lengths, "tokens": total, "H": w.H, "dk": w.dk,
+                                 "padded_fraction": 1 - total / (w.B * w.T)},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                   "frac": gbs / peak, "algorithmic_bytes": abytes,
+                                   "note": "whole call (gather, kernels, scatter) against the real tokens' bytes"},
+                      "clocks": clk}), flush=True)
+
+
 def main():
     args = parse()
     if args.mode == "decode":
@@ -368,6 +443,9 @@ def main():
         w = w.with_(name=w.name + "_same_step", pairing="same")
     if args.mode == "backward":
         run_backward(args, w)
+        return
+    if args.mode == "varlen":
+        run_varlen(args, w)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -393,8 +471,11 @@ def main():
     p = F.Params(B=w.B, T=w.T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk, window=w.window,
                  eps=w.eps, eps_gamma=w.eps_gamma, variant=w.variant,
                  dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32,
-                 pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX)
-    sets = [make_inputs(w, seed=w.seed + 100 * rank + i, device=dev) for i in range(args.sets)]
+                 pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX,
+                 prologue=3 if args.prologue else 0)
+    from workloads import make_raw_inputs
+    gen = make_raw_inputs if args.prologue else make_inputs
+    sets = [gen(w, seed=w.seed + 100 * rank + i, device=dev) for i in range(args.sets)]
     o = torch.empty((w.B, w.T, w.H, w.dv), dtype=sets[0]["q"].dtype, device=dev)
     carry = F.empty_carry(p, dev)
     ws_n = F.falcon_workspace_size(p)
@@ -505,6 +586,12 @@ def main():
         else:
             names = ["tc_wy_kernel", "tc_fwd_kernel"]
         kbytes = kernel_bytes(w, names)
+        if args.prologue:  # the gather pass: q, k, v and gates in, the same out
+            es = 2 if w.dtype == "bf16" else 4
+            th = w.B * w.T * w.H
+            pb = 2 * (th * (2 * w.dk + w.dv) * es + th * ((w.dv if w.per_channel else 1) + 1) * 4)
+            names = ["prologue_kernel"] + names
+            kbytes = [pb] + kbytes
         dom = max(range(launches), key=lambda j: kern_ms[j])
         kernel = names[dom]
         achieved = kbytes[dom] / (kern_ms[dom] / 1e3) / 1e9
@@ -527,8 +614,9 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
             "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                       "chunk": w.chunk, "variant": "falcon1", "global_batch": w.B * world,
+            "config": {"workload": w.name + ("_prologue" if args.prologue else ""), "B": w.B, "T": w.T,
+                       "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk, "variant": VARIANT_NAMES[w.variant], "global_batch": w.B * world,
                        "seq_len": w.T, "parallelism": f"replicas x{world}",
                        "l2": f"rotating {len(sets)} input sets ({len(sets) * abytes / 1e6:.0f} MB)"},
             "roofline": dict(roof, traffic=traffic_for(kernel), kernel=kernel,

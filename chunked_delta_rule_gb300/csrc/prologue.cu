@@ -96,6 +96,62 @@ __global__ void __launch_bounds__(32 * kProWarps) prologue_kernel(ProArgs a) {
   }
 }
 
+// Vectorised form for 16-byte aligned rows: a row of q or k is LPR lanes of
+// 16 bytes; a warp takes 32 / LPR rows at a time.
+template <typename Tin>
+__global__ void __launch_bounds__(32 * kProWarps) prologue_vec_kernel(ProArgs a, int LPR) {
+  constexpr int EC = 16 / (int)sizeof(Tin);  // elements per 16 bytes
+  const int lane = threadIdx.x & 31, sub = lane % LPR;
+  const int rpw = 32 / LPR;
+  const long long nrows = (long long)a.B * a.T * a.H;
+  const long long row = ((long long)blockIdx.x * kProWarps + (threadIdx.x >> 5)) * rpw + lane / LPR;
+  const bool live = row < nrows;
+  const int h = live ? (int)(row % a.H) : 0;
+  const long long bt = live ? row / a.H : 0;
+  const int t = (int)(bt % a.T), b = (int)(bt / a.T);
+  const long long sr = live ? src_row(a, b, t) : -1;
+  const size_t dst = (size_t)row, srow = (size_t)(sr < 0 ? 0 : sr) * a.H + h;
+  const bool l2 = (a.flags & FALCON_PROLOGUE_L2NORM_QK) != 0;
+  const bool logits = (a.flags & FALCON_PROLOGUE_GATE_LOGITS) != 0;
+  const unsigned full = 0xffffffffu;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {  // q, then k: one 16-byte piece per lane
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (sr >= 0) raw = *reinterpret_cast<const uint4*>(cptr<Tin>(which == 0 ? a.q : a.k) + srow * a.dk + sub * EC);
+    float x[EC];
+    const Tin* e = reinterpret_cast<const Tin*>(&raw);
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < EC; ++i) {
+      x[i] = to_f32(e[i]);
+      ss = fmaf(x[i], x[i], ss);
+    }
+    for (int o = 1; o < LPR; o <<= 1) ss += __shfl_xor_sync(full, ss, o);
+    const float scale = l2 ? 1.f / fmaxf(sqrtf(ss), 1e-12f) : 1.f;
+    uint4 outv;
+    Tin* oe = reinterpret_cast<Tin*>(&outv);
+#pragma unroll
+    for (int i = 0; i < EC; ++i) oe[i] = from_f32<Tin>(x[i] * scale);
+    if (live) *reinterpret_cast<uint4*>(reinterpret_cast<Tin*>(which == 0 ? a.qo : a.ko) + dst * a.dk + sub * EC) = outv;
+  }
+  if (!live) return;
+  const int vc = a.dv / EC;  // 16-byte pieces per value row
+  for (int c = sub; c < vc; c += LPR) {
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (sr >= 0) raw = *reinterpret_cast<const uint4*>(cptr<Tin>(a.v) + srow * a.dv + c * EC);
+    *reinterpret_cast<uint4*>(reinterpret_cast<Tin*>(a.vo) + dst * a.dv + c * EC) = raw;
+  }
+  const int nb = a.perch ? a.dv : 1;
+  for (int i = sub; i < nb; i += LPR) {
+    const float bv = sr >= 0 ? a.beta[srow * nb + i] : 0.f;
+    a.bo[dst * nb + i] = (sr >= 0 && logits) ? sigmoidf(bv) : bv;
+  }
+  if (sub == 0) {
+    const float lv = sr >= 0 ? a.lam[srow] : 0.f;
+    a.lo[dst] = (sr >= 0 && logits) ? sigmoidf(lv) : lv;
+  }
+}
+
 template <typename Tin>
 __global__ void __launch_bounds__(32 * kProWarps) varlen_scatter_kernel(ProArgs a, const void* o_pad, void* o) {
   const int lane = threadIdx.x & 31;
@@ -190,9 +246,23 @@ void prologue_carve(ProArgs& a, void* base, bool with_o, void** o_pad) {
 }
 
 int launch_prologue(const ProArgs& a, cudaStream_t s) {
-  if ((long long)a.B * a.T * a.H == 0) return FALCON_OK;
-  if (a.dtype == FALCON_BF16) prologue_kernel<__nv_bfloat16><<<rows_grid(a), 32 * kProWarps, 0, s>>>(a);
-  else prologue_kernel<float><<<rows_grid(a), 32 * kProWarps, 0, s>>>(a);
+  const long long nrows = (long long)a.B * a.T * a.H;
+  if (nrows == 0) return FALCON_OK;
+  const size_t es = a.dtype == FALCON_BF16 ? 2 : 4;
+  const void* ps[3] = {a.q, a.k, a.v};
+  bool aligned = true;
+  for (const void* x : ps) aligned = aligned && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  const int LPR = (int)(a.dk * es / 16);
+  if (aligned && (a.dv * es) % 16 == 0 && LPR >= 1 && LPR <= 32) {
+    const long long rows_per_cta = (long long)kProWarps * (32 / LPR);
+    const unsigned grid = (unsigned)((nrows + rows_per_cta - 1) / rows_per_cta);
+    if (a.dtype == FALCON_BF16) prologue_vec_kernel<__nv_bfloat16><<<grid, 32 * kProWarps, 0, s>>>(a, LPR);
+    else prologue_vec_kernel<float><<<grid, 32 * kProWarps, 0, s>>>(a, LPR);
+  } else if (a.dtype == FALCON_BF16) {
+    prologue_kernel<__nv_bfloat16><<<rows_grid(a), 32 * kProWarps, 0, s>>>(a);
+  } else {
+    prologue_kernel<float><<<rows_grid(a), 32 * kProWarps, 0, s>>>(a);
+  }
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
 

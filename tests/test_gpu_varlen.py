@@ -188,3 +188,19 @@ def test_prologue_refused_where_not_taken(F):
         F.falcon_chunk_fwd_noalloc(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None,
                                    torch.empty_like(x["v"]), None)
     assert e.value.code == -2
+
+
+def test_prologue_misaligned_rows(F):
+    """q off a 16-byte boundary: the gather pass takes its element-wise form."""
+    w = wl(FALCON_1, T=70, B=1, H=2, seed=1301)
+    x = make_raw_inputs(w, device="cuda")
+    q2 = torch.empty(x["q"].numel() + 1, dtype=x["q"].dtype, device="cuda")
+    q2[1:].copy_(x["q"].reshape(-1))
+    xq = dict(x, q=q2[1:].view(x["q"].shape))
+    assert xq["q"].data_ptr() % 16 != 0
+    p = params_for(F, w)
+    p.prologue = BOTH
+    o, co = F.chunk_forward(p, xq["q"], xq["k"], xq["v"], xq["beta"], xq["lam"])
+    torch.cuda.synchronize()
+    o_ref, c_ref = oracle_pro(w, x, BOTH)
+    check(w, o, co["S"], o_ref, c_ref["S"])
