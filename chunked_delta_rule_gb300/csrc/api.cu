@@ -312,7 +312,7 @@ int falcon_masked_parallel_ref_gpu(const falcon_params_t* p, const void* q, cons
 size_t falcon_backward_workspace_size(const falcon_params_t* p) {
   if (check_params(p, false) != FALCON_OK || !backward_supported(p->variant, p->dk, p->dv) || p->prologue)
     return 0;
-  return backward_ws_bytes(p->B, p->T, p->H, p->dk);
+  return backward_ws_bytes(p->variant, p->B, p->T, p->H, p->dk);
 }
 
 int falcon_backward(const falcon_params_t* p, const void* q, const void* k, const void* v,
@@ -325,7 +325,7 @@ int falcon_backward(const falcon_params_t* p, const void* q, const void* k, cons
   if (!backward_supported(p->variant, p->dk, p->dv) || p->prologue) return FALCON_ERR_UNSUPPORTED;
   if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !dO || !dq || !dk || !dv || !dbeta || !dlambda))
     return FALCON_ERR_INVALID_ARG;
-  const size_t need = backward_ws_bytes(p->B, p->T, p->H, p->dk);
+  const size_t need = backward_ws_bytes(p->variant, p->B, p->T, p->H, p->dk);
   if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0))
     return FALCON_ERR_WORKSPACE;
   FwdArgs a = make_args(p, q, k, v, beta, lambda, nullptr, stream);

@@ -316,7 +316,8 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t backward_ws_bytes(int B, int T, int H, int d) {
+size_t backward_ws_bytes(int variant, int B, int T, int H, int d) {
+  if (backward_chunk_supported(variant, d, d, T)) return backward_chunk_ws_bytes(B, T, H);
   const size_t NB = (size_t)(T + kBB - 1) / kBB;
   return (size_t)B * H * (NB + kBB) * d * d * sizeof(float);
 }
@@ -334,6 +335,8 @@ int launch_backward(const FwdArgs& f, const void* dO, const float* dS_final, voi
   a.q = f.q; a.k = f.k; a.v = f.v; a.dO = dO; a.beta = f.beta; a.lam = f.lam;
   a.S_in = f.S_in; a.kprev_in = f.kprev_in; a.pos_in = f.pos_in; a.dS_final = dS_final;
   a.dq = dq; a.dk = dk; a.dv = dv; a.dbeta = dbeta; a.dlam = dlam; a.dS_in = dS_in; a.dk_prev = dk_prev;
+  if (backward_chunk_supported(f.variant, f.dk, f.dv, f.T))
+    return launch_backward_chunk(f, dO, dS_final, dq, dk, dv, dbeta, dlam, dS_in, dk_prev);
   a.ws = reinterpret_cast<float*>(f.ws);
   if (f.dk == 64)
     return f.dtype == FALCON_BF16 ? launch_bwd_d<__nv_bfloat16, 64>(a, f.stream) : launch_bwd_d<float, 64>(a, f.stream);

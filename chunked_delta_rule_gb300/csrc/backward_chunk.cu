@@ -1,0 +1,871 @@
+// Chunked (WY-form) backward of Falcon-1 / Falcon-1A, d_k = d_v = 64, chunk
+// 64, fp32 arithmetic on CUDA cores [FW 三种等价形式; JC 三种视角看同一个更新].
+//
+// Forward of one chunk (rows r, i = 0..63; g the in-chunk cumulative log of
+// the clamped decay, Gamma = exp(g), E_r = exp(g_63 - g_r),
+// D_ri = exp(g_r - g_i) for i <= r, eta_r = beta_r / (eps + |x_r|^2)):
+//   L = D (.) X X^T (i < r),  T = (I + diag(eta) L)^{-1},
+//   W = T diag(eta Gamma) X,  U = T diag(eta) V,  Delta = U - W S0
+//   (Falcon-1A: Delta = diag(eta) V),
+//   O = diag(Gamma) Q S0 + (Q X^T (.) D) Delta,   S1 = Gamma_63 S0 + (diag(E) X)^T Delta.
+// Its transpose gives the backward: with dS1 the gradient of the chunk's end
+// state,
+//   dDelta = (P (.) D)^T dO + diag(E) X dS1,  dR = T^T dDelta  (Falcon-1A: dR = dDelta),
+//   dS0 = Gamma_63 dS1 + Q^T diag(Gamma) dO - W^T dDelta,
+// a chain over chunks as sequential as the forward's, and per chunk
+//   dV = diag(eta) dR,  d eta_r = sum_j dR_rj (V - Gamma X S0 - L Delta)_rj,
+//   dQ = diag(Gamma) dO S0^T + dP X,  dP = (dO Delta^T) (.) D,
+//   dX = (dG + dG^T) X - diag(eta Gamma) dR S0^T + dP^T Q + diag(E) Delta dS1^T + 2 dn x,
+//   dG = -(diag(eta) dR Delta^T) (.) D (i < r),
+// and the log-decay gradients from Gamma, E and D (row minus column sums of
+// D (.) dD), summed back over the chunk's steps.  Four kernels:
+//  (a) bwdc_prep_kernel, per chunk: gates, T, W, U, diag(E) X and the chain's
+//      constant Y = Q^T diag(Gamma) dO - W^T (P (.) D)^T dO, into the workspace;
+//  (b) bwdc_fwd_chain_kernel, per (b, h, 16 value columns): chunk start states;
+//  (c) bwdc_bwd_chain_kernel, per (b, h, 16 value columns): dS at chunk ends;
+//  (d) bwdc_grad_kernel, per chunk: every gradient.
+// 64 x 64 products run on 256 threads from shared memory (4 x 4 outputs per
+// thread, 16-byte loads; the layout of each product chosen so that no load
+// conflicts on a bank).
+
+#include "common.cuh"
+
+namespace falcon {
+
+namespace {
+
+constexpr int kN = 64;       // chunk rows and head dim
+constexpr int LDM = 68;      // fp32 row stride of the shared-memory matrices
+constexpr int kThr = 256;
+constexpr size_t kMat = (size_t)kN * kN;
+enum { M_T = 0, M_W, M_U, M_XT, M_Y, M_S0, M_DS1, kMats };
+constexpr int kGateVecs = 8;  // per chunk: g, Gamma, E, eta, nrm, exists, (2 spare)
+constexpr int NN = 0, TN = 1, NT = 2;
+
+struct CbArgs {
+  int B, T, H, NC, shift, additive;
+  float eps, eps_gamma;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dO;
+  const float* beta;
+  const float* lam;
+  const float* S_in;
+  const void* kprev_in;
+  const int64_t* pos_in;
+  const float* dS_final;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dbeta;
+  float* dlam;
+  float* dS_in;
+  void* dk_prev;
+  float* ws;
+};
+
+__device__ __forceinline__ float* wsmat(const CbArgs& a, size_t cg, int which) {
+  return a.ws + (cg * kMats + which) * kMat;
+}
+__device__ __forceinline__ float* wsgate(const CbArgs& a, size_t cg) {
+  return a.ws + (size_t)a.B * a.H * a.NC * kMats * kMat + cg * kGateVecs * kN;
+}
+
+// C (4 x 4 per thread) = op(A) op(B) over K = 64, both operands in shared
+// memory with row stride LDM.  NN: A [M][K], B [K][N]; TN: A [K][M], B [K][N];
+// NT: A [M][K], B [N][K].  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
+// 4 ty + i and columns 4 tx + j (NN, TN) or tx + 16 j (NT).
+template <int MODE>
+__device__ __forceinline__ void mm64(float (&acc)[4][4], const float* __restrict__ A,
+                                     const float* __restrict__ B) {
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  if (MODE == TN) {
+#pragma unroll 8
+    for (int k = 0; k < kN; ++k) {
+      const float4 av = *reinterpret_cast<const float4*>(&A[k * LDM + 4 * ty]);
+      const float4 bv = *reinterpret_cast<const float4*>(&B[k * LDM + 4 * tx]);
+      const float a4[4] = {av.x, av.y, av.z, av.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a4[i], b4[j], acc[i][j]);
+    }
+  } else {
+#pragma unroll 2
+    for (int k = 0; k < kN; k += 4) {
+      float a4[4][4], b4[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 av = *reinterpret_cast<const float4*>(&A[(4 * ty + i) * LDM + k]);
+        a4[i][0] = av.x; a4[i][1] = av.y; a4[i][2] = av.z; a4[i][3] = av.w;
+      }
+      if (MODE == NN) {  // b4[kk][j] = B[k + kk][4 tx + j]
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 bv = *reinterpret_cast<const float4*>(&B[(k + kk) * LDM + 4 * tx]);
+          b4[kk][0] = bv.x; b4[kk][1] = bv.y; b4[kk][2] = bv.z; b4[kk][3] = bv.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a4[i][kk], b4[kk][j], acc[i][j]);
+      } else {  // NT: b4[j][kk] = B[tx + 16 j][k + kk]
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 bv = *reinterpret_cast<const float4*>(&B[(tx + 16 * j) * LDM + k]);
+          b4[j][0] = bv.x; b4[j][1] = bv.y; b4[j][2] = bv.z; b4[j][3] = bv.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) acc[i][j] = fmaf(a4[i][kk], b4[j][kk], acc[i][j]);
+      }
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ int out_row(int i) { return 4 * (threadIdx.x >> 4) + i; }
+template <int MODE>
+__device__ __forceinline__ int out_col(int j) {
+  return MODE == NT ? (int)(threadIdx.x & 15) + 16 * j : 4 * (int)(threadIdx.x & 15) + j;
+}
+
+__device__ __forceinline__ void zero_acc(float (&acc)[4][4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+}
+
+// sum over the 64 columns of f(r, c), 4 threads per row; every thread of the
+// row's group returns the row's sum (row = tid / 4)
+template <typename Fn>
+__device__ __forceinline__ float row_sum(Fn f) {
+  const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
+  float s = 0.f;
+#pragma unroll 4
+  for (int c = part * 16; c < part * 16 + 16; ++c) s += f(r, c);
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  return s;
+}
+
+template <typename Tin>
+__device__ __forceinline__ float ldx(const void* p, size_t i) { return to_f32(reinterpret_cast<const Tin*>(p)[i]); }
+template <typename Tin>
+__device__ __forceinline__ void stx(void* p, size_t i, float x) { reinterpret_cast<Tin*>(p)[i] = from_f32<Tin>(x); }
+
+// rows of a chunk into shared memory (zero past the end of the call)
+template <typename Tin>
+__device__ void load_rows(float* dst, const void* src, const CbArgs& a, int b, int h, int t0) {
+  for (int i = threadIdx.x; i < kN * kN; i += kThr) {
+    const int r = i / kN, c = i % kN, t = t0 + r;
+    dst[r * LDM + c] = t < a.T ? ldx<Tin>(src, (((size_t)b * a.T + t) * a.H + h) * kN + c) : 0.f;
+  }
+}
+// keys of the chunk's pairs: x_r = k_{t - shift}, the carried key for the
+// first pair (prefix), zero where the pair does not exist
+template <typename Tin>
+__device__ void load_keys(float* dst, const CbArgs& a, int b, int h, int t0, int64_t pos) {
+  for (int i = threadIdx.x; i < kN * kN; i += kThr) {
+    const int r = i / kN, c = i % kN, t = t0 + r;
+    float x = 0.f;
+    if (t < a.T && pos + t >= a.shift) {
+      if (t - a.shift >= 0) x = ldx<Tin>(a.k, (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN + c);
+      else if (a.kprev_in) x = ldx<Tin>(a.kprev_in, ((size_t)b * a.H + h) * kN + c);
+    }
+    dst[r * LDM + c] = x;
+  }
+}
+
+struct GateSm {
+  float g[kN], Gam[kN], E[kN], eta[kN], nrm[kN], ex[kN], gam[kN];
+};
+
+// gates of the chunk (needs the keys in X); threads < 64, then a barrier
+__device__ void make_gates(GateSm& gs, const float* X, const CbArgs& a, int b, int h, int t0, int64_t pos) {
+  const int r = threadIdx.x;
+  if (r < kN) {
+    const int t = t0 + r;
+    float n = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < kN; ++c) n = fmaf(X[r * LDM + c], X[r * LDM + c], n);
+    const bool live = t < a.T, ex = live && pos + t >= a.shift;
+    const size_t gi = ((size_t)b * a.T + (live ? t : 0)) * a.H + h;
+    gs.nrm[r] = n;
+    gs.ex[r] = ex ? 1.f : 0.f;
+    gs.eta[r] = ex ? a.beta[gi] / (a.eps + n) : 0.f;
+    const float gm = live ? fminf(fmaxf(1.f - a.lam[gi], a.eps_gamma), 1.f) : 1.f;
+    gs.gam[r] = gm;
+    gs.g[r] = live ? logf(gm) : 0.f;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // inclusive prefix sum over the 64 rows
+    float v0 = gs.g[threadIdx.x], v1 = gs.g[threadIdx.x + 32];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n0 = __shfl_up_sync(0xffffffffu, v0, o), n1 = __shfl_up_sync(0xffffffffu, v1, o);
+      if ((int)threadIdx.x >= o) { v0 += n0; v1 += n1; }
+    }
+    v1 += __shfl_sync(0xffffffffu, v0, 31);
+    gs.g[threadIdx.x] = v0;
+    gs.g[threadIdx.x + 32] = v1;
+  }
+  __syncthreads();
+  if (r < kN) {
+    gs.Gam[r] = __expf(gs.g[r]);
+    gs.E[r] = __expf(gs.g[kN - 1] - gs.g[r]);
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ float dmask(const GateSm& gs, int r, int i) {  // D_ri (i <= r), else 0
+  return i <= r ? __expf(gs.g[r] - gs.g[i]) : 0.f;
+}
+
+// ---------------------------------------------------------------- (a)
+template <typename Tin>
+__global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
+  extern __shared__ float4 smem_f4[];
+  float* sm = reinterpret_cast<float*>(smem_f4);
+  float* X = sm;
+  float* Q = X + kN * LDM;
+  float* V = Q + kN * LDM;
+  float* dO = V + kN * LDM;
+  float* M1 = dO + kN * LDM;
+  float* Tm = M1 + kN * LDM;
+  float* M3 = Tm + kN * LDM;
+  float* Wm = M3 + kN * LDM;
+  GateSm& gs = *reinterpret_cast<GateSm*>(Wm + kN * LDM);
+  float* red = reinterpret_cast<float*>(&gs + 1);  // [4][64]
+  const size_t cg = blockIdx.x;
+  const int c = (int)(cg % a.NC), bh = (int)(cg / a.NC), b = bh / a.H, h = bh % a.H, t0 = c * kN;
+  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+  const int tid = threadIdx.x;
+  load_keys<Tin>(X, a, b, h, t0, pos);
+  load_rows<Tin>(Q, a.q, a, b, h, t0);
+  load_rows<Tin>(V, a.v, a, b, h, t0);
+  load_rows<Tin>(dO, a.dO, a, b, h, t0);
+  __syncthreads();
+  make_gates(gs, X, a, b, h, t0, pos);
+  float acc[4][4];
+  if (!a.additive) {
+    // A = diag(eta) (D (.) X X^T), strictly lower
+    zero_acc(acc);
+    mm64<NT>(acc, X, X);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = out_row<NT>(i), ci = out_col<NT>(j);
+        M1[r * LDM + ci] = ci < r ? gs.eta[r] * __expf(gs.g[r] - gs.g[ci]) * acc[i][j] : 0.f;
+      }
+    __syncthreads();
+    // T = (I + A)^{-1} row by row: T_r = e_r - sum_{i<r} A_ri T_i (column per thread, 4 partial sums)
+    {
+      const int col = tid & 63, part = tid >> 6;
+      for (int r = 0; r < kN; ++r) {
+        float s = 0.f;
+        for (int i = part; i < r; i += 4) s = fmaf(M1[r * LDM + i], Tm[i * LDM + col], s);
+        red[part * kN + col] = s;
+        __syncthreads();
+        if (part == 0)
+          Tm[r * LDM + col] = (r == col ? 1.f : 0.f) - (red[col] + red[kN + col] + red[2 * kN + col] + red[3 * kN + col]);
+        __syncthreads();
+      }
+    }
+    // W = T diag(eta Gamma) X, U = T diag(eta) V
+    for (int i = tid; i < kN * kN; i += kThr) {
+      const int r = i / kN, cc = i % kN;
+      M3[r * LDM + cc] = gs.eta[r] * gs.Gam[r] * X[r * LDM + cc];
+      M1[r * LDM + cc] = gs.eta[r] * V[r * LDM + cc];
+    }
+    __syncthreads();
+    zero_acc(acc);
+    mm64<NN>(acc, Tm, M3);
+    float* wW = wsmat(a, cg, M_W);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = out_row<NN>(i), cc = out_col<NN>(j);
+        Wm[r * LDM + cc] = acc[i][j];
+        wW[r * kN + cc] = acc[i][j];
+      }
+    zero_acc(acc);
+    mm64<NN>(acc, Tm, M1);
+    float* wU = wsmat(a, cg, M_U);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wU[out_row<NN>(i) * kN + out_col<NN>(j)] = acc[i][j];
+    float* wT = wsmat(a, cg, M_T);
+    for (int i = tid; i < kN * kN; i += kThr) wT[i] = Tm[(i / kN) * LDM + i % kN];
+  } else {
+    float* wU = wsmat(a, cg, M_U);
+    for (int i = tid; i < kN * kN; i += kThr) wU[i] = gs.eta[i / kN] * V[(i / kN) * LDM + i % kN];
+  }
+  {  // diag(E) X, gates
+    float* wX = wsmat(a, cg, M_XT);
+    for (int i = tid; i < kN * kN; i += kThr) wX[i] = gs.E[i / kN] * X[(i / kN) * LDM + i % kN];
+    float* gv = wsgate(a, cg);
+    if (tid < kN) {
+      gv[tid] = gs.g[tid];
+      gv[kN + tid] = gs.Gam[tid];
+      gv[2 * kN + tid] = gs.E[tid];
+      gv[3 * kN + tid] = gs.eta[tid];
+      gv[4 * kN + tid] = gs.nrm[tid];
+      gv[5 * kN + tid] = gs.ex[tid];
+      gv[6 * kN + tid] = gs.gam[tid];
+    }
+  }
+  __syncthreads();
+  // Y = Q^T diag(Gamma) dO - W^T (P (.) D)^T dO
+  zero_acc(acc);
+  mm64<NT>(acc, Q, X);  // P = Q X^T
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = out_row<NT>(i), ci = out_col<NT>(j);
+      M1[r * LDM + ci] = dmask(gs, r, ci) * acc[i][j];
+    }
+  for (int i = tid; i < kN * kN; i += kThr) {
+    const int r = i / kN, cc = i % kN;
+    M3[r * LDM + cc] = gs.Gam[r] * dO[r * LDM + cc];
+  }
+  __syncthreads();
+  float yacc[4][4];
+  zero_acc(yacc);
+  mm64<TN>(yacc, Q, M3);  // Q^T diag(Gamma) dO
+  if (!a.additive) {
+    zero_acc(acc);
+    mm64<TN>(acc, M1, dO);  // Z = (P (.) D)^T dO
+    __syncthreads();        // M3 is read by every thread above
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) M3[out_row<TN>(i) * LDM + out_col<TN>(j)] = acc[i][j];
+    __syncthreads();
+    float wz[4][4];
+    zero_acc(wz);
+    mm64<TN>(wz, Wm, M3);  // W^T Z
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) yacc[i][j] -= wz[i][j];
+  }
+  float* wY = wsmat(a, cg, M_Y);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wY[out_row<TN>(i) * kN + out_col<TN>(j)] = yacc[i][j];
+}
+
+// ---------------------------------------------------------------- (b), (c)
+// One CTA per (b, h, 16 value columns); S (or dS) slice 64 x 16 in shared
+// memory.  Thread (r = tid / 4, quad = tid % 4) owns row r, columns 4 quad..
+constexpr int kSC = 16;
+constexpr int LDS_ = kSC + 4;
+
+__global__ void __launch_bounds__(kThr) bwdc_fwd_chain_kernel(CbArgs a) {
+  __shared__ __align__(16) float Wsm[kN * LDM];
+  __shared__ __align__(16) float Xsm[kN * LDM];
+  __shared__ __align__(16) float S[kN * LDS_];
+  __shared__ __align__(16) float Dl[kN * LDS_];
+  const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
+  const int r = tid >> 2, q4 = (tid & 3) * 4;
+  for (int i = tid; i < kN * kSC; i += kThr) {
+    const int rr = i / kSC, cc = i % kSC;
+    S[rr * LDS_ + cc] = a.S_in ? a.S_in[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
+  }
+  for (int c = 0; c < a.NC; ++c) {
+    const size_t cg = (size_t)bh * a.NC + c;
+    __syncthreads();
+    {  // chunk start state out; this chunk's W, diag(E) X in
+      float* wS = wsmat(a, cg, M_S0);
+      for (int i = tid; i < kN * kSC; i += kThr) wS[(i / kSC) * kN + c0 + i % kSC] = S[(i / kSC) * LDS_ + i % kSC];
+      const float* wW = wsmat(a, cg, M_W);
+      const float* wX = wsmat(a, cg, M_XT);
+      for (int i = tid; i < kN * kN / 4; i += kThr) {
+        const int rr = i / (kN / 4), cc = 4 * (i % (kN / 4));
+        if (!a.additive) *reinterpret_cast<float4*>(&Wsm[rr * LDM + cc]) = *reinterpret_cast<const float4*>(&wW[rr * kN + cc]);
+        *reinterpret_cast<float4*>(&Xsm[rr * LDM + cc]) = *reinterpret_cast<const float4*>(&wX[rr * kN + cc]);
+      }
+    }
+    __syncthreads();
+    const float* wU = wsmat(a, cg, M_U);
+    float d[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] = wU[(size_t)r * kN + c0 + q4 + j];
+    if (!a.additive) {  // Delta = U - W S
+      for (int k = 0; k < kN; ++k) {
+        const float w = Wsm[r * LDM + k];
+        const float4 s4 = *reinterpret_cast<const float4*>(&S[k * LDS_ + q4]);
+        d[0] -= w * s4.x; d[1] -= w * s4.y; d[2] -= w * s4.z; d[3] -= w * s4.w;
+      }
+    }
+    *reinterpret_cast<float4*>(&Dl[r * LDS_ + q4]) = make_float4(d[0], d[1], d[2], d[3]);
+    __syncthreads();
+    // S = Gamma_63 S + (diag(E) X)^T Delta   (row r of S is key index r)
+    const float G63 = wsgate(a, cg)[kN + kN - 1];
+    float s[4];
+    {
+      const float4 s4 = *reinterpret_cast<const float4*>(&S[r * LDS_ + q4]);
+      s[0] = G63 * s4.x; s[1] = G63 * s4.y; s[2] = G63 * s4.z; s[3] = G63 * s4.w;
+    }
+    for (int i = 0; i < kN; ++i) {
+      const float x = Xsm[i * LDM + r];
+      const float4 d4 = *reinterpret_cast<const float4*>(&Dl[i * LDS_ + q4]);
+      s[0] = fmaf(x, d4.x, s[0]); s[1] = fmaf(x, d4.y, s[1]); s[2] = fmaf(x, d4.z, s[2]); s[3] = fmaf(x, d4.w, s[3]);
+    }
+    __syncthreads();
+    *reinterpret_cast<float4*>(&S[r * LDS_ + q4]) = make_float4(s[0], s[1], s[2], s[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThr) bwdc_bwd_chain_kernel(CbArgs a) {
+  __shared__ __align__(16) float Wsm[kN * LDM];
+  __shared__ __align__(16) float Xsm[kN * LDM];
+  __shared__ __align__(16) float dS[kN * LDS_];
+  __shared__ __align__(16) float Z[kN * LDS_];
+  const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
+  const int r = tid >> 2, q4 = (tid & 3) * 4;
+  for (int i = tid; i < kN * kSC; i += kThr) {
+    const int rr = i / kSC, cc = i % kSC;
+    dS[rr * LDS_ + cc] = a.dS_final ? a.dS_final[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
+  }
+  for (int c = a.NC - 1; c >= 0; --c) {
+    const size_t cg = (size_t)bh * a.NC + c;
+    __syncthreads();
+    {
+      float* wD = wsmat(a, cg, M_DS1);
+      for (int i = tid; i < kN * kSC; i += kThr) wD[(i / kSC) * kN + c0 + i % kSC] = dS[(i / kSC) * LDS_ + i % kSC];
+      const float* wW = wsmat(a, cg, M_W);
+      const float* wX = wsmat(a, cg, M_XT);
+      for (int i = tid; i < kN * kN / 4; i += kThr) {
+        const int rr = i / (kN / 4), cc = 4 * (i % (kN / 4));
+        if (!a.additive) *reinterpret_cast<float4*>(&Wsm[rr * LDM + cc]) = *reinterpret_cast<const float4*>(&wW[rr * kN + cc]);
+        *reinterpret_cast<float4*>(&Xsm[rr * LDM + cc]) = *reinterpret_cast<const float4*>(&wX[rr * kN + cc]);
+      }
+    }
+    __syncthreads();
+    if (!a.additive) {  // Z = diag(E) X dS  (row r = chunk row)
+      float z[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k = 0; k < kN; ++k) {
+        const float x = Xsm[r * LDM + k];
+        const float4 d4 = *reinterpret_cast<const float4*>(&dS[k * LDS_ + q4]);
+        z[0] = fmaf(x, d4.x, z[0]); z[1] = fmaf(x, d4.y, z[1]); z[2] = fmaf(x, d4.z, z[2]); z[3] = fmaf(x, d4.w, z[3]);
+      }
+      *reinterpret_cast<float4*>(&Z[r * LDS_ + q4]) = make_float4(z[0], z[1], z[2], z[3]);
+    }
+    __syncthreads();
+    // dS = Gamma_63 dS - W^T Z + Y   (row r = key index)
+    const float G63 = wsgate(a, cg)[kN + kN - 1];
+    const float* wY = wsmat(a, cg, M_Y);
+    float s[4];
+    {
+      const float4 d4 = *reinterpret_cast<const float4*>(&dS[r * LDS_ + q4]);
+      s[0] = G63 * d4.x + wY[(size_t)r * kN + c0 + q4];
+      s[1] = G63 * d4.y + wY[(size_t)r * kN + c0 + q4 + 1];
+      s[2] = G63 * d4.z + wY[(size_t)r * kN + c0 + q4 + 2];
+      s[3] = G63 * d4.w + wY[(size_t)r * kN + c0 + q4 + 3];
+    }
+    if (!a.additive) {
+      for (int i = 0; i < kN; ++i) {
+        const float w = Wsm[i * LDM + r];
+        const float4 z4 = *reinterpret_cast<const float4*>(&Z[i * LDS_ + q4]);
+        s[0] -= w * z4.x; s[1] -= w * z4.y; s[2] -= w * z4.z; s[3] -= w * z4.w;
+      }
+    }
+    __syncthreads();
+    *reinterpret_cast<float4*>(&dS[r * LDS_ + q4]) = make_float4(s[0], s[1], s[2], s[3]);
+  }
+  __syncthreads();
+  if (a.dS_in)
+    for (int i = tid; i < kN * kSC; i += kThr)
+      a.dS_in[((size_t)bh * kN + i / kSC) * kN + c0 + i % kSC] = dS[(i / kSC) * LDS_ + i % kSC];
+}
+
+// ---------------------------------------------------------------- (d)
+template <typename Tin>
+__global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
+  extern __shared__ float4 smem_f4[];
+  float* sm = reinterpret_cast<float*>(smem_f4);
+  float* X = sm;
+  float* Q = X + kN * LDM;
+  float* V = Q + kN * LDM;
+  float* dO = V + kN * LDM;
+  float* S0 = dO + kN * LDM;
+  float* dS1 = S0 + kN * LDM;
+  float* s1 = dS1 + kN * LDM;
+  float* s2 = s1 + kN * LDM;
+  float* s3 = s2 + kN * LDM;
+  float* s4 = s3 + kN * LDM;
+  float* s5 = s4 + kN * LDM;
+  float* s6 = s5 + kN * LDM;
+  GateSm& gs = *reinterpret_cast<GateSm*>(s6 + kN * LDM);
+  float* vec = reinterpret_cast<float*>(&gs + 1);  // dGo, dGr, EdE, deta, rowM, colM, dg, misc
+  float* dGo = vec;
+  float* dGr = vec + kN;
+  float* EdE = vec + 2 * kN;
+  float* deta = vec + 3 * kN;
+  float* rowM = vec + 4 * kN;
+  float* colM = vec + 5 * kN;
+  float* dgv = vec + 6 * kN;
+  const size_t cg = blockIdx.x;
+  const int c = (int)(cg % a.NC), bh = (int)(cg / a.NC), b = bh / a.H, h = bh % a.H, t0 = c * kN;
+  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+  const int tid = threadIdx.x;
+  const bool reg = !a.additive;
+  load_keys<Tin>(X, a, b, h, t0, pos);
+  load_rows<Tin>(Q, a.q, a, b, h, t0);
+  load_rows<Tin>(V, a.v, a, b, h, t0);
+  load_rows<Tin>(dO, a.dO, a, b, h, t0);
+  {
+    const float* wS = wsmat(a, cg, M_S0);
+    const float* wD = wsmat(a, cg, M_DS1);
+    const float* wW = wsmat(a, cg, M_W);
+    const float* wU = wsmat(a, cg, M_U);
+    for (int i = tid; i < kN * kN; i += kThr) {
+      const int r = i / kN, cc = i % kN;
+      S0[r * LDM + cc] = wS[i];
+      dS1[r * LDM + cc] = wD[i];
+      if (reg) { s1[r * LDM + cc] = wW[i]; s2[r * LDM + cc] = wU[i]; }
+    }
+    const float* gv = wsgate(a, cg);
+    if (tid < kN) {
+      gs.g[tid] = gv[tid]; gs.Gam[tid] = gv[kN + tid]; gs.E[tid] = gv[2 * kN + tid]; gs.eta[tid] = gv[3 * kN + tid];
+      gs.nrm[tid] = gv[4 * kN + tid]; gs.ex[tid] = gv[5 * kN + tid]; gs.gam[tid] = gv[6 * kN + tid];
+    }
+  }
+  __syncthreads();
+  float acc[4][4];
+  // Delta -> s2
+  if (reg) {
+    zero_acc(acc);
+    mm64<NN>(acc, s1, S0);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = out_row<NN>(i), cc = out_col<NN>(j);
+        s2[r * LDM + cc] -= acc[i][j];
+      }
+  } else {
+    for (int i = tid; i < kN * kN; i += kThr) {
+      const int r = i / kN, cc = i % kN;
+      s2[r * LDM + cc] = gs.eta[r] * V[r * LDM + cc];
+    }
+  }
+  // X S0 -> s1 (regression); Q S0 -> s3
+  if (reg) {
+    zero_acc(acc);
+    mm64<NN>(acc, X, S0);
+    __syncthreads();  // s1 (W) is consumed
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s1[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
+  }
+  zero_acc(acc);
+  mm64<NN>(acc, Q, S0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s3[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
+  __syncthreads();
+  {
+    const float v = row_sum([&](int r, int cc) { return dO[r * LDM + cc] * s3[r * LDM + cc]; });
+    if ((tid & 3) == 0) dGo[tid >> 2] = v;
+  }
+  __syncthreads();
+  // P (.) D -> s3 (lower incl. diagonal)
+  zero_acc(acc);
+  mm64<NT>(acc, Q, X);
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = out_row<NT>(i), ci = out_col<NT>(j);
+      s3[r * LDM + ci] = dmask(gs, r, ci) * acc[i][j];
+    }
+  // X dS1 -> s4
+  zero_acc(acc);
+  mm64<NN>(acc, X, dS1);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s4[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
+  __syncthreads();
+  {
+    const float v = row_sum([&](int r, int cc) { return s4[r * LDM + cc] * s2[r * LDM + cc]; });
+    if ((tid & 3) == 0) EdE[tid >> 2] = gs.E[tid >> 2] * v;
+  }
+  // dDelta = (P (.) D)^T dO + diag(E) X dS1 -> s5
+  zero_acc(acc);
+  mm64<TN>(acc, s3, dO);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = out_row<TN>(i), cc = out_col<TN>(j);
+      s5[r * LDM + cc] = acc[i][j] + gs.E[r] * s4[r * LDM + cc];
+    }
+  __syncthreads();
+  // dR = T^T dDelta -> s6 (additive: dR = dDelta)
+  if (reg) {
+    const float* wT = wsmat(a, cg, M_T);
+    for (int i = tid; i < kN * kN; i += kThr) s4[(i / kN) * LDM + i % kN] = wT[i];
+    __syncthreads();
+    zero_acc(acc);
+    mm64<TN>(acc, s4, s5);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s6[out_row<TN>(i) * LDM + out_col<TN>(j)] = acc[i][j];
+  } else {
+    for (int i = tid; i < kN * kN; i += kThr) s6[(i / kN) * LDM + i % kN] = s5[(i / kN) * LDM + i % kN];
+  }
+  __syncthreads();
+  // dV, d eta (residual part), dGamma (residual part)
+  for (int i = tid; i < kN * kN; i += kThr) {
+    const int r = i / kN, cc = i % kN, t = t0 + r;
+    if (t < a.T) stx<Tin>(a.dv, (((size_t)b * a.T + t) * a.H + h) * kN + cc, gs.eta[r] * s6[r * LDM + cc]);
+  }
+  {
+    const int r = tid >> 2;
+    float de, dgr = 0.f;
+    if (reg) {
+      de = row_sum([&](int rr, int cc) { return s6[rr * LDM + cc] * (V[rr * LDM + cc] - gs.Gam[rr] * s1[rr * LDM + cc]); });
+      dgr = -gs.eta[r] * row_sum([&](int rr, int cc) { return s6[rr * LDM + cc] * s1[rr * LDM + cc]; });
+    } else {
+      de = row_sum([&](int rr, int cc) { return s6[rr * LDM + cc] * V[rr * LDM + cc]; });
+    }
+    if ((tid & 3) == 0) { deta[r] = de; dGr[r] = dgr; }
+  }
+  __syncthreads();
+  // M = D (.) dD -> s5;  dX -> s4
+  if (reg) {
+    zero_acc(acc);
+    mm64<NT>(acc, s6, s2);  // dR Delta^T
+    float gacc[4][4];
+    zero_acc(gacc);
+    mm64<NT>(gacc, X, X);   // G
+    __syncthreads();        // s4 (T), s5 consumed
+    float dea[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = out_row<NT>(i), ci = out_col<NT>(j);
+        float dg = 0.f, m = 0.f;
+        if (ci < r) {
+          const float D = __expf(gs.g[r] - gs.g[ci]);
+          const float dA = -acc[i][j];
+          dea[i] += dA * D * gacc[i][j];          // d eta through A = diag(eta) L
+          const float dL = gs.eta[r] * dA;
+          dg = dL * D;                              // dG (strictly lower)
+          m = D * dL * gacc[i][j];                  // D (.) dD
+        }
+        s1[r * LDM + ci] = dg;
+        s5[r * LDM + ci] = m;
+      }
+    // d eta: reduce the 16 threads of a row group (same ty), 4 rows each
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float v = dea[i];
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if ((tid & 15) == 0) deta[out_row<NT>(i)] += v;  // one writer per row
+    }
+    __syncthreads();
+    zero_acc(acc);
+    mm64<NN>(acc, s1, X);   // dG X
+    mm64<TN>(acc, s1, X);   // dG^T X
+    float dx2[4][4];
+    zero_acc(dx2);
+    mm64<NT>(dx2, s6, S0);  // dR S0^T (NT layout)
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s4[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = out_row<NT>(i), cc = out_col<NT>(j);
+        s4[r * LDM + cc] -= gs.eta[r] * gs.Gam[r] * dx2[i][j];
+      }
+  } else {
+    for (int i = tid; i < kN * kN; i += kThr) {
+      s4[(i / kN) * LDM + i % kN] = 0.f;
+      s5[(i / kN) * LDM + i % kN] = 0.f;
+    }
+  }
+  __syncthreads();
+  // dO Delta^T -> M += (dO Delta^T) (.) (P (.) D); dP = (dO Delta^T) (.) D -> s1
+  zero_acc(acc);
+  mm64<NT>(acc, dO, s2);
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = out_row<NT>(i), ci = out_col<NT>(j);
+      s5[r * LDM + ci] += acc[i][j] * s3[r * LDM + ci];
+      s1[r * LDM + ci] = dmask(gs, r, ci) * acc[i][j];
+    }
+  __syncthreads();
+  // dQ = diag(Gamma) dO S0^T + dP X
+  {
+    float qa[4][4], qb[4][4];
+    zero_acc(qa);
+    mm64<NT>(qa, dO, S0);
+    zero_acc(qb);
+    mm64<NN>(qb, s1, X);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s6[out_row<NT>(i) * LDM + out_col<NT>(j)] = gs.Gam[out_row<NT>(i)] * qa[i][j];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s6[out_row<NN>(i) * LDM + out_col<NN>(j)] += qb[i][j];
+  }
+  // dX += dP^T Q + diag(E) Delta dS1^T
+  zero_acc(acc);
+  mm64<TN>(acc, s1, Q);
+  {
+    float xa[4][4];
+    zero_acc(xa);
+    mm64<NT>(xa, s2, dS1);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s4[out_row<TN>(i) * LDM + out_col<TN>(j)] += acc[i][j];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = out_row<NT>(i);
+        s4[r * LDM + out_col<NT>(j)] += gs.E[r] * xa[i][j];
+      }
+  }
+  // row and column sums of M, <S0, dS1>
+  {
+    const float rs = row_sum([&](int r, int cc) { return s5[r * LDM + cc]; });
+    const float cs = row_sum([&](int r, int cc) { return s5[cc * LDM + r]; });
+    const float sd = row_sum([&](int r, int cc) { return S0[r * LDM + cc] * dS1[r * LDM + cc]; });
+    if ((tid & 3) == 0) { rowM[tid >> 2] = rs; colM[tid >> 2] = cs; dgv[tid >> 2] = sd; }
+  }
+  __syncthreads();
+  // outputs: dq, dk (with the norm term), dbeta, dlambda
+  for (int i = tid; i < kN * kN; i += kThr) {
+    const int r = i / kN, cc = i % kN, t = t0 + r;
+    if (t >= a.T) continue;
+    stx<Tin>(a.dq, (((size_t)b * a.T + t) * a.H + h) * kN + cc, s6[r * LDM + cc]);
+    const float dn = gs.ex[r] != 0.f ? -deta[r] * gs.eta[r] / (a.eps + gs.nrm[r]) : 0.f;
+    const float dx = s4[r * LDM + cc] + 2.f * dn * X[r * LDM + cc];
+    if (t - a.shift >= 0) stx<Tin>(a.dk, (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN + cc, dx);
+    else if (a.dk_prev) stx<Tin>(a.dk_prev, (size_t)bh * kN + cc, dx);
+  }
+  if (tid < 32) {  // gate gradients: dg_r, then the reverse cumulative sum over the chunk
+    const float sdS = [&] {
+      float s = 0.f;
+      for (int r = tid; r < kN; r += 32) s += dgv[r];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      return s;
+    }();
+    float sE = EdE[tid] + EdE[tid + 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sE += __shfl_xor_sync(0xffffffffu, sE, o);
+    float d[2];
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int r = tid + 32 * hlf;
+      float dG = dGo[r] + dGr[r] + (r == kN - 1 ? sdS : 0.f);
+      d[hlf] = gs.Gam[r] * dG + rowM[r] - colM[r] - EdE[r] + (r == kN - 1 ? sE : 0.f);
+    }
+    // reverse inclusive scan: dl_s = sum_{r >= s} dg_r
+    float v1 = d[1], v0 = d[0];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n1 = __shfl_down_sync(0xffffffffu, v1, o), n0 = __shfl_down_sync(0xffffffffu, v0, o);
+      if (tid + o < 32) { v1 += n1; v0 += n0; }
+    }
+    v0 += __shfl_sync(0xffffffffu, v1, 0);
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int r = tid + 32 * hlf, t = t0 + r;
+      if (t >= a.T) continue;
+      const size_t gi = ((size_t)b * a.T + t) * a.H + h;
+      const float dl = hlf ? v1 : v0;
+      const float om = 1.f - a.lam[gi];
+      a.dlam[gi] = (om >= a.eps_gamma && om <= 1.f) ? -dl / gs.gam[r] : 0.f;
+      a.dbeta[gi] = gs.ex[r] != 0.f ? deta[r] / (a.eps + gs.nrm[r]) : 0.f;
+    }
+  }
+  if (a.shift == 1 && c == a.NC - 1)  // the last key is the x of no pair of this call
+    for (int cc = tid; cc < kN; cc += kThr) stx<Tin>(a.dk, (((size_t)b * a.T + (a.T - 1)) * a.H + h) * kN + cc, 0.f);
+  if (c == 0 && a.dk_prev && a.shift == 0)
+    for (int cc = tid; cc < kN; cc += kThr) stx<Tin>(a.dk_prev, (size_t)bh * kN + cc, 0.f);
+}
+
+constexpr size_t prep_smem() { return 8 * kN * LDM * sizeof(float) + sizeof(GateSm) + 4 * kN * sizeof(float); }
+constexpr size_t grad_smem() { return 12 * kN * LDM * sizeof(float) + sizeof(GateSm) + 8 * kN * sizeof(float); }
+
+template <typename Tin>
+int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
+  const unsigned nch = (unsigned)(a.B * a.H * a.NC);
+  auto prep = bwdc_prep_kernel<Tin>;
+  auto grad = bwdc_grad_kernel<Tin>;
+  if (!set_smem_limit(reinterpret_cast<const void*>(prep), prep_smem())) return FALCON_ERR_CUDA;
+  if (!set_smem_limit(reinterpret_cast<const void*>(grad), grad_smem())) return FALCON_ERR_CUDA;
+  prep<<<nch, kThr, prep_smem(), s>>>(a);
+  bwdc_fwd_chain_kernel<<<dim3(a.B * a.H, kN / kSC), kThr, 0, s>>>(a);
+  bwdc_bwd_chain_kernel<<<dim3(a.B * a.H, kN / kSC), kThr, 0, s>>>(a);
+  grad<<<nch, kThr, grad_smem(), s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
+}
+
+}  // namespace
+
+bool backward_chunk_supported(int variant, int dk, int dv, int T) {
+  return (variant == FALCON_1 || variant == FALCON_1A) && dk == 64 && dv == 64 && T >= 1;
+}
+
+size_t backward_chunk_ws_bytes(int B, int T, int H) {
+  const size_t NC = (size_t)(T + kN - 1) / kN;
+  return (size_t)B * H * NC * (kMats * kMat + kGateVecs * kN) * sizeof(float);
+}
+
+int launch_backward_chunk(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk, void* dv,
+                          float* dbeta, float* dlam, float* dS_in, void* dk_prev) {
+  CbArgs a;
+  a.B = f.B; a.T = f.T; a.H = f.H; a.NC = (f.T + kN - 1) / kN;
+  a.shift = f.shift; a.additive = variant_additive(f.variant) ? 1 : 0;
+  a.eps = f.eps; a.eps_gamma = f.eps_gamma;
+  a.q = f.q; a.k = f.k; a.v = f.v; a.dO = dO; a.beta = f.beta; a.lam = f.lam;
+  a.S_in = f.S_in; a.kprev_in = f.kprev_in; a.pos_in = f.pos_in; a.dS_final = dS_final;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dbeta = dbeta; a.dlam = dlam; a.dS_in = dS_in; a.dk_prev = dk_prev;
+  a.ws = reinterpret_cast<float*>(f.ws);
+  return f.dtype == FALCON_BF16 ? launch_bwdc_t<__nv_bfloat16>(a, f.stream) : launch_bwdc_t<float>(a, f.stream);
+}
+
+}  // namespace falcon

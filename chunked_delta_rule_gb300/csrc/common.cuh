@@ -122,7 +122,11 @@ int launch_tc_f3a(const FwdArgs& a);
 bool window_scan_supported(const FwdArgs& a);
 size_t window_scan_ws_bytes(int B, int T, int H, int W);
 int launch_window_scan(const FwdArgs& a);
-size_t backward_ws_bytes(int B, int T, int H, int d);
+size_t backward_ws_bytes(int variant, int B, int T, int H, int d);
+bool backward_chunk_supported(int variant, int dk, int dv, int T);
+size_t backward_chunk_ws_bytes(int B, int T, int H);
+int launch_backward_chunk(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk,
+                          void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev);
 bool backward_supported(int variant, int dk, int dv);
 int launch_backward(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk,
                     void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev);
