@@ -36,7 +36,12 @@ namespace {
 
 constexpr int kN = 64;       // chunk rows and head dim
 constexpr int LDM = 68;      // fp32 row stride of the shared-memory matrices
-constexpr int kThr = 256;
+constexpr int kThr = 256;     // per-chunk kernels
+constexpr int kRows = kN * 16 / kThr;  // product rows per thread (16 column groups of 4)
+constexpr int kRowT = kThr / kN;       // threads per row in row sums
+static_assert(kRows * (kThr / 16) == kN && (kRows == 2 || kRows == 4), "product tile must cover 64 rows");
+static_assert(kRowT * kN == kThr && (kN % kRowT) == 0, "row sums must cover 64 rows");
+constexpr int kThrC = 256;    // chain kernels
 constexpr size_t kMat = (size_t)kN * kN;
 enum { M_T = 0, M_W, M_U, M_XT, M_Y, M_S0, M_DS1, kMats };
 constexpr int kGateVecs = 8;  // per chunk: g, Gamma, E, eta, nrm, exists, (2 spare)
@@ -75,29 +80,36 @@ __device__ __forceinline__ float* wsgate(const CbArgs& a, size_t cg) {
 // C (4 x 4 per thread) = op(A) op(B) over K = 64, both operands in shared
 // memory with row stride LDM.  NN: A [M][K], B [K][N]; TN: A [K][M], B [K][N];
 // NT: A [M][K], B [N][K].  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
-// 4 ty + i and columns 4 tx + j (NN, TN) or tx + 16 j (NT).
+// kRows ty + i and columns 4 tx + j (NN, TN) or tx + 16 j (NT).
 template <int MODE>
-__device__ __forceinline__ void mm64(float (&acc)[4][4], const float* __restrict__ A,
+__device__ __forceinline__ void mm64(float (&acc)[kRows][4], const float* __restrict__ A,
                                      const float* __restrict__ B) {
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   if (MODE == TN) {
 #pragma unroll 8
     for (int k = 0; k < kN; ++k) {
-      const float4 av = *reinterpret_cast<const float4*>(&A[k * LDM + 4 * ty]);
+      float a4[kRows];
+      if (kRows == 4) {
+        const float4 av = *reinterpret_cast<const float4*>(&A[k * LDM + kRows * ty]);
+        a4[0] = av.x; a4[1] = av.y; a4[kRows > 2 ? 2 : 0] = av.z; a4[kRows > 3 ? 3 : 0] = av.w;
+      } else {
+        const float2 av = *reinterpret_cast<const float2*>(&A[k * LDM + kRows * ty]);
+        a4[0] = av.x; a4[1] = av.y;
+      }
       const float4 bv = *reinterpret_cast<const float4*>(&B[k * LDM + 4 * tx]);
-      const float a4[4] = {av.x, av.y, av.z, av.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w};
+      const float b4[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < kRows; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a4[i], b4[j], acc[i][j]);
     }
   } else {
 #pragma unroll 2
     for (int k = 0; k < kN; k += 4) {
-      float a4[4][4], b4[4][4];
+      float a4[kRows][4], b4[4][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 av = *reinterpret_cast<const float4*>(&A[(4 * ty + i) * LDM + k]);
+      for (int i = 0; i < kRows; ++i) {
+        const float4 av = *reinterpret_cast<const float4*>(&A[(kRows * ty + i) * LDM + k]);
         a4[i][0] = av.x; a4[i][1] = av.y; a4[i][2] = av.z; a4[i][3] = av.w;
       }
       if (MODE == NN) {  // b4[kk][j] = B[k + kk][4 tx + j]
@@ -107,7 +119,7 @@ __device__ __forceinline__ void mm64(float (&acc)[4][4], const float* __restrict
           b4[kk][0] = bv.x; b4[kk][1] = bv.y; b4[kk][2] = bv.z; b4[kk][3] = bv.w;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < kRows; ++i)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
@@ -119,7 +131,7 @@ __device__ __forceinline__ void mm64(float (&acc)[4][4], const float* __restrict
           b4[j][0] = bv.x; b4[j][1] = bv.y; b4[j][2] = bv.z; b4[j][3] = bv.w;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < kRows; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -130,29 +142,30 @@ __device__ __forceinline__ void mm64(float (&acc)[4][4], const float* __restrict
 }
 
 template <int MODE>
-__device__ __forceinline__ int out_row(int i) { return 4 * (threadIdx.x >> 4) + i; }
+__device__ __forceinline__ int out_row(int i) { return kRows * (threadIdx.x >> 4) + i; }
 template <int MODE>
 __device__ __forceinline__ int out_col(int j) {
   return MODE == NT ? (int)(threadIdx.x & 15) + 16 * j : 4 * (int)(threadIdx.x & 15) + j;
 }
 
-__device__ __forceinline__ void zero_acc(float (&acc)[4][4]) {
+__device__ __forceinline__ void zero_acc(float (&acc)[kRows][4]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 }
 
-// sum over the 64 columns of f(r, c), 4 threads per row; every thread of the
-// row's group returns the row's sum (row = tid / 4)
+// sum over the 64 columns of f(r, c), kRowT threads per row; every thread of
+// the row's group returns the row's sum (row = tid / kRowT)
 template <typename Fn>
 __device__ __forceinline__ float row_sum(Fn f) {
-  const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
+  constexpr int NC_ = kN / kRowT;
+  const int r = threadIdx.x / kRowT, part = threadIdx.x % kRowT;
   float s = 0.f;
 #pragma unroll 4
-  for (int c = part * 16; c < part * 16 + 16; ++c) s += f(r, c);
-  s += __shfl_xor_sync(0xffffffffu, s, 1);
-  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  for (int c = part * NC_; c < part * NC_ + NC_; ++c) s += f(r, c);
+#pragma unroll
+  for (int o = 1; o < kRowT; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   return s;
 }
 
@@ -161,26 +174,68 @@ __device__ __forceinline__ float ldx(const void* p, size_t i) { return to_f32(re
 template <typename Tin>
 __device__ __forceinline__ void stx(void* p, size_t i, float x) { reinterpret_cast<Tin*>(p)[i] = from_f32<Tin>(x); }
 
-// rows of a chunk into shared memory (zero past the end of the call)
+// rows of a chunk into shared memory (zero past the end of the call): every
+// thread issues all of its 16-byte loads before it stores any
 template <typename Tin>
-__device__ void load_rows(float* dst, const void* src, const CbArgs& a, int b, int h, int t0) {
-  for (int i = threadIdx.x; i < kN * kN; i += kThr) {
-    const int r = i / kN, c = i % kN, t = t0 + r;
-    dst[r * LDM + c] = t < a.T ? ldx<Tin>(src, (((size_t)b * a.T + t) * a.H + h) * kN + c) : 0.f;
+__device__ __forceinline__ void load_rows(float* dst, const void* src, const CbArgs& a, int b, int h, int t0) {
+  constexpr int EC = 16 / (int)sizeof(Tin), PR = kN / EC, PT = kN * PR / kThr;  // pieces per row / thread
+  uint4 raw[PT];
+#pragma unroll
+  for (int k = 0; k < PT; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i / PR, c = (i % PR) * EC, t = t0 + r;
+    raw[k] = t < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(src) +
+                                                     (((size_t)b * a.T + t) * a.H + h) * kN + c)
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < PT; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i / PR, c = (i % PR) * EC;
+    const Tin* e = reinterpret_cast<const Tin*>(&raw[k]);
+#pragma unroll
+    for (int q = 0; q < EC; q += 4)
+      *reinterpret_cast<float4*>(&dst[r * LDM + c + q]) =
+          make_float4(to_f32(e[q]), to_f32(e[q + 1]), to_f32(e[q + 2]), to_f32(e[q + 3]));
   }
 }
 // keys of the chunk's pairs: x_r = k_{t - shift}, the carried key for the
 // first pair (prefix), zero where the pair does not exist
 template <typename Tin>
-__device__ void load_keys(float* dst, const CbArgs& a, int b, int h, int t0, int64_t pos) {
-  for (int i = threadIdx.x; i < kN * kN; i += kThr) {
-    const int r = i / kN, c = i % kN, t = t0 + r;
-    float x = 0.f;
+__device__ __forceinline__ void load_keys(float* dst, const CbArgs& a, int b, int h, int t0, int64_t pos) {
+  constexpr int EC = 16 / (int)sizeof(Tin), PR = kN / EC, PT = kN * PR / kThr;
+  uint4 raw[PT];
+#pragma unroll
+  for (int k = 0; k < PT; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i / PR, c = (i % PR) * EC, t = t0 + r;
+    const Tin* row = nullptr;
     if (t < a.T && pos + t >= a.shift) {
-      if (t - a.shift >= 0) x = ldx<Tin>(a.k, (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN + c);
-      else if (a.kprev_in) x = ldx<Tin>(a.kprev_in, ((size_t)b * a.H + h) * kN + c);
+      if (t - a.shift >= 0) row = reinterpret_cast<const Tin*>(a.k) + (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN;
+      else if (a.kprev_in) row = reinterpret_cast<const Tin*>(a.kprev_in) + ((size_t)b * a.H + h) * kN;
     }
-    dst[r * LDM + c] = x;
+    raw[k] = row ? *reinterpret_cast<const uint4*>(row + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < PT; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i / PR, c = (i % PR) * EC;
+    const Tin* e = reinterpret_cast<const Tin*>(&raw[k]);
+#pragma unroll
+    for (int q = 0; q < EC; q += 4)
+      *reinterpret_cast<float4*>(&dst[r * LDM + c + q]) =
+          make_float4(to_f32(e[q]), to_f32(e[q + 1]), to_f32(e[q + 2]), to_f32(e[q + 3]));
+  }
+}
+// a 64 x 64 fp32 workspace matrix into shared memory
+__device__ __forceinline__ void load_mat(float* dst, const float* src) {
+  constexpr int PT = kN * kN / 4 / kThr;
+  float4 v[PT];
+#pragma unroll
+  for (int k = 0; k < PT; ++k) {
+    const int i = threadIdx.x + kThr * k;
+    v[k] = *reinterpret_cast<const float4*>(&src[(i >> 4) * kN + (i & 15) * 4]);
+  }
+#pragma unroll
+  for (int k = 0; k < PT; ++k) {
+    const int i = threadIdx.x + kThr * k;
+    *reinterpret_cast<float4*>(&dst[(i >> 4) * LDM + (i & 15) * 4]) = v[k];
   }
 }
 
@@ -243,7 +298,6 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   float* M3 = Tm + kN * LDM;
   float* Wm = M3 + kN * LDM;
   GateSm& gs = *reinterpret_cast<GateSm*>(Wm + kN * LDM);
-  float* red = reinterpret_cast<float*>(&gs + 1);  // [4][64]
   const size_t cg = blockIdx.x;
   const int c = (int)(cg % a.NC), bh = (int)(cg / a.NC), b = bh / a.H, h = bh % a.H, t0 = c * kN;
   const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
@@ -254,32 +308,38 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   load_rows<Tin>(dO, a.dO, a, b, h, t0);
   __syncthreads();
   make_gates(gs, X, a, b, h, t0, pos);
-  float acc[4][4];
+  float acc[kRows][4];
   if (!a.additive) {
     // A = diag(eta) (D (.) X X^T), strictly lower
     zero_acc(acc);
     mm64<NT>(acc, X, X);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = out_row<NT>(i), ci = out_col<NT>(j);
         M1[r * LDM + ci] = ci < r ? gs.eta[r] * __expf(gs.g[r] - gs.g[ci]) * acc[i][j] : 0.f;
       }
     __syncthreads();
-    // T = (I + A)^{-1} row by row: T_r = e_r - sum_{i<r} A_ri T_i (column per thread, 4 partial sums)
-    {
-      const int col = tid & 63, part = tid >> 6;
+    // T = (I + A)^{-1}: thread j < 64 solves column j by forward substitution,
+    // the column in registers, the rows of A read as broadcasts
+    if (tid < kN) {
+      const int j = tid;
+      float tcol[kN];
+#pragma unroll
       for (int r = 0; r < kN; ++r) {
-        float s = 0.f;
-        for (int i = part; i < r; i += 4) s = fmaf(M1[r * LDM + i], Tm[i * LDM + col], s);
-        red[part * kN + col] = s;
-        __syncthreads();
-        if (part == 0)
-          Tm[r * LDM + col] = (r == col ? 1.f : 0.f) - (red[col] + red[kN + col] + red[2 * kN + col] + red[3 * kN + col]);
-        __syncthreads();
+        float s0 = (r == j) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < r; i += 2) {
+          s0 = fmaf(-M1[r * LDM + i], tcol[i], s0);
+          if (i + 1 < r) s1 = fmaf(-M1[r * LDM + i + 1], tcol[i + 1], s1);
+        }
+        tcol[r] = s0 + s1;
       }
+#pragma unroll
+      for (int r = 0; r < kN; ++r) Tm[r * LDM + j] = tcol[r];
     }
+    __syncthreads();
     // W = T diag(eta Gamma) X, U = T diag(eta) V
     for (int i = tid; i < kN * kN; i += kThr) {
       const int r = i / kN, cc = i % kN;
@@ -291,7 +351,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
     mm64<NN>(acc, Tm, M3);
     float* wW = wsmat(a, cg, M_W);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = out_row<NN>(i), cc = out_col<NN>(j);
@@ -302,7 +362,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
     mm64<NN>(acc, Tm, M1);
     float* wU = wsmat(a, cg, M_U);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) wU[out_row<NN>(i) * kN + out_col<NN>(j)] = acc[i][j];
     float* wT = wsmat(a, cg, M_T);
@@ -330,7 +390,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   zero_acc(acc);
   mm64<NT>(acc, Q, X);  // P = Q X^T
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = out_row<NT>(i), ci = out_col<NT>(j);
@@ -341,7 +401,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
     M3[r * LDM + cc] = gs.Gam[r] * dO[r * LDM + cc];
   }
   __syncthreads();
-  float yacc[4][4];
+  float yacc[kRows][4];
   zero_acc(yacc);
   mm64<TN>(yacc, Q, M3);  // Q^T diag(Gamma) dO
   if (!a.additive) {
@@ -349,148 +409,207 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
     mm64<TN>(acc, M1, dO);  // Z = (P (.) D)^T dO
     __syncthreads();        // M3 is read by every thread above
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) M3[out_row<TN>(i) * LDM + out_col<TN>(j)] = acc[i][j];
     __syncthreads();
-    float wz[4][4];
+    float wz[kRows][4];
     zero_acc(wz);
     mm64<TN>(wz, Wm, M3);  // W^T Z
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) yacc[i][j] -= wz[i][j];
   }
   float* wY = wsmat(a, cg, M_Y);
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) wY[out_row<TN>(i) * kN + out_col<TN>(j)] = yacc[i][j];
 }
 
 // ---------------------------------------------------------------- (b), (c)
-// One CTA per (b, h, 16 value columns); S (or dS) slice 64 x 16 in shared
-// memory.  Thread (r = tid / 4, quad = tid % 4) owns row r, columns 4 quad..
+// One CTA of 256 threads per (b, h, 16 value columns); the S (or dS) slice,
+// 64 x 16, in shared memory.  Thread (r = tid / 4, quad = tid % 4) owns row r,
+// columns 4 quad .. 4 quad + 3.  The next chunk's W, diag(E) X, value slice (U
+// or Y) and decay arrive by cp.async into the other of two stages.
 constexpr int kSC = 16;
+constexpr int CPT = kSC / 4;  // columns per thread
 constexpr int LDS_ = kSC + 4;
 
-__global__ void __launch_bounds__(kThr) bwdc_fwd_chain_kernel(CbArgs a) {
-  __shared__ __align__(16) float Wsm[kN * LDM];
-  __shared__ __align__(16) float Xsm[kN * LDM];
-  __shared__ __align__(16) float S[kN * LDS_];
-  __shared__ __align__(16) float Dl[kN * LDS_];
-  const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
-  const int r = tid >> 2, q4 = (tid & 3) * 4;
-  for (int i = tid; i < kN * kSC; i += kThr) {
-    const int rr = i / kSC, cc = i % kSC;
-    S[rr * LDS_ + cc] = a.S_in ? a.S_in[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
-  }
-  for (int c = 0; c < a.NC; ++c) {
-    const size_t cg = (size_t)bh * a.NC + c;
-    __syncthreads();
-    {  // chunk start state out; this chunk's W, diag(E) X in
-      float* wS = wsmat(a, cg, M_S0);
-      for (int i = tid; i < kN * kSC; i += kThr) wS[(i / kSC) * kN + c0 + i % kSC] = S[(i / kSC) * LDS_ + i % kSC];
-      const float* wW = wsmat(a, cg, M_W);
-      const float* wX = wsmat(a, cg, M_XT);
-      for (int i = tid; i < kN * kN / 4; i += kThr) {
-        const int rr = i / (kN / 4), cc = 4 * (i % (kN / 4));
-        if (!a.additive) *reinterpret_cast<float4*>(&Wsm[rr * LDM + cc]) = *reinterpret_cast<const float4*>(&wW[rr * kN + cc]);
-        *reinterpret_cast<float4*>(&Xsm[rr * LDM + cc]) = *reinterpret_cast<const float4*>(&wX[rr * kN + cc]);
-      }
-    }
-    __syncthreads();
-    const float* wU = wsmat(a, cg, M_U);
-    float d[4];
+struct ChainStage {
+  float W[kN * LDM];
+  float X[kN * LDM];
+  float C[kN * LDS_];   // U (forward) or Y (backward) slice
+  float g4[4];          // Gamma of rows 60..63
+};
+struct ChainSmem {
+  ChainStage st[2];
+  float S[kN * LDS_];
+  float Dl[kN * LDS_];
+};
+
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void chain_stage(const CbArgs& a, ChainStage& st, size_t cg, int c0, int which_c) {
+  const int tid = threadIdx.x;
+  const float* wW = wsmat(a, cg, M_W);
+  const float* wX = wsmat(a, cg, M_XT);
+  const float* wC = wsmat(a, cg, which_c);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) d[j] = wU[(size_t)r * kN + c0 + q4 + j];
-    if (!a.additive) {  // Delta = U - W S
-      for (int k = 0; k < kN; ++k) {
-        const float w = Wsm[r * LDM + k];
-        const float4 s4 = *reinterpret_cast<const float4*>(&S[k * LDS_ + q4]);
-        d[0] -= w * s4.x; d[1] -= w * s4.y; d[2] -= w * s4.z; d[3] -= w * s4.w;
-      }
-    }
-    *reinterpret_cast<float4*>(&Dl[r * LDS_ + q4]) = make_float4(d[0], d[1], d[2], d[3]);
-    __syncthreads();
-    // S = Gamma_63 S + (diag(E) X)^T Delta   (row r of S is key index r)
-    const float G63 = wsgate(a, cg)[kN + kN - 1];
-    float s[4];
-    {
-      const float4 s4 = *reinterpret_cast<const float4*>(&S[r * LDS_ + q4]);
-      s[0] = G63 * s4.x; s[1] = G63 * s4.y; s[2] = G63 * s4.z; s[3] = G63 * s4.w;
-    }
-    for (int i = 0; i < kN; ++i) {
-      const float x = Xsm[i * LDM + r];
-      const float4 d4 = *reinterpret_cast<const float4*>(&Dl[i * LDS_ + q4]);
-      s[0] = fmaf(x, d4.x, s[0]); s[1] = fmaf(x, d4.y, s[1]); s[2] = fmaf(x, d4.z, s[2]); s[3] = fmaf(x, d4.w, s[3]);
-    }
-    __syncthreads();
-    *reinterpret_cast<float4*>(&S[r * LDS_ + q4]) = make_float4(s[0], s[1], s[2], s[3]);
+  for (int k = 0; k < kN * kN / 4 / kThrC; ++k) {
+    const int i = tid + kThrC * k, r = i >> 4, c = (i & 15) * 4;
+    if (!a.additive) cp16(&st.W[r * LDM + c], &wW[r * kN + c]);
+    cp16(&st.X[r * LDM + c], &wX[r * kN + c]);
   }
+#pragma unroll
+  for (int k = 0; k < kN * kSC / 4 / kThrC; ++k) {
+    const int i = tid + kThrC * k, r = i / (kSC / 4), c = (i % (kSC / 4)) * 4;
+    cp16(&st.C[r * LDS_ + c], &wC[r * kN + c0 + c]);
+  }
+  if (tid == 0) cp16(st.g4, wsgate(a, cg) + kN + kN - 4);
 }
 
-__global__ void __launch_bounds__(kThr) bwdc_bwd_chain_kernel(CbArgs a) {
-  __shared__ __align__(16) float Wsm[kN * LDM];
-  __shared__ __align__(16) float Xsm[kN * LDM];
-  __shared__ __align__(16) float dS[kN * LDS_];
-  __shared__ __align__(16) float Z[kN * LDS_];
-  const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
-  const int r = tid >> 2, q4 = (tid & 3) * 4;
-  for (int i = tid; i < kN * kSC; i += kThr) {
-    const int rr = i / kSC, cc = i % kSC;
-    dS[rr * LDS_ + cc] = a.dS_final ? a.dS_final[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
+__device__ __forceinline__ void ldcs(float (&v)[CPT], const float* p) {
+#pragma unroll
+  for (int q = 0; q < CPT; q += 4) {
+    const float4 a = *reinterpret_cast<const float4*>(p + q);
+    v[q] = a.x; v[q + 1] = a.y; v[q + 2] = a.z; v[q + 3] = a.w;
   }
-  for (int c = a.NC - 1; c >= 0; --c) {
+}
+__device__ __forceinline__ void stcs(float* p, const float (&v)[CPT]) {
+#pragma unroll
+  for (int q = 0; q < CPT; q += 4) *reinterpret_cast<float4*>(p + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+}
+
+__global__ void __launch_bounds__(kThrC) bwdc_fwd_chain_kernel(CbArgs a) {
+  extern __shared__ float4 smem_f4[];
+  ChainSmem& sm = *reinterpret_cast<ChainSmem*>(smem_f4);
+  const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
+  const int r = tid >> 2, q8 = (tid & 3) * CPT;
+  for (int i = tid; i < kN * kSC; i += kThrC) {
+    const int rr = i / kSC, cc = i % kSC;
+    sm.S[rr * LDS_ + cc] = a.S_in ? a.S_in[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
+  }
+  chain_stage(a, sm.st[0], (size_t)bh * a.NC, c0, M_U);
+  cp_commit();
+  if (a.NC > 1) chain_stage(a, sm.st[1], (size_t)bh * a.NC + 1, c0, M_U);
+  cp_commit();
+  for (int c = 0; c < a.NC; ++c) {
     const size_t cg = (size_t)bh * a.NC + c;
+    ChainStage& st = sm.st[c & 1];
+    cp_wait1();
     __syncthreads();
-    {
-      float* wD = wsmat(a, cg, M_DS1);
-      for (int i = tid; i < kN * kSC; i += kThr) wD[(i / kSC) * kN + c0 + i % kSC] = dS[(i / kSC) * LDS_ + i % kSC];
-      const float* wW = wsmat(a, cg, M_W);
-      const float* wX = wsmat(a, cg, M_XT);
-      for (int i = tid; i < kN * kN / 4; i += kThr) {
-        const int rr = i / (kN / 4), cc = 4 * (i % (kN / 4));
-        if (!a.additive) *reinterpret_cast<float4*>(&Wsm[rr * LDM + cc]) = *reinterpret_cast<const float4*>(&wW[rr * kN + cc]);
-        *reinterpret_cast<float4*>(&Xsm[rr * LDM + cc]) = *reinterpret_cast<const float4*>(&wX[rr * kN + cc]);
+    float v[CPT];
+    ldcs(v, &sm.S[r * LDS_ + q8]);
+    {  // chunk start state out
+      stcs(&wsmat(a, cg, M_S0)[(size_t)r * kN + c0 + q8], v);
+    }
+    float d[CPT];
+    ldcs(d, &st.C[r * LDS_ + q8]);
+    if (!a.additive) {  // Delta = U - W S
+#pragma unroll 4
+      for (int k = 0; k < kN; ++k) {
+        const float w = st.W[r * LDM + k];
+        float sk[CPT];
+        ldcs(sk, &sm.S[k * LDS_ + q8]);
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) d[e] = fmaf(-w, sk[e], d[e]);
       }
     }
+    stcs(&sm.Dl[r * LDS_ + q8], d);
     __syncthreads();
+    // S = Gamma_63 S + (diag(E) X)^T Delta   (row r of S is key index r)
+    const float G63 = st.g4[3];
+#pragma unroll
+    for (int e = 0; e < CPT; ++e) v[e] *= G63;
+#pragma unroll 4
+    for (int i = 0; i < kN; ++i) {
+      const float x = st.X[i * LDM + r];
+      float di[CPT];
+      ldcs(di, &sm.Dl[i * LDS_ + q8]);
+#pragma unroll
+      for (int e = 0; e < CPT; ++e) v[e] = fmaf(x, di[e], v[e]);
+    }
+    __syncthreads();  // every read of S and of this stage is done
+    stcs(&sm.S[r * LDS_ + q8], v);
+    if (c + 2 < a.NC) chain_stage(a, st, cg + 2, c0, M_U);
+    cp_commit();
+  }
+  cp_wait0();
+}
+
+__global__ void __launch_bounds__(kThrC) bwdc_bwd_chain_kernel(CbArgs a) {
+  extern __shared__ float4 smem_f4[];
+  ChainSmem& sm = *reinterpret_cast<ChainSmem*>(smem_f4);
+  const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
+  const int r = tid >> 2, q8 = (tid & 3) * CPT;
+  for (int i = tid; i < kN * kSC; i += kThrC) {
+    const int rr = i / kSC, cc = i % kSC;
+    sm.S[rr * LDS_ + cc] = a.dS_final ? a.dS_final[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
+  }
+  const size_t base = (size_t)bh * a.NC;
+  chain_stage(a, sm.st[0], base + a.NC - 1, c0, M_Y);
+  cp_commit();
+  if (a.NC > 1) chain_stage(a, sm.st[1], base + a.NC - 2, c0, M_Y);
+  cp_commit();
+  for (int n = 0; n < a.NC; ++n) {
+    const int c = a.NC - 1 - n;
+    const size_t cg = base + c;
+    ChainStage& st = sm.st[n & 1];
+    cp_wait1();
+    __syncthreads();
+    float v[CPT];
+    ldcs(v, &sm.S[r * LDS_ + q8]);
+    {  // gradient of the chunk's end state out
+      stcs(&wsmat(a, cg, M_DS1)[(size_t)r * kN + c0 + q8], v);
+    }
     if (!a.additive) {  // Z = diag(E) X dS  (row r = chunk row)
-      float z[4] = {0.f, 0.f, 0.f, 0.f};
+      float z[CPT] = {};
+#pragma unroll 4
       for (int k = 0; k < kN; ++k) {
-        const float x = Xsm[r * LDM + k];
-        const float4 d4 = *reinterpret_cast<const float4*>(&dS[k * LDS_ + q4]);
-        z[0] = fmaf(x, d4.x, z[0]); z[1] = fmaf(x, d4.y, z[1]); z[2] = fmaf(x, d4.z, z[2]); z[3] = fmaf(x, d4.w, z[3]);
+        const float x = st.X[r * LDM + k];
+        float sk[CPT];
+        ldcs(sk, &sm.S[k * LDS_ + q8]);
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) z[e] = fmaf(x, sk[e], z[e]);
       }
-      *reinterpret_cast<float4*>(&Z[r * LDS_ + q4]) = make_float4(z[0], z[1], z[2], z[3]);
+      stcs(&sm.Dl[r * LDS_ + q8], z);
     }
     __syncthreads();
     // dS = Gamma_63 dS - W^T Z + Y   (row r = key index)
-    const float G63 = wsgate(a, cg)[kN + kN - 1];
-    const float* wY = wsmat(a, cg, M_Y);
-    float s[4];
-    {
-      const float4 d4 = *reinterpret_cast<const float4*>(&dS[r * LDS_ + q4]);
-      s[0] = G63 * d4.x + wY[(size_t)r * kN + c0 + q4];
-      s[1] = G63 * d4.y + wY[(size_t)r * kN + c0 + q4 + 1];
-      s[2] = G63 * d4.z + wY[(size_t)r * kN + c0 + q4 + 2];
-      s[3] = G63 * d4.w + wY[(size_t)r * kN + c0 + q4 + 3];
-    }
+    const float G63 = st.g4[3];
+    float y[CPT];
+    ldcs(y, &st.C[r * LDS_ + q8]);
+#pragma unroll
+    for (int e = 0; e < CPT; ++e) v[e] = fmaf(G63, v[e], y[e]);
     if (!a.additive) {
+#pragma unroll 4
       for (int i = 0; i < kN; ++i) {
-        const float w = Wsm[i * LDM + r];
-        const float4 z4 = *reinterpret_cast<const float4*>(&Z[i * LDS_ + q4]);
-        s[0] -= w * z4.x; s[1] -= w * z4.y; s[2] -= w * z4.z; s[3] -= w * z4.w;
+        const float w = st.W[i * LDM + r];
+        float zi[CPT];
+        ldcs(zi, &sm.Dl[i * LDS_ + q8]);
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) v[e] = fmaf(-w, zi[e], v[e]);
       }
     }
     __syncthreads();
-    *reinterpret_cast<float4*>(&dS[r * LDS_ + q4]) = make_float4(s[0], s[1], s[2], s[3]);
+    stcs(&sm.S[r * LDS_ + q8], v);
+    if (n + 2 < a.NC) chain_stage(a, st, base + a.NC - 3 - n, c0, M_Y);
+    cp_commit();
   }
+  cp_wait0();
   __syncthreads();
   if (a.dS_in)
-    for (int i = tid; i < kN * kSC; i += kThr)
-      a.dS_in[((size_t)bh * kN + i / kSC) * kN + c0 + i % kSC] = dS[(i / kSC) * LDS_ + i % kSC];
+    for (int i = tid; i < kN * kSC; i += kThrC)
+      a.dS_in[((size_t)bh * kN + i / kSC) * kN + c0 + i % kSC] = sm.S[(i / kSC) * LDS_ + i % kSC];
 }
 
 // ---------------------------------------------------------------- (d)
@@ -529,15 +648,11 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   load_rows<Tin>(V, a.v, a, b, h, t0);
   load_rows<Tin>(dO, a.dO, a, b, h, t0);
   {
-    const float* wS = wsmat(a, cg, M_S0);
-    const float* wD = wsmat(a, cg, M_DS1);
-    const float* wW = wsmat(a, cg, M_W);
-    const float* wU = wsmat(a, cg, M_U);
-    for (int i = tid; i < kN * kN; i += kThr) {
-      const int r = i / kN, cc = i % kN;
-      S0[r * LDM + cc] = wS[i];
-      dS1[r * LDM + cc] = wD[i];
-      if (reg) { s1[r * LDM + cc] = wW[i]; s2[r * LDM + cc] = wU[i]; }
+    load_mat(S0, wsmat(a, cg, M_S0));
+    load_mat(dS1, wsmat(a, cg, M_DS1));
+    if (reg) {
+      load_mat(s1, wsmat(a, cg, M_W));
+      load_mat(s2, wsmat(a, cg, M_U));
     }
     const float* gv = wsgate(a, cg);
     if (tid < kN) {
@@ -546,14 +661,14 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     }
   }
   __syncthreads();
-  float acc[4][4];
+  float acc[kRows][4];
   // Delta -> s2
   if (reg) {
     zero_acc(acc);
     mm64<NN>(acc, s1, S0);
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = out_row<NN>(i), cc = out_col<NN>(j);
@@ -571,20 +686,20 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     mm64<NN>(acc, X, S0);
     __syncthreads();  // s1 (W) is consumed
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s1[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
   }
   zero_acc(acc);
   mm64<NN>(acc, Q, S0);
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) s3[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
   __syncthreads();
   {
     const float v = row_sum([&](int r, int cc) { return dO[r * LDM + cc] * s3[r * LDM + cc]; });
-    if ((tid & 3) == 0) dGo[tid >> 2] = v;
+    if (tid % kRowT == 0) dGo[tid / kRowT] = v;
   }
   __syncthreads();
   // P (.) D -> s3 (lower incl. diagonal)
@@ -592,7 +707,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   mm64<NT>(acc, Q, X);
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = out_row<NT>(i), ci = out_col<NT>(j);
@@ -602,19 +717,19 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   zero_acc(acc);
   mm64<NN>(acc, X, dS1);
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) s4[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
   __syncthreads();
   {
     const float v = row_sum([&](int r, int cc) { return s4[r * LDM + cc] * s2[r * LDM + cc]; });
-    if ((tid & 3) == 0) EdE[tid >> 2] = gs.E[tid >> 2] * v;
+    if (tid % kRowT == 0) EdE[tid / kRowT] = gs.E[tid / kRowT] * v;
   }
   // dDelta = (P (.) D)^T dO + diag(E) X dS1 -> s5
   zero_acc(acc);
   mm64<TN>(acc, s3, dO);
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = out_row<TN>(i), cc = out_col<TN>(j);
@@ -623,13 +738,12 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   __syncthreads();
   // dR = T^T dDelta -> s6 (additive: dR = dDelta)
   if (reg) {
-    const float* wT = wsmat(a, cg, M_T);
-    for (int i = tid; i < kN * kN; i += kThr) s4[(i / kN) * LDM + i % kN] = wT[i];
+    load_mat(s4, wsmat(a, cg, M_T));
     __syncthreads();
     zero_acc(acc);
     mm64<TN>(acc, s4, s5);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s6[out_row<TN>(i) * LDM + out_col<TN>(j)] = acc[i][j];
   } else {
@@ -642,7 +756,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     if (t < a.T) stx<Tin>(a.dv, (((size_t)b * a.T + t) * a.H + h) * kN + cc, gs.eta[r] * s6[r * LDM + cc]);
   }
   {
-    const int r = tid >> 2;
+    const int r = tid / kRowT;
     float de, dgr = 0.f;
     if (reg) {
       de = row_sum([&](int rr, int cc) { return s6[rr * LDM + cc] * (V[rr * LDM + cc] - gs.Gam[rr] * s1[rr * LDM + cc]); });
@@ -650,20 +764,20 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     } else {
       de = row_sum([&](int rr, int cc) { return s6[rr * LDM + cc] * V[rr * LDM + cc]; });
     }
-    if ((tid & 3) == 0) { deta[r] = de; dGr[r] = dgr; }
+    if (tid % kRowT == 0) { deta[r] = de; dGr[r] = dgr; }
   }
   __syncthreads();
   // M = D (.) dD -> s5;  dX -> s4
   if (reg) {
     zero_acc(acc);
     mm64<NT>(acc, s6, s2);  // dR Delta^T
-    float gacc[4][4];
+    float gacc[kRows][4];
     zero_acc(gacc);
     mm64<NT>(gacc, X, X);   // G
     __syncthreads();        // s4 (T), s5 consumed
-    float dea[4] = {0.f, 0.f, 0.f, 0.f};
+    float dea[kRows] = {};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = out_row<NT>(i), ci = out_col<NT>(j);
@@ -681,7 +795,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
       }
     // d eta: reduce the 16 threads of a row group (same ty), 4 rows each
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kRows; ++i) {
       float v = dea[i];
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -691,17 +805,17 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     zero_acc(acc);
     mm64<NN>(acc, s1, X);   // dG X
     mm64<TN>(acc, s1, X);   // dG^T X
-    float dx2[4][4];
+    float dx2[kRows][4];
     zero_acc(dx2);
     mm64<NT>(dx2, s6, S0);  // dR S0^T (NT layout)
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s4[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = out_row<NT>(i), cc = out_col<NT>(j);
@@ -719,7 +833,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   mm64<NT>(acc, dO, s2);
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = out_row<NT>(i), ci = out_col<NT>(j);
@@ -729,19 +843,19 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   __syncthreads();
   // dQ = diag(Gamma) dO S0^T + dP X
   {
-    float qa[4][4], qb[4][4];
+    float qa[kRows][4], qb[kRows][4];
     zero_acc(qa);
     mm64<NT>(qa, dO, S0);
     zero_acc(qb);
     mm64<NN>(qb, s1, X);
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s6[out_row<NT>(i) * LDM + out_col<NT>(j)] = gs.Gam[out_row<NT>(i)] * qa[i][j];
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s6[out_row<NN>(i) * LDM + out_col<NN>(j)] += qb[i][j];
   }
@@ -749,17 +863,17 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   zero_acc(acc);
   mm64<TN>(acc, s1, Q);
   {
-    float xa[4][4];
+    float xa[kRows][4];
     zero_acc(xa);
     mm64<NT>(xa, s2, dS1);
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s4[out_row<TN>(i) * LDM + out_col<TN>(j)] += acc[i][j];
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = out_row<NT>(i);
@@ -771,7 +885,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     const float rs = row_sum([&](int r, int cc) { return s5[r * LDM + cc]; });
     const float cs = row_sum([&](int r, int cc) { return s5[cc * LDM + r]; });
     const float sd = row_sum([&](int r, int cc) { return S0[r * LDM + cc] * dS1[r * LDM + cc]; });
-    if ((tid & 3) == 0) { rowM[tid >> 2] = rs; colM[tid >> 2] = cs; dgv[tid >> 2] = sd; }
+    if (tid % kRowT == 0) { rowM[tid / kRowT] = rs; colM[tid / kRowT] = cs; dgv[tid / kRowT] = sd; }
   }
   __syncthreads();
   // outputs: dq, dk (with the norm term), dbeta, dlambda
@@ -837,9 +951,12 @@ int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
   auto grad = bwdc_grad_kernel<Tin>;
   if (!set_smem_limit(reinterpret_cast<const void*>(prep), prep_smem())) return FALCON_ERR_CUDA;
   if (!set_smem_limit(reinterpret_cast<const void*>(grad), grad_smem())) return FALCON_ERR_CUDA;
+  if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_fwd_chain_kernel), sizeof(ChainSmem)) ||
+      !set_smem_limit(reinterpret_cast<const void*>(bwdc_bwd_chain_kernel), sizeof(ChainSmem)))
+    return FALCON_ERR_CUDA;
   prep<<<nch, kThr, prep_smem(), s>>>(a);
-  bwdc_fwd_chain_kernel<<<dim3(a.B * a.H, kN / kSC), kThr, 0, s>>>(a);
-  bwdc_bwd_chain_kernel<<<dim3(a.B * a.H, kN / kSC), kThr, 0, s>>>(a);
+  bwdc_fwd_chain_kernel<<<dim3(a.B * a.H, kN / kSC), kThrC, sizeof(ChainSmem), s>>>(a);
+  bwdc_bwd_chain_kernel<<<dim3(a.B * a.H, kN / kSC), kThrC, sizeof(ChainSmem), s>>>(a);
   grad<<<nch, kThr, grad_smem(), s>>>(a);
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
