@@ -357,9 +357,12 @@ def run_backward(args, w):
                                  "pairing": w.pairing, "l2": f"rotating {len(sets)} input sets"},
                       "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                                    "frac": gbs / peak, "algorithmic_bytes": nbytes,
-                                   "kernel": "falcon_bwd_kernel",
+                                   "kernel": ("bwdc_prep_kernel + bwdc_fwd_chain_kernel + bwdc_bwd_chain_kernel + "
+                                              "bwdc_grad_kernel (whole call)")
+                                   if (w.variant in (0, 1) and w.dk == 64 and w.dv == 64) else "falcon_bwd_kernel",
                                    "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
-                      "gpu_launches": args.steps, "clocks": clk}), flush=True)
+                      "gpu_launches": args.steps * (4 if (w.variant in (0, 1) and w.dk == 64) else 1),
+                      "clocks": clk}), flush=True)
 
 
 VARLEN_FRACTIONS = (1.0, 0.75, 0.5, 0.25, 1.0, 0.125, 0.875, 0.375)
