@@ -210,8 +210,10 @@ __global__ void __launch_bounds__(kRecThreads) recurrent_step_kernel(FwdArgs a) 
 // accesses (every warp moves whole 256/512-byte rows), partial predictions
 // reduced with shuffles and one shared-memory pass, two CTA barriers.
 // Thread t owns 4 value columns (quad t % NQ) of the rows rg + RGS * i.
+// (d = 64: at most 64 registers a thread so that eight CTAs share an SM and
+// keep eight states in flight per SM)
 template <typename Tin, int D, int NT, int MAXW>
-__global__ void __launch_bounds__(NT) recurrent_step_vec_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(NT, D == 64 ? 8 : 1) recurrent_step_vec_kernel(FwdArgs a) {
   constexpr int NQ = D / 4;          // column quads
   constexpr int RGS = NT / NQ;       // row groups
   constexpr int RPT = D / RGS;       // rows per thread
