@@ -30,6 +30,30 @@ sys.path.insert(0, ROOT)
 
 N_SETS = 4
 VARIANT_NAMES = ("falcon1", "falcon1a", "falcon2", "falcon2a", "falcon3", "falcon3a")
+METRIC = "Falcon-1 chunked fwd tokens/s and % of roofline (GB300, T=2048, H=12, d=64)"
+
+
+# ---- replicas across ranks (the path has no exchange step: each rank runs
+# its own batch; only the timing is combined)
+def replica_seed(w, rank: int, i: int) -> int:
+    """Seed of input set i on rank `rank`: every replica draws its own batch."""
+    return w.seed + 100 * rank + i
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (the job's time); world 1 passes it through."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(w, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return w.B * w.T * world / (ms_per_step / 1e3)
 
 
 def parse():
@@ -207,12 +231,14 @@ def run_reference(args, w, rank):
         oracle.recurrent(**x, variant=w.variant, window=w.window, pairing=w.pairing)
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
     value = nb * T / dt
-    line = {"impl": "reference", "metric": "Falcon-1 chunked fwd tokens/s", "value": value,
+    line = {"impl": "reference", "metric": METRIC, "value": value,
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                       "chunk": w.chunk, "variant": "falcon1", "reference_sample": f"{nb}x{T}x{w.H}"},
+                       "chunk": w.chunk, "variant": VARIANT_NAMES[w.variant], "global_batch": w.B * args.gpus,
+                       "seq_len": w.T, "parallelism": f"replicas x{args.gpus}",
+                       "reference_sample": f"{nb}x{T}x{w.H}"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"{nb} sequence x {T} tokens x {w.H} heads per step, fp64 "
                                        "numpy recurrence, single thread"},
@@ -478,7 +504,7 @@ def main():
                  prologue=3 if args.prologue else 0)
     from workloads import make_raw_inputs
     gen = make_raw_inputs if args.prologue else make_inputs
-    sets = [gen(w, seed=w.seed + 100 * rank + i, device=dev) for i in range(args.sets)]
+    sets = [gen(w, seed=replica_seed(w, rank, i), device=dev) for i in range(args.sets)]
     o = torch.empty((w.B, w.T, w.H, w.dv), dtype=sets[0]["q"].dtype, device=dev)
     carry = F.empty_carry(p, dev)
     ws_n = F.falcon_workspace_size(p)
@@ -523,17 +549,13 @@ def main():
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), world, dev)
     kern_ms = [statistics.mean(evs[j].elapsed_time(evs[j + 1]) for evs in ev)
                for j in range(launches)]
     per_call_ms = statistics.mean(evs[0].elapsed_time(evs[-1]) for evs in ev)
     ms_step = ms / args.steps
     tokens = w.B * w.T * world
-    value = tokens / (ms_step / 1e3)
+    value = job_tokens_per_s(w, world, ms_step)
 
     # end to end through the C ABI with host buffers: pinned host -> device
     # copies of the step's inputs, the call, and the output read back
@@ -562,11 +584,7 @@ def main():
         o_host.copy_(o, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
 
     if rank == 0:
         peaks = {}
@@ -612,7 +630,7 @@ def main():
                     "frac": fl / alu_peak, "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 "
                     "flop x SM clock", "hbm_achieved_gbs": achieved, "hbm_frac": achieved / hbm_peak}
         line = {
-            "metric": "Falcon-1 chunked fwd tokens/s and % of roofline (GB300, T=2048, H=12, d=64)",
+            "metric": METRIC,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
