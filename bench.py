@@ -527,13 +527,6 @@ def main():
     clocks = ClockSampler(gpu_index)
     clocks.start()
     time.sleep(0.3)
-    # per-kernel events: the library records them around each kernel it launches
-    nev = launches + 1
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
-    for evs in ev:
-        for e in evs:
-            e.record(stream)   # creates the event handles before they are handed over
-    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -541,15 +534,27 @@ def main():
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(args.steps):
-        x = sets[i % len(sets)]
-        F.falcon_chunk_fwd_timed(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o, carry,
-                                 ws, ws_n, stream, ev[i])
+        step(i)
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    # per-kernel times, in a separate pass: the library records the caller's
+    # events around each kernel it launches (which keeps every kernel apart)
+    nev = launches + 1
+    n_k = min(args.steps, 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n_k)]
+    for evs in ev:
+        for e in evs:
+            e.record(stream)   # creates the event handles before they are handed over
+    torch.cuda.synchronize()
+    for i in range(n_k):
+        x = sets[i % len(sets)]
+        F.falcon_chunk_fwd_timed(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o, carry,
+                                 ws, ws_n, stream, ev[i])
+    torch.cuda.synchronize()
     kern_ms = [statistics.mean(evs[j].elapsed_time(evs[j + 1]) for evs in ev)
                for j in range(launches)]
     per_call_ms = statistics.mean(evs[0].elapsed_time(evs[-1]) for evs in ev)
@@ -616,7 +621,7 @@ def main():
         dom = max(range(launches), key=lambda j: kern_ms[j])
         kernel = names[dom]
         achieved = kbytes[dom] / (kern_ms[dom] / 1e3) / 1e9
-        step_achieved = abytes / (per_call_ms / 1e3) / 1e9
+        step_achieved = abytes / (ms_step / 1e3) / 1e9  # the whole step, kernels overlapped
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak,
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}

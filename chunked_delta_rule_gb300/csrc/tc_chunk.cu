@@ -368,6 +368,9 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = a.NC * a.B * a.H;  // work item = (b, h, chunk), chunk fastest
+  // every CTA of this persistent grid is resident from the start: the
+  // sequential kernel may launch now and wait for this grid in hardware
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -1130,6 +1133,10 @@ __global__ void __launch_bounds__(288, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // the per-chunk kernel's images and gates: wait until that grid has
+      // completed (a no-op when this grid was launched without overlap)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");
       int c = 0;
       for (; c < NC; ++c) {
         const int s = c % NST;
@@ -1467,7 +1474,21 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       const size_t smem = PipeSmem<SOLVE>::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
-      k<<<BH, 288, smem, fa.stream>>>(mq, mk, mo, ta);
+      if (fa.events) {  // timed: every kernel stands alone between its events
+        k<<<BH, 288, smem, fa.stream>>>(mq, mk, mo, ta);
+      } else {  // overlap the launch and set-up with the per-chunk kernel's tail
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(BH);
+        cfg.blockDim = dim3(288);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = fa.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, k, mq, mk, mo, ta) != cudaSuccess) return FALCON_ERR_CUDA;
+      }
       record_event(fa, 2);
     }
   } else {
