@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUte
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = blockIdx.x, bh = blockIdx.y;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream's previous grid (overlapped launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = bh / a.H, h = bh % a.H;
   const int t_base = pair * 128;
 
@@ -368,8 +370,10 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = a.NC * a.B * a.H;  // work item = (b, h, chunk), chunk fastest
-  // every CTA of this persistent grid is resident from the start: the
-  // sequential kernel may launch now and wait for this grid in hardware
+  // launched overlapping the stream's previous grid: wait for it before any
+  // read; then (every CTA of this persistent grid being resident) let the
+  // sequential kernel launch and wait for this grid in hardware
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
@@ -774,6 +778,8 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = *tmem_slot;
   int issued[2] = {0, 0};  // loads issued per stage (thread 0's bookkeeping)
   if (tid == 0 && NC > 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the per-chunk kernel's images and gates
+    asm volatile("fence.proxy.async.global;" ::: "memory");
     issue_stage(0, 0);
     issued[0] = 1;
   }
@@ -1449,6 +1455,29 @@ int sm_count() {
   return cached[dev];
 }
 
+// Launch overlapping the stream's previous grid (programmatic stream
+// serialization): the kernel waits for it in hardware (griddepcontrol.wait)
+// before it reads what that grid wrote.  Plain launch when the caller times
+// each kernel with events.
+template <typename Kern, typename... Args>
+int launch_overlapped(const FwdArgs& fa, Kern k, dim3 grid, dim3 block, size_t smem, Args... args) {
+  if (fa.events) {
+    k<<<grid, block, smem, fa.stream>>>(args...);
+    return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = fa.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...) == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
+}
+
 template <int DK, int NV, bool SOLVE>
 int launch_t(const FwdArgs& fa, const TcArgs& ta) {
   const int BH = fa.B * fa.H;
@@ -1466,7 +1495,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       const long items = (long)ta.NC * BH;
       dim3 grid((unsigned)std::min<long>(items, 4L * sm_count()));
       record_event(fa, 0);
-      k<<<grid, 128, smem, fa.stream>>>(mk, mv, ta);
+      if (launch_overlapped(fa, k, grid, dim3(128), smem, mk, mv, ta) != FALCON_OK) return FALCON_ERR_CUDA;
       record_event(fa, 1);
     }
     {  // pipelined: producer warp, front and back warpgroups
@@ -1474,21 +1503,8 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       const size_t smem = PipeSmem<SOLVE>::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
-      if (fa.events) {  // timed: every kernel stands alone between its events
-        k<<<BH, 288, smem, fa.stream>>>(mq, mk, mo, ta);
-      } else {  // overlap the launch and set-up with the per-chunk kernel's tail
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(BH);
-        cfg.blockDim = dim3(288);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = fa.stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, k, mq, mk, mo, ta) != cudaSuccess) return FALCON_ERR_CUDA;
-      }
+      // overlaps the per-chunk kernel's tail with its launch and set-up
+      if (launch_overlapped(fa, k, dim3(BH), dim3(288), smem, mq, mk, mo, ta) != FALCON_OK) return FALCON_ERR_CUDA;
       record_event(fa, 2);
     }
   } else {
@@ -1501,7 +1517,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
         return FALCON_ERR_CUDA;
       dim3 grid((ta.NC + 1) / 2, BH);
       record_event(fa, 0);
-      k<<<grid, 128, smem, fa.stream>>>(mk128, ta);
+      if (launch_overlapped(fa, k, grid, dim3(128), smem, mk128, ta) != FALCON_OK) return FALCON_ERR_CUDA;
       record_event(fa, 1);
     }
     {
@@ -1510,7 +1526,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
       dim3 grid(BH, fa.dv / NV);
-      k<<<grid, 256, smem, fa.stream>>>(mq, mk, mv, mo, ta);
+      if (launch_overlapped(fa, k, grid, dim3(256), smem, mq, mk, mv, mo, ta) != FALCON_OK) return FALCON_ERR_CUDA;
       record_event(fa, 2);
     }
   }
