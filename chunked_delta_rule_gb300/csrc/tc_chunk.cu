@@ -394,7 +394,9 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
   // finishes: TMA into the tile buffers once the products that read them are
   // done, lambda and beta into registers
   int issued = 0;  // tile loads issued (thread 0); item `it` waits for the it-th
-  auto fetch = [&](int item, float& ell, float& beta) {
+  // raw loads only: their values are first used by the next item, so the
+  // loads stay in flight meanwhile
+  auto fetch = [&](int item, float& lam_r, float& beta_r, int64_t& pos_r) {
     const int chunk = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
     if (tid == 0) {
       ++issued;
@@ -404,19 +406,22 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     }
     const int t = t0 + tid;
     const bool step_ok = tid < 64 && t < a.T;
-    const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
-    const bool exists = step_ok && (pos + t >= a.shift);
     const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
-    ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
-    beta = exists ? a.beta[gi] : 0.f;
+    lam_r = a.lam[gi];
+    beta_r = a.beta[gi];
+    pos_r = a.pos_in ? a.pos_in[bh] : 0;
   };
-  float ell_n = 0.f, beta_n = 0.f;
-  if (blockIdx.x < n_items) fetch(blockIdx.x, ell_n, beta_n);
+  float lam_n = 0.f, beta_n = 0.f;
+  int64_t pos_n = 0;
+  if (blockIdx.x < n_items) fetch(blockIdx.x, lam_n, beta_n, pos_n);
   int it = 0;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
   const int chunk = item % a.NC, bh = item / a.NC;
   const int next = item + gridDim.x;
-  const float ell = ell_n, beta = beta_n;
+  const int t_row = chunk * kC + tid;
+  const bool step_ok = tid < 64 && t_row < a.T;
+  const float ell = step_ok ? clamped_log_decay(lam_n, a.eps_gamma) : 0.f;
+  const float beta = (step_ok && pos_n + t_row >= a.shift) ? beta_n : 0.f;
   {  // gates: row tid <-> step chunk * 64 + tid
     float g = ell;  // inclusive prefix sum over the chunk
 #pragma unroll
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
   }
   // NLMS step from the key energy, and the decay factors of each row
   if (tid < 64) {
-    float n = 0.f;
+    float n4[4] = {0.f, 0.f, 0.f, 0.f};  // four short chains
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint4 raw = *reinterpret_cast<const uint4*>(Xs + sw128(tid, 8 * j));
@@ -459,10 +464,11 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 x = __bfloat1622float2(px[e]);
-        n = fmaf(x.x, x.x, n);
-        n = fmaf(x.y, x.y, n);
+        n4[e] = fmaf(x.x, x.x, n4[e]);
+        n4[e] = fmaf(x.y, x.y, n4[e]);
       }
     }
+    const float n = (n4[0] + n4[1]) + (n4[2] + n4[3]);
     const float eta = bs[tid] != 0.f ? bs[tid] / (a.eps + n) : 0.f;
     const float g = gs[tid];
     es[tid] = eta;
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     }
     __syncthreads();  // the tiles are read
     if (__syncthreads_or(*abort_flag)) break;
-    if (next < n_items) fetch(next, ell_n, beta_n);
+    if (next < n_items) fetch(next, lam_n, beta_n, pos_n);
     continue;
   }
 
@@ -505,30 +511,37 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     atomicExch(a.status, kStatusTimeout);
   }
   tc_fence_after();
-  const bool rowlane = lane < 16;
-  const int rl = 16 * warp + (lane & 15);  // this lane's Gram row (lanes 0..15)
-  float grow[64];
-  tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16), grow);
-  tmem_wait_ld();
+  const int rl = 16 * warp + (lane & 15);  // this lane's Gram row
+  const int hf = lane >> 4;                // and its half of the columns
+  float grow[32];
+  {
+    uint32_t r32[32];
+    tmem_ld16x2_32(tmem + ((uint32_t)(warp * 32) << 16), r32);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) grow[i] = __uint_as_float(r32[i]);
+  }
   tc_fence_before();
-  if (rowlane) {  // A_ri = eta_r exp(g_r - g_i) G_ri (i < r), the decay factored per 16-block
+  {  // A_ri = eta_r exp(g_r - g_i) G_ri (i < r), the decay factored per 16-block
     const float eta = es[rl], g = gs[rl], cfr = cfs[rl];
     const bool ratio_ok = cfr > 1e-30f;  // inside the row's block exp(g_r - g_i) = cf_i / cf_r
     const float inv = ratio_ok ? __fdividef(eta, cfr) : 0.f;
     float* Arow = T + rl * kLD;
     const int I = rl >> 4;
 #pragma unroll
-    for (int J = 0; J < 4; ++J) {
+    for (int jj = 0; jj < 2; ++jj) {
+      const int J = 2 * hf + jj;
+      const float* gr = grow + 16 * jj;  // columns 16 J .. 16 J + 15
       float av[16];
       if (J < I) {
         const float rf = eta * __expf(g - gs[16 * J + 15]);
 #pragma unroll
         for (int i = 0; i < 16; i += 4) {
           const float4 c4 = *reinterpret_cast<const float4*>(cfs + 16 * J + i);
-          av[i] = rf * c4.x * grow[16 * J + i];
-          av[i + 1] = rf * c4.y * grow[16 * J + i + 1];
-          av[i + 2] = rf * c4.z * grow[16 * J + i + 2];
-          av[i + 3] = rf * c4.w * grow[16 * J + i + 3];
+          av[i] = rf * c4.x * gr[i];
+          av[i + 1] = rf * c4.y * gr[i + 1];
+          av[i + 2] = rf * c4.z * gr[i + 2];
+          av[i + 3] = rf * c4.w * gr[i + 3];
         }
       } else if (J == I) {
         if (ratio_ok) {
@@ -538,12 +551,12 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
             const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              av[i + e] = (16 * J + i + e < rl) ? inv * cc[e] * grow[16 * J + i + e] : 0.f;
+              av[i + e] = (16 * J + i + e < rl) ? inv * cc[e] * gr[i + e] : 0.f;
           }
         } else {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            av[i] = (16 * J + i < rl) ? eta * __expf(g - gs[16 * J + i]) * grow[16 * J + i] : 0.f;
+            av[i] = (16 * J + i < rl) ? eta * __expf(g - gs[16 * J + i]) * gr[i] : 0.f;
         }
       } else {
 #pragma unroll
@@ -554,6 +567,7 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
         *reinterpret_cast<float4*>(Arow + 16 * J + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
     }
   }
+  if (tid == 0) bulk_wait_read0();  // the previous item's image store has read the buffer
   __syncthreads();
 
   // ---- T = (I + A)^{-1} in place; the 16x16 scratch blocks live in the
@@ -623,13 +637,11 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
       const float4 lo4 = *reinterpret_cast<const float4*>(T + R * kLD + 8 * j);
       const float4 hi4 = *reinterpret_cast<const float4*>(T + R * kLD + 8 * j + 4);
       const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-      uint32_t pw[4], pu[4];
+      uint32_t pw[4], pu[4];  // T's strict upper triangle holds exact zeros (A's did)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int c0 = 8 * j + 2 * e;
-        const float q0 = (c0 <= R) ? v[2 * e] : 0.f, q1 = (c0 + 1 <= R) ? v[2 * e + 1] : 0.f;
-        pu[e] = pack_bf16(q0 * eu[2 * e], q1 * eu[2 * e + 1]);
-        pw[e] = pack_bf16(q0 * ew[2 * e], q1 * ew[2 * e + 1]);
+        pu[e] = pack_bf16(v[2 * e] * eu[2 * e], v[2 * e + 1] * eu[2 * e + 1]);
+        pw[e] = pack_bf16(v[2 * e] * ew[2 * e], v[2 * e + 1] * ew[2 * e + 1]);
       }
       const int off = R * 128 + 16 * (j ^ (R & 7));
       *reinterpret_cast<uint4*>(TI + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
@@ -652,27 +664,32 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     atomicExch(a.status, kStatusTimeout);
   }
   tc_fence_after();
-  if (next < n_items && !*abort_flag) fetch(next, ell_n, beta_n);  // the tiles are read
-  {  // rows 0..63: U (columns 0..63); rows 64..127: W (columns 64..127)
+  if (next < n_items && !*abort_flag) fetch(next, lam_n, beta_n, pos_n);  // the tiles are read
+  {  // rows 0..63: U (columns 0..63); rows 64..127: W (columns 64..127), staged
+     // in the T image buffer (the product that read it is done) in the
+     // workspace layout, then stored by one bulk copy
     float rv[64];
     tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + (warp < 2 ? 0 : 64), rv);
     tmem_wait_ld();
-    if (!*abort_flag) {
-      const int r = (32 * warp + lane) & 63;
-      uint8_t* dst = warp < 2 ? Wo + 8192 : Wo;
+    const int r = (32 * warp + lane) & 63;
+    uint8_t* dst = warp < 2 ? TI + 8192 : TI;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t pk[4];
+    for (int j = 0; j < 8; ++j) {
+      uint32_t pk[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(rv[8 * j + 2 * e], rv[8 * j + 2 * e + 1]);
-        *reinterpret_cast<uint4*>(dst + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-
+      for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(rv[8 * j + 2 * e], rv[8 * j + 2 * e + 1]);
+      *reinterpret_cast<uint4*>(dst + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   }
+  fence_proxy_async();
   tc_fence_before();
   if (__syncthreads_or(*abort_flag)) break;
+  if (tid == 0) {
+    bulk_store(Wo, TI, 16384);
+    bulk_commit();
+  }
   }  // items
+  if (tid == 0) bulk_wait0();  // the last images are written
   if (tid == 0 && issued > it) mbar_wait(&bar[0], (uint32_t)(it & 1));  // a load still in flight
   tc_fence_before();
   __syncthreads();
