@@ -29,6 +29,7 @@
 // conflicts on a bank).
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace falcon {
 
@@ -77,75 +78,85 @@ __device__ __forceinline__ float* wsgate(const CbArgs& a, size_t cg) {
   return a.ws + (size_t)a.B * a.H * a.NC * kMats * kMat + cg * kGateVecs * kN;
 }
 
-// C (4 x 4 per thread) = op(A) op(B) over K = 64, both operands in shared
-// memory with row stride LDM.  NN: A [M][K], B [K][N]; TN: A [K][M], B [K][N];
-// NT: A [M][K], B [N][K].  Thread (ty, tx) = (tid / 16, tid % 16) owns rows
-// kRows ty + i and columns 4 tx + j (NN, TN) or tx + 16 j (NT).
+// C (4 x 4 per thread) += op(A) op(B) over K = 64, both operands fp32 in
+// shared memory with row stride LDM.  NN: A [M][K], B [K][N]; TN: A [K][M],
+// B [K][N]; NT: A [M][K], B [N][K].  Tensor-core m16n8k8 products with the
+// three-term tf32 split (a = a_hi + a_lo, a b ~ a_hi b_hi + a_hi b_lo +
+// a_lo b_hi), whose error stays at the level of fp32 accumulation.  Warp w
+// covers rows 32 (w / 4) .. + 31 and columns 16 (w % 4) .. + 15; thread
+// (gid, tig) = (lane / 4, lane % 4) owns rows 32 (w / 4) + gid + 8 i and
+// columns 16 (w % 4) + 8 (j / 2) + 2 tig + j % 2.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = tc::to_tf32(x);
+  lo = tc::to_tf32(x - __uint_as_float(hi));
+}
+
 template <int MODE>
 __device__ __forceinline__ void mm64(float (&acc)[kRows][4], const float* __restrict__ A,
                                      const float* __restrict__ B) {
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  if (MODE == TN) {
-#pragma unroll 8
-    for (int k = 0; k < kN; ++k) {
-      float a4[kRows];
-      if (kRows == 4) {
-        const float4 av = *reinterpret_cast<const float4*>(&A[k * LDM + kRows * ty]);
-        a4[0] = av.x; a4[1] = av.y; a4[kRows > 2 ? 2 : 0] = av.z; a4[kRows > 3 ? 3 : 0] = av.w;
-      } else {
-        const float2 av = *reinterpret_cast<const float2*>(&A[k * LDM + kRows * ty]);
-        a4[0] = av.x; a4[1] = av.y;
-      }
-      const float4 bv = *reinterpret_cast<const float4*>(&B[k * LDM + 4 * tx]);
-      const float b4[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-      for (int i = 0; i < kRows; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a4[i], b4[j], acc[i][j]);
-    }
-  } else {
+  static_assert(kRows == 4, "two 16-row tiles of two 8-column tiles per warp");
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int m0 = 32 * (w >> 2), n0 = 16 * (w & 3);
 #pragma unroll 2
-    for (int k = 0; k < kN; k += 4) {
-      float a4[kRows][4], b4[4][4];
+  for (int k0 = 0; k0 < kN; k0 += 8) {
+    uint32_t ah[2][4], al[2][4], bh[2][2], bl[2][2];
 #pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        const float4 av = *reinterpret_cast<const float4*>(&A[(kRows * ty + i) * LDM + k]);
-        a4[i][0] = av.x; a4[i][1] = av.y; a4[i][2] = av.z; a4[i][3] = av.w;
+    for (int mt = 0; mt < 2; ++mt) {
+      const int m = m0 + 16 * mt + gid;
+      float x[4];
+      if (MODE == TN) {
+        x[0] = A[(k0 + tig) * LDM + m];
+        x[1] = A[(k0 + tig) * LDM + m + 8];
+        x[2] = A[(k0 + tig + 4) * LDM + m];
+        x[3] = A[(k0 + tig + 4) * LDM + m + 8];
+      } else {
+        x[0] = A[m * LDM + k0 + tig];
+        x[1] = A[(m + 8) * LDM + k0 + tig];
+        x[2] = A[m * LDM + k0 + tig + 4];
+        x[3] = A[(m + 8) * LDM + k0 + tig + 4];
       }
-      if (MODE == NN) {  // b4[kk][j] = B[k + kk][4 tx + j]
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float4 bv = *reinterpret_cast<const float4*>(&B[(k + kk) * LDM + 4 * tx]);
-          b4[kk][0] = bv.x; b4[kk][1] = bv.y; b4[kk][2] = bv.z; b4[kk][3] = bv.w;
-        }
-#pragma unroll
-        for (int i = 0; i < kRows; ++i)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a4[i][kk], b4[kk][j], acc[i][j]);
-      } else {  // NT: b4[j][kk] = B[tx + 16 j][k + kk]
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 bv = *reinterpret_cast<const float4*>(&B[(tx + 16 * j) * LDM + k]);
-          b4[j][0] = bv.x; b4[j][1] = bv.y; b4[j][2] = bv.z; b4[j][3] = bv.w;
-        }
-#pragma unroll
-        for (int i = 0; i < kRows; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) acc[i][j] = fmaf(a4[i][kk], b4[j][kk], acc[i][j]);
-      }
+      for (int e = 0; e < 4; ++e) split_tf32(x[e], ah[mt][e], al[mt][e]);
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int n = n0 + 8 * nt + gid;
+      float y[2];
+      if (MODE == NT) {
+        y[0] = B[n * LDM + k0 + tig];
+        y[1] = B[n * LDM + k0 + tig + 4];
+      } else {
+        y[0] = B[(k0 + tig) * LDM + n];
+        y[1] = B[(k0 + tig + 4) * LDM + n];
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) split_tf32(y[e], bh[nt][e], bl[nt][e]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float c[4] = {acc[2 * mt][2 * nt], acc[2 * mt][2 * nt + 1], acc[2 * mt + 1][2 * nt],
+                      acc[2 * mt + 1][2 * nt + 1]};
+        tc::mma_tf32_16x8x8(c, al[mt], bh[nt]);
+        tc::mma_tf32_16x8x8(c, ah[mt], bl[nt]);
+        tc::mma_tf32_16x8x8(c, ah[mt], bh[nt]);
+        acc[2 * mt][2 * nt] = c[0];
+        acc[2 * mt][2 * nt + 1] = c[1];
+        acc[2 * mt + 1][2 * nt] = c[2];
+        acc[2 * mt + 1][2 * nt + 1] = c[3];
+      }
   }
 }
 
 template <int MODE>
-__device__ __forceinline__ int out_row(int i) { return kRows * (threadIdx.x >> 4) + i; }
+__device__ __forceinline__ int out_row(int i) {
+  return 32 * (int)(threadIdx.x >> 7) + (int)((threadIdx.x & 31) >> 2) + 8 * i;
+}
 template <int MODE>
 __device__ __forceinline__ int out_col(int j) {
-  return MODE == NT ? (int)(threadIdx.x & 15) + 16 * j : 4 * (int)(threadIdx.x & 15) + j;
+  return 16 * (int)((threadIdx.x >> 5) & 3) + 8 * (j >> 1) + 2 * (int)(threadIdx.x & 3) + (j & 1);
 }
 
 __device__ __forceinline__ void zero_acc(float (&acc)[kRows][4]) {
@@ -173,72 +184,108 @@ template <typename Tin>
 __device__ __forceinline__ float ldx(const void* p, size_t i) { return to_f32(reinterpret_cast<const Tin*>(p)[i]); }
 template <typename Tin>
 __device__ __forceinline__ void stx(void* p, size_t i, float x) { reinterpret_cast<Tin*>(p)[i] = from_f32<Tin>(x); }
-
-// rows of a chunk into shared memory (zero past the end of the call): every
-// thread issues all of its 16-byte loads before it stores any
+// eight consecutive elements p[i .. i + 7] (i a multiple of 8) in 16-byte stores
 template <typename Tin>
-__device__ __forceinline__ void load_rows(float* dst, const void* src, const CbArgs& a, int b, int h, int t0) {
-  constexpr int EC = 16 / (int)sizeof(Tin), PR = kN / EC, PT = kN * PR / kThr;  // pieces per row / thread
-  uint4 raw[PT];
+__device__ __forceinline__ void stx8(void* p, size_t i, const float (&v)[8]) {
+  if constexpr (sizeof(Tin) == 2) {
+    uint32_t pk[4];
 #pragma unroll
-  for (int k = 0; k < PT; ++k) {
-    const int i = threadIdx.x + kThr * k, r = i / PR, c = (i % PR) * EC, t = t0 + r;
-    raw[k] = t < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(src) +
-                                                     (((size_t)b * a.T + t) * a.H + h) * kN + c)
-                     : make_uint4(0u, 0u, 0u, 0u);
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+      pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(reinterpret_cast<Tin*>(p) + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  } else {
+    float4* q = reinterpret_cast<float4*>(reinterpret_cast<Tin*>(p) + i);
+    q[0] = make_float4(v[0], v[1], v[2], v[3]);
+    q[1] = make_float4(v[4], v[5], v[6], v[7]);
   }
+}
+// eight consecutive fp32 values of a shared-memory row
+__device__ __forceinline__ void lds8(float (&v)[8], const float* p) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Rows of a chunk into shared memory (zero past the end of the call) in two
+// halves, so that a kernel can have the loads of several tiles in flight
+// together: fetch_* issues a thread's 16-byte loads into registers, put_rows
+// converts them to fp32 rows.
+template <typename Tin>
+struct RowRaw {
+  static constexpr int EC = 16 / (int)sizeof(Tin), PR = kN / EC, PT = kN * PR / kThr;  // per row / thread
+  uint4 v[PT];
+};
+template <typename Tin>
+__device__ __forceinline__ void fetch_rows(RowRaw<Tin>& raw, const void* src, const CbArgs& a, int b, int h, int t0) {
+  using R = RowRaw<Tin>;
 #pragma unroll
-  for (int k = 0; k < PT; ++k) {
-    const int i = threadIdx.x + kThr * k, r = i / PR, c = (i % PR) * EC;
-    const Tin* e = reinterpret_cast<const Tin*>(&raw[k]);
-#pragma unroll
-    for (int q = 0; q < EC; q += 4)
-      *reinterpret_cast<float4*>(&dst[r * LDM + c + q]) =
-          make_float4(to_f32(e[q]), to_f32(e[q + 1]), to_f32(e[q + 2]), to_f32(e[q + 3]));
+  for (int k = 0; k < R::PT; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i / R::PR, c = (i % R::PR) * R::EC, t = t0 + r;
+    raw.v[k] = t < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(src) +
+                                                       (((size_t)b * a.T + t) * a.H + h) * kN + c)
+                       : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 // keys of the chunk's pairs: x_r = k_{t - shift}, the carried key for the
 // first pair (prefix), zero where the pair does not exist
 template <typename Tin>
-__device__ __forceinline__ void load_keys(float* dst, const CbArgs& a, int b, int h, int t0, int64_t pos) {
-  constexpr int EC = 16 / (int)sizeof(Tin), PR = kN / EC, PT = kN * PR / kThr;
-  uint4 raw[PT];
+__device__ __forceinline__ void fetch_keys(RowRaw<Tin>& raw, const CbArgs& a, int b, int h, int t0, int64_t pos) {
+  using R = RowRaw<Tin>;
 #pragma unroll
-  for (int k = 0; k < PT; ++k) {
-    const int i = threadIdx.x + kThr * k, r = i / PR, c = (i % PR) * EC, t = t0 + r;
+  for (int k = 0; k < R::PT; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i / R::PR, c = (i % R::PR) * R::EC, t = t0 + r;
     const Tin* row = nullptr;
     if (t < a.T && pos + t >= a.shift) {
       if (t - a.shift >= 0) row = reinterpret_cast<const Tin*>(a.k) + (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN;
       else if (a.kprev_in) row = reinterpret_cast<const Tin*>(a.kprev_in) + ((size_t)b * a.H + h) * kN;
     }
-    raw[k] = row ? *reinterpret_cast<const uint4*>(row + c) : make_uint4(0u, 0u, 0u, 0u);
+    raw.v[k] = row ? *reinterpret_cast<const uint4*>(row + c) : make_uint4(0u, 0u, 0u, 0u);
   }
+}
+template <typename Tin>
+__device__ __forceinline__ void put_rows(float* dst, const RowRaw<Tin>& raw) {
+  using R = RowRaw<Tin>;
 #pragma unroll
-  for (int k = 0; k < PT; ++k) {
-    const int i = threadIdx.x + kThr * k, r = i / PR, c = (i % PR) * EC;
-    const Tin* e = reinterpret_cast<const Tin*>(&raw[k]);
+  for (int k = 0; k < R::PT; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i / R::PR, c = (i % R::PR) * R::EC;
+    const Tin* e = reinterpret_cast<const Tin*>(&raw.v[k]);
 #pragma unroll
-    for (int q = 0; q < EC; q += 4)
+    for (int q = 0; q < R::EC; q += 4)
       *reinterpret_cast<float4*>(&dst[r * LDM + c + q]) =
           make_float4(to_f32(e[q]), to_f32(e[q + 1]), to_f32(e[q + 2]), to_f32(e[q + 3]));
   }
 }
-// a 64 x 64 fp32 workspace matrix into shared memory
-__device__ __forceinline__ void load_mat(float* dst, const float* src) {
-  constexpr int PT = kN * kN / 4 / kThr;
-  float4 v[PT];
+// keys, queries, values and output gradients of the chunk, all loads in flight together
+template <typename Tin>
+__device__ __forceinline__ void load_inputs(float* X, float* Q, float* V, float* dO, const CbArgs& a, int b, int h,
+                                            int t0, int64_t pos) {
+  RowRaw<Tin> rx, rq, rv, rd;
+  fetch_keys<Tin>(rx, a, b, h, t0, pos);
+  fetch_rows<Tin>(rq, a.q, a, b, h, t0);
+  fetch_rows<Tin>(rv, a.v, a, b, h, t0);
+  fetch_rows<Tin>(rd, a.dO, a, b, h, t0);
+  put_rows<Tin>(X, rx);
+  put_rows<Tin>(Q, rq);
+  put_rows<Tin>(V, rv);
+  put_rows<Tin>(dO, rd);
+}
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// a 64 x 64 fp32 workspace matrix into shared memory by cp.async (no wait)
+__device__ __forceinline__ void cp_mat(float* dst, const float* src) {
 #pragma unroll
-  for (int k = 0; k < PT; ++k) {
+  for (int k = 0; k < kN * kN / 4 / kThr; ++k) {
     const int i = threadIdx.x + kThr * k;
-    v[k] = *reinterpret_cast<const float4*>(&src[(i >> 4) * kN + (i & 15) * 4]);
-  }
-#pragma unroll
-  for (int k = 0; k < PT; ++k) {
-    const int i = threadIdx.x + kThr * k;
-    *reinterpret_cast<float4*>(&dst[(i >> 4) * LDM + (i & 15) * 4]) = v[k];
+    cp16(&dst[(i >> 4) * LDM + (i & 15) * 4], &src[(i >> 4) * kN + (i & 15) * 4]);
   }
 }
-
 struct GateSm {
   float g[kN], Gam[kN], E[kN], eta[kN], nrm[kN], ex[kN], gam[kN];
 };
@@ -302,10 +349,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   const int c = (int)(cg % a.NC), bh = (int)(cg / a.NC), b = bh / a.H, h = bh % a.H, t0 = c * kN;
   const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
   const int tid = threadIdx.x;
-  load_keys<Tin>(X, a, b, h, t0, pos);
-  load_rows<Tin>(Q, a.q, a, b, h, t0);
-  load_rows<Tin>(V, a.v, a, b, h, t0);
-  load_rows<Tin>(dO, a.dO, a, b, h, t0);
+  load_inputs<Tin>(X, Q, V, dO, a, b, h, t0, pos);
   __syncthreads();
   make_gates(gs, X, a, b, h, t0, pos);
   float acc[kRows][4];
@@ -430,12 +474,14 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
 
 // ---------------------------------------------------------------- (b), (c)
 // One CTA of 256 threads per (b, h, 16 value columns); the S (or dS) slice,
-// 64 x 16, in shared memory.  Thread (r = tid / 4, quad = tid % 4) owns row r,
-// columns 4 quad .. 4 quad + 3.  The next chunk's W, diag(E) X, value slice (U
-// or Y) and decay arrive by cp.async into the other of two stages.
+// 64 x 16, in shared memory.  Each chunk step is two 64 x 64 x 16 products on
+// the tensor cores (three-term tf32 split, as in mm64): warp w owns the 16 x 8
+// tile at rows 16 (w / 2), columns 8 (w % 2).  The next chunk's W, diag(E) X,
+// value slice (U or Y) and decay arrive by cp.async into the other of two
+// stages.
 constexpr int kSC = 16;
-constexpr int CPT = kSC / 4;  // columns per thread
-constexpr int LDS_ = kSC + 4;
+constexpr int CPT = kSC / 4;  // columns per thread in the row-wise copies
+constexpr int LDS_ = kSC + 8;  // row stride of the slices: fragment loads free of bank conflicts
 
 struct ChainStage {
   float W[kN * LDM];
@@ -448,15 +494,6 @@ struct ChainSmem {
   float S[kN * LDS_];
   float Dl[kN * LDS_];
 };
-
-__device__ __forceinline__ void cp16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-               "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void chain_stage(const CbArgs& a, ChainStage& st, size_t cg, int c0, int which_c) {
   const int tid = threadIdx.x;
@@ -478,15 +515,57 @@ __device__ __forceinline__ void chain_stage(const CbArgs& a, ChainStage& st, siz
 }
 
 __device__ __forceinline__ void ldcs(float (&v)[CPT], const float* p) {
-#pragma unroll
-  for (int q = 0; q < CPT; q += 4) {
-    const float4 a = *reinterpret_cast<const float4*>(p + q);
-    v[q] = a.x; v[q + 1] = a.y; v[q + 2] = a.z; v[q + 3] = a.w;
-  }
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
 }
-__device__ __forceinline__ void stcs(float* p, const float (&v)[CPT]) {
+
+// c (this warp's 16 x 8 tile at rows m0, columns n0) += sgn A B over K = 64:
+// A [M][K] at A[m * LDM + k] (AT: A[k * LDM + m]), B [K][16] at B[k * LDS_ + n].
+// Two accumulators over alternate k steps shorten the dependent chain.
+template <bool AT>
+__device__ __forceinline__ void tile_mma(float (&c)[4], const float* __restrict__ A, const float* __restrict__ B,
+                                         int m0, int n0, float sgn) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  float c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int q = 0; q < CPT; q += 4) *reinterpret_cast<float4*>(p + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+  for (int k0 = 0; k0 < kN; k0 += 8) {
+    float x[4];
+    if (AT) {
+      x[0] = A[(k0 + tig) * LDM + m0 + gid];
+      x[1] = A[(k0 + tig) * LDM + m0 + gid + 8];
+      x[2] = A[(k0 + tig + 4) * LDM + m0 + gid];
+      x[3] = A[(k0 + tig + 4) * LDM + m0 + gid + 8];
+    } else {
+      x[0] = A[(m0 + gid) * LDM + k0 + tig];
+      x[1] = A[(m0 + gid + 8) * LDM + k0 + tig];
+      x[2] = A[(m0 + gid) * LDM + k0 + tig + 4];
+      x[3] = A[(m0 + gid + 8) * LDM + k0 + tig + 4];
+    }
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_tf32(sgn * x[e], ah[e], al[e]);
+    split_tf32(B[(k0 + tig) * LDS_ + n0 + gid], bh[0], bl[0]);
+    split_tf32(B[(k0 + tig + 4) * LDS_ + n0 + gid], bh[1], bl[1]);
+    float (&acc)[4] = (k0 & 8) ? c2 : c;
+    tc::mma_tf32_16x8x8(acc, al, bh);
+    tc::mma_tf32_16x8x8(acc, ah, bl);
+    tc::mma_tf32_16x8x8(acc, ah, bh);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) c[e] += c2[e];
+}
+// the tile's four elements of a [64][LDS_] slice: (row, column) =
+// (m0 + gid + 8 (e / 2), n0 + 2 tig + e % 2)
+__device__ __forceinline__ void tile_ld(float (&v)[4], const float* p, int m0, int n0) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const float2 a = *reinterpret_cast<const float2*>(&p[(m0 + gid) * LDS_ + n0 + 2 * tig]);
+  const float2 b = *reinterpret_cast<const float2*>(&p[(m0 + gid + 8) * LDS_ + n0 + 2 * tig]);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+__device__ __forceinline__ void tile_st(float* p, const float (&v)[4], int m0, int n0) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  *reinterpret_cast<float2*>(&p[(m0 + gid) * LDS_ + n0 + 2 * tig]) = make_float2(v[0], v[1]);
+  *reinterpret_cast<float2*>(&p[(m0 + gid + 8) * LDS_ + n0 + 2 * tig]) = make_float2(v[2], v[3]);
 }
 
 __global__ void __launch_bounds__(kThrC) bwdc_fwd_chain_kernel(CbArgs a) {
@@ -494,6 +573,7 @@ __global__ void __launch_bounds__(kThrC) bwdc_fwd_chain_kernel(CbArgs a) {
   ChainSmem& sm = *reinterpret_cast<ChainSmem*>(smem_f4);
   const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
   const int r = tid >> 2, q8 = (tid & 3) * CPT;
+  const int m0 = 16 * (tid >> 6), n0 = 8 * ((tid >> 5) & 1);
   for (int i = tid; i < kN * kSC; i += kThrC) {
     const int rr = i / kSC, cc = i % kSC;
     sm.S[rr * LDS_ + cc] = a.S_in ? a.S_in[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
@@ -507,39 +587,24 @@ __global__ void __launch_bounds__(kThrC) bwdc_fwd_chain_kernel(CbArgs a) {
     ChainStage& st = sm.st[c & 1];
     cp_wait1();
     __syncthreads();
-    float v[CPT];
-    ldcs(v, &sm.S[r * LDS_ + q8]);
     {  // chunk start state out
-      stcs(&wsmat(a, cg, M_S0)[(size_t)r * kN + c0 + q8], v);
+      float v[CPT];
+      ldcs(v, &sm.S[r * LDS_ + q8]);
+      *reinterpret_cast<float4*>(&wsmat(a, cg, M_S0)[(size_t)r * kN + c0 + q8]) = make_float4(v[0], v[1], v[2], v[3]);
     }
-    float d[CPT];
-    ldcs(d, &st.C[r * LDS_ + q8]);
-    if (!a.additive) {  // Delta = U - W S
-#pragma unroll 4
-      for (int k = 0; k < kN; ++k) {
-        const float w = st.W[r * LDM + k];
-        float sk[CPT];
-        ldcs(sk, &sm.S[k * LDS_ + q8]);
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) d[e] = fmaf(-w, sk[e], d[e]);
-      }
-    }
-    stcs(&sm.Dl[r * LDS_ + q8], d);
+    float d[4];  // Delta = U - W S  (additive: Delta = U)
+    tile_ld(d, st.C, m0, n0);
+    if (!a.additive) tile_mma<false>(d, st.W, sm.S, m0, n0, -1.f);
+    tile_st(sm.Dl, d, m0, n0);
     __syncthreads();
-    // S = Gamma_63 S + (diag(E) X)^T Delta   (row r of S is key index r)
-    const float G63 = st.g4[3];
+    // S = Gamma_63 S + (diag(E) X)^T Delta   (row of S = key index)
+    float v[4];
+    tile_ld(v, sm.S, m0, n0);
 #pragma unroll
-    for (int e = 0; e < CPT; ++e) v[e] *= G63;
-#pragma unroll 4
-    for (int i = 0; i < kN; ++i) {
-      const float x = st.X[i * LDM + r];
-      float di[CPT];
-      ldcs(di, &sm.Dl[i * LDS_ + q8]);
-#pragma unroll
-      for (int e = 0; e < CPT; ++e) v[e] = fmaf(x, di[e], v[e]);
-    }
+    for (int e = 0; e < 4; ++e) v[e] *= st.g4[3];
+    tile_mma<true>(v, st.X, sm.Dl, m0, n0, 1.f);
     __syncthreads();  // every read of S and of this stage is done
-    stcs(&sm.S[r * LDS_ + q8], v);
+    tile_st(sm.S, v, m0, n0);
     if (c + 2 < a.NC) chain_stage(a, st, cg + 2, c0, M_U);
     cp_commit();
   }
@@ -551,6 +616,7 @@ __global__ void __launch_bounds__(kThrC) bwdc_bwd_chain_kernel(CbArgs a) {
   ChainSmem& sm = *reinterpret_cast<ChainSmem*>(smem_f4);
   const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
   const int r = tid >> 2, q8 = (tid & 3) * CPT;
+  const int m0 = 16 * (tid >> 6), n0 = 8 * ((tid >> 5) & 1);
   for (int i = tid; i < kN * kSC; i += kThrC) {
     const int rr = i / kSC, cc = i % kSC;
     sm.S[rr * LDS_ + cc] = a.dS_final ? a.dS_final[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
@@ -566,42 +632,26 @@ __global__ void __launch_bounds__(kThrC) bwdc_bwd_chain_kernel(CbArgs a) {
     ChainStage& st = sm.st[n & 1];
     cp_wait1();
     __syncthreads();
-    float v[CPT];
-    ldcs(v, &sm.S[r * LDS_ + q8]);
     {  // gradient of the chunk's end state out
-      stcs(&wsmat(a, cg, M_DS1)[(size_t)r * kN + c0 + q8], v);
+      float v[CPT];
+      ldcs(v, &sm.S[r * LDS_ + q8]);
+      *reinterpret_cast<float4*>(&wsmat(a, cg, M_DS1)[(size_t)r * kN + c0 + q8]) = make_float4(v[0], v[1], v[2], v[3]);
     }
-    if (!a.additive) {  // Z = diag(E) X dS  (row r = chunk row)
-      float z[CPT] = {};
-#pragma unroll 4
-      for (int k = 0; k < kN; ++k) {
-        const float x = st.X[r * LDM + k];
-        float sk[CPT];
-        ldcs(sk, &sm.S[k * LDS_ + q8]);
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) z[e] = fmaf(x, sk[e], z[e]);
-      }
-      stcs(&sm.Dl[r * LDS_ + q8], z);
+    if (!a.additive) {  // Z = diag(E) X dS  (row = chunk row)
+      float z[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_mma<false>(z, st.X, sm.S, m0, n0, 1.f);
+      tile_st(sm.Dl, z, m0, n0);
     }
     __syncthreads();
-    // dS = Gamma_63 dS - W^T Z + Y   (row r = key index)
-    const float G63 = st.g4[3];
-    float y[CPT];
-    ldcs(y, &st.C[r * LDS_ + q8]);
+    // dS = Gamma_63 dS - W^T Z + Y   (row = key index)
+    float v[4], y[4];
+    tile_ld(v, sm.S, m0, n0);
+    tile_ld(y, st.C, m0, n0);
 #pragma unroll
-    for (int e = 0; e < CPT; ++e) v[e] = fmaf(G63, v[e], y[e]);
-    if (!a.additive) {
-#pragma unroll 4
-      for (int i = 0; i < kN; ++i) {
-        const float w = st.W[i * LDM + r];
-        float zi[CPT];
-        ldcs(zi, &sm.Dl[i * LDS_ + q8]);
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) v[e] = fmaf(-w, zi[e], v[e]);
-      }
-    }
+    for (int e = 0; e < 4; ++e) v[e] = fmaf(st.g4[3], v[e], y[e]);
+    if (!a.additive) tile_mma<true>(v, st.W, sm.Dl, m0, n0, -1.f);
     __syncthreads();
-    stcs(&sm.S[r * LDS_ + q8], v);
+    tile_st(sm.S, v, m0, n0);
     if (n + 2 < a.NC) chain_stage(a, st, base + a.NC - 3 - n, c0, M_Y);
     cp_commit();
   }
@@ -643,22 +693,19 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
   const int tid = threadIdx.x;
   const bool reg = !a.additive;
-  load_keys<Tin>(X, a, b, h, t0, pos);
-  load_rows<Tin>(Q, a.q, a, b, h, t0);
-  load_rows<Tin>(V, a.v, a, b, h, t0);
-  load_rows<Tin>(dO, a.dO, a, b, h, t0);
-  {
-    load_mat(S0, wsmat(a, cg, M_S0));
-    load_mat(dS1, wsmat(a, cg, M_DS1));
+  {  // the workspace matrices by cp.async, the input rows meanwhile
+    cp_mat(S0, wsmat(a, cg, M_S0));
+    cp_mat(dS1, wsmat(a, cg, M_DS1));
     if (reg) {
-      load_mat(s1, wsmat(a, cg, M_W));
-      load_mat(s2, wsmat(a, cg, M_U));
+      cp_mat(s1, wsmat(a, cg, M_W));
+      cp_mat(s2, wsmat(a, cg, M_U));
     }
-    const float* gv = wsgate(a, cg);
-    if (tid < kN) {
-      gs.g[tid] = gv[tid]; gs.Gam[tid] = gv[kN + tid]; gs.E[tid] = gv[2 * kN + tid]; gs.eta[tid] = gv[3 * kN + tid];
-      gs.nrm[tid] = gv[4 * kN + tid]; gs.ex[tid] = gv[5 * kN + tid]; gs.gam[tid] = gv[6 * kN + tid];
-    }
+    // the gate vectors g, Gamma, E, eta, |x|^2, exists, gamma: GateSm's order
+    static_assert(sizeof(GateSm) == 7 * kN * sizeof(float), "gate rows back to back");
+    if (tid < (int)(sizeof(GateSm) / 16)) cp16(reinterpret_cast<float*>(&gs) + 4 * tid, wsgate(a, cg) + 4 * tid);
+    cp_commit();
+    load_inputs<Tin>(X, Q, V, dO, a, b, h, t0, pos);
+    cp_wait0();
   }
   __syncthreads();
   float acc[kRows][4];
@@ -738,7 +785,9 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   __syncthreads();
   // dR = T^T dDelta -> s6 (additive: dR = dDelta)
   if (reg) {
-    load_mat(s4, wsmat(a, cg, M_T));
+    cp_mat(s4, wsmat(a, cg, M_T));
+    cp_commit();
+    cp_wait0();
     __syncthreads();
     zero_acc(acc);
     mm64<TN>(acc, s4, s5);
@@ -751,9 +800,14 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   }
   __syncthreads();
   // dV, d eta (residual part), dGamma (residual part)
-  for (int i = tid; i < kN * kN; i += kThr) {
-    const int r = i / kN, cc = i % kN, t = t0 + r;
-    if (t < a.T) stx<Tin>(a.dv, (((size_t)b * a.T + t) * a.H + h) * kN + cc, gs.eta[r] * s6[r * LDM + cc]);
+  for (int i = tid; i < kN * kN / 8; i += kThr) {
+    const int r = i / (kN / 8), cc = (i % (kN / 8)) * 8, t = t0 + r;
+    if (t >= a.T) continue;
+    float v8[8];
+    lds8(v8, &s6[r * LDM + cc]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v8[e] *= gs.eta[r];
+    stx8<Tin>(a.dv, (((size_t)b * a.T + t) * a.H + h) * kN + cc, v8);
   }
   {
     const int r = tid / kRowT;
@@ -793,13 +847,14 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
         s1[r * LDM + ci] = dg;
         s5[r * LDM + ci] = m;
       }
-    // d eta: reduce the 16 threads of a row group (same ty), 4 rows each
+    // d eta: a row's columns sit in the four lanes of one gid and in four
+    // warps; reduce over the lanes, then one shared-memory add per warp
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       float v = dea[i];
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if ((tid & 15) == 0) deta[out_row<NT>(i)] += v;  // one writer per row
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if ((tid & 3) == 0) atomicAdd(&deta[out_row<NT>(i)], v);
     }
     __syncthreads();
     zero_acc(acc);
@@ -889,14 +944,19 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   }
   __syncthreads();
   // outputs: dq, dk (with the norm term), dbeta, dlambda
-  for (int i = tid; i < kN * kN; i += kThr) {
-    const int r = i / kN, cc = i % kN, t = t0 + r;
+  for (int i = tid; i < kN * kN / 8; i += kThr) {
+    const int r = i / (kN / 8), cc = (i % (kN / 8)) * 8, t = t0 + r;
     if (t >= a.T) continue;
-    stx<Tin>(a.dq, (((size_t)b * a.T + t) * a.H + h) * kN + cc, s6[r * LDM + cc]);
+    float v8[8], x8[8];
+    lds8(v8, &s6[r * LDM + cc]);
+    stx8<Tin>(a.dq, (((size_t)b * a.T + t) * a.H + h) * kN + cc, v8);
     const float dn = gs.ex[r] != 0.f ? -deta[r] * gs.eta[r] / (a.eps + gs.nrm[r]) : 0.f;
-    const float dx = s4[r * LDM + cc] + 2.f * dn * X[r * LDM + cc];
-    if (t - a.shift >= 0) stx<Tin>(a.dk, (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN + cc, dx);
-    else if (a.dk_prev) stx<Tin>(a.dk_prev, (size_t)bh * kN + cc, dx);
+    lds8(v8, &s4[r * LDM + cc]);
+    lds8(x8, &X[r * LDM + cc]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v8[e] += 2.f * dn * x8[e];
+    if (t - a.shift >= 0) stx8<Tin>(a.dk, (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN + cc, v8);
+    else if (a.dk_prev) stx8<Tin>(a.dk_prev, (size_t)bh * kN + cc, v8);
   }
   if (tid < 32) {  // gate gradients: dg_r, then the reverse cumulative sum over the chunk
     const float sdS = [&] {
