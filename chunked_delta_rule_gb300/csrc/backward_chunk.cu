@@ -1,5 +1,5 @@
 // Chunked (WY-form) backward of Falcon-1 / Falcon-1A, d_k = d_v = 64, chunk
-// 64, fp32 arithmetic on CUDA cores [FW 三种等价形式; JC 三种视角看同一个更新].
+// 64, fp32-accurate arithmetic [FW 三种等价形式; JC 三种视角看同一个更新].
 //
 // Forward of one chunk (rows r, i = 0..63; g the in-chunk cumulative log of
 // the clamped decay, Gamma = exp(g), E_r = exp(g_63 - g_r),
@@ -24,9 +24,10 @@
 //  (b) bwdc_fwd_chain_kernel, per (b, h, 16 value columns): chunk start states;
 //  (c) bwdc_bwd_chain_kernel, per (b, h, 16 value columns): dS at chunk ends;
 //  (d) bwdc_grad_kernel, per chunk: every gradient.
-// 64 x 64 products run on 256 threads from shared memory (4 x 4 outputs per
-// thread, 16-byte loads; the layout of each product chosen so that no load
-// conflicts on a bank).
+// The 64 x 64 products read fp32 operands from shared memory and run on the
+// tensor cores as warp-level m16n8k8 tf32 products with the three-term split
+// of each operand (hi + lo), which keeps their error at the level of fp32
+// accumulation; the element-wise work and the reductions stay in fp32.
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
