@@ -1059,17 +1059,17 @@ __global__ void __launch_bounds__(256, 1)
 // (b') pipelined sequential kernel, d_k = d_v = 64.  W, U and the gates of
 // every chunk come from the per-chunk kernel; four roles:
 //   warp 8      producer: TMA of chunk c into one of NST stages
-//   warps 4..7  front: P^T = [X ; X] Q^T (one 128-row product, each half of
-//               it read by two warps) -> decay-masked P~^T, and
-//               X~ = diag(exp(g_last - g)) X in place of X
+//   warps 4..7  front: P^T = X Q^T (an M = 64 product; each warp reads 16
+//               rows, its half-warps 32 columns each) -> decay-masked P~^T,
+//               and X~ = diag(exp(g_last - g)) X in place of X
 //   warps 0, 1  state chain: [D1 ; Oa] = [W ; Q] S0, Delta = U - D1,
 //               [D2 ; Ob] = [X~ | P~^T]^T Delta, S1 = Gamma_last S0 + D2
 //   warps 2, 3  outputs: O = diag(Gamma) Oa + Ob from the TMEM of the chunk
 //               the chain has just finished (two TMEM buffers), TMA store
 // The front works up to NST chunks ahead of the chain; the output warps run
 // one chunk behind it, off the chain's critical path.  Stage layout: X (then
-// X~) | X copy (then P~^T) | W | Q | U | gates, so that [X ; X], [W ; Q] and
-// [X~ | P~^T] are single operands.  Hand-offs are mbarriers: full/empty and
+// X~) | P~^T | W | Q | U | gates, so that [W ; Q] and [X~ | P~^T] are single
+// operands.  Hand-offs are mbarriers: full/empty and
 // front-done per stage, product completions, output-done per TMEM buffer.
 // ----------------------------------------------------------------------
 template <bool SOLVE>
@@ -1083,10 +1083,10 @@ struct PipeSmem {
   static constexpr size_t BAR = OST + 2 * 8192;
   static constexpr size_t MISC = BAR + 160;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
-  static constexpr uint32_t TX = 3 * 8192 + (SOLVE ? 8192 : 0) + 8192 + 1024;
+  static constexpr uint32_t TX = 2 * 8192 + (SOLVE ? 8192 : 0) + 8192 + 1024;
   static_assert(TOTAL <= 232448, "shared memory budget");
   static_assert(STAGE % 1024 == 0, "1 KB aligned stages");
-  // TMEM: P^T (M = 128 layout) | per buffer p: [D1 ; Oa] at 64 + 128 p, [D2 ; Ob] at 128 + 128 p
+  // TMEM: P^T (M = 64 layout) | per buffer p: [D1 ; Oa] at 64 + 128 p, [D2 ; Ob] at 128 + 128 p
   static constexpr uint32_t COL_PT = 0, NCOLS = 512;
   __host__ __device__ static constexpr uint32_t col_b1(int p) { return 64 + 128 * p; }
   __host__ __device__ static constexpr uint32_t col_b2(int p) { return 128 + 128 * p; }
@@ -1169,7 +1169,6 @@ __global__ void __launch_bounds__(288, 1)
         const size_t ci = (size_t)bh * NC + c;
         mbar_arrive_expect_tx(&full[s], L::TX);
         tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - a.shift, b);
-        tma_load_4d(st + L::PO, &tm_k, &full[s], 0, h, c * kC - a.shift, b);
         tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
         if (SOLVE) bulk_load(st + L::WO, a.ws_T + ci * 16384, 8192, &full[s]);
         bulk_load(st + L::UO, a.ws_T + ci * 16384 + 8192, 8192, &full[s]);
@@ -1183,27 +1182,24 @@ __global__ void __launch_bounds__(288, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ front
     const int ftid = tid - 128;
-    const int r = (32 * quad + lane) & 63;  // P^T row (key index) of this lane
-    const int half = quad >> 1;             // P^T columns 32 half .. 32 half + 31
+    const int r = 16 * quad + (lane & 15);  // P^T row (key index) of this lane
+    const int half = lane >> 4;             // P^T columns 32 half .. 32 half + 31
     uint32_t fph = 0;
     for (int c = 0; c < NC; ++c) {
       const int s = c % NST;
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
       uint8_t* st = stage(s);
       const float* gt = reinterpret_cast<const float*>(st + L::GO);
-      if (c == 0 && a.kprev_in && a.shift && ftid < 64) {  // x_0 = carried key, in both copies of X
-        const __nv_bfloat16 kv = a.kprev_in[(size_t)bh * 64 + ftid];
-        *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = kv;
-        *reinterpret_cast<__nv_bfloat16*>(st + L::PO + sw128(0, ftid)) = kv;
-      }
+      if (c == 0 && a.kprev_in && a.shift && ftid < 64)  // x_0 = carried key
+        *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = a.kprev_in[(size_t)bh * 64 + ftid];
       fence_proxy_async();
       tc_fence_before();
       if (named_bar_any(1, 128, *abort_flag != 0)) break;
       tc_fence_after();
-      if (ftid == 0) {  // P^T = [X ; X] Q^T
+      if (ftid == 0) {  // P^T = X Q^T
         const uint32_t sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + L::COL_PT, kdesc<128>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(128, 64),
+          umma_bf16(tmem + L::COL_PT, kdesc<64>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(64, 64),
                     ks > 0 ? 1u : 0u);
         umma_commit(fmma);
       }
@@ -1231,7 +1227,7 @@ __global__ void __launch_bounds__(288, 1)
       {  // P~^T[r][t] = P[t][r] exp(g_t - g_r) for t >= r.  With cf_t = exp(g_t - g_{16 J(t)}):
          // exp(g_t - g_r) = cf_t exp(g_{16 J} - g_r) across blocks and cf_t / cf_r inside one
         uint32_t pr[32];
-        tmem_ld32(tmem + lane_off + L::COL_PT + 32 * half, pr);
+        tmem_ld16x2_32(tmem + lane_off + L::COL_PT, pr);
         tmem_wait_ld();
         float pv[32];
 #pragma unroll
