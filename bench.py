@@ -99,10 +99,8 @@ def algorithmic_bytes(w) -> int:
 def kernel_bytes(w, names) -> list:
     """Algorithmic bytes each kernel of the path must move (the method's own
     inputs and outputs that the kernel touches; intermediates are not
-    counted).  d = 64: the per-chunk kernel reads k, v and the gate inputs,
-    the sequential one q and k and writes o and the final state.  d = 128:
-    the per-chunk kernel reads k and the gate inputs, the sequential one q,
-    k, v and writes o and the final state."""
+    counted).  The per-chunk kernel reads k, v and the gate inputs, the
+    sequential one q and k and writes o and the final state."""
     es = 2 if w.dtype == "bf16" else 4
     th = w.B * w.T * w.H
     beta = th * (w.dv if w.per_channel else 1) * 4
@@ -111,11 +109,7 @@ def kernel_bytes(w, names) -> list:
     state = w.B * w.H * w.dk * w.dv * 4
     if names[0] == "window_prep_kernel":  # keys and gate inputs; then the whole forward
         return [th * w.dk * es + beta + th * 4, algorithmic_bytes(w)]
-    if names[0] == "tc_wyu_kernel":
-        return [th * (w.dk + w.dv) * es + beta + th * 4, th * (2 * w.dk + w.dv) * es + state]
-    wy = th * w.dk * es + beta + th * 4
-    fwd = th * (2 * w.dk + 2 * w.dv) * es + state
-    return [wy, fwd]
+    return [th * (w.dk + w.dv) * es + beta + th * 4, th * (2 * w.dk + w.dv) * es + state]
 
 
 def algorithmic_flops(w) -> int:
@@ -610,7 +604,7 @@ def main():
         elif w.dk == 64:
             names = ["tc_wyu_kernel", "tc_fwd_pipe_kernel"]
         else:
-            names = ["tc_wy_kernel", "tc_fwd_kernel"]
+            names = ["tc_wyu_kernel", "tc_fwd_kernel"]
         kbytes = kernel_bytes(w, names)
         if args.prologue:  # the gather pass: q, k, v and gates in, the same out
             es = 2 if w.dtype == "bf16" else 4

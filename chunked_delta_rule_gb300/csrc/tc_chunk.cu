@@ -11,17 +11,16 @@
 //   S1      = Gamma_last S0 + (diag(exp(g_last - g)) X)^T Delta
 //
 // Two kernels per call:
-//  (a) per-chunk kernel, fully parallel: TMA loads the shifted keys (and, for
-//      d = 64, the values), one tcgen05 MMA forms the Gram matrix in TMEM,
+//  (a) per-chunk kernel, fully parallel: TMA loads the shifted keys and the
+//      values, one tcgen05 MMA forms the Gram matrix in TMEM,
 //      the gates (clamped log-decay, its in-chunk prefix sum, NLMS step) are
 //      formed from lambda, beta and the Gram diagonal, and T = (I + A)^{-1}
 //      is found by blocked forward substitution: 16x16 diagonal blocks in
 //      registers, off-diagonal blocks merged with warp-level tf32 MMAs in
-//      shared memory.  d = 64 (tc_wyu_kernel, one chunk per CTA): a second
-//      MMA forms [U ; W] = [T diag(eta) ; T diag(eta Gamma)] [V | X] and
-//      both leave as bf16 images of 128B-swizzled tiles.  d = 128
-//      (tc_wy_kernel, two chunks per CTA): T diag(eta) and T diag(eta Gamma)
-//      leave as such images.  Gates eta and g per row go along.
+//      shared memory (tc_wyu_kernel, one chunk per CTA, persistent).  A
+//      second MMA forms [U ; W] = [T diag(eta) ; T diag(eta Gamma)] [V | X]
+//      and both leave as bf16 images of 128B-swizzled tiles, with the gate
+//      rows Gamma, exp(g_last - g), g and exp(g - g_block).
 //  (b) sequential kernel, one CTA per (b, h) (per value slice for d = 128),
 //      the fp32 state in registers: TMA and bulk copies bring the chunk's
 //      operands while earlier chunks compute; every contraction is a
@@ -63,282 +62,24 @@ struct TcArgs {
   float* S_out;
   __nv_bfloat16* kprev_out;
   int64_t* pos_out;
-  uint8_t* ws_T;      // [B*H*NC][16384]: bf16 swizzled images, d = 64: W | U; d = 128: T diag(eta) | T diag(eta Gamma)
-  float* ws_g;        // [B*H*NC][kGateF]: d = 64: Gamma, exp(g_last - g), g, exp(g - g_block); d = 128: eta, g
+  uint8_t* ws_T;      // [B*H*NC][2 d_k 128]: bf16 128B-swizzled images, W slabs | U slabs
+  float* ws_g;        // [B*H*NC][kGateF]: Gamma, exp(g_last - g), g, exp(g - g_block)
   uint32_t* status;   // workspace status word
 };
 
 // ======================================================================
-// (a) per-chunk gates, Gram matrix and T = (I + A)^{-1}
-// ======================================================================
-template <int DK>
-struct WySmem {
-  static constexpr int kSlabs = DK / 64;
-  static constexpr size_t X = 0;                                  // kSlabs x 128 rows x 128 B
-  static constexpr size_t A = X + kSlabs * 16384;                 // [2][64][kLD] fp32
-  static constexpr size_t Tm = A + 2 * 64 * kLD * 4;              // [2][64][kLD] fp32
-  static constexpr size_t Y = Tm + 2 * 64 * kLD * 4;              // [2 chunks][2][2][16*kYL]
-  static constexpr size_t Ysc = Y + 2 * 4 * 16 * kYL * 4;         // [4 warps][16*kYL]
-  static constexpr size_t G = Ysc + 4 * 16 * kYL * 4;             // g[128]
-  static constexpr size_t E = G + 128 * 4;                        // eta, column factors, Gamma [128] each
-  static constexpr size_t WS = E + 384 * 4;                       // warp sums [4]
-  static constexpr size_t BAR = WS + 8 * 4;                       // 2 mbarriers
-  static constexpr size_t MISC = BAR + 16;                        // tmem addr, abort flag
-  static constexpr size_t TOTAL = MISC + 16 + 1024;               // + alignment slack
-};
-
-template <int DK, bool SOLVE>
-__global__ void __launch_bounds__(128) tc_wy_kernel(const __grid_constant__ CUtensorMap tm_k128,
-                                                    TcArgs a) {
-  using L = WySmem<DK>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  uint8_t* Xs = sm + L::X;
-  float* Am = reinterpret_cast<float*>(sm + L::A);
-  float* Tf = reinterpret_cast<float*>(sm + L::Tm);
-  float* Yb = reinterpret_cast<float*>(sm + L::Y);
-  float* Ysc = reinterpret_cast<float*>(sm + L::Ysc);
-  float* gs = reinterpret_cast<float*>(sm + L::G);
-  float* es = reinterpret_cast<float*>(sm + L::E);
-  float* wsum = reinterpret_cast<float*>(sm + L::WS);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pair = blockIdx.x, bh = blockIdx.y;
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream's previous grid (overlapped launch)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int b = bh / a.H, h = bh % a.H;
-  const int t_base = pair * 128;
-
-  if (tid == 0) {
-    *abort_flag = 0;
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbar_init();
-  }
-  if (SOLVE && warp == 0) {
-    tmem_alloc(tmem_slot, 128);
-    tmem_relinquish();
-    tc_fence_before();
-  }
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar[0], L::kSlabs * 128 * 128);
-    for (int s = 0; s < L::kSlabs; ++s)
-      tma_load_4d(Xs + s * 16384, &tm_k128, &bar[0], 64 * s, h, t_base - a.shift, b);
-  }
-  // gates while the keys are in flight: row tid <-> step t_base + tid
-  const int t = t_base + tid;
-  const bool step_ok = t < a.T;
-  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
-  const bool exists = step_ok && (pos + t >= a.shift);
-  const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
-  const float ell = step_ok ? clamped_log_decay(a.lam[gi], a.eps_gamma) : 0.f;
-  const float beta = step_ok ? a.beta[gi] : 0.f;
-  float g = ell;  // inclusive prefix sum inside each 64-step chunk
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float n = __shfl_up_sync(0xffffffffu, g, o);
-    if (lane >= o) g += n;
-  }
-  if (lane == 31) wsum[warp] = g;
-  __syncthreads();
-  if (warp & 1) g += wsum[warp - 1];
-  gs[tid] = g;
-
-  if (!mbar_wait(&bar[0], 0)) {
-    *abort_flag = 1;
-    atomicExch(a.status, kStatusTimeout);
-  }
-  if (pair == 0 && a.kprev_in && a.shift) {  // x_0 = carried key (row 0 of the first chunk)
-    for (int i = tid; i < DK; i += 128)
-      *reinterpret_cast<__nv_bfloat16*>(Xs + (i >> 6) * 16384 + sw128(0, i & 63)) =
-          a.kprev_in[(size_t)bh * DK + i];
-  }
-  fence_proxy_async();
-  __syncthreads();
-  const int cidx = tid >> 6, rl = tid & 63;
-  const int chunk = 2 * pair + cidx;
-  const bool aborted = *abort_flag != 0;
-
-  if (!SOLVE) {
-    // additive variants need only the gates: eta from the key energy
-    float n = 0.f;
-    if (!aborted) {
-      for (int i = 0; i < DK; ++i) {
-        const float x = __bfloat162float(
-            *reinterpret_cast<const __nv_bfloat16*>(Xs + (i >> 6) * 16384 + sw128(tid, i & 63)));
-        n += x * x;
-      }
-    }
-    const float eta = exists ? beta / (a.eps + n) : 0.f;
-    if (chunk < a.NC && !aborted) {
-      float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * kGateF;
-      go[rl] = eta;
-      go[64 + rl] = g;
-    }
-    return;
-  }
-
-  const uint32_t tmem = *tmem_slot;
-  if (!aborted && tid == 0) {
-    tc_fence_after();
-    mma_chain(tmem, Xs, 128, Xs, 128, DK, idesc_bf16(128, 128), false);
-    umma_commit(&bar[1]);
-  }
-  bool ok = aborted ? false : mbar_wait(&bar[1], 0);
-  if (!ok && !aborted) atomicExch(a.status, kStatusTimeout);
-  tc_fence_after();
-  float grow[64];
-  tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + 64 * cidx, grow);
-  tmem_wait_ld();
-  float n = 0.f;
-#pragma unroll
-  for (int j = 0; j < 64; ++j) n = (j == rl) ? grow[j] : n;
-  const float eta = exists ? beta / (a.eps + n) : 0.f;
-  es[tid] = eta;
-  // column factor exp(g_end(J) - g_i) of this row as a column, J = its 16-block
-  float* cfs = es + 128;
-  cfs[tid] = __expf(gs[cidx * 64 + (rl | 15)] - g);
-  float* gms = es + 256;
-  gms[tid] = __expf(g);
-  tc_fence_before();
-  __syncthreads();
-  {  // A_ri = eta_r exp(g_r - g_i) G_ri (i < r), the decay factored per 16-block
-    float* Arow = Am + cidx * 64 * kLD + rl * kLD;
-    const float* gc = gs + cidx * 64;
-    const float* cf = cfs + cidx * 64;
-    const int I = rl >> 4;
-#pragma unroll
-    for (int J = 0; J < 4; ++J) {
-      float av[16];
-      if (J < I) {
-        const float rf = eta * __expf(g - gc[16 * J + 15]);
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-          const float4 c4 = *reinterpret_cast<const float4*>(cf + 16 * J + i);
-          av[i] = rf * c4.x * grow[16 * J + i];
-          av[i + 1] = rf * c4.y * grow[16 * J + i + 1];
-          av[i + 2] = rf * c4.z * grow[16 * J + i + 2];
-          av[i + 3] = rf * c4.w * grow[16 * J + i + 3];
-        }
-      } else if (J == I) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          av[i] = (16 * J + i < rl) ? eta * __expf(g - gc[16 * J + i]) * grow[16 * J + i] : 0.f;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) av[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; i += 4)
-        *reinterpret_cast<float4*>(Arow + 16 * J + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 128);
-  }
-
-  // ---- T = (I + A)^{-1}: two warps per chunk
-  const int w2 = warp & 1;
-  const int nb_id = 1 + cidx;
-  float* A = Am + cidx * 64 * kLD;
-  float* Tm = Tf + cidx * 64 * kLD;
-  {  // 16x16 diagonal blocks, one column per lane, forward substitution
-    const int I = 2 * w2 + (lane >> 4), l = lane & 15;
-    float tv[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float s = (r == l) ? 1.f : 0.f;
-#pragma unroll
-      for (int i = 0; i < r; ++i) s -= A[(16 * I + r) * kLD + 16 * I + i] * tv[i];
-      tv[r] = s;
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) Tm[(16 * I + r) * kLD + 16 * I + l] = tv[r];
-  }
-  named_bar(nb_id, 64);
-  {  // T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22
-    const int I = w2 == 0 ? 1 : 3, J = I - 1;
-    float acc[2][4] = {};
-    warp_mm16(acc, A + 16 * I * kLD + 16 * J, kLD, Tm + 16 * J * kLD + 16 * J, kLD, lane);
-    float* ys = Ysc + warp * 16 * kYL;
-    warp_store16(ys, kYL, acc, 1.f, lane);
-    __syncwarp();
-    float acc2[2][4] = {};
-    warp_mm16(acc2, Tm + 16 * I * kLD + 16 * I, kLD, ys, kYL, lane);
-    warp_store16(Tm + 16 * I * kLD + 16 * J, kLD, acc2, -1.f, lane);
-  }
-  named_bar(nb_id, 64);
-  float* Yc = Yb + cidx * 4 * 16 * kYL;  // [I-2][J] blocks
-  {  // Y = A[32:64, 0:32] T[0:32, 0:32], row block I = 2 + w2
-    const int I = 2 + w2;
-    float acc[2][4] = {};
-    warp_mm16(acc, A + 16 * I * kLD, kLD, Tm, kLD, lane);
-    warp_mm16(acc, A + 16 * I * kLD + 16, kLD, Tm + 16 * kLD, kLD, lane);
-    warp_store16(Yc + (2 * w2 + 0) * 16 * kYL, kYL, acc, 1.f, lane);
-    float acc1[2][4] = {};
-    warp_mm16(acc1, A + 16 * I * kLD + 16, kLD, Tm + 16 * kLD + 16, kLD, lane);
-    warp_store16(Yc + (2 * w2 + 1) * 16 * kYL, kYL, acc1, 1.f, lane);
-  }
-  named_bar(nb_id, 64);
-  {  // T[32:64, 0:32] = -T[32:64, 32:64] Y
-    const int I = 2 + w2;
-#pragma unroll
-    for (int J = 0; J < 2; ++J) {
-      float acc[2][4] = {};
-      for (int K = 2; K <= I; ++K)
-        warp_mm16(acc, Tm + 16 * I * kLD + 16 * K, kLD, Yc + (2 * (K - 2) + J) * 16 * kYL, kYL,
-                  lane);
-      warp_store16(Tm + 16 * I * kLD + 16 * J, kLD, acc, -1.f, lane);
-    }
-  }
-  named_bar(nb_id, 64);
-  if (chunk < a.NC && !aborted) {
-    // bf16 images of T diag(eta) (for U) and T diag(eta Gamma) (for W) as
-    // 128B-swizzled K-major tiles, in that order; the upper triangle is zero
-    uint8_t* To = a.ws_T + ((size_t)bh * a.NC + chunk) * 16384;
-    const float* ec = es + cidx * 64;
-    const float* gc = gms + cidx * 64;
-    for (int idx = rl; idx < 512; idx += 64) {
-      const int R = idx >> 3, j = idx & 7;
-      const float4 lo4 = *reinterpret_cast<const float4*>(Tm + R * kLD + 8 * j);
-      const float4 hi4 = *reinterpret_cast<const float4*>(Tm + R * kLD + 8 * j + 4);
-      const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-      uint32_t pw[4], pu[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c0 = 8 * j + 2 * e;
-        const float t0 = (c0 <= R) ? v[2 * e] : 0.f, t1 = (c0 + 1 <= R) ? v[2 * e + 1] : 0.f;
-        pw[e] = pack_bf16(t0 * ec[c0] * gc[c0], t1 * ec[c0 + 1] * gc[c0 + 1]);
-        pu[e] = pack_bf16(t0 * ec[c0], t1 * ec[c0 + 1]);
-      }
-      const int off = R * 128 + 16 * (j ^ (R & 7));
-      *reinterpret_cast<uint4*>(To + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
-      *reinterpret_cast<uint4*>(To + 8192 + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-    }
-    float* go = a.ws_g + ((size_t)bh * a.NC + chunk) * kGateF;
-    go[rl] = eta;
-    go[64 + rl] = g;
-  }
-}
-
-// ======================================================================
-// (a') per-chunk WY products for the pipelined d = 64 path: one CTA per
-// chunk.  Besides the gates it leaves W = T diag(eta Gamma) X and
-// U = T diag(eta) V (Falcon-1) or U = diag(eta) V (Falcon-1A) in the
-// workspace as bf16 images of 128B-swizzled 64 x 64 tiles, so that the
+// (a) per-chunk gates and WY products, one chunk per CTA (persistent):
+// besides the gates it leaves W = T diag(eta Gamma) X and U = T diag(eta) V
+// (Falcon-1) or U = diag(eta) V (Falcon-1A) in the workspace as bf16 images
+// of 128B-swizzled 64 x 64 tiles (d_k / 64 slabs each), so that the
 // sequential kernel needs no per-chunk products of its own beyond P.
 // ======================================================================
+template <int DK>
 struct WyuSmem {
-  static constexpr size_t VX = 0;                  // V tile | X tile: [V | X] as a two-atom MN-major B
-  static constexpr size_t TI = 16384;              // [T diag(eta) ; T diag(eta Gamma)], 128 K-major rows;
-                                                   // the solve's 16x16 scratch blocks before that
+  static constexpr size_t VX = 0;                  // V slabs | X slabs: [V | X] as one MN-major B of 2 DK / 64 atoms
+  static constexpr size_t TI = 2 * DK * 128;       // [T diag(eta) ; T diag(eta Gamma)], 128 K-major rows;
+                                                   // the solve's 16x16 scratch blocks before that; the
+                                                   // W | U images (2 DK 128 bytes) after the product
   static constexpr size_t AT = TI + 16384;         // A, then T in place: [64][kLD] fp32
   static constexpr size_t E = AT + 64 * kLD * 4;   // g, eta, column factors, Gamma, beta (64 each)
   static constexpr size_t WS = E + 5 * 64 * 4;     // warp sums
@@ -347,15 +88,18 @@ struct WyuSmem {
   static constexpr size_t TOTAL = MISC + 16 + 1024;
 };
 
-template <bool SOLVE>
-__global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                     const __grid_constant__ CUtensorMap tm_v,
-                                                     TcArgs a) {
-  using L = WyuSmem;
+template <bool SOLVE, int DK>
+__global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                    const __grid_constant__ CUtensorMap tm_v,
+                                                                    TcArgs a) {
+  using L = WyuSmem<DK>;
+  constexpr int kSl = DK / 64;                  // 64-column slabs of keys and values
+  constexpr uint32_t kImg = 2 * DK * 128;       // W | U images of one chunk
+  static_assert(kImg <= 16384 + 64 * kLD * 4, "the images are staged over the T image and A / T");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* Vs = sm + L::VX;
-  uint8_t* Xs = sm + L::VX + 8192;
+  uint8_t* Xs = sm + L::VX + DK * 128;
   uint8_t* TI = sm + L::TI;
   float* T = reinterpret_cast<float*>(sm + L::AT);  // A, overwritten by T block by block
   float* gs = reinterpret_cast<float*>(sm + L::E);
@@ -383,7 +127,7 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     fence_mbar_init();
   }
   if (SOLVE && warp == 0) {
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, 2 * DK);
     tmem_relinquish();
     tc_fence_before();
   }
@@ -400,9 +144,11 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     const int chunk = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
     if (tid == 0) {
       ++issued;
-      mbar_arrive_expect_tx(&bar[0], 16384);
-      tma_load_4d(Vs, &tm_v, &bar[0], 0, h, t0, b);
-      tma_load_4d(Xs, &tm_k, &bar[0], 0, h, t0 - a.shift, b);
+      mbar_arrive_expect_tx(&bar[0], kImg);
+      for (int k = 0; k < kSl; ++k) {
+        tma_load_4d(Vs + k * 8192, &tm_v, &bar[0], 64 * k, h, t0, b);
+        tma_load_4d(Xs + k * 8192, &tm_k, &bar[0], 64 * k, h, t0 - a.shift, b);
+      }
     }
     const int t = t0 + tid;
     const bool step_ok = tid < 64 && t < a.T;
@@ -441,25 +187,25 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
   }
-  if (chunk == 0 && a.kprev_in && a.shift && tid < 64)  // x_0 = carried key (row 0 of the first chunk)
-    *reinterpret_cast<__nv_bfloat16*>(Xs + sw128(0, tid)) = a.kprev_in[(size_t)bh * 64 + tid];
+  if (chunk == 0 && a.kprev_in && a.shift && tid < DK)  // x_0 = carried key (row 0 of the first chunk)
+    *reinterpret_cast<__nv_bfloat16*>(Xs + (tid >> 6) * 8192 + sw128(0, tid & 63)) = a.kprev_in[(size_t)bh * DK + tid];
   fence_proxy_async();
   __syncthreads();
   const bool aborted = *abort_flag != 0;
   const size_t ci = (size_t)bh * a.NC + chunk;
-  uint8_t* Wo = a.ws_T + ci * 16384;  // W image, then the U image 8 KB further
+  uint8_t* Wo = a.ws_T + ci * kImg;  // W slabs, then the U slabs DK 128 bytes further
   float* go = a.ws_g + ci * kGateF;
   if (SOLVE && !aborted && tid == 0) {  // Gram matrix X X^T (M = 64: row r in lane 32 (r / 16) + r % 16)
     tc_fence_after();
-    mma_chain(tmem, Xs, 64, Xs, 64, 64, idesc_bf16(64, 64), false);
+    mma_chain(tmem, Xs, 64, Xs, 64, DK, idesc_bf16(64, 64), false);
     umma_commit(&bar[1]);
   }
   // NLMS step from the key energy, and the decay factors of each row
   if (tid < 64) {
     float n4[4] = {0.f, 0.f, 0.f, 0.f};  // four short chains
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(Xs + sw128(tid, 8 * j));
+    for (int j = 0; j < DK / 8; ++j) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(Xs + (j >> 3) * 8192 + sw128(tid, 8 * (j & 7)));
       const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -481,23 +227,24 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
       go[192 + tid] = __expf(g - gs[tid & ~15]);  // decay from the 16-block start
     }
   }
+  if (tid == 0) bulk_wait_read0();  // the previous item's image store has read its staging
   __syncthreads();
 
   if (!SOLVE) {  // additive write: U = diag(eta) V
     if (!aborted) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 4 * kSl; ++k) {
         const int idx = tid + 128 * k;
         const uint4 in = *reinterpret_cast<const uint4*>(Vs + idx * 16);
         const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-        const float fr = es[idx >> 3];
+        const float fr = es[(idx & 511) >> 3];
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 x = __bfloat1622float2(pin[e]);
           pk[e] = pack_bf16(x.x * fr, x.y * fr);
         }
-        *reinterpret_cast<uint4*>(Wo + 8192 + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(Wo + DK * 128 + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
     __syncthreads();  // the tiles are read
@@ -567,7 +314,6 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
         *reinterpret_cast<float4*>(Arow + 16 * J + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
     }
   }
-  if (tid == 0) bulk_wait_read0();  // the previous item's image store has read the buffer
   __syncthreads();
 
   // ---- T = (I + A)^{-1} in place; the 16x16 scratch blocks live in the
@@ -656,7 +402,7 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
     const uint32_t sT = smem_u32(TI), sV = smem_u32(Vs);
     for (int ks = 0; ks < 4; ++ks)
       umma_bf16(tmem, sdesc_k128(sT + ks * 32), sdesc_mn128_wide(sV + ks * 2048, 8192),
-                idesc_bf16(128, 128, false, true), ks > 0 ? 1u : 0u);
+                idesc_bf16(128, 2 * DK, false, true), ks > 0 ? 1u : 0u);
     umma_commit(&bar[1]);
   }
   if (!aborted && !mbar_wait(&bar[1], 1)) {
@@ -665,27 +411,30 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
   }
   tc_fence_after();
   if (next < n_items && !*abort_flag) fetch(next, lam_n, beta_n, pos_n);  // the tiles are read
-  {  // rows 0..63: U (columns 0..63); rows 64..127: W (columns 64..127), staged
-     // in the T image buffer (the product that read it is done) in the
-     // workspace layout, then stored by one bulk copy
-    float rv[64];
-    tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + (warp < 2 ? 0 : 64), rv);
-    tmem_wait_ld();
+  {  // rows 0..63: U (columns 0..DK-1); rows 64..127: W (columns DK..2 DK-1),
+     // staged from the T image buffer on (the product that read it and T is
+     // done) in the workspace layout, then stored by one bulk copy
     const int r = (32 * warp + lane) & 63;
-    uint8_t* dst = warp < 2 ? TI + 8192 : TI;
+#pragma unroll 1
+    for (int sl = 0; sl < kSl; ++sl) {
+      float rv[64];
+      tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + (warp < 2 ? 0 : DK) + 64 * sl, rv);
+      tmem_wait_ld();
+      uint8_t* dst = TI + (warp < 2 ? DK * 128 : 0) + sl * 8192;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t pk[4];
+      for (int j = 0; j < 8; ++j) {
+        uint32_t pk[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(rv[8 * j + 2 * e], rv[8 * j + 2 * e + 1]);
-      *reinterpret_cast<uint4*>(dst + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(rv[8 * j + 2 * e], rv[8 * j + 2 * e + 1]);
+        *reinterpret_cast<uint4*>(dst + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
     }
   }
   fence_proxy_async();
   tc_fence_before();
   if (__syncthreads_or(*abort_flag)) break;
   if (tid == 0) {
-    bulk_store(Wo, TI, 16384);
+    bulk_store(Wo, TI, kImg);
     bulk_commit();
   }
   }  // items
@@ -695,7 +444,7 @@ __global__ void __launch_bounds__(128, 4) tc_wyu_kernel(const __grid_constant__ 
   __syncthreads();
   if (SOLVE && warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 2 * DK);
   }
 }
 
@@ -706,13 +455,11 @@ template <int DK, int NV, bool SOLVE>
 struct FwdSmem {
   static constexpr int kKS = DK / 64;                 // 64-column slabs of the d_k contractions
   static constexpr size_t XSZ = DK * 128, QSZ = DK * 128, VSZ = NV * 128;
-  static constexpr size_t TSZ = SOLVE ? 16384 : 0, GSZ = 512;   // T diag(eta Gamma) | T diag(eta)
-  static constexpr size_t STAGE = XSZ + QSZ + VSZ + TSZ + 1024;  // gates padded to 1 KB
+  static constexpr size_t WSZ = SOLVE ? DK * 128 : 0, GSZ = 1024;  // W rows (K-major [64][DK]); 4 gate rows
+  static constexpr size_t STAGE = XSZ + QSZ + VSZ + WSZ + GSZ;     // X | Q | U slice | W | gates
   static constexpr size_t ST0 = 0;
-  static constexpr size_t VH = 2 * STAGE;              // additive: diag(eta) V rows (MN-major B)
-  static constexpr size_t PM = VH + (SOLVE ? 0 : VSZ); // decay-masked Q X^T, K-major rows
-  static constexpr size_t WB = PM + 8192;              // W rows, K-major [64][DK]
-  static constexpr size_t SB = WB + (SOLVE ? DK * 128 : 0);   // S rows, MN-major [DK][NV]
+  static constexpr size_t PM = 2 * STAGE;              // decay-masked Q X^T, K-major rows
+  static constexpr size_t SB = PM + 8192;              // S rows, MN-major [DK][NV]
   static constexpr size_t DL = SB + DK * 128;          // Delta rows (MN-major B)
   static constexpr size_t DD = DL + (SOLVE ? VSZ : 0); // diag(exp(g_last - g)) Delta rows
   static constexpr size_t OST = DD + VSZ;              // output staging [64][NV]
@@ -720,9 +467,10 @@ struct FwdSmem {
   static constexpr size_t BAR = SMALL + 4 * 64 * 4;    // full[2], mma
   static constexpr size_t MISC = BAR + 32;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
-  // TMEM columns: P and later P~ Delta share one block, W and later X~^T Delta another
-  static constexpr uint32_t COL_P = 0, COL_W = 64, COL_U = 64 + DK, COL_D1 = COL_U + NV,
-                            COL_OA = COL_D1 + NV, NCOL = COL_OA + NV;
+  // TMEM columns: P and later P~ Delta share one block; X~^T Delta (DK rows as
+  // DK / 64 blocks of 64), W S0 and Q S0 one block each
+  static constexpr uint32_t COL_P = 0, COL_W = 64, COL_D1 = COL_W + DK, COL_OA = COL_D1 + NV,
+                            NCOL = COL_OA + NV;
   static_assert(NCOL <= 512, "TMEM budget");
   static_assert(NV == 64, "value slice of 64 channels");
 };
@@ -730,22 +478,18 @@ struct FwdSmem {
 template <int DK, int NV, bool SOLVE>
 __global__ void __launch_bounds__(256, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  TcArgs a) {
+                  const __grid_constant__ CUtensorMap tm_o, TcArgs a) {
   using L = FwdSmem<DK, NV, SOLVE>;
+  constexpr uint32_t kImg = 2 * DK * 128;  // W | U images of a chunk in the workspace
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* VH = sm + L::VH;
   uint8_t* Pm = sm + L::PM;
-  uint8_t* Wb = sm + L::WB;
   uint8_t* SB = sm + L::SB;
-  uint8_t* DL = SOLVE ? sm + L::DL : sm + L::VH;  // additive write: Delta = diag(eta) V
   uint8_t* DD = sm + L::DD;
   uint8_t* Ost = sm + L::OST;
   float* Gam = reinterpret_cast<float*>(sm + L::SMALL);
   float* dec = Gam + 64;
   float* gl = dec + 64;
-  float* et = gl + 64;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* mbar = full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
@@ -759,23 +503,24 @@ __global__ void __launch_bounds__(256, 1)
   auto stage = [&](int s) { return sm + L::ST0 + s * L::STAGE; };
   auto Xst = [&](int s) { return stage(s); };
   auto Qst = [&](int s) { return stage(s) + L::XSZ; };
-  auto Vst = [&](int s) { return stage(s) + L::XSZ + L::QSZ; };
-  auto Tst = [&](int s) { return stage(s) + L::XSZ + L::QSZ + L::VSZ; };
+  auto Ust = [&](int s) { return stage(s) + L::XSZ + L::QSZ; };
+  auto Wst = [&](int s) { return stage(s) + L::XSZ + L::QSZ + L::VSZ; };
   auto Gst = [&](int s) {
-    return reinterpret_cast<float*>(stage(s) + L::XSZ + L::QSZ + L::VSZ + L::TSZ);
+    return reinterpret_cast<float*>(stage(s) + L::XSZ + L::QSZ + L::VSZ + L::WSZ);
   };
 
   auto issue_stage = [&](int c, int s) {
-    const uint32_t bytes = (uint32_t)(L::XSZ + L::QSZ + L::VSZ + L::TSZ + L::GSZ);
+    const uint32_t bytes = (uint32_t)(L::XSZ + L::QSZ + L::VSZ + L::WSZ + L::GSZ);
     mbar_arrive_expect_tx(&full[s], bytes);
     for (int k = 0; k < L::kKS; ++k) {
       tma_load_4d(Xst(s) + k * 8192, &tm_k, &full[s], 64 * k, h, c * kC - a.shift, b);
       tma_load_4d(Qst(s) + k * 8192, &tm_q, &full[s], 64 * k, h, c * kC, b);
     }
-    tma_load_4d(Vst(s), &tm_v, &full[s], c0, h, c * kC, b);
     const size_t ci = (size_t)bh * NC + c;
-    if (SOLVE) bulk_load(Tst(s), a.ws_T + ci * 16384, 16384, &full[s]);
-    bulk_load(Gst(s), a.ws_g + ci * kGateF, 512, &full[s]);
+    const uint8_t* img = a.ws_T + ci * kImg;  // W slabs | U slabs
+    bulk_load(Ust(s), img + DK * 128 + (c0 / 64) * 8192, (uint32_t)L::VSZ, &full[s]);
+    if (SOLVE) bulk_load(Wst(s), img, (uint32_t)L::WSZ, &full[s]);
+    bulk_load(Gst(s), a.ws_g + ci * kGateF, (uint32_t)L::GSZ, &full[s]);
   };
 
   if (tid == 0) {
@@ -828,9 +573,7 @@ __global__ void __launch_bounds__(256, 1)
   fence_proxy_async();
   __syncthreads();
 
-  const uint32_t sP = smem_u32(Pm), sW = smem_u32(Wb), sS = smem_u32(SB), sDL = smem_u32(DL),
-                 sDD = smem_u32(DD);
-  float ureg[NV];
+  const uint32_t sP = smem_u32(Pm), sS = smem_u32(SB), sDD = smem_u32(DD);
   uint32_t mph = 0;
   for (int c = 0; c < NC; ++c) {
     const int s = c & 1;
@@ -848,27 +591,23 @@ __global__ void __launch_bounds__(256, 1)
         *reinterpret_cast<__nv_bfloat16*>(Xst(0) + (i >> 6) * 8192 + sw128(0, i & 63)) =
             a.kprev_in[(size_t)bh * DK + i];
     }
-    if (tid < 64) {
+    if (tid < 64) {  // Gamma, exp(g_last - g), g of the chunk's rows
       const float* G = Gst(s);
-      const float g = G[64 + tid], glast = G[64 + 63], e = G[tid];
-      const float gm = __expf(g);
-      Gam[tid] = gm;
-      dec[tid] = __expf(glast - g);
-      gl[tid] = g;
-      et[tid] = SOLVE ? e * gm : e;  // row scale of X (Falcon-1) or of V (Falcon-1A)
+      Gam[tid] = G[tid];
+      dec[tid] = G[64 + tid];
+      gl[tid] = G[128 + tid];
     }
     if (__syncthreads_or(*abort_flag)) break;
     const float gam_last = Gam[63];
+    // Delta rows: U - W S0 (Falcon-1, formed below) or U itself (Falcon-1A)
+    const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(Ust(s));
 
-    // ---- row-scaled operands of the additive write (16-byte chunks)
-    if (SOLVE) {
-    } else {
-      scale_rows(VH, Vst(s), et, tid, 256);  // Delta = diag(eta) V
-      for (int idx = tid; idx < 512; idx += 256) {  // diag(exp(g_last - g) eta) V
+    if (!SOLVE) {  // diag(exp(g_last - g)) U (16-byte chunks)
+      for (int idx = tid; idx < 512; idx += 256) {
         const int R = idx >> 3;
-        const uint4 in = *reinterpret_cast<const uint4*>(Vst(s) + idx * 16);
+        const uint4 in = *reinterpret_cast<const uint4*>(Ust(s) + idx * 16);
         const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-        const float fr = et[R] * dec[R];
+        const float fr = dec[R];
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -878,22 +617,18 @@ __global__ void __launch_bounds__(256, 1)
         *reinterpret_cast<uint4*>(DD + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
-    fence_proxy_async();
+    fence_proxy_async();  // the carried key and the scaled rows, for the products
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- P = Q X^T, W = T X^, U = T V^, Oa = Q S0
+    // ---- P = Q X^T, D1 = W S0, Oa = Q S0 (W and U come from the per-chunk kernel)
     if (tid == 0) {
-      const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s)), sT = smem_u32(Tst(s));
+      const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s));
       mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, DK, idesc_bf16(64, 64), false);
-      if (SOLVE) {
-        for (int k = 0; k < L::kKS; ++k)  // W = T diag(eta Gamma) X, U = T diag(eta) V
-          mma_chain_mn(tmem + L::COL_W + 64 * k, kdesc<64>, sT + 8192, mndesc, sX + k * 8192, 64,
-                       idesc_bf16(64, 64, false, true), false);
-        mma_chain_mn(tmem + L::COL_U, kdesc<64>, sT, mndesc, smem_u32(Vst(s)), 64,
+      if (SOLVE)
+        mma_chain_mn(tmem + L::COL_D1, kdesc<64>, smem_u32(Wst(s)), mndesc, sS, DK,
                      idesc_bf16(64, NV, false, true), false);
-      }
       mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
                    false);
       umma_commit(mbar);
@@ -914,19 +649,28 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = 0; i < 64; ++i) pv[i] = (i <= r64) ? __expf(gr - gl[i]) * pv[i] : 0.f;
         store_row64(Pm, r64, pv);
       }
-    } else if (SOLVE) {  // W rows -> K-major operand, U rows -> registers
-#pragma unroll
-      for (int k = 0; k < L::kKS; ++k) {
-        float wv[64];
-        tmem_ld64(tmem + lane_off + L::COL_W + 64 * k, wv);
-        tmem_wait_ld();
-        if (row64) store_row64(Wb + k * 8192, r64, wv);
-      }
-      float uv[64];
-      tmem_ld64(tmem + lane_off + L::COL_U, uv);
+    } else if (SOLVE) {  // Delta = U - W S0, and diag(exp(g_last - g)) Delta
+      float dv1[64];
+      tmem_ld64(tmem + lane_off + L::COL_D1, dv1);
       tmem_wait_ld();
+      if (row64) {
 #pragma unroll
-      for (int n = 0; n < NV; ++n) ureg[n] = uv[n];
+        for (int j = 0; j < 8; ++j) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(Ust(s) + sw128(r64, 8 * j));
+          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 u2 = __bfloat1622float2(pu[e]);
+            dv1[8 * j + 2 * e] = u2.x - dv1[8 * j + 2 * e];
+            dv1[8 * j + 2 * e + 1] = u2.y - dv1[8 * j + 2 * e + 1];
+          }
+        }
+        store_row64(sm + L::DL, r64, dv1);
+        const float dr = dec[r64];
+#pragma unroll
+        for (int n = 0; n < NV; ++n) dv1[n] *= dr;
+        store_row64(DD, r64, dv1);
+      }
     }
     fence_proxy_async();
     tc_fence_before();
@@ -934,39 +678,6 @@ __global__ void __launch_bounds__(256, 1)
     const bool ab2 = __syncthreads_or(*abort_flag);
     tc_fence_after();
     if (ab2) break;
-
-    if (SOLVE) {  // Delta = U - W S0
-      if (tid == 0) {
-        mma_chain_mn(tmem + L::COL_D1, kdesc<64>, sW, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
-                     false);
-        umma_commit(mbar);
-      }
-      if (!mbar_wait(mbar, mph)) {
-        *abort_flag = 1;
-        atomicExch(a.status, kStatusTimeout);
-      }
-      mph ^= 1;
-      tc_fence_after();
-      if (!lo) {
-        float dv1[64];
-        tmem_ld64(tmem + lane_off + L::COL_D1, dv1);
-        tmem_wait_ld();
-        if (row64) {
-#pragma unroll
-          for (int n = 0; n < NV; ++n) dv1[n] = ureg[n] - dv1[n];
-          store_row64(DL, r64, dv1);
-          const float dr = dec[r64];
-#pragma unroll
-          for (int n = 0; n < NV; ++n) dv1[n] *= dr;
-          store_row64(DD, r64, dv1);
-        }
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      const bool ab3 = __syncthreads_or(*abort_flag);
-      tc_fence_after();
-      if (ab3) break;
-    }
 
     // ---- D2 = X^T diag(exp(g_last - g)) Delta, Ob = P~ Delta
     if (tid == 0) {
@@ -1443,12 +1154,13 @@ __global__ void __launch_bounds__(288, 1)
 struct WsLayout {
   size_t status, T, g, total;
 };
-WsLayout ws_layout(int B, int T, int H, int chunk) {
+// Per chunk: the bf16 W | U images (2 d_k 128 bytes) and kGateF gate floats.
+WsLayout ws_layout(int B, int T, int H, int chunk, int dk) {
   const size_t NC = (size_t)(T + chunk - 1) / chunk;
   WsLayout w;
   w.status = 0;
   w.T = 256;
-  w.g = w.T + (size_t)B * H * NC * 16384;
+  w.g = w.T + (size_t)B * H * NC * (2 * (size_t)dk * 128);
   w.total = align_up(w.g + (size_t)B * H * NC * kGateF * 4, 256);
   return w;
 }
@@ -1500,8 +1212,8 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
     return FALCON_ERR_CUDA;
   if constexpr (DK == 64) {
     {  // per-chunk gates, W and U
-      auto k = tc_wyu_kernel<SOLVE>;
-      const size_t smem = WyuSmem::TOTAL;
+      auto k = tc_wyu_kernel<SOLVE, 64>;
+      const size_t smem = WyuSmem<64>::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
       // persistent: four CTAs per SM (shared memory and TMEM both allow four)
@@ -1521,16 +1233,15 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       record_event(fa, 2);
     }
   } else {
-    CUtensorMap mk128;
-    if (!make_map(&mk128, fa.k, fa.B, fa.T, fa.H, DK, 128)) return FALCON_ERR_CUDA;
-    {
-      auto k = tc_wy_kernel<DK, SOLVE>;
-      const size_t smem = WySmem<DK>::TOTAL;
+    {  // per-chunk gates, W and U (d = 128: two CTAs per SM)
+      auto k = tc_wyu_kernel<SOLVE, DK>;
+      const size_t smem = WyuSmem<DK>::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
-      dim3 grid((ta.NC + 1) / 2, BH);
+      const long items = (long)ta.NC * BH;
+      dim3 grid((unsigned)std::min<long>(items, 2L * sm_count()));
       record_event(fa, 0);
-      if (launch_overlapped(fa, k, grid, dim3(128), smem, mk128, ta) != FALCON_OK) return FALCON_ERR_CUDA;
+      if (launch_overlapped(fa, k, grid, dim3(128), smem, mk, mv, ta) != FALCON_OK) return FALCON_ERR_CUDA;
       record_event(fa, 1);
     }
     {
@@ -1539,7 +1250,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
       dim3 grid(BH, fa.dv / NV);
-      if (launch_overlapped(fa, k, grid, dim3(256), smem, mq, mk, mv, mo, ta) != FALCON_OK) return FALCON_ERR_CUDA;
+      if (launch_overlapped(fa, k, grid, dim3(256), smem, mq, mk, mo, ta) != FALCON_OK) return FALCON_ERR_CUDA;
       record_event(fa, 2);
     }
   }
@@ -1558,15 +1269,15 @@ bool tc_chunk_supported(const FwdArgs& a) {
 
 int tc_chunk_launches(const FwdArgs& a) { return tc_f2_supported(a) || tc_f3a_supported(a) ? 1 : 2; }
 
-size_t tc_chunk_ws_bytes(int B, int T, int H, int, int, int chunk, int variant) {
+size_t tc_chunk_ws_bytes(int B, int T, int H, int dk, int, int chunk, int variant) {
   if (variant == FALCON_2 || variant == FALCON_2A || variant == FALCON_3A) return 256;  // status word only
-  return ws_layout(B, T, H, chunk).total;
+  return ws_layout(B, T, H, chunk, dk).total;
 }
 
 int launch_tc_chunk(const FwdArgs& fa) {
   if (tc_f2_supported(fa)) return launch_tc_f2(fa);
   if (tc_f3a_supported(fa)) return launch_tc_f3a(fa);
-  const WsLayout w = ws_layout(fa.B, fa.T, fa.H, 64);
+  const WsLayout w = ws_layout(fa.B, fa.T, fa.H, 64, fa.dk);
   uint8_t* ws = reinterpret_cast<uint8_t*>(fa.ws);
   TcArgs ta;
   ta.B = fa.B; ta.T = fa.T; ta.H = fa.H; ta.NC = (fa.T + kC - 1) / kC;

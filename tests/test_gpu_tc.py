@@ -1,9 +1,9 @@
 """Tensor-core chunk path (tcgen05 / TMEM / TMA): parity with the oracle when
 forced, agreement with the portable path, and a white-box check of the
 per-chunk WY stage and what it leaves in the workspace, with T = (I + A)^{-1}:
-d = 64, the bf16 images of W = T diag(eta Gamma) X and U = T diag(eta) V and
-the decay gates of the sequential kernel; d = 128, the images of T diag(eta)
-and T diag(eta Gamma), eta and the in-chunk log-decay."""
+the bf16 images of W = T diag(eta Gamma) X and U = T diag(eta) V (d / 64
+slabs of 64 columns each, d = 64 and 128) and the decay gates of the
+sequential kernel."""
 
 from __future__ import annotations
 
@@ -54,7 +54,8 @@ def test_wy_stage_workspace(F, d):
     wsn = ws.cpu().numpy()
     assert int(wsn[:4].view(np.uint32)[0]) == 0, "status word set"
     t_off = 256
-    g_off = t_off + w.B * w.H * NC * 16384
+    img_bytes = 2 * d * 128  # W slabs | U slabs
+    g_off = t_off + w.B * w.H * NC * img_bytes
     k = x["k"].float().cpu().numpy().astype(np.float64)
     vv = x["v"].float().cpu().numpy().astype(np.float64)
     lam = x["lam"].cpu().numpy().astype(np.float64)
@@ -75,27 +76,23 @@ def test_wy_stage_workspace(F, d):
             A = eta[:, None] * np.exp(np.minimum(g[:, None] - g[None, :], 0)) * G * np.tril(np.ones((64, 64)), -1)
             Tref = np.linalg.inv(np.eye(64) + A)
             ci = bh * NC + c
-            img = wsn[t_off + ci * 16384: t_off + (ci + 1) * 16384]
+            img = wsn[t_off + ci * img_bytes: t_off + (ci + 1) * img_bytes]
             Tw_ref = Tref * (eta * np.exp(g))[None, :]
             Tu_ref = Tref * eta[None, :]
-            if d == 64:
-                V = np.zeros((64, d))
-                V[ok] = vv[b, rows[ok], h]
-                pairs = [(decode_T(img[:8192]), Tw_ref @ X), (decode_T(img[8192:]), Tu_ref @ V)]
-            else:
-                pairs = [(decode_T(img[:8192]), Tu_ref), (decode_T(img[8192:]), Tw_ref)]
-            for got, ref in pairs:
+            V = np.zeros((64, d))
+            V[ok] = vv[b, rows[ok], h]
+            slabs = range(d // 64)
+            got_W = np.hstack([decode_T(img[8192 * sl:8192 * (sl + 1)]) for sl in slabs])
+            got_U = np.hstack([decode_T(img[d * 128 + 8192 * sl:d * 128 + 8192 * (sl + 1)]) for sl in slabs])
+            for got, ref in ((got_W, Tw_ref @ X), (got_U, Tu_ref @ V)):
                 assert np.abs(got - ref).max() <= 2e-2 * max(np.abs(ref).max(), 1e-30), (bh, c)
+            # Gamma, exp(g_last - g), g, exp(g - g at the start of the 16-row block)
             gates = wsn[g_off + ci * 1024: g_off + (ci + 1) * 1024].view(np.float32)
-            if d == 64:  # Gamma, exp(g_last - g), g, exp(g - g at the start of the 16-row block)
-                assert np.allclose(gates[:64], np.exp(g), rtol=1e-4, atol=1e-6), (bh, c)
-                assert np.allclose(gates[64:128], np.exp(g[-1] - g), rtol=1e-4, atol=1e-6), (bh, c)
-                assert np.allclose(gates[128:192], g, rtol=1e-4, atol=1e-5), (bh, c)
-                assert np.allclose(gates[192:256], np.exp(g - g[np.arange(64) & ~15]), rtol=1e-4,
-                                   atol=1e-6), (bh, c)
-            else:  # eta, g
-                assert np.allclose(gates[:64], eta, rtol=2e-3, atol=1e-6), (bh, c)
-                assert np.allclose(gates[64:128], g, rtol=1e-4, atol=1e-5), (bh, c)
+            assert np.allclose(gates[:64], np.exp(g), rtol=1e-4, atol=1e-6), (bh, c)
+            assert np.allclose(gates[64:128], np.exp(g[-1] - g), rtol=1e-4, atol=1e-6), (bh, c)
+            assert np.allclose(gates[128:192], g, rtol=1e-4, atol=1e-5), (bh, c)
+            assert np.allclose(gates[192:256], np.exp(g - g[np.arange(64) & ~15]), rtol=1e-4,
+                               atol=1e-6), (bh, c)
 
 
 @pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])
