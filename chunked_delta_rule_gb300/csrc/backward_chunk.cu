@@ -92,7 +92,9 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
   lo = tc::to_tf32(x - __uint_as_float(hi));
 }
 
-template <int MODE>
+// AX / BX: that operand holds values exact in tf32 (bf16 inputs as loaded),
+// so its low part is zero and the product term that would use it is skipped.
+template <int MODE, bool AX = false, bool BX = false>
 __device__ __forceinline__ void mm64(float (&acc)[kRows][4], const float* __restrict__ A,
                                      const float* __restrict__ B) {
   static_assert(kRows == 4, "two 16-row tiles of two 8-column tiles per warp");
@@ -118,7 +120,10 @@ __device__ __forceinline__ void mm64(float (&acc)[kRows][4], const float* __rest
         x[3] = A[(m + 8) * LDM + k0 + tig + 4];
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) split_tf32(x[e], ah[mt][e], al[mt][e]);
+      for (int e = 0; e < 4; ++e) {
+        if (AX) ah[mt][e] = __float_as_uint(x[e]);
+        else split_tf32(x[e], ah[mt][e], al[mt][e]);
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -132,7 +137,10 @@ __device__ __forceinline__ void mm64(float (&acc)[kRows][4], const float* __rest
         y[1] = B[(k0 + tig + 4) * LDM + n];
       }
 #pragma unroll
-      for (int e = 0; e < 2; ++e) split_tf32(y[e], bh[nt][e], bl[nt][e]);
+      for (int e = 0; e < 2; ++e) {
+        if (BX) bh[nt][e] = __float_as_uint(y[e]);
+        else split_tf32(y[e], bh[nt][e], bl[nt][e]);
+      }
     }
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
@@ -140,8 +148,8 @@ __device__ __forceinline__ void mm64(float (&acc)[kRows][4], const float* __rest
       for (int nt = 0; nt < 2; ++nt) {
         float c[4] = {acc[2 * mt][2 * nt], acc[2 * mt][2 * nt + 1], acc[2 * mt + 1][2 * nt],
                       acc[2 * mt + 1][2 * nt + 1]};
-        tc::mma_tf32_16x8x8(c, al[mt], bh[nt]);
-        tc::mma_tf32_16x8x8(c, ah[mt], bl[nt]);
+        if (!AX) tc::mma_tf32_16x8x8(c, al[mt], bh[nt]);
+        if (!BX) tc::mma_tf32_16x8x8(c, ah[mt], bl[nt]);
         tc::mma_tf32_16x8x8(c, ah[mt], bh[nt]);
         acc[2 * mt][2 * nt] = c[0];
         acc[2 * mt][2 * nt + 1] = c[1];
@@ -350,6 +358,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   const int c = (int)(cg % a.NC), bh = (int)(cg / a.NC), b = bh / a.H, h = bh % a.H, t0 = c * kN;
   const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
   const int tid = threadIdx.x;
+  constexpr bool kE = sizeof(Tin) == 2;  // bf16 inputs: X, Q, V, dO exact in tf32
   load_inputs<Tin>(X, Q, V, dO, a, b, h, t0, pos);
   __syncthreads();
   make_gates(gs, X, a, b, h, t0, pos);
@@ -357,7 +366,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   if (!a.additive) {
     // A = diag(eta) (D (.) X X^T), strictly lower
     zero_acc(acc);
-    mm64<NT>(acc, X, X);
+    mm64<NT, kE, kE>(acc, X, X);
 #pragma unroll
     for (int i = 0; i < kRows; ++i)
 #pragma unroll
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   __syncthreads();
   // Y = Q^T diag(Gamma) dO - W^T (P (.) D)^T dO
   zero_acc(acc);
-  mm64<NT>(acc, Q, X);  // P = Q X^T
+  mm64<NT, kE, kE>(acc, Q, X);  // P = Q X^T
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
 #pragma unroll
@@ -448,10 +457,10 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   __syncthreads();
   float yacc[kRows][4];
   zero_acc(yacc);
-  mm64<TN>(yacc, Q, M3);  // Q^T diag(Gamma) dO
+  mm64<TN, kE>(yacc, Q, M3);  // Q^T diag(Gamma) dO
   if (!a.additive) {
     zero_acc(acc);
-    mm64<TN>(acc, M1, dO);  // Z = (P (.) D)^T dO
+    mm64<TN, false, kE>(acc, M1, dO);  // Z = (P (.) D)^T dO
     __syncthreads();        // M3 is read by every thread above
 #pragma unroll
     for (int i = 0; i < kRows; ++i)
@@ -694,6 +703,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
   const int tid = threadIdx.x;
   const bool reg = !a.additive;
+  constexpr bool kE = sizeof(Tin) == 2;  // bf16 inputs: X, Q, V, dO exact in tf32
   {  // the workspace matrices by cp.async, the input rows meanwhile
     cp_mat(S0, wsmat(a, cg, M_S0));
     cp_mat(dS1, wsmat(a, cg, M_DS1));
@@ -731,7 +741,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   // X S0 -> s1 (regression); Q S0 -> s3
   if (reg) {
     zero_acc(acc);
-    mm64<NN>(acc, X, S0);
+    mm64<NN, kE>(acc, X, S0);
     __syncthreads();  // s1 (W) is consumed
 #pragma unroll
     for (int i = 0; i < kRows; ++i)
@@ -739,7 +749,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
       for (int j = 0; j < 4; ++j) s1[out_row<NN>(i) * LDM + out_col<NN>(j)] = acc[i][j];
   }
   zero_acc(acc);
-  mm64<NN>(acc, Q, S0);
+  mm64<NN, kE>(acc, Q, S0);
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
 #pragma unroll
@@ -752,7 +762,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   __syncthreads();
   // P (.) D -> s3 (lower incl. diagonal)
   zero_acc(acc);
-  mm64<NT>(acc, Q, X);
+  mm64<NT, kE, kE>(acc, Q, X);
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
@@ -763,7 +773,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     }
   // X dS1 -> s4
   zero_acc(acc);
-  mm64<NN>(acc, X, dS1);
+  mm64<NN, kE>(acc, X, dS1);
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
 #pragma unroll
@@ -775,7 +785,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   }
   // dDelta = (P (.) D)^T dO + diag(E) X dS1 -> s5
   zero_acc(acc);
-  mm64<TN>(acc, s3, dO);
+  mm64<TN, false, kE>(acc, s3, dO);
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
 #pragma unroll
@@ -828,7 +838,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     mm64<NT>(acc, s6, s2);  // dR Delta^T
     float gacc[kRows][4];
     zero_acc(gacc);
-    mm64<NT>(gacc, X, X);   // G
+    mm64<NT, kE, kE>(gacc, X, X);   // G
     __syncthreads();        // s4 (T), s5 consumed
     float dea[kRows] = {};
 #pragma unroll
@@ -859,8 +869,8 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     }
     __syncthreads();
     zero_acc(acc);
-    mm64<NN>(acc, s1, X);   // dG X
-    mm64<TN>(acc, s1, X);   // dG^T X
+    mm64<NN, false, kE>(acc, s1, X);   // dG X
+    mm64<TN, false, kE>(acc, s1, X);   // dG^T X
     float dx2[kRows][4];
     zero_acc(dx2);
     mm64<NT>(dx2, s6, S0);  // dR S0^T (NT layout)
@@ -886,7 +896,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   __syncthreads();
   // dO Delta^T -> M += (dO Delta^T) (.) (P (.) D); dP = (dO Delta^T) (.) D -> s1
   zero_acc(acc);
-  mm64<NT>(acc, dO, s2);
+  mm64<NT, kE>(acc, dO, s2);
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
@@ -901,9 +911,9 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   {
     float qa[kRows][4], qb[kRows][4];
     zero_acc(qa);
-    mm64<NT>(qa, dO, S0);
+    mm64<NT, kE>(qa, dO, S0);
     zero_acc(qb);
-    mm64<NN>(qb, s1, X);
+    mm64<NN, false, kE>(qb, s1, X);
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kRows; ++i)
@@ -917,7 +927,7 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
   }
   // dX += dP^T Q + diag(E) Delta dS1^T
   zero_acc(acc);
-  mm64<TN>(acc, s1, Q);
+  mm64<TN, false, kE>(acc, s1, Q);
   {
     float xa[kRows][4];
     zero_acc(xa);
