@@ -556,31 +556,55 @@ def main():
     tokens = w.B * w.T * world
     value = job_tokens_per_s(w, world, ms_step)
 
-    # end to end through the C ABI with host buffers: pinned host -> device
-    # copies of the step's inputs, the call, and the output read back
+    # end to end through the C ABI with host buffers: every step copies its
+    # inputs from pinned host memory to the device, makes the call and reads
+    # its output back.  Two buffer sets and three streams let step i's input
+    # copy run while step i-1 computes and step i-2's output comes back (the
+    # copy engines of both directions work at once); each buffer is reused
+    # only after the step that last used it is done with it.
     host = {k: v.cpu().pin_memory() for k, v in sets[0].items()}
-    dev_in = {k: torch.empty_like(v) for k, v in sets[0].items()}
-    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    dev_in = [{k: torch.empty_like(v) for k, v in sets[0].items()} for _ in range(2)]
+    o_dev = [o, torch.empty_like(o)]
+    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = o.numel() * o.element_size()
-    for _ in range(3):
-        for k2 in host:
-            dev_in[k2].copy_(host[k2], non_blocking=True)
-        F.falcon_chunk_fwd(p, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["beta"], dev_in["lam"],
-                           None, o, carry, ws, ws_n, stream)
-        o_host.copy_(o, non_blocking=True)
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of set j on the device
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # the call on set j is done
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # output j is back on the host
+
+    def e2e_step(i):
+        j = i & 1
+        s_h2d.wait_event(ev_used[j])
+        with torch.cuda.stream(s_h2d):
+            for k2 in host:
+                dev_in[j][k2].copy_(host[k2], non_blocking=True)
+        ev_in[j].record(s_h2d)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])
+        x = dev_in[j]
+        F.falcon_chunk_fwd(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o_dev[j], carry, ws, ws_n,
+                           stream)
+        ev_used[j].record(stream)
+        s_d2h.wait_event(ev_used[j])
+        with torch.cuda.stream(s_d2h):
+            o_host[j].copy_(o_dev[j], non_blocking=True)
+        ev_out[j].record(s_d2h)
+
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        for k2 in host:
-            dev_in[k2].copy_(host[k2], non_blocking=True)
-        F.falcon_chunk_fwd(p, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["beta"], dev_in["lam"],
-                           None, o, carry, ws, ws_n, stream)
-        o_host.copy_(o, non_blocking=True)
+    s_h2d.wait_event(e0)
+    s_d2h.wait_event(e0)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    stream.wait_event(ev_out[0])
+    stream.wait_event(ev_out[1])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
