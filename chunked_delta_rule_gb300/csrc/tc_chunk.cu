@@ -546,30 +546,47 @@ __global__ void __launch_bounds__(256, 1)
     issued[0] = 1;
   }
 
-  // Thread roles on the M = 64 accumulators: rows r = 16 * quadrant + lane
-  // live in lanes 0..15 of each TMEM quadrant.  Warps 0..3 keep S rows 0..63
-  // in registers; for d_k = 128, warps 4..7 keep rows 64..127.  The output
-  // epilogue runs on the warps that hold no second S half.
+  // Thread roles on the M = 64 accumulators: row r = 16 * quadrant + lane % 16
+  // lives in lanes 0..15 of each TMEM quadrant; the half-warps read its
+  // columns 0..31 and 32..63 (hf = lane / 16), so every thread owns half a
+  // row.  Warps 0..3 keep S rows 0..63 (that half) in registers and write the
+  // outputs; warps 4..7 keep rows 64..127 and form Delta.
+  static_assert(DK == 128 && NV == 64, "d_k = 128, 64-channel value slices");
   const int quad = warp & 3;
-  const bool row64 = lane < 16;
-  const int r64 = 16 * quad + lane;
+  const int hf = lane >> 4;
+  const int r64 = 16 * quad + (lane & 15);
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
   const bool lo = warp < 4;
-  const bool s_warp = lo || DK == 128;
   const int s_row = lo ? r64 : 64 + r64;
-  const bool o_warp = (DK == 64) ? !lo : lo;
   const uint32_t col_d2 = L::COL_W + (lo ? 0 : 64);
+  // 32 fp32 values as bf16 into columns 32 hf .. 32 hf + 31 of a swizzled row
+  auto store_half = [&](uint8_t* tile, int row, const float* v) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+      *reinterpret_cast<uint4*>(tile + sw128(row, 32 * hf + 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  };
+  auto ld_half = [&](uint32_t col, float* v) {  // this thread's row, its 32 columns from col
+    uint32_t r32[32];
+    tmem_ld16x2_32(tmem + lane_off + col, r32);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r32[i]);
+  };
 
-  float sreg[NV];
+  float sreg[32];
 #pragma unroll
-  for (int n = 0; n < NV; ++n) sreg[n] = 0.f;
-  if (s_warp && row64 && a.S_in) {
+  for (int n = 0; n < 32; ++n) sreg[n] = 0.f;
+  if (a.S_in) {
     const size_t dv = (size_t)gridDim.y * NV;
-    const float* src = a.S_in + ((size_t)bh * DK + s_row) * dv + c0;
+    const float* src = a.S_in + ((size_t)bh * DK + s_row) * dv + c0 + 32 * hf;
 #pragma unroll
-    for (int n = 0; n < NV; ++n) sreg[n] = src[n];
+    for (int n = 0; n < 32; ++n) sreg[n] = src[n];
   }
-  if (s_warp && row64) store_row64(SB, s_row, sreg);
+  store_half(SB, s_row, sreg);
   fence_proxy_async();
   __syncthreads();
 
@@ -639,38 +656,35 @@ __global__ void __launch_bounds__(256, 1)
     }
     mph ^= 1;
     tc_fence_after();
-    if (lo) {  // P~ = decay-masked P
-      float pv[64];
-      tmem_ld64(tmem + lane_off + L::COL_P, pv);
-      tmem_wait_ld();
-      if (row64) {
-        const float gr = gl[r64];
+    if (lo) {  // P~ = decay-masked P, columns 32 hf .. 32 hf + 31 of row r64
+      float pv[32];
+      ld_half(L::COL_P, pv);
+      const float gr = gl[r64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) pv[i] = (i <= r64) ? __expf(gr - gl[i]) * pv[i] : 0.f;
-        store_row64(Pm, r64, pv);
+      for (int i = 0; i < 32; ++i) {
+        const int t = 32 * hf + i;
+        pv[i] = (t <= r64) ? __expf(gr - gl[t]) * pv[i] : 0.f;
       }
+      store_half(Pm, r64, pv);
     } else if (SOLVE) {  // Delta = U - W S0, and diag(exp(g_last - g)) Delta
-      float dv1[64];
-      tmem_ld64(tmem + lane_off + L::COL_D1, dv1);
-      tmem_wait_ld();
-      if (row64) {
+      float dv1[32];
+      ld_half(L::COL_D1, dv1);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(Ust(s) + sw128(r64, 8 * j));
-          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      for (int j = 0; j < 4; ++j) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(Ust(s) + sw128(r64, 32 * hf + 8 * j));
+        const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 u2 = __bfloat1622float2(pu[e]);
-            dv1[8 * j + 2 * e] = u2.x - dv1[8 * j + 2 * e];
-            dv1[8 * j + 2 * e + 1] = u2.y - dv1[8 * j + 2 * e + 1];
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float2 u2 = __bfloat1622float2(pu[e]);
+          dv1[8 * j + 2 * e] = u2.x - dv1[8 * j + 2 * e];
+          dv1[8 * j + 2 * e + 1] = u2.y - dv1[8 * j + 2 * e + 1];
         }
-        store_row64(sm + L::DL, r64, dv1);
-        const float dr = dec[r64];
-#pragma unroll
-        for (int n = 0; n < NV; ++n) dv1[n] *= dr;
-        store_row64(DD, r64, dv1);
       }
+      store_half(sm + L::DL, r64, dv1);
+      const float dr = dec[r64];
+#pragma unroll
+      for (int n = 0; n < 32; ++n) dv1[n] *= dr;
+      store_half(DD, r64, dv1);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -695,39 +709,21 @@ __global__ void __launch_bounds__(256, 1)
     }
     mph ^= 1;
     tc_fence_after();
-    if (s_warp) {  // S1 = Gamma_last S0 + D2
-      float d2[64];
-      tmem_ld64(tmem + lane_off + col_d2, d2);
-      tmem_wait_ld();
-      if (row64) {
+    {  // S1 = Gamma_last S0 + D2 (every warp holds half rows of S)
+      float d2[32];
+      ld_half(col_d2, d2);
 #pragma unroll
-        for (int n = 0; n < NV; ++n) sreg[n] = gam_last * sreg[n] + d2[n];
-        store_row64(SB, s_row, sreg);
-      }
+      for (int n = 0; n < 32; ++n) sreg[n] = gam_last * sreg[n] + d2[n];
+      store_half(SB, s_row, sreg);
     }
-    if (o_warp) {  // O = diag(Gamma) Oa + Ob, in two 32-column halves
+    if (lo) {  // O = diag(Gamma) Oa + Ob, this thread's 32 columns
+      float oa[32], ob[32];
+      ld_half(L::COL_OA, oa);
+      ld_half(L::COL_P, ob);
       const float gr = Gam[r64];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t oa[32], ob[32];
-        tmem_ld32(tmem + lane_off + L::COL_OA + 32 * hf, oa);
-        tmem_ld32(tmem + lane_off + L::COL_P + 32 * hf, ob);
-        tmem_wait_ld();
-        if (row64) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int n = 8 * j + 2 * e;
-              pk[e] = pack_bf16(gr * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
-                                gr * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
-            }
-            *reinterpret_cast<uint4*>(Ost + sw128(r64, 32 * hf + 8 * j)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-        }
-      }
+      for (int n = 0; n < 32; ++n) oa[n] = gr * oa[n] + ob[n];
+      store_half(Ost, r64, oa);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -741,11 +737,11 @@ __global__ void __launch_bounds__(256, 1)
   if (tid == 0) bulk_wait0();
   // ---- carry out
   if (!*abort_flag) {
-    if (s_warp && row64 && a.S_out) {
+    if (a.S_out) {
       const size_t dv = (size_t)gridDim.y * NV;
-      float* dst = a.S_out + ((size_t)bh * DK + s_row) * dv + c0;
+      float* dst = a.S_out + ((size_t)bh * DK + s_row) * dv + c0 + 32 * hf;
 #pragma unroll
-      for (int n = 0; n < NV; ++n) dst[n] = sreg[n];
+      for (int n = 0; n < 32; ++n) dst[n] = sreg[n];
     }
     if (split == 0) {
       if (a.kprev_out)
