@@ -476,7 +476,7 @@ struct FwdSmem {
 };
 
 template <int DK, int NV, bool SOLVE>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(288, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_o, TcArgs a) {
   using L = FwdSmem<DK, NV, SOLVE>;
@@ -491,7 +491,8 @@ __global__ void __launch_bounds__(256, 1)
   float* dec = Gam + 64;
   float* gl = dec + 64;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  uint64_t* mbar = full + 2;
+  uint64_t* mbar = full + 2;   // D1 (then the second product group) done
+  uint64_t* mbar_p = full + 3; // P done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -528,6 +529,7 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
     mbar_init(mbar, 1);
+    mbar_init(mbar_p, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -538,8 +540,11 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  int issued[2] = {0, 0};  // loads issued per stage (thread 0's bookkeeping)
-  if (tid == 0 && NC > 0) {
+  // warp 8, lane 0 (tid 256) issues every load and product; warps 0..7 do
+  // the epilogues and hold the state
+  const bool issuer = tid == 256;
+  int issued[2] = {0, 0};  // loads issued per stage (the issuer's bookkeeping)
+  if (issuer && NC > 0) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the per-chunk kernel's images and gates
     asm volatile("fence.proxy.async.global;" ::: "memory");
     issue_stage(0, 0);
@@ -556,7 +561,7 @@ __global__ void __launch_bounds__(256, 1)
   const int hf = lane >> 4;
   const int r64 = 16 * quad + (lane & 15);
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-  const bool lo = warp < 4;
+  const bool lo = warp < 4, hi = warp >= 4 && warp < 8;
   const int s_row = lo ? r64 : 64 + r64;
   const uint32_t col_d2 = L::COL_W + (lo ? 0 : 64);
   // 32 fp32 values as bf16 into columns 32 hf .. 32 hf + 31 of a swizzled row
@@ -580,22 +585,22 @@ __global__ void __launch_bounds__(256, 1)
   float sreg[32];
 #pragma unroll
   for (int n = 0; n < 32; ++n) sreg[n] = 0.f;
-  if (a.S_in) {
+  if (a.S_in && warp < 8) {
     const size_t dv = (size_t)gridDim.y * NV;
     const float* src = a.S_in + ((size_t)bh * DK + s_row) * dv + c0 + 32 * hf;
 #pragma unroll
     for (int n = 0; n < 32; ++n) sreg[n] = src[n];
   }
-  store_half(SB, s_row, sreg);
+  if (warp < 8) store_half(SB, s_row, sreg);
   fence_proxy_async();
   __syncthreads();
 
   const uint32_t sP = smem_u32(Pm), sS = smem_u32(SB), sDD = smem_u32(DD);
-  uint32_t mph = 0;
+  uint32_t mph = 0, pph = 0;
   for (int c = 0; c < NC; ++c) {
     const int s = c & 1;
     const int t0 = c * kC;
-    if (tid == 0 && c + 1 < NC) {
+    if (issuer && c + 1 < NC) {
       issue_stage(c + 1, s ^ 1);
       ++issued[s ^ 1];
     }
@@ -604,7 +609,7 @@ __global__ void __launch_bounds__(256, 1)
       atomicExch(a.status, kStatusTimeout);
     }
     if (c == 0 && a.kprev_in && a.shift) {  // x_0 = carried key
-      for (int i = tid; i < DK; i += 256)
+      for (int i = tid; i < DK; i += 288)
         *reinterpret_cast<__nv_bfloat16*>(Xst(0) + (i >> 6) * 8192 + sw128(0, i & 63)) =
             a.kprev_in[(size_t)bh * DK + i];
     }
@@ -620,7 +625,7 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(Ust(s));
 
     if (!SOLVE) {  // diag(exp(g_last - g)) U (16-byte chunks)
-      for (int idx = tid; idx < 512; idx += 256) {
+      for (int idx = tid; idx < 512; idx += 288) {
         const int R = idx >> 3;
         const uint4 in = *reinterpret_cast<const uint4*>(Ust(s) + idx * 16);
         const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
@@ -639,21 +644,24 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     tc_fence_after();
 
-    // ---- P = Q X^T, D1 = W S0, Oa = Q S0 (W and U come from the per-chunk kernel)
-    if (tid == 0) {
+    // ---- P = Q X^T (committed alone: the P~ warps start on it), D1 = W S0,
+    // then Oa = Q S0 (read only after the second group, whose commit covers it)
+    if (issuer) {
       const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s));
       mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, DK, idesc_bf16(64, 64), false);
+      umma_commit(mbar_p);
       if (SOLVE)
         mma_chain_mn(tmem + L::COL_D1, kdesc<64>, smem_u32(Wst(s)), mndesc, sS, DK,
                      idesc_bf16(64, NV, false, true), false);
+      umma_commit(mbar);
       mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
                    false);
-      umma_commit(mbar);
     }
-    if (!mbar_wait(mbar, mph)) {
+    if ((lo && !mbar_wait(mbar_p, pph)) || (hi && SOLVE && !mbar_wait(mbar, mph))) {
       *abort_flag = 1;
       atomicExch(a.status, kStatusTimeout);
     }
+    pph ^= 1;
     mph ^= 1;
     tc_fence_after();
     if (lo) {  // P~ = decay-masked P, columns 32 hf .. 32 hf + 31 of row r64
@@ -666,7 +674,7 @@ __global__ void __launch_bounds__(256, 1)
         pv[i] = (t <= r64) ? __expf(gr - gl[t]) * pv[i] : 0.f;
       }
       store_half(Pm, r64, pv);
-    } else if (SOLVE) {  // Delta = U - W S0, and diag(exp(g_last - g)) Delta
+    } else if (hi && SOLVE) {  // Delta = U - W S0, and diag(exp(g_last - g)) Delta
       float dv1[32];
       ld_half(L::COL_D1, dv1);
 #pragma unroll
@@ -694,7 +702,7 @@ __global__ void __launch_bounds__(256, 1)
     if (ab2) break;
 
     // ---- D2 = X^T diag(exp(g_last - g)) Delta, Ob = P~ Delta
-    if (tid == 0) {
+    if (issuer) {
       const uint32_t sX = smem_u32(Xst(s));
       for (int k = 0; k < L::kKS; ++k)
         mma_chain_mn(tmem + L::COL_W + 64 * k, mndesc, sX + k * 8192, mndesc, sDD, 64,
@@ -703,13 +711,13 @@ __global__ void __launch_bounds__(256, 1)
                    false);
       umma_commit(mbar);
     }
-    if (!mbar_wait(mbar, mph)) {
+    if (warp < 8 && !mbar_wait(mbar, mph)) {
       *abort_flag = 1;
       atomicExch(a.status, kStatusTimeout);
     }
     mph ^= 1;
     tc_fence_after();
-    {  // S1 = Gamma_last S0 + D2 (every warp holds half rows of S)
+    if (warp < 8) {  // S1 = Gamma_last S0 + D2 (warps 0..7 hold half rows of S)
       float d2[32];
       ld_half(col_d2, d2);
 #pragma unroll
@@ -737,7 +745,7 @@ __global__ void __launch_bounds__(256, 1)
   if (tid == 0) bulk_wait0();
   // ---- carry out
   if (!*abort_flag) {
-    if (a.S_out) {
+    if (a.S_out && warp < 8) {
       const size_t dv = (size_t)gridDim.y * NV;
       float* dst = a.S_out + ((size_t)bh * DK + s_row) * dv + c0 + 32 * hf;
 #pragma unroll
@@ -745,11 +753,11 @@ __global__ void __launch_bounds__(256, 1)
     }
     if (split == 0) {
       if (a.kprev_out)
-        for (int i = tid; i < DK; i += 256)
+        for (int i = tid; i < DK; i += 288)
           a.kprev_out[(size_t)bh * DK + i] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * DK + i];
       if (a.pos_out && tid == 0) a.pos_out[bh] = (a.pos_in ? a.pos_in[bh] : 0) + a.T;
     }
-  } else if (tid == 0) {
+  } else if (issuer) {
     // drain the loads still in flight before the shared memory goes away
     for (int s = 0; s < 2; ++s)
       if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1));
@@ -1246,7 +1254,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
       dim3 grid(BH, fa.dv / NV);
-      if (launch_overlapped(fa, k, grid, dim3(256), smem, mq, mk, mo, ta) != FALCON_OK) return FALCON_ERR_CUDA;
+      if (launch_overlapped(fa, k, grid, dim3(288), smem, mq, mk, mo, ta) != FALCON_OK) return FALCON_ERR_CUDA;
       record_event(fa, 2);
     }
   }
