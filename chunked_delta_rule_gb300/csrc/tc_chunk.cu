@@ -470,7 +470,10 @@ struct FwdSmem {
   // TMEM columns: P and later P~ Delta share one block; X~^T Delta (DK rows as
   // DK / 64 blocks of 64), W S0 and Q S0 one block each
   static constexpr uint32_t COL_P = 0, COL_W = 64, COL_D1 = COL_W + DK, COL_OA = COL_D1 + NV,
-                            NCOL = COL_OA + NV;
+                            COL_P2 = COL_OA + NV, NCOL = COL_P2 + 64;
+  // P (then P~ Delta) of chunk c in buffer c % 2: the next chunk's P is
+  // issued while this chunk's epilogues run
+  __host__ __device__ static constexpr uint32_t col_p(int c) { return (c & 1) ? COL_P2 : COL_P; }
   static_assert(NCOL <= 512, "TMEM budget");
   static_assert(NV == 64, "value slice of 64 channels");
 };
@@ -597,6 +600,7 @@ __global__ void __launch_bounds__(288, 1)
 
   const uint32_t sP = smem_u32(Pm), sS = smem_u32(SB), sDD = smem_u32(DD);
   uint32_t mph = 0, pph = 0;
+  int n_pc = 0, n_mc = 0;  // the issuer's commits on mbar_p and mbar
   for (int c = 0; c < NC; ++c) {
     const int s = c & 1;
     const int t0 = c * kC;
@@ -648,12 +652,16 @@ __global__ void __launch_bounds__(288, 1)
     // then Oa = Q S0 (read only after the second group, whose commit covers it)
     if (issuer) {
       const uint32_t sQ = smem_u32(Qst(s)), sX = smem_u32(Xst(s));
-      mma_chain_mn(tmem + L::COL_P, kdesc<64>, sQ, kdesc<64>, sX, DK, idesc_bf16(64, 64), false);
-      umma_commit(mbar_p);
+      if (c == 0) {  // later chunks' P was issued during the chunk before
+        mma_chain_mn(tmem + L::col_p(c), kdesc<64>, sQ, kdesc<64>, sX, DK, idesc_bf16(64, 64), false);
+        umma_commit(mbar_p);
+        ++n_pc;
+      }
       if (SOLVE)
         mma_chain_mn(tmem + L::COL_D1, kdesc<64>, smem_u32(Wst(s)), mndesc, sS, DK,
                      idesc_bf16(64, NV, false, true), false);
       umma_commit(mbar);
+      ++n_mc;
       mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
                    false);
     }
@@ -666,7 +674,7 @@ __global__ void __launch_bounds__(288, 1)
     tc_fence_after();
     if (lo) {  // P~ = decay-masked P, columns 32 hf .. 32 hf + 31 of row r64
       float pv[32];
-      ld_half(L::COL_P, pv);
+      ld_half(L::col_p(c), pv);
       const float gr = gl[r64];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -707,9 +715,22 @@ __global__ void __launch_bounds__(288, 1)
       for (int k = 0; k < L::kKS; ++k)
         mma_chain_mn(tmem + L::COL_W + 64 * k, mndesc, sX + k * 8192, mndesc, sDD, 64,
                      idesc_bf16(64, NV, true, true), false);
-      mma_chain_mn(tmem + L::COL_P, kdesc<64>, sP, mndesc, sDL, 64, idesc_bf16(64, NV, false, true),
+      mma_chain_mn(tmem + L::col_p(c), kdesc<64>, sP, mndesc, sDL, 64, idesc_bf16(64, NV, false, true),
                    false);
       umma_commit(mbar);
+      ++n_mc;
+      if (c + 1 < NC) {  // the next chunk's P = Q X^T: its stage is loaded, its buffer free
+        if (!mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1))) {
+          *abort_flag = 1;
+          atomicExch(a.status, kStatusTimeout);
+        } else {
+          tc_fence_after();
+          mma_chain_mn(tmem + L::col_p(c + 1), kdesc<64>, smem_u32(Qst(s ^ 1)), kdesc<64>,
+                       smem_u32(Xst(s ^ 1)), DK, idesc_bf16(64, 64), false);
+          umma_commit(mbar_p);
+          ++n_pc;
+        }
+      }
     }
     if (warp < 8 && !mbar_wait(mbar, mph)) {
       *abort_flag = 1;
@@ -727,7 +748,7 @@ __global__ void __launch_bounds__(288, 1)
     if (lo) {  // O = diag(Gamma) Oa + Ob, this thread's 32 columns
       float oa[32], ob[32];
       ld_half(L::COL_OA, oa);
-      ld_half(L::COL_P, ob);
+      ld_half(L::col_p(c), ob);
       const float gr = Gam[r64];
 #pragma unroll
       for (int n = 0; n < 32; ++n) oa[n] = gr * oa[n] + ob[n];
@@ -761,6 +782,10 @@ __global__ void __launch_bounds__(288, 1)
     // drain the loads still in flight before the shared memory goes away
     for (int s = 0; s < 2; ++s)
       if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1));
+  }
+  if (issuer) {  // no product may still write TMEM when it is freed (the abort path)
+    if (n_pc > 0) mbar_wait(mbar_p, (uint32_t)((n_pc - 1) & 1));
+    if (n_mc > 0) mbar_wait(mbar, (uint32_t)((n_mc - 1) & 1));
   }
   tc_fence_before();
   __syncthreads();
