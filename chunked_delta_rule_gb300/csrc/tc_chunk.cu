@@ -554,29 +554,33 @@ __global__ void __launch_bounds__(288, 1)
     issued[0] = 1;
   }
 
-  // Thread roles on the M = 64 accumulators: row r = 16 * quadrant + lane % 16
-  // lives in lanes 0..15 of each TMEM quadrant; the half-warps read its
-  // columns 0..31 and 32..63 (hf = lane / 16), so every thread owns half a
-  // row.  Warps 0..3 keep S rows 0..63 (that half) in registers and write the
-  // outputs; warps 4..7 keep rows 64..127 and form Delta.
+  // Thread roles on the M = 64 accumulators (P, W S0, Q S0, P~ Delta): row
+  // r = 16 * quadrant + lane % 16 lives in lanes 0..15 of each TMEM quadrant;
+  // the half-warps read its columns 0..31 and 32..63 (hf = lane / 16), so
+  // every thread owns half a row.  Warps 0..3 form P~ and write the outputs,
+  // warps 4..7 form Delta.
   static_assert(DK == 128 && NV == 64, "d_k = 128, 64-channel value slices");
   const int quad = warp & 3;
   const int hf = lane >> 4;
   const int r64 = 16 * quad + (lane & 15);
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
   const bool lo = warp < 4, hi = warp >= 4 && warp < 8;
-  const int s_row = lo ? r64 : 64 + r64;
-  const uint32_t col_d2 = L::COL_W + (lo ? 0 : 64);
-  // 32 fp32 values as bf16 into columns 32 hf .. 32 hf + 31 of a swizzled row
-  auto store_half = [&](uint8_t* tile, int row, const float* v) {
+  // The state update D2 is an M = 128 product (S row r in TMEM lane r):
+  // warps w and w + 4 share quadrant w % 4, rows 32 (w % 4) + lane, columns
+  // 0..31 and 32..63 of them; sreg holds those 32 values of S.
+  const int s_row = 32 * quad + lane;
+  const int s_c0 = (warp >= 4) ? 32 : 0;
+  // 32 fp32 values as bf16 into columns col0 .. col0 + 31 of a swizzled row
+  auto store_32 = [&](uint8_t* tile, int row, int col0, const float* v) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t pk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
-      *reinterpret_cast<uint4*>(tile + sw128(row, 32 * hf + 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(tile + sw128(row, col0 + 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   };
+  auto store_half = [&](uint8_t* tile, int row, const float* v) { store_32(tile, row, 32 * hf, v); };
   auto ld_half = [&](uint32_t col, float* v) {  // this thread's row, its 32 columns from col
     uint32_t r32[32];
     tmem_ld16x2_32(tmem + lane_off + col, r32);
@@ -590,11 +594,11 @@ __global__ void __launch_bounds__(288, 1)
   for (int n = 0; n < 32; ++n) sreg[n] = 0.f;
   if (a.S_in && warp < 8) {
     const size_t dv = (size_t)gridDim.y * NV;
-    const float* src = a.S_in + ((size_t)bh * DK + s_row) * dv + c0 + 32 * hf;
+    const float* src = a.S_in + ((size_t)bh * DK + s_row) * dv + c0 + s_c0;
 #pragma unroll
     for (int n = 0; n < 32; ++n) sreg[n] = src[n];
   }
-  if (warp < 8) store_half(SB, s_row, sreg);
+  if (warp < 8) store_32(SB, s_row, s_c0, sreg);
   fence_proxy_async();
   __syncthreads();
 
@@ -712,9 +716,9 @@ __global__ void __launch_bounds__(288, 1)
     // ---- D2 = X^T diag(exp(g_last - g)) Delta, Ob = P~ Delta
     if (issuer) {
       const uint32_t sX = smem_u32(Xst(s));
-      for (int k = 0; k < L::kKS; ++k)
-        mma_chain_mn(tmem + L::COL_W + 64 * k, mndesc, sX + k * 8192, mndesc, sDD, 64,
-                     idesc_bf16(64, NV, true, true), false);
+      for (int ks = 0; ks < 4; ++ks)  // X^T over both 64-row atoms of d_k: one M = 128 product
+        umma_bf16(tmem + L::COL_W, sdesc_mn128_wide(sX + ks * 2048, 8192), mndesc(sDD, ks),
+                  idesc_bf16(128, NV, true, true), ks > 0 ? 1u : 0u);
       mma_chain_mn(tmem + L::col_p(c), kdesc<64>, sP, mndesc, sDL, 64, idesc_bf16(64, NV, false, true),
                    false);
       umma_commit(mbar);
@@ -738,12 +742,18 @@ __global__ void __launch_bounds__(288, 1)
     }
     mph ^= 1;
     tc_fence_after();
-    if (warp < 8) {  // S1 = Gamma_last S0 + D2 (warps 0..7 hold half rows of S)
+    if (warp < 8) {  // S1 = Gamma_last S0 + D2
       float d2[32];
-      ld_half(col_d2, d2);
+      {
+        uint32_t r32[32];
+        tmem_ld32(tmem + lane_off + L::COL_W + s_c0, r32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) d2[i] = __uint_as_float(r32[i]);
+      }
 #pragma unroll
       for (int n = 0; n < 32; ++n) sreg[n] = gam_last * sreg[n] + d2[n];
-      store_half(SB, s_row, sreg);
+      store_32(SB, s_row, s_c0, sreg);
     }
     if (lo) {  // O = diag(Gamma) Oa + Ob, this thread's 32 columns
       float oa[32], ob[32];
@@ -768,7 +778,7 @@ __global__ void __launch_bounds__(288, 1)
   if (!*abort_flag) {
     if (a.S_out && warp < 8) {
       const size_t dv = (size_t)gridDim.y * NV;
-      float* dst = a.S_out + ((size_t)bh * DK + s_row) * dv + c0 + 32 * hf;
+      float* dst = a.S_out + ((size_t)bh * DK + s_row) * dv + c0 + s_c0;
 #pragma unroll
       for (int n = 0; n < 32; ++n) dst[n] = sreg[n];
     }
