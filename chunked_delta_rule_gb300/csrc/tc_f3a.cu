@@ -17,9 +17,10 @@
 //
 // One CTA per (b, h), warp-specialised like the Falcon-1 sequential kernel:
 //   warp 8      producer: TMA of the 80 key rows, 80 value rows and 64 query rows
-//   warps 4..7  front (up to NST chunks ahead): window statistics, P^T = X Q^T
-//               (keys in TMEM lanes), M' by the recurrence along t, P~^T and
-//               X~ = diag(m) X in place
+//   warps 4..7  front, even chunks, and warps 9..12 front, odd chunks (each up
+//               to NST chunks ahead of the back): window statistics, P^T = X Q^T
+//               (keys in TMEM lanes; one TMEM block per front), M' by the
+//               recurrence along t, P~^T and X~ = diag(m) X in place
 //   warps 0..3  back: [0 ; Oa] = [0 ; Q] S0 and [D2 ; Ob] = [X~ | P~^T]^T V in one
 //               go, S1 = Gamma_last S0 + D2, O = diag(Gamma) Oa + Ob
 // Every wait is bounded; on timeout the kernel records an error in the
@@ -76,8 +77,10 @@ struct F3aSmem {
   // gates (fp32 offsets in GO): key energy, key existence, c, gamma, Gamma, g, warp sums
   static constexpr int G_NRM = 0, G_EX = 80, G_C = 160, G_GMA = 224, G_GAM = 288, G_G = 352, G_WS = 416;
   static_assert(GO + (G_WS + 2) * 4 <= STAGE, "gates fit the stage");
-  // TMEM: P^T (keys in lanes) | [0 ; Oa] | [D2 ; Ob]
-  static constexpr uint32_t COL_PT = 0, COL_B1 = 64, COL_B2 = 128, NCOLS = 256;
+  // TMEM: P^T of the even-chunk front (keys in lanes) | [0 ; Oa] | [D2 ; Ob] |
+  // P^T of the odd-chunk front
+  static constexpr uint32_t COL_PT = 0, COL_B1 = 64, COL_B2 = 128, COL_PT1 = 192, NCOLS = 256;
+  static constexpr int kThreads = 416;  // 13 warps
 };
 
 // Key (x) and value of local pair j of (b, h): j >= 1 from the sequence,
@@ -96,7 +99,7 @@ __device__ __forceinline__ __nv_bfloat16 pair_v(const F3aArgs& a, int b, int h, 
   return a.winv_in[(((size_t)b * a.H + h) * Wr + ring_slot(pos + j, Wr)) * 64 + col];
 }
 
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(F3aSmem::kThreads, 1)
     tc_f3a_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k80,
                   const __grid_constant__ CUtensorMap tm_v80, const __grid_constant__ CUtensorMap tm_o,
                   F3aArgs a) {
@@ -108,8 +111,8 @@ __global__ void __launch_bounds__(288, 1)
   uint64_t* full = bars;              // [NST]
   uint64_t* empty = bars + NST;       // [NST]
   uint64_t* fdone = bars + 2 * NST;   // [NST]
-  uint64_t* fmma = bars + 3 * NST;    // P^T done
-  uint64_t* bmma = fmma + 1;          // both back products done
+  uint64_t* fmma = bars + 3 * NST;    // [2]: P^T of front 0 / 1 done
+  uint64_t* bmma = fmma + 2;          // both back products done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -130,11 +133,12 @@ __global__ void __launch_bounds__(288, 1)
       mbar_init(&empty[i], 1);
       mbar_init(&fdone[i], 128);
     }
-    mbar_init(fmma, 1);
+    mbar_init(&fmma[0], 1);
+    mbar_init(&fmma[1], 1);
     mbar_init(bmma, 1);
     fence_mbar_init();
   }
-  for (int i = tid; i < NST * 512; i += 288)  // the zero rows of [0 ; Q]
+  for (int i = tid; i < NST * 512; i += L::kThreads)  // the zero rows of [0 ; Q]
     *reinterpret_cast<uint4*>(stage(i >> 9) + L::ZO + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
     tmem_alloc(tmem_slot, L::NCOLS);
@@ -171,7 +175,12 @@ __global__ void __launch_bounds__(288, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ front
-    const int ftid = tid - 128;
+    // fg = 0: warps 4..7, chunks 0, 2, 4, ...; fg = 1: warps 9..12, chunks 1, 3, ...
+    const int fg = warp >= 9 ? 1 : 0;
+    const int ftid = tid - (fg ? 288 : 128);
+    const int fbar = fg ? 5 : 1;  // named barrier of this front
+    const uint32_t col_pt = fg ? L::COL_PT1 : L::COL_PT;
+    uint64_t* fm = &fmma[fg];
     uint32_t fph = 0;
     // gate inputs of step c * 64 + ftid, loaded one chunk ahead
     auto gate_in = [&](int c, float& lam, float& beta) {
@@ -182,13 +191,13 @@ __global__ void __launch_bounds__(288, 1)
       beta = ok ? a.beta[gi] : 0.f;
     };
     float lam_n, beta_n;
-    gate_in(0, lam_n, beta_n);
-    for (int c = 0; c < NC; ++c) {
+    gate_in(fg, lam_n, beta_n);
+    for (int c = fg; c < NC; c += 2) {
       const int s = c % NST;
       const int t0 = c * kC, j0 = t0 - W + 1;
       const bool step_ok = ftid < 64 && t0 + ftid < a.T;
       const float lam_c = lam_n, beta = beta_n;
-      gate_in(c + 1, lam_n, beta_n);
+      gate_in(c + 2, lam_n, beta_n);
       const float ell = step_ok ? clamped_log_decay(lam_c, a.eps_gamma) : 0.f;
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
       uint8_t* st = stage(s);
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(288, 1)
           }
         }
       }
-      named_bar(1, 128);
+      named_bar(fbar, 128);
       if (ftid < kKeys) {  // key energy and existence of pair j0 + kappa
         const int j = j0 + ftid;
         float n = 0.f;
@@ -228,11 +237,11 @@ __global__ void __launch_bounds__(288, 1)
           const float n = __shfl_up_sync(0xffffffffu, g, o);
           if (lane >= o) g += n;
         }
-        if (lane == 31) gt[L::G_WS + (warp - 4)] = g;
+        if (lane == 31) gt[L::G_WS + (ftid >> 5)] = g;
       }
-      named_bar(1, 128);
+      named_bar(fbar, 128);
       if (ftid < 64) {  // step t = ftid: window statistics and decays
-        if (warp == 5) g += gt[L::G_WS];
+        if ((ftid >> 5) == 1) g += gt[L::G_WS];
         float n = 0.f, e = 0.f;
         for (int q = 0; q < W; ++q) {
           const float ex = gt[L::G_EX + ftid + q];
@@ -247,22 +256,22 @@ __global__ void __launch_bounds__(288, 1)
       }
       fence_proxy_async();
       tc_fence_before();
-      if (named_bar_any(1, 128, *abort_flag != 0)) break;
+      if (named_bar_any(fbar, 128, *abort_flag != 0)) break;
       tc_fence_after();
       if (ftid == 0) {  // P^T = X Q^T over 128 A rows (rows >= 80 are not read back)
         const uint32_t sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + L::COL_PT, kdesc<128>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(128, 64),
+          umma_bf16(tmem + col_pt, kdesc<128>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(128, 64),
                     ks > 0 ? 1u : 0u);
-        umma_commit(fmma);
+        umma_commit(fm);
       }
-      if (!mbar_wait(fmma, fph)) fail();
+      if (!mbar_wait(fm, fph)) fail();
       fph ^= 1;
       tc_fence_after();
       if (quad < 3) {  // keys kappa = 32 quad + lane < 80
         const int kap = 32 * quad + lane;
         float pv[64];
-        tmem_ld64(tmem + lane_off + L::COL_PT, pv);
+        tmem_ld64(tmem + lane_off + col_pt, pv);
         tmem_wait_ld();
         if (kap < kKeys) {
           const float* cs = gt + L::G_C;
@@ -296,7 +305,7 @@ __global__ void __launch_bounds__(288, 1)
       tc_fence_before();
       mbar_arrive(&fdone[s]);
     }
-    if (!*abort_flag) {  // carry: last key, the last W - 1 pairs, position
+    if (!*abort_flag && fg == 0) {  // carry: last key, the last W - 1 pairs, position
       if (a.kprev_out && ftid < 64)
         a.kprev_out[(size_t)bh * 64 + ftid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + ftid];
       const int Wr = W - 1;
@@ -452,7 +461,7 @@ int launch_tc_f3a(const FwdArgs& fa) {
   const size_t smem = F3aSmem::TOTAL;
   if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
   record_event(fa, 0);
-  k<<<fa.B * fa.H, 288, smem, fa.stream>>>(mq, mk, mv, mo, ta);
+  k<<<fa.B * fa.H, F3aSmem::kThreads, smem, fa.stream>>>(mq, mk, mv, mo, ta);
   record_event(fa, 1);
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
