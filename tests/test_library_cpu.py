@@ -181,3 +181,16 @@ def test_prologue_and_varlen_sizes_and_flags(F):
     with pytest.raises(F.FalconError) as e:  # workspace too small
         F.falcon_chunk_fwd_varlen(p, fake, 10, fake, fake, fake, fake, fake, None, fake, None, 1 << 24, 16, 0)
     assert e.value.code == -3
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_tc_workspace_layout(F, d):
+    """Tensor-core forward workspace: a 256-byte status word, then per chunk
+    the bf16 W | U images (2 d x 128 bytes) and a 1 KB gate slot, rounded up
+    to 256 bytes (the layout the per-chunk and sequential kernels share)."""
+    B, T, H = 2, 130, 3
+    p = _p(F, B=B, T=T, H=H, dk=d, dv=d, impl=F.FALCON_IMPL_TC)
+    nc = (T + 63) // 64
+    want = 256 + B * H * nc * (2 * d * 128) + B * H * nc * 1024
+    want = (want + 255) // 256 * 256
+    assert F.falcon_workspace_size(p) == want
