@@ -630,7 +630,7 @@ def main():
         else:
             names = ["tc_wyu_kernel", "tc_fwd_kernel"]
         kbytes = kernel_bytes(w, names)
-        if args.prologue:  # the gather pass: q, k, v and gates in, the same out
+        if args.prologue and launches > len(names):  # the gather pass: q, k, v and gates in, the same out
             es = 2 if w.dtype == "bf16" else 4
             th = w.B * w.T * w.H
             pb = 2 * (th * (2 * w.dk + w.dv) * es + th * ((w.dv if w.per_channel else 1) + 1) * 4)

@@ -125,6 +125,21 @@ size_t falcon_varlen_workspace_size(const falcon_params_t* p) {
   return kernel_ws_bytes(p) + prologue_bytes(p, true);
 }
 
+// The prologue runs inside the kernels on the pipelined d = 64 tensor-core
+// path (Falcon-1 / 1A): the per-chunk kernel normalises its key rows and
+// forms the gates from logits, the sequential kernel scales its products by
+// the rows' inverse norms.  Every other path, and rows off a 16-byte
+// boundary (which the tensor maps cannot take; pass null pointers to ask
+// about the plan alone), take it from a gather pass.
+static bool prologue_fused(const falcon_params_t* p, const void* q = nullptr, const void* k = nullptr,
+                           const void* v = nullptr) {
+  if (!p->prologue || p->dk != 64 || (p->variant != FALCON_1 && p->variant != FALCON_1A)) return false;
+  for (const void* x : {q, k, v})
+    if (reinterpret_cast<uintptr_t>(x) & 15) return false;
+  return pick_impl(p, make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr)) ==
+         FALCON_IMPL_TC;
+}
+
 static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k, const void* v,
                           const float* beta, const float* lambda, const falcon_carry_t* carry_in,
                           void* o, falcon_carry_t* carry_out, void* workspace,
@@ -132,7 +147,7 @@ static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k
   int st = check_params(p, false);
   if (st != FALCON_OK) return st;
   if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !o)) return FALCON_ERR_INVALID_ARG;
-  if (p->prologue) {  // phi / gate logits: one pass into the workspace, then the features path
+  if (p->prologue && !prologue_fused(p, q, k, v)) {  // phi / gate logits: one pass into the workspace, then the features path
     if (pick_impl(p, make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr)) < 0)
       return FALCON_ERR_UNSUPPORTED;
     const size_t kws = kernel_ws_bytes(p);
@@ -151,6 +166,7 @@ static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k
                           events ? n_events - 1 : 0);
   }
   FwdArgs a = make_args(p, q, k, v, beta, lambda, o, stream);
+  a.prologue = p->prologue;  // nonzero here only on the fused path
   const size_t es = elem_size(p->dtype);
   const size_t BH = (size_t)p->B * p->H;
   const int Wr = a.W - 1;
@@ -231,7 +247,7 @@ int falcon_chunk_fwd_plan(const falcon_params_t* p, int32_t* impl_out, int32_t* 
   if (impl_out) *impl_out = impl;
   if (launches_out)
     *launches_out = (impl == FALCON_IMPL_TC ? tc_chunk_launches(a) : impl == FALCON_IMPL_SCAN ? 2 : 1) +
-                    (p->prologue ? 1 : 0);
+                    (p->prologue && !prologue_fused(p) ? 1 : 0);
   return FALCON_OK;
 }
 

@@ -65,6 +65,7 @@ struct TcArgs {
   uint8_t* ws_T;      // [B*H*NC][2 d_k 128]: bf16 128B-swizzled images, W slabs | U slabs
   float* ws_g;        // [B*H*NC][kGateF]: Gamma, exp(g_last - g), g, exp(g - g_block)
   uint32_t* status;   // workspace status word
+  int pro;            // prologue flags applied inside the d = 64 kernels (falcon_prologue_t)
 };
 
 // ======================================================================
@@ -166,8 +167,9 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   const int next = item + gridDim.x;
   const int t_row = chunk * kC + tid;
   const bool step_ok = tid < 64 && t_row < a.T;
-  const float ell = step_ok ? clamped_log_decay(lam_n, a.eps_gamma) : 0.f;
-  const float beta = (step_ok && pos_n + t_row >= a.shift) ? beta_n : 0.f;
+  // the clamped decay and the step size, from gate logits when the prologue asks
+  const float ell = step_ok ? logf(gate_gamma(lam_n, a.eps_gamma, a.pro)) : 0.f;
+  const float beta = (step_ok && pos_n + t_row >= a.shift) ? gate_beta(beta_n, a.pro) : 0.f;
   {  // gates: row tid <-> step chunk * 64 + tid
     float g = ell;  // inclusive prefix sum over the chunk
 #pragma unroll
@@ -187,8 +189,40 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
   }
-  if (chunk == 0 && a.kprev_in && a.shift && tid < DK)  // x_0 = carried key (row 0 of the first chunk)
+  const bool carried = chunk == 0 && a.kprev_in && a.shift;  // x_0 = the carried key
+  if (carried && tid < DK)
     *reinterpret_cast<__nv_bfloat16*>(Xs + (tid >> 6) * 8192 + sw128(0, tid & 63)) = a.kprev_in[(size_t)bh * DK + tid];
+  if constexpr (DK == 64) {  // the prologue is fused into the d = 64 path only
+    // phi(k) = k / max(|k|, 1e-12) per key row, in place (the carried key is
+    // a feature already)
+    if ((a.pro & FALCON_PROLOGUE_L2NORM_QK) && tid < 64 && !(carried && tid == 0)) {
+      uint4 raw[DK / 8];
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < DK / 8; ++j) {
+        raw[j] = *reinterpret_cast<const uint4*>(Xs + (j >> 3) * 8192 + sw128(tid, 8 * (j & 7)));
+        const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(px[e]);
+          ss = fmaf(x.x, x.x, ss);
+          ss = fmaf(x.y, x.y, ss);
+        }
+      }
+      const float sc = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+#pragma unroll
+      for (int j = 0; j < DK / 8; ++j) {
+        const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(px[e]);
+          pk[e] = pack_bf16(x.x * sc, x.y * sc);
+        }
+        *reinterpret_cast<uint4*>(Xs + (j >> 3) * 8192 + sw128(tid, 8 * (j & 7))) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+  }
   fence_proxy_async();
   __syncthreads();
   const bool aborted = *abort_flag != 0;
@@ -822,11 +856,12 @@ __global__ void __launch_bounds__(288, 1)
 // operands.  Hand-offs are mbarriers: full/empty and
 // front-done per stage, product completions, output-done per TMEM buffer.
 // ----------------------------------------------------------------------
-template <bool SOLVE>
+template <bool SOLVE, bool L2N>
 struct PipeSmem {
   static constexpr int NST = 4;
   static constexpr size_t XO = 0, PO = 8192, WO = 16384, QO = 24576, UO = 32768, GO = 40960;
-  static constexpr size_t STAGE = GO + 1024;         // gates: Gamma, exp(g_last - g), g, exp(g - g_block)
+  static constexpr size_t STAGE = GO + (L2N ? 2048 : 1024);  // gates: Gamma, exp(g_last - g), g,
+                                                             // exp(g - g_block) (loaded), then phi's row scales
   static constexpr size_t SB = NST * STAGE;          // S rows (MN-major B)
   static constexpr size_t DL = SB + 8192;            // Delta rows (MN-major B)
   static constexpr size_t OST = DL + 8192;           // two output staging tiles
@@ -841,13 +876,16 @@ struct PipeSmem {
   __host__ __device__ static constexpr uint32_t col_b1(int p) { return 64 + 128 * p; }
   __host__ __device__ static constexpr uint32_t col_b2(int p) { return 128 + 128 * p; }
   static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192;
+  static constexpr int G_SQ = 256, G_SX = 320;  // L2N: 1 / |q_t|, 1 / |x_r| (L2-normalised features)
 };
 
-template <bool SOLVE>
+// L2N: q and k are L2-normalised by the prologue; the raw rows enter the
+// products and the rows' inverse norms their epilogues.
+template <bool SOLVE, bool L2N>
 __global__ void __launch_bounds__(288, 1)
     tc_fwd_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_o, TcArgs a) {
-  using L = PipeSmem<SOLVE>;
+  using L = PipeSmem<SOLVE, L2N>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   constexpr int NST = L::NST;
@@ -940,8 +978,39 @@ __global__ void __launch_bounds__(288, 1)
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
       uint8_t* st = stage(s);
       const float* gt = reinterpret_cast<const float*>(st + L::GO);
-      if (c == 0 && a.kprev_in && a.shift && ftid < 64)  // x_0 = carried key
+      const bool carried = c == 0 && a.kprev_in && a.shift;  // x_0 = the carried key
+      if (carried && ftid < 64)
         *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = a.kprev_in[(size_t)bh * 64 + ftid];
+      if constexpr (L2N) {  // row scales of the prologue's phi, 1 / max(|row|, 1e-12), of the query
+                            // row and the key row r (the carried key is a feature already); the raw
+                            // rows enter the products and the scales their epilogues
+        float* gw = reinterpret_cast<float*>(st + L::GO);
+        float sq, sx;
+        {
+          float pq = 0.f, px = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 rq = *reinterpret_cast<const uint4*>(st + L::QO + sw128(r, 32 * half + 8 * j));
+            const uint4 rx = *reinterpret_cast<const uint4*>(st + L::XO + sw128(r, 32 * half + 8 * j));
+            const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&rq);
+            const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&rx);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 q2 = __bfloat1622float2(hq[e]), x2 = __bfloat1622float2(hx[e]);
+              pq = fmaf(q2.x, q2.x, fmaf(q2.y, q2.y, pq));
+              px = fmaf(x2.x, x2.x, fmaf(x2.y, x2.y, px));
+            }
+          }
+          pq += __shfl_xor_sync(0xffffffffu, pq, 16);
+          px += __shfl_xor_sync(0xffffffffu, px, 16);
+          sq = 1.f / fmaxf(sqrtf(pq), 1e-12f);
+          sx = (carried && r == 0) ? 1.f : 1.f / fmaxf(sqrtf(px), 1e-12f);
+        }
+        if (half == 0) {
+          gw[L::G_SQ + r] = sq;
+          gw[L::G_SX + r] = sx;
+        }
+      }
       fence_proxy_async();
       tc_fence_before();
       if (named_bar_any(1, 128, *abort_flag != 0)) break;
@@ -998,6 +1067,14 @@ __global__ void __launch_bounds__(288, 1)
             }
           }
         }
+        if constexpr (L2N) {  // phi(x_r) . phi(q_t) from the raw rows
+          const float sxr = gt[L::G_SX + r];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 s4 = *reinterpret_cast<const float4*>(gt + L::G_SQ + 32 * half + i);
+            pv[i] *= sxr * s4.x; pv[i + 1] *= sxr * s4.y; pv[i + 2] *= sxr * s4.z; pv[i + 3] *= sxr * s4.w;
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t pk[4];
@@ -1014,7 +1091,8 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int idx = ftid + 128 * k;
-          const float fr = gt[L::G_DEC + (idx >> 3)];
+          const float fr = L2N ? gt[L::G_DEC + (idx >> 3)] * gt[L::G_SX + (idx >> 3)]  // decay x phi's scale
+                               : gt[L::G_DEC + (idx >> 3)];
           const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in[k]);
           uint32_t pk[4];
 #pragma unroll
@@ -1029,8 +1107,20 @@ __global__ void __launch_bounds__(288, 1)
       tc_fence_before();
       mbar_arrive(&fdone[s]);
     }
-    if (a.kprev_out && !*abort_flag && ftid < 64)
-      a.kprev_out[(size_t)bh * 64 + ftid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + ftid];
+    const bool ab = __any_sync(0xffffffffu, *abort_flag != 0);  // one answer per warp
+    if (a.kprev_out && !ab && ftid < 32) {  // the last key, as a feature (warp 4)
+      const __nv_bfloat16* kl = a.k + (((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64;
+      const float k0 = __bfloat162float(kl[ftid]), k1 = __bfloat162float(kl[ftid + 32]);
+      float sc = 1.f;
+      if (L2N) {
+        float ss = fmaf(k0, k0, k1 * k1);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        sc = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+      }
+      a.kprev_out[(size_t)bh * 64 + ftid] = __float2bfloat16_rn(k0 * sc);
+      a.kprev_out[(size_t)bh * 64 + ftid + 32] = __float2bfloat16_rn(k1 * sc);
+    }
     if (a.pos_out && !*abort_flag && ftid == 0) a.pos_out[bh] = (a.pos_in ? a.pos_in[bh] : 0) + a.T;
   } else if (warp < 2) {
     // ------------------------------------------------------------ state chain
@@ -1143,7 +1233,9 @@ __global__ void __launch_bounds__(288, 1)
       const int s = c % NST, p = c & 1;
       if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1))) fail();
       if (named_bar_any(4, 64, *abort_flag != 0)) break;
-      const float gr = reinterpret_cast<const float*>(stage(s) + L::GO)[L::G_GAM + r];
+      // Gamma_t, times 1 / |q_t| when the products saw raw queries (phi(q) in the prologue)
+      const float* gq = reinterpret_cast<const float*>(stage(s) + L::GO);
+      const float gr = L2N ? gq[L::G_GAM + r] * gq[L::G_SQ + r] : gq[L::G_GAM + r];
       mbar_arrive(&empty[s]);  // this thread reads nothing more of the stage
       if (!mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1))) fail();  // both products of the chunk
       tc_fence_after();
@@ -1263,8 +1355,9 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       record_event(fa, 1);
     }
     {  // pipelined: producer warp, front and back warpgroups
-      auto k = tc_fwd_pipe_kernel<SOLVE>;
-      const size_t smem = PipeSmem<SOLVE>::TOTAL;
+      const bool l2n = (ta.pro & FALCON_PROLOGUE_L2NORM_QK) != 0;
+      auto k = l2n ? tc_fwd_pipe_kernel<SOLVE, true> : tc_fwd_pipe_kernel<SOLVE, false>;
+      const size_t smem = l2n ? PipeSmem<SOLVE, true>::TOTAL : PipeSmem<SOLVE, false>::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
       // overlaps the per-chunk kernel's tail with its launch and set-up
@@ -1333,6 +1426,7 @@ int launch_tc_chunk(const FwdArgs& fa) {
   ta.ws_g = reinterpret_cast<float*>(ws + w.g);
   ta.status = reinterpret_cast<uint32_t*>(ws + w.status);
   ta.NV = 64;
+  ta.pro = fa.dk == 64 ? fa.prologue : 0;  // fused into the d = 64 kernels (else applied before)
   const bool solve = fa.variant == FALCON_1;
   if (fa.dk == 64) return solve ? launch_t<64, 64, true>(fa, ta) : launch_t<64, 64, false>(fa, ta);
   return solve ? launch_t<128, 64, true>(fa, ta) : launch_t<128, 64, false>(fa, ta);

@@ -69,18 +69,47 @@ def test_prologue_dense(F, variant, flags):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_prologue_dense_fp32_and_timed_plan(F, dtype):
+    """bf16 Falcon-1 at d = 64 takes the prologue inside its two kernels (no
+    extra launch); the fp32 path applies it in a gather pass first."""
     w = wl(FALCON_1, dtype=dtype)
     x = make_raw_inputs(w, device="cuda")
     p = params_for(F, w)
     p.prologue = BOTH
     impl, launches = F.falcon_chunk_fwd_plan(p)
     p0 = params_for(F, w)
-    assert launches == F.falcon_chunk_fwd_plan(p0)[1] + 1
+    assert launches == F.falcon_chunk_fwd_plan(p0)[1] + (0 if dtype == "bf16" else 1)
     assert F.falcon_workspace_size(p) > F.falcon_workspace_size(p0)
     o, co = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"])
     torch.cuda.synchronize()
     o_ref, c_ref = oracle_pro(w, x, BOTH)
     check(w, o, co["S"], o_ref, c_ref["S"])
+
+
+@pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])
+@pytest.mark.parametrize("pairing", ["prefix", "same"])
+@pytest.mark.parametrize("flags", [1, BOTH])
+def test_prologue_fused_continuation(F, variant, pairing, flags):
+    """The prologue inside the d = 64 tensor-core kernels across two calls:
+    the second takes the first's carry (its carried key a feature), and the
+    two outputs and the final state match the oracle on the whole sequence."""
+    T1, T2 = 100, 150
+    w = wl(variant, T=T1 + T2, pairing=pairing)
+    x = make_raw_inputs(w, device="cuda")
+    if not flags & 2:
+        g = make_inputs(w, device="cuda")
+        x["beta"], x["lam"] = g["beta"], g["lam"]
+    outs, carry = [], None
+    for t0, t1 in ((0, T1), (T1, T1 + T2)):
+        wp = w.with_(T=t1 - t0)
+        p = params_for(F, wp)
+        p.prologue = flags
+        assert F.falcon_chunk_fwd_plan(p)[1] == F.falcon_chunk_fwd_plan(params_for(F, wp))[1]
+        xs = {n: v[:, t0:t1].contiguous() for n, v in x.items()}
+        o, carry = F.chunk_forward(p, xs["q"], xs["k"], xs["v"], xs["beta"], xs["lam"], carry)
+        outs.append(o)
+    torch.cuda.synchronize()
+    o_ref, c_ref = oracle_pro(w, x, flags)
+    check(w, torch.cat(outs, dim=1), carry["S"], o_ref, c_ref["S"])
 
 
 def varlen_case(F, w, lengths, flags=0, carries=None, raw=False):
