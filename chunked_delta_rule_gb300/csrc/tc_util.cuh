@@ -103,24 +103,6 @@ __device__ __forceinline__ void store_row64(uint8_t* tile, int r, const float* v
   }
 }
 
-// Scale every row of a [64 x 64] bf16 swizzled tile by f[row] into dst (16-byte chunks).
-__device__ __forceinline__ void scale_rows(uint8_t* dst, const uint8_t* src, const float* f,
-                                           int tid, int nthreads) {
-  for (int idx = tid; idx < 512; idx += nthreads) {
-    const int R = idx >> 3;
-    const uint4 in = *reinterpret_cast<const uint4*>(src + idx * 16);
-    const __nv_bfloat162* pin = reinterpret_cast<const __nv_bfloat162*>(&in);
-    const float fr = f[R];
-    uint32_t pk[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 x = __bfloat1622float2(pin[e]);
-      pk[e] = pack_bf16(x.x * fr, x.y * fr);
-    }
-    *reinterpret_cast<uint4*>(dst + idx * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  }
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
