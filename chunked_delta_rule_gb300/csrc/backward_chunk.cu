@@ -483,29 +483,33 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
 }
 
 // ---------------------------------------------------------------- (b), (c)
-// One CTA of 256 threads per (b, h, 16 value columns); the S (or dS) slice,
-// 64 x 16, in shared memory.  Each chunk step is two 64 x 64 x 16 products on
-// the tensor cores (three-term tf32 split, as in mm64): warp w owns the 16 x 8
-// tile at rows 16 (w / 2), columns 8 (w % 2).  The next chunk's W, diag(E) X,
-// value slice (U or Y) and decay arrive by cp.async into the other of two
-// stages.
-constexpr int kSC = 16;
-constexpr int CPT = kSC / 4;  // columns per thread in the row-wise copies
-constexpr int LDS_ = kSC + 8;  // row stride of the slices: fragment loads free of bank conflicts
-
+// One CTA of 256 threads per (b, h, SC value columns), SC = 16, or 32 when
+// the 16-column CTAs would not fit one wave (two CTAs per SM); the S (or dS)
+// slice, 64 x SC, in shared memory.  Each chunk step is two 64 x 64 x SC
+// products on the tensor cores (three-term tf32 split, as in mm64): warp w
+// owns the SC / 16 tiles of 16 x 8 at rows 16 (w / 2), columns from
+// (SC / 2) (w % 2).  The next chunk's W, diag(E) X, value slice (U or Y) and
+// decay arrive by cp.async into the other of two stages.
+template <int SC>
 struct ChainStage {
+  static constexpr int CPT = SC / 4;  // columns per thread in the row-wise copies
+  static constexpr int LDS_ = SC + 8; // row stride of the slices: fragment loads free of bank conflicts
+  static constexpr int NTW = SC / 16; // 8-column tiles per warp
   float W[kN * LDM];
   float X[kN * LDM];
   float C[kN * LDS_];   // U (forward) or Y (backward) slice
   float g4[4];          // Gamma of rows 60..63
 };
+template <int SC>
 struct ChainSmem {
-  ChainStage st[2];
-  float S[kN * LDS_];
-  float Dl[kN * LDS_];
+  ChainStage<SC> st[2];
+  float S[kN * ChainStage<SC>::LDS_];
+  float Dl[kN * ChainStage<SC>::LDS_];
 };
 
-__device__ __forceinline__ void chain_stage(const CbArgs& a, ChainStage& st, size_t cg, int c0, int which_c) {
+template <int SC>
+__device__ __forceinline__ void chain_stage(const CbArgs& a, ChainStage<SC>& st, size_t cg, int c0, int which_c) {
+  constexpr int LDS_ = ChainStage<SC>::LDS_;
   const int tid = threadIdx.x;
   const float* wW = wsmat(a, cg, M_W);
   const float* wX = wsmat(a, cg, M_XT);
@@ -517,26 +521,23 @@ __device__ __forceinline__ void chain_stage(const CbArgs& a, ChainStage& st, siz
     cp16(&st.X[r * LDM + c], &wX[r * kN + c]);
   }
 #pragma unroll
-  for (int k = 0; k < kN * kSC / 4 / kThrC; ++k) {
-    const int i = tid + kThrC * k, r = i / (kSC / 4), c = (i % (kSC / 4)) * 4;
+  for (int k = 0; k < kN * SC / 4 / kThrC; ++k) {
+    const int i = tid + kThrC * k, r = i / (SC / 4), c = (i % (SC / 4)) * 4;
     cp16(&st.C[r * LDS_ + c], &wC[r * kN + c0 + c]);
   }
   if (tid == 0) cp16(st.g4, wsgate(a, cg) + kN + kN - 4);
 }
 
-__device__ __forceinline__ void ldcs(float (&v)[CPT], const float* p) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-}
-
-// c (this warp's 16 x 8 tile at rows m0, columns n0) += sgn A B over K = 64:
-// A [M][K] at A[m * LDM + k] (AT: A[k * LDM + m]), B [K][16] at B[k * LDS_ + n].
-// Two accumulators over alternate k steps shorten the dependent chain.
-template <bool AT>
-__device__ __forceinline__ void tile_mma(float (&c)[4], const float* __restrict__ A, const float* __restrict__ B,
-                                         int m0, int n0, float sgn) {
+// c[j] (this warp's 16 x 8 tiles at rows m0, columns n0 + 8 j) += sgn A B over
+// K = 64: A [M][K] at A[m * LDM + k] (AT: A[k * LDM + m]), B [K][SC] at
+// B[k * LDS_ + n]; the A fragments serve every tile.  Two accumulators per
+// tile over alternate k steps shorten the dependent chain.
+template <int SC, bool AT>
+__device__ __forceinline__ void tile_mma(float (&c)[SC / 16][4], const float* __restrict__ A,
+                                         const float* __restrict__ B, int m0, int n0, float sgn) {
+  constexpr int LDS_ = ChainStage<SC>::LDS_, NTW = SC / 16;
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-  float c2[4] = {0.f, 0.f, 0.f, 0.f};
+  float c2[NTW][4] = {};
 #pragma unroll
   for (int k0 = 0; k0 < kN; k0 += 8) {
     float x[4];
@@ -551,125 +552,149 @@ __device__ __forceinline__ void tile_mma(float (&c)[4], const float* __restrict_
       x[2] = A[(m0 + gid) * LDM + k0 + tig + 4];
       x[3] = A[(m0 + gid + 8) * LDM + k0 + tig + 4];
     }
-    uint32_t ah[4], al[4], bh[2], bl[2];
+    uint32_t ah[4], al[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) split_tf32(sgn * x[e], ah[e], al[e]);
-    split_tf32(B[(k0 + tig) * LDS_ + n0 + gid], bh[0], bl[0]);
-    split_tf32(B[(k0 + tig + 4) * LDS_ + n0 + gid], bh[1], bl[1]);
-    float (&acc)[4] = (k0 & 8) ? c2 : c;
-    tc::mma_tf32_16x8x8(acc, al, bh);
-    tc::mma_tf32_16x8x8(acc, ah, bl);
-    tc::mma_tf32_16x8x8(acc, ah, bh);
+#pragma unroll
+    for (int j = 0; j < NTW; ++j) {
+      uint32_t bh[2], bl[2];
+      split_tf32(B[(k0 + tig) * LDS_ + n0 + 8 * j + gid], bh[0], bl[0]);
+      split_tf32(B[(k0 + tig + 4) * LDS_ + n0 + 8 * j + gid], bh[1], bl[1]);
+      float (&acc)[4] = (k0 & 8) ? c2[j] : c[j];
+      tc::mma_tf32_16x8x8(acc, al, bh);
+      tc::mma_tf32_16x8x8(acc, ah, bl);
+      tc::mma_tf32_16x8x8(acc, ah, bh);
+    }
   }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) c[e] += c2[e];
+  for (int j = 0; j < NTW; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[j][e] += c2[j][e];
 }
-// the tile's four elements of a [64][LDS_] slice: (row, column) =
-// (m0 + gid + 8 (e / 2), n0 + 2 tig + e % 2)
-__device__ __forceinline__ void tile_ld(float (&v)[4], const float* p, int m0, int n0) {
+// the tiles' elements of a [64][LDS_] slice: tile j, (row, column) =
+// (m0 + gid + 8 (e / 2), n0 + 8 j + 2 tig + e % 2)
+template <int SC>
+__device__ __forceinline__ void tile_ld(float (&v)[SC / 16][4], const float* p, int m0, int n0) {
+  constexpr int LDS_ = ChainStage<SC>::LDS_;
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-  const float2 a = *reinterpret_cast<const float2*>(&p[(m0 + gid) * LDS_ + n0 + 2 * tig]);
-  const float2 b = *reinterpret_cast<const float2*>(&p[(m0 + gid + 8) * LDS_ + n0 + 2 * tig]);
-  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+#pragma unroll
+  for (int j = 0; j < SC / 16; ++j) {
+    const float2 a = *reinterpret_cast<const float2*>(&p[(m0 + gid) * LDS_ + n0 + 8 * j + 2 * tig]);
+    const float2 b = *reinterpret_cast<const float2*>(&p[(m0 + gid + 8) * LDS_ + n0 + 8 * j + 2 * tig]);
+    v[j][0] = a.x; v[j][1] = a.y; v[j][2] = b.x; v[j][3] = b.y;
+  }
 }
-__device__ __forceinline__ void tile_st(float* p, const float (&v)[4], int m0, int n0) {
+template <int SC>
+__device__ __forceinline__ void tile_st(float* p, const float (&v)[SC / 16][4], int m0, int n0) {
+  constexpr int LDS_ = ChainStage<SC>::LDS_;
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-  *reinterpret_cast<float2*>(&p[(m0 + gid) * LDS_ + n0 + 2 * tig]) = make_float2(v[0], v[1]);
-  *reinterpret_cast<float2*>(&p[(m0 + gid + 8) * LDS_ + n0 + 2 * tig]) = make_float2(v[2], v[3]);
+#pragma unroll
+  for (int j = 0; j < SC / 16; ++j) {
+    *reinterpret_cast<float2*>(&p[(m0 + gid) * LDS_ + n0 + 8 * j + 2 * tig]) = make_float2(v[j][0], v[j][1]);
+    *reinterpret_cast<float2*>(&p[(m0 + gid + 8) * LDS_ + n0 + 8 * j + 2 * tig]) = make_float2(v[j][2], v[j][3]);
+  }
+}
+// CPT consecutive fp32 values of shared-memory row p to global row q (16-byte pieces)
+template <int CPT>
+__device__ __forceinline__ void copy_row(float* q, const float* p) {
+#pragma unroll
+  for (int i = 0; i < CPT; i += 4) *reinterpret_cast<float4*>(q + i) = *reinterpret_cast<const float4*>(p + i);
 }
 
+template <int SC>
 __global__ void __launch_bounds__(kThrC) bwdc_fwd_chain_kernel(CbArgs a) {
+  using St = ChainStage<SC>;
+  constexpr int CPT = St::CPT, LDS_ = St::LDS_, NTW = St::NTW;
   extern __shared__ float4 smem_f4[];
-  ChainSmem& sm = *reinterpret_cast<ChainSmem*>(smem_f4);
-  const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
+  ChainSmem<SC>& sm = *reinterpret_cast<ChainSmem<SC>*>(smem_f4);
+  const int bh = blockIdx.x, c0 = blockIdx.y * SC, tid = threadIdx.x;
   const int r = tid >> 2, q8 = (tid & 3) * CPT;
-  const int m0 = 16 * (tid >> 6), n0 = 8 * ((tid >> 5) & 1);
-  for (int i = tid; i < kN * kSC; i += kThrC) {
-    const int rr = i / kSC, cc = i % kSC;
+  const int m0 = 16 * (tid >> 6), n0 = (SC / 2) * ((tid >> 5) & 1);
+  for (int i = tid; i < kN * SC; i += kThrC) {
+    const int rr = i / SC, cc = i % SC;
     sm.S[rr * LDS_ + cc] = a.S_in ? a.S_in[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
   }
-  chain_stage(a, sm.st[0], (size_t)bh * a.NC, c0, M_U);
+  chain_stage<SC>(a, sm.st[0], (size_t)bh * a.NC, c0, M_U);
   cp_commit();
-  if (a.NC > 1) chain_stage(a, sm.st[1], (size_t)bh * a.NC + 1, c0, M_U);
+  if (a.NC > 1) chain_stage<SC>(a, sm.st[1], (size_t)bh * a.NC + 1, c0, M_U);
   cp_commit();
   for (int c = 0; c < a.NC; ++c) {
     const size_t cg = (size_t)bh * a.NC + c;
-    ChainStage& st = sm.st[c & 1];
+    St& st = sm.st[c & 1];
     cp_wait1();
     __syncthreads();
-    {  // chunk start state out
-      float v[CPT];
-      ldcs(v, &sm.S[r * LDS_ + q8]);
-      *reinterpret_cast<float4*>(&wsmat(a, cg, M_S0)[(size_t)r * kN + c0 + q8]) = make_float4(v[0], v[1], v[2], v[3]);
-    }
-    float d[4];  // Delta = U - W S  (additive: Delta = U)
-    tile_ld(d, st.C, m0, n0);
-    if (!a.additive) tile_mma<false>(d, st.W, sm.S, m0, n0, -1.f);
-    tile_st(sm.Dl, d, m0, n0);
+    copy_row<CPT>(&wsmat(a, cg, M_S0)[(size_t)r * kN + c0 + q8], &sm.S[r * LDS_ + q8]);  // chunk start state out
+    float d[NTW][4];  // Delta = U - W S  (additive: Delta = U)
+    tile_ld<SC>(d, st.C, m0, n0);
+    if (!a.additive) tile_mma<SC, false>(d, st.W, sm.S, m0, n0, -1.f);
+    tile_st<SC>(sm.Dl, d, m0, n0);
     __syncthreads();
     // S = Gamma_63 S + (diag(E) X)^T Delta   (row of S = key index)
-    float v[4];
-    tile_ld(v, sm.S, m0, n0);
+    float v[NTW][4];
+    tile_ld<SC>(v, sm.S, m0, n0);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) v[e] *= st.g4[3];
-    tile_mma<true>(v, st.X, sm.Dl, m0, n0, 1.f);
+    for (int j = 0; j < NTW; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[j][e] *= st.g4[3];
+    tile_mma<SC, true>(v, st.X, sm.Dl, m0, n0, 1.f);
     __syncthreads();  // every read of S and of this stage is done
-    tile_st(sm.S, v, m0, n0);
-    if (c + 2 < a.NC) chain_stage(a, st, cg + 2, c0, M_U);
+    tile_st<SC>(sm.S, v, m0, n0);
+    if (c + 2 < a.NC) chain_stage<SC>(a, st, cg + 2, c0, M_U);
     cp_commit();
   }
   cp_wait0();
 }
 
+template <int SC>
 __global__ void __launch_bounds__(kThrC) bwdc_bwd_chain_kernel(CbArgs a) {
+  using St = ChainStage<SC>;
+  constexpr int CPT = St::CPT, LDS_ = St::LDS_, NTW = St::NTW;
   extern __shared__ float4 smem_f4[];
-  ChainSmem& sm = *reinterpret_cast<ChainSmem*>(smem_f4);
-  const int bh = blockIdx.x, c0 = blockIdx.y * kSC, tid = threadIdx.x;
+  ChainSmem<SC>& sm = *reinterpret_cast<ChainSmem<SC>*>(smem_f4);
+  const int bh = blockIdx.x, c0 = blockIdx.y * SC, tid = threadIdx.x;
   const int r = tid >> 2, q8 = (tid & 3) * CPT;
-  const int m0 = 16 * (tid >> 6), n0 = 8 * ((tid >> 5) & 1);
-  for (int i = tid; i < kN * kSC; i += kThrC) {
-    const int rr = i / kSC, cc = i % kSC;
+  const int m0 = 16 * (tid >> 6), n0 = (SC / 2) * ((tid >> 5) & 1);
+  for (int i = tid; i < kN * SC; i += kThrC) {
+    const int rr = i / SC, cc = i % SC;
     sm.S[rr * LDS_ + cc] = a.dS_final ? a.dS_final[((size_t)bh * kN + rr) * kN + c0 + cc] : 0.f;
   }
   const size_t base = (size_t)bh * a.NC;
-  chain_stage(a, sm.st[0], base + a.NC - 1, c0, M_Y);
+  chain_stage<SC>(a, sm.st[0], base + a.NC - 1, c0, M_Y);
   cp_commit();
-  if (a.NC > 1) chain_stage(a, sm.st[1], base + a.NC - 2, c0, M_Y);
+  if (a.NC > 1) chain_stage<SC>(a, sm.st[1], base + a.NC - 2, c0, M_Y);
   cp_commit();
   for (int n = 0; n < a.NC; ++n) {
     const int c = a.NC - 1 - n;
     const size_t cg = base + c;
-    ChainStage& st = sm.st[n & 1];
+    St& st = sm.st[n & 1];
     cp_wait1();
     __syncthreads();
-    {  // gradient of the chunk's end state out
-      float v[CPT];
-      ldcs(v, &sm.S[r * LDS_ + q8]);
-      *reinterpret_cast<float4*>(&wsmat(a, cg, M_DS1)[(size_t)r * kN + c0 + q8]) = make_float4(v[0], v[1], v[2], v[3]);
-    }
+    copy_row<CPT>(&wsmat(a, cg, M_DS1)[(size_t)r * kN + c0 + q8], &sm.S[r * LDS_ + q8]);  // end-state gradient out
     if (!a.additive) {  // Z = diag(E) X dS  (row = chunk row)
-      float z[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_mma<false>(z, st.X, sm.S, m0, n0, 1.f);
-      tile_st(sm.Dl, z, m0, n0);
+      float z[NTW][4] = {};
+      tile_mma<SC, false>(z, st.X, sm.S, m0, n0, 1.f);
+      tile_st<SC>(sm.Dl, z, m0, n0);
     }
     __syncthreads();
     // dS = Gamma_63 dS - W^T Z + Y   (row = key index)
-    float v[4], y[4];
-    tile_ld(v, sm.S, m0, n0);
-    tile_ld(y, st.C, m0, n0);
+    float v[NTW][4], y[NTW][4];
+    tile_ld<SC>(v, sm.S, m0, n0);
+    tile_ld<SC>(y, st.C, m0, n0);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) v[e] = fmaf(st.g4[3], v[e], y[e]);
-    if (!a.additive) tile_mma<true>(v, st.W, sm.Dl, m0, n0, -1.f);
+    for (int j = 0; j < NTW; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[j][e] = fmaf(st.g4[3], v[j][e], y[j][e]);
+    if (!a.additive) tile_mma<SC, true>(v, st.W, sm.Dl, m0, n0, -1.f);
     __syncthreads();
-    tile_st(sm.S, v, m0, n0);
-    if (n + 2 < a.NC) chain_stage(a, st, base + a.NC - 3 - n, c0, M_Y);
+    tile_st<SC>(sm.S, v, m0, n0);
+    if (n + 2 < a.NC) chain_stage<SC>(a, st, base + a.NC - 3 - n, c0, M_Y);
     cp_commit();
   }
   cp_wait0();
   __syncthreads();
   if (a.dS_in)
-    for (int i = tid; i < kN * kSC; i += kThrC)
-      a.dS_in[((size_t)bh * kN + i / kSC) * kN + c0 + i % kSC] = sm.S[(i / kSC) * LDS_ + i % kSC];
+    for (int i = tid; i < kN * SC; i += kThrC)
+      a.dS_in[((size_t)bh * kN + i / SC) * kN + c0 + i % SC] = sm.S[(i / SC) * LDS_ + i % SC];
 }
 
 // ---------------------------------------------------------------- (d)
@@ -1015,6 +1040,17 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
 constexpr size_t prep_smem() { return 8 * kN * LDM * sizeof(float) + sizeof(GateSm) + 4 * kN * sizeof(float); }
 constexpr size_t grad_smem() { return 12 * kN * LDM * sizeof(float) + sizeof(GateSm) + 8 * kN * sizeof(float); }
 
+template <int SC>
+int launch_chains(const CbArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(ChainSmem<SC>);
+  if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_fwd_chain_kernel<SC>), smem) ||
+      !set_smem_limit(reinterpret_cast<const void*>(bwdc_bwd_chain_kernel<SC>), smem))
+    return FALCON_ERR_CUDA;
+  bwdc_fwd_chain_kernel<SC><<<dim3(a.B * a.H, kN / SC), kThrC, smem, s>>>(a);
+  bwdc_bwd_chain_kernel<SC><<<dim3(a.B * a.H, kN / SC), kThrC, smem, s>>>(a);
+  return FALCON_OK;
+}
+
 template <typename Tin>
 int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
   const unsigned nch = (unsigned)(a.B * a.H * a.NC);
@@ -1022,12 +1058,14 @@ int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
   auto grad = bwdc_grad_kernel<Tin>;
   if (!set_smem_limit(reinterpret_cast<const void*>(prep), prep_smem())) return FALCON_ERR_CUDA;
   if (!set_smem_limit(reinterpret_cast<const void*>(grad), grad_smem())) return FALCON_ERR_CUDA;
-  if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_fwd_chain_kernel), sizeof(ChainSmem)) ||
-      !set_smem_limit(reinterpret_cast<const void*>(bwdc_bwd_chain_kernel), sizeof(ChainSmem)))
-    return FALCON_ERR_CUDA;
   prep<<<nch, kThr, prep_smem(), s>>>(a);
-  bwdc_fwd_chain_kernel<<<dim3(a.B * a.H, kN / kSC), kThrC, sizeof(ChainSmem), s>>>(a);
-  bwdc_bwd_chain_kernel<<<dim3(a.B * a.H, kN / kSC), kThrC, sizeof(ChainSmem), s>>>(a);
+  // 16-column chain slices when their CTAs fit one wave at two per SM, else 32
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FALCON_ERR_CUDA;
+  const int st = (long)a.B * a.H * (kN / 16) <= 2L * sms ? launch_chains<16>(a, s) : launch_chains<32>(a, s);
+  if (st != FALCON_OK) return st;
   grad<<<nch, kThr, grad_smem(), s>>>(a);
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
