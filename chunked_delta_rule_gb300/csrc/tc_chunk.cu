@@ -14,7 +14,7 @@
 //  (a) per-chunk kernel, fully parallel: TMA loads the shifted keys and the
 //      values, one tcgen05 MMA forms the Gram matrix in TMEM,
 //      the gates (clamped log-decay, its in-chunk prefix sum, NLMS step) are
-//      formed from lambda, beta and the Gram diagonal, and T = (I + A)^{-1}
+//      formed from lambda, beta and the key norms, and T = (I + A)^{-1}
 //      is found by blocked forward substitution: 16x16 diagonal blocks in
 //      registers, off-diagonal blocks merged with warp-level tf32 MMAs in
 //      shared memory (tc_wyu_kernel, one chunk per CTA, persistent).  A
@@ -25,7 +25,13 @@
 //      the fp32 state in registers: TMA and bulk copies bring the chunk's
 //      operands while earlier chunks compute; every contraction is a
 //      tcgen05 MMA with the accumulator in TMEM; the output tile leaves by
-//      TMA store.  d = 64 is warp-specialised (tc_fwd_pipe_kernel).
+//      TMA store.  d = 64 is warp-specialised (tc_fwd_pipe_kernel: producer,
+//      front, state chain and output warps); d = 128 (tc_fwd_kernel) has one
+//      warp that issues every load and product for eight epilogue warps.
+//  The input prologue (phi = L2 normalisation of q and k, gates from logits)
+//  runs inside the d = 64 kernels when asked for.
+// The second kernel is launched to overlap the first one's tail (programmatic
+// dependent launch) and waits for it in hardware before reading its images.
 // Every mbarrier wait is bounded; on timeout a kernel records an error in the
 // workspace status word and leaves its chunk loop.
 
