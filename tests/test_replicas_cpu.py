@@ -67,3 +67,21 @@ def test_job_throughput_counts_every_rank():
     one = bench.job_tokens_per_s(LM_F1, 1, 0.1)
     assert bench.job_tokens_per_s(LM_F1, 4, 0.1) == pytest.approx(4 * one)
     assert bench.max_over_ranks(3.0, 1, "cpu") == 3.0
+
+
+def test_roofline_byte_counts():
+    """The numerators of the reported roofline fractions, by hand for the
+    headline workload (8 x 2048 x 12 heads, d = 64, bf16): q, k, v in and o
+    out at 128 bytes a row, beta and lambda at 4 bytes a step, the final
+    state once (96 heads x 64 x 64 fp32); the sequential kernel's share is
+    q, k, o and the state."""
+    import bench
+    from workloads import LM_F1, LONG_F1
+    rows = 8 * 2048 * 12
+    state = 96 * 64 * 64 * 4
+    assert bench.algorithmic_bytes(LM_F1) == rows * 4 * 128 + rows * 8 + state == 103809024
+    assert bench.kernel_bytes(LM_F1, ["tc_wyu_kernel", "tc_fwd_pipe_kernel"]) == [
+        rows * 2 * 128 + rows * 8, rows * 3 * 128 + state]
+    rows_l = 2 * 16384 * 16
+    assert bench.kernel_bytes(LONG_F1, ["tc_wyu_kernel", "tc_fwd_kernel"])[1] == \
+        rows_l * 3 * 256 + 32 * 128 * 128 * 4
