@@ -21,8 +21,8 @@
 // D (.) dD), summed back over the chunk's steps.  Four kernels:
 //  (a) bwdc_prep_kernel, per chunk: gates, T, W, U, diag(E) X and the chain's
 //      constant Y = Q^T diag(Gamma) dO - W^T (P (.) D)^T dO, into the workspace;
-//  (b) bwdc_fwd_chain_kernel, per (b, h, 16 value columns): chunk start states;
-//  (c) bwdc_bwd_chain_kernel, per (b, h, 16 value columns): dS at chunk ends;
+//  (b) bwdc_fwd_chain_kernel, per (b, h, 16 or 32 value columns): chunk start states;
+//  (c) bwdc_bwd_chain_kernel, per (b, h, 16 or 32 value columns): dS at chunk ends;
 //  (d) bwdc_grad_kernel, per chunk: every gradient.
 // The 64 x 64 products read fp32 operands from shared memory and run on the
 // tensor cores as warp-level m16n8k8 tf32 products with the three-term split
