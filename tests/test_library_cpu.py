@@ -200,3 +200,24 @@ def test_tc_workspace_layout(F, d):
     want = 256 + B * H * nc * (2 * d * 128) + B * H * nc * 1024
     want = (want + 255) // 256 * 256
     assert F.falcon_workspace_size(p) == want
+
+
+@pytest.mark.parametrize("kw,impl,launches", [
+    # the tensor-core path: per-chunk kernel + sequential kernel (Falcon-1 / 1A)
+    (dict(), "TC", 2), (dict(variant=1), "TC", 2), (dict(dk=128, dv=128), "TC", 2),
+    # one tensor-core kernel each (Falcon-2 / 2A at d = 64 and 128, Falcon-3A)
+    (dict(variant=2), "TC", 1), (dict(variant=3, dk=128, dv=128), "TC", 1),
+    (dict(variant=5, window=8), "TC", 1),
+    # Falcon-3: band prep + column-parallel window recurrence
+    (dict(variant=4, window=8), "SCAN", 2),
+    # fp32 inputs, or a chunk other than 64: the portable chunk kernel
+    (dict(dtype=1), "GENERIC", 1), (dict(chunk=32), "GENERIC", 1),
+    # the prologue: inside the d = 64 Falcon-1 kernels, a gather launch elsewhere
+    (dict(prologue=3), "TC", 2), (dict(prologue=3, variant=2), "TC", 2),
+    (dict(prologue=1, dk=128, dv=128), "TC", 3),
+])
+def test_chunk_forward_plan(F, kw, impl, launches):
+    """Which kernel family the AUTO plan picks and how many kernels it launches."""
+    p = _p(F, **kw)
+    got_impl, got_n = F.falcon_chunk_fwd_plan(p)
+    assert got_impl == getattr(F, "FALCON_IMPL_" + impl) and got_n == launches
