@@ -223,17 +223,58 @@ def test_p4_window_one_is_falcon1():
 
 
 @pytest.mark.parametrize("W", [2, 4, 8])
-def test_p4_identical_pairs_give_falcon1_update(W):
+@pytest.mark.parametrize("pair", [(O.FALCON_3, O.FALCON_1), (O.FALCON_3A, O.FALCON_1A)])
+def test_p4_identical_pairs_give_falcon1_update(W, pair):
     """Averaging (not summing): W copies of one pair move the state exactly
-    as one copy does, for every window size."""
+    as one copy does, for every window size; for the regression window
+    (Falcon-3 against Falcon-1) and the additive one (Falcon-3A against
+    Falcon-1A)."""
+    windowed, single = pair
     rng = np.random.default_rng(10)
     B, T, H, dk, dv = 1, 20, 1, 6, 4
     x = rand_inputs(rng, B, T, H, dk, dv)
     x["k"][:] = x["k"][:, :1]
     x["v"][:] = x["v"][:, :1]
-    o1, c1 = O.recurrent(**x, variant=O.FALCON_1)
-    o3, c3 = O.recurrent(**x, variant=O.FALCON_3, window=W)
+    o1, c1 = O.recurrent(**x, variant=single)
+    o3, c3 = O.recurrent(**x, variant=windowed, window=W)
     assert rel(o3, o1) <= 1e-12 and rel(c3["S"], c1["S"]) <= 1e-12
+
+
+@pytest.mark.parametrize("W", [2, 3, 8])
+def test_p4_falcon3a_is_window_masked_linear_attention(W):
+    """Falcon-3A, written out by brute force from the additive window write
+    [给记忆装一个“及时纠错”的开关, Falcon家族六个变体各管一段]: with the decay
+    products D(t, s) = prod_{s < u <= t} gamma_u, every step s writes
+    (eta_s / n_s) x_j v_j^T for each existing pair j of its window, so
+    o_t = sum_{s <= t} D(t, s) (eta_s / n_s) sum_{j in W(s)} (q_t . x_j) v_j,
+    eta_s = beta_s / (eps + mean_{j in W(s)} |x_j|^2).  Keys of varied
+    energy, so the window-average energy is not a constant."""
+    rng = np.random.default_rng(40 + W)
+    B, T, H, dk, dv = 1, 29, 2, 5, 3
+    x = rand_inputs(rng, B, T, H, dk, dv)
+    x["k"] = x["k"] * rng.uniform(0.3, 2.5, size=(B, T, H, 1))
+    eps, eg = 1e-6, 1e-3
+    o, c = O.recurrent(**x, variant=O.FALCON_3A, window=W, eps=eps, eps_gamma=eg)
+    gam = np.clip(1.0 - x["lam"], eg, 1.0)
+    brute = np.zeros((B, T, H, dv))
+    Sb = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            keys = {j: x["k"][b, j - 1, h] for j in range(1, T)}  # pair j = (k_{j-1}, v_j), j >= 1
+            for t in range(T):
+                for s in range(t + 1):
+                    win = [j for j in range(s - W + 1, s + 1) if j >= 1]
+                    if not win:
+                        continue
+                    e = np.mean([keys[j] @ keys[j] for j in win])
+                    coef = x["beta"][b, s, h] / (eps + e) / len(win)
+                    D = np.prod(gam[b, s + 1:t + 1, h])
+                    for j in win:
+                        brute[b, t, h] += D * coef * (x["q"][b, t, h] @ keys[j]) * x["v"][b, j, h]
+                        if t == T - 1:
+                            Sb[b, h] += D * coef * np.outer(keys[j], x["v"][b, j, h])
+    assert np.abs(o - brute).max() <= 1e-12 * max(1.0, np.abs(brute).max())
+    assert np.abs(c["S"] - Sb).max() <= 1e-12 * max(1.0, np.abs(Sb).max())
 
 
 def test_p4_planted_sum_instead_of_average_is_caught(monkeypatch):
