@@ -22,13 +22,16 @@ FALCON_IMPL_AUTO, FALCON_IMPL_GENERIC, FALCON_IMPL_TC, FALCON_IMPL_SCAN = 0, 1, 
 FALCON_PAIR_PREFIX, FALCON_PAIR_SAME_STEP = 0, 1
 FALCON_PROLOGUE_L2NORM_QK, FALCON_PROLOGUE_GATE_LOGITS = 1, 2
 FALCON_OK = 0
+FALCON_ERR_INVALID_ARG, FALCON_ERR_UNSUPPORTED, FALCON_ERR_WORKSPACE = -1, -2, -3
+FALCON_ERR_CUDA, FALCON_ERR_TIMEOUT = -4, -5
 
 EXPORTED = [
     "falcon_workspace_size", "falcon_chunk_fwd", "falcon_recurrent_step",
     "falcon_masked_parallel_workspace_size", "falcon_masked_parallel_ref_gpu",
     "falcon_strerror", "falcon_version", "falcon_chunk_fwd_plan", "falcon_chunk_fwd_timed",
     "falcon_chunk_fwd_noalloc", "falcon_backward_workspace_size", "falcon_backward",
-    "falcon_varlen_workspace_size", "falcon_chunk_fwd_varlen",
+    "falcon_varlen_workspace_size", "falcon_chunk_fwd_varlen", "falcon_workspace_status",
+    "falcon_test_hooks",
 ]
 
 
@@ -89,6 +92,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.falcon_backward_workspace_size.restype = S
     lib.falcon_backward.argtypes = [P, V, V, V, V, V, C, V, V, V, V, V, V, V, V, V, V, S, V]
     lib.falcon_backward.restype = ctypes.c_int
+    lib.falcon_workspace_status.argtypes = [V, V]
+    lib.falcon_workspace_status.restype = ctypes.c_int
+    lib.falcon_test_hooks.argtypes = [ctypes.c_uint64, ctypes.c_int32]
+    lib.falcon_test_hooks.restype = None
     lib.falcon_strerror.argtypes = [ctypes.c_int]
     lib.falcon_strerror.restype = ctypes.c_char_p
     lib.falcon_version.argtypes = []
@@ -220,6 +227,23 @@ def falcon_chunk_fwd_noalloc(p: Params, q, k, v, beta, lam, carry_in: dict | Non
                                         _ptr(o), ctypes.byref(co) if co is not None else None,
                                         _stream(stream))
     _check(code, "falcon_chunk_fwd_noalloc")
+
+
+def falcon_workspace_status(workspace=None, stream=None) -> int:
+    """Status code of the last tensor-core call that used ``workspace`` (None:
+    the last falcon_chunk_fwd_noalloc call on the current device): FALCON_OK
+    or FALCON_ERR_TIMEOUT.  Synchronises the stream; clears the word."""
+    code = load_library().falcon_workspace_status(_ptr(workspace), _stream(stream))
+    if code not in (FALCON_OK, FALCON_ERR_TIMEOUT):
+        _check(code, "falcon_workspace_status")
+    return code
+
+
+def falcon_test_hooks(wait_limit_ns: int = 0, stall: bool = False) -> None:
+    """Failure-detection test hook: the bounded-wait limit of later calls
+    (0 = the default 2 s) and a one-shot stall of the next Falcon-1/1A
+    tensor-core call's per-chunk kernel."""
+    load_library().falcon_test_hooks(int(wait_limit_ns), 1 if stall else 0)
 
 
 def falcon_recurrent_step(p: Params, q, k, v, beta, lam, carry: dict, o, stream=None):

@@ -1,12 +1,29 @@
 // C ABI of libfalcon.so: argument checks on the host, workspace sizing and
 // dispatch to the kernels.  Nothing here allocates device memory.
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 using namespace falcon;
+
+namespace falcon {
+
+// Failure-detection test hook state (falcon_test_hooks): process-wide.
+static std::atomic<uint64_t> g_wait_limit_ns{0};
+static std::atomic<int> g_stall{0};
+
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : tc::kWaitLimitNs;
+}
+
+bool take_test_stall() { return g_stall.exchange(0, std::memory_order_relaxed) != 0; }
+
+}  // namespace falcon
 
 namespace {
 
@@ -85,6 +102,31 @@ const char* falcon_strerror(int code) {
 }
 
 const char* falcon_version(void) { return "falcon-gb300 0.1 sm_103a"; }
+
+void falcon_test_hooks(uint64_t wait_limit_ns, int32_t stall) {
+  g_wait_limit_ns.store(wait_limit_ns, std::memory_order_relaxed);
+  g_stall.store(stall ? 1 : 0, std::memory_order_relaxed);
+}
+
+int falcon_workspace_status(const void* workspace, void* stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const void* word = workspace;
+  if (!word) {
+    void* scratch = nullptr;
+    const int st = noalloc_scratch(&scratch);
+    if (st != FALCON_OK) return st;
+    word = scratch;
+  }
+  if (reinterpret_cast<uintptr_t>(word) & 255) return FALCON_ERR_WORKSPACE;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FALCON_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FALCON_ERR_CUDA;
+  if (v == 0) return FALCON_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(const_cast<void*>(word), &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return FALCON_ERR_CUDA;
+  return FALCON_ERR_TIMEOUT;
+}
 
 // workspace of the kernel family alone (no prologue buffers), 256-byte multiple
 static size_t kernel_ws_bytes(const falcon_params_t* p) {

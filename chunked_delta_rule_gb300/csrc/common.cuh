@@ -133,6 +133,15 @@ int launch_backward(const FwdArgs& f, const void* dO, const float* dS_final, voi
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Limit of the bounded device-side waits of the next launch (2 s unless the
+// failure-detection test hook set another), and whether that hook asked the
+// next Falcon-1 / 1A tensor-core call to stall one wait (consumed here).
+uint64_t wait_limit_ns();
+bool take_test_stall();
+// Device address of the allocation-free entry point's scratch array on the
+// current device (its first 4 bytes are that entry point's status word).
+int noalloc_scratch(void** out);
+
 // Raise a kernel's dynamic shared-memory limit, once per kernel and device
 // (the attribute call costs host time on every launch otherwise).
 inline bool set_smem_limit(const void* kernel, size_t bytes) {

@@ -8,40 +8,35 @@
 // kernels with their scratch in a fixed array that lives in the library's
 // own device image instead.
 
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
 
-// 32 MiB: enough for B * H * ceil(T / 64) <= 1927 chunks of the tensor-core
-// path (16 KB of bf16 images + 1 KB of gates per chunk, plus a 256-byte status
-// word).  Every device that loads the library holds this array until exit.
+// 32 MiB: enough for every call whose falcon_workspace_size is at most that,
+// i.e. B * H * ceil(T / 64) <= 1927 chunks at d = 64 (16 KB of bf16 images +
+// 1 KB of gates per chunk) and <= 992 chunks at d = 128 (32 KB + 1 KB), after
+// a 256-byte status word.  Every device that loads the library holds this
+// array until exit.
 constexpr size_t kScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
 
-// Device address of the array on the current device (looked up once per
-// device).  In host code the array's name is only a host-side stand-in, so
-// the address must come from the runtime.
-int scratch_on_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FALCON_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FALCON_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FALCON_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+namespace falcon {
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address comes from the
+// runtime; it is looked up on every call (cheap once the library's device
+// code is loaded on the device) so that it stays right if the module is
+// loaded again, e.g. after a cudaDeviceReset.
+int noalloc_scratch(void** out) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FALCON_ERR_CUDA;
+  *out = p;
   return FALCON_OK;
 }
 
-}  // namespace
+}  // namespace falcon
 
 extern "C" int falcon_chunk_fwd_noalloc(const falcon_params_t* p, const void* q, const void* k,
                                         const void* v, const float* beta, const float* lambda,
@@ -56,7 +51,7 @@ extern "C" int falcon_chunk_fwd_noalloc(const falcon_params_t* p, const void* q,
   if (impl != FALCON_IMPL_TC) return FALCON_ERR_UNSUPPORTED;
   if (falcon_workspace_size(p) > kScratchBytes) return FALCON_ERR_WORKSPACE;
   void* scratch = nullptr;
-  st = scratch_on_current_device(&scratch);
+  st = falcon::noalloc_scratch(&scratch);
   if (st != FALCON_OK) return st;
   // the status word is the one part of the scratch that must start at zero
   if (cudaMemsetAsync(scratch, 0, 256, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -72,6 +72,9 @@ struct TcArgs {
   float* ws_g;        // [B*H*NC][kGateF]: Gamma, exp(g_last - g), g, exp(g - g_block)
   uint32_t* status;   // workspace status word
   int pro;            // prologue flags applied inside the d = 64 kernels (falcon_prologue_t)
+  uint64_t wait_ns;   // limit of every bounded wait
+  int stall;          // failure-detection test hook: the per-chunk kernel's first CTA waits on
+                      // a barrier that nothing completes (the wait runs out, a timeout is recorded)
 };
 
 // ======================================================================
@@ -90,8 +93,8 @@ struct WyuSmem {
   static constexpr size_t AT = TI + 16384;         // A, then T in place: [64][kLD] fp32
   static constexpr size_t E = AT + 64 * kLD * 4;   // g, eta, column factors, Gamma, beta (64 each)
   static constexpr size_t WS = E + 5 * 64 * 4;     // warp sums
-  static constexpr size_t BAR = WS + 16;           // 2 mbarriers
-  static constexpr size_t MISC = BAR + 16;         // tmem addr, abort flag
+  static constexpr size_t BAR = WS + 16;           // 3 mbarriers (the third only for the stall hook)
+  static constexpr size_t MISC = BAR + 32;         // tmem addr, abort flag
   static constexpr size_t TOTAL = MISC + 16 + 1024;
 };
 
@@ -126,11 +129,15 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   // sequential kernel launch and wait for this grid in hardware
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the call's status word starts clear (the grid is resident as a whole,
+  // so no CTA of it records a timeout a full wait limit before this runs)
+  if (blockIdx.x == 0 && tid == 0) atomicExch(a.status, 0u);
 
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
+    mbar_init(&bar[2], 1);
     fence_mbar_init();
   }
   if (SOLVE && warp == 0) {
@@ -141,6 +148,15 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = SOLVE ? *tmem_slot : 0u;
+  // failure-detection test hook: the first CTA waits, before it loads
+  // anything, on a barrier that nothing completes; the bounded wait runs
+  // out, the timeout is recorded and the CTA takes no item
+  if (a.stall && blockIdx.x == 0 && tid == 0 && !mbar_wait(&bar[2], 0, a.wait_ns)) {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  }
+  __syncthreads();
+  const int first_item = *abort_flag ? n_items : (int)blockIdx.x;
   // the tiles and gate inputs of an item are fetched while the previous item
   // finishes: TMA into the tile buffers once the products that read them are
   // done, lambda and beta into registers
@@ -166,9 +182,9 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   };
   float lam_n = 0.f, beta_n = 0.f;
   int64_t pos_n = 0;
-  if (blockIdx.x < n_items) fetch(blockIdx.x, lam_n, beta_n, pos_n);
+  if (first_item < n_items) fetch(first_item, lam_n, beta_n, pos_n);
   int it = 0;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+  for (int item = first_item; item < n_items; item += gridDim.x, ++it) {
   const int chunk = item % a.NC, bh = item / a.NC;
   const int next = item + gridDim.x;
   const int t_row = chunk * kC + tid;
@@ -191,7 +207,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
       bs[tid] = beta;
     }
   }
-  if (!mbar_wait(&bar[0], (uint32_t)(it & 1))) {
+  if (!mbar_wait(&bar[0], (uint32_t)(it & 1), a.wait_ns)) {
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
   }
@@ -293,7 +309,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
     continue;
   }
 
-  if (!aborted && !mbar_wait(&bar[1], 0)) {
+  if (!aborted && !mbar_wait(&bar[1], 0, a.wait_ns)) {
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
   }
@@ -445,7 +461,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
                 idesc_bf16(128, 2 * DK, false, true), ks > 0 ? 1u : 0u);
     umma_commit(&bar[1]);
   }
-  if (!aborted && !mbar_wait(&bar[1], 1)) {
+  if (!aborted && !mbar_wait(&bar[1], 1, a.wait_ns)) {
     *abort_flag = 1;
     atomicExch(a.status, kStatusTimeout);
   }
@@ -479,7 +495,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   }
   }  // items
   if (tid == 0) bulk_wait0();  // the last images are written
-  if (tid == 0 && issued > it) mbar_wait(&bar[0], (uint32_t)(it & 1));  // a load still in flight
+  if (tid == 0 && issued > it) mbar_wait(&bar[0], (uint32_t)(it & 1), a.wait_ns);  // a load still in flight
   tc_fence_before();
   __syncthreads();
   if (SOLVE && warp == 0) {
@@ -543,7 +559,6 @@ __global__ void __launch_bounds__(288, 1)
   const int bh = blockIdx.x, split = blockIdx.y;
   const int b = bh / a.H, h = bh % a.H;
   const int c0 = split * NV;  // first value channel of this CTA
-  const int NC = a.NC;
   auto stage = [&](int s) { return sm + L::ST0 + s * L::STAGE; };
   auto Xst = [&](int s) { return stage(s); };
   auto Qst = [&](int s) { return stage(s) + L::XSZ; };
@@ -560,7 +575,7 @@ __global__ void __launch_bounds__(288, 1)
       tma_load_4d(Xst(s) + k * 8192, &tm_k, &full[s], 64 * k, h, c * kC - a.shift, b);
       tma_load_4d(Qst(s) + k * 8192, &tm_q, &full[s], 64 * k, h, c * kC, b);
     }
-    const size_t ci = (size_t)bh * NC + c;
+    const size_t ci = (size_t)bh * a.NC + c;
     const uint8_t* img = a.ws_T + ci * kImg;  // W slabs | U slabs
     bulk_load(Ust(s), img + DK * 128 + (c0 / 64) * 8192, (uint32_t)L::VSZ, &full[s]);
     if (SOLVE) bulk_load(Wst(s), img, (uint32_t)L::WSZ, &full[s]);
@@ -583,6 +598,13 @@ __global__ void __launch_bounds__(288, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the per-chunk kernel has completed (and its writes are visible) past
+  // this wait; a timeout it recorded leaves its images incomplete: then no
+  // chunk is computed and no carry is written
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const bool upstream_failed = *reinterpret_cast<volatile uint32_t*>(a.status) != 0u;
+  if (upstream_failed) *abort_flag = 1;
+  const int NC = upstream_failed ? 0 : a.NC;
   // warp 8, lane 0 (tid 256) issues every load and product; warps 0..7 do
   // the epilogues and hold the state
   const bool issuer = tid == 256;
@@ -652,7 +674,7 @@ __global__ void __launch_bounds__(288, 1)
       issue_stage(c + 1, s ^ 1);
       ++issued[s ^ 1];
     }
-    if (!mbar_wait(&full[s], (c >> 1) & 1)) {
+    if (!mbar_wait(&full[s], (c >> 1) & 1, a.wait_ns)) {
       *abort_flag = 1;
       atomicExch(a.status, kStatusTimeout);
     }
@@ -709,7 +731,7 @@ __global__ void __launch_bounds__(288, 1)
       mma_chain_mn(tmem + L::COL_OA, kdesc<64>, sQ, mndesc, sS, DK, idesc_bf16(64, NV, false, true),
                    false);
     }
-    if ((lo && !mbar_wait(mbar_p, pph)) || (hi && SOLVE && !mbar_wait(mbar, mph))) {
+    if ((lo && !mbar_wait(mbar_p, pph, a.wait_ns)) || (hi && SOLVE && !mbar_wait(mbar, mph, a.wait_ns))) {
       *abort_flag = 1;
       atomicExch(a.status, kStatusTimeout);
     }
@@ -764,7 +786,7 @@ __global__ void __launch_bounds__(288, 1)
       umma_commit(mbar);
       ++n_mc;
       if (c + 1 < NC) {  // the next chunk's P = Q X^T: its stage is loaded, its buffer free
-        if (!mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1))) {
+        if (!mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1), a.wait_ns)) {
           *abort_flag = 1;
           atomicExch(a.status, kStatusTimeout);
         } else {
@@ -776,7 +798,7 @@ __global__ void __launch_bounds__(288, 1)
         }
       }
     }
-    if (warp < 8 && !mbar_wait(mbar, mph)) {
+    if (warp < 8 && !mbar_wait(mbar, mph, a.wait_ns)) {
       *abort_flag = 1;
       atomicExch(a.status, kStatusTimeout);
     }
@@ -831,11 +853,11 @@ __global__ void __launch_bounds__(288, 1)
   } else if (issuer) {
     // drain the loads still in flight before the shared memory goes away
     for (int s = 0; s < 2; ++s)
-      if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1));
+      if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), a.wait_ns);
   }
   if (issuer) {  // no product may still write TMEM when it is freed (the abort path)
-    if (n_pc > 0) mbar_wait(mbar_p, (uint32_t)((n_pc - 1) & 1));
-    if (n_mc > 0) mbar_wait(mbar, (uint32_t)((n_mc - 1) & 1));
+    if (n_pc > 0) mbar_wait(mbar_p, (uint32_t)((n_pc - 1) & 1), a.wait_ns);
+    if (n_mc > 0) mbar_wait(mbar, (uint32_t)((n_mc - 1) & 1), a.wait_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -909,7 +931,6 @@ __global__ void __launch_bounds__(288, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x;
   const int b = bh / a.H, h = bh % a.H;
-  const int NC = a.NC;
   auto stage = [&](int s) { return sm + s * L::STAGE; };
   auto fail = [&]() {
     *abort_flag = 1;
@@ -946,6 +967,13 @@ __global__ void __launch_bounds__(288, 1)
   const uint32_t tmem = *tmem_slot;
   const int quad = warp & 3;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+  // the per-chunk kernel has completed (and its writes are visible) past
+  // this wait; a timeout it recorded leaves its images incomplete: then no
+  // chunk is computed and no carry is written
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const bool upstream_failed = *reinterpret_cast<volatile uint32_t*>(a.status) != 0u;
+  if (upstream_failed) *abort_flag = 1;
+  const int NC = upstream_failed ? 0 : a.NC;
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -957,10 +985,10 @@ __global__ void __launch_bounds__(288, 1)
       int c = 0;
       for (; c < NC; ++c) {
         const int s = c % NST;
-        if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1))) { fail(); break; }
+        if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1), a.wait_ns)) { fail(); break; }
         if (*abort_flag) break;
         uint8_t* st = stage(s);
-        const size_t ci = (size_t)bh * NC + c;
+        const size_t ci = (size_t)bh * a.NC + c;
         mbar_arrive_expect_tx(&full[s], L::TX);
         tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - a.shift, b);
         tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
@@ -970,7 +998,7 @@ __global__ void __launch_bounds__(288, 1)
       }
       if (*abort_flag) {  // drain the loads still in flight
         for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
-          mbar_wait(&full[cc % NST], (uint32_t)((cc / NST) & 1));
+          mbar_wait(&full[cc % NST], (uint32_t)((cc / NST) & 1), a.wait_ns);
       }
     }
   } else if (warp >= 4) {
@@ -981,7 +1009,7 @@ __global__ void __launch_bounds__(288, 1)
     uint32_t fph = 0;
     for (int c = 0; c < NC; ++c) {
       const int s = c % NST;
-      if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
+      if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
       uint8_t* st = stage(s);
       const float* gt = reinterpret_cast<const float*>(st + L::GO);
       const bool carried = c == 0 && a.kprev_in && a.shift;  // x_0 = the carried key
@@ -1046,7 +1074,7 @@ __global__ void __launch_bounds__(288, 1)
         const int J = 2 * half + J2;
         f[J2] = J > I ? __expf(gl[16 * J] - gi) : (J == I && ratio_ok ? __fdividef(1.f, cfr) : 0.f);
       }
-      if (!mbar_wait(fmma, fph)) fail();
+      if (!mbar_wait(fmma, fph, a.wait_ns)) fail();
       fph ^= 1;
       tc_fence_after();
       {  // P~^T[r][t] = P[t][r] exp(g_t - g_r) for t >= r.  With cf_t = exp(g_t - g_{16 J(t)}):
@@ -1151,14 +1179,14 @@ __global__ void __launch_bounds__(288, 1)
     uint32_t b1ph = 0;
     for (int c = 0; c < NC; ++c) {
       const int s = c % NST, p = c & 1;
-      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1))) fail();
+      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
       tc_fence_after();
       uint8_t* st = stage(s);
       if (named_bar_any(3, 64, *abort_flag != 0)) break;
       const float gl_ = reinterpret_cast<const float*>(st + L::GO)[L::G_GAM + 63];
       if (tid == 0) {
         // the output warps are done with this TMEM buffer (chunk c - 2)
-        if (c >= 2 && !mbar_wait(&odone[p], (uint32_t)(((c - 2) >> 1) & 1))) fail();
+        if (c >= 2 && !mbar_wait(&odone[p], (uint32_t)(((c - 2) >> 1) & 1), a.wait_ns)) fail();
         tc_fence_after();
         // [D1 ; Oa] = [W ; Q] S0
         const uint32_t sA1 = smem_u32(st + L::WO);
@@ -1174,7 +1202,7 @@ __global__ void __launch_bounds__(288, 1)
         uint4 uu[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) uu[j] = *reinterpret_cast<const uint4*>(st + L::UO + sw128(r, 8 * j));
-        if (!mbar_wait(b1mma, b1ph)) fail();
+        if (!mbar_wait(b1mma, b1ph, a.wait_ns)) fail();
         tc_fence_after();
         uint32_t d1[2][32];
         tmem_ld32(tmem + lane_off + L::col_b1(p), d1[0]);
@@ -1206,8 +1234,8 @@ __global__ void __launch_bounds__(288, 1)
                     idesc_bf16(128, 64, true, true), ks > 0 ? 1u : 0u);
         umma_commit(&b2mma[p]);
       }
-      bool okb = mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1));
-      if (!SOLVE) okb = mbar_wait(b1mma, b1ph ^ 1) && okb;
+      bool okb = mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1), a.wait_ns);
+      if (!SOLVE) okb = mbar_wait(b1mma, b1ph ^ 1, a.wait_ns) && okb;
       if (!okb) fail();
       tc_fence_after();
       if (tid == 0) mbar_arrive(&empty[s]);  // the chain reads nothing more of this stage
@@ -1237,13 +1265,13 @@ __global__ void __launch_bounds__(288, 1)
     const int r = 32 * (warp - 2) + lane;
     for (int c = 0; c < NC; ++c) {
       const int s = c % NST, p = c & 1;
-      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1))) fail();
+      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
       if (named_bar_any(4, 64, *abort_flag != 0)) break;
       // Gamma_t, times 1 / |q_t| when the products saw raw queries (phi(q) in the prologue)
       const float* gq = reinterpret_cast<const float*>(stage(s) + L::GO);
       const float gr = L2N ? gq[L::G_GAM + r] * gq[L::G_SQ + r] : gq[L::G_GAM + r];
       mbar_arrive(&empty[s]);  // this thread reads nothing more of the stage
-      if (!mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1))) fail();  // both products of the chunk
+      if (!mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1), a.wait_ns)) fail();  // both products of the chunk
       tc_fence_after();
       uint8_t* Ost = sm + L::OST + p * 8192;
       if (tid == 64) bulk_wait_read1();  // the tile stored from this buffer two chunks ago is out
@@ -1433,6 +1461,8 @@ int launch_tc_chunk(const FwdArgs& fa) {
   ta.status = reinterpret_cast<uint32_t*>(ws + w.status);
   ta.NV = 64;
   ta.pro = fa.dk == 64 ? fa.prologue : 0;  // fused into the d = 64 kernels (else applied before)
+  ta.wait_ns = wait_limit_ns();
+  ta.stall = take_test_stall() ? 1 : 0;
   const bool solve = fa.variant == FALCON_1;
   if (fa.dk == 64) return solve ? launch_t<64, 64, true>(fa, ta) : launch_t<64, 64, false>(fa, ta);
   return solve ? launch_t<128, 64, true>(fa, ta) : launch_t<128, 64, false>(fa, ta);

@@ -557,6 +557,8 @@ int launch_f2_t(const FwdArgs& fa, const F2Args& ta) {
   const size_t smem = F2Smem<DK>::TOTAL;
   if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
   dim3 grid(fa.B * fa.H, fa.dv / 64);
+  // the call's status word starts clear; a bounded wait that runs out sets it
+  if (cudaMemsetAsync(ta.status, 0, sizeof(uint32_t), fa.stream) != cudaSuccess) return FALCON_ERR_CUDA;
   record_event(fa, 0);
   k<<<grid, 256, smem, fa.stream>>>(mk, mq, mv, mb, mo, ta);
   record_event(fa, 1);

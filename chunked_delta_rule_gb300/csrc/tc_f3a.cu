@@ -460,6 +460,8 @@ int launch_tc_f3a(const FwdArgs& fa) {
   auto k = tc_f3a_kernel;
   const size_t smem = F3aSmem::TOTAL;
   if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
+  // the call's status word starts clear; a bounded wait that runs out sets it
+  if (cudaMemsetAsync(ta.status, 0, sizeof(uint32_t), fa.stream) != cudaSuccess) return FALCON_ERR_CUDA;
   record_event(fa, 0);
   k<<<fa.B * fa.H, F3aSmem::kThreads, smem, fa.stream>>>(mq, mk, mv, mo, ta);
   record_event(fa, 1);

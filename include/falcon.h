@@ -203,15 +203,19 @@ int falcon_chunk_fwd_timed(const falcon_params_t* p, const void* q, const void* 
  * image, held by every device that loads the library until the process
  * exits.  The call itself allocates nothing (no cudaMalloc/cudaFree).
  * Covered: Falcon-1 and Falcon-1A with prologue 0 on the tensor-core path (bf16,
- * d_k = d_v in {64, 128}, chunk 64; see falcon_chunk_fwd_plan) needing at most
- * 32 MiB of scratch, i.e. B * H * ceil(T / 64) <= 1927.  Larger problems
- * return FALCON_ERR_WORKSPACE, other shapes FALCON_ERR_UNSUPPORTED (they
- * need no workspace: call falcon_chunk_fwd with workspace = NULL).
- * The first call on a device looks up the array's device address (which may
- * also load the library's device code there); make that first call before
- * any stream capture.  All calls share the one array: calls that overlap on
- * the GPU (other streams, other host threads) race and must be serialised
- * by the caller.  Arguments, outputs and other errors as falcon_chunk_fwd. */
+ * d_k = d_v in {64, 128}, chunk 64; see falcon_chunk_fwd_plan) whose
+ * falcon_workspace_size is at most 32 MiB: B * H * ceil(T / 64) <= 1927 at
+ * d = 64 (17 KB of scratch per chunk) and <= 992 at d = 128 (33 KB per
+ * chunk).  Larger problems return FALCON_ERR_WORKSPACE, other shapes
+ * FALCON_ERR_UNSUPPORTED (they need no workspace: call falcon_chunk_fwd with
+ * workspace = NULL).  Both are found on the host before anything is enqueued.
+ * Every call looks up the array's device address (the first call on a
+ * device may also load the library's device code there); make that first
+ * call before any stream capture.  All calls share the one array: calls that
+ * overlap on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller.  The status of the last call is read with
+ * falcon_workspace_status(NULL, stream).  Arguments, outputs and other
+ * errors as falcon_chunk_fwd. */
 int falcon_chunk_fwd_noalloc(const falcon_params_t* p, const void* q, const void* k,
                              const void* v, const float* beta, const float* lambda,
                              const falcon_carry_t* carry_in, void* o, falcon_carry_t* carry_out,
@@ -306,6 +310,37 @@ int falcon_backward(const falcon_params_t* p, const void* q, const void* k, cons
                     const void* dO, const float* dS_final, void* dq, void* dk, void* dv,
                     float* dbeta, float* dlambda, float* dS_in, void* dk_prev, void* workspace,
                     size_t workspace_bytes, void* stream);
+
+/* Status of the last tensor-core chunk forward that used `workspace`
+ * (falcon_chunk_fwd_plan reports FALCON_IMPL_TC for it; falcon_chunk_fwd,
+ * _timed, _varlen), or, with workspace == NULL, of the last
+ * falcon_chunk_fwd_noalloc call on the current device.  The pages have no
+ * counterpart: this is the library's failure detection.  Every wait of
+ * those kernels on another warp, a copy or a product is bounded in time
+ * (2 s); a wait that runs out makes its kernel record a timeout in the
+ * status word (the first 4 bytes of the workspace), skip its remaining
+ * chunks, wait for its own copies in flight, free its tensor memory and
+ * return, and the kernels after it in the call compute nothing.  The call
+ * itself returned FALCON_OK before the kernels ran, so this is how the
+ * caller learns of it.  Each such call clears the word when it starts.
+ * The function synchronises `stream` (the call's stream), reads the word
+ * and clears it.  Returns FALCON_OK, FALCON_ERR_TIMEOUT (the outputs and
+ * carry of that call are incomplete), FALCON_ERR_WORKSPACE (workspace not
+ * 256-byte aligned) or FALCON_ERR_CUDA.  Other kernel families have no
+ * device-side waits and do not write the word. */
+int falcon_workspace_status(const void* workspace, void* stream);
+
+/* Test hook of the failure-detection path (no counterpart on the pages; not
+ * for production use).  wait_limit_ns > 0 sets the limit of the bounded
+ * device-side waits of the Falcon-1 / 1A tensor-core kernels launched from
+ * now on in this process (0 restores 2 s).  stall != 0 makes the next such
+ * call's per-chunk kernel wait once, before it loads anything, on a barrier
+ * that nothing completes: that wait runs out after the limit, the timeout is
+ * recorded as described at falcon_workspace_status and the call's later
+ * kernels skip their work.  No fault, trap or unbounded wait is involved;
+ * the CUDA context stays usable.  Process-wide; not thread-safe against
+ * concurrent calls that should not see it. */
+void falcon_test_hooks(uint64_t wait_limit_ns, int32_t stall);
 
 /* Static description of an error code (never NULL). */
 const char* falcon_strerror(int code);
