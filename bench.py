@@ -167,29 +167,96 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def cpu_baseline(w, budget_s=20.0) -> dict:
-    """The oracle as it stands (fp64 token-by-token recurrence) on a bounded
-    sample of the workload: the first sequences, all heads, all tokens."""
-    import numpy as np
-
+def _oracle_task(task):
+    """One oracle run (fp64 numpy recurrence) on a slice of the inputs; runs
+    in a worker process."""
+    x, variant, window, eps, eps_gamma, pairing = task
     import oracle
+    oracle.recurrent(**x, variant=variant, window=window, eps=eps, eps_gamma=eps_gamma,
+                     pairing=pairing)
+    return x["q"].shape[0] * x["q"].shape[1]
+
+
+def _oracle_import(_):
+    """Worker warm-up: import the oracle (and numpy) before anything is timed."""
+    import oracle  # noqa: F401
+    return os.getpid()
+
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+class OraclePool:
+    """The oracle over all host cores: one single-threaded worker process per
+    core (spawned, so no CUDA state is inherited), the workload split by
+    sequence and head so every core has work."""
+
+    def __init__(self):
+        import multiprocessing as mp
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"   # workers inherit it: one thread each
+        self.cores = os.cpu_count() or 1
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+        self.pool.map(_oracle_import, range(4 * self.cores), chunksize=1)
+
+    def tasks(self, w, x):
+        """Split [B, T, H, ...] inputs into about `cores` (sequence, head group) slices."""
+        B, H = x["q"].shape[0], x["q"].shape[2]
+        groups = max(1, min(H, -(-self.cores // B)))
+        bounds = [(H * g) // groups for g in range(groups + 1)]
+        out = []
+        for b in range(B):
+            for g in range(groups):
+                h0, h1 = bounds[g], bounds[g + 1]
+                sl = {k: v[b:b + 1, :, h0:h1] for k, v in x.items()}
+                out.append((sl, w.variant, w.window, w.eps, w.eps_gamma, w.pairing))
+        return out
+
+    def run(self, tasks) -> float:
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_task, tasks, chunksize=1)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(w, budget_s=20.0) -> dict:
+    """The oracle as it stands (fp64 token-by-token recurrence) over every
+    host core on the whole workload (all sequences, heads and tokens),
+    repeated while the budget lasts."""
     from workloads import make_inputs
-    nb = 1
-    x = {k: v.double().numpy() for k, v in make_inputs(w.with_(B=nb)).items()}
-    t0 = time.perf_counter()
-    oracle.recurrent(**x, variant=w.variant, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma,
-                     pairing=w.pairing)
-    dt = time.perf_counter() - t0
-    reps = 1
-    while time.perf_counter() - t0 < min(budget_s, 5 * dt) and reps < 3:
-        oracle.recurrent(**x, variant=w.variant, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma,
-                     pairing=w.pairing)
-        reps += 1
-    dt = (time.perf_counter() - t0) / reps
-    del np
-    return {"value": nb * w.T / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{nb} of {w.B} sequences x {w.T} tokens x {w.H} heads, fp64 numpy "
-                      f"recurrence, {reps} run(s), single thread"}
+    x = {k: v.double().numpy() for k, v in make_inputs(w).items()}
+    pool = OraclePool()
+    try:
+        tasks = pool.tasks(w, x)
+        times = [pool.run(tasks)]
+        while sum(times) < budget_s / 2 and len(times) < 5:
+            times.append(pool.run(tasks))
+    finally:
+        pool.close()
+    dt = statistics.median(times)
+    return {"value": w.B * w.T / dt, "unit": "tokens/s", "cores": pool.cores, "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": f"the whole workload ({w.B} sequences x {w.T} tokens x {w.H} heads), fp64 numpy "
+                      f"recurrence, {len(tasks)} (sequence, head group) tasks on {pool.cores} "
+                      f"single-threaded worker processes, median of {len(times)} run(s)"}
 
 
 def traffic_for(kernel: str):
@@ -212,33 +279,57 @@ def traffic_for(kernel: str):
 
 
 def run_reference(args, w, rank):
+    """The reference arm: the oracle, as it stands, over every host core.
+    Each step runs a bounded sample of the workload (the first sequences'
+    first tokens, all heads), sized so that the whole run stays within about
+    two minutes of CPU time; the throughput is the sample's tokens over its
+    time."""
     if rank != 0:
         return
-    import oracle
     from workloads import make_inputs
-    nb, T = 1, min(w.T, 512)
-    x = {k: v.double().numpy() for k, v in make_inputs(w.with_(B=nb, T=T)).items()}
-    for _ in range(args.warmup):
-        oracle.recurrent(**x, variant=w.variant, window=w.window, pairing=w.pairing)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.recurrent(**x, variant=w.variant, window=w.window, pairing=w.pairing)
-    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    pool = OraclePool()
+    try:
+        full = {k: v.double().numpy() for k, v in make_inputs(w).items()}
+        per_step = 90.0 / max(args.steps + args.warmup, 1)   # seconds of wall time per step
+        Tp = min(w.T, 128)
+        t_seq = pool.run(pool.tasks(w, {k: v[:1, :Tp] for k, v in full.items()})) / Tp  # s per token
+        busy = min(w.H, pool.cores) / pool.cores   # share of the cores one sequence keeps busy
+        if t_seq * w.T * w.B * busy <= per_step:   # the whole workload fits in a step
+            nb, T = w.B, w.T
+        else:
+            nb, T = 1, int(max(16, min(w.T, per_step / max(t_seq, 1e-9))))
+        x = {k: v[:nb, :T] for k, v in full.items()}
+        tasks = pool.tasks(w, x)
+        for _ in range(args.warmup):
+            pool.run(tasks)
+        times = [pool.run(tasks) for _ in range(args.steps)]
+    finally:
+        pool.close()
+    dt = statistics.mean(times)
     value = nb * T / dt
     line = {"impl": "reference", "metric": METRIC, "value": value,
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                       "chunk": w.chunk, "variant": VARIANT_NAMES[w.variant], "global_batch": w.B * args.gpus,
-                       "seq_len": w.T, "parallelism": f"replicas x{args.gpus}",
-                       "reference_sample": f"{nb}x{T}x{w.H}"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{nb} sequence x {T} tokens x {w.H} heads per step, fp64 "
-                                       "numpy recurrence, single thread"},
+            "config": bench_config(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": pool.cores, "kind": "oracle",
+                             "cpu": cpu_model(),
+                             "sample": f"per step {nb} of {w.B} sequences x the first {T} of {w.T} tokens "
+                                       f"x {w.H} heads, fp64 numpy recurrence, {len(tasks)} tasks on "
+                                       f"{pool.cores} single-threaded worker processes"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def bench_config(w, world, n_sets=N_SETS, abytes=None, prologue=False) -> dict:
+    """The workload description shared by both arms' JSON lines."""
+    cfg = {"workload": w.name + ("_prologue" if prologue else ""), "B": w.B, "T": w.T, "H": w.H,
+           "dk": w.dk, "dv": w.dv, "chunk": w.chunk, "variant": VARIANT_NAMES[w.variant],
+           "global_batch": w.B * world, "seq_len": w.T, "parallelism": f"replicas x{world}"}
+    if abytes is not None:
+        cfg["l2"] = f"rotating {n_sets} input sets ({n_sets * abytes / 1e6:.0f} MB)"
+    return cfg
 
 
 def run_decode(args):
@@ -566,8 +657,10 @@ def main():
     dev_in = [{k: torch.empty_like(v) for k, v in sets[0].items()} for _ in range(2)]
     o_dev = [o, torch.empty_like(o)]
     o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    carry_dev = [carry, F.empty_carry(p, dev)]
+    S_host = [torch.empty(carry["S"].shape, dtype=torch.float32, pin_memory=True) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = o.numel() * o.element_size()
+    d2h = o.numel() * o.element_size() + carry["S"].numel() * 4   # outputs and the final state
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of set j on the device
     ev_used = [torch.cuda.Event() for _ in range(2)]  # the call on set j is done
@@ -583,12 +676,13 @@ def main():
         stream.wait_event(ev_in[j])
         stream.wait_event(ev_out[j])
         x = dev_in[j]
-        F.falcon_chunk_fwd(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o_dev[j], carry, ws, ws_n,
-                           stream)
+        F.falcon_chunk_fwd(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], None, o_dev[j], carry_dev[j],
+                           ws, ws_n, stream)
         ev_used[j].record(stream)
         s_d2h.wait_event(ev_used[j])
         with torch.cuda.stream(s_d2h):
             o_host[j].copy_(o_dev[j], non_blocking=True)
+            S_host[j].copy_(carry_dev[j]["S"], non_blocking=True)
         ev_out[j].record(s_d2h)
 
     for i in range(3):
@@ -658,11 +752,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
             "data": "synthetic",
-            "config": {"workload": w.name + ("_prologue" if args.prologue else ""), "B": w.B, "T": w.T,
-                       "H": w.H, "dk": w.dk, "dv": w.dv,
-                       "chunk": w.chunk, "variant": VARIANT_NAMES[w.variant], "global_batch": w.B * world,
-                       "seq_len": w.T, "parallelism": f"replicas x{world}",
-                       "l2": f"rotating {len(sets)} input sets ({len(sets) * abytes / 1e6:.0f} MB)"},
+            "config": bench_config(w, world, len(sets), abytes, args.prologue),
             "roofline": dict(roof, traffic=traffic_for(kernel), kernel=kernel,
                              algorithmic_bytes=abytes, algorithmic_flops=algorithmic_flops(w),
                              kernel_algorithmic_bytes=kbytes[dom], step_achieved=step_achieved,
