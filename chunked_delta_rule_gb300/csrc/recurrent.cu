@@ -374,6 +374,152 @@ __global__ void __launch_bounds__(NT, D == 64 ? 8 : 1) recurrent_step_vec_kernel
   if (tid == 0) a.pos_out[bhi] = pos + 1;
 }
 
+// Column-per-thread variant for d_k = d_v = 64: one CTA of 64 threads per
+// (b, h), thread j holding the state's value column S[:, j] in 64 registers.
+// Its 64 loads are one 128-byte row slice per warp each (coalesced), issued
+// before anything else; S^T x_j and S^T q are then sums over the thread's own
+// registers (the window keys and the query broadcast from shared memory), so
+// no reduction over the state crosses threads.  The only block-wide step is
+// staging the few input rows (one barrier); the dot products of the inputs
+// (x_j . q, |x_j|^2, the phi scales) are formed by each warp on its own.
+template <typename Tin, int MAXW>
+__global__ void __launch_bounds__(64, 8) recurrent_step_col_kernel(FwdArgs a) {
+  constexpr int D = 64;
+  __shared__ __align__(16) float xw[MAXW][D];  // window keys, oldest first; the last is the current pair
+  __shared__ __align__(16) float qv[D];
+  __shared__ float kr[D];                      // the current raw key
+  const int j = threadIdx.x, lane = j & 31;
+  const size_t bhi = blockIdx.x;
+  const int W = a.W, Wr = W - 1;
+  float* Sg = a.S_out + bhi * D * D + j;  // column j, rows r at r * D (in place)
+  float s[D];
+#pragma unroll
+  for (int r = 0; r < D; ++r) s[r] = Sg[r * D];
+
+  const int64_t pos = a.pos_out[bhi];
+  const Tin* kin = reinterpret_cast<const Tin*>(a.k) + bhi * D;
+  const float qraw = to_f32(reinterpret_cast<const Tin*>(a.q)[bhi * D + j]);
+  const float kraw = to_f32(kin[j]);
+  float vv[MAXW];  // this column's entry of each window value
+  const float vcur = to_f32(reinterpret_cast<const Tin*>(a.v)[bhi * D + j]);  // the current pair's
+#pragma unroll
+  for (int w = 0; w < MAXW; ++w) {
+    if (w >= W) break;
+    const int64_t p = pos - Wr + w;
+    float x = 0.f, v = 0.f;
+    if (p >= a.shift) {
+      if (w == Wr) {
+        x = a.shift ? to_f32(reinterpret_cast<const Tin*>(a.kprev_out)[bhi * D + j]) : kraw;
+        v = vcur;
+      } else {
+        const size_t o = (bhi * Wr + ring_slot(p, Wr)) * D + j;
+        x = to_f32(reinterpret_cast<const Tin*>(a.winx_out)[o]);
+        v = to_f32(reinterpret_cast<const Tin*>(a.winv_out)[o]);
+      }
+    }
+    xw[w][j] = x;
+    vv[w] = v;
+  }
+  qv[j] = qraw;
+  kr[j] = kraw;
+  __syncthreads();
+  // per-warp sums over all 64 entries: lane l takes entries l and l + 32
+  auto wsum = [&](float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+  };
+  float sq = 1.f, sk = 1.f;  // phi scales (prologue), 1 otherwise
+  if (a.prologue & FALCON_PROLOGUE_L2NORM_QK) {
+    const float q0 = qv[lane], q1 = qv[lane + 32], k0 = kr[lane], k1 = kr[lane + 32];
+    sq = 1.f / fmaxf(sqrtf(wsum(q0 * q0 + q1 * q1)), 1e-12f);
+    sk = 1.f / fmaxf(sqrtf(wsum(k0 * k0 + k1 * k1)), 1e-12f);
+  }
+  // the current key enters the window as phi(k) under same-step pairing
+  const float xsc_cur = a.shift ? 1.f : sk;
+  float xq[MAXW], n = 0.f, e = 0.f;
+#pragma unroll
+  for (int w = 0; w < MAXW; ++w) {
+    if (w >= W) break;
+    const float sc = (w == Wr) ? xsc_cur : 1.f;
+    const float x0 = sc * xw[w][lane], x1 = sc * xw[w][lane + 32];
+    xq[w] = sq * wsum(x0 * qv[lane] + x1 * qv[lane + 32]);
+    const bool ok = pos - Wr + w >= a.shift;
+    n += ok ? 1.f : 0.f;
+    e += ok ? wsum(x0 * x0 + x1 * x1) : 0.f;
+  }
+  const float gamma = gate_gamma(a.lam[bhi], a.eps_gamma, a.prologue);
+  float cf = 0.f;  // eta / n for this column
+  if (n > 0.f) {
+    const float bt = gate_beta(variant_per_channel(a.variant) ? a.beta[bhi * D + j] : a.beta[bhi], a.prologue);
+    cf = bt / (a.eps + e / n) / n;
+  }
+  // S^T q and, for the regression variants, S^T x_w: this column's sums
+  const bool additive = variant_additive(a.variant);
+  float c = 0.f;
+#pragma unroll
+  for (int r = 0; r < D; r += 4) {
+    const float4 q4 = *reinterpret_cast<const float4*>(&qv[r]);
+    c = fmaf(s[r], q4.x, c); c = fmaf(s[r + 1], q4.y, c); c = fmaf(s[r + 2], q4.z, c); c = fmaf(s[r + 3], q4.w, c);
+  }
+  c *= sq;
+  float dl[MAXW];
+  float o = gamma * c;
+#pragma unroll
+  for (int w = 0; w < MAXW; ++w) {
+    if (w >= W) break;
+    float r_w = vv[w];
+    if (!additive) {
+      float aw = 0.f;
+#pragma unroll
+      for (int r = 0; r < D; r += 4) {
+        const float4 x4 = *reinterpret_cast<const float4*>(&xw[w][r]);
+        aw = fmaf(s[r], x4.x, aw); aw = fmaf(s[r + 1], x4.y, aw);
+        aw = fmaf(s[r + 2], x4.z, aw); aw = fmaf(s[r + 3], x4.w, aw);
+      }
+      if (w == Wr) aw *= xsc_cur;
+      r_w -= gamma * aw;
+    }
+    const bool ok = pos - Wr + w >= a.shift;
+    dl[w] = ok ? cf * r_w : 0.f;
+    o = fmaf(xq[w], dl[w], o);
+  }
+  reinterpret_cast<Tin*>(a.o)[bhi * D + j] = from_f32<Tin>(o);
+  // S' = gamma S + sum_w x_w dl_w^T, column j, written back in place (the
+  // current key's row sits unscaled in shared memory: its scale goes to dl)
+#pragma unroll
+  for (int w = 0; w < MAXW; ++w)
+    if (w == Wr) dl[w] *= xsc_cur;
+#pragma unroll
+  for (int r = 0; r < D; r += 4) {
+    float4 acc = make_float4(gamma * s[r], gamma * s[r + 1], gamma * s[r + 2], gamma * s[r + 3]);
+#pragma unroll
+    for (int w = 0; w < MAXW; ++w) {
+      if (w >= W) break;
+      const float4 x4 = *reinterpret_cast<const float4*>(&xw[w][r]);
+      acc.x = fmaf(x4.x, dl[w], acc.x); acc.y = fmaf(x4.y, dl[w], acc.y);
+      acc.z = fmaf(x4.z, dl[w], acc.z); acc.w = fmaf(x4.w, dl[w], acc.w);
+    }
+    Sg[r * D] = acc.x;
+    Sg[(r + 1) * D] = acc.y;
+    Sg[(r + 2) * D] = acc.z;
+    Sg[(r + 3) * D] = acc.w;
+  }
+  // carry: ring push of the current pair, the new k_prev (phi(k) under the
+  // prologue), the position
+  const Tin kout = from_f32<Tin>((a.prologue & FALCON_PROLOGUE_L2NORM_QK) ? sk * kraw : kraw);
+  if (Wr > 0) {
+    const int slot = ring_slot(pos, Wr);
+    const bool ok = pos >= a.shift;
+    reinterpret_cast<Tin*>(a.winx_out)[(bhi * Wr + slot) * D + j] =
+        from_f32<Tin>(ok ? xsc_cur * xw[Wr][j] : 0.f);
+    reinterpret_cast<Tin*>(a.winv_out)[(bhi * Wr + slot) * D + j] = from_f32<Tin>(ok ? vcur : 0.f);
+  }
+  reinterpret_cast<Tin*>(a.kprev_out)[bhi * D + j] =
+      (a.prologue & FALCON_PROLOGUE_L2NORM_QK) ? kout : kin[j];
+  if (j == 0) a.pos_out[bhi] = pos + 1;
+}
+
 template <typename Tin, int EPT>
 int launch_rec(const FwdArgs& a) {
   const int RG = kRecThreads / a.dv;
@@ -416,7 +562,18 @@ int launch_rec_vec(const FwdArgs& a) {
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
 
+template <typename Tin>
+int launch_rec_col(const FwdArgs& a) {
+  if (a.W <= 1)
+    recurrent_step_col_kernel<Tin, 1><<<a.B * a.H, 64, 0, a.stream>>>(a);
+  else
+    recurrent_step_col_kernel<Tin, 8><<<a.B * a.H, 64, 0, a.stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
+}
+
 int launch_recurrent_step(const FwdArgs& a) {
+  if (a.dk == 64 && a.dv == 64 && a.W <= 8)
+    return a.dtype == FALCON_BF16 ? launch_rec_col<__nv_bfloat16>(a) : launch_rec_col<float>(a);
   if (a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.W <= 8) {
     int st;
     if (a.dk == 64)
