@@ -720,7 +720,7 @@ def main():
         elif w.variant == 5:  # Falcon-3A
             names = ["tc_f3a_kernel"]
         elif w.dk == 64:
-            names = ["tc_wyu_kernel", "tc_fwd_pipe_kernel"]
+            names = ["tc_wyu_kernel", "tc_fwd_chain_kernel"]
         else:
             names = ["tc_wyu_kernel", "tc_fwd_kernel"]
         kbytes = kernel_bytes(w, names)

@@ -25,9 +25,11 @@
 //      the fp32 state in registers: TMA and bulk copies bring the chunk's
 //      operands while earlier chunks compute; every contraction is a
 //      tcgen05 MMA with the accumulator in TMEM; the output tile leaves by
-//      TMA store.  d = 64 is warp-specialised (tc_fwd_pipe_kernel: producer,
-//      front, state chain and output warps); d = 128 (tc_fwd_kernel) has one
-//      warp that issues every load and product for eight epilogue warps.
+//      TMA store.  d = 64 runs in transition form (tc_fwd_chain_kernel:
+//      three front warpgroups form each chunk's state-independent operands
+//      [-M ; Q'] and [b ; P~ U] = [X~^T ; P~] [W | U], so the state chain is
+//      one product per chunk); d = 128 (tc_fwd_kernel) has one warp that
+//      issues every load and product for eight epilogue warps.
 //  The input prologue (phi = L2 normalisation of q and k, gates from logits)
 //  runs inside the d = 64 kernels when asked for.
 // The second kernel is launched to overlap the first one's tail (programmatic
@@ -868,65 +870,79 @@ __global__ void __launch_bounds__(288, 1)
 }
 
 // ----------------------------------------------------------------------
-// (b') pipelined sequential kernel, d_k = d_v = 64.  W, U and the gates of
-// every chunk come from the per-chunk kernel; four roles:
-//   warp 8      producer: TMA of chunk c into one of NST stages
-//   warps 4..7  front: P^T = X Q^T (an M = 64 product; each warp reads 16
-//               rows, its half-warps 32 columns each) -> decay-masked P~^T,
-//               and X~ = diag(exp(g_last - g)) X in place of X
-//   warps 0, 1  state chain: [D1 ; Oa] = [W ; Q] S0, Delta = U - D1,
-//               [D2 ; Ob] = [X~ | P~^T]^T Delta, S1 = Gamma_last S0 + D2
-//   warps 2, 3  outputs: O = diag(Gamma) Oa + Ob from the TMEM of the chunk
-//               the chain has just finished (two TMEM buffers), TMA store
-// The front works up to NST chunks ahead of the chain; the output warps run
-// one chunk behind it, off the chain's critical path.  Stage layout: X (then
-// X~) | P~^T | W | Q | U | gates, so that [W ; Q] and [X~ | P~^T] are single
-// operands.  Hand-offs are mbarriers: full/empty and
-// front-done per stage, product completions, output-done per TMEM buffer.
+// (b'') sequential kernel in transition form, d_k = d_v = 64.  With the
+// chunk's state-independent operands formed ahead of the chain,
+//   S1 = Gamma_last S0 + X~^T U - (X~^T W) S0 = Gamma_last S0 + b - M S0
+//   O  = (diag(Gamma) Q - P~ W) S0 + P~ U     = Q' S0 + P~ U
+// so the state chain carries ONE product per chunk, [-M ; Q'] S0 (M = 128,
+// N = 64, K = 64), accumulated onto [b ; P~ U], which a front product
+// [X~^T ; P~] [W | U] (M = 128, N = 128) left in TMEM: rows 0..63 of the
+// result are the next state less Gamma_last S0, rows 64..127 the chunk's
+// outputs.  Roles:
+//   warps 4..15   NF = 3 fronts of four warps, chunk c on front c % NF:
+//                 P^T = X Q^T -> P~^T (decay-masked) and X~ = diag(exp(g_last - g)) X,
+//                 then [X~^T ; P~] [W | U] into TMEM buffer c % 2; its rows
+//                 0..63 give -M, rows 64..127 (with the stage's Q) give Q',
+//                 both as bf16 rows of one 128-row K-major operand
+//   warps 0, 1    state chain: the product, then S1 = Gamma_last S0 + acc
+//   warps 2, 3    outputs: O = acc rows 64..127, TMA store
+// The fronts run up to two chunks ahead of the chain (two TMEM buffers and
+// operand tiles); the chain's round trip per chunk is one product and one
+// TMEM -> register -> shared-memory pass.  A front's own latency per chunk
+// (two products, each with its epilogue) is several times the chain's, so
+// three of them take turns.  Loads: the first NST chunks are issued at the
+// start, and the front that finishes chunk c refills its stage with chunk
+// c + NST (no producer warp: 16 warps keep 128 registers a thread).
 // ----------------------------------------------------------------------
 template <bool SOLVE, bool L2N>
-struct PipeSmem {
+struct ChainSmem {
   static constexpr int NST = 4;
   static constexpr size_t XO = 0, PO = 8192, WO = 16384, QO = 24576, UO = 32768, GO = 40960;
   static constexpr size_t STAGE = GO + (L2N ? 2048 : 1024);  // gates: Gamma, exp(g_last - g), g,
-                                                             // exp(g - g_block) (loaded), then phi's row scales
-  static constexpr size_t SB = NST * STAGE;          // S rows (MN-major B)
-  static constexpr size_t DL = SB + 8192;            // Delta rows (MN-major B)
-  static constexpr size_t OST = DL + 8192;           // two output staging tiles
-  static constexpr size_t BAR = OST + 2 * 8192;
-  static constexpr size_t MISC = BAR + 160;
-  static constexpr size_t TOTAL = MISC + 16 + 1024;
+                                                             // exp(g - g_block), then phi's row scales
+  static constexpr size_t AM = NST * STAGE;          // 2 x [-M ; Q']: 128 K-major bf16 rows
+  static constexpr size_t SB = AM + 2 * 16384;       // S rows (MN-major B)
+  static constexpr size_t OST = SB + 8192;           // two output staging tiles
+  static constexpr size_t GL = OST + 2 * 8192;       // Gamma_last of each TMEM buffer's chunk
+  static constexpr size_t BAR = GL + 16;
+  static constexpr size_t MISC = BAR + 256;          // tmem address, abort flag, loads issued per stage
+  static constexpr size_t TOTAL = MISC + 64 + 1024;
   static constexpr uint32_t TX = 2 * 8192 + (SOLVE ? 8192 : 0) + 8192 + 1024;
   static_assert(TOTAL <= 232448, "shared memory budget");
-  static_assert(STAGE % 1024 == 0, "1 KB aligned stages");
-  // TMEM: P^T (M = 64 layout) | per buffer p: [D1 ; Oa] at 64 + 128 p, [D2 ; Ob] at 128 + 128 p
-  static constexpr uint32_t COL_PT = 0, NCOLS = 512;
-  __host__ __device__ static constexpr uint32_t col_b1(int p) { return 64 + 128 * p; }
-  __host__ __device__ static constexpr uint32_t col_b2(int p) { return 128 + 128 * p; }
+  static_assert(STAGE % 1024 == 0 && AM % 1024 == 0, "1 KB aligned tiles");
+  static constexpr int NF = 3;                    // fronts
+  static constexpr int kThreads = 32 * (4 + 4 * NF);  // chain, outputs, fronts
+  // TMEM: P^T of front f (M = 64 layout) at 64 f; buffer p of the front product
+  // at 64 NF + 128 p (columns 0..63: [M ; P~ W], 64..127: [b ; P~ U], the
+  // chain's accumulator)
+  static constexpr uint32_t NCOLS = 512;
+  __host__ __device__ static constexpr uint32_t col_pt(int f) { return 64 * f; }
+  static_assert(64 * NF + 256 <= NCOLS, "TMEM budget");
+  __host__ __device__ static constexpr uint32_t col_f(int p) { return 64 * NF + 128 * p; }
   static constexpr int G_GAM = 0, G_DEC = 64, G_GL = 128, G_CF = 192;
-  static constexpr int G_SQ = 256, G_SX = 320;  // L2N: 1 / |q_t|, 1 / |x_r| (L2-normalised features)
+  static constexpr int G_SQ = 256, G_SX = 320;
 };
 
-// L2N: q and k are L2-normalised by the prologue; the raw rows enter the
-// products and the rows' inverse norms their epilogues.
 template <bool SOLVE, bool L2N>
-__global__ void __launch_bounds__(288, 1)
-    tc_fwd_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_o, TcArgs a) {
-  using L = PipeSmem<SOLVE, L2N>;
+__global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
+    tc_fwd_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_o, TcArgs a) {
+  using L = ChainSmem<SOLVE, L2N>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   constexpr int NST = L::NST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  uint64_t* full = bars;              // [NST]
-  uint64_t* empty = bars + NST;       // [NST]: the chain's thread 0 and the 64 output threads
-  uint64_t* fdone = bars + 2 * NST;   // [NST]
-  uint64_t* fmma = bars + 3 * NST;    // P^T done
-  uint64_t* b1mma = fmma + 1;         // [D1 ; Oa] done
-  uint64_t* b2mma = fmma + 2;         // [2]: [D2 ; Ob] of buffer p done
-  uint64_t* odone = fmma + 4;         // [2]: output warps finished buffer p
+  uint64_t* full = bars;              // [NST] stage loaded
+  constexpr int NF = L::NF;
+  uint64_t* fmma = bars + NST;        // [NF] P^T of front f done
+  uint64_t* f2mma = fmma + NF;        // [NF] front product of front f done
+  uint64_t* fdone = f2mma + NF;       // [2] operand tile and TMEM buffer p ready for the chain
+  uint64_t* cmma = fdone + 2;         // [2] chain product of buffer p done
+  uint64_t* tdone = cmma + 2;         // [2] chain and output warps read buffer p (128 arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+  int* issued = reinterpret_cast<int*>(sm + L::MISC + 8);  // [NST] loads issued into each stage
+  float* glast = reinterpret_cast<float*>(sm + L::GL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x;
@@ -941,19 +957,21 @@ __global__ void __launch_bounds__(288, 1)
     *abort_flag = 0;
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1 + 64);
-      mbar_init(&fdone[i], 128);
+      issued[i] = 0;
     }
-    mbar_init(fmma, 1);
-    mbar_init(b1mma, 1);
-    mbar_init(&b2mma[0], 1);
-    mbar_init(&b2mma[1], 1);
-    mbar_init(&odone[0], 64);
-    mbar_init(&odone[1], 64);
+    for (int f = 0; f < NF; ++f) {
+      mbar_init(&fmma[f], 1);
+      mbar_init(&f2mma[f], 1);
+    }
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(&fdone[p], 128);
+      mbar_init(&cmma[p], 1);
+      mbar_init(&tdone[p], 128);
+    }
     fence_mbar_init();
   }
-  if (!SOLVE) {  // additive write: the W rows of [W ; Q] stay zero
-    for (int i = tid; i < NST * 512; i += 288)
+  if (!SOLVE) {  // additive write: the W tiles stay zero, so M = 0 and Q' = diag(Gamma) Q
+    for (int i = tid; i < NST * 512; i += L::kThreads)
       *reinterpret_cast<uint4*>(stage(i >> 9) + L::WO + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
   }
   if (warp == 0) {
@@ -974,41 +992,35 @@ __global__ void __launch_bounds__(288, 1)
   const bool upstream_failed = *reinterpret_cast<volatile uint32_t*>(a.status) != 0u;
   if (upstream_failed) *abort_flag = 1;
   const int NC = upstream_failed ? 0 : a.NC;
+  // chunk c into stage c % NST (one thread; the stage's previous chunk is done)
+  auto load_chunk = [&](int c) {
+    const int s = c % NST;
+    uint8_t* st = stage(s);
+    const size_t ci = (size_t)bh * a.NC + c;
+    mbar_arrive_expect_tx(&full[s], L::TX);
+    tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - a.shift, b);
+    tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
+    if (SOLVE) bulk_load(st + L::WO, a.ws_T + ci * 16384, 8192, &full[s]);
+    bulk_load(st + L::UO, a.ws_T + ci * 16384 + 8192, 8192, &full[s]);
+    bulk_load(st + L::GO, a.ws_g + ci * kGateF, 1024, &full[s]);
+    atomicAdd(&issued[s], 1);
+  };
+  if (tid == 0) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    for (int c = 0; c < NST && c < NC; ++c) load_chunk(c);
+  }
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      // the per-chunk kernel's images and gates: wait until that grid has
-      // completed (a no-op when this grid was launched without overlap)
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      int c = 0;
-      for (; c < NC; ++c) {
-        const int s = c % NST;
-        if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1), a.wait_ns)) { fail(); break; }
-        if (*abort_flag) break;
-        uint8_t* st = stage(s);
-        const size_t ci = (size_t)bh * a.NC + c;
-        mbar_arrive_expect_tx(&full[s], L::TX);
-        tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - a.shift, b);
-        tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
-        if (SOLVE) bulk_load(st + L::WO, a.ws_T + ci * 16384, 8192, &full[s]);
-        bulk_load(st + L::UO, a.ws_T + ci * 16384 + 8192, 8192, &full[s]);
-        bulk_load(st + L::GO, a.ws_g + ci * kGateF, 1024, &full[s]);
-      }
-      if (*abort_flag) {  // drain the loads still in flight
-        for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
-          mbar_wait(&full[cc % NST], (uint32_t)((cc / NST) & 1), a.wait_ns);
-      }
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ front
-    const int ftid = tid - 128;
+  if (warp >= 4) {
+    // ------------------------------------------------------------ fronts
+    const int fr = (warp - 4) >> 2;          // this front; it takes the chunks c with c % NF == fr
+    const int ftid = tid - 128 - 128 * fr;
+    const int fbar = fr == 0 ? 1 : 4 + fr;   // its named barrier (3 and 4 are the chain's and the outputs')
     const int r = 16 * quad + (lane & 15);  // P^T row (key index) of this lane
     const int half = lane >> 4;             // P^T columns 32 half .. 32 half + 31
-    uint32_t fph = 0;
-    for (int c = 0; c < NC; ++c) {
-      const int s = c % NST;
+    uint32_t fph = 0, f2ph = 0;
+    int n_f2 = 0;  // front products issued (ftid 0's bookkeeping)
+    for (int c = fr; c < NC; c += NF) {
+      const int s = c % NST, p = c & 1;
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
       uint8_t* st = stage(s);
       const float* gt = reinterpret_cast<const float*>(st + L::GO);
@@ -1019,42 +1031,37 @@ __global__ void __launch_bounds__(288, 1)
                             // row and the key row r (the carried key is a feature already); the raw
                             // rows enter the products and the scales their epilogues
         float* gw = reinterpret_cast<float*>(st + L::GO);
-        float sq, sx;
-        {
-          float pq = 0.f, px = 0.f;
+        float pq = 0.f, px = 0.f;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 rq = *reinterpret_cast<const uint4*>(st + L::QO + sw128(r, 32 * half + 8 * j));
-            const uint4 rx = *reinterpret_cast<const uint4*>(st + L::XO + sw128(r, 32 * half + 8 * j));
-            const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&rq);
-            const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&rx);
+        for (int j = 0; j < 4; ++j) {
+          const uint4 rq = *reinterpret_cast<const uint4*>(st + L::QO + sw128(r, 32 * half + 8 * j));
+          const uint4 rx = *reinterpret_cast<const uint4*>(st + L::XO + sw128(r, 32 * half + 8 * j));
+          const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&rq);
+          const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&rx);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 q2 = __bfloat1622float2(hq[e]), x2 = __bfloat1622float2(hx[e]);
-              pq = fmaf(q2.x, q2.x, fmaf(q2.y, q2.y, pq));
-              px = fmaf(x2.x, x2.x, fmaf(x2.y, x2.y, px));
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float2 q2 = __bfloat1622float2(hq[e]), x2 = __bfloat1622float2(hx[e]);
+            pq = fmaf(q2.x, q2.x, fmaf(q2.y, q2.y, pq));
+            px = fmaf(x2.x, x2.x, fmaf(x2.y, x2.y, px));
           }
-          pq += __shfl_xor_sync(0xffffffffu, pq, 16);
-          px += __shfl_xor_sync(0xffffffffu, px, 16);
-          sq = 1.f / fmaxf(sqrtf(pq), 1e-12f);
-          sx = (carried && r == 0) ? 1.f : 1.f / fmaxf(sqrtf(px), 1e-12f);
         }
+        pq += __shfl_xor_sync(0xffffffffu, pq, 16);
+        px += __shfl_xor_sync(0xffffffffu, px, 16);
         if (half == 0) {
-          gw[L::G_SQ + r] = sq;
-          gw[L::G_SX + r] = sx;
+          gw[L::G_SQ + r] = 1.f / fmaxf(sqrtf(pq), 1e-12f);
+          gw[L::G_SX + r] = (carried && r == 0) ? 1.f : 1.f / fmaxf(sqrtf(px), 1e-12f);
         }
       }
       fence_proxy_async();
       tc_fence_before();
-      if (named_bar_any(1, 128, *abort_flag != 0)) break;
+      if (named_bar_any(fbar, 128, *abort_flag != 0)) break;
       tc_fence_after();
       if (ftid == 0) {  // P^T = X Q^T
         const uint32_t sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + L::COL_PT, kdesc<64>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(64, 64),
+          umma_bf16(tmem + L::col_pt(fr), kdesc<64>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(64, 64),
                     ks > 0 ? 1u : 0u);
-        umma_commit(fmma);
+        umma_commit(&fmma[fr]);
       }
       // the factors of this thread's 32 columns, gathered while the product runs
       const float* gl = gt + L::G_GL;
@@ -1074,13 +1081,13 @@ __global__ void __launch_bounds__(288, 1)
         const int J = 2 * half + J2;
         f[J2] = J > I ? __expf(gl[16 * J] - gi) : (J == I && ratio_ok ? __fdividef(1.f, cfr) : 0.f);
       }
-      if (!mbar_wait(fmma, fph, a.wait_ns)) fail();
+      if (!mbar_wait(&fmma[fr], fph, a.wait_ns)) fail();
       fph ^= 1;
       tc_fence_after();
       {  // P~^T[r][t] = P[t][r] exp(g_t - g_r) for t >= r.  With cf_t = exp(g_t - g_{16 J(t)}):
          // exp(g_t - g_r) = cf_t exp(g_{16 J} - g_r) across blocks and cf_t / cf_r inside one
         uint32_t pr[32];
-        tmem_ld16x2_32(tmem + lane_off + L::COL_PT, pr);
+        tmem_ld16x2_32(tmem + lane_off + L::col_pt(fr), pr);
         tmem_wait_ld();
         float pv[32];
 #pragma unroll
@@ -1139,10 +1146,61 @@ __global__ void __launch_bounds__(288, 1)
       }
       fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(&fdone[s]);
+      named_bar(fbar, 128);
+      tc_fence_after();
+      if (ftid == 0) {  // [X~^T ; P~] [W | U] into TMEM buffer p, once the chunk two back left it
+        if (c >= 2 && !mbar_wait(&tdone[p], (uint32_t)(((c - 2) >> 1) & 1), a.wait_ns)) {
+          fail();
+        } else {
+          tc_fence_after();
+          const uint32_t sA = smem_u32(st + L::XO), sB = smem_u32(st + L::WO);
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + L::col_f(p), sdesc_mn128_wide(sA + ks * 2048, 8192),
+                      sdesc_mn128_wide(sB + ks * 2048, 16384), idesc_bf16(128, 128, true, true),
+                      ks > 0 ? 1u : 0u);
+          umma_commit(&f2mma[fr]);
+          ++n_f2;
+        }
+      }
+      if (!mbar_wait(&f2mma[fr], f2ph, a.wait_ns)) fail();
+      f2ph ^= 1;
+      tc_fence_after();
+      if (named_bar_any(fbar, 128, *abort_flag != 0)) break;
+      {  // rows 0..63: -M -> tile rows 0..63; rows 64..127: Q' = diag(Gamma) Q - P~ W -> rows 64..127
+        const int row = 32 * quad + lane;   // TMEM lane of this thread
+        float mv[64];
+        tmem_ld64(tmem + lane_off + L::col_f(p), mv);
+        tmem_wait_ld();
+        uint8_t* AMp = sm + L::AM + p * 16384;
+        if (quad < 2) {
+#pragma unroll
+          for (int n = 0; n < 64; ++n) mv[n] = -mv[n];
+        } else {
+          const int t = row - 64;
+          const float gq = L2N ? gt[L::G_GAM + t] * gt[L::G_SQ + t] : gt[L::G_GAM + t];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(st + L::QO + sw128(t, 8 * j));
+            const __nv_bfloat162* pq2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 q2 = __bfloat1622float2(pq2[e]);
+              mv[8 * j + 2 * e] = fmaf(gq, q2.x, -mv[8 * j + 2 * e]);
+              mv[8 * j + 2 * e + 1] = fmaf(gq, q2.y, -mv[8 * j + 2 * e + 1]);
+            }
+          }
+        }
+        store_row64(AMp, row, mv);
+        if (ftid == 0) glast[p] = gt[L::G_GAM + 63];
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(&fdone[p]);
+      named_bar(fbar, 128);  // nothing of the stage is read after this: refill it
+      if (ftid == 0 && c + NST < NC && !*abort_flag) load_chunk(c + NST);
     }
     const bool ab = __any_sync(0xffffffffu, *abort_flag != 0);  // one answer per warp
-    if (a.kprev_out && !ab && ftid < 32) {  // the last key, as a feature (warp 4)
+    if (a.kprev_out && !ab && fr == 0 && ftid < 32) {  // the last key, as a feature (warp 4)
       const __nv_bfloat16* kl = a.k + (((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64;
       const float k0 = __bfloat162float(kl[ftid]), k1 = __bfloat162float(kl[ftid + 32]);
       float sc = 1.f;
@@ -1155,13 +1213,13 @@ __global__ void __launch_bounds__(288, 1)
       a.kprev_out[(size_t)bh * 64 + ftid] = __float2bfloat16_rn(k0 * sc);
       a.kprev_out[(size_t)bh * 64 + ftid + 32] = __float2bfloat16_rn(k1 * sc);
     }
-    if (a.pos_out && !*abort_flag && ftid == 0) a.pos_out[bh] = (a.pos_in ? a.pos_in[bh] : 0) + a.T;
+    if (a.pos_out && !*abort_flag && fr == 0 && ftid == 0) a.pos_out[bh] = (a.pos_in ? a.pos_in[bh] : 0) + a.T;
+    if (ftid == 0 && n_f2 > 0) mbar_wait(&f2mma[fr], (uint32_t)((n_f2 - 1) & 1), a.wait_ns);  // TMEM quiet
   } else if (warp < 2) {
     // ------------------------------------------------------------ state chain
-    // S rows 32 w + lane (lanes 0..63 of the stacked products)
     uint8_t* SB = sm + L::SB;
     const uint32_t sS = smem_u32(SB);
-    const int r = 32 * warp + lane;
+    const int r = 32 * warp + lane;  // S row = TMEM lane
     float sreg[64];
 #pragma unroll
     for (int n = 0; n < 64; ++n) sreg[n] = 0.f;
@@ -1176,82 +1234,38 @@ __global__ void __launch_bounds__(288, 1)
     store_row64(SB, r, sreg);
     fence_proxy_async();
     named_bar(3, 64);
-    uint32_t b1ph = 0;
+    int n_c = 0;  // chain products issued (thread 0's bookkeeping)
     for (int c = 0; c < NC; ++c) {
-      const int s = c % NST, p = c & 1;
-      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
+      const int p = c & 1;
+      if (!mbar_wait(&fdone[p], (uint32_t)((c >> 1) & 1), a.wait_ns)) fail();
       tc_fence_after();
-      uint8_t* st = stage(s);
       if (named_bar_any(3, 64, *abort_flag != 0)) break;
-      const float gl_ = reinterpret_cast<const float*>(st + L::GO)[L::G_GAM + 63];
-      if (tid == 0) {
-        // the output warps are done with this TMEM buffer (chunk c - 2)
-        if (c >= 2 && !mbar_wait(&odone[p], (uint32_t)(((c - 2) >> 1) & 1), a.wait_ns)) fail();
-        tc_fence_after();
-        // [D1 ; Oa] = [W ; Q] S0
-        const uint32_t sA1 = smem_u32(st + L::WO);
+      const float gl_ = glast[p];
+      if (tid == 0) {  // [b ; P~ U] += [-M ; Q'] S0
+        const uint32_t sA = smem_u32(sm + L::AM + p * 16384);
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + L::col_b1(p), kdesc<128>(sA1, ks), mndesc(sS, ks), idesc_bf16(128, 64, false, true),
-                    ks > 0 ? 1u : 0u);
-        umma_commit(b1mma);
+          umma_bf16(tmem + L::col_f(p) + 64, kdesc<128>(sA, ks), mndesc(sS, ks), idesc_bf16(128, 64, false, true),
+                    1u);
+        umma_commit(&cmma[p]);
+        ++n_c;
       }
-      // Delta = U - W S0; the additive write has W = 0 and feeds U to the
-      // second product directly
-      const uint32_t sDL = SOLVE ? smem_u32(sm + L::DL) : smem_u32(st + L::UO);
-      if (SOLVE) {
-        uint4 uu[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) uu[j] = *reinterpret_cast<const uint4*>(st + L::UO + sw128(r, 8 * j));
-        if (!mbar_wait(b1mma, b1ph, a.wait_ns)) fail();
-        tc_fence_after();
-        uint32_t d1[2][32];
-        tmem_ld32(tmem + lane_off + L::col_b1(p), d1[0]);
-        tmem_ld32(tmem + lane_off + L::col_b1(p) + 32, d1[1]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&uu[j]);
-          uint32_t pd[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int n = 8 * j + 2 * e;
-            const float2 u2 = __bfloat1622float2(pu[e]);
-            pd[e] = pack_bf16(u2.x - __uint_as_float(d1[n >> 5][n & 31]),
-                              u2.y - __uint_as_float(d1[(n + 1) >> 5][(n + 1) & 31]));
-          }
-          *reinterpret_cast<uint4*>(sm + L::DL + sw128(r, 8 * j)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        named_bar(3, 64);
-        tc_fence_after();
-      }
-      b1ph ^= 1;
-      if (tid == 0) {  // [D2 ; Ob] = [X~ | P~^T] Delta, A MN-major over two atoms
-        const uint32_t sA2 = smem_u32(st + L::XO);
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + L::col_b2(p), sdesc_mn128_wide(sA2 + ks * 2048, 8192), mndesc(sDL, ks),
-                    idesc_bf16(128, 64, true, true), ks > 0 ? 1u : 0u);
-        umma_commit(&b2mma[p]);
-      }
-      bool okb = mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1), a.wait_ns);
-      if (!SOLVE) okb = mbar_wait(b1mma, b1ph ^ 1, a.wait_ns) && okb;
-      if (!okb) fail();
+      if (!mbar_wait(&cmma[p], (uint32_t)((c >> 1) & 1), a.wait_ns)) fail();
       tc_fence_after();
-      if (tid == 0) mbar_arrive(&empty[s]);  // the chain reads nothing more of this stage
-      {  // S1 = Gamma_last S0 + D2
-        uint32_t d2[2][32];
-        tmem_ld32(tmem + lane_off + L::col_b2(p), d2[0]);
-        tmem_ld32(tmem + lane_off + L::col_b2(p) + 32, d2[1]);
-        tmem_wait_ld();
+      {  // S1 = Gamma_last S0 + acc, 32 columns at a time
 #pragma unroll
-        for (int n = 0; n < 64; ++n) sreg[n] = gl_ * sreg[n] + __uint_as_float(d2[n >> 5][n & 31]);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t d2[32];
+          tmem_ld32(tmem + lane_off + L::col_f(p) + 64 + 32 * hh, d2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int n = 0; n < 32; ++n) sreg[32 * hh + n] = fmaf(gl_, sreg[32 * hh + n], __uint_as_float(d2[n]));
+        }
+        tc_fence_before();
+        mbar_arrive(&tdone[p]);
         store_row64(SB, r, sreg);
       }
       fence_proxy_async();
-      tc_fence_before();
       named_bar(3, 64);
-      tc_fence_after();
     }
     if (!*abort_flag && a.S_out) {
       float* dst = a.S_out + ((size_t)bh * 64 + r) * 64;
@@ -1259,43 +1273,37 @@ __global__ void __launch_bounds__(288, 1)
       for (int n = 0; n < 64; n += 4)
         *reinterpret_cast<float4*>(dst + n) = make_float4(sreg[n], sreg[n + 1], sreg[n + 2], sreg[n + 3]);
     }
+    if (tid == 0 && n_c > 0) {  // TMEM quiet before it is freed
+      const int cl = n_c - 1;
+      mbar_wait(&cmma[cl & 1], (uint32_t)((cl >> 1) & 1), a.wait_ns);
+    }
   } else {
     // ------------------------------------------------------------ outputs
-    // rows 32 (w - 2) + lane (lanes 64..127 of the stacked products)
-    const int r = 32 * (warp - 2) + lane;
+    const int t = 32 * (warp - 2) + lane;  // output row = TMEM lane 64 + t
     for (int c = 0; c < NC; ++c) {
-      const int s = c % NST, p = c & 1;
-      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
-      if (named_bar_any(4, 64, *abort_flag != 0)) break;
-      // Gamma_t, times 1 / |q_t| when the products saw raw queries (phi(q) in the prologue)
-      const float* gq = reinterpret_cast<const float*>(stage(s) + L::GO);
-      const float gr = L2N ? gq[L::G_GAM + r] * gq[L::G_SQ + r] : gq[L::G_GAM + r];
-      mbar_arrive(&empty[s]);  // this thread reads nothing more of the stage
-      if (!mbar_wait(&b2mma[p], (uint32_t)((c >> 1) & 1), a.wait_ns)) fail();  // both products of the chunk
+      const int p = c & 1;
+      if (!mbar_wait(&cmma[p], (uint32_t)((c >> 1) & 1), a.wait_ns)) fail();
       tc_fence_after();
+      if (named_bar_any(4, 64, *abort_flag != 0)) break;
       uint8_t* Ost = sm + L::OST + p * 8192;
       if (tid == 64) bulk_wait_read1();  // the tile stored from this buffer two chunks ago is out
       named_bar(4, 64);
-      {  // O = diag(Gamma) Oa + Ob
-        uint32_t oa[2][32], ob[2][32];
-        tmem_ld32(tmem + lane_off + L::col_b1(p), oa[0]);
-        tmem_ld32(tmem + lane_off + L::col_b1(p) + 32, oa[1]);
-        tmem_ld32(tmem + lane_off + L::col_b2(p), ob[0]);
-        tmem_ld32(tmem + lane_off + L::col_b2(p) + 32, ob[1]);
+      {
+        uint32_t ov[2][32];
+        tmem_ld32(tmem + lane_off + L::col_f(p) + 64, ov[0]);
+        tmem_ld32(tmem + lane_off + L::col_f(p) + 96, ov[1]);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&odone[p]);  // the TMEM buffer is free
+        mbar_arrive(&tdone[p]);  // the TMEM buffer is read
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int n = 8 * j + 2 * e;
-            pk[e] = pack_bf16(gr * __uint_as_float(oa[n >> 5][n & 31]) + __uint_as_float(ob[n >> 5][n & 31]),
-                              gr * __uint_as_float(oa[(n + 1) >> 5][(n + 1) & 31]) +
-                                  __uint_as_float(ob[(n + 1) >> 5][(n + 1) & 31]));
+            pk[e] = pack_bf16(__uint_as_float(ov[n >> 5][n & 31]), __uint_as_float(ov[(n + 1) >> 5][(n + 1) & 31]));
           }
-          *reinterpret_cast<uint4*>(Ost + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(Ost + sw128(t, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
       fence_proxy_async();
@@ -1309,6 +1317,10 @@ __global__ void __launch_bounds__(288, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && *abort_flag) {  // loads still in flight complete before the shared memory goes away
+    for (int s = 0; s < NST; ++s)
+      if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), a.wait_ns);
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, L::NCOLS);
@@ -1388,14 +1400,16 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
       if (launch_overlapped(fa, k, grid, dim3(128), smem, mk, mv, ta) != FALCON_OK) return FALCON_ERR_CUDA;
       record_event(fa, 1);
     }
-    {  // pipelined: producer warp, front and back warpgroups
+    {  // transition form: producer warp, front warpgroup, chain and output warps
       const bool l2n = (ta.pro & FALCON_PROLOGUE_L2NORM_QK) != 0;
-      auto k = l2n ? tc_fwd_pipe_kernel<SOLVE, true> : tc_fwd_pipe_kernel<SOLVE, false>;
-      const size_t smem = l2n ? PipeSmem<SOLVE, true>::TOTAL : PipeSmem<SOLVE, false>::TOTAL;
+      auto k = l2n ? tc_fwd_chain_kernel<SOLVE, true> : tc_fwd_chain_kernel<SOLVE, false>;
+      const size_t smem = l2n ? ChainSmem<SOLVE, true>::TOTAL : ChainSmem<SOLVE, false>::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
       // overlaps the per-chunk kernel's tail with its launch and set-up
-      if (launch_overlapped(fa, k, dim3(BH), dim3(288), smem, mq, mk, mo, ta) != FALCON_OK) return FALCON_ERR_CUDA;
+      if (launch_overlapped(fa, k, dim3(BH), dim3(ChainSmem<SOLVE, false>::kThreads), smem, mq, mk, mo, ta) !=
+          FALCON_OK)
+        return FALCON_ERR_CUDA;
       record_event(fa, 2);
     }
   } else {

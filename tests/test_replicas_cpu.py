@@ -80,7 +80,7 @@ def test_roofline_byte_counts():
     rows = 8 * 2048 * 12
     state = 96 * 64 * 64 * 4
     assert bench.algorithmic_bytes(LM_F1) == rows * 4 * 128 + rows * 8 + state == 103809024
-    assert bench.kernel_bytes(LM_F1, ["tc_wyu_kernel", "tc_fwd_pipe_kernel"]) == [
+    assert bench.kernel_bytes(LM_F1, ["tc_wyu_kernel", "tc_fwd_chain_kernel"]) == [
         rows * 2 * 128 + rows * 8, rows * 3 * 128 + state]
     rows_l = 2 * 16384 * 16
     assert bench.kernel_bytes(LONG_F1, ["tc_wyu_kernel", "tc_fwd_kernel"])[1] == \
