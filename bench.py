@@ -109,6 +109,8 @@ def kernel_bytes(w, names) -> list:
     state = w.B * w.H * w.dk * w.dv * 4
     if names[0] == "window_prep_kernel":  # keys and gate inputs; then the whole forward
         return [th * w.dk * es + beta + th * 4, algorithmic_bytes(w)]
+    if names[0] == "f3a_chunk_kernel":  # q, k, v and gate inputs; then q in, o and the state out
+        return [th * (2 * w.dk + w.dv) * es + beta + th * 4, th * (w.dk + w.dv) * es + state]
     return [th * (w.dk + w.dv) * es + beta + th * 4, th * (2 * w.dk + w.dv) * es + state]
 
 
@@ -718,7 +720,7 @@ def main():
         elif w.per_channel:
             names = ["tc_f2_kernel"]
         elif w.variant == 5:  # Falcon-3A
-            names = ["tc_f3a_kernel"]
+            names = ["f3a_chunk_kernel", "f3a_chain_kernel"]
         elif w.dk == 64:
             names = ["tc_wyu_kernel", "tc_fwd_chain_kernel"]
         else:

@@ -1342,44 +1342,6 @@ WsLayout ws_layout(int B, int T, int H, int chunk, int dk) {
   return w;
 }
 
-// Streaming multiprocessors of the current device (looked up once per device).
-int sm_count() {
-  static std::mutex mu;
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cached[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
-// Launch overlapping the stream's previous grid (programmatic stream
-// serialization): the kernel waits for it in hardware (griddepcontrol.wait)
-// before it reads what that grid wrote.  Plain launch when the caller times
-// each kernel with events.
-template <typename Kern, typename... Args>
-int launch_overlapped(const FwdArgs& fa, Kern k, dim3 grid, dim3 block, size_t smem, Args... args) {
-  if (fa.events) {
-    k<<<grid, block, smem, fa.stream>>>(args...);
-    return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = fa.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, args...) == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
-}
-
 template <int DK, int NV, bool SOLVE>
 int launch_t(const FwdArgs& fa, const TcArgs& ta) {
   const int BH = fa.B * fa.H;
@@ -1447,10 +1409,11 @@ bool tc_chunk_supported(const FwdArgs& a) {
   return true;
 }
 
-int tc_chunk_launches(const FwdArgs& a) { return tc_f2_supported(a) || tc_f3a_supported(a) ? 1 : 2; }
+int tc_chunk_launches(const FwdArgs& a) { return tc_f2_supported(a) ? 1 : 2; }
 
 size_t tc_chunk_ws_bytes(int B, int T, int H, int dk, int, int chunk, int variant) {
-  if (variant == FALCON_2 || variant == FALCON_2A || variant == FALCON_3A) return 256;  // status word only
+  if (variant == FALCON_2 || variant == FALCON_2A) return 256;  // status word only
+  if (variant == FALCON_3A) return tc_f3a_ws_bytes(B, T, H);
   return ws_layout(B, T, H, chunk, dk).total;
 }
 

@@ -9,24 +9,32 @@
 // v_kappa of the pairs j = t0 - W + 1 + kappa, kappa = 0 .. 62 + W, and
 //   M'_{t,kappa} = sum_{s <= t, kappa in window(s)} exp(g_t - g_s) c_s
 //                = gamma_t M'_{t-1,kappa} + c_t [t <= kappa <= t + W - 1]
-//   O    = diag(Gamma) Q S0 + (Q X^T (.) M') V
-//   S1   = Gamma_last S0 + (diag(m) X)^T V,     m_kappa = M'_{63,kappa}
+//   O    = diag(Gamma) Q S0 + (Q X^T (.) M') V  = diag(Gamma) Q S0 + O0
+//   S1   = Gamma_last S0 + (diag(m) X)^T V      = Gamma_last S0 + b,   m_kappa = M'_{63,kappa}
 // (in-chunk cumulative log-decay g, Gamma = exp(g), clamped decay
 // [JC 数学上的稳定阀门:正衰减钳制]).  The recurrence for M' only multiplies by
-// gamma <= 1, so no decay ratio is ever formed.
-//
-// One CTA per (b, h), warp-specialised like the Falcon-1 sequential kernel:
-//   warp 8      producer: TMA of the 80 key rows, 80 value rows and 64 query rows
-//   warps 4..7  front, even chunks, and warps 9..12 front, odd chunks (each up
-//               to NST chunks ahead of the back): window statistics, P^T = X Q^T
-//               (keys in TMEM lanes; one TMEM block per front), M' by the
-//               recurrence along t, P~^T and X~ = diag(m) X in place
-//   warps 0..3  back: [0 ; Oa] = [0 ; Q] S0 and [D2 ; Ob] = [X~ | P~^T]^T V in one
-//               go, S1 = Gamma_last S0 + D2, O = diag(Gamma) Oa + Ob
-// Every wait is bounded; on timeout the kernel records an error in the
-// workspace status word and leaves its chunk loop.
+// gamma <= 1, so no decay ratio is ever formed.  The state enters only
+// through the scalar decay Gamma_last and the product Q S0, so everything
+// else is formed for all chunks at once:
+//  (a) f3a_chunk_kernel, persistent over (b, h, chunk) on every SM (four
+//      CTAs per SM): TMA of the 80 key rows, 80 value rows and 64 query rows;
+//      window statistics, P^T = X Q^T (keys in TMEM lanes), M' by the
+//      recurrence along t, P~^T and X~ = diag(m) X in place, then
+//      [b ; O0] = [X~ | P~^T]^T V in one product (M = 128, K = 80); b, O0
+//      (bf16, 128B-swizzled 64 x 64 tiles) and Gamma leave by bulk copies.
+//  (b) f3a_chain_kernel, two CTAs per (b, h), each owning 32 value columns
+//      (S's columns evolve independently): S1 = Gamma_last S0 + b on the
+//      fp32 state in registers (no product on the chain), and off it
+//      O = diag(Gamma) Q S0 + O0 with Q S0 one tcgen05 product per chunk
+//      (N = 32), the outputs stored by 32-byte rows; a producer warp streams
+//      Q, b, O0 and the gates seven chunks ahead.
+// Every wait is bounded; on timeout a kernel records an error in the
+// workspace status word and leaves its loop (the chain kernel computes
+// nothing when the first kernel recorded one).
 
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -60,27 +68,44 @@ struct F3aArgs {
   __nv_bfloat16* winv_out;
   int64_t* pos_out;
   uint32_t* status;
+  uint8_t* ws_f3a;    // per chunk: b | Gamma | O0 (kF3aChunkWs bytes)
+  __nv_bfloat16* o;   // [B, T, H, 64]
+  uint64_t wait_ns;   // limit of every bounded wait
 };
 
-struct F3aSmem {
-  static constexpr int NST = 4;
-  // X (80 key rows, then X~) | P~^T (80 rows) | zero rows | Q | V (80 rows) | gates
-  static constexpr size_t XO = 0, PO = 10240, ZO = 20480, QO = 28672, VO = 36864, GO = 47104;
-  static constexpr size_t STAGE = 49152;
-  static constexpr size_t SB = NST * STAGE;         // S rows (MN-major B)
-  static constexpr size_t OST = SB + 8192;          // two output staging tiles
-  static constexpr size_t BAR = OST + 2 * 8192;
-  static constexpr size_t MISC = BAR + 128;
-  static constexpr size_t TOTAL = MISC + 16 + 1024;
+// per chunk in the workspace: b (bf16 tile) | Gamma (64 fp32) | O0 (bf16 tile)
+constexpr size_t kF3aChunkWs = 8192 + 256 + 8192;
+
+struct F3aChunkSmem {
+  // X (80 key rows, then X~) | P~^T (80 rows; then O0's staging) | V (80 rows) | Q | gates | b's staging
+  static constexpr size_t XO = 0, PO = 10240, VO = 20480, QO = 30720, GO = 38912, BST = 40960;
+  static constexpr size_t BAR = BST + 8192 + 256;
+  static constexpr size_t MISC = BAR + 32;
+  static constexpr size_t TOTAL = MISC + 64 + 1024;
   static constexpr uint32_t TX = 2 * 10240 + 8192;
-  static_assert(TOTAL <= 232448, "shared memory budget");
   // gates (fp32 offsets in GO): key energy, key existence, c, gamma, Gamma, g, warp sums
   static constexpr int G_NRM = 0, G_EX = 80, G_C = 160, G_GMA = 224, G_GAM = 288, G_G = 352, G_WS = 416;
-  static_assert(GO + (G_WS + 2) * 4 <= STAGE, "gates fit the stage");
-  // TMEM: P^T of the even-chunk front (keys in lanes) | [0 ; Oa] | [D2 ; Ob] |
-  // P^T of the odd-chunk front
-  static constexpr uint32_t COL_PT = 0, COL_B1 = 64, COL_B2 = 128, COL_PT1 = 192, NCOLS = 256;
-  static constexpr int kThreads = 416;  // 13 warps
+  static_assert(GO + (G_WS + 2) * 4 <= BST, "gates fit");
+  // TMEM: P^T (keys in lanes) | [b ; O0]
+  static constexpr uint32_t COL_PT = 0, COL_D = 64, NCOLS = 128;
+};
+
+struct F3aChainSmem {
+  // stages in flight: each CTA streams ~25 KB per chunk, so the loads in
+  // flight (NST stages) set its bandwidth at the memory latency
+  static constexpr int NST = 7;
+  // stage: Q | b | Gamma | O0
+  static constexpr size_t QO = 0, BO = 8192, GO = BO + 8192, OO = GO + 256, STAGE = 25600;
+  static constexpr int NB = 3;                     // S0 tiles and TMEM accumulators in flight
+  static constexpr size_t SB = NST * STAGE;        // S0 of chunk c in SB + (c % NB) 8192 (MN-major B,
+                                                   // this CTA's 32 columns in columns 0..31)
+  static constexpr size_t BAR = SB + NB * 8192;
+  static constexpr size_t MISC = BAR + 256;
+  static constexpr size_t TOTAL = MISC + 16 + 1024;
+  static constexpr uint32_t TX = 8192 + 8192 + 256 + 8192;
+  static constexpr int kThreads = 256;  // outputs 0..3, chain 4..5, producer 6, issuer 7
+  static_assert(OO + 8192 <= STAGE && STAGE % 1024 == 0, "stage layout");
+  static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
 // Key (x) and value of local pair j of (b, h): j >= 1 from the sequence,
@@ -99,326 +124,266 @@ __device__ __forceinline__ __nv_bfloat16 pair_v(const F3aArgs& a, int b, int h, 
   return a.winv_in[(((size_t)b * a.H + h) * Wr + ring_slot(pos + j, Wr)) * 64 + col];
 }
 
-__global__ void __launch_bounds__(F3aSmem::kThreads, 1)
-    tc_f3a_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k80,
-                  const __grid_constant__ CUtensorMap tm_v80, const __grid_constant__ CUtensorMap tm_o,
-                  F3aArgs a) {
-  using L = F3aSmem;
+
+// ======================================================================
+// (a) per-chunk operands b, O0 and Gamma, every (b, h, chunk) in parallel
+// ======================================================================
+__global__ void __launch_bounds__(128, 4)
+    f3a_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k80,
+                     const __grid_constant__ CUtensorMap tm_v80, F3aArgs a) {
+  using L = F3aChunkSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  constexpr int NST = L::NST;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  uint64_t* full = bars;              // [NST]
-  uint64_t* empty = bars + NST;       // [NST]
-  uint64_t* fdone = bars + 2 * NST;   // [NST]
-  uint64_t* fmma = bars + 3 * NST;    // [2]: P^T of front 0 / 1 done
-  uint64_t* bmma = fmma + 2;          // both back products done
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);  // [0] keys and values, [1] products, [2] queries
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
-
+  float* gt = reinterpret_cast<float*>(sm + L::GO);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x;
-  const int b = bh / a.H, h = bh % a.H;
-  const int NC = a.NC, W = a.W;
-  auto stage = [&](int s) { return sm + s * L::STAGE; };
-  auto fail = [&]() {
-    *abort_flag = 1;
-    atomicExch(a.status, kStatusTimeout);
-  };
-
+  const int W = a.W;
+  const int n_items = a.NC * a.B * a.H;  // item = (b, h, chunk), chunk fastest
+  // launched overlapping the stream's previous grid: wait for it before any
+  // read; then (every CTA of this persistent grid being resident) let the
+  // chain kernel launch and wait for this grid in hardware
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the call's status word starts clear (the grid is resident as a whole, so
+  // no CTA of it records a timeout a full wait limit before this runs)
+  if (blockIdx.x == 0 && tid == 0) atomicExch(a.status, 0u);
   if (tid == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-      mbar_init(&fdone[i], 128);
-    }
-    mbar_init(&fmma[0], 1);
-    mbar_init(&fmma[1], 1);
-    mbar_init(bmma, 1);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    mbar_init(&bar[2], 1);
     fence_mbar_init();
   }
-  for (int i = tid; i < NST * 512; i += L::kThreads)  // the zero rows of [0 ; Q]
-    *reinterpret_cast<uint4*>(stage(i >> 9) + L::ZO + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
     tmem_alloc(tmem_slot, L::NCOLS);
     tmem_relinquish();
     tc_fence_before();
   }
-  fence_proxy_async();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int quad = warp & 3;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int c = 0;
-      for (; c < NC; ++c) {
-        const int s = c % NST;
-        if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1))) { fail(); break; }
-        if (*abort_flag) break;
-        uint8_t* st = stage(s);
-        const int j0 = c * kC - W + 1;  // first pair of the chunk's keys
-        mbar_arrive_expect_tx(&full[s], L::TX);
-        tma_load_4d(st + L::XO, &tm_k80, &full[s], 0, h, j0 - a.shift, b);
-        tma_load_4d(st + L::VO, &tm_v80, &full[s], 0, h, j0, b);
-        tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
-      }
-      if (*abort_flag) {  // drain the loads still in flight
-        for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
-          mbar_wait(&full[cc % NST], (uint32_t)((cc / NST) & 1));
+  // keys and values of an item (their tiles are free once its second
+  // product is done), and its queries (free once P^T is done): thread 0
+  auto issue_xv = [&](int item) {
+    const int c = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H;
+    const int j0 = c * kC - W + 1;  // first pair of the chunk's keys
+    mbar_arrive_expect_tx(&bar[0], 2 * 10240);
+    tma_load_4d(sm + L::XO, &tm_k80, &bar[0], 0, h, j0 - a.shift, b);
+    tma_load_4d(sm + L::VO, &tm_v80, &bar[0], 0, h, j0, b);
+  };
+  auto issue_q = [&](int item) {
+    const int c = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H;
+    mbar_arrive_expect_tx(&bar[2], 8192);
+    tma_load_4d(sm + L::QO, &tm_q, &bar[2], 0, h, c * kC, b);
+  };
+  auto gate_in = [&](int item, float& lam, float& beta) {  // step c * 64 + tid
+    lam = 0.f;
+    beta = 0.f;
+    if (tid >= 64 || item >= n_items) return;
+    const int c = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H;
+    const int tg = c * kC + tid;
+    if (tg >= a.T) return;
+    const size_t gi = ((size_t)b * a.T + tg) * a.H + h;
+    lam = a.lam[gi];
+    beta = a.beta[gi];
+  };
+  int issued = 0, issued_q = 0, n_mma = 0;  // loads issued, product groups committed (thread 0)
+  if (tid == 0 && (int)blockIdx.x < n_items) {
+    issue_xv(blockIdx.x);
+    issue_q(blockIdx.x);
+    ++issued;
+    ++issued_q;
+  }
+  float lam_n = 0.f, beta_n = 0.f;
+  if ((int)blockIdx.x < n_items) gate_in(blockIdx.x, lam_n, beta_n);
+  int it = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+    const int c = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H;
+    const int t0 = c * kC, j0 = t0 - W + 1;
+    const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+    const bool step_ok = tid < 64 && t0 + tid < a.T;
+    const float lam_c = lam_n, beta = beta_n;
+    gate_in(item + gridDim.x, lam_n, beta_n);  // the next item's gate inputs, in flight meanwhile
+    const float ell = step_ok ? clamped_log_decay(lam_c, a.eps_gamma) : 0.f;
+    if (!mbar_wait(&bar[0], (uint32_t)(it & 1), a.wait_ns)) {
+      *abort_flag = 1;
+      atomicExch(a.status, kStatusTimeout);
+    }
+    if (j0 < 1) {  // keys before the sequence: carried key and window ring
+      for (int idx = tid; idx < W * 64; idx += 128) {
+        const int kap = idx >> 6, col = idx & 63, j = j0 + kap;
+        if (j < a.shift) {
+          *reinterpret_cast<__nv_bfloat16*>(sm + L::XO + sw128(kap, col)) = pair_x(a, b, h, j, col, pos);
+          if (j < 0)
+            *reinterpret_cast<__nv_bfloat16*>(sm + L::VO + sw128(kap, col)) = pair_v(a, b, h, j, col, pos);
+        }
       }
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ front
-    // fg = 0: warps 4..7, chunks 0, 2, 4, ...; fg = 1: warps 9..12, chunks 1, 3, ...
-    const int fg = warp >= 9 ? 1 : 0;
-    const int ftid = tid - (fg ? 288 : 128);
-    const int fbar = fg ? 5 : 1;  // named barrier of this front
-    const uint32_t col_pt = fg ? L::COL_PT1 : L::COL_PT;
-    uint64_t* fm = &fmma[fg];
-    uint32_t fph = 0;
-    // gate inputs of step c * 64 + ftid, loaded one chunk ahead
-    auto gate_in = [&](int c, float& lam, float& beta) {
-      const int tg = c * kC + ftid;
-      const bool ok = ftid < 64 && c < NC && tg < a.T;
-      const size_t gi = ((size_t)b * a.T + (ok ? tg : 0)) * a.H + h;
-      lam = ok ? a.lam[gi] : 0.f;
-      beta = ok ? a.beta[gi] : 0.f;
-    };
-    float lam_n, beta_n;
-    gate_in(fg, lam_n, beta_n);
-    for (int c = fg; c < NC; c += 2) {
-      const int s = c % NST;
-      const int t0 = c * kC, j0 = t0 - W + 1;
-      const bool step_ok = ftid < 64 && t0 + ftid < a.T;
-      const float lam_c = lam_n, beta = beta_n;
-      gate_in(c + 2, lam_n, beta_n);
-      const float ell = step_ok ? clamped_log_decay(lam_c, a.eps_gamma) : 0.f;
-      if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1))) fail();
-      uint8_t* st = stage(s);
-      float* gt = reinterpret_cast<float*>(st + L::GO);
-      if (j0 < 1) {  // keys before the sequence: carried key and window ring
-        for (int idx = ftid; idx < W * 64; idx += 128) {
-          const int kap = idx >> 6, col = idx & 63, j = j0 + kap;
-          if (j < a.shift) {
-            *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(kap, col)) = pair_x(a, b, h, j, col, pos);
-            if (j < 0)
-              *reinterpret_cast<__nv_bfloat16*>(st + L::VO + sw128(kap, col)) = pair_v(a, b, h, j, col, pos);
-          }
+    __syncthreads();
+    if (tid < kKeys) {  // key energy and existence of pair j0 + kappa
+      const int j = j0 + tid;
+      float n = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::XO + sw128(tid, 8 * m));
+        const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x2 = __bfloat1622float2(px[e]);
+          n = fmaf(x2.x, x2.x, n);
+          n = fmaf(x2.y, x2.y, n);
         }
       }
-      named_bar(fbar, 128);
-      if (ftid < kKeys) {  // key energy and existence of pair j0 + kappa
-        const int j = j0 + ftid;
-        float n = 0.f;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(st + L::XO + sw128(ftid, 8 * m));
-          const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 x2 = __bfloat1622float2(px[e]);
-            n = fmaf(x2.x, x2.x, n);
-            n = fmaf(x2.y, x2.y, n);
-          }
-        }
-        gt[L::G_NRM + ftid] = n;
-        gt[L::G_EX + ftid] = (pos + j >= a.shift && j < a.T) ? 1.f : 0.f;
-      }
-      float g = ell;  // inclusive prefix sum of the log-decay over the chunk
-      if (ftid < 64) {
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float n = __shfl_up_sync(0xffffffffu, g, o);
-          if (lane >= o) g += n;
-        }
-        if (lane == 31) gt[L::G_WS + (ftid >> 5)] = g;
-      }
-      named_bar(fbar, 128);
-      if (ftid < 64) {  // step t = ftid: window statistics and decays
-        if ((ftid >> 5) == 1) g += gt[L::G_WS];
-        float n = 0.f, e = 0.f;
-        for (int q = 0; q < W; ++q) {
-          const float ex = gt[L::G_EX + ftid + q];
-          n += ex;
-          e += ex * gt[L::G_NRM + ftid + q];
-        }
-        const float cs = (step_ok && n > 0.f) ? beta / (a.eps + e / n) / n : 0.f;
-        gt[L::G_C + ftid] = cs;
-        gt[L::G_GMA + ftid] = __expf(ell);
-        gt[L::G_GAM + ftid] = __expf(g);
-        gt[L::G_G + ftid] = g;
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      if (named_bar_any(fbar, 128, *abort_flag != 0)) break;
-      tc_fence_after();
-      if (ftid == 0) {  // P^T = X Q^T over 128 A rows (rows >= 80 are not read back)
-        const uint32_t sX = smem_u32(st + L::XO), sQ = smem_u32(st + L::QO);
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + col_pt, kdesc<128>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(128, 64),
-                    ks > 0 ? 1u : 0u);
-        umma_commit(fm);
-      }
-      if (!mbar_wait(fm, fph)) fail();
-      fph ^= 1;
-      tc_fence_after();
-      if (quad < 3) {  // keys kappa = 32 quad + lane < 80
-        const int kap = 32 * quad + lane;
-        float pv[64];
-        tmem_ld64(tmem + lane_off + col_pt, pv);
-        tmem_wait_ld();
-        if (kap < kKeys) {
-          const float* cs = gt + L::G_C;
-          const float* gm = gt + L::G_GMA;
-          const bool kex = gt[L::G_EX + kap] != 0.f;  // a pair that does not exist writes nothing
-          float mcur = 0.f;
-#pragma unroll
-          for (int t = 0; t < 64; ++t) {
-            const bool in_win = kex && t <= kap && kap <= t + W - 1;
-            mcur = fmaf(gm[t], mcur, in_win ? cs[t] : 0.f);
-            pv[t] *= mcur;
-          }
-          store_row64(st + L::PO, kap, pv);
-          // X~ row kappa = m_kappa x_kappa in place
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            uint4* ptr = reinterpret_cast<uint4*>(st + L::XO + sw128(kap, 8 * m));
-            const uint4 in = *ptr;
-            const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&in);
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 x2 = __bfloat1622float2(px[e]);
-              pk[e] = pack_bf16(x2.x * mcur, x2.y * mcur);
-            }
-            *ptr = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-        }
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(&fdone[s]);
+      gt[L::G_NRM + tid] = n;
+      gt[L::G_EX + tid] = (pos + j >= a.shift && j < a.T) ? 1.f : 0.f;
     }
-    if (!*abort_flag && fg == 0) {  // carry: last key, the last W - 1 pairs, position
-      if (a.kprev_out && ftid < 64)
-        a.kprev_out[(size_t)bh * 64 + ftid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + ftid];
-      const int Wr = W - 1;
-      for (int idx = ftid; idx < Wr * 64; idx += 128) {
-        const int i = idx >> 6, col = idx & 63;
-        const int64_t p = pos + a.T - Wr + i;  // global pair index
-        const int j = (int)(p - pos);
-        const int slot = (int)(((p % Wr) + Wr) % Wr);
-        const bool ok = p >= a.shift;  // slots of pairs that do not exist hold zeros
-        const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
-        if (a.winx_out)
-          a.winx_out[((size_t)bh * Wr + slot) * 64 + col] = ok ? pair_x(a, b, h, j, col, pos) : z;
-        if (a.winv_out)
-          a.winv_out[((size_t)bh * Wr + slot) * 64 + col] = ok ? pair_v(a, b, h, j, col, pos) : z;
-      }
-      if (a.pos_out && ftid == 0) a.pos_out[bh] = pos + a.T;
-    }
-  } else {
-    // ------------------------------------------------------------ back
-    // warps 0, 1: S rows 32 w + lane (lanes 0..63 of the stacked products);
-    // warps 2, 3: output rows 32 (w - 2) + lane (lanes 64..127)
-    uint8_t* SB = sm + L::SB;
-    const uint32_t sS = smem_u32(SB);
-    const bool srow = warp < 2;
-    const int r = 32 * (warp & 1) + lane;
-    float sreg[64];
+    float g = ell;  // inclusive prefix sum of the log-decay over the chunk
+    if (tid < 64) {
 #pragma unroll
-    for (int n = 0; n < 64; ++n) sreg[n] = 0.f;
-    if (srow && a.S_in) {
-      const float* src = a.S_in + ((size_t)bh * 64 + r) * 64;
-#pragma unroll
-      for (int n = 0; n < 64; n += 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(src + n);
-        sreg[n] = v4.x; sreg[n + 1] = v4.y; sreg[n + 2] = v4.z; sreg[n + 3] = v4.w;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, g, o);
+        if (lane >= o) g += n;
       }
+      if (lane == 31) gt[L::G_WS + (tid >> 5)] = g;
     }
-    if (srow) store_row64(SB, r, sreg);
+    __syncthreads();
+    if (tid < 64) {  // step t = tid: window statistics and decays
+      if ((tid >> 5) == 1) g += gt[L::G_WS];
+      float n = 0.f, e = 0.f;
+      for (int q = 0; q < W; ++q) {
+        const float ex = gt[L::G_EX + tid + q];
+        n += ex;
+        e += ex * gt[L::G_NRM + tid + q];
+      }
+      const float cs = (step_ok && n > 0.f) ? beta / (a.eps + e / n) / n : 0.f;
+      gt[L::G_C + tid] = cs;
+      gt[L::G_GMA + tid] = __expf(ell);
+      gt[L::G_GAM + tid] = __expf(g);
+      gt[L::G_G + tid] = g;
+    }
+    if (tid == 0) bulk_wait_read0();  // the previous item's tiles have left P~^T's and b's staging
     fence_proxy_async();
-    named_bar(2, 128);
-    uint32_t bph = 0;
-    for (int c = 0; c < NC; ++c) {
-      const int s = c % NST;
-      if (!mbar_wait(&fdone[s], (uint32_t)((c / NST) & 1))) fail();
-      tc_fence_after();
-      uint8_t* st = stage(s);
-      if (named_bar_any(2, 128, *abort_flag != 0)) break;
-      const float* gt = reinterpret_cast<const float*>(st + L::GO);
-      const float gfac = srow ? gt[L::G_GAM + 63] : gt[L::G_GAM + r];
-      if (tid == 0) {
-        // [0 ; Oa] = [0 ; Q] S0
-        const uint32_t sA1 = smem_u32(st + L::ZO);
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + L::COL_B1, kdesc<128>(sA1, ks), mndesc(sS, ks), idesc_bf16(128, 64, false, true),
-                    ks > 0 ? 1u : 0u);
-        // [D2 ; Ob] = [X~ | P~^T]^T V, A MN-major over two 80-row atoms, K = 80 keys
-        const uint32_t sA2 = smem_u32(st + L::XO), sV = smem_u32(st + L::VO);
-        for (int ks = 0; ks < kKeys / 16; ++ks)
-          umma_bf16(tmem + L::COL_B2, sdesc_mn128_wide(sA2 + ks * 2048, 10240), mndesc(sV, ks),
-                    idesc_bf16(128, 64, true, true), ks > 0 ? 1u : 0u);
-        umma_commit(bmma);
-      }
-      uint8_t* Ost = sm + L::OST + (c & 1) * 8192;
-      if (!mbar_wait(bmma, bph)) fail();
-      bph ^= 1;
-      tc_fence_after();
-      if (tid == 0) mbar_arrive(&empty[s]);  // nothing reads this stage any more
-      if (srow) {  // S1 = Gamma_last S0 + D2
+    tc_fence_before();
+    if (__syncthreads_or(*abort_flag)) break;
+    tc_fence_after();
+    if (tid == 0 && !mbar_wait(&bar[2], (uint32_t)(it & 1), a.wait_ns)) {
+      *abort_flag = 1;
+      atomicExch(a.status, kStatusTimeout);
+    }
+    if (tid == 0 && !*abort_flag) {  // P^T = X Q^T over 128 A rows (rows >= 80 are not read back)
+      const uint32_t sX = smem_u32(sm + L::XO), sQ = smem_u32(sm + L::QO);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tmem + L::COL_PT, kdesc<128>(sX, ks), kdesc<64>(sQ, ks), idesc_bf16(128, 64),
+                  ks > 0 ? 1u : 0u);
+      umma_commit(&bar[1]);
+      ++n_mma;
+    }
+    if (!mbar_wait(&bar[1], 0u, a.wait_ns)) {  // each item commits bar[1] twice: parities 0, 1
+      *abort_flag = 1;
+      atomicExch(a.status, kStatusTimeout);
+    }
+    tc_fence_after();
+    if (tid == 0 && item + (int)gridDim.x < n_items && !*abort_flag) {  // the query tile is read
+      issue_q(item + gridDim.x);
+      ++issued_q;
+    }
+    if (quad < 3) {  // keys kappa = 32 quad + lane < 80
+      const int kap = 32 * quad + lane;
+      const float* cs = gt + L::G_C;
+      const float* gm = gt + L::G_GMA;
+      const bool kex = kap < kKeys && gt[L::G_EX + kap] != 0.f;  // a pair that does not exist writes nothing
+      float mcur = 0.f;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t d2[32];
-          tmem_ld32(tmem + lane_off + L::COL_B2 + 32 * hf, d2);
-          tmem_wait_ld();
+      for (int hh = 0; hh < 2; ++hh) {  // 32 columns t of P^T at a time, M' carried along t
+        uint32_t pr[32];
+        tmem_ld32(tmem + lane_off + L::COL_PT + 32 * hh, pr);
+        tmem_wait_ld();
+        float pv[32];
 #pragma unroll
-          for (int n = 0; n < 32; ++n) sreg[32 * hf + n] = gfac * sreg[32 * hf + n] + __uint_as_float(d2[n]);
+        for (int i = 0; i < 32; ++i) {
+          const int t = 32 * hh + i;
+          const bool in_win = kex && t <= kap && kap <= t + W - 1;
+          mcur = fmaf(gm[t], mcur, in_win ? cs[t] : 0.f);
+          pv[i] = __uint_as_float(pr[i]) * mcur;
         }
-        store_row64(SB, r, sreg);
-      } else {  // O = diag(Gamma) Oa + Ob
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t oa[32], ob[32];
-          tmem_ld32(tmem + lane_off + L::COL_B1 + 32 * hf, oa);
-          tmem_ld32(tmem + lane_off + L::COL_B2 + 32 * hf, ob);
-          tmem_wait_ld();
+        if (kap < kKeys) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t pk[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int n = 8 * j + 2 * e;
-              pk[e] = pack_bf16(gfac * __uint_as_float(oa[n]) + __uint_as_float(ob[n]),
-                                gfac * __uint_as_float(oa[n + 1]) + __uint_as_float(ob[n + 1]));
-            }
-            *reinterpret_cast<uint4*>(Ost + sw128(r, 32 * hf + 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(pv[8 * j + 2 * e], pv[8 * j + 2 * e + 1]);
+            *reinterpret_cast<uint4*>(sm + L::PO + sw128(kap, 32 * hh + 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
       }
-      fence_proxy_async();
-      tc_fence_before();
-      named_bar(2, 128);
-      tc_fence_after();
-      if (tid == 0) {
-        tma_store_4d(&tm_o, Ost, 0, h, c * kC, b);
-        bulk_commit();
-        bulk_wait_read1();  // the tile stored one chunk ago has left its buffer
+      if (kap < kKeys) {
+        // X~ row kappa = m_kappa x_kappa in place
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          uint4* ptr = reinterpret_cast<uint4*>(sm + L::XO + sw128(kap, 8 * m));
+          const uint4 in = *ptr;
+          const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&in);
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x2 = __bfloat1622float2(px[e]);
+            pk[e] = pack_bf16(x2.x * mcur, x2.y * mcur);
+          }
+          *ptr = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       }
     }
-    if (tid == 0) bulk_wait0();
-    if (!*abort_flag && srow && a.S_out) {
-      float* dst = a.S_out + ((size_t)bh * 64 + r) * 64;
-#pragma unroll
-      for (int n = 0; n < 64; n += 4)
-        *reinterpret_cast<float4*>(dst + n) = make_float4(sreg[n], sreg[n + 1], sreg[n + 2], sreg[n + 3]);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && !*abort_flag) {  // [b ; O0] = [X~ | P~^T]^T V, A MN-major over two 80-row atoms, K = 80
+      const uint32_t sA = smem_u32(sm + L::XO), sV = smem_u32(sm + L::VO);
+      for (int ks = 0; ks < kKeys / 16; ++ks)
+        umma_bf16(tmem + L::COL_D, sdesc_mn128_wide(sA + ks * 2048, 10240), mndesc(sV, ks),
+                  idesc_bf16(128, 64, true, true), ks > 0 ? 1u : 0u);
+      umma_commit(&bar[1]);
+      ++n_mma;
     }
+    if (!*abort_flag && !mbar_wait(&bar[1], 1u, a.wait_ns)) {
+      *abort_flag = 1;
+      atomicExch(a.status, kStatusTimeout);
+    }
+    tc_fence_after();
+    // the tiles are read: the next item's loads go out while this one leaves
+    const int next = item + gridDim.x;
+    if (tid == 0 && next < n_items && !*abort_flag) {
+      issue_xv(next);
+      ++issued;
+    }
+    {  // rows 0..63: b -> its staging; rows 64..127: O0 -> P~^T's region
+      const int row = 32 * quad + lane;
+      float dv[64];
+      tmem_ld64(tmem + lane_off + L::COL_D, dv);
+      tmem_wait_ld();
+      store_row64(quad < 2 ? sm + L::BST : sm + L::PO, row & 63, dv);
+      if (tid < 64) reinterpret_cast<float*>(sm + L::BST + 8192)[tid] = gt[L::G_GAM + tid];
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    if (__syncthreads_or(*abort_flag)) break;
+    if (tid == 0) {
+      uint8_t* dst = a.ws_f3a + (size_t)(bh * a.NC + c) * kF3aChunkWs;
+      bulk_store(dst, sm + L::BST, 8192 + 256);
+      bulk_store(dst + 8192 + 256, sm + L::PO, 8192);
+      bulk_commit();
+    }
+  }
+  if (tid == 0) {
+    bulk_wait0();
+    if (issued > it) mbar_wait(&bar[0], (uint32_t)(it & 1), a.wait_ns);  // loads still in flight
+    if (issued_q > it) mbar_wait(&bar[2], (uint32_t)(it & 1), a.wait_ns);
+    // a product still in flight (abort between issue and wait) completes before TMEM is freed
+    if (n_mma > 0) mbar_wait(&bar[1], (uint32_t)((n_mma - 1) & 1), a.wait_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -428,11 +393,242 @@ __global__ void __launch_bounds__(F3aSmem::kThreads, 1)
   }
 }
 
+// ======================================================================
+// (b) the chain: S1 = Gamma_last S0 + b, O = diag(Gamma) Q S0 + O0
+// ======================================================================
+__global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
+    f3a_chain_kernel(const __grid_constant__ CUtensorMap tm_q, F3aArgs a) {
+  using L = F3aChainSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  constexpr int NST = L::NST;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint64_t* full = bars;              // [NST] stage loaded
+  uint64_t* empty = bars + NST;       // [NST] chain (64) and outputs (128) done with the stage
+  constexpr int NB = L::NB;
+  uint64_t* sready = bars + 2 * NST;  // [NB] S0 of the chunk in SB buffer p written (64)
+  uint64_t* mdone = sready + NB;      // [NB] Q S0 into TMEM buffer p done
+  uint64_t* odone = mdone + NB;       // [NB] outputs read TMEM buffer p (128)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x >> 1, half = blockIdx.x & 1, b = bh / a.H, h = bh % a.H;
+  const int c0 = 32 * half;  // this CTA's value columns c0 .. c0 + 31
+  const int W = a.W;
+  auto stage = [&](int s) { return sm + s * L::STAGE; };
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  };
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 64 + 128);
+    }
+    for (int p = 0; p < NB; ++p) {
+      mbar_init(&sready[p], 64);
+      mbar_init(&mdone[p], 1);
+      mbar_init(&odone[p], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // the per-chunk kernel has completed (and its writes are visible) past
+  // this wait; a timeout it recorded leaves its tiles incomplete: then no
+  // chunk is computed and no carry is written
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const bool upstream_failed = *reinterpret_cast<volatile uint32_t*>(a.status) != 0u;
+  if (upstream_failed) *abort_flag = 1;
+  const int NC = upstream_failed ? 0 : a.NC;
+  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+
+  if (warp == 6) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      int c = 0;
+      for (; c < NC; ++c) {
+        const int s = c % NST;
+        if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1), a.wait_ns)) { fail(); break; }
+        if (*abort_flag) break;
+        uint8_t* st = stage(s);
+        const uint8_t* src = a.ws_f3a + (size_t)(bh * a.NC + c) * kF3aChunkWs;
+        mbar_arrive_expect_tx(&full[s], L::TX);
+        tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
+        bulk_load(st + L::BO, src, 8192 + 256, &full[s]);
+        bulk_load(st + L::OO, src + 8192 + 256, 8192, &full[s]);
+      }
+      if (*abort_flag) {  // drain the loads still in flight
+        for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
+          mbar_wait(&full[cc % NST], (uint32_t)((cc / NST) & 1), a.wait_ns);
+      }
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ product issuer
+    if (lane == 0) {
+      int n = 0;
+      for (int c = 0; c < NC; ++c) {
+        const int s = c % NST, p = c % NB;
+        bool ok = mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns) &&
+                  mbar_wait(&sready[p], (uint32_t)((c / NB) & 1), a.wait_ns) &&
+                  (c < NB || mbar_wait(&odone[p], (uint32_t)(((c - NB) / NB) & 1), a.wait_ns));
+        if (!ok || *abort_flag) { fail(); break; }
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(stage(s) + L::QO), sS = smem_u32(sm + L::SB + p * 8192);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + 32 * p, kdesc<64>(sQ, ks), mndesc(sS, ks), idesc_bf16(64, 32, false, true),
+                    ks > 0 ? 1u : 0u);
+        umma_commit(&mdone[p]);
+        ++n;
+      }
+      if (n > 0) mbar_wait(&mdone[(n - 1) % NB], (uint32_t)(((n - 1) / NB) & 1), a.wait_ns);  // TMEM quiet
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ state chain
+    const int r = 32 * (warp - 4) + lane;  // S row; columns c0 .. c0 + 31
+    float sreg[32];
+#pragma unroll
+    for (int n = 0; n < 32; ++n) sreg[n] = 0.f;
+    if (a.S_in) {
+      const float* src = a.S_in + ((size_t)bh * 64 + r) * 64 + c0;
+#pragma unroll
+      for (int n = 0; n < 32; n += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(src + n);
+        sreg[n] = v4.x; sreg[n + 1] = v4.y; sreg[n + 2] = v4.z; sreg[n + 3] = v4.w;
+      }
+    }
+    auto store_s = [&](int buf) {  // row r, columns 0..31 of the tile
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(sreg[8 * j + 2 * e], sreg[8 * j + 2 * e + 1]);
+        *reinterpret_cast<uint4*>(sm + L::SB + buf * 8192 + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    };
+    if (NC > 0) {
+      store_s(0);
+      fence_proxy_async();
+      mbar_arrive(&sready[0]);
+    }
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % NST;
+      if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
+      if (named_bar_any(1, 64, *abort_flag != 0)) break;
+      const uint8_t* st = stage(s);
+      const float gl = reinterpret_cast<const float*>(st + L::GO)[63];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // S1 = Gamma_last S0 + b, row r, this CTA's columns
+        const uint4 raw = *reinterpret_cast<const uint4*>(st + L::BO + sw128(r, c0 + 8 * j));
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 b2 = __bfloat1622float2(pb[e]);
+          sreg[8 * j + 2 * e] = fmaf(gl, sreg[8 * j + 2 * e], b2.x);
+          sreg[8 * j + 2 * e + 1] = fmaf(gl, sreg[8 * j + 2 * e + 1], b2.y);
+        }
+      }
+      mbar_arrive(&empty[s]);
+      if (c + 1 < NC) {  // the next chunk's S0 into its buffer, once the product that read it last is done
+        const int pn = (c + 1) % NB;
+        if (c + 1 >= NB && !mbar_wait(&mdone[pn], (uint32_t)(((c + 1 - NB) / NB) & 1), a.wait_ns)) fail();
+        store_s(pn);
+        fence_proxy_async();
+        mbar_arrive(&sready[pn]);
+      }
+    }
+    if (!*abort_flag && a.S_out) {
+      float* dst = a.S_out + ((size_t)bh * 64 + r) * 64 + c0;
+#pragma unroll
+      for (int n = 0; n < 32; n += 4)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(sreg[n], sreg[n + 1], sreg[n + 2], sreg[n + 3]);
+    }
+  } else {
+    // ------------------------------------------------------------ outputs
+    // M = 64 accumulator (N = 32): row t = 16 warp + lane % 16 in lanes 0..15
+    // of the warp's quadrant; the half-warps read columns 0..15 and 16..31
+    const int t = 16 * warp + (lane & 15), hf = lane >> 4;
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % NST, p = c % NB;
+      if (!mbar_wait(&mdone[p], (uint32_t)((c / NB) & 1), a.wait_ns)) fail();
+      tc_fence_after();
+      if (named_bar_any(2, 128, *abort_flag != 0)) break;
+      uint32_t acc[16];
+      tmem_ld16x2_16(tmem + lane_off + 32 * p, acc);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&odone[p]);
+      const uint8_t* st = stage(s);
+      const float gq = reinterpret_cast<const float*>(st + L::GO)[t];
+      const int col = c0 + 16 * hf;  // this thread's 16 value columns
+      uint4 o0[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) o0[j] = *reinterpret_cast<const uint4*>(st + L::OO + sw128(t, col + 8 * j));
+      mbar_arrive(&empty[s]);
+      uint32_t pk[8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(&o0[j]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 b2 = __bfloat1622float2(po[e]);
+          const int n = 8 * j + 2 * e;
+          pk[4 * j + e] = pack_bf16(fmaf(gq, __uint_as_float(acc[n]), b2.x), fmaf(gq, __uint_as_float(acc[n + 1]), b2.y));
+        }
+      }
+      const int tg = c * kC + t;
+      if (tg < a.T) {
+        uint4* dst = reinterpret_cast<uint4*>(a.o + (((size_t)b * a.T + tg) * a.H + h) * 64 + col);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+    if (half == 0 && !*abort_flag) {  // carry: last key, the last W - 1 pairs, position
+      if (a.kprev_out && tid < 64)
+        a.kprev_out[(size_t)bh * 64 + tid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + tid];
+      const int Wr = W - 1;
+      for (int idx = tid; idx < Wr * 64; idx += 128) {
+        const int i = idx >> 6, col = idx & 63;
+        const int64_t pp = pos + a.T - Wr + i;  // global pair index
+        const int j = (int)(pp - pos);
+        const int slot = (int)(((pp % Wr) + Wr) % Wr);
+        const bool ok = pp >= a.shift;  // slots of pairs that do not exist hold zeros
+        const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+        if (a.winx_out)
+          a.winx_out[((size_t)bh * Wr + slot) * 64 + col] = ok ? pair_x(a, b, h, j, col, pos) : z;
+        if (a.winv_out)
+          a.winv_out[((size_t)bh * Wr + slot) * 64 + col] = ok ? pair_v(a, b, h, j, col, pos) : z;
+      }
+      if (a.pos_out && tid == 0) a.pos_out[bh] = pos + a.T;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
 }  // namespace
 
 bool tc_f3a_supported(const FwdArgs& a) {
   if (a.variant != FALCON_3A || a.dtype != FALCON_BF16 || a.chunk != 64 || a.T < 1) return false;
   return a.dk == 64 && a.dv == 64 && a.W >= 2 && a.W <= 16;
+}
+
+size_t tc_f3a_ws_bytes(int B, int T, int H) {
+  const size_t NC = (size_t)(T + kC - 1) / kC;
+  return 256 + (size_t)B * H * NC * kF3aChunkWs;
 }
 
 int launch_tc_f3a(const FwdArgs& fa) {
@@ -453,18 +649,32 @@ int launch_tc_f3a(const FwdArgs& fa) {
   ta.winv_out = reinterpret_cast<__nv_bfloat16*>(fa.winv_out);
   ta.pos_out = fa.pos_out;
   ta.status = reinterpret_cast<uint32_t*>(fa.ws);
-  CUtensorMap mq, mk, mv, mo;
+  ta.ws_f3a = reinterpret_cast<uint8_t*>(fa.ws) + 256;
+  ta.o = reinterpret_cast<__nv_bfloat16*>(fa.o);
+  ta.wait_ns = wait_limit_ns();
+  CUtensorMap mq, mk, mv;
   if (!make_map(&mq, fa.q, fa.B, fa.T, fa.H, 64, 64) || !make_map(&mk, fa.k, fa.B, fa.T, fa.H, 64, kKeys) ||
-      !make_map(&mv, fa.v, fa.B, fa.T, fa.H, 64, kKeys) || !make_map(&mo, fa.o, fa.B, fa.T, fa.H, 64, 64))
+      !make_map(&mv, fa.v, fa.B, fa.T, fa.H, 64, kKeys))
     return FALCON_ERR_CUDA;
-  auto k = tc_f3a_kernel;
-  const size_t smem = F3aSmem::TOTAL;
-  if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
-  // the call's status word starts clear; a bounded wait that runs out sets it
-  if (cudaMemsetAsync(ta.status, 0, sizeof(uint32_t), fa.stream) != cudaSuccess) return FALCON_ERR_CUDA;
-  record_event(fa, 0);
-  k<<<fa.B * fa.H, F3aSmem::kThreads, smem, fa.stream>>>(mq, mk, mv, mo, ta);
-  record_event(fa, 1);
+  {  // per-chunk operands, persistent: four CTAs per SM (TMEM and shared memory both allow four)
+    auto k = f3a_chunk_kernel;
+    const size_t smem = F3aChunkSmem::TOTAL;
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
+    const long items = (long)ta.NC * fa.B * fa.H;
+    dim3 grid((unsigned)std::min<long>(items, 4L * sm_count()));
+    record_event(fa, 0);
+    if (launch_overlapped(fa, k, grid, dim3(128), smem, mq, mk, mv, ta) != FALCON_OK) return FALCON_ERR_CUDA;
+    record_event(fa, 1);
+  }
+  {  // the chain and the outputs, two CTAs per (b, h) (32 value columns each)
+    auto k = f3a_chain_kernel;
+    const size_t smem = F3aChainSmem::TOTAL;
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
+    if (launch_overlapped(fa, k, dim3(2 * fa.B * fa.H), dim3(F3aChainSmem::kThreads), smem, mq, ta) !=
+        FALCON_OK)
+      return FALCON_ERR_CUDA;
+    record_event(fa, 2);
+  }
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
 

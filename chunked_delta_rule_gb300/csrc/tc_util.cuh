@@ -9,6 +9,7 @@
 
 #include <mutex>
 
+#include "common.cuh"
 #include "tc_ptx.cuh"
 
 namespace falcon {
@@ -184,6 +185,44 @@ inline bool make_map_f32(CUtensorMap* m, const void* base, int B, int T, int H, 
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Streaming multiprocessors of the current device (looked up once per device).
+inline int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Launch overlapping the stream's previous grid (programmatic stream
+// serialization): the kernel waits for it in hardware (griddepcontrol.wait)
+// before it reads what that grid wrote.  Plain launch when the caller times
+// each kernel with events.
+template <typename Kern, typename... Args>
+inline int launch_overlapped(const FwdArgs& fa, Kern k, dim3 grid, dim3 block, size_t smem, Args... args) {
+  if (fa.events) {
+    k<<<grid, block, smem, fa.stream>>>(args...);
+    return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = fa.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...) == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
 
 }  // namespace tcu

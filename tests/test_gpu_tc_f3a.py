@@ -31,7 +31,7 @@ def test_f3a_tc_forced_matches_oracle(F, W):
     w = w_f3a(W)
     x = make_inputs(w, device="cuda")
     p = params_for(F, w, impl=F.FALCON_IMPL_TC)
-    assert F.falcon_chunk_fwd_plan(p) == (F.FALCON_IMPL_TC, 1)
+    assert F.falcon_chunk_fwd_plan(p) == (F.FALCON_IMPL_TC, 2)
     o, co = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"])
     torch.cuda.synchronize()
     o_ref, c_ref = oracle_full(w, x)

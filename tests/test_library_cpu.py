@@ -205,9 +205,10 @@ def test_tc_workspace_layout(F, d):
 @pytest.mark.parametrize("kw,impl,launches", [
     # the tensor-core path: per-chunk kernel + sequential kernel (Falcon-1 / 1A)
     (dict(), "TC", 2), (dict(variant=1), "TC", 2), (dict(dk=128, dv=128), "TC", 2),
-    # one tensor-core kernel each (Falcon-2 / 2A at d = 64 and 128, Falcon-3A)
+    # one tensor-core kernel each (Falcon-2 / 2A at d = 64 and 128)
     (dict(variant=2), "TC", 1), (dict(variant=3, dk=128, dv=128), "TC", 1),
-    (dict(variant=5, window=8), "TC", 1),
+    # Falcon-3A: per-chunk kernel + chain kernel
+    (dict(variant=5, window=8), "TC", 2),
     # Falcon-3: band prep + column-parallel window recurrence
     (dict(variant=4, window=8), "SCAN", 2),
     # fp32 inputs, or a chunk other than 64: the portable chunk kernel
