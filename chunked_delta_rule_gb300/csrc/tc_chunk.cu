@@ -159,13 +159,12 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   }
   __syncthreads();
   const int first_item = *abort_flag ? n_items : (int)blockIdx.x;
-  // the tiles and gate inputs of an item are fetched while the previous item
-  // finishes: TMA into the tile buffers once the products that read them are
-  // done, lambda and beta into registers
+  // the tiles of an item are fetched while the previous item finishes (TMA
+  // into the tile buffers once the products that read them are done); its
+  // gate inputs two items ahead, into registers (raw loads: their values are
+  // first used two items later, so the loads stay in flight meanwhile)
   int issued = 0;  // tile loads issued (thread 0); item `it` waits for the it-th
-  // raw loads only: their values are first used by the next item, so the
-  // loads stay in flight meanwhile
-  auto fetch = [&](int item, float& lam_r, float& beta_r, int64_t& pos_r) {
+  auto fetch_tiles = [&](int item) {
     const int chunk = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
     if (tid == 0) {
       ++issued;
@@ -175,6 +174,13 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
         tma_load_4d(Xs + k * 8192, &tm_k, &bar[0], 64 * k, h, t0 - a.shift, b);
       }
     }
+  };
+  auto fetch_gates = [&](int item, float& lam_r, float& beta_r, int64_t& pos_r) {
+    lam_r = 0.f;
+    beta_r = 0.f;
+    pos_r = 0;
+    if (item >= n_items) return;
+    const int chunk = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
     const int t = t0 + tid;
     const bool step_ok = tid < 64 && t < a.T;
     const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
@@ -182,9 +188,14 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
     beta_r = a.beta[gi];
     pos_r = a.pos_in ? a.pos_in[bh] : 0;
   };
-  float lam_n = 0.f, beta_n = 0.f;
-  int64_t pos_n = 0;
-  if (first_item < n_items) fetch(first_item, lam_n, beta_n, pos_n);
+  constexpr int kIss = 96;  // issues the products and the image stores (warp 3 computes no key norms)
+  float lam_n = 0.f, beta_n = 0.f, lam_nn = 0.f, beta_nn = 0.f;
+  int64_t pos_n = 0, pos_nn = 0;
+  if (first_item < n_items) {
+    fetch_tiles(first_item);
+    fetch_gates(first_item, lam_n, beta_n, pos_n);
+    fetch_gates(first_item + gridDim.x, lam_nn, beta_nn, pos_nn);
+  }
   int it = 0;
   for (int item = first_item; item < n_items; item += gridDim.x, ++it) {
   const int chunk = item % a.NC, bh = item / a.NC;
@@ -194,6 +205,10 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   // the clamped decay and the step size, from gate logits when the prologue asks
   const float ell = step_ok ? logf(gate_gamma(lam_n, a.eps_gamma, a.pro)) : 0.f;
   const float beta = (step_ok && pos_n + t_row >= a.shift) ? gate_beta(beta_n, a.pro) : 0.f;
+  lam_n = lam_nn;
+  beta_n = beta_nn;
+  pos_n = pos_nn;
+  fetch_gates(item + 2 * gridDim.x, lam_nn, beta_nn, pos_nn);
   {  // gates: row tid <-> step chunk * 64 + tid
     float g = ell;  // inclusive prefix sum over the chunk
 #pragma unroll
@@ -253,7 +268,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   const size_t ci = (size_t)bh * a.NC + chunk;
   uint8_t* Wo = a.ws_T + ci * kImg;  // W slabs, then the U slabs DK 128 bytes further
   float* go = a.ws_g + ci * kGateF;
-  if (SOLVE && !aborted && tid == 0) {  // Gram matrix X X^T (M = 64: row r in lane 32 (r / 16) + r % 16)
+  if (SOLVE && !aborted && tid == kIss) {  // Gram matrix X X^T (M = 64: row r in lane 32 (r / 16) + r % 16)
     tc_fence_after();
     mma_chain(tmem, Xs, 64, Xs, 64, DK, idesc_bf16(64, 64), false);
     umma_commit(&bar[1]);
@@ -285,7 +300,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
       go[192 + tid] = __expf(g - gs[tid & ~15]);  // decay from the 16-block start
     }
   }
-  if (tid == 0) bulk_wait_read0();  // the previous item's image store has read its staging
+  if (tid == kIss) bulk_wait_read0();  // the previous item's image store has read its staging
   __syncthreads();
 
   if (!SOLVE) {  // additive write: U = diag(eta) V
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
     }
     __syncthreads();  // the tiles are read
     if (__syncthreads_or(*abort_flag)) break;
-    if (next < n_items) fetch(next, lam_n, beta_n, pos_n);
+    if (next < n_items) fetch_tiles(next);
     continue;
   }
 
@@ -455,7 +470,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
-  if (!aborted && tid == 0) {  // [U . ; . W] = [T diag(eta) ; T diag(eta Gamma)] [V | X]
+  if (!aborted && tid == kIss) {  // [U . ; . W] = [T diag(eta) ; T diag(eta Gamma)] [V | X]
     tc_fence_after();
     const uint32_t sT = smem_u32(TI), sV = smem_u32(Vs);
     for (int ks = 0; ks < 4; ++ks)
@@ -468,7 +483,7 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
     atomicExch(a.status, kStatusTimeout);
   }
   tc_fence_after();
-  if (next < n_items && !*abort_flag) fetch(next, lam_n, beta_n, pos_n);  // the tiles are read
+  if (next < n_items && !*abort_flag) fetch_tiles(next);  // the tiles are read
   {  // rows 0..63: U (columns 0..DK-1); rows 64..127: W (columns DK..2 DK-1),
      // staged from the T image buffer on (the product that read it and T is
      // done) in the workspace layout, then stored by one bulk copy
@@ -491,12 +506,12 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   fence_proxy_async();
   tc_fence_before();
   if (__syncthreads_or(*abort_flag)) break;
-  if (tid == 0) {
+  if (tid == kIss) {
     bulk_store(Wo, TI, kImg);
     bulk_commit();
   }
   }  // items
-  if (tid == 0) bulk_wait0();  // the last images are written
+  if (tid == kIss) bulk_wait0();  // the last images are written
   if (tid == 0 && issued > it) mbar_wait(&bar[0], (uint32_t)(it & 1), a.wait_ns);  // a load still in flight
   tc_fence_before();
   __syncthreads();
