@@ -397,6 +397,8 @@ __global__ void __launch_bounds__(64, 8) recurrent_step_col_kernel(FwdArgs a) {
   for (int r = 0; r < D; ++r) s[r] = Sg[r * D];
 
   const int64_t pos = a.pos_out[bhi];
+  // ring slot of window pair w (global index pos - Wr + w): (pos + w) mod Wr
+  const int slot0 = Wr > 0 ? (int)(pos % Wr) : 0;
   const Tin* kin = reinterpret_cast<const Tin*>(a.k) + bhi * D;
   const float qraw = to_f32(reinterpret_cast<const Tin*>(a.q)[bhi * D + j]);
   const float kraw = to_f32(kin[j]);
@@ -412,7 +414,8 @@ __global__ void __launch_bounds__(64, 8) recurrent_step_col_kernel(FwdArgs a) {
         x = a.shift ? to_f32(reinterpret_cast<const Tin*>(a.kprev_out)[bhi * D + j]) : kraw;
         v = vcur;
       } else {
-        const size_t o = (bhi * Wr + ring_slot(p, Wr)) * D + j;
+        const int sl = slot0 + w >= Wr ? slot0 + w - Wr : slot0 + w;
+        const size_t o = (bhi * Wr + sl) * D + j;
         x = to_f32(reinterpret_cast<const Tin*>(a.winx_out)[o]);
         v = to_f32(reinterpret_cast<const Tin*>(a.winv_out)[o]);
       }
@@ -437,30 +440,54 @@ __global__ void __launch_bounds__(64, 8) recurrent_step_col_kernel(FwdArgs a) {
   }
   // the current key enters the window as phi(k) under same-step pairing
   const float xsc_cur = a.shift ? 1.f : sk;
+  // x_w . q for every window slot and the window's total key energy (a
+  // slot whose pair does not exist holds a zero key): the partial sums of
+  // all slots first, then their warp reductions side by side
   float xq[MAXW], n = 0.f, e = 0.f;
 #pragma unroll
   for (int w = 0; w < MAXW; ++w) {
-    if (w >= W) break;
-    const float sc = (w == Wr) ? xsc_cur : 1.f;
-    const float x0 = sc * xw[w][lane], x1 = sc * xw[w][lane + 32];
-    xq[w] = sq * wsum(x0 * qv[lane] + x1 * qv[lane + 32]);
-    const bool ok = pos - Wr + w >= a.shift;
-    n += ok ? 1.f : 0.f;
-    e += ok ? wsum(x0 * x0 + x1 * x1) : 0.f;
+    xq[w] = 0.f;
+    if (w < W) {
+      const float sc = (w == Wr) ? xsc_cur : 1.f;
+      const float x0 = sc * xw[w][lane], x1 = sc * xw[w][lane + 32];
+      xq[w] = x0 * qv[lane] + x1 * qv[lane + 32];
+      e = fmaf(x0, x0, fmaf(x1, x1, e));
+      n += (pos - Wr + w >= a.shift) ? 1.f : 0.f;
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int w = 0; w < MAXW; ++w) xq[w] += __shfl_xor_sync(0xffffffffu, xq[w], o);
+    e += __shfl_xor_sync(0xffffffffu, e, o);
+  }
+#pragma unroll
+  for (int w = 0; w < MAXW; ++w) xq[w] *= sq;
   const float gamma = gate_gamma(a.lam[bhi], a.eps_gamma, a.prologue);
   float cf = 0.f;  // eta / n for this column
   if (n > 0.f) {
     const float bt = gate_beta(variant_per_channel(a.variant) ? a.beta[bhi * D + j] : a.beta[bhi], a.prologue);
     cf = bt / (a.eps + e / n) / n;
   }
-  // S^T q and, for the regression variants, S^T x_w: this column's sums
+  // S^T q and, for the regression variants, S^T x_w: this column's sums,
+  // the window's sums advanced together row by row (independent chains)
   const bool additive = variant_additive(a.variant);
-  float c = 0.f;
+  float c = 0.f, aw[MAXW];
+#pragma unroll
+  for (int w = 0; w < MAXW; ++w) aw[w] = 0.f;
+  const int Wp = additive ? 0 : W;  // window sums needed
 #pragma unroll
   for (int r = 0; r < D; r += 4) {
     const float4 q4 = *reinterpret_cast<const float4*>(&qv[r]);
     c = fmaf(s[r], q4.x, c); c = fmaf(s[r + 1], q4.y, c); c = fmaf(s[r + 2], q4.z, c); c = fmaf(s[r + 3], q4.w, c);
+#pragma unroll
+    for (int w = 0; w < MAXW; ++w) {
+      if (w < Wp) {
+        const float4 x4 = *reinterpret_cast<const float4*>(&xw[w][r]);
+        aw[w] = fmaf(s[r], x4.x, aw[w]); aw[w] = fmaf(s[r + 1], x4.y, aw[w]);
+        aw[w] = fmaf(s[r + 2], x4.z, aw[w]); aw[w] = fmaf(s[r + 3], x4.w, aw[w]);
+      }
+    }
   }
   c *= sq;
   float dl[MAXW];
@@ -469,17 +496,7 @@ __global__ void __launch_bounds__(64, 8) recurrent_step_col_kernel(FwdArgs a) {
   for (int w = 0; w < MAXW; ++w) {
     if (w >= W) break;
     float r_w = vv[w];
-    if (!additive) {
-      float aw = 0.f;
-#pragma unroll
-      for (int r = 0; r < D; r += 4) {
-        const float4 x4 = *reinterpret_cast<const float4*>(&xw[w][r]);
-        aw = fmaf(s[r], x4.x, aw); aw = fmaf(s[r + 1], x4.y, aw);
-        aw = fmaf(s[r + 2], x4.z, aw); aw = fmaf(s[r + 3], x4.w, aw);
-      }
-      if (w == Wr) aw *= xsc_cur;
-      r_w -= gamma * aw;
-    }
+    if (!additive) r_w -= gamma * (w == Wr ? aw[w] * xsc_cur : aw[w]);
     const bool ok = pos - Wr + w >= a.shift;
     dl[w] = ok ? cf * r_w : 0.f;
     o = fmaf(xq[w], dl[w], o);
@@ -509,7 +526,7 @@ __global__ void __launch_bounds__(64, 8) recurrent_step_col_kernel(FwdArgs a) {
   // prologue), the position
   const Tin kout = from_f32<Tin>((a.prologue & FALCON_PROLOGUE_L2NORM_QK) ? sk * kraw : kraw);
   if (Wr > 0) {
-    const int slot = ring_slot(pos, Wr);
+    const int slot = slot0;
     const bool ok = pos >= a.shift;
     reinterpret_cast<Tin*>(a.winx_out)[(bhi * Wr + slot) * D + j] =
         from_f32<Tin>(ok ? xsc_cur * xw[Wr][j] : 0.f);
