@@ -27,7 +27,8 @@
 //      fp32 state in registers (no product on the chain), and off it
 //      O = diag(Gamma) Q S0 + O0 with Q S0 one tcgen05 product per chunk
 //      (N = 32), the outputs stored by 32-byte rows; a producer warp streams
-//      Q, b, O0 and the gates seven chunks ahead.
+//      Q, b, O0 and the gates six chunks ahead; two output warpgroups take
+//      alternate chunks.
 // Every wait is bounded; on timeout a kernel records an error in the
 // workspace status word and leaves its loop (the chain kernel computes
 // nothing when the first kernel recorded one).
@@ -93,17 +94,18 @@ struct F3aChunkSmem {
 struct F3aChainSmem {
   // stages in flight: each CTA streams ~25 KB per chunk, so the loads in
   // flight (NST stages) set its bandwidth at the memory latency
-  static constexpr int NST = 7;
+  static constexpr int NST = 6;
   // stage: Q | b | Gamma | O0
   static constexpr size_t QO = 0, BO = 8192, GO = BO + 8192, OO = GO + 256, STAGE = 25600;
-  static constexpr int NB = 3;                     // S0 tiles and TMEM accumulators in flight
+  static constexpr int NB = 6;                     // S0 tiles and TMEM accumulators in flight
   static constexpr size_t SB = NST * STAGE;        // S0 of chunk c in SB + (c % NB) 8192 (MN-major B,
                                                    // this CTA's 32 columns in columns 0..31)
   static constexpr size_t BAR = SB + NB * 8192;
   static constexpr size_t MISC = BAR + 256;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
   static constexpr uint32_t TX = 8192 + 8192 + 256 + 8192;
-  static constexpr int kThreads = 256;  // outputs 0..3, chain 4..5, producer 6, issuer 7
+  static constexpr int kThreads = 384;  // outputs 0..3 and 8..11 (alternate chunks), chain 4..5,
+                                        // producer 6, issuer 7
   static_assert(OO + 8192 <= STAGE && STAGE % 1024 == 0, "stage layout");
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
     tc_fence_before();
   }
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
       }
       if (n > 0) mbar_wait(&mdone[(n - 1) % NB], (uint32_t)(((n - 1) / NB) & 1), a.wait_ns);  // TMEM quiet
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ state chain
     const int r = 32 * (warp - 4) + lane;  // S row; columns c0 .. c0 + 31
     float sreg[32];
@@ -553,15 +555,18 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ outputs
-    // M = 64 accumulator (N = 32): row t = 16 warp + lane % 16 in lanes 0..15
-    // of the warp's quadrant; the half-warps read columns 0..15 and 16..31
-    const int t = 16 * warp + (lane & 15), hf = lane >> 4;
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-    for (int c = 0; c < NC; ++c) {
+    // M = 64 accumulator (N = 32): row t = 16 quad + lane % 16 in lanes 0..15
+    // of the warp's quadrant; the half-warps read columns 0..15 and 16..31.
+    // Group og (warps 0..3, then 8..11) takes the chunks c with c % 2 == og.
+    const int og = warp >= 8 ? 1 : 0, quad = warp & 3, otid = tid - (og ? 256 : 0);
+    const int obar = 2 + og;
+    const int t = 16 * quad + (lane & 15), hf = lane >> 4;
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    for (int c = og; c < NC; c += 2) {
       const int s = c % NST, p = c % NB;
       if (!mbar_wait(&mdone[p], (uint32_t)((c / NB) & 1), a.wait_ns)) fail();
       tc_fence_after();
-      if (named_bar_any(2, 128, *abort_flag != 0)) break;
+      if (named_bar_any(obar, 128, *abort_flag != 0)) break;
       uint32_t acc[16];
       tmem_ld16x2_16(tmem + lane_off + 32 * p, acc);
       tmem_wait_ld();
@@ -592,11 +597,11 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
         dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
     }
-    if (half == 0 && !*abort_flag) {  // carry: last key, the last W - 1 pairs, position
-      if (a.kprev_out && tid < 64)
-        a.kprev_out[(size_t)bh * 64 + tid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + tid];
+    if (half == 0 && og == 0 && !*abort_flag) {  // carry: last key, the last W - 1 pairs, position
+      if (a.kprev_out && otid < 64)
+        a.kprev_out[(size_t)bh * 64 + otid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + otid];
       const int Wr = W - 1;
-      for (int idx = tid; idx < Wr * 64; idx += 128) {
+      for (int idx = otid; idx < Wr * 64; idx += 128) {
         const int i = idx >> 6, col = idx & 63;
         const int64_t pp = pos + a.T - Wr + i;  // global pair index
         const int j = (int)(pp - pos);
@@ -608,14 +613,14 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
         if (a.winv_out)
           a.winv_out[((size_t)bh * Wr + slot) * 64 + col] = ok ? pair_v(a, b, h, j, col, pos) : z;
       }
-      if (a.pos_out && tid == 0) a.pos_out[bh] = pos + a.T;
+      if (a.pos_out && otid == 0) a.pos_out[bh] = pos + a.T;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 
