@@ -206,9 +206,11 @@ int falcon_chunk_fwd_timed(const falcon_params_t* p, const void* q, const void* 
  * d_k = d_v in {64, 128}, chunk 64; see falcon_chunk_fwd_plan) whose
  * falcon_workspace_size is at most 32 MiB: B * H * ceil(T / 64) <= 1927 at
  * d = 64 (17 KB of scratch per chunk) and <= 992 at d = 128 (33 KB per
- * chunk).  Larger problems return FALCON_ERR_WORKSPACE, other shapes
- * FALCON_ERR_UNSUPPORTED (they need no workspace: call falcon_chunk_fwd with
- * workspace = NULL).  Both are found on the host before anything is enqueued.
+ * chunk).  Larger problems return FALCON_ERR_WORKSPACE, other variants and
+ * shapes FALCON_ERR_UNSUPPORTED (falcon_chunk_fwd serves them; its
+ * falcon_workspace_size says whether they need a workspace, 0 for the
+ * portable CUDA-core path).  Both are found on the host before anything is
+ * enqueued.
  * Every call looks up the array's device address (the first call on a
  * device may also load the library's device code there); make that first
  * call before any stream capture.  All calls share the one array: calls that
