@@ -953,10 +953,14 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
   uint64_t* f2mma = fmma + NF;        // [NF] front product of front f done
   uint64_t* fdone = f2mma + NF;       // [2] operand tile and TMEM buffer p ready for the chain
   uint64_t* cmma = fdone + 2;         // [2] chain product of buffer p done
-  uint64_t* tdone = cmma + 2;         // [2] chain and output warps read buffer p (128 arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
-  int* issued = reinterpret_cast<int*>(sm + L::MISC + 8);  // [NST] loads issued into each stage
+  volatile int* issued = reinterpret_cast<volatile int*>(sm + L::MISC + 8);  // [NST] loads issued per stage
+  // chunks whose accumulators the chain / the output warps have read (monotonic
+  // counts: a front that runs ahead waits on them rather than on an mbarrier
+  // phase, whose parity could alias across two pending phases)
+  volatile int* chain_read = reinterpret_cast<volatile int*>(sm + L::MISC + 24);
+  volatile int* out_read = reinterpret_cast<volatile int*>(sm + L::MISC + 28);
   float* glast = reinterpret_cast<float*>(sm + L::GL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -974,6 +978,8 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
       mbar_init(&full[i], 1);
       issued[i] = 0;
     }
+    *chain_read = 0;
+    *out_read = 0;
     for (int f = 0; f < NF; ++f) {
       mbar_init(&fmma[f], 1);
       mbar_init(&f2mma[f], 1);
@@ -981,7 +987,6 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
     for (int p = 0; p < 2; ++p) {
       mbar_init(&fdone[p], 128);
       mbar_init(&cmma[p], 1);
-      mbar_init(&tdone[p], 128);
     }
     fence_mbar_init();
   }
@@ -1018,7 +1023,17 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
     if (SOLVE) bulk_load(st + L::WO, a.ws_T + ci * 16384, 8192, &full[s]);
     bulk_load(st + L::UO, a.ws_T + ci * 16384 + 8192, 8192, &full[s]);
     bulk_load(st + L::GO, a.ws_g + ci * kGateF, 1024, &full[s]);
-    atomicAdd(&issued[s], 1);
+    __threadfence_block();
+    issued[s] = issued[s] + 1;  // one issuing thread per stage and chunk at a time
+  };
+  // bounded spin until a shared counter reaches a value (false on a timeout
+  // or once another role gave up)
+  auto spin_until = [&](volatile int* x, int target) {
+    if (*x >= target) return true;
+    const uint64_t t0 = globaltimer();
+    while (*x < target)
+      if (*abort_flag || globaltimer() - t0 > a.wait_ns) return false;
+    return true;
   };
   if (tid == 0) {
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -1036,7 +1051,10 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
     int n_f2 = 0;  // front products issued (ftid 0's bookkeeping)
     for (int c = fr; c < NC; c += NF) {
       const int s = c % NST, p = c & 1;
-      if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
+      // a front can reach chunk c before the stage's previous chunk c - NST
+      // was even loaded: first see the load of chunk c issued, so that the
+      // wait below is on the latest phase of the stage's barrier
+      if (!spin_until(&issued[s], c / NST + 1) || !mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
       uint8_t* st = stage(s);
       const float* gt = reinterpret_cast<const float*>(st + L::GO);
       const bool carried = c == 0 && a.kprev_in && a.shift;  // x_0 = the carried key
@@ -1164,7 +1182,7 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
       named_bar(fbar, 128);
       tc_fence_after();
       if (ftid == 0) {  // [X~^T ; P~] [W | U] into TMEM buffer p, once the chunk two back left it
-        if (c >= 2 && !mbar_wait(&tdone[p], (uint32_t)(((c - 2) >> 1) & 1), a.wait_ns)) {
+        if (c >= 2 && !(spin_until(chain_read, c - 1) && spin_until(out_read, c - 1))) {
           fail();
         } else {
           tc_fence_after();
@@ -1276,11 +1294,11 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
           for (int n = 0; n < 32; ++n) sreg[32 * hh + n] = fmaf(gl_, sreg[32 * hh + n], __uint_as_float(d2[n]));
         }
         tc_fence_before();
-        mbar_arrive(&tdone[p]);
         store_row64(SB, r, sreg);
       }
       fence_proxy_async();
       named_bar(3, 64);
+      if (tid == 0) *chain_read = c + 1;  // both chain warps read this chunk's accumulator
     }
     if (!*abort_flag && a.S_out) {
       float* dst = a.S_out + ((size_t)bh * 64 + r) * 64;
@@ -1309,7 +1327,6 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
         tmem_ld32(tmem + lane_off + L::col_f(p) + 96, ov[1]);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&tdone[p]);  // the TMEM buffer is read
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           uint32_t pk[4];
@@ -1324,6 +1341,7 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
       fence_proxy_async();
       named_bar(4, 64);
       if (tid == 64) {
+        *out_read = c + 1;  // both output warps read this chunk's accumulator
         tma_store_4d(&tm_o, Ost, 0, h, c * kC, b);
         bulk_commit();
       }
