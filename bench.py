@@ -111,6 +111,8 @@ def kernel_bytes(w, names) -> list:
         return [th * w.dk * es + beta + th * 4, algorithmic_bytes(w)]
     if names[0] == "f3a_chunk_kernel":  # q, k, v and gate inputs; then q in, o and the state out
         return [th * (2 * w.dk + w.dv) * es + beta + th * 4, th * (w.dk + w.dv) * es + state]
+    if names[0] == "f3_chunk_kernel":  # q, k, v and gate inputs; then o and the state out
+        return [th * (2 * w.dk + w.dv) * es + beta + th * 4, th * w.dv * es + state]
     return [th * (w.dk + w.dv) * es + beta + th * 4, th * (2 * w.dk + w.dv) * es + state]
 
 
@@ -721,6 +723,8 @@ def main():
             names = ["tc_f2_kernel"]
         elif w.variant == 5:  # Falcon-3A
             names = ["f3a_chunk_kernel", "f3a_chain_kernel"]
+        elif w.variant == 4:  # Falcon-3
+            names = ["f3_chunk_kernel", "f3_chain_kernel"]
         elif w.dk == 64:
             names = ["tc_wyu_kernel", "tc_fwd_chain_kernel"]
         else:

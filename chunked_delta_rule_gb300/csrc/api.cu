@@ -66,7 +66,7 @@ FwdArgs make_args(const falcon_params_t* p, const void* q, const void* k, const 
 }
 
 bool aligned16(const FwdArgs& a) {
-  const void* ps[6] = {a.q, a.k, a.v, a.kprev_in, a.winx_in, a.winv_in};
+  const void* ps[7] = {a.q, a.k, a.v, a.o, a.kprev_in, a.winx_in, a.winv_in};
   for (const void* x : ps)
     if (reinterpret_cast<uintptr_t>(x) & 15) return false;
   return true;
@@ -236,8 +236,10 @@ static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k
   a.n_events = n_events;
   int impl = pick_impl(p, a);
   if (impl < 0) return FALCON_ERR_UNSUPPORTED;
-  if (impl == FALCON_IMPL_SCAN && !aligned16(a)) {  // its 16-byte async copies need aligned rows
-    if (p->impl == FALCON_IMPL_SCAN) return FALCON_ERR_INVALID_ARG;
+  // the window recurrence's 16-byte async copies and the tensor-core
+  // kernels' TMA maps and 16-byte stores need rows on 16-byte boundaries
+  if ((impl == FALCON_IMPL_SCAN || impl == FALCON_IMPL_TC) && !aligned16(a)) {
+    if (p->impl == impl) return FALCON_ERR_INVALID_ARG;
     impl = FALCON_IMPL_GENERIC;
   }
   if (impl == FALCON_IMPL_SCAN) {

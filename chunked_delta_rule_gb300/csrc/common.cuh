@@ -120,6 +120,9 @@ int launch_tc_f2(const FwdArgs& a);
 bool tc_f3a_supported(const FwdArgs& a);
 int launch_tc_f3a(const FwdArgs& a);
 size_t tc_f3a_ws_bytes(int B, int T, int H);
+bool tc_f3_supported(const FwdArgs& a);
+int launch_tc_f3(const FwdArgs& a);
+size_t tc_f3_ws_bytes(int B, int T, int H);
 bool window_scan_supported(const FwdArgs& a);
 size_t window_scan_ws_bytes(int B, int T, int H, int W);
 int launch_window_scan(const FwdArgs& a);

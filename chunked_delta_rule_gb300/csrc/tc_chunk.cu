@@ -1435,7 +1435,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
 }  // namespace
 
 bool tc_chunk_supported(const FwdArgs& a) {
-  if (tc_f2_supported(a) || tc_f3a_supported(a)) return true;
+  if (tc_f2_supported(a) || tc_f3a_supported(a) || tc_f3_supported(a)) return true;
   if (a.variant != FALCON_1 && a.variant != FALCON_1A) return false;
   if (a.dtype != FALCON_BF16 || a.chunk != 64 || a.T < 1) return false;
   if (a.dk != a.dv || (a.dk != 64 && a.dk != 128)) return false;
@@ -1447,12 +1447,14 @@ int tc_chunk_launches(const FwdArgs& a) { return tc_f2_supported(a) ? 1 : 2; }
 size_t tc_chunk_ws_bytes(int B, int T, int H, int dk, int, int chunk, int variant) {
   if (variant == FALCON_2 || variant == FALCON_2A) return 256;  // status word only
   if (variant == FALCON_3A) return tc_f3a_ws_bytes(B, T, H);
+  if (variant == FALCON_3) return tc_f3_ws_bytes(B, T, H);
   return ws_layout(B, T, H, chunk, dk).total;
 }
 
 int launch_tc_chunk(const FwdArgs& fa) {
   if (tc_f2_supported(fa)) return launch_tc_f2(fa);
   if (tc_f3a_supported(fa)) return launch_tc_f3a(fa);
+  if (tc_f3_supported(fa)) return launch_tc_f3(fa);
   const WsLayout w = ws_layout(fa.B, fa.T, fa.H, 64, fa.dk);
   uint8_t* ws = reinterpret_cast<uint8_t*>(fa.ws);
   TcArgs ta;

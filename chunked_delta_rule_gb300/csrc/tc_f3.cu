@@ -1,0 +1,902 @@
+// Tensor-core chunk forward for Falcon-3 (NLMS regression write averaged over
+// a window of the last W pairs), bf16 inputs, fp32 state, chunk 64,
+// d_k = d_v = 64, 2 <= W <= 9.
+//
+// The step [JC Falcon家族六个变体各管一段 (Falcon-3 window mini-batch);
+// FW Falcon 家族], with c_t = eta_t / n_t (eta_t from the window-average key
+// energy, n_t the existing pairs of the window W(t) of step t) and the
+// clamped decay gamma_t [JC 数学上的稳定阀门:正衰减钳制]:
+//   S_t = gamma_t S_{t-1} + c_t sum_{p in W(t)} x_p (v_p - gamma_t S_{t-1}^T x_p)^T,  o_t = S_t^T q_t.
+// Chunked form used here (a reading of the pages' chunk-parallel form
+// [FW 三种等价形式; JC 三种视角看同一个更新] for the window write).  A chunk
+// of 64 steps is cut into four sub-chunks of 16 steps; sub-chunk i reads the
+// K = 15 + W keys x_{(i,kappa)} (pairs t0 - W + 1 + 16 i + kappa), and every
+// write of a step of it lies in their span.  So, from a sub-chunk's start
+// state S', S_t = Gamma_tau S' + X_i^T z_tau with z (K x d_v) obeying
+//   z_tau = gamma (I - c D_tau G_i) z_{tau-1} + c D_tau (V_i - Gamma_tau X_i S'),
+// D_tau selecting the window rows of step tau (existing pairs only) and G_i
+// the sub-chunk's key Gram.  Hence z_tau = H_tau V_i - Gamma_tau F~_tau X_i S'
+// with two K x K recurrences that do not see the state,
+//   F~_tau = (I - c D G) F~_{tau-1} + c D          (no decay: it cancels),
+//   H_tau  = gamma (I - c D G) H_{tau-1} + c D,
+// and o_t = Gamma_tau q_t^T S' + h_tau^T V_i - Gamma_tau a~_tau^T X_i S' with
+// a~ = F~^T X_i q_t, h = H^T X_i q_t.  The four sub-chunks then couple through
+// the key-space unknowns w_i = z_16 of each: (I + N) w = [H_i V_i] - [g F~_i X_i] S0
+// with N_ij = exp(g_i - g_j) F~_i X_i X_j^T (j < i; g the chunk's cumulative
+// log-decay at sub-chunk ends), so with Tf = (I + N)^{-1} bd(exp(g_i) F~_i) and
+// Th = (I + N)^{-1} bd(H_i) (96 x 96, block lower triangular) the chunk is
+//   S1 = Gamma_last S0 - M S0 + b,   O = Q' S0 + O0,
+//   M  = X~^T Tf X_s,  b = X~^T Th V_s,
+//   Q' = diag(Gamma) Q - (bd(Gamma a~) + P Tf) X_s,  O0 = (bd(h) + P Th) V_s,
+// X_s / V_s the stacked sub-chunk keys / values, X~ their rows scaled by
+// exp(g_last - g_j), P_t,(j,.) = exp(g_t - g_j) (X_j q_t - G_ij^T a~_t) (j < i(t)).
+// That is the Falcon-1 chain form, so:
+//  (a) f3_chunk_kernel, persistent over (b, h, chunk), one CTA per SM:
+//      TMA of the stacked keys, values and queries; the key Gram band and
+//      X_s Q^T in one tcgen05 product (M = 128, N = 160); the eight small
+//      recurrences (sub-chunk x {F~, H}) on the CUDA cores, a lane per column;
+//      N, P, X~ and the block substitution for [Tf | Th] (bf16 image); then
+//      [X~^T ; P] [Tf | Th] (M = 128, N = 192, K = 96) and, from its rows
+//      plus the block-diagonal terms, [-M ; Q' - Gamma Q] and [b ; O0] by
+//      two more products (K = 96); the four tiles leave by one bulk copy.
+//  (b) f3_chain_kernel, two CTAs per (b, h), each owning 32 value columns:
+//      acc = [-M ; Q'] S0 (one tcgen05 product per chunk, N = 32), then
+//      S1 = Gamma_last S0 + b + acc_top on the fp32 state in registers and
+//      O = acc_bottom + O0; a producer warp streams the chunk records.
+// Every wait is bounded; a timeout is recorded in the workspace status word
+// (the chain computes nothing when the first kernel recorded one).
+
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "tc_util.cuh"
+
+namespace falcon {
+
+using namespace tc;
+using namespace tcu;
+
+namespace {
+
+constexpr int kL = 16;        // steps per sub-chunk
+constexpr int kNS = 4;        // sub-chunks per chunk
+constexpr int kKP = 24;       // key slots per sub-chunk (15 + W <= 24)
+constexpr int kNK = kNS * kKP;  // stacked key-space rows of a chunk (96)
+constexpr int kWMax = 9;
+constexpr int kGS = 100;      // fp32 row stride of the Gram and X_s Q^T scratch
+
+struct F3Args {
+  int B, T, H, W, NC;
+  int shift;  // pair t uses key t - shift (1 prefix alignment, 0 same-step)
+  float eps, eps_gamma;
+  const float* beta;
+  const float* lam;
+  const int64_t* pos_in;
+  const __nv_bfloat16* kprev_in;
+  const __nv_bfloat16* winx_in;
+  const __nv_bfloat16* winv_in;
+  const float* S_in;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  float* S_out;
+  __nv_bfloat16* kprev_out;
+  __nv_bfloat16* winx_out;
+  __nv_bfloat16* winv_out;
+  int64_t* pos_out;
+  uint32_t* status;
+  uint8_t* ws_f3;     // per chunk: [-M ; Q'] | b | O0 | Gamma_last (kF3ChunkWs bytes)
+  __nv_bfloat16* o;   // [B, T, H, 64]
+  uint64_t wait_ns;   // limit of every bounded wait
+};
+
+// per chunk in the workspace: [-M ; Q'] (128-row bf16 tile) | b | O0 (64-row
+// bf16 tiles, 128B-swizzled) | Gamma_last (first of 64 fp32)
+constexpr size_t kF3Rec = 16384 + 8192 + 8192 + 256;
+
+struct F3ChunkSmem {
+  // 1024-aligned tiles: stacked keys (96 rows) then queries (64 rows), one
+  // K-major B operand of 160 rows; stacked values (96 rows)
+  static constexpr size_t XS = 0, QS = 12288, VS = 20480;
+  // Gram (96 x 96) and (X_s Q^T)^T (64 x 96) in fp32, later the K-major
+  // A tiles -R_F and R_H (128 rows x 96, two 64-column slabs each)
+  static constexpr size_t R1 = 32768, GS = R1, XQT = R1 + 96 * kGS * 4, RF = R1, RH = R1 + 32768;
+  // [X~ | P^T] (MN-major A, two 96-row atoms), then [Tf | Th] (MN-major B,
+  // three 96-row atoms); the output tiles reuse both once the product read them
+  static constexpr size_t AT = 98304, TB = AT + 24576;
+  static constexpr size_t OMQ = AT, OB = AT + 16384, OO = AT + 24576, OG = AT + 32768;
+  // fp32: F~_i, H_i (24 x 24 each), a~_t, h_t (64 x 24 each), N_ij (6 blocks)
+  static constexpr size_t FH = TB + 36864, AH = FH + 8 * 2304, NB = AH + 2 * 64 * 96;
+  static constexpr size_t GT = NB + 6 * 2304;
+  // gates (fp32 offsets in GT)
+  static constexpr int G_C = 0, G_GMA = 64, G_G = 128, G_GAM = 192, G_EX = 256, G_NRM = 352, G_END = 448,
+                       G_WS = 452, G_N = 456;
+  static constexpr size_t BAR = GT + G_N * 4;
+  static constexpr size_t MISC = BAR + 32;
+  static constexpr size_t TOTAL = MISC + 16 + 1024;
+  static constexpr uint32_t TX = 4 * 3072 * 2 + 8192;
+  static constexpr uint32_t NCOLS = 256;
+  static_assert(XQT + 64 * kGS * 4 <= RH + 32768 && RH + 32768 == AT, "R1 region");
+  static_assert(OG + 256 <= FH, "output tiles inside the product operands");
+  static_assert(TOTAL <= 232448, "shared memory budget");
+};
+
+struct F3ChainSmem {
+  static constexpr int NST = 4;                    // chunk records in flight
+  static constexpr size_t MQ = 0, BO = 16384, OO = 24576, GO = 32768, STAGE = 33792;
+  static constexpr int NB = 4;                     // S0 tiles and TMEM accumulators
+  static constexpr size_t SB = NST * STAGE;        // S0 of chunk c in SB + (c % NB) 8192 (MN-major B,
+                                                   // this CTA's 32 columns in columns 0..31)
+  static constexpr size_t BAR = SB + NB * 8192;
+  static constexpr size_t MISC = BAR + 256;
+  static constexpr size_t TOTAL = MISC + 16 + 1024;
+  static constexpr int kThreads = 160;             // chain 0..1, outputs 2..3, producer 4
+  static_assert(STAGE % 1024 == 0 && GO + 256 <= STAGE, "stage layout");
+  static_assert(TOTAL <= 232448, "shared memory budget");
+};
+
+// Key (x) and value of local pair j of (b, h): j >= shift from the sequence,
+// j = 0 (prefix alignment) the carried key with the first value, j < 0 the
+// carried window ring.
+__device__ __forceinline__ __nv_bfloat16 pair_x(const F3Args& a, int b, int h, int j, int col, int64_t pos) {
+  if (j >= a.shift) return a.k[(((size_t)b * a.T + (j - a.shift)) * a.H + h) * 64 + col];
+  if (j == 0) return a.kprev_in ? a.kprev_in[((size_t)b * a.H + h) * 64 + col] : __float2bfloat16_rn(0.f);
+  if (!a.winx_in || pos + j < a.shift) return __float2bfloat16_rn(0.f);
+  const int Wr = a.W - 1;
+  return a.winx_in[(((size_t)b * a.H + h) * Wr + ring_slot(pos + j, Wr)) * 64 + col];
+}
+__device__ __forceinline__ __nv_bfloat16 pair_v(const F3Args& a, int b, int h, int j, int col, int64_t pos) {
+  if (j >= 0) return a.v[(((size_t)b * a.T + j) * a.H + h) * 64 + col];
+  if (!a.winv_in || pos + j < a.shift) return __float2bfloat16_rn(0.f);
+  const int Wr = a.W - 1;
+  return a.winv_in[(((size_t)b * a.H + h) * Wr + ring_slot(pos + j, Wr)) * 64 + col];
+}
+
+__device__ __forceinline__ float dot4(float4 g, float a, float b, float c, float d, float acc) {
+  return fmaf(g.w, d, fmaf(g.z, c, fmaf(g.y, b, fmaf(g.x, a, acc))));
+}
+
+// One of the sub-chunk's two K x K recurrences, lane j holding column j.
+// DECAY = false: F~ (undecayed), DECAY = true: H.  Per step tau, after the
+// update: out[tau][j] = (column j) . (X_i q_t).  Rows above tau + W - 1 are
+// still zero, so the sums stop there.
+template <bool DECAY>
+__device__ __forceinline__ void sub_recurrence(const float* __restrict__ Gi, const float* __restrict__ xqt,
+                                               const float* __restrict__ gc, const float* __restrict__ ggm,
+                                               const float* __restrict__ ex, int i, int W, int j,
+                                               float* __restrict__ out, float (&f)[kKP]) {
+#pragma unroll
+  for (int k = 0; k < kKP; ++k) f[k] = 0.f;
+#pragma unroll
+  for (int tau = 0; tau < kL; ++tau) {
+    const int t = kL * i + tau;
+    const int nz = (tau + kWMax + 3) / 4 * 4 < kKP ? (tau + kWMax + 3) / 4 * 4 : kKP;  // compile-time per tau
+    const float cs = gc[t];
+    float dot[kWMax];
+#pragma unroll
+    for (int r = 0; r < kWMax; ++r) {
+      dot[r] = 0.f;
+      if (r < W) {
+        const float* grow = Gi + (tau + r) * kGS;
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < kKP; q += 4)
+          if (q < nz) acc = dot4(*reinterpret_cast<const float4*>(grow + q), f[q], f[q + 1], f[q + 2], f[q + 3], acc);
+        dot[r] = acc;
+      }
+    }
+    float gm = 1.f;
+    if (DECAY) {
+      gm = ggm[t];
+#pragma unroll
+      for (int k = 0; k < kKP; ++k)
+        if (k < nz) f[k] *= gm;
+    }
+#pragma unroll
+    for (int r = 0; r < kWMax; ++r) {
+      if (r < W) {
+        const int row = tau + r;
+        const float sc = cs * ex[row];
+        f[row] = fmaf(-(DECAY ? gm * sc : sc), dot[r], f[row]) + (j == row ? sc : 0.f);
+      }
+    }
+    const float* xq = xqt + t * kGS;
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < kKP; q += 4)
+      if (q < nz) s = dot4(*reinterpret_cast<const float4*>(xq + q), f[q], f[q + 1], f[q + 2], f[q + 3], s);
+    if (j < kKP) out[t * kKP + j] = s;
+  }
+}
+
+// ======================================================================
+// (a) per-chunk operators, every (b, h, chunk) in parallel
+// ======================================================================
+__global__ void __launch_bounds__(256, 1)
+    f3_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k24,
+                    const __grid_constant__ CUtensorMap tm_v24, F3Args a) {
+  using L = F3ChunkSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);  // [0] loads, [1] products
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+  float* gt = reinterpret_cast<float*>(sm + L::GT);
+  float* GS = reinterpret_cast<float*>(sm + L::GS);
+  float* XQT = reinterpret_cast<float*>(sm + L::XQT);
+  float* FH = reinterpret_cast<float*>(sm + L::FH);
+  float* AHf = reinterpret_cast<float*>(sm + L::AH);  // a~ [64][24], then h [64][24]
+  float* NBf = reinterpret_cast<float*>(sm + L::NB);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int W = a.W;
+  const int n_items = a.NC * a.B * a.H;  // item = (b, h, chunk), chunk fastest
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0 && tid == 0) atomicExch(a.status, 0u);
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, L::NCOLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int quad = warp & 3;
+  const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  };
+  // the stacked keys and values of sub-chunk j are the 24 pairs from
+  // t0 - W + 1 + 16 j; and the 64 queries (thread 0)
+  auto issue_loads = [&](int item) {
+    const int c = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H;
+    const int j0 = c * kC - W + 1;
+    mbar_arrive_expect_tx(&bar[0], L::TX);
+    for (int j = 0; j < kNS; ++j) {
+      tma_load_4d(sm + L::XS + 3072 * j, &tm_k24, &bar[0], 0, h, j0 + 16 * j - a.shift, b);
+      tma_load_4d(sm + L::VS + 3072 * j, &tm_v24, &bar[0], 0, h, j0 + 16 * j, b);
+    }
+    tma_load_4d(sm + L::QS, &tm_q, &bar[0], 0, h, c * kC, b);
+  };
+  auto gate_in = [&](int item, float& lam, float& beta) {  // step c * 64 + tid
+    lam = 0.f;
+    beta = 0.f;
+    if (tid >= 64 || item >= n_items) return;
+    const int c = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H;
+    const int tg = c * kC + tid;
+    if (tg >= a.T) return;
+    const size_t gi = ((size_t)b * a.T + tg) * a.H + h;
+    lam = a.lam[gi];
+    beta = a.beta[gi];
+  };
+  // loads issued and load phases seen complete (thread 0); products committed
+  // (thread 0) and product phases seen complete (every thread)
+  int issued = 0, n_loaded = 0, n_commit = 0, n_mma = 0;
+  if (tid == 0 && (int)blockIdx.x < n_items) {
+    issue_loads(blockIdx.x);
+    ++issued;
+  }
+  float lam_n = 0.f, beta_n = 0.f;
+  if ((int)blockIdx.x < n_items) gate_in(blockIdx.x, lam_n, beta_n);
+  auto wait_mma = [&]() {
+    if (mbar_wait(&bar[1], (uint32_t)(n_mma & 1), a.wait_ns)) ++n_mma;
+    else fail();
+    tc_fence_after();
+  };
+  int it = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+    const int c = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H;
+    const int t0 = c * kC, j0 = t0 - W + 1;
+    const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+    const bool step_ok = tid < 64 && t0 + tid < a.T;
+    const float lam_c = lam_n, beta = beta_n;
+    gate_in(item + gridDim.x, lam_n, beta_n);
+    const float ell = step_ok ? clamped_log_decay(lam_c, a.eps_gamma) : 0.f;
+    if (mbar_wait(&bar[0], (uint32_t)(it & 1), a.wait_ns)) {
+      if (tid == 0) ++n_loaded;
+    } else {
+      fail();
+    }
+    if (j0 < a.shift) {  // sub-chunk 0's keys before the sequence: carried key and window ring
+      for (int idx = tid; idx < kKP * 64; idx += 256) {
+        const int kap = idx >> 6, col = idx & 63, p = j0 + kap;
+        if (p < a.shift) {
+          *reinterpret_cast<__nv_bfloat16*>(sm + L::XS + sw128(kap, col)) = pair_x(a, b, h, p, col, pos);
+          if (p < 0) *reinterpret_cast<__nv_bfloat16*>(sm + L::VS + sw128(kap, col)) = pair_v(a, b, h, p, col, pos);
+        }
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    if (__syncthreads_or(*abort_flag)) break;
+    tc_fence_after();
+    if (tid == 0) {  // [G | (X_s Q^T)] = X_s [X_s ; Q]^T (A rows >= 96 are not read back)
+      const uint32_t sX = smem_u32(sm + L::XS);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tmem, kdesc<128>(sX, ks), kdesc<160>(sX, ks), idesc_bf16(128, 160), ks > 0 ? 1u : 0u);
+      umma_commit(&bar[1]);
+      ++n_commit;
+    }
+    // gates meanwhile: key energies and existence of the stacked rows
+    if (tid < kNK) {
+      const int jb = tid / kKP, kap = tid - kKP * jb, p = j0 + 16 * jb + kap;
+      float n = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::XS + sw128(tid, 8 * m));
+        const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x2 = __bfloat1622float2(px[e]);
+          n = fmaf(x2.x, x2.x, n);
+          n = fmaf(x2.y, x2.y, n);
+        }
+      }
+      gt[L::G_NRM + tid] = n;
+      gt[L::G_EX + tid] = (pos + p >= a.shift && p < a.T && kap < kL + W - 1) ? 1.f : 0.f;
+    }
+    float g = ell;  // inclusive prefix sum of the log-decay over the chunk
+    if (tid < 64) {
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, g, o);
+        if (lane >= o) g += n;
+      }
+      if (lane == 31) gt[L::G_WS + (tid >> 5)] = g;
+    }
+    __syncthreads();
+    if (tid < 64) {  // step t = tid: window statistics and decays
+      if ((tid >> 5) == 1) g += gt[L::G_WS];
+      const int i = tid >> 4, tau = tid & 15;
+      float n = 0.f, e = 0.f;
+      for (int r = 0; r < W; ++r) {
+        const float ex = gt[L::G_EX + kKP * i + tau + r];
+        n += ex;
+        e += ex * gt[L::G_NRM + kKP * i + tau + r];
+      }
+      gt[L::G_C + tid] = (step_ok && n > 0.f) ? beta / (a.eps + e / n) / n : 0.f;
+      gt[L::G_GMA + tid] = __expf(ell);
+      gt[L::G_G + tid] = g;
+      gt[L::G_GAM + tid] = __expf(g);
+      if (tau == 15) gt[L::G_END + i] = g;
+    }
+    wait_mma();
+    {  // Gram (columns 0..95) and X_s Q^T (96..159): warp group 0 columns 0..79, group 1 80..159
+      const int grp = warp >> 2;
+      const int row = 32 * quad + lane;
+      if (quad < 3) {
+#pragma unroll
+        for (int blk = 0; blk < 5; ++blk) {
+          const int col0 = 80 * grp + 16 * blk;
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_off + col0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = col0 + e;
+            if (col < kNK) GS[row * kGS + col] = __uint_as_float(r[e]);
+            else XQT[(col - kNK) * kGS + row] = __uint_as_float(r[e]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    {  // the eight recurrences: warp w takes sub-chunk w % 4, F~ (w < 4) or H (w >= 4)
+      const int i = warp & 3;
+      const float* Gi = GS + (kKP * i) * kGS + kKP * i;
+      const float* xq = XQT + kKP * i;
+      float f[kKP];
+      if (warp < 4) sub_recurrence<false>(Gi, xq, gt + L::G_C, gt + L::G_GMA, gt + L::G_EX + kKP * i, i, W, lane, AHf, f);
+      else sub_recurrence<true>(Gi, xq, gt + L::G_C, gt + L::G_GMA, gt + L::G_EX + kKP * i, i, W, lane, AHf + 64 * kKP, f);
+      if (lane < kKP) {
+        float* dst = FH + (warp >= 4 ? 4 * 576 : 0) + i * 576;
+#pragma unroll
+        for (int k = 0; k < kKP; ++k) dst[k * kKP + lane] = f[k];
+      }
+    }
+    if (tid == 0) bulk_wait_read0();  // the previous item's output tiles have left
+    __syncthreads();
+    // N_ij = exp(g_i - g_j) F~_i G_ij (j < i), P^T, X~ and a zeroed [Tf | Th] image
+    for (int u = tid; u < 6 * kKP * 6; u += 256) {
+      const int pi = u / (kKP * 6), rem = u - pi * kKP * 6, kap = rem / 6, q4 = 4 * (rem - 6 * (rem / 6));
+      const int i = pi < 1 ? 1 : pi < 3 ? 2 : 3, j = pi - (i * (i - 1)) / 2;
+      const float* Fr = FH + i * 576 + kap * kKP;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < kKP; ++kk) {
+        const float fv = Fr[kk];
+        const float4 g4 = *reinterpret_cast<const float4*>(GS + (kKP * i + kk) * kGS + kKP * j + q4);
+        acc[0] = fmaf(fv, g4.x, acc[0]);
+        acc[1] = fmaf(fv, g4.y, acc[1]);
+        acc[2] = fmaf(fv, g4.z, acc[2]);
+        acc[3] = fmaf(fv, g4.w, acc[3]);
+      }
+      const float sc = __expf(gt[L::G_END + i] - gt[L::G_END + j]);
+      *reinterpret_cast<float4*>(NBf + pi * 576 + kap * kKP + q4) =
+          make_float4(sc * acc[0], sc * acc[1], sc * acc[2], sc * acc[3]);
+    }
+    for (int u = tid; u < kNK * 8; u += 256) {  // P^T row (j, kappa), steps 8 tg .. 8 tg + 7
+      const int k = u >> 3, tg = u & 7, jb = k / kKP, i = tg >> 1;
+      uint32_t pk[4] = {0u, 0u, 0u, 0u};
+      if (jb < i) {
+        float gcol[kKP];  // G[(i, .)][(j, kappa)] = G[(j, kappa)][(i, .)]
+#pragma unroll
+        for (int q = 0; q < kKP; q += 4) {
+          const float4 g4 = *reinterpret_cast<const float4*>(GS + k * kGS + kKP * i + q);
+          gcol[q] = g4.x; gcol[q + 1] = g4.y; gcol[q + 2] = g4.z; gcol[q + 3] = g4.w;
+        }
+        const float gj = gt[L::G_END + jb];
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int t = 8 * tg + e;
+          const float* at = AHf + t * kKP;
+          float s = 0.f;
+#pragma unroll
+          for (int q = 0; q < kKP; q += 4) s = dot4(*reinterpret_cast<const float4*>(at + q), gcol[q], gcol[q + 1], gcol[q + 2], gcol[q + 3], s);
+          pv[e] = __expf(gt[L::G_G + t] - gj) * (XQT[t * kGS + k] - s);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(pv[2 * e], pv[2 * e + 1]);
+      }
+      *reinterpret_cast<uint4*>(sm + L::AT + 12288 + sw128(k, 8 * tg)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    for (int u = tid; u < kNK * 8; u += 256) {  // X~ row (j, kappa) = exp(g_last - g_j) x
+      const int k = u >> 3, dg = u & 7;
+      const float sc = __expf(gt[L::G_END + 3] - gt[L::G_END + k / kKP]);
+      const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::XS + sw128(k, 8 * dg));
+      const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x2 = __bfloat1622float2(px[e]);
+        pk[e] = pack_bf16(sc * x2.x, sc * x2.y);
+      }
+      *reinterpret_cast<uint4*>(sm + L::AT + sw128(k, 8 * dg)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    for (int u = tid; u < 36864 / 16; u += 256)
+      *reinterpret_cast<uint4*>(sm + L::TB + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    // [Tf | Th]: diagonal blocks exp(g_i) F~_i and H_i, then block rows 1..3
+    // by substitution, T_i = R_i - sum_{k < i} N_ik T_k (bf16 image, fp32 sums)
+    auto tb_at = [&](int row, int n) { return sm + L::TB + (n >> 6) * 12288 + sw128(row, n & 63); };
+    for (int u = tid; u < kNS * kKP * 6; u += 256) {
+      const int i = u / (kKP * 6), rem = u - i * kKP * 6, kap = rem / 6, gsel = rem - 6 * kap;
+      const bool hpart = gsel >= 3;
+      const int n0 = 8 * (gsel % 3);
+      const float* src = FH + (hpart ? 4 * 576 : 0) + i * 576 + kap * kKP + n0;
+      const float sc = hpart ? 1.f : __expf(gt[L::G_END + i]);
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(sc * src[2 * e], sc * src[2 * e + 1]);
+      *reinterpret_cast<uint4*>(tb_at(kKP * i + kap, (hpart ? kNK : 0) + kKP * i + n0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    __syncthreads();
+    for (int i = 1; i < kNS; ++i) {
+      const int ng = 3 * i;  // 8-column groups per part left of the diagonal
+      for (int u = tid; u < kKP * 2 * ng; u += 256) {
+        const int kap = u / (2 * ng), rem = u - kap * 2 * ng;
+        const bool hpart = rem >= ng;
+        const int gidx = hpart ? rem - ng : rem;
+        const int n = (hpart ? kNK : 0) + 8 * gidx;
+        const int jb = (8 * gidx) / kKP;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int kb = jb; kb < i; ++kb) {
+          const float* nr = NBf + ((i * (i - 1)) / 2 + kb) * 576 + kap * kKP;
+#pragma unroll 4
+          for (int kk = 0; kk < kKP; ++kk) {
+            const float nv = nr[kk];
+            const uint4 raw = *reinterpret_cast<const uint4*>(tb_at(kKP * kb + kk, n));
+            const __nv_bfloat162* pt = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 t2 = __bfloat1622float2(pt[e]);
+              acc[2 * e] = fmaf(nv, t2.x, acc[2 * e]);
+              acc[2 * e + 1] = fmaf(nv, t2.y, acc[2 * e + 1]);
+            }
+          }
+        }
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(-acc[2 * e], -acc[2 * e + 1]);
+        *reinterpret_cast<uint4*>(tb_at(kKP * i + kap, n)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      __syncthreads();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    if (__syncthreads_or(*abort_flag)) break;
+    tc_fence_after();
+    if (tid == 0) {  // [X~^T ; P] [Tf | Th]: A MN-major (two atoms), B MN-major (three atoms), K = 96
+      const uint32_t sA = smem_u32(sm + L::AT), sB = smem_u32(sm + L::TB);
+      for (int ks = 0; ks < kNK / 16; ++ks)
+        umma_bf16(tmem, sdesc_mn128_wide(sA + ks * 2048, 12288), sdesc_mn128_wide(sB + ks * 2048, 12288),
+                  idesc_bf16(128, 192, true, true), ks > 0 ? 1u : 0u);
+      umma_commit(&bar[1]);
+      ++n_commit;
+    }
+    wait_mma();
+    {  // rows m: group 0 writes -R_F, group 1 R_H (K-major, K = 96 in two slabs)
+      const int grp = warp >> 2, m = 32 * quad + lane;
+      const int t = m - 64, ib = t >> 4;
+      const float* add = nullptr;
+      float asc = 0.f;
+      if (m >= 64) {
+        add = grp == 0 ? AHf + t * kKP : AHf + 64 * kKP + t * kKP;
+        asc = grp == 0 ? gt[L::G_GAM + t] : 1.f;
+      }
+      uint8_t* tile = sm + (grp == 0 ? L::RF : L::RH);
+      const float sg = grp == 0 ? -1.f : 1.f;
+#pragma unroll
+      for (int blk = 0; blk < 3; ++blk) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kNK * grp + 32 * blk, r);
+        tmem_wait_ld();
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int k = 32 * blk + e;
+          float x = __uint_as_float(r[e]);
+          if (add && k >= kKP * ib && k < kKP * ib + kKP) x = fmaf(asc, add[k - kKP * ib], x);
+          v[e] = sg * x;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int k0 = 32 * blk + 8 * q;
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+          *reinterpret_cast<uint4*>(tile + (k0 >> 6) * 16384 + sw128(m, k0 & 63)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && !*abort_flag) {  // [-M ; Q' - Gamma Q] = -R_F X_s, [b ; O0] = R_H V_s
+      const uint32_t sF = smem_u32(sm + L::RF), sH = smem_u32(sm + L::RH);
+      const uint32_t sX = smem_u32(sm + L::XS), sV = smem_u32(sm + L::VS);
+      for (int ks = 0; ks < kNK / 16; ++ks)
+        umma_bf16(tmem, kdesc<128>(sF, ks), mndesc(sX, ks), idesc_bf16(128, 64, false, true), ks > 0 ? 1u : 0u);
+      for (int ks = 0; ks < kNK / 16; ++ks)
+        umma_bf16(tmem + 64, kdesc<128>(sH, ks), mndesc(sV, ks), idesc_bf16(128, 64, false, true), ks > 0 ? 1u : 0u);
+      umma_commit(&bar[1]);
+      ++n_commit;
+    }
+    if (!*abort_flag) wait_mma();
+    // the query rows the epilogue needs, then the tiles are free for the next item
+    const int m = 32 * quad + lane, grp = warp >> 2;
+    uint4 qrow[8];
+    if (grp == 0 && m >= 64) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) qrow[q] = *reinterpret_cast<const uint4*>(sm + L::QS + sw128(m - 64, 8 * q));
+    }
+    __syncthreads();
+    const int next = item + gridDim.x;
+    if (tid == 0 && next < n_items && !*abort_flag) {
+      issue_loads(next);
+      ++issued;
+    }
+    {
+      float d[64];
+      tmem_ld64(tmem + lane_off + 64 * grp, d);
+      tmem_wait_ld();
+      if (grp == 0) {
+        if (m >= 64) {
+          const float gq = gt[L::G_GAM + m - 64];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const __nv_bfloat162* pq = reinterpret_cast<const __nv_bfloat162*>(&qrow[q]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 q2 = __bfloat1622float2(pq[e]);
+              d[8 * q + 2 * e] = fmaf(gq, q2.x, d[8 * q + 2 * e]);
+              d[8 * q + 2 * e + 1] = fmaf(gq, q2.y, d[8 * q + 2 * e + 1]);
+            }
+          }
+        }
+        store_row64(sm + L::OMQ, m, d);
+      } else {
+        store_row64(sm + (m < 64 ? L::OB : L::OO), m & 63, d);
+      }
+      if (tid == 0) reinterpret_cast<float*>(sm + L::OG)[0] = gt[L::G_GAM + 63];
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    if (__syncthreads_or(*abort_flag)) break;
+    if (tid == 0) {
+      bulk_store(a.ws_f3 + (size_t)(bh * a.NC + c) * kF3Rec, sm + L::OMQ, (uint32_t)kF3Rec);
+      bulk_commit();
+    }
+  }
+  if (tid == 0) {  // loads and a product still in flight complete before the memory goes away
+    bulk_wait0();
+    for (int w = n_loaded; w < issued; ++w) mbar_wait(&bar[0], (uint32_t)(w & 1), a.wait_ns);
+    if (n_commit > n_mma) mbar_wait(&bar[1], (uint32_t)(n_mma & 1), a.wait_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::NCOLS);
+  }
+}
+
+// ======================================================================
+// (b) the chain: acc = [-M ; Q'] S0, S1 = Gamma_last S0 + b + acc_top, O = acc_bottom + O0
+// ======================================================================
+__global__ void __launch_bounds__(F3ChainSmem::kThreads, 1) f3_chain_kernel(F3Args a) {
+  using L = F3ChainSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  constexpr int NST = L::NST, NB = L::NB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint64_t* full = bars;              // [NST] record loaded
+  uint64_t* empty = bars + NST;       // [NST] chain (64) and outputs (64) done with the record
+  uint64_t* mdone = bars + 2 * NST;   // [NB] product of the chunk in TMEM buffer p done
+  uint64_t* odone = mdone + NB;       // [NB] outputs read TMEM buffer p (64)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x >> 1, half = blockIdx.x & 1, b = bh / a.H, h = bh % a.H;
+  const int c0 = 32 * half;  // this CTA's value columns c0 .. c0 + 31
+  const int W = a.W;
+  auto stage = [&](int s) { return sm + s * L::STAGE; };
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicExch(a.status, kStatusTimeout);
+  };
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 128);
+    }
+    for (int p = 0; p < NB; ++p) {
+      mbar_init(&mdone[p], 1);
+      mbar_init(&odone[p], 64);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const bool upstream_failed = *reinterpret_cast<volatile uint32_t*>(a.status) != 0u;
+  if (upstream_failed) *abort_flag = 1;
+  const int NC = upstream_failed ? 0 : a.NC;
+  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      int c = 0;
+      for (; c < NC; ++c) {
+        const int s = c % NST;
+        if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1), a.wait_ns)) { fail(); break; }
+        if (*abort_flag) break;
+        const uint8_t* src = a.ws_f3 + (size_t)(bh * a.NC + c) * kF3Rec;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)kF3Rec);
+        bulk_load(stage(s), src, (uint32_t)kF3Rec, &full[s]);
+      }
+      if (*abort_flag) {  // drain the loads still in flight
+        for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
+          mbar_wait(&full[cc % NST], (uint32_t)((cc / NST) & 1), a.wait_ns);
+      }
+    }
+  } else if (warp < 2) {
+    // ------------------------------------------------------------ state chain
+    const int r = tid;  // S row; columns c0 .. c0 + 31
+    float sreg[32];
+#pragma unroll
+    for (int n = 0; n < 32; ++n) sreg[n] = 0.f;
+    if (a.S_in) {
+      const float* src = a.S_in + ((size_t)bh * 64 + r) * 64 + c0;
+#pragma unroll
+      for (int n = 0; n < 32; n += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(src + n);
+        sreg[n] = v4.x; sreg[n + 1] = v4.y; sreg[n + 2] = v4.z; sreg[n + 3] = v4.w;
+      }
+    }
+    auto store_s = [&](int buf) {  // row r, columns 0..31 of the tile
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(sreg[8 * j + 2 * e], sreg[8 * j + 2 * e + 1]);
+        *reinterpret_cast<uint4*>(sm + L::SB + buf * 8192 + sw128(r, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    };
+    store_s(0);
+    fence_proxy_async();
+    named_bar(1, 64);
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % NST, p = c % NB;
+      bool ok = mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns);
+      if (ok && tid == 0) {  // the TMEM buffer's previous chunk has been read by the outputs
+        ok = c < NB || mbar_wait(&odone[p], (uint32_t)(((c - NB) / NB) & 1), a.wait_ns);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t sA = smem_u32(stage(s) + L::MQ), sS = smem_u32(sm + L::SB + p * 8192);
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + 32 * p, kdesc<128>(sA, ks), mndesc(sS, ks), idesc_bf16(128, 32, false, true),
+                      ks > 0 ? 1u : 0u);
+          umma_commit(&mdone[p]);
+        }
+      }
+      if (!ok) fail();
+      if (named_bar_any(1, 64, *abort_flag != 0)) break;
+      if (!mbar_wait(&mdone[p], (uint32_t)((c / NB) & 1), a.wait_ns)) fail();
+      if (named_bar_any(1, 64, *abort_flag != 0)) break;
+      tc_fence_after();
+      uint32_t acc[32];
+      tmem_ld32(tmem + lane_off + 32 * p, acc);
+      tmem_wait_ld();
+      tc_fence_before();
+      const uint8_t* st = stage(s);
+      const float gl = reinterpret_cast<const float*>(st + L::GO)[0];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // S1 = Gamma_last S0 + b + (-M S0), row r, this CTA's columns
+        const uint4 raw = *reinterpret_cast<const uint4*>(st + L::BO + sw128(r, c0 + 8 * j));
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 b2 = __bfloat1622float2(pb[e]);
+          const int n = 8 * j + 2 * e;
+          sreg[n] = fmaf(gl, sreg[n], b2.x + __uint_as_float(acc[n]));
+          sreg[n + 1] = fmaf(gl, sreg[n + 1], b2.y + __uint_as_float(acc[n + 1]));
+        }
+      }
+      mbar_arrive(&empty[s]);
+      if (c + 1 < NC) store_s((c + 1) % NB);  // its previous reader (chunk c + 1 - NB) is done
+      fence_proxy_async();
+      named_bar(1, 64);
+    }
+    if (!*abort_flag && a.S_out) {
+      float* dst = a.S_out + ((size_t)bh * 64 + r) * 64 + c0;
+#pragma unroll
+      for (int n = 0; n < 32; n += 4)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(sreg[n], sreg[n + 1], sreg[n + 2], sreg[n + 3]);
+    }
+  } else {
+    // ------------------------------------------------------------ outputs (TMEM lanes 64..127)
+    const int otid = tid - 64, t = otid;
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % NST, p = c % NB;
+      if (!mbar_wait(&mdone[p], (uint32_t)((c / NB) & 1), a.wait_ns) ||
+          !mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns))
+        fail();
+      if (named_bar_any(2, 64, *abort_flag != 0)) break;
+      tc_fence_after();
+      uint32_t acc[32];
+      tmem_ld32(tmem + lane_off + 32 * p, acc);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&odone[p]);
+      const uint8_t* st = stage(s);
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(st + L::OO + sw128(t, c0 + 8 * j));
+        const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 o2 = __bfloat1622float2(po[e]);
+          const int n = 8 * j + 2 * e;
+          pk[4 * j + e] = pack_bf16(__uint_as_float(acc[n]) + o2.x, __uint_as_float(acc[n + 1]) + o2.y);
+        }
+      }
+      mbar_arrive(&empty[s]);
+      const int tg = c * kC + t;
+      if (tg < a.T) {
+        uint4* dst = reinterpret_cast<uint4*>(a.o + (((size_t)b * a.T + tg) * a.H + h) * 64 + c0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      }
+    }
+    if (half == 0 && !*abort_flag) {  // carry: last key, the last W - 1 pairs, position
+      if (a.kprev_out)
+        a.kprev_out[(size_t)bh * 64 + otid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + otid];
+      const int Wr = W - 1;
+      for (int idx = otid; idx < Wr * 64; idx += 64) {
+        const int i = idx >> 6, col = idx & 63;
+        const int64_t pp = pos + a.T - Wr + i;  // global pair index
+        const int j = (int)(pp - pos);
+        const int slot = (int)(((pp % Wr) + Wr) % Wr);
+        const bool ok = pp >= a.shift;  // slots of pairs that do not exist hold zeros
+        const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+        if (a.winx_out)
+          a.winx_out[((size_t)bh * Wr + slot) * 64 + col] = ok ? pair_x(a, b, h, j, col, pos) : z;
+        if (a.winv_out)
+          a.winv_out[((size_t)bh * Wr + slot) * 64 + col] = ok ? pair_v(a, b, h, j, col, pos) : z;
+      }
+      if (a.pos_out && otid == 0) a.pos_out[bh] = pos + a.T;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+}  // namespace
+
+bool tc_f3_supported(const FwdArgs& a) {
+  if (a.variant != FALCON_3 || a.dtype != FALCON_BF16 || a.chunk != 64 || a.T < 1) return false;
+  return a.dk == 64 && a.dv == 64 && a.W >= 2 && a.W <= kWMax;
+}
+
+size_t tc_f3_ws_bytes(int B, int T, int H) {
+  const size_t NC = (size_t)(T + kC - 1) / kC;
+  return 256 + (size_t)B * H * NC * kF3Rec;
+}
+
+int launch_tc_f3(const FwdArgs& fa) {
+  F3Args ta;
+  ta.B = fa.B; ta.T = fa.T; ta.H = fa.H; ta.W = fa.W; ta.NC = (fa.T + kC - 1) / kC;
+  ta.shift = fa.shift;
+  ta.eps = fa.eps; ta.eps_gamma = fa.eps_gamma;
+  ta.beta = fa.beta; ta.lam = fa.lam; ta.pos_in = fa.pos_in;
+  ta.kprev_in = reinterpret_cast<const __nv_bfloat16*>(fa.kprev_in);
+  ta.winx_in = reinterpret_cast<const __nv_bfloat16*>(fa.winx_in);
+  ta.winv_in = reinterpret_cast<const __nv_bfloat16*>(fa.winv_in);
+  ta.S_in = fa.S_in;
+  ta.k = reinterpret_cast<const __nv_bfloat16*>(fa.k);
+  ta.v = reinterpret_cast<const __nv_bfloat16*>(fa.v);
+  ta.S_out = fa.S_out;
+  ta.kprev_out = reinterpret_cast<__nv_bfloat16*>(fa.kprev_out);
+  ta.winx_out = reinterpret_cast<__nv_bfloat16*>(fa.winx_out);
+  ta.winv_out = reinterpret_cast<__nv_bfloat16*>(fa.winv_out);
+  ta.pos_out = fa.pos_out;
+  ta.status = reinterpret_cast<uint32_t*>(fa.ws);
+  ta.ws_f3 = reinterpret_cast<uint8_t*>(fa.ws) + 256;
+  ta.o = reinterpret_cast<__nv_bfloat16*>(fa.o);
+  ta.wait_ns = wait_limit_ns();
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, fa.q, fa.B, fa.T, fa.H, 64, 64) || !make_map(&mk, fa.k, fa.B, fa.T, fa.H, 64, kKP) ||
+      !make_map(&mv, fa.v, fa.B, fa.T, fa.H, 64, kKP))
+    return FALCON_ERR_CUDA;
+  {  // per-chunk operators, persistent: one CTA per SM
+    auto k = f3_chunk_kernel;
+    const size_t smem = F3ChunkSmem::TOTAL;
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
+    const long items = (long)ta.NC * fa.B * fa.H;
+    dim3 grid((unsigned)std::min<long>(items, (long)sm_count()));
+    record_event(fa, 0);
+    if (launch_overlapped(fa, k, grid, dim3(256), smem, mq, mk, mv, ta) != FALCON_OK) return FALCON_ERR_CUDA;
+    record_event(fa, 1);
+  }
+  {  // the chain and the outputs, two CTAs per (b, h) (32 value columns each)
+    auto k = f3_chain_kernel;
+    const size_t smem = F3ChainSmem::TOTAL;
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
+    if (launch_overlapped(fa, k, dim3(2 * fa.B * fa.H), dim3(F3ChainSmem::kThreads), smem, ta) != FALCON_OK)
+      return FALCON_ERR_CUDA;
+    record_event(fa, 2);
+  }
+  return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
+}
+
+}  // namespace falcon

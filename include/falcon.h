@@ -105,12 +105,14 @@ typedef enum {
  * path.  GENERIC, TC and SCAN force one (TC and SCAN return
  * FALCON_ERR_UNSUPPORTED for shapes they do not cover).  The tensor-core
  * path covers Falcon-1, 1A, 2 and 2A with bf16 inputs, chunk 64 and
- * d_k = d_v in {64, 128}, and Falcon-3A with bf16, chunk 64, d = 64 and
- * 2 <= window <= 16.  SCAN (Falcon-3, 2 <= window <= 8, d_k in {32, 64},
- * d_v a multiple of 16, bf16 or fp32, 16-byte aligned q, k, v and carried
- * keys / values) walks the steps with the state's value columns spread over
- * threads and ignores `chunk`; AUTO falls back to the portable path for
- * misaligned tensors, a forced SCAN returns FALCON_ERR_INVALID_ARG. */
+ * d_k = d_v in {64, 128}, Falcon-3A with bf16, chunk 64, d = 64 and
+ * 2 <= window <= 16, and Falcon-3 with bf16, chunk 64, d = 64 and
+ * 2 <= window <= 9.  SCAN (Falcon-3, 2 <= window <= 8, d_k in {32, 64},
+ * d_v a multiple of 16, bf16 or fp32) walks the steps with the state's
+ * value columns spread over threads and ignores `chunk`.  TC and SCAN need
+ * q, k, v, o and the carried keys / values on 16-byte boundaries: AUTO falls
+ * back to the portable path for misaligned tensors, a forced TC or SCAN
+ * returns FALCON_ERR_INVALID_ARG. */
 typedef enum {
   FALCON_IMPL_AUTO = 0,
   FALCON_IMPL_GENERIC = 1,

@@ -3,8 +3,8 @@ the C ABI: windows 2..8, d_k = 32 / 64, bf16 and fp32, several staged blocks
 with a ragged tail, carries in and out (window rings bit-exact with the
 portable chunk kernel's), fresh and continued sequences with the window not
 yet full, same-step pairing, empty and one-step calls, clamped decays, and
-sampled heads of the 4 x 8192 x 12, d = 64, W = 8 workload in the launch
-configuration the benchmark times."""
+sampled heads of the 4 x 8192 x 12, d = 64, W = 8 workload (forced: AUTO
+takes the tensor-core path at d = 64 in bf16)."""
 
 from __future__ import annotations
 
@@ -48,7 +48,8 @@ def check(w, o, co, o_ref, c_ref):
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_scan_matches_oracle(F, W, d, dtype):
     w = wl(W=W, d=d, dtype=dtype)
-    assert F.falcon_chunk_fwd_plan(params_for(F, w))[0] == F.FALCON_IMPL_SCAN
+    auto = F.falcon_chunk_fwd_plan(params_for(F, w))[0]  # d = 64 bf16 runs on the tensor cores
+    assert auto == (F.FALCON_IMPL_TC if (d == 64 and dtype == "bf16") else F.FALCON_IMPL_SCAN)
     x = make_inputs(w, device="cuda")
     o, co = run(F, w, x)
     o_ref, c_ref = oracle_full(w, x)
@@ -117,6 +118,8 @@ def test_scan_coverage(F):
         run(F, w9, make_inputs(w9, device="cuda"))
     assert e.value.code == -2
     p = params_for(F, w.with_(window=9), impl=F.FALCON_IMPL_AUTO)
+    assert F.falcon_chunk_fwd_plan(p)[0] == F.FALCON_IMPL_TC
+    p = params_for(F, w.with_(window=10), impl=F.FALCON_IMPL_AUTO)
     assert F.falcon_chunk_fwd_plan(p)[0] == F.FALCON_IMPL_GENERIC
     p = params_for(F, w.with_(variant=FALCON_1, window=1), impl=F.FALCON_IMPL_SCAN)
     with pytest.raises(F.FalconError) as e:
@@ -130,7 +133,7 @@ def test_scan_full_size_sampled_heads(F):
     """Falcon-3, 4 x 8192 x 12 heads, d = 64, W = 8 in one call (the launch
     the benchmark times); three heads recomputed by the oracle's recurrence."""
     w = WINDOW_F3
-    p = params_for(F, w)
+    p = params_for(F, w, impl=F.FALCON_IMPL_SCAN)
     assert F.falcon_chunk_fwd_plan(p)[0] == F.FALCON_IMPL_SCAN
     x = make_inputs(w, device="cuda")
     o, co = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"])

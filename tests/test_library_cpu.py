@@ -209,8 +209,10 @@ def test_tc_workspace_layout(F, d):
     (dict(variant=2), "TC", 1), (dict(variant=3, dk=128, dv=128), "TC", 1),
     # Falcon-3A: per-chunk kernel + chain kernel
     (dict(variant=5, window=8), "TC", 2),
-    # Falcon-3: band prep + column-parallel window recurrence
-    (dict(variant=4, window=8), "SCAN", 2),
+    # Falcon-3: per-chunk key-space kernel + chain kernel at d = 64 (W <= 9);
+    # band prep + column-parallel window recurrence at d = 32
+    (dict(variant=4, window=8), "TC", 2), (dict(variant=4, window=9), "TC", 2),
+    (dict(variant=4, window=8, dk=32, dv=32), "SCAN", 2),
     # fp32 inputs, or a chunk other than 64: the portable chunk kernel
     (dict(dtype=1), "GENERIC", 1), (dict(chunk=32), "GENERIC", 1),
     # the prologue: inside the d = 64 Falcon-1 kernels, a gather launch elsewhere
