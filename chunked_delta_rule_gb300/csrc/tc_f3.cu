@@ -103,6 +103,10 @@ struct F3ChunkSmem {
   // Gram (96 x 96) and (X_s Q^T)^T (64 x 96) in fp32, later the K-major
   // A tiles -R_F and R_H (128 rows x 96, two 64-column slabs each)
   static constexpr size_t R1 = 32768, GS = R1, XQT = R1 + 96 * kGS * 4, RF = R1, RH = R1 + 32768;
+  // in between (Gram and X_s Q^T read, -R_F / R_H not yet written): the
+  // bf16 image of T = (I + N)^{-1} (MN-major B, two 96-row atoms) and the
+  // K-major A tile Z = [X~^T ; P] T (128 rows x 96, two slabs)
+  static constexpr size_t TI = R1, ZT = R1 + 24576;
   // [X~ | P^T] (MN-major A, two 96-row atoms), then [Tf | Th] (MN-major B,
   // three 96-row atoms); the output tiles reuse both once the product read them
   static constexpr size_t AT = 98304, TB = AT + 24576;
@@ -119,6 +123,8 @@ struct F3ChunkSmem {
   static constexpr uint32_t TX = 4 * 3072 * 2 + 8192;
   static constexpr uint32_t NCOLS = 256;
   static_assert(XQT + 64 * kGS * 4 <= RH + 32768 && RH + 32768 == AT, "R1 region");
+  static_assert(ZT + 32768 <= AT, "T image and Z inside R1");
+  static_assert(4 * (kKP + 2) * 32 * 4 <= 6 * 2304, "recurrence scratch inside the N blocks");
   static_assert(OG + 256 <= FH, "output tiles inside the product operands");
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
@@ -158,56 +164,120 @@ __device__ __forceinline__ float dot4(float4 g, float a, float b, float c, float
   return fmaf(g.w, d, fmaf(g.z, c, fmaf(g.y, b, fmaf(g.x, a, acc))));
 }
 
-// One of the sub-chunk's two K x K recurrences, lane j holding column j.
-// DECAY = false: F~ (undecayed), DECAY = true: H.  Per step tau, after the
-// update: out[tau][j] = (column j) . (X_i q_t).  Rows above tau + W - 1 are
-// still zero, so the sums stop there.
-template <bool DECAY>
-__device__ __forceinline__ void sub_recurrence(const float* __restrict__ Gi, const float* __restrict__ xqt,
-                                               const float* __restrict__ gc, const float* __restrict__ ggm,
-                                               const float* __restrict__ ex, int i, int W, int j,
-                                               float* __restrict__ out, float (&f)[kKP]) {
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  const unsigned long long pa = (unsigned long long)__float_as_uint(a.x) | ((unsigned long long)__float_as_uint(a.y) << 32);
+  const unsigned long long pb = (unsigned long long)__float_as_uint(b.x) | ((unsigned long long)__float_as_uint(b.y) << 32);
+  const unsigned long long pc = (unsigned long long)__float_as_uint(c.x) | ((unsigned long long)__float_as_uint(c.y) << 32);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pa), "l"(pb), "l"(pc));
+  return make_float2(__uint_as_float((unsigned)d), __uint_as_float((unsigned)(d >> 32)));
+}
+
+// The sub-chunk's two K x K recurrences, F~ (undecayed) and H, side by side:
+// lane j holds column j of both (rows in pairs).  Step tau: the window rows
+// tau + r (r < W) take
+//   d_r = G[tau + r, :] M_{tau-1},  M_tau = gamma M_{tau-1} + Delta_tau,
+//   Delta_tau[tau + r] = -gamma c m_{tau+r} d_r + c m_{tau+r} [j == tau + r]
+// (gamma = 1 for F~).  A row that stays in the window needs no new sum over
+// the K slots: d_r(tau) = gamma_{tau-1} d_{r+1}(tau - 1) + sum_a G[tau + r][tau - 1 + a]
+// Delta_{tau-1}[a]; only the row entering the window takes the full sum, and
+// one Gram element feeds both matrices.  The window is handled as kWMax rows
+// with the increments of rows past W masked to zero, so every index but the
+// step is static.  The increments reach their (moving) rows through this
+// lane's column of `dbuf` ([kKP + 2][32] floats, zero between uses: the K
+// slots, F~'s increments then H's, and a spare pair of rows).  After the update, outF[t][j] =
+// F~ column j . (X_i q_t) and outH[t][j] = H column j . (X_i q_t).
+__device__ __forceinline__ void sub_recurrences(const float* __restrict__ Gi, const float* __restrict__ xqt,
+                                                const float* __restrict__ gc, const float* __restrict__ ggm,
+                                                const float* __restrict__ ex, int i, int W, int j,
+                                                float* __restrict__ outF, float* __restrict__ outH,
+                                                float* __restrict__ dbuf, float2 (&f)[kKP / 2],
+                                                float2 (&hc)[kKP / 2]) {
+  float* spare = dbuf + kKP * 32;
 #pragma unroll
-  for (int k = 0; k < kKP; ++k) f[k] = 0.f;
+  for (int k = 0; k < kKP / 2; ++k) {
+    f[k] = make_float2(0.f, 0.f);
+    hc[k] = make_float2(0.f, 0.f);
+  }
 #pragma unroll
+  for (int k = 0; k < kKP; ++k) dbuf[k * 32 + j] = 0.f;
+  float pf[kWMax], ph[kWMax], lf[kWMax], lh[kWMax];  // previous step's window sums and increments
+#pragma unroll
+  for (int r = 0; r < kWMax; ++r) {
+    pf[r] = 0.f; ph[r] = 0.f; lf[r] = 0.f; lh[r] = 0.f;
+  }
+  float gprev = 1.f;
+#pragma unroll 1
   for (int tau = 0; tau < kL; ++tau) {
     const int t = kL * i + tau;
-    const int nz = (tau + kWMax + 3) / 4 * 4 < kKP ? (tau + kWMax + 3) / 4 * 4 : kKP;  // compile-time per tau
-    const float cs = gc[t];
-    float dot[kWMax];
+    const float cs = gc[t], gm = ggm[t];
+    float df[kWMax], dh[kWMax];
+    const float* gblk = Gi + tau * kGS + (tau > 0 ? tau - 1 : 0);
+#pragma unroll
+    for (int r = 0; r < kWMax - 1; ++r) {  // rows that stay: carried sums plus last step's increments
+      float af = pf[r + 1], ah = gprev * ph[r + 1];
+#pragma unroll
+      for (int a = 0; a < kWMax; ++a) {
+        const float g = gblk[r * kGS + a];
+        af = fmaf(g, lf[a], af);
+        ah = fmaf(g, lh[a], ah);
+      }
+      df[r] = af;
+      dh[r] = ah;
+    }
+    {  // the row entering the window: the full sums
+      const float* grow = Gi + (tau + kWMax - 1) * kGS;
+      float2 af = make_float2(0.f, 0.f), ah = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kKP; q += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(grow + q);
+        const float2 g01 = make_float2(g4.x, g4.y), g23 = make_float2(g4.z, g4.w);
+        af = ffma2(g01, f[q / 2], af);
+        af = ffma2(g23, f[q / 2 + 1], af);
+        ah = ffma2(g01, hc[q / 2], ah);
+        ah = ffma2(g23, hc[q / 2 + 1], ah);
+      }
+      df[kWMax - 1] = af.x + af.y;
+      dh[kWMax - 1] = ah.x + ah.y;
+    }
 #pragma unroll
     for (int r = 0; r < kWMax; ++r) {
-      dot[r] = 0.f;
-      if (r < W) {
-        const float* grow = Gi + (tau + r) * kGS;
-        float acc = 0.f;
-#pragma unroll
-        for (int q = 0; q < kKP; q += 4)
-          if (q < nz) acc = dot4(*reinterpret_cast<const float4*>(grow + q), f[q], f[q + 1], f[q + 2], f[q + 3], acc);
-        dot[r] = acc;
-      }
+      const float sc = r < W ? cs * ex[tau + r] : 0.f;
+      const float inj = j == tau + r ? sc : 0.f;
+      const float incf = fmaf(-sc, df[r], inj), inch = fmaf(-gm * sc, dh[r], inj);
+      dbuf[(tau + r) * 32 + j] = incf;
+      pf[r] = df[r]; ph[r] = dh[r]; lf[r] = incf; lh[r] = inch;
     }
-    float gm = 1.f;
-    if (DECAY) {
-      gm = ggm[t];
+    gprev = gm;
+    const float2 gm2 = make_float2(gm, gm), one2 = make_float2(1.f, 1.f);
 #pragma unroll
-      for (int k = 0; k < kKP; ++k)
-        if (k < nz) f[k] *= gm;
-    }
+    for (int k = 0; k < kKP / 2; ++k)  // F~ += Delta
+      f[k] = ffma2(make_float2(dbuf[(2 * k) * 32 + j], dbuf[(2 * k + 1) * 32 + j]), one2, f[k]);
 #pragma unroll
-    for (int r = 0; r < kWMax; ++r) {
-      if (r < W) {
-        const int row = tau + r;
-        const float sc = cs * ex[row];
-        f[row] = fmaf(-(DECAY ? gm * sc : sc), dot[r], f[row]) + (j == row ? sc : 0.f);
-      }
-    }
+    for (int r = 0; r < kWMax; ++r) dbuf[(tau + r) * 32 + j] = lh[r];
+#pragma unroll
+    for (int k = 0; k < kKP / 2; ++k)  // H = gamma H + Delta
+      hc[k] = ffma2(hc[k], gm2, make_float2(dbuf[(2 * k) * 32 + j], dbuf[(2 * k + 1) * 32 + j]));
+#pragma unroll
+    for (int r = 0; r < kWMax; ++r) dbuf[(tau + r) * 32 + j] = 0.f;
     const float* xq = xqt + t * kGS;
-    float s = 0.f;
+    float2 sf = make_float2(0.f, 0.f), sh = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < kKP; q += 4)
-      if (q < nz) s = dot4(*reinterpret_cast<const float4*>(xq + q), f[q], f[q + 1], f[q + 2], f[q + 3], s);
-    if (j < kKP) out[t * kKP + j] = s;
+    for (int q = 0; q < kKP; q += 4) {
+      const float4 x4 = *reinterpret_cast<const float4*>(xq + q);
+      const float2 x01 = make_float2(x4.x, x4.y), x23 = make_float2(x4.z, x4.w);
+      sf = ffma2(x01, f[q / 2], sf);
+      sf = ffma2(x23, f[q / 2 + 1], sf);
+      sh = ffma2(x01, hc[q / 2], sh);
+      sh = ffma2(x23, hc[q / 2 + 1], sh);
+    }
+    // lanes past the key slots store into the spare rows: no branch, so the
+    // warp stays converged through the steps
+    float* of = j < kKP ? outF + t * kKP + j : spare + j;
+    float* oh = j < kKP ? outH + t * kKP + j : spare + 32 + j;
+    *of = sf.x + sf.y;
+    *oh = sh.x + sh.y;
+    __syncwarp();
   }
 }
 
@@ -391,22 +461,45 @@ __global__ void __launch_bounds__(256, 1)
     }
     tc_fence_before();
     __syncthreads();
-    {  // the eight recurrences: warp w takes sub-chunk w % 4, F~ (w < 4) or H (w >= 4)
-      const int i = warp & 3;
-      const float* Gi = GS + (kKP * i) * kGS + kKP * i;
-      const float* xq = XQT + kKP * i;
-      float f[kKP];
-      if (warp < 4) sub_recurrence<false>(Gi, xq, gt + L::G_C, gt + L::G_GMA, gt + L::G_EX + kKP * i, i, W, lane, AHf, f);
-      else sub_recurrence<true>(Gi, xq, gt + L::G_C, gt + L::G_GMA, gt + L::G_EX + kKP * i, i, W, lane, AHf + 64 * kKP, f);
+    if (warp < 4) {  // the recurrences: warp i takes sub-chunk i, F~ and H side by side
+      const int i = warp;
+      float2 f[kKP / 2], hc[kKP / 2];
+      sub_recurrences(GS + (kKP * i) * kGS + kKP * i, XQT + kKP * i, gt + L::G_C, gt + L::G_GMA,
+                      gt + L::G_EX + kKP * i, i, W, lane, AHf, AHf + 64 * kKP,
+                      NBf + i * (kKP + 2) * 32, f, hc);
       if (lane < kKP) {
-        float* dst = FH + (warp >= 4 ? 4 * 576 : 0) + i * 576;
 #pragma unroll
-        for (int k = 0; k < kKP; ++k) dst[k * kKP + lane] = f[k];
+        for (int k = 0; k < kKP / 2; ++k) {
+          FH[i * 576 + (2 * k) * kKP + lane] = f[k].x;
+          FH[i * 576 + (2 * k + 1) * kKP + lane] = f[k].y;
+          FH[4 * 576 + i * 576 + (2 * k) * kKP + lane] = hc[k].x;
+          FH[4 * 576 + i * 576 + (2 * k + 1) * kKP + lane] = hc[k].y;
+        }
       }
+    } else {
+      // meanwhile, once the previous item's output tiles have left (they
+      // overlay these): X~ row (j, kappa) = exp(g_last - g_j) x, and a zeroed
+      // [Tf | Th] image
+      if (tid == 128) bulk_wait_read0();
+      named_bar(1, 128);
+      for (int u = tid - 128; u < kNK * 8; u += 128) {
+        const int k = u >> 3, dg = u & 7;
+        const float sc = __expf(gt[L::G_END + 3] - gt[L::G_END + k / kKP]);
+        const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::XS + sw128(k, 8 * dg));
+        const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x2 = __bfloat1622float2(px[e]);
+          pk[e] = pack_bf16(sc * x2.x, sc * x2.y);
+        }
+        *reinterpret_cast<uint4*>(sm + L::AT + sw128(k, 8 * dg)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      for (int u = tid - 128; u < 36864 / 16; u += 128)
+        *reinterpret_cast<uint4*>(sm + L::TB + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (tid == 0) bulk_wait_read0();  // the previous item's output tiles have left
     __syncthreads();
-    // N_ij = exp(g_i - g_j) F~_i G_ij (j < i), P^T, X~ and a zeroed [Tf | Th] image
+    // N_ij = exp(g_i - g_j) F~_i G_ij (j < i) and P^T
     for (int u = tid; u < 6 * kKP * 6; u += 256) {
       const int pi = u / (kKP * 6), rem = u - pi * kKP * 6, kap = rem / 6, q4 = 4 * (rem - 6 * (rem / 6));
       const int i = pi < 1 ? 1 : pi < 3 ? 2 : 3, j = pi - (i * (i - 1)) / 2;
@@ -426,7 +519,7 @@ __global__ void __launch_bounds__(256, 1)
           make_float4(sc * acc[0], sc * acc[1], sc * acc[2], sc * acc[3]);
     }
     for (int u = tid; u < kNK * 8; u += 256) {  // P^T row (j, kappa), steps 8 tg .. 8 tg + 7
-      const int k = u >> 3, tg = u & 7, jb = k / kKP, i = tg >> 1;
+      const int k = u % kNK, tg = u / kNK, jb = k / kKP, i = tg >> 1;  // a warp shares tg
       uint32_t pk[4] = {0u, 0u, 0u, 0u};
       if (jb < i) {
         float gcol[kKP];  // G[(i, .)][(j, kappa)] = G[(j, kappa)][(i, .)]
@@ -451,24 +544,8 @@ __global__ void __launch_bounds__(256, 1)
       }
       *reinterpret_cast<uint4*>(sm + L::AT + 12288 + sw128(k, 8 * tg)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
-    for (int u = tid; u < kNK * 8; u += 256) {  // X~ row (j, kappa) = exp(g_last - g_j) x
-      const int k = u >> 3, dg = u & 7;
-      const float sc = __expf(gt[L::G_END + 3] - gt[L::G_END + k / kKP]);
-      const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::XS + sw128(k, 8 * dg));
-      const __nv_bfloat162* px = reinterpret_cast<const __nv_bfloat162*>(&raw);
-      uint32_t pk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 x2 = __bfloat1622float2(px[e]);
-        pk[e] = pack_bf16(sc * x2.x, sc * x2.y);
-      }
-      *reinterpret_cast<uint4*>(sm + L::AT + sw128(k, 8 * dg)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-    for (int u = tid; u < 36864 / 16; u += 256)
-      *reinterpret_cast<uint4*>(sm + L::TB + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
-    __syncthreads();
-    // [Tf | Th]: diagonal blocks exp(g_i) F~_i and H_i, then block rows 1..3
-    // by substitution, T_i = R_i - sum_{k < i} N_ik T_k (bf16 image, fp32 sums)
+    // the block-diagonal right factor [bd(exp(g_i) F~_i) | bd(H_i)] (bf16
+    // image, MN-major B over three atoms; the rest of it was zeroed above)
     auto tb_at = [&](int row, int n) { return sm + L::TB + (n >> 6) * 12288 + sw128(row, n & 63); };
     for (int u = tid; u < kNS * kKP * 6; u += 256) {
       const int i = u / (kKP * 6), rem = u - i * kKP * 6, kap = rem / 6, gsel = rem - 6 * kap;
@@ -482,48 +559,124 @@ __global__ void __launch_bounds__(256, 1)
       *reinterpret_cast<uint4*>(tb_at(kKP * i + kap, (hpart ? kNK : 0) + kKP * i + n0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
     __syncthreads();
-    for (int i = 1; i < kNS; ++i) {
-      const int ng = 3 * i;  // 8-column groups per part left of the diagonal
-      for (int u = tid; u < kKP * 2 * ng; u += 256) {
-        const int kap = u / (2 * ng), rem = u - kap * 2 * ng;
-        const bool hpart = rem >= ng;
-        const int gidx = hpart ? rem - ng : rem;
-        const int n = (hpart ? kNK : 0) + 8 * gidx;
-        const int jb = (8 * gidx) / kKP;
-        float acc[8];
+    // T = (I + N)^{-1}, block lower triangular with identity diagonal blocks:
+    // T_{i,i-1} = -N_{i,i-1}, T_20 = -N_20 + N_21 N_10, T_31 = -N_31 + N_32 N_21,
+    // then T_30 = -N_30 + N_31 N_10 - N_32 T_20.  bf16 image: MN-major B (rows
+    // k, 96 columns over two atoms); T_20 also kept in fp32 (F~ and H are in
+    // the image by now, so their scratch is free).
+    auto ti_at = [&](int row, int n) { return sm + L::TI + (n >> 6) * 12288 + sw128(row, n & 63); };
+    auto nblk = [&](int i, int j) { return NBf + ((i * (i - 1)) / 2 + j) * 576; };
+    float* T20 = FH;
+    // rows k, columns 8 g .. 8 g + 7 (inside one block), by units of 8
+    auto put8 = [&](int k, int n0, const float (&v)[8]) {
+      uint32_t pk[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int kb = jb; kb < i; ++kb) {
-          const float* nr = NBf + ((i * (i - 1)) / 2 + kb) * 576 + kap * kKP;
-#pragma unroll 4
-          for (int kk = 0; kk < kKP; ++kk) {
-            const float nv = nr[kk];
-            const uint4 raw = *reinterpret_cast<const uint4*>(tb_at(kKP * kb + kk, n));
-            const __nv_bfloat162* pt = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+      *reinterpret_cast<uint4*>(ti_at(k, n0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    };
+    // v = -N_ij[kap][c0..] + A[kap][:] B[:][c0..] (A, B 24 x 24 fp32, row stride kKP)
+    auto prod8 = [&](const float* nij, const float* A, const float* Bm, int kap, int c0, float (&v)[8]) {
+      const float4 n0 = *reinterpret_cast<const float4*>(nij + kap * kKP + c0);
+      const float4 n1 = *reinterpret_cast<const float4*>(nij + kap * kKP + c0 + 4);
+      v[0] = -n0.x; v[1] = -n0.y; v[2] = -n0.z; v[3] = -n0.w;
+      v[4] = -n1.x; v[5] = -n1.y; v[6] = -n1.z; v[7] = -n1.w;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 t2 = __bfloat1622float2(pt[e]);
-              acc[2 * e] = fmaf(nv, t2.x, acc[2 * e]);
-              acc[2 * e + 1] = fmaf(nv, t2.y, acc[2 * e + 1]);
-            }
-          }
+      for (int kk = 0; kk < kKP; kk += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(A + kap * kKP + kk);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 b0 = *reinterpret_cast<const float4*>(Bm + (kk + q) * kKP + c0);
+          const float4 b1 = *reinterpret_cast<const float4*>(Bm + (kk + q) * kKP + c0 + 4);
+          v[0] = fmaf(av[q], b0.x, v[0]); v[1] = fmaf(av[q], b0.y, v[1]);
+          v[2] = fmaf(av[q], b0.z, v[2]); v[3] = fmaf(av[q], b0.w, v[3]);
+          v[4] = fmaf(av[q], b1.x, v[4]); v[5] = fmaf(av[q], b1.y, v[5]);
+          v[6] = fmaf(av[q], b1.z, v[6]); v[7] = fmaf(av[q], b1.w, v[7]);
         }
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(-acc[2 * e], -acc[2 * e + 1]);
-        *reinterpret_cast<uint4*>(tb_at(kKP * i + kap, n)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      __syncthreads();
+    };
+    // stage A: the two products T_20 and T_31 (144 units), then every other
+    // block of the image: identity, -N_{i,i-1}, zero (T_30 below)
+    for (int u = tid; u < 2 * kKP * 3 + kNK * 12; u += 256) {
+      float v[8];
+      if (u < 2 * kKP * 3) {
+        const int which = u / (kKP * 3), rem = u - which * kKP * 3, kap = rem / 3, c0 = 8 * (rem - 3 * kap);
+        const int bi = which ? 3 : 2, bj = bi - 2;
+        prod8(nblk(bi, bj), nblk(bi, bi - 1), nblk(bi - 1, bj), kap, c0, v);
+        if (bi == 2) {
+          *reinterpret_cast<float4*>(T20 + kap * kKP + c0) = make_float4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<float4*>(T20 + kap * kKP + c0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+        }
+        put8(kKP * bi + kap, kKP * bj + c0, v);
+      } else {
+        const int w = u - 2 * kKP * 3, k = w / 12, g = w - 12 * (w / 12);
+        const int bi = k / kKP, kap = k - kKP * bi, n0 = 8 * g, bj = n0 / kKP, c0 = n0 - kKP * bj;
+        if (bj == bi - 2 || bj == bi - 3) continue;  // the products (T_30 in stage B)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+        if (bj == bi) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = c0 + e == kap ? 1.f : 0.f;
+        } else if (bj == bi - 1) {
+          const float* nij = nblk(bi, bj) + kap * kKP + c0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = -nij[e];
+        }
+        put8(k, n0, v);
+      }
+    }
+    __syncthreads();
+    if (tid < kKP * 3) {  // stage B: T_30 = (-N_30 + N_31 N_10) - N_32 T_20
+      const int kap = tid / 3, c0 = 8 * (tid - 3 * kap);
+      float v[8], w8[8];
+      prod8(nblk(3, 0), nblk(3, 1), nblk(1, 0), kap, c0, v);
+      prod8(nblk(3, 0), nblk(3, 2), T20, kap, c0, w8);  // -N_30 + N_32 T_20
+      const float* n30 = nblk(3, 0) + kap * kKP + c0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = v[e] - (w8[e] + n30[e]);
+      put8(3 * kKP + kap, c0, v);
     }
     fence_proxy_async();
     tc_fence_before();
     if (__syncthreads_or(*abort_flag)) break;
     tc_fence_after();
-    if (tid == 0) {  // [X~^T ; P] [Tf | Th]: A MN-major (two atoms), B MN-major (three atoms), K = 96
-      const uint32_t sA = smem_u32(sm + L::AT), sB = smem_u32(sm + L::TB);
+    if (tid == 0) {  // Z = [X~^T ; P] T: A MN-major (two atoms), B MN-major (two atoms, N = 96), K = 96
+      const uint32_t sA = smem_u32(sm + L::AT), sT = smem_u32(sm + L::TI);
       for (int ks = 0; ks < kNK / 16; ++ks)
-        umma_bf16(tmem, sdesc_mn128_wide(sA + ks * 2048, 12288), sdesc_mn128_wide(sB + ks * 2048, 12288),
-                  idesc_bf16(128, 192, true, true), ks > 0 ? 1u : 0u);
+        umma_bf16(tmem, sdesc_mn128_wide(sA + ks * 2048, 12288), sdesc_mn128_wide(sT + ks * 2048, 12288),
+                  idesc_bf16(128, kNK, true, true), ks > 0 ? 1u : 0u);
+      umma_commit(&bar[1]);
+      ++n_commit;
+    }
+    wait_mma();
+    {  // Z rows m as bf16, K-major (K = 96 in two slabs): group 0 columns 0..47, group 1 48..95
+      const int grp = warp >> 2, m = 32 * quad + lane;
+#pragma unroll
+      for (int b16 = 0; b16 < 3; ++b16) {
+        const int k0 = 48 * grp + 16 * b16;
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_off + k0, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h8 = 0; h8 < 2; ++h8) {
+          const int k = k0 + 8 * h8;
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            pk[e] = pack_bf16(__uint_as_float(r[8 * h8 + 2 * e]), __uint_as_float(r[8 * h8 + 2 * e + 1]));
+          *reinterpret_cast<uint4*>(sm + L::ZT + (k >> 6) * 16384 + sw128(m, k & 63)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {  // [X~^T ; P] [Tf | Th] = Z [bd | bd]: A K-major, B MN-major (three atoms), K = 96
+      const uint32_t sZ = smem_u32(sm + L::ZT), sB = smem_u32(sm + L::TB);
+      for (int ks = 0; ks < kNK / 16; ++ks)
+        umma_bf16(tmem, kdesc<128>(sZ, ks), sdesc_mn128_wide(sB + ks * 2048, 12288),
+                  idesc_bf16(128, 192, false, true), ks > 0 ? 1u : 0u);
       umma_commit(&bar[1]);
       ++n_commit;
     }
@@ -617,13 +770,13 @@ __global__ void __launch_bounds__(256, 1)
     fence_proxy_async();
     tc_fence_before();
     if (__syncthreads_or(*abort_flag)) break;
-    if (tid == 0) {
+    if (tid == 128) {  // the thread that waits for the tiles to leave before they are rewritten
       bulk_store(a.ws_f3 + (size_t)(bh * a.NC + c) * kF3Rec, sm + L::OMQ, (uint32_t)kF3Rec);
       bulk_commit();
     }
   }
+  if (tid == 128) bulk_wait0();
   if (tid == 0) {  // loads and a product still in flight complete before the memory goes away
-    bulk_wait0();
     for (int w = n_loaded; w < issued; ++w) mbar_wait(&bar[0], (uint32_t)(w & 1), a.wait_ns);
     if (n_commit > n_mma) mbar_wait(&bar[1], (uint32_t)(n_mma & 1), a.wait_ns);
   }
