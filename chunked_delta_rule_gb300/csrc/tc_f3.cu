@@ -124,7 +124,8 @@ struct F3ChunkSmem {
   static constexpr uint32_t NCOLS = 256;
   static_assert(XQT + 64 * kGS * 4 <= RH + 32768 && RH + 32768 == AT, "R1 region");
   static_assert(ZT + 32768 <= AT, "T image and Z inside R1");
-  static_assert(4 * (kKP + 2) * 32 * 4 <= 6 * 2304, "recurrence scratch inside the N blocks");
+  static_assert(4 * 64 * 4 <= 6 * 2304, "spare rows of the recurrences inside the N blocks");
+  static_assert((128 * kKP + 64 * 12) * 4 <= 8 * 2304, "step operands inside F~ / H's region");
   static_assert(OG + 256 <= FH, "output tiles inside the product operands");
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
@@ -164,43 +165,34 @@ __device__ __forceinline__ float dot4(float4 g, float a, float b, float c, float
   return fmaf(g.w, d, fmaf(g.z, c, fmaf(g.y, b, fmaf(g.x, a, acc))));
 }
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  const unsigned long long pa = (unsigned long long)__float_as_uint(a.x) | ((unsigned long long)__float_as_uint(a.y) << 32);
-  const unsigned long long pb = (unsigned long long)__float_as_uint(b.x) | ((unsigned long long)__float_as_uint(b.y) << 32);
-  const unsigned long long pc = (unsigned long long)__float_as_uint(c.x) | ((unsigned long long)__float_as_uint(c.y) << 32);
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pa), "l"(pb), "l"(pc));
-  return make_float2(__uint_as_float((unsigned)d), __uint_as_float((unsigned)(d >> 32)));
-}
-
 // The sub-chunk's two K x K recurrences, F~ (undecayed) and H, side by side:
-// lane j holds column j of both (rows in pairs).  Step tau: the window rows
-// tau + r (r < W) take
+// lane j holds column j of both.  Step tau: the window rows tau + r (r < W) take
 //   d_r = G[tau + r, :] M_{tau-1},  M_tau = gamma M_{tau-1} + Delta_tau,
 //   Delta_tau[tau + r] = -gamma c m_{tau+r} d_r + c m_{tau+r} [j == tau + r]
 // (gamma = 1 for F~).  A row that stays in the window needs no new sum over
 // the K slots: d_r(tau) = gamma_{tau-1} d_{r+1}(tau - 1) + sum_a G[tau + r][tau - 1 + a]
 // Delta_{tau-1}[a]; only the row entering the window takes the full sum, and
 // one Gram element feeds both matrices.  The window is handled as kWMax rows
-// with the increments of rows past W masked to zero, so every index but the
-// step is static.  The increments reach their (moving) rows through this
-// lane's column of `dbuf` ([kKP + 2][32] floats, zero between uses: the K
-// slots, F~'s increments then H's, and a spare pair of rows).  After the update, outF[t][j] =
-// F~ column j . (X_i q_t) and outH[t][j] = H column j . (X_i q_t).
-__device__ __forceinline__ void sub_recurrences(const float* __restrict__ Gi, const float* __restrict__ xqt,
-                                                const float* __restrict__ gc, const float* __restrict__ ggm,
-                                                const float* __restrict__ ex, int i, int W, int j,
-                                                float* __restrict__ outF, float* __restrict__ outH,
-                                                float* __restrict__ dbuf, float2 (&f)[kKP / 2],
-                                                float2 (&hc)[kKP / 2]) {
-  float* spare = dbuf + kKP * 32;
+// with the increments of rows past W masked to zero.  The columns are kept in
+// rotated order (register k holds row (tau + k) mod kKP at step tau) so that
+// the window's rows sit in fixed registers while the steps run as a loop;
+// the rotation is a register move per row and step.  After the update,
+// outF[t][j] = F~ column j . (X_i q_t) and outH[t][j] = H column j . (X_i q_t);
+// lanes past the key slots store into `spare` ([2][32] floats).  The step's
+// operands are read as aligned 16-byte rows: `gr` [kL][kKP] the entering
+// row's Gram entries in the registers' order, `xqr` [kL][kKP] X_i q_t in that
+// order, `scg` [kL][12] the window rows' c m (zero past W) and gamma.  On
+// return f / hc hold the columns in row order.
+__device__ __forceinline__ void sub_recurrences(const float* __restrict__ Gi, const float* __restrict__ gr,
+                                                const float* __restrict__ xqr, const float* __restrict__ scg,
+                                                int i, int j, float* __restrict__ outF, float* __restrict__ outH,
+                                                float* __restrict__ spare, float (&f)[kKP], float (&hc)[kKP]) {
+  float fr[kKP], hr[kKP];
 #pragma unroll
-  for (int k = 0; k < kKP / 2; ++k) {
-    f[k] = make_float2(0.f, 0.f);
-    hc[k] = make_float2(0.f, 0.f);
+  for (int k = 0; k < kKP; ++k) {
+    fr[k] = 0.f;
+    hr[k] = 0.f;
   }
-#pragma unroll
-  for (int k = 0; k < kKP; ++k) dbuf[k * 32 + j] = 0.f;
   float pf[kWMax], ph[kWMax], lf[kWMax], lh[kWMax];  // previous step's window sums and increments
 #pragma unroll
   for (int r = 0; r < kWMax; ++r) {
@@ -210,74 +202,88 @@ __device__ __forceinline__ void sub_recurrences(const float* __restrict__ Gi, co
 #pragma unroll 1
   for (int tau = 0; tau < kL; ++tau) {
     const int t = kL * i + tau;
-    const float cs = gc[t], gm = ggm[t];
+    float sc[12];  // the window rows' c m (zero past W), then gamma
+#pragma unroll
+    for (int q = 0; q < 12; q += 4) {
+      const float4 v4 = *reinterpret_cast<const float4*>(scg + t * 12 + q);
+      sc[q] = v4.x; sc[q + 1] = v4.y; sc[q + 2] = v4.z; sc[q + 3] = v4.w;
+    }
+    const float gm = sc[kWMax];
     float df[kWMax], dh[kWMax];
+    // rows that stay: carried sums plus last step's increments (side by side)
     const float* gblk = Gi + tau * kGS + (tau > 0 ? tau - 1 : 0);
 #pragma unroll
-    for (int r = 0; r < kWMax - 1; ++r) {  // rows that stay: carried sums plus last step's increments
-      float af = pf[r + 1], ah = gprev * ph[r + 1];
-#pragma unroll
-      for (int a = 0; a < kWMax; ++a) {
-        const float g = gblk[r * kGS + a];
-        af = fmaf(g, lf[a], af);
-        ah = fmaf(g, lh[a], ah);
-      }
-      df[r] = af;
-      dh[r] = ah;
+    for (int r = 0; r < kWMax - 1; ++r) {
+      df[r] = pf[r + 1];
+      dh[r] = gprev * ph[r + 1];
     }
-    {  // the row entering the window: the full sums
-      const float* grow = Gi + (tau + kWMax - 1) * kGS;
-      float2 af = make_float2(0.f, 0.f), ah = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int a = 0; a < kWMax; ++a) {
+#pragma unroll
+      for (int r = 0; r < kWMax - 1; ++r) {
+        const float g = gblk[r * kGS + a];
+        df[r] = fmaf(g, lf[a], df[r]);
+        dh[r] = fmaf(g, lh[a], dh[r]);
+      }
+    }
+    {  // the row entering the window: the full sums (register k is row (tau + k) mod kKP,
+       // `gr` holds that row's Gram entries in the same order)
+      const float* grow = gr + tau * kKP;
+      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
       for (int q = 0; q < kKP; q += 4) {
         const float4 g4 = *reinterpret_cast<const float4*>(grow + q);
-        const float2 g01 = make_float2(g4.x, g4.y), g23 = make_float2(g4.z, g4.w);
-        af = ffma2(g01, f[q / 2], af);
-        af = ffma2(g23, f[q / 2 + 1], af);
-        ah = ffma2(g01, hc[q / 2], ah);
-        ah = ffma2(g23, hc[q / 2 + 1], ah);
+        a0 = fmaf(g4.x, fr[q], a0); a1 = fmaf(g4.y, fr[q + 1], a1);
+        a0 = fmaf(g4.z, fr[q + 2], a0); a1 = fmaf(g4.w, fr[q + 3], a1);
+        b0 = fmaf(g4.x, hr[q], b0); b1 = fmaf(g4.y, hr[q + 1], b1);
+        b0 = fmaf(g4.z, hr[q + 2], b0); b1 = fmaf(g4.w, hr[q + 3], b1);
       }
-      df[kWMax - 1] = af.x + af.y;
-      dh[kWMax - 1] = ah.x + ah.y;
+      df[kWMax - 1] = a0 + a1;
+      dh[kWMax - 1] = b0 + b1;
     }
 #pragma unroll
-    for (int r = 0; r < kWMax; ++r) {
-      const float sc = r < W ? cs * ex[tau + r] : 0.f;
-      const float inj = j == tau + r ? sc : 0.f;
-      const float incf = fmaf(-sc, df[r], inj), inch = fmaf(-gm * sc, dh[r], inj);
-      dbuf[(tau + r) * 32 + j] = incf;
+    for (int k = 0; k < kKP; ++k) hr[k] *= gm;
+#pragma unroll
+    for (int r = 0; r < kWMax; ++r) {  // the window rows sit in registers 0 .. kWMax - 1
+      const float inj = j == tau + r ? sc[r] : 0.f;
+      const float incf = fmaf(-sc[r], df[r], inj), inch = fmaf(-gm * sc[r], dh[r], inj);
+      fr[r] += incf;
+      hr[r] += inch;
       pf[r] = df[r]; ph[r] = dh[r]; lf[r] = incf; lh[r] = inch;
     }
     gprev = gm;
-    const float2 gm2 = make_float2(gm, gm), one2 = make_float2(1.f, 1.f);
-#pragma unroll
-    for (int k = 0; k < kKP / 2; ++k)  // F~ += Delta
-      f[k] = ffma2(make_float2(dbuf[(2 * k) * 32 + j], dbuf[(2 * k + 1) * 32 + j]), one2, f[k]);
-#pragma unroll
-    for (int r = 0; r < kWMax; ++r) dbuf[(tau + r) * 32 + j] = lh[r];
-#pragma unroll
-    for (int k = 0; k < kKP / 2; ++k)  // H = gamma H + Delta
-      hc[k] = ffma2(hc[k], gm2, make_float2(dbuf[(2 * k) * 32 + j], dbuf[(2 * k + 1) * 32 + j]));
-#pragma unroll
-    for (int r = 0; r < kWMax; ++r) dbuf[(tau + r) * 32 + j] = 0.f;
-    const float* xq = xqt + t * kGS;
-    float2 sf = make_float2(0.f, 0.f), sh = make_float2(0.f, 0.f);
+    const float* xq = xqr + t * kKP;  // X_i q_t in the registers' row order
+    float s0 = 0.f, s1 = 0.f, u0 = 0.f, u1 = 0.f;
 #pragma unroll
     for (int q = 0; q < kKP; q += 4) {
       const float4 x4 = *reinterpret_cast<const float4*>(xq + q);
-      const float2 x01 = make_float2(x4.x, x4.y), x23 = make_float2(x4.z, x4.w);
-      sf = ffma2(x01, f[q / 2], sf);
-      sf = ffma2(x23, f[q / 2 + 1], sf);
-      sh = ffma2(x01, hc[q / 2], sh);
-      sh = ffma2(x23, hc[q / 2 + 1], sh);
+      s0 = fmaf(x4.x, fr[q], s0); s1 = fmaf(x4.y, fr[q + 1], s1);
+      s0 = fmaf(x4.z, fr[q + 2], s0); s1 = fmaf(x4.w, fr[q + 3], s1);
+      u0 = fmaf(x4.x, hr[q], u0); u1 = fmaf(x4.y, hr[q + 1], u1);
+      u0 = fmaf(x4.z, hr[q + 2], u0); u1 = fmaf(x4.w, hr[q + 3], u1);
     }
     // lanes past the key slots store into the spare rows: no branch, so the
     // warp stays converged through the steps
     float* of = j < kKP ? outF + t * kKP + j : spare + j;
     float* oh = j < kKP ? outH + t * kKP + j : spare + 32 + j;
-    *of = sf.x + sf.y;
-    *oh = sh.x + sh.y;
+    *of = s0 + s1;
+    *oh = u0 + u1;
+    // rotate: register k takes row (tau + 1 + k) mod kKP
+    const float f0 = fr[0], h0 = hr[0];
+#pragma unroll
+    for (int k = 0; k < kKP - 1; ++k) {
+      fr[k] = fr[k + 1];
+      hr[k] = hr[k + 1];
+    }
+    fr[kKP - 1] = f0;
+    hr[kKP - 1] = h0;
     __syncwarp();
+  }
+  // after kL steps register k holds row (kL + k) mod kKP
+#pragma unroll
+  for (int k = 0; k < kKP; ++k) {
+    f[(kL + k) % kKP] = fr[k];
+    hc[(kL + k) % kKP] = hr[k];
   }
 }
 
@@ -461,19 +467,38 @@ __global__ void __launch_bounds__(256, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // the recurrences' step operands as aligned rows (in F~ / H's region, free
+    // until the recurrences end): per step t = 16 i + tau, the Gram row of key
+    // tau + kWMax - 1 and X_i q_t in the rotated order (slot (tau + k) mod kKP
+    // at k), and c m of the window rows with gamma
+    float* GRr = FH;
+    float* XQR = FH + 64 * kKP;
+    float* SCg = FH + 128 * kKP;
+    for (int u = tid; u < 64 * kKP; u += 256) {
+      const int t = u / kKP, k = u - kKP * t, i = t >> 4, tau = t & 15;
+      const int col = tau + k >= kKP ? tau + k - kKP : tau + k;
+      GRr[u] = GS[(kKP * i + tau + kWMax - 1) * kGS + kKP * i + col];
+      XQR[u] = XQT[t * kGS + kKP * i + col];
+    }
+    for (int u = tid; u < 64 * 12; u += 256) {
+      const int t = u / 12, r = u - 12 * t, i = t >> 4, tau = t & 15;
+      float v = 0.f;
+      if (r < W && r < kWMax) v = gt[L::G_C + t] * gt[L::G_EX + kKP * i + tau + r];
+      else if (r == kWMax) v = gt[L::G_GMA + t];
+      SCg[u] = v;
+    }
+    __syncthreads();
     if (warp < 4) {  // the recurrences: warp i takes sub-chunk i, F~ and H side by side
       const int i = warp;
-      float2 f[kKP / 2], hc[kKP / 2];
-      sub_recurrences(GS + (kKP * i) * kGS + kKP * i, XQT + kKP * i, gt + L::G_C, gt + L::G_GMA,
-                      gt + L::G_EX + kKP * i, i, W, lane, AHf, AHf + 64 * kKP,
-                      NBf + i * (kKP + 2) * 32, f, hc);
+      float f[kKP], hc[kKP];
+      sub_recurrences(GS + (kKP * i) * kGS + kKP * i, GRr + kL * i * kKP, XQR, SCg, i, lane, AHf,
+                      AHf + 64 * kKP, NBf + i * 64, f, hc);
+      named_bar(2, 128);  // every recurrence is done with the step operands in F~ / H's region
       if (lane < kKP) {
 #pragma unroll
-        for (int k = 0; k < kKP / 2; ++k) {
-          FH[i * 576 + (2 * k) * kKP + lane] = f[k].x;
-          FH[i * 576 + (2 * k + 1) * kKP + lane] = f[k].y;
-          FH[4 * 576 + i * 576 + (2 * k) * kKP + lane] = hc[k].x;
-          FH[4 * 576 + i * 576 + (2 * k + 1) * kKP + lane] = hc[k].y;
+        for (int k = 0; k < kKP; ++k) {
+          FH[i * 576 + k * kKP + lane] = f[k];
+          FH[4 * 576 + i * 576 + k * kKP + lane] = hc[k];
         }
       }
     } else {
