@@ -124,7 +124,7 @@ struct F3ChunkSmem {
   static constexpr uint32_t NCOLS = 256;
   static_assert(XQT + 64 * kGS * 4 <= RH + 32768 && RH + 32768 == AT, "R1 region");
   static_assert(ZT + 32768 <= AT, "T image and Z inside R1");
-  static_assert(4 * 64 * 4 <= 6 * 2304, "spare rows of the recurrences inside the N blocks");
+  static_assert((4 * 64 + kNS * kKP * 16) * 4 <= 6 * 2304, "spare rows and Gram band inside the N blocks");
   static_assert((128 * kKP + 64 * 12) * 4 <= 8 * 2304, "step operands inside F~ / H's region");
   static_assert(OG + 256 <= FH, "output tiles inside the product operands");
   static_assert(TOTAL <= 232448, "shared memory budget");
@@ -180,10 +180,12 @@ __device__ __forceinline__ float dot4(float4 g, float a, float b, float c, float
 // outF[t][j] = F~ column j . (X_i q_t) and outH[t][j] = H column j . (X_i q_t);
 // lanes past the key slots store into `spare` ([2][32] floats).  The step's
 // operands are read as aligned 16-byte rows: `gr` [kL][kKP] the entering
-// row's Gram entries in the registers' order, `xqr` [kL][kKP] X_i q_t in that
+// row's Gram entries in the registers' order, `gb` [kKP][16] the Gram band
+// around the diagonal (row rho: G[rho][rho - 8 + o], zero off the block),
+// `xqr` [kL][kKP] X_i q_t in that
 // order, `scg` [kL][12] the window rows' c m (zero past W) and gamma.  On
 // return f / hc hold the columns in row order.
-__device__ __forceinline__ void sub_recurrences(const float* __restrict__ Gi, const float* __restrict__ gr,
+__device__ __forceinline__ void sub_recurrences(const float* __restrict__ gb, const float* __restrict__ gr,
                                                 const float* __restrict__ xqr, const float* __restrict__ scg,
                                                 int i, int j, float* __restrict__ outF, float* __restrict__ outH,
                                                 float* __restrict__ spare, float (&f)[kKP], float (&hc)[kKP]) {
@@ -210,21 +212,28 @@ __device__ __forceinline__ void sub_recurrences(const float* __restrict__ Gi, co
     }
     const float gm = sc[kWMax];
     float df[kWMax], dh[kWMax];
-    // rows that stay: carried sums plus last step's increments (side by side)
-    const float* gblk = Gi + tau * kGS + (tau > 0 ? tau - 1 : 0);
+    // rows that stay: carried sums plus last step's increments (side by side);
+    // `gb` row rho holds G[rho][rho - 8 + o] at o, so row tau + r needs
+    // o = 7 - r + a for the columns tau - 1 + a
 #pragma unroll
     for (int r = 0; r < kWMax - 1; ++r) {
-      df[r] = pf[r + 1];
-      dh[r] = gprev * ph[r + 1];
-    }
+      float gv[12];
+      const int b0 = (7 - r) / 4;  // first aligned block covering o = 7 - r .. 15 - r
+      const float* row = gb + (tau + r) * 16 + 4 * b0;
 #pragma unroll
-    for (int a = 0; a < kWMax; ++a) {
-#pragma unroll
-      for (int r = 0; r < kWMax - 1; ++r) {
-        const float g = gblk[r * kGS + a];
-        df[r] = fmaf(g, lf[a], df[r]);
-        dh[r] = fmaf(g, lh[a], dh[r]);
+      for (int q = 0; q < 3; ++q) {
+        const float4 v4 = *reinterpret_cast<const float4*>(row + 4 * q);
+        gv[4 * q] = v4.x; gv[4 * q + 1] = v4.y; gv[4 * q + 2] = v4.z; gv[4 * q + 3] = v4.w;
       }
+      float af = pf[r + 1], ah = gprev * ph[r + 1];
+#pragma unroll
+      for (int a = 0; a < kWMax; ++a) {
+        const float g = gv[7 - r + a - 4 * b0];
+        af = fmaf(g, lf[a], af);
+        ah = fmaf(g, lh[a], ah);
+      }
+      df[r] = af;
+      dh[r] = ah;
     }
     {  // the row entering the window: the full sums (register k is row (tau + k) mod kKP,
        // `gr` holds that row's Gram entries in the same order)
@@ -480,6 +489,11 @@ __global__ void __launch_bounds__(256, 1)
       GRr[u] = GS[(kKP * i + tau + kWMax - 1) * kGS + kKP * i + col];
       XQR[u] = XQT[t * kGS + kKP * i + col];
     }
+    float* GBd = NBf + 256;  // after the recurrences' spare rows
+    for (int u = tid; u < kNS * kKP * 16; u += 256) {
+      const int i = u / (kKP * 16), rem = u - i * kKP * 16, rho = rem >> 4, o = rem & 15, col = rho - 8 + o;
+      GBd[u] = (col >= 0 && col < kKP) ? GS[(kKP * i + rho) * kGS + kKP * i + col] : 0.f;
+    }
     for (int u = tid; u < 64 * 12; u += 256) {
       const int t = u / 12, r = u - 12 * t, i = t >> 4, tau = t & 15;
       float v = 0.f;
@@ -491,7 +505,7 @@ __global__ void __launch_bounds__(256, 1)
     if (warp < 4) {  // the recurrences: warp i takes sub-chunk i, F~ and H side by side
       const int i = warp;
       float f[kKP], hc[kKP];
-      sub_recurrences(GS + (kKP * i) * kGS + kKP * i, GRr + kL * i * kKP, XQR, SCg, i, lane, AHf,
+      sub_recurrences(GBd + i * kKP * 16, GRr + kL * i * kKP, XQR, SCg, i, lane, AHf,
                       AHf + 64 * kKP, NBf + i * 64, f, hc);
       named_bar(2, 128);  // every recurrence is done with the step operands in F~ / H's region
       if (lane < kKP) {
