@@ -263,15 +263,15 @@ def cpu_baseline(w, budget_s=20.0) -> dict:
                       f"single-threaded worker processes, median of {len(times)} run(s)"}
 
 
-def traffic_for(kernel: str):
+def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel (else None)."""
+    on the current source of that kernel and on this workload (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path)).get(kernel)
     except Exception:
         return None
-    if not rec:
+    if not rec or rec.get("workload") != workload:
         return None
     import hashlib
     src = os.path.join(ROOT, "chunked_delta_rule_gb300", "csrc", rec["source"])
@@ -759,7 +759,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
             "data": "synthetic",
             "config": bench_config(w, world, len(sets), abytes, args.prologue),
-            "roofline": dict(roof, traffic=traffic_for(kernel), kernel=kernel,
+            "roofline": dict(roof, traffic=traffic_for(kernel, w.name), kernel=kernel,
                              algorithmic_bytes=abytes, algorithmic_flops=algorithmic_flops(w),
                              kernel_algorithmic_bytes=kbytes[dom], step_achieved=step_achieved,
                              step_frac=step_achieved / hbm_peak),
