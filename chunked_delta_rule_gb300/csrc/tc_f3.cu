@@ -161,10 +161,6 @@ __device__ __forceinline__ __nv_bfloat16 pair_v(const F3Args& a, int b, int h, i
   return a.winv_in[(((size_t)b * a.H + h) * Wr + ring_slot(pos + j, Wr)) * 64 + col];
 }
 
-__device__ __forceinline__ float dot4(float4 g, float a, float b, float c, float d, float acc) {
-  return fmaf(g.w, d, fmaf(g.z, c, fmaf(g.y, b, fmaf(g.x, a, acc))));
-}
-
 // The sub-chunk's two K x K recurrences, F~ (undecayed) and H, side by side:
 // lane j holds column j of both.  Step tau: the window rows tau + r (r < W) take
 //   d_r = G[tau + r, :] M_{tau-1},  M_tau = gamma M_{tau-1} + Delta_tau,
@@ -517,8 +513,8 @@ __global__ void __launch_bounds__(256, 1)
       }
     } else {
       // meanwhile, once the previous item's output tiles have left (they
-      // overlay these): X~ row (j, kappa) = exp(g_last - g_j) x, and a zeroed
-      // [Tf | Th] image
+      // overlay these): X~ row (j, kappa) = exp(g_last - g_j) x, and zeroed
+      // [Tf | Th] and P^T images
       if (tid == 128) bulk_wait_read0();
       named_bar(1, 128);
       for (int u = tid - 128; u < kNK * 8; u += 128) {
@@ -536,52 +532,77 @@ __global__ void __launch_bounds__(256, 1)
       }
       for (int u = tid - 128; u < 36864 / 16; u += 128)
         *reinterpret_cast<uint4*>(sm + L::TB + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
+      for (int u = tid - 128; u < 12288 / 16; u += 128)  // P^T: its nonzero blocks are written below
+        *reinterpret_cast<uint4*>(sm + L::AT + 12288 + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
-    // N_ij = exp(g_i - g_j) F~_i G_ij (j < i) and P^T
-    for (int u = tid; u < 6 * kKP * 6; u += 256) {
-      const int pi = u / (kKP * 6), rem = u - pi * kKP * 6, kap = rem / 6, q4 = 4 * (rem - 6 * (rem / 6));
-      const int i = pi < 1 ? 1 : pi < 3 ? 2 : 3, j = pi - (i * (i - 1)) / 2;
-      const float* Fr = FH + i * 576 + kap * kKP;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // N_ij = exp(g_i - g_j) F~_i G_ij (j < i) and the nonzero blocks of P^T,
+    // in 4 x 4 register tiles (the zero blocks of P^T were written above)
+    for (int u = tid; u < 6 * 36 + 6 * 24; u += 256) {
+      if (u < 6 * 36) {  // N tile: rows 4 tr.., columns 4 tc.. of pair pi
+        const int pi = u / 36, rem = u - 36 * pi, tr = rem / 6, tc = rem - 6 * tr;
+        const int i = pi < 1 ? 1 : pi < 3 ? 2 : 3, j = pi - (i * (i - 1)) / 2;
+        float acc[4][4] = {};
 #pragma unroll
-      for (int kk = 0; kk < kKP; ++kk) {
-        const float fv = Fr[kk];
-        const float4 g4 = *reinterpret_cast<const float4*>(GS + (kKP * i + kk) * kGS + kKP * j + q4);
-        acc[0] = fmaf(fv, g4.x, acc[0]);
-        acc[1] = fmaf(fv, g4.y, acc[1]);
-        acc[2] = fmaf(fv, g4.z, acc[2]);
-        acc[3] = fmaf(fv, g4.w, acc[3]);
-      }
-      const float sc = __expf(gt[L::G_END + i] - gt[L::G_END + j]);
-      *reinterpret_cast<float4*>(NBf + pi * 576 + kap * kKP + q4) =
-          make_float4(sc * acc[0], sc * acc[1], sc * acc[2], sc * acc[3]);
-    }
-    for (int u = tid; u < kNK * 8; u += 256) {  // P^T row (j, kappa), steps 8 tg .. 8 tg + 7
-      const int k = u % kNK, tg = u / kNK, jb = k / kKP, i = tg >> 1;  // a warp shares tg
-      uint32_t pk[4] = {0u, 0u, 0u, 0u};
-      if (jb < i) {
-        float gcol[kKP];  // G[(i, .)][(j, kappa)] = G[(j, kappa)][(i, .)]
+        for (int kk = 0; kk < kKP; kk += 4) {
+          float fa[4][4], gb4[4][4];
 #pragma unroll
-        for (int q = 0; q < kKP; q += 4) {
-          const float4 g4 = *reinterpret_cast<const float4*>(GS + k * kGS + kKP * i + q);
-          gcol[q] = g4.x; gcol[q + 1] = g4.y; gcol[q + 2] = g4.z; gcol[q + 3] = g4.w;
+          for (int a = 0; a < 4; ++a) {
+            const float4 f4 = *reinterpret_cast<const float4*>(FH + i * 576 + (4 * tr + a) * kKP + kk);
+            fa[a][0] = f4.x; fa[a][1] = f4.y; fa[a][2] = f4.z; fa[a][3] = f4.w;
+            const float4 g4 = *reinterpret_cast<const float4*>(GS + (kKP * i + kk + a) * kGS + kKP * j + 4 * tc);
+            gb4[a][0] = g4.x; gb4[a][1] = g4.y; gb4[a][2] = g4.z; gb4[a][3] = g4.w;
+          }
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(fa[a][q], gb4[q][b], acc[a][b]);
         }
-        const float gj = gt[L::G_END + jb];
-        float pv[8];
+        const float sc = __expf(gt[L::G_END + i] - gt[L::G_END + j]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int t = 8 * tg + e;
-          const float* at = AHf + t * kKP;
-          float s = 0.f;
+        for (int a = 0; a < 4; ++a)
+          *reinterpret_cast<float4*>(NBf + pi * 576 + (4 * tr + a) * kKP + 4 * tc) =
+              make_float4(sc * acc[a][0], sc * acc[a][1], sc * acc[a][2], sc * acc[a][3]);
+      } else {  // P tile: steps 16 i + 4 tt.., keys (j, 4 tk..) of block pair pi
+        const int w = u - 6 * 36, pi = w / 24, rem = w - 24 * pi, tt = rem / 6, tk = rem - 6 * tt;
+        const int i = pi < 1 ? 1 : pi < 3 ? 2 : 3, j = pi - (i * (i - 1)) / 2;
+        const int t0 = kL * i + 4 * tt, k0 = kKP * j + 4 * tk;
+        float acc[4][4] = {};  // [step a][key b]: sum_kk a~_t[kk] G[(j, kappa)][(i, kk)]
 #pragma unroll
-          for (int q = 0; q < kKP; q += 4) s = dot4(*reinterpret_cast<const float4*>(at + q), gcol[q], gcol[q + 1], gcol[q + 2], gcol[q + 3], s);
-          pv[e] = __expf(gt[L::G_G + t] - gj) * (XQT[t * kGS + k] - s);
+        for (int kk = 0; kk < kKP; kk += 4) {
+          float av[4][4], gv[4][4];
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const float4 a4 = *reinterpret_cast<const float4*>(AHf + (t0 + a) * kKP + kk);
+            av[a][0] = a4.x; av[a][1] = a4.y; av[a][2] = a4.z; av[a][3] = a4.w;
+            const float4 g4 = *reinterpret_cast<const float4*>(GS + (k0 + a) * kGS + kKP * i + kk);
+            gv[a][0] = g4.x; gv[a][1] = g4.y; gv[a][2] = g4.z; gv[a][3] = g4.w;
+          }
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc[a][b] = fmaf(av[a][q], gv[b][q], acc[a][b]);
+        }
+        const float gj = gt[L::G_END + j];
+        float pv[4][4];  // [key b][step a]
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float e = __expf(gt[L::G_G + t0 + a] - gj);
+          const float4 x4 = *reinterpret_cast<const float4*>(XQT + (t0 + a) * kGS + k0);
+          pv[0][a] = e * (x4.x - acc[a][0]);
+          pv[1][a] = e * (x4.y - acc[a][1]);
+          pv[2][a] = e * (x4.z - acc[a][2]);
+          pv[3][a] = e * (x4.w - acc[a][3]);
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(pv[2 * e], pv[2 * e + 1]);
+        for (int b = 0; b < 4; ++b)  // P^T row (j, kappa), steps t0 .. t0 + 3: one 8-byte store
+          *reinterpret_cast<uint2*>(sm + L::AT + 12288 + sw128(k0 + b, t0)) =
+              make_uint2(pack_bf16(pv[b][0], pv[b][1]), pack_bf16(pv[b][2], pv[b][3]));
       }
-      *reinterpret_cast<uint4*>(sm + L::AT + 12288 + sw128(k, 8 * tg)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
     // the block-diagonal right factor [bd(exp(g_i) F~_i) | bd(H_i)] (bf16
     // image, MN-major B over three atoms; the rest of it was zeroed above)
