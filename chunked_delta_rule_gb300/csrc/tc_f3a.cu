@@ -524,7 +524,9 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
     for (int c = 0; c < NC; ++c) {
       const int s = c % NST;
       if (!mbar_wait(&full[s], (uint32_t)((c / NST) & 1), a.wait_ns)) fail();
-      if (named_bar_any(1, 64, *abort_flag != 0)) break;
+      // each chain thread leaves on its own after a failure: nothing in this
+      // loop waits on the other chain threads (every wait is bounded)
+      if (*abort_flag) break;
       const uint8_t* st = stage(s);
       const float gl = reinterpret_cast<const float*>(st + L::GO)[63];
 #pragma unroll
