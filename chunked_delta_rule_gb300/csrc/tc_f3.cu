@@ -33,12 +33,13 @@
 // That is the Falcon-1 chain form, so:
 //  (a) f3_chunk_kernel, persistent over (b, h, chunk), one CTA per SM:
 //      TMA of the stacked keys, values and queries; the key Gram band and
-//      X_s Q^T in one tcgen05 product (M = 128, N = 160); the eight small
-//      recurrences (sub-chunk x {F~, H}) on the CUDA cores, a lane per column;
-//      N, P, X~ and the block substitution for [Tf | Th] (bf16 image); then
-//      [X~^T ; P] [Tf | Th] (M = 128, N = 192, K = 96) and, from its rows
-//      plus the block-diagonal terms, [-M ; Q' - Gamma Q] and [b ; O0] by
-//      two more products (K = 96); the four tiles leave by one bulk copy.
+//      X_s Q^T in one tcgen05 product (M = 128, N = 160); the sub-chunk
+//      recurrences (F~ and H of a sub-chunk per warp) on the CUDA cores, a
+//      lane per column; N, P, X~ and T = (I + N)^{-1} in closed block form
+//      (bf16 image); then Z = [X~^T ; P] T (N = 96), [X~^T ; P] [Tf | Th] =
+//      Z [bd(exp(g_i) F~_i) | bd(H_i)] (N = 192) and, from its rows plus the
+//      block-diagonal terms, [-M ; Q' - Gamma Q] and [b ; O0] by two more
+//      products (K = 96); the four tiles leave by one bulk copy.
 //  (b) f3_chain_kernel, two CTAs per (b, h), each owning 32 value columns:
 //      acc = [-M ; Q'] S0 (one tcgen05 product per chunk, N = 32), then
 //      S1 = Gamma_last S0 + b + acc_top on the fp32 state in registers and
@@ -87,7 +88,7 @@ struct F3Args {
   __nv_bfloat16* winv_out;
   int64_t* pos_out;
   uint32_t* status;
-  uint8_t* ws_f3;     // per chunk: [-M ; Q'] | b | O0 | Gamma_last (kF3ChunkWs bytes)
+  uint8_t* ws_f3;     // per chunk: [-M ; Q'] | b | O0 | Gamma_last (kF3Rec bytes)
   __nv_bfloat16* o;   // [B, T, H, 64]
   uint64_t wait_ns;   // limit of every bounded wait
 };
@@ -107,11 +108,14 @@ struct F3ChunkSmem {
   // bf16 image of T = (I + N)^{-1} (MN-major B, two 96-row atoms) and the
   // K-major A tile Z = [X~^T ; P] T (128 rows x 96, two slabs)
   static constexpr size_t TI = R1, ZT = R1 + 24576;
-  // [X~ | P^T] (MN-major A, two 96-row atoms), then [Tf | Th] (MN-major B,
-  // three 96-row atoms); the output tiles reuse both once the product read them
+  // [X~ | P^T] (MN-major A, two 96-row atoms), then the block-diagonal right
+  // factor [bd(exp(g_i) F~_i) | bd(H_i)] (MN-major B, three 96-row atoms);
+  // the output tiles reuse both once the products read them
   static constexpr size_t AT = 98304, TB = AT + 24576;
   static constexpr size_t OMQ = AT, OB = AT + 16384, OO = AT + 24576, OG = AT + 32768;
-  // fp32: F~_i, H_i (24 x 24 each), a~_t, h_t (64 x 24 each), N_ij (6 blocks)
+  // fp32: F~_i, H_i (24 x 24 each; before them the recurrences' step
+  // operands, after them T_20), a~_t, h_t (64 x 24 each), N_ij (6 blocks;
+  // before them the recurrences' spare rows and Gram band)
   static constexpr size_t FH = TB + 36864, AH = FH + 8 * 2304, NB = AH + 2 * 64 * 96;
   static constexpr size_t GT = NB + 6 * 2304;
   // gates (fp32 offsets in GT)
