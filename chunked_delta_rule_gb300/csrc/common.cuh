@@ -139,7 +139,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Limit of the bounded device-side waits of the next launch (2 s unless the
 // failure-detection test hook set another), and whether that hook asked the
-// next Falcon-1 / 1A tensor-core call to stall one wait (consumed here).
+// next Falcon-1 / 1A, 3 or 3A tensor-core call to stall one wait (consumed here).
 uint64_t wait_limit_ns();
 bool take_test_stall();
 // Device address of the allocation-free entry point's scratch array on the

@@ -91,6 +91,8 @@ struct F3Args {
   uint8_t* ws_f3;     // per chunk: [-M ; Q'] | b | O0 | Gamma_last (kF3Rec bytes)
   __nv_bfloat16* o;   // [B, T, H, 64]
   uint64_t wait_ns;   // limit of every bounded wait
+  int stall;          // failure-detection test hook: the per-chunk kernel's first CTA waits on
+                      // a barrier that nothing completes, and so records a timeout
 };
 
 // per chunk in the workspace: [-M ; Q'] (128-row bf16 tile) | b | O0 (64-row
@@ -324,6 +326,7 @@ __global__ void __launch_bounds__(256, 1)
     *abort_flag = 0;
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
+    mbar_init(&bar[2], 1);  // the test hook's (never completed)
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -366,19 +369,25 @@ __global__ void __launch_bounds__(256, 1)
   // loads issued and load phases seen complete (thread 0); products committed
   // (thread 0) and product phases seen complete (every thread)
   int issued = 0, n_loaded = 0, n_commit = 0, n_mma = 0;
-  if (tid == 0 && (int)blockIdx.x < n_items) {
-    issue_loads(blockIdx.x);
+  // failure-detection test hook: the first CTA waits, before it loads
+  // anything, on a barrier that nothing completes; the bounded wait runs
+  // out, the timeout is recorded and the CTA takes no item
+  if (a.stall && blockIdx.x == 0 && tid == 0 && !mbar_wait(&bar[2], 0, a.wait_ns)) fail();
+  __syncthreads();
+  const int first_item = *abort_flag ? n_items : (int)blockIdx.x;
+  if (tid == 0 && first_item < n_items) {
+    issue_loads(first_item);
     ++issued;
   }
   float lam_n = 0.f, beta_n = 0.f;
-  if ((int)blockIdx.x < n_items) gate_in(blockIdx.x, lam_n, beta_n);
+  if (first_item < n_items) gate_in(first_item, lam_n, beta_n);
   auto wait_mma = [&]() {
     if (mbar_wait(&bar[1], (uint32_t)(n_mma & 1), a.wait_ns)) ++n_mma;
     else fail();
     tc_fence_after();
   };
   int it = 0;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+  for (int item = first_item; item < n_items; item += gridDim.x, ++it) {
     const int c = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H;
     const int t0 = c * kC, j0 = t0 - W + 1;
     const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
@@ -1091,6 +1100,7 @@ int launch_tc_f3(const FwdArgs& fa) {
   ta.ws_f3 = reinterpret_cast<uint8_t*>(fa.ws) + 256;
   ta.o = reinterpret_cast<__nv_bfloat16*>(fa.o);
   ta.wait_ns = wait_limit_ns();
+  ta.stall = take_test_stall() ? 1 : 0;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, fa.q, fa.B, fa.T, fa.H, 64, 64) || !make_map(&mk, fa.k, fa.B, fa.T, fa.H, 64, kKP) ||
       !make_map(&mv, fa.v, fa.B, fa.T, fa.H, 64, kKP))

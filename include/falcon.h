@@ -336,8 +336,9 @@ int falcon_workspace_status(const void* workspace, void* stream);
 
 /* Test hook of the failure-detection path (no counterpart on the pages; not
  * for production use).  wait_limit_ns > 0 sets the limit of the bounded
- * device-side waits of the Falcon-1 / 1A tensor-core kernels launched from
- * now on in this process (0 restores 2 s).  stall != 0 makes the next such
+ * device-side waits of the Falcon-1 / 1A, 3 and 3A tensor-core kernels
+ * launched from now on in this process (0 restores 2 s; the Falcon-2 kernel
+ * keeps 2 s).  stall != 0 makes the next such
  * call's per-chunk kernel wait once, before it loads anything, on a barrier
  * that nothing completes: that wait runs out after the limit, the timeout is
  * recorded as described at falcon_workspace_status and the call's later

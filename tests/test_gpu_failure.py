@@ -1,5 +1,5 @@
-"""Failure detection of the tensor-core chunk forward, tested without a GPU
-fault.  Every wait of those kernels is bounded; the test hook shortens the
+"""Failure detection of the tensor-core chunk forward (Falcon-1 at d = 64
+and 128, Falcon-3 and Falcon-3A), tested without a GPU fault.  Every wait of those kernels is bounded; the test hook shortens the
 limit and makes one wait, on a barrier that nothing completes, run out.  The
 kernel must record the timeout in the workspace status word, give up its
 chunks, free what it holds and return; the kernel after it must compute
@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from helpers import TOL, oracle_full, params_for, rel_err
-from workloads import LM_F1, LONG_F1, make_inputs
+from workloads import LM_F1, LONG_F1, WINDOW_F3, WINDOW_F3A, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -26,8 +26,9 @@ def F():
 
 
 @pytest.mark.parametrize("w", [LM_F1.with_(B=1, T=300, H=2), LONG_F1.with_(B=1, T=200, H=2,
-                                                                             force_zero_gamma=0.0)],
-                         ids=["d64", "d128"])
+                                                                             force_zero_gamma=0.0),
+                               WINDOW_F3.with_(B=1, T=300, H=2), WINDOW_F3A.with_(B=1, T=300, H=2)],
+                         ids=["d64", "d128", "falcon3", "falcon3a"])
 def test_stalled_wait_is_reported_and_the_context_survives(F, w):
     x = make_inputs(w, device="cuda")
     p = params_for(F, w)
