@@ -971,32 +971,37 @@ __global__ void __launch_bounds__(F3ChainSmem::kThreads, 1) f3_chain_kernel(F3Ar
         }
       }
       if (!ok) fail();
-      if (named_bar_any(1, 64, *abort_flag != 0)) break;
+      // a product that was not issued leaves mdone incomplete: the bounded
+      // wait runs out and the barrier below takes every chain thread out
       if (!mbar_wait(&mdone[p], (uint32_t)((c / NB) & 1), a.wait_ns)) fail();
-      if (named_bar_any(1, 64, *abort_flag != 0)) break;
-      tc_fence_after();
-      uint32_t acc[32];
-      tmem_ld32(tmem + lane_off + 32 * p, acc);
-      tmem_wait_ld();
-      tc_fence_before();
-      const uint8_t* st = stage(s);
-      const float gl = reinterpret_cast<const float*>(st + L::GO)[0];
+      // the accumulator is read warp by warp (a warp that saw a failure
+      // skips it); the barrier at the end of the chunk takes both warps out
+      if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+        tc_fence_after();
+        uint32_t acc[32];
+        tmem_ld32(tmem + lane_off + 32 * p, acc);
+        tmem_wait_ld();
+        tc_fence_before();
+        const uint8_t* st = stage(s);
+        const float gl = reinterpret_cast<const float*>(st + L::GO)[0];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {  // S1 = Gamma_last S0 + b + (-M S0), row r, this CTA's columns
-        const uint4 raw = *reinterpret_cast<const uint4*>(st + L::BO + sw128(r, c0 + 8 * j));
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        for (int j = 0; j < 4; ++j) {  // S1 = Gamma_last S0 + b + (-M S0), row r, this CTA's columns
+          const uint4 raw = *reinterpret_cast<const uint4*>(st + L::BO + sw128(r, c0 + 8 * j));
+          const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 b2 = __bfloat1622float2(pb[e]);
-          const int n = 8 * j + 2 * e;
-          sreg[n] = fmaf(gl, sreg[n], b2.x + __uint_as_float(acc[n]));
-          sreg[n + 1] = fmaf(gl, sreg[n + 1], b2.y + __uint_as_float(acc[n + 1]));
+          for (int e = 0; e < 4; ++e) {
+            const float2 b2 = __bfloat1622float2(pb[e]);
+            const int n = 8 * j + 2 * e;
+            sreg[n] = fmaf(gl, sreg[n], b2.x + __uint_as_float(acc[n]));
+            sreg[n + 1] = fmaf(gl, sreg[n + 1], b2.y + __uint_as_float(acc[n + 1]));
+          }
         }
+        mbar_arrive(&empty[s]);
+        if (c + 1 < NC) store_s((c + 1) % NB);  // its previous reader (chunk c + 1 - NB) is done
+        fence_proxy_async();
       }
-      mbar_arrive(&empty[s]);
-      if (c + 1 < NC) store_s((c + 1) % NB);  // its previous reader (chunk c + 1 - NB) is done
-      fence_proxy_async();
-      named_bar(1, 64);
+      // the next chunk's S0 image is complete before thread 0 issues its product
+      if (named_bar_any(1, 64, *abort_flag != 0)) break;
     }
     if (!*abort_flag && a.S_out) {
       float* dst = a.S_out + ((size_t)bh * 64 + r) * 64 + c0;
