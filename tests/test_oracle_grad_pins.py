@@ -8,6 +8,9 @@ G2  its gradients equal central finite differences of
     state and key
 G3  a clamped decay passes no gradient to lambda, and a step whose pair does
     not exist passes none to beta
+G4  the window variants (Falcon-3/3A): G1 and G2 with a carried window ring
+    whose slots hold existing and missing pairs (the gradient of every ring
+    entry included), and W = 1 gives Falcon-1's / 1A's gradients
 """
 
 import numpy as np
@@ -94,3 +97,85 @@ def test_g3_clamp_and_missing_pairs_pass_no_gradient():
     assert np.abs(g["dlam"]).sum() > 0
     assert g["dbeta"][0, 0, 0] == 0.0   # fresh sequence: pair 0 does not exist
     assert np.abs(g["dbeta"][0, 1:, 0]).min() > 0
+
+
+WIN = [O.FALCON_3, O.FALCON_3A]
+
+
+def ring_carry(rng, B, H, dk, dv, W, pos):
+    """A carry with window ring: pos [H] tokens consumed per head (same for
+    every batch row)."""
+    c = carry_for(rng, B, H, dk, dv)
+    c["pos"] = np.array([pos] * B, dtype=np.int64)
+    c["win_x"] = rng.standard_normal((B, H, W - 1, dk)) / np.sqrt(dk)
+    c["win_v"] = rng.standard_normal((B, H, W - 1, dv))
+    return c
+
+
+@pytest.mark.parametrize("variant", WIN)
+@pytest.mark.parametrize("pairing", ["prefix", "same"])
+@pytest.mark.parametrize("W", [2, 4])
+def test_g4_window_torch_forward_is_the_oracle(variant, pairing, W):
+    rng = np.random.default_rng(430 + variant + 10 * W)
+    x = inputs(rng, 2, 9, 3, 5, 4, False)
+    carry = ring_carry(rng, 2, 3, 5, 4, W, [0, 2, 7])
+    o_n, c_n = O.recurrent(**x, variant=variant, window=W, carry=carry, pairing=pairing)
+    g = O.recurrent_vjp(**x, variant=variant, do=np.zeros_like(o_n), carry=carry, pairing=pairing, window=W)
+    assert np.abs(g["o"] - o_n).max() <= 1e-12 * max(1.0, np.abs(o_n).max())
+    assert np.abs(g["S"] - c_n["S"]).max() <= 1e-12 * max(1.0, np.abs(c_n["S"]).max())
+
+
+def _loss_w(x, variant, do, dS, carry, pairing, W):
+    o, c = O.recurrent(**x, variant=variant, window=W, carry=carry, pairing=pairing)
+    return (o * do).sum() + (c["S"] * dS).sum()
+
+
+@pytest.mark.parametrize("variant", WIN)
+@pytest.mark.parametrize("pairing", ["prefix", "same"])
+def test_g4_window_gradients_match_finite_differences(variant, pairing):
+    rng = np.random.default_rng(440 + variant)
+    B, T, H, dk, dv, W = 1, 6, 3, 3, 2, 3
+    x = inputs(rng, B, T, H, dk, dv, False)
+    carry = ring_carry(rng, B, H, dk, dv, W, [0, 2, 5])
+    do = rng.standard_normal((B, T, H, dv))
+    dS = rng.standard_normal((B, H, dk, dv))
+    g = O.recurrent_vjp(**x, variant=variant, do=do, dS_final=dS, carry=carry, pairing=pairing, window=W)
+    h = 1e-6
+    L = lambda xx, cc: _loss_w(xx, variant, do, dS, cc, pairing, W)
+    for name, gname in {"q": "dq", "k": "dk", "v": "dv", "beta": "dbeta", "lam": "dlam"}.items():
+        fd = np.zeros_like(x[name])
+        for idx in np.ndindex(x[name].shape):
+            xp = {kk: vv.copy() for kk, vv in x.items()}
+            xm = {kk: vv.copy() for kk, vv in x.items()}
+            xp[name][idx] += h
+            xm[name][idx] -= h
+            fd[idx] = (L(xp, carry) - L(xm, carry)) / (2 * h)
+        assert np.abs(fd - g[gname]).max() <= 1e-6 * max(1.0, np.abs(fd).max()), name
+    for cname, gname in (("S", "dS_in"), ("k_prev", "dk_prev"), ("win_x", "dwin_x"), ("win_v", "dwin_v")):
+        fd = np.zeros_like(carry[cname])
+        for idx in np.ndindex(carry[cname].shape):
+            cp = dict(carry, **{cname: carry[cname].copy()})
+            cm = dict(carry, **{cname: carry[cname].copy()})
+            cp[cname][idx] += h
+            cm[cname][idx] -= h
+            fd[idx] = (L(x, cp) - L(x, cm)) / (2 * h)
+        assert np.abs(fd - g[gname]).max() <= 1e-6 * max(1.0, np.abs(fd).max()), cname
+    # ring slots of pairs that do not exist (global index below the first pair) get nothing
+    first = 1 if pairing == "prefix" else 0
+    for hh, p0 in enumerate([0, 2, 5]):
+        for p in range(p0 - (W - 1), p0):
+            if p < first:
+                s = p % (W - 1)
+                assert not g["dwin_x"][0, hh, s].any() and not g["dwin_v"][0, hh, s].any()
+
+
+@pytest.mark.parametrize("pair", [(O.FALCON_3, O.FALCON_1), (O.FALCON_3A, O.FALCON_1A)])
+def test_g4_window_one_is_the_one_pair_gradient(pair):
+    rng = np.random.default_rng(450 + pair[0])
+    x = inputs(rng, 1, 8, 2, 4, 3, False)
+    carry = carry_for(rng, 1, 2, 4, 3)
+    do = rng.standard_normal((1, 8, 2, 3))
+    g3 = O.recurrent_vjp(**x, variant=pair[0], do=do, carry=carry, window=1)
+    g1 = O.recurrent_vjp(**x, variant=pair[1], do=do, carry=carry)
+    for n in ("dq", "dk", "dv", "dbeta", "dlam", "dS_in", "dk_prev"):
+        assert np.abs(g3[n] - g1[n]).max() <= 1e-13 * max(1.0, np.abs(g1[n]).max()), n
