@@ -30,6 +30,7 @@ EXPORTED = [
     "falcon_masked_parallel_workspace_size", "falcon_masked_parallel_ref_gpu",
     "falcon_strerror", "falcon_version", "falcon_chunk_fwd_plan", "falcon_chunk_fwd_timed",
     "falcon_chunk_fwd_noalloc", "falcon_backward_workspace_size", "falcon_backward",
+    "falcon_backward_carry",
     "falcon_varlen_workspace_size", "falcon_chunk_fwd_varlen", "falcon_workspace_status",
     "falcon_test_hooks",
 ]
@@ -92,6 +93,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.falcon_backward_workspace_size.restype = S
     lib.falcon_backward.argtypes = [P, V, V, V, V, V, C, V, V, V, V, V, V, V, V, V, V, S, V]
     lib.falcon_backward.restype = ctypes.c_int
+    lib.falcon_backward_carry.argtypes = [P, V, V, V, V, V, C, V, V, V, V, V, V, V, C, V, S, V]
+    lib.falcon_backward_carry.restype = ctypes.c_int
     lib.falcon_workspace_status.argtypes = [V, V]
     lib.falcon_workspace_status.restype = ctypes.c_int
     lib.falcon_test_hooks.argtypes = [ctypes.c_uint64, ctypes.c_int32]
@@ -303,6 +306,22 @@ def falcon_backward(p: Params, q, k, v, beta, lam, carry_in: dict | None, dO, dS
     _check(code, "falcon_backward")
 
 
+def falcon_backward_carry(p: Params, q, k, v, beta, lam, carry_in: dict | None, dO, dS_final, dq, dk, dv,
+                          dbeta, dlam, dcarry: dict | None, workspace, workspace_bytes: int = 0, stream=None):
+    """dcarry: dict of output buffers {S, k_prev, win_x, win_v} (any may be None)."""
+    lib = load_library()
+    ci = make_carry(carry_in)
+    dc = make_carry(dcarry)
+    if workspace is not None and not workspace_bytes and not isinstance(workspace, int):
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    code = lib.falcon_backward_carry(ctypes.byref(p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam),
+                                     ctypes.byref(ci) if ci is not None else None, _ptr(dO), _ptr(dS_final),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dlam),
+                                     ctypes.byref(dc) if dc is not None else None, _ptr(workspace),
+                                     workspace_bytes, _stream(stream))
+    _check(code, "falcon_backward_carry")
+
+
 # ---------------------------------------------------------------- tensor helpers
 def alloc_workspace(nbytes: int, device="cuda"):
     """A 256-byte aligned byte buffer (torch's caching allocator aligns to 512)."""
@@ -362,20 +381,25 @@ def masked_parallel(p: Params, q, k, v, beta, lam, stream=None):
 
 def backward(p: Params, q, k, v, beta, lam, dO, dS_final=None, carry_in: dict | None = None,
              stream=None) -> dict:
-    """Allocate the gradients / workspace with torch and call falcon_backward.
+    """Allocate the gradients / workspace with torch and call falcon_backward_carry.
 
-    Returns dq, dk, dv, dbeta, dlam, and dS_in / dk_prev (gradients of the
-    carried state and key)."""
+    Returns dq, dk, dv, dbeta, dlam, dS_in / dk_prev (gradients of the
+    carried state and key) and, for Falcon-3/3A with W > 1, dwin_x / dwin_v
+    (gradients of the carried window ring)."""
     import torch
     dev = q.device
     g = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
          "dbeta": torch.empty_like(beta), "dlam": torch.empty_like(lam),
          "dS_in": torch.empty((p.B, p.H, p.dk, p.dv), dtype=torch.float32, device=dev),
          "dk_prev": torch.empty((p.B, p.H, p.dk), dtype=q.dtype, device=dev)}
+    dc = {"S": g["dS_in"], "k_prev": g["dk_prev"]}
+    if p.variant in (FALCON_3, FALCON_3A) and p.window > 1:
+        g["dwin_x"] = dc["win_x"] = torch.empty((p.B, p.H, p.window - 1, p.dk), dtype=q.dtype, device=dev)
+        g["dwin_v"] = dc["win_v"] = torch.empty((p.B, p.H, p.window - 1, p.dv), dtype=q.dtype, device=dev)
     ws_n = falcon_backward_workspace_size(p)
     ws = alloc_workspace(ws_n, dev) if ws_n else None
-    falcon_backward(p, q, k, v, beta, lam, carry_in, dO, dS_final, g["dq"], g["dk"], g["dv"],
-                    g["dbeta"], g["dlam"], g["dS_in"], g["dk_prev"], ws, ws_n, stream)
+    falcon_backward_carry(p, q, k, v, beta, lam, carry_in, dO, dS_final, g["dq"], g["dk"], g["dv"],
+                          g["dbeta"], g["dlam"], dc, ws, ws_n, stream)
     return g
 
 

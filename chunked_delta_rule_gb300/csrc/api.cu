@@ -370,9 +370,56 @@ int falcon_masked_parallel_ref_gpu(const falcon_params_t* p, const void* q, cons
 }
 
 size_t falcon_backward_workspace_size(const falcon_params_t* p) {
-  if (check_params(p, false) != FALCON_OK || !backward_supported(p->variant, p->dk, p->dv) || p->prologue)
+  if (check_params(p, false) != FALCON_OK || !backward_supported(p->variant, p->dk, p->dv, p->window) ||
+      p->prologue)
     return 0;
-  return backward_ws_bytes(p->variant, p->B, p->T, p->H, p->dk);
+  return backward_ws_bytes(p->variant, p->B, p->T, p->H, p->dk, p->window);
+}
+
+int falcon_backward_carry(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                          const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                          const void* dO, const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
+                          float* dlambda, const falcon_carry_t* dcarry, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  int st = check_params(p, false);
+  if (st != FALCON_OK) return st;
+  if (!backward_supported(p->variant, p->dk, p->dv, p->window) || p->prologue) return FALCON_ERR_UNSUPPORTED;
+  if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !dO || !dq || !dk || !dv || !dbeta || !dlambda))
+    return FALCON_ERR_INVALID_ARG;
+  const size_t need = backward_ws_bytes(p->variant, p->B, p->T, p->H, p->dk, p->window);
+  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0))
+    return FALCON_ERR_WORKSPACE;
+  FwdArgs a = make_args(p, q, k, v, beta, lambda, nullptr, stream);
+  const int Wr = a.W - 1;
+  if (carry_in) {
+    a.S_in = carry_in->S; a.kprev_in = carry_in->k_prev; a.pos_in = carry_in->pos;
+    if (Wr > 0) { a.winx_in = carry_in->win_x; a.winv_in = carry_in->win_v; }
+    if ((a.winx_in == nullptr) != (a.winv_in == nullptr)) return FALCON_ERR_INVALID_ARG;
+  }
+  float* dS_in = dcarry ? dcarry->S : nullptr;
+  void* dk_prev = dcarry ? dcarry->k_prev : nullptr;
+  void* dwin_x = dcarry && Wr > 0 ? dcarry->win_x : nullptr;
+  void* dwin_v = dcarry && Wr > 0 ? dcarry->win_v : nullptr;
+  if ((dwin_x == nullptr) != (dwin_v == nullptr)) return FALCON_ERR_INVALID_ARG;
+  // the gradients must not overlap the inputs or one another
+  const size_t es = elem_size(p->dtype), BH = (size_t)p->B * p->H, BTH = BH * p->T;
+  const size_t nbeta = BTH * (variant_per_channel(p->variant) ? p->dv : 1) * 4;
+  const size_t nring_x = BH * (Wr > 0 ? Wr : 0) * p->dk * es, nring_v = BH * (Wr > 0 ? Wr : 0) * p->dv * es;
+  const void* ins[11] = {q, k, v, beta, lambda, dO, dS_final, a.S_in, a.kprev_in, a.winx_in, a.winv_in};
+  const size_t nin[11] = {BTH * p->dk * es, BTH * p->dk * es, BTH * p->dv * es, nbeta, BTH * 4,
+                          BTH * p->dv * es, BH * p->dk * p->dv * 4, BH * p->dk * p->dv * 4, BH * p->dk * es,
+                          nring_x, nring_v};
+  const void* outs[9] = {dq, dk, dv, dbeta, dlambda, dS_in, dk_prev, dwin_x, dwin_v};
+  const size_t nout[9] = {BTH * p->dk * es, BTH * p->dk * es, BTH * p->dv * es, nbeta, BTH * 4,
+                          BH * p->dk * p->dv * 4, BH * p->dk * es, nring_x, nring_v};
+  for (int i = 0; i < 9; ++i) {
+    for (int j = 0; j < 11; ++j)
+      if (overlaps(outs[i], nout[i], ins[j], nin[j])) return FALCON_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 9; ++j)
+      if (overlaps(outs[i], nout[i], outs[j], nout[j])) return FALCON_ERR_INVALID_ARG;
+  }
+  a.ws = workspace; a.ws_bytes = workspace_bytes;
+  return launch_backward(a, dO, dS_final, dq, dk, dv, dbeta, dlambda, dS_in, dk_prev, dwin_x, dwin_v);
 }
 
 int falcon_backward(const falcon_params_t* p, const void* q, const void* k, const void* v,
@@ -380,33 +427,10 @@ int falcon_backward(const falcon_params_t* p, const void* q, const void* k, cons
                     const void* dO, const float* dS_final, void* dq, void* dk, void* dv,
                     float* dbeta, float* dlambda, float* dS_in, void* dk_prev, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  int st = check_params(p, false);
-  if (st != FALCON_OK) return st;
-  if (!backward_supported(p->variant, p->dk, p->dv) || p->prologue) return FALCON_ERR_UNSUPPORTED;
-  if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !dO || !dq || !dk || !dv || !dbeta || !dlambda))
-    return FALCON_ERR_INVALID_ARG;
-  const size_t need = backward_ws_bytes(p->variant, p->B, p->T, p->H, p->dk);
-  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0))
-    return FALCON_ERR_WORKSPACE;
-  FwdArgs a = make_args(p, q, k, v, beta, lambda, nullptr, stream);
-  if (carry_in) { a.S_in = carry_in->S; a.kprev_in = carry_in->k_prev; a.pos_in = carry_in->pos; }
-  // the gradients must not overlap the inputs
-  const size_t es = elem_size(p->dtype), BH = (size_t)p->B * p->H, BTH = BH * p->T;
-  const size_t nbeta = BTH * (variant_per_channel(p->variant) ? p->dv : 1) * 4;
-  const void* ins[9] = {q, k, v, beta, lambda, dO, dS_final, a.S_in, a.kprev_in};
-  const size_t nin[9] = {BTH * p->dk * es, BTH * p->dk * es, BTH * p->dv * es, nbeta, BTH * 4,
-                         BTH * p->dv * es, BH * p->dk * p->dv * 4, BH * p->dk * p->dv * 4, BH * p->dk * es};
-  const void* outs[7] = {dq, dk, dv, dbeta, dlambda, dS_in, dk_prev};
-  const size_t nout[7] = {BTH * p->dk * es, BTH * p->dk * es, BTH * p->dv * es, nbeta, BTH * 4,
-                          BH * p->dk * p->dv * 4, BH * p->dk * es};
-  for (int i = 0; i < 7; ++i) {
-    for (int j = 0; j < 9; ++j)
-      if (overlaps(outs[i], nout[i], ins[j], nin[j])) return FALCON_ERR_INVALID_ARG;
-    for (int j = i + 1; j < 7; ++j)
-      if (overlaps(outs[i], nout[i], outs[j], nout[j])) return FALCON_ERR_INVALID_ARG;
-  }
-  a.ws = workspace; a.ws_bytes = workspace_bytes;
-  return launch_backward(a, dO, dS_final, dq, dk, dv, dbeta, dlambda, dS_in, dk_prev);
+  falcon_carry_t dc;
+  dc.S = dS_in; dc.k_prev = dk_prev; dc.win_x = nullptr; dc.win_v = nullptr; dc.pos = nullptr;
+  return falcon_backward_carry(p, q, k, v, beta, lambda, carry_in, dO, dS_final, dq, dk, dv, dbeta, dlambda, &dc,
+                               workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -1,5 +1,6 @@
 // Backward of the Falcon forward for the one-pair variants (Falcon-1, 1A, 2,
-// 2A), d_k = d_v = D in {32, 64}, bf16 or fp32 inputs, fp32 arithmetic.
+// 2A), d_k = d_v = D in {32, 64}, bf16 or fp32 inputs, fp32 arithmetic (the
+// dispatch at the end sends Falcon-3/3A and d = 128 to the window kernel).
 //
 // The pages give no gradient formulas; they follow from the update of
 // [JC 把记忆更新变成一次梯度下降; FW 三种等价形式] written per step,
@@ -316,18 +317,26 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t backward_ws_bytes(int variant, int B, int T, int H, int d) {
+// The window kernel (backward_window.cu) takes Falcon-3/3A and d = 128; the
+// chunked kernel Falcon-1/1A at d = 64; this file's kernel the rest.
+static bool use_window_kernel(int variant, int d) { return variant_windowed(variant) || d == 128; }
+
+size_t backward_ws_bytes(int variant, int B, int T, int H, int d, int window) {
+  if (use_window_kernel(variant, d)) return backward_window_ws_bytes(B, T, H, d);
   if (backward_chunk_supported(variant, d, d, T)) return backward_chunk_ws_bytes(B, T, H);
   const size_t NB = (size_t)(T + kBB - 1) / kBB;
   return (size_t)B * H * (NB + kBB) * d * d * sizeof(float);
 }
 
-bool backward_supported(int variant, int dk, int dv) {
-  return !variant_windowed(variant) && dk == dv && (dk == 32 || dk == 64);
+bool backward_supported(int variant, int dk, int dv, int window) {
+  if (use_window_kernel(variant, dk)) return backward_window_supported(variant, dk, dv, window);
+  return dk == dv && (dk == 32 || dk == 64);
 }
 
 int launch_backward(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk, void* dv,
-                    float* dbeta, float* dlam, float* dS_in, void* dk_prev) {
+                    float* dbeta, float* dlam, float* dS_in, void* dk_prev, void* dwin_x, void* dwin_v) {
+  if (use_window_kernel(f.variant, f.dk))
+    return launch_backward_window(f, dO, dS_final, dq, dk, dv, dbeta, dlam, dS_in, dk_prev, dwin_x, dwin_v);
   BwdArgs a;
   a.B = f.B; a.T = f.T; a.H = f.H;
   a.eps = f.eps; a.eps_gamma = f.eps_gamma;

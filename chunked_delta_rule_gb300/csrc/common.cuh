@@ -126,14 +126,20 @@ size_t tc_f3_ws_bytes(int B, int T, int H);
 bool window_scan_supported(const FwdArgs& a);
 size_t window_scan_ws_bytes(int B, int T, int H, int W);
 int launch_window_scan(const FwdArgs& a);
-size_t backward_ws_bytes(int variant, int B, int T, int H, int d);
+size_t backward_ws_bytes(int variant, int B, int T, int H, int d, int window);
 bool backward_chunk_supported(int variant, int dk, int dv, int T);
 size_t backward_chunk_ws_bytes(int B, int T, int H);
 int launch_backward_chunk(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk,
                           void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev);
-bool backward_supported(int variant, int dk, int dv);
+bool backward_supported(int variant, int dk, int dv, int window);
 int launch_backward(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk,
-                    void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev);
+                    void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev, void* dwin_x,
+                    void* dwin_v);
+bool backward_window_supported(int variant, int dk, int dv, int window);
+size_t backward_window_ws_bytes(int B, int T, int H, int d);
+int launch_backward_window(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk,
+                           void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev, void* dwin_x,
+                           void* dwin_v);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -293,22 +293,40 @@ size_t falcon_backward_workspace_size(const falcon_params_t* p);
 /* Gradient of the chunk forward, for training in the chunked framework
  * [FW 三种等价形式; JC 三种视角看同一个更新] (the pages give the forward
  * only; the backward is the chain rule through the update written at the
- * top of this header).  For the loss L = <o, dO> + <S_T, dS_final> of
- * falcon_chunk_fwd(p, q, k, v, beta, lambda, carry_in) it writes
+ * top of this header, Falcon-3/3A's window of pairs included).  For the loss
+ * L = <o, dO> + <S_T, dS_final> of falcon_chunk_fwd(p, q, k, v, beta,
+ * lambda, carry_in) it writes
  *   dq, dk [B, T, H, dk], dv [B, T, H, dv] (the params' dtype),
  *   dbeta (the shape of beta), dlambda [B, T, H] (fp32),
- *   dS_in [B, H, dk, dv] fp32 (gradient of carry_in->S; may be NULL),
- *   dk_prev [B, H, dk] dtype (gradient of carry_in->k_prev; may be NULL).
- * dO has the shape and dtype of o; dS_final (fp32 [B, H, dk, dv]) may be NULL
- * (zero).  carry_in supplies S, k_prev and pos as for the forward (NULL =
- * fresh sequence); a key that no pair reads gets a zero gradient.  The decay
- * clamp passes the gradient where eps_gamma <= 1 - lambda <= 1.  The
- * forward is recomputed inside (states kept at every 64th step in the
- * workspace), so o need not be saved.  Covered: Falcon-1, 1A, 2, 2A, both
- * pairings, bf16 or fp32, d_k = d_v in {32, 64}, any T >= 0 (chunk and impl
- * are ignored).  Gradients must not overlap inputs or one another.
- * Errors: FALCON_ERR_INVALID_ARG, FALCON_ERR_UNSUPPORTED (Falcon-3/3A,
- * other dims), FALCON_ERR_WORKSPACE, FALCON_ERR_CUDA. */
+ * and, through the fields of dcarry (NULL, or any field NULL, skips them):
+ *   dcarry->S      [B, H, dk, dv] fp32  gradient of carry_in->S,
+ *   dcarry->k_prev [B, H, dk] dtype      gradient of carry_in->k_prev,
+ *   dcarry->win_x  [B, H, W-1, dk], dcarry->win_v [B, H, W-1, dv] dtype
+ *                  gradients of the carried window ring (Falcon-3/3A, W > 1;
+ *                  both or neither; slot layout as in the carry);
+ * dcarry->pos is ignored.  dO has the shape and dtype of o; dS_final (fp32
+ * [B, H, dk, dv]) may be NULL (zero).  carry_in supplies S, k_prev, the
+ * window ring and pos as for the forward (NULL = fresh sequence); a key or
+ * ring entry that no existing pair reads gets a zero gradient.  The decay
+ * clamp passes the gradient where eps_gamma <= 1 - lambda <= 1.  The forward
+ * is recomputed inside (states kept at every 64th step in the workspace), so
+ * o need not be saved.  Covered: every variant, both pairings, bf16 or fp32,
+ * d_k = d_v in {32, 64, 128}; Falcon-3/3A with W up to 64 (up to 43 at
+ * d = 128, the window kernel's shared memory); any T >= 0 (chunk and impl
+ * are ignored).  Falcon-1/1A at d = 64 run a chunked kernel, Falcon-3/3A
+ * and d = 128 a step-by-step kernel that carries the window's key and value
+ * gradients in a ring, the rest a step-by-step one-pair kernel.  Gradients
+ * must not overlap inputs or one another.
+ * Errors: FALCON_ERR_INVALID_ARG, FALCON_ERR_UNSUPPORTED (other dims, the
+ * prologue, a window past the limit), FALCON_ERR_WORKSPACE, FALCON_ERR_CUDA. */
+int falcon_backward_carry(const falcon_params_t* p, const void* q, const void* k, const void* v,
+                          const float* beta, const float* lambda, const falcon_carry_t* carry_in,
+                          const void* dO, const float* dS_final, void* dq, void* dk, void* dv,
+                          float* dbeta, float* dlambda, const falcon_carry_t* dcarry, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* falcon_backward_carry with dcarry = {dS_in, dk_prev} (no ring gradients):
+ * dS_in [B, H, dk, dv] fp32 and dk_prev [B, H, dk] dtype may each be NULL. */
 int falcon_backward(const falcon_params_t* p, const void* q, const void* k, const void* v,
                     const float* beta, const float* lambda, const falcon_carry_t* carry_in,
                     const void* dO, const float* dS_final, void* dq, void* dk, void* dv,

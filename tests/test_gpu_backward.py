@@ -1,5 +1,6 @@
 """Backward pass (falcon_backward through the C ABI) against the backward
-oracle (torch fp64 autodiff of the one-pair recurrence): every gradient
+oracle (torch fp64 autodiff of the one-pair recurrence; the window variants
+and d = 128 are in test_gpu_backward_window.py): every gradient
 element by element, for Falcon-1/1A/2/2A, both pairings, bf16 and fp32,
 d = 32 and 64, carried state / key / positions, clamped decays, the empty
 and one-step sequences, block boundaries (64 steps) and a ragged tail; and,
@@ -122,14 +123,15 @@ def test_backward_clamped_decay(F, variant):
     assert float(g["dlam"].cpu()[clamped].abs().max()) == 0.0
 
 
-def test_backward_rejects_window_variants(F):
-    for v in (FALCON_3, FALCON_3A):
-        w = wl(v, T=10, window=4)
-        x = make_inputs(w, device="cuda")
-        c = make_cotangents(w, 1, device="cuda")
-        with pytest.raises(F.FalconError) as e:
-            F.backward(params_for(F, w), x["q"], x["k"], x["v"], x["beta"], x["lam"], c["dO"], None)
-        assert e.value.code == -2
+def test_backward_rejects_window_past_the_limit(F):
+    """Falcon-3/3A are covered up to the window the window kernel's shared
+    memory holds (43 at d = 128); a wider one is refused on the host."""
+    w = wl(FALCON_3, d=128, T=10, window=44)
+    x = make_inputs(w, device="cuda")
+    c = make_cotangents(w, 1, device="cuda")
+    with pytest.raises(F.FalconError) as e:
+        F.backward(params_for(F, w), x["q"], x["k"], x["v"], x["beta"], x["lam"], c["dO"], None)
+    assert e.value.code == -2
 
 
 @pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])

@@ -112,10 +112,12 @@ def test_workspace_size_is_deterministic(F):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(variant=4, window=4), -2), (dict(variant=5, window=1), -2), (dict(dk=128, dv=128), -2),
+    (dict(variant=4, window=44, dk=128, dv=128), -2), (dict(variant=5, window=65), -2),
     (dict(dk=32, dv=64), -2), (dict(dk=16, dv=16), -2), (dict(variant=9), -1), (dict(T=-1), -1),
 ])
 def test_backward_rejects_bad_params_on_host(F, kw, code):
+    """Params the host refuses before anything reaches the device (the
+    addresses handed in are never dereferenced)."""
     p = _p(F, **kw)
     fake = 1 << 20
     with pytest.raises(F.FalconError) as e:
@@ -123,6 +125,17 @@ def test_backward_rejects_bad_params_on_host(F, kw, code):
                           1 << 24, 1 << 25, 1 << 26, None, None, 1 << 30, 1 << 30, 0)
     assert e.value.code == code
     assert F.falcon_backward_workspace_size(p) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(variant=4, window=8), dict(variant=5, window=43, dk=128, dv=128),
+                                dict(variant=4, window=64), dict(variant=1, dk=128, dv=128),
+                                dict(variant=2, dk=128, dv=128), dict(variant=4, window=1, dk=32, dv=32)])
+def test_backward_window_kernel_workspace(F, kw):
+    """Falcon-3/3A and d = 128 take the window kernel: the states at every
+    64th step plus one recomputed block of 64 states, fp32."""
+    p = _p(F, **kw)
+    d = p.dk
+    assert F.falcon_backward_workspace_size(p) == 2 * 3 * (2 + 64) * d * d * 4
 
 
 def test_backward_workspace_and_overlap_checks(F):
