@@ -414,10 +414,14 @@ def run_backward(args, w):
     import chunked_delta_rule_gb300 as F
     from workloads import make_cotangents, make_inputs
     torch.cuda.set_device(0)
-    p = F.Params(B=w.B, T=w.T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk, eps=w.eps,
+    p = F.Params(B=w.B, T=w.T, H=w.H, dk=w.dk, dv=w.dv, chunk=w.chunk, window=w.window, eps=w.eps,
                  eps_gamma=w.eps_gamma, variant=w.variant,
                  dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32,
                  pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX)
+    chunked = w.variant in (0, 1) and w.dk == 64 and w.dv == 64
+    kernel = ("bwdc_prep_kernel + bwdc_fwd_chain_kernel + bwdc_bwd_chain_kernel + bwdc_grad_kernel (whole call)"
+              if chunked else "falcon_bwd_win_kernel" if (w.variant in (4, 5) or w.dk == 128)
+              else "falcon_bwd_kernel")
     sets = []
     for i in range(args.sets):
         x = make_inputs(w, seed=w.seed + i, device="cuda")
@@ -468,15 +472,13 @@ def run_backward(args, w):
                       "warmup": args.warmup, "higher_is_better": True,
                       "dtype": "bf16" if w.dtype == "bf16" else "f32",
                       "config": {"workload": w.name + "_backward", "B": w.B, "T": w.T, "H": w.H,
-                                 "dk": w.dk, "dv": w.dv, "variant": w.variant,
+                                 "dk": w.dk, "dv": w.dv, "variant": w.variant, "window": w.window,
                                  "pairing": w.pairing, "l2": f"rotating {len(sets)} input sets"},
                       "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                                    "frac": gbs / peak, "algorithmic_bytes": nbytes,
-                                   "kernel": ("bwdc_prep_kernel + bwdc_fwd_chain_kernel + bwdc_bwd_chain_kernel + "
-                                              "bwdc_grad_kernel (whole call)")
-                                   if (w.variant in (0, 1) and w.dk == 64 and w.dv == 64) else "falcon_bwd_kernel",
+                                   "kernel": kernel,
                                    "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
-                      "gpu_launches": args.steps * (4 if (w.variant in (0, 1) and w.dk == 64) else 1),
+                      "gpu_launches": args.steps * (4 if chunked else 1),
                       "clocks": clk}), flush=True)
 
 

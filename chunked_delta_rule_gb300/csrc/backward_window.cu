@@ -53,12 +53,14 @@ struct WinCfg {
   static constexpr int VPL = D / 32;  // elements of a D-vector per lane (one warp)
 };
 
-// Shared-memory layout in floats (W chosen at run time).
+// Shared-memory layout in floats (W chosen at run time).  The rings hold
+// W + 2 pairs: the window of the step, the pair a step ahead (written while
+// the step runs) and the slot a slower warp may still read from the step before.
 struct WinLayout {
-  int xf, vf, ef, mf;          // forward ring: keys, values [W][D]; |x|^2, exists [W]
-  int xb, vb, eb, mb, gx, gv;  // backward ring and its key / value gradients [W][D]
+  int xf, vf, ef, mf;          // forward ring: keys, values [W+2][D]; |x|^2, exists [W+2]
+  int xb, vb, eb, mb, gx, gv;  // backward ring and its key / value gradients [W+2][D]
   int dl, dr;                  // delta_a, dr_a of the step's pairs [W][D] (by window position a)
-  int qs, ds, y0;              // q_t, do_t, S_{t-1} do_t [D]
+  int qs, ds, y0;              // q_t, do_t [2][D] (by step parity), S_{t-1} do_t [D]
   int part;                    // row-sum partials [RS][2 kGP][D]
   int cpart;                   // column-sum partials [NCB][kGP + 1][D]
   int dots;                    // delta_a . do [W]
@@ -69,12 +71,13 @@ struct WinLayout {
 __host__ __device__ inline WinLayout win_layout(int D, int W, int RS, int NCB, int NW) {
   WinLayout L;
   int o = 0;
+  const int R = W + 2;
   auto take = [&](int n) { const int at = o; o += (n + 3) & ~3; return at; };
-  L.xf = take(W * D); L.vf = take(W * D); L.ef = take(W); L.mf = take(W);
-  L.xb = take(W * D); L.vb = take(W * D); L.eb = take(W); L.mb = take(W);
-  L.gx = take(W * D); L.gv = take(W * D);
+  L.xf = take(R * D); L.vf = take(R * D); L.ef = take(R); L.mf = take(R);
+  L.xb = take(R * D); L.vb = take(R * D); L.eb = take(R); L.mb = take(R);
+  L.gx = take(R * D); L.gv = take(R * D);
   L.dl = take(W * D); L.dr = take(W * D);
-  L.qs = take(D); L.ds = take(D); L.y0 = take(D);
+  L.qs = take(2 * D); L.ds = take(2 * D); L.y0 = take(D);
   L.part = take(RS * 2 * kGP * D);
   L.cpart = take(NCB * (kGP + 1) * D);
   L.dots = take(W);
@@ -150,9 +153,10 @@ template <typename Tin, int D, bool ADD, bool PERCH>
 __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArgs a) {
   using C = WinCfg<D>;
   constexpr int NT = C::NT, RS = C::RS, EPT = C::EPT, NW = C::NW, VPL = C::VPL;
+  constexpr bool PRE_SP = EPT <= 16;  // registers allow the next step's saved state to load early
   extern __shared__ float4 smem_f4[];
   float* sm = reinterpret_cast<float*>(smem_f4);
-  const int W = a.W;
+  const int W = a.W, R = W + 2;
   const WinLayout L = win_layout(D, W, RS, C::NCB, NW);
   float *xf = sm + L.xf, *vf = sm + L.vf, *ef = sm + L.ef, *mf = sm + L.mf;
   float *xb = sm + L.xb, *vb = sm + L.vb, *eb = sm + L.eb, *mb = sm + L.mb;
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
   float* sts = ckpt + (size_t)NB * D * D;
   auto row = [&](int m) { return rg + RS * m; };
   auto gidx = [&](int t) { return ((size_t)b * T + t) * a.H + h; };
-  auto slot = [&](int p) { const int s = p % W; return s < 0 ? s + W : s; };
+  auto slot = [&](int p) { const int s = p % R; return s < 0 ? s + R : s; };
   // slot of the carried window ring (W > 1) that holds pair p < 0 of this call
   auto ring_slot = [&](int p) {
     const int s = (int)((pos + p) % (W - 1));
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
   };
 
   // ---- pairs: warp 0 fetches pair p into registers, then puts it into a
-  // ring; a pair that does not exist (or lies past the call) reads as zeros
+  // ring; a pair that does not exist (or lies outside the call) reads as zeros
   auto fetch_pair = [&](int p, float (&X)[VPL], float (&V)[VPL], bool& ex) {
     ex = pos + p >= a.shift && p < T && p >= -(W - 1);
 #pragma unroll
@@ -219,9 +223,19 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
   float fx[VPL], fv[VPL], bx[VPL], bv[VPL];  // warp 0: the next pair of the forward / backward ring
   bool fex = false, bex = false;
 
-  // ---- the step's scalars from a ring holding the pairs t-W+1 .. t
+  // ---- the step's gates (fetched a step ahead) and its scalars from a ring
+  // holding the pairs t-W+1 .. t
+  struct Gate {
+    float lam, beta;  // lambda_t and beta_t (this thread's channel for Falcon-2/2A)
+  };
+  auto load_gate = [&](int t) {
+    Gate g;
+    g.lam = a.lam[gidx(t)];
+    g.beta = PERCH ? a.beta[gidx(t) * D + j] : a.beta[gidx(t)];
+    return g;
+  };
   struct Scal {
-    float inv_n, den, eta;  // eta: the scalar step (0 with no pair); per channel: 1 / den or 0
+    float inv_n, den;
     bool has;
   };
   auto scalars = [&](int t, const float* er, const float* mr) {
@@ -235,60 +249,67 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
     c.has = n > 0.f;
     c.inv_n = 1.f / fmaxf(n, 1.f);
     c.den = c.has ? a.eps + es * c.inv_n : 1.f;
-    const float bt = PERCH ? 1.f : a.beta[gidx(t)];
-    c.eta = c.has ? bt / c.den : 0.f;
     return c;
   };
-  auto gamma_of = [&](int t) { return fminf(fmaxf(1.f - a.lam[gidx(t)], a.eps_gamma), 1.f); };
+  auto gamma_of = [&](float lam) { return fminf(fmaxf(1.f - lam, a.eps_gamma), 1.f); };
 
-  // ---- one forward step on the register state S (S_{t-1} in, S_t out); the
-  // forward ring holds the pairs t-W+1 .. t
-  auto fwd_step = [&](int t, float (&S)[EPT]) {
+  // ---- one forward step on the register state S (S_{t-1} in, S_t out) with
+  // the forward ring holding the pairs t-W+1 .. t.  Warp 0 first puts pair
+  // t + 1 into the ring (its slot is read by no step in flight) and fetches
+  // pair t + 2; the step's barriers make the put visible to step t + 1.
+  auto fwd_one = [&](int t, int t_end, float (&S)[EPT], Gate& gn) {
+    const Gate g = gn;
+    if (t + 1 < t_end) gn = load_gate(t + 1);
+    if (warp == 0) {
+      put_pair(t + 1, fx, fv, fex, xf, vf, ef, mf);
+      fetch_pair(t + 2, fx, fv, fex);
+    }
     const Scal c = scalars(t, ef, mf);
-    const float gam = gamma_of(t);
-    const float eta_j = PERCH ? c.eta * a.beta[gidx(t) * D + j] : c.eta;
+    const float gam = gamma_of(g.lam);
+    const float ce = c.has ? c.inv_n * g.beta / c.den : 0.f;  // c_a / m_a for this column
     if (!ADD) {
       for (int g0 = 0; g0 < W; g0 += kGP) {
         const int ng = min(kGP, W - g0);
         for (int q = 0; q < ng; ++q) {  // S^T x_a over this thread's rows
           const float* xs = xf + slot(t - g0 - q) * D;
-          float s = 0.f;
+          float su = 0.f;
 #pragma unroll
-          for (int m = 0; m < EPT; ++m) s = fmaf(xs[row(m)], S[m], s);
-          part[(rg * 2 * kGP + q) * D + j] = s;
+          for (int m = 0; m < EPT; ++m) su = fmaf(xs[row(m)], S[m], su);
+          part[(rg * 2 * kGP + q) * D + j] = su;
         }
         __syncthreads();
-        if (rg == 0) {
-          for (int q = 0; q < ng; ++q) {
-            float u = 0.f;
+        for (int q = rg; q < ng; q += RS) {  // pair q's sums for column j, one row group each
+          float u = 0.f;
 #pragma unroll
-            for (int g = 0; g < RS; ++g) u += part[(g * 2 * kGP + q) * D + j];
-            const int s = slot(t - g0 - q);
-            dl[(g0 + q) * D + j] = mf[s] * c.inv_n * eta_j * (vf[s * D + j] - gam * u);
-          }
+          for (int gg = 0; gg < RS; ++gg) u += part[(gg * 2 * kGP + q) * D + j];
+          const int s = slot(t - g0 - q);
+          dl[(g0 + q) * D + j] = mf[s] * ce * (vf[s * D + j] - gam * u);
         }
         __syncthreads();
       }
-    } else {
-      if (rg == 0) {
-        for (int q = 0; q < W; ++q) {
-          const int s = slot(t - q);
-          dl[q * D + j] = mf[s] * c.inv_n * eta_j * vf[s * D + j];
-        }
+#pragma unroll
+      for (int m = 0; m < EPT; ++m) S[m] *= gam;
+      for (int q = 0; q < W; ++q) {
+        const float* xs = xf + slot(t - q) * D;
+        const float dj = dl[q * D + j];
+#pragma unroll
+        for (int m = 0; m < EPT; ++m) S[m] = fmaf(xs[row(m)], dj, S[m]);
+      }
+    } else {  // additive: delta_a = c_a v_a needs no sum over rows
+#pragma unroll
+      for (int m = 0; m < EPT; ++m) S[m] *= gam;
+      for (int q = 0; q < W; ++q) {
+        const int s = slot(t - q);
+        const float* xs = xf + s * D;
+        const float dj = mf[s] * ce * vf[s * D + j];
+#pragma unroll
+        for (int m = 0; m < EPT; ++m) S[m] = fmaf(xs[row(m)], dj, S[m]);
       }
       __syncthreads();
     }
-#pragma unroll
-    for (int m = 0; m < EPT; ++m) S[m] *= gam;
-    for (int q = 0; q < W; ++q) {
-      const float* xs = xf + slot(t - q) * D;
-      const float dj = dl[q * D + j];
-#pragma unroll
-      for (int m = 0; m < EPT; ++m) S[m] = fmaf(xs[row(m)], dj, S[m]);
-    }
   };
   // forward ring for a run of steps from t0: pairs t0-W+1 .. t0 in place,
-  // pair t0 + 1 fetched
+  // pair t0 + 1 fetched; returns the gates of step t0
   auto fwd_ring_start = [&](int t0) {
     __syncthreads();
     if (warp == 0) {
@@ -298,32 +319,23 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
       }
       fetch_pair(t0 + 1, fx, fv, fex);
     }
+    const Gate g = load_gate(t0);
     __syncthreads();
-  };
-  // after step t: pair t + 1 into the slot of pair t + 1 - W, fetch t + 2
-  auto fwd_ring_advance = [&](int t) {
-    __syncthreads();
-    if (warp == 0) {
-      put_pair(t + 1, fx, fv, fex, xf, vf, ef, mf);
-      fetch_pair(t + 2, fx, fv, fex);
-    }
-    __syncthreads();
+    return g;
   };
 
   // ---- pass 1: forward, the state at every block start
-  {
+  if (T > 0) {
     float S[EPT];
 #pragma unroll
     for (int m = 0; m < EPT; ++m) S[m] = a.S_in ? a.S_in[(size_t)bh * D * D + row(m) * D + j] : 0.f;
-    if (T > 0) fwd_ring_start(0);
-    for (int blk = 0; blk < NB; ++blk) {
+    Gate gn = fwd_ring_start(0);
+    for (int t = 0; t < T; ++t) {
+      if (t % kBW == 0) {
 #pragma unroll
-      for (int m = 0; m < EPT; ++m) ckpt[(size_t)blk * D * D + row(m) * D + j] = S[m];
-      const int t1 = min(T, (blk + 1) * kBW);
-      for (int t = blk * kBW; t < t1; ++t) {
-        fwd_step(t, S);
-        fwd_ring_advance(t);
+        for (int m = 0; m < EPT; ++m) ckpt[(size_t)(t / kBW) * D * D + row(m) * D + j] = S[m];
       }
+      fwd_one(t, T, S, gn);
     }
   }
 
@@ -338,13 +350,14 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
     for (int i = tid; i < D; i += NT) stw<Tin>(a.dk_prev, (size_t)bh * D + i, 0.f);
   }
   __syncthreads();
-  for (int i = tid; i < W * D; i += NT) {
+  for (int i = tid; i < R * D; i += NT) {
     gx[i] = 0.f;
     gv[i] = 0.f;
   }
-  float qn = 0.f, dn = 0.f;  // q_t and do_t of the next step (threads tid < D)
+  float qn = 0.f, dn = 0.f;  // q and do of the step after next (threads tid < D)
+  Gate gb{0.f, 0.f};         // the gates of the next step
   if (T > 0) {
-    if (warp == 0) {  // the window of step T - 1, and the pair that enters after it
+    if (warp == 0) {  // the window of step T - 1, and the pair that enters at its start
       for (int p = T - W; p < T; ++p) {
         fetch_pair(p, bx, bv, bex);
         put_pair(p, bx, bv, bex, xb, vb, eb, mb);
@@ -352,9 +365,14 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
       fetch_pair(T - 1 - W, bx, bv, bex);
     }
     if (tid < D) {
-      qn = ldw<Tin>(a.q, gidx(T - 1) * D + tid);
-      dn = ldw<Tin>(a.dO, gidx(T - 1) * D + tid);
+      qs[((T - 1) & 1) * D + tid] = ldw<Tin>(a.q, gidx(T - 1) * D + tid);
+      ds[((T - 1) & 1) * D + tid] = ldw<Tin>(a.dO, gidx(T - 1) * D + tid);
+      if (T >= 2) {
+        qn = ldw<Tin>(a.q, gidx(T - 2) * D + tid);
+        dn = ldw<Tin>(a.dO, gidx(T - 2) * D + tid);
+      }
     }
+    gb = load_gate(T - 1);
   }
   for (int blk = NB - 1; blk >= 0; --blk) {
     const int t0 = blk * kBW, t1 = min(T, t0 + kBW);
@@ -362,39 +380,55 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
       float S[EPT];
 #pragma unroll
       for (int m = 0; m < EPT; ++m) S[m] = ckpt[(size_t)blk * D * D + row(m) * D + j];
-      fwd_ring_start(t0);
+      Gate gn = fwd_ring_start(t0);
       for (int t = t0; t < t1; ++t) {
 #pragma unroll
         for (int m = 0; m < EPT; ++m) sts[(size_t)(t - t0) * D * D + row(m) * D + j] = S[m];
-        if (t + 1 < t1) {  // the last step's state is not needed
-          fwd_step(t, S);
-          fwd_ring_advance(t);
-        }
+        if (t + 1 < t1) fwd_one(t, t1, S, gn);  // the block's last state is not needed
       }
+      __syncthreads();
     }
+    float Spn[PRE_SP ? EPT : 1];
     for (int t = t1 - 1; t >= t0; --t) {
       const int tl = t - t0;
-      if (tid < D) {
-        qs[tid] = qn;
-        ds[tid] = dn;
-        if (t >= 1) {
-          qn = ldw<Tin>(a.q, gidx(t - 1) * D + tid);
-          dn = ldw<Tin>(a.dO, gidx(t - 1) * D + tid);
+      const Gate g = gb;
+      if (t >= 1) gb = load_gate(t - 1);
+      float Sp[EPT];
+      if (PRE_SP && t < t1 - 1) {
+#pragma unroll
+        for (int m = 0; m < EPT; ++m) Sp[m] = Spn[PRE_SP ? m : 0];
+      } else {
+#pragma unroll
+        for (int m = 0; m < EPT; ++m) Sp[m] = sts[(size_t)tl * D * D + row(m) * D + j];
+      }
+      if (PRE_SP && tl >= 1) {
+#pragma unroll
+        for (int m = 0; m < EPT; ++m) Spn[PRE_SP ? m : 0] = sts[(size_t)(tl - 1) * D * D + row(m) * D + j];
+      }
+      // pair t - W enters the ring (its slot held pair t + 2, written out two
+      // steps ago); q and do of step t - 1 go to the other parity's buffer
+      if (warp == 0 && t >= 1) {
+        put_pair(t - W, bx, bv, bex, xb, vb, eb, mb);
+        fetch_pair(t - W - 1, bx, bv, bex);
+      }
+      if (tid < D && t >= 1) {
+        qs[((t - 1) & 1) * D + tid] = qn;
+        ds[((t - 1) & 1) * D + tid] = dn;
+        if (t >= 2) {
+          qn = ldw<Tin>(a.q, gidx(t - 2) * D + tid);
+          dn = ldw<Tin>(a.dO, gidx(t - 2) * D + tid);
         }
       }
-      float Sp[EPT];
-#pragma unroll
-      for (int m = 0; m < EPT; ++m) Sp[m] = sts[(size_t)tl * D * D + row(m) * D + j];
+      const float* qc = qs + (t & 1) * D;
+      const float* dc = ds + (t & 1) * D;
       const Scal c = scalars(t, eb, mb);
-      const float lam_t = a.lam[gidx(t)];
-      const float gam = fminf(fmaxf(1.f - lam_t, a.eps_gamma), 1.f);
-      const float eta_j = PERCH ? c.eta * a.beta[gidx(t) * D + j] : c.eta;
-      __syncthreads();
+      const float gam = gamma_of(g.lam);
+      const float eta_j = c.has ? g.beta / c.den : 0.f;
       // dS += q do^T
-      const float doj = ds[j];
+      const float doj = dc[j];
 #pragma unroll
-      for (int m = 0; m < EPT; ++m) dS[m] = fmaf(qs[row(m)], doj, dS[m]);
-      float deta = 0.f;  // sum over the column's pairs of m_a r_a dd_a / max(n, 1) (row group 0)
+      for (int m = 0; m < EPT; ++m) dS[m] = fmaf(qc[row(m)], doj, dS[m]);
+      float deta = 0.f;  // sum over this thread's pairs of m_a r_a dd_a / max(n, 1) (column j)
       for (int g0 = 0; g0 < W; g0 += kGP) {
         const int ng = min(kGP, W - g0);
         // S_{t-1}^T x_a and dS^T x_a over this thread's rows
@@ -407,30 +441,29 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
             if (!ADD) su = fmaf(xv, Sp[m], su);
             sd = fmaf(xv, dS[m], sd);
           }
-          part[(rg * 2 * kGP + 2 * q) * D + j] = su;
+          if (!ADD) part[(rg * 2 * kGP + 2 * q) * D + j] = su;
           part[(rg * 2 * kGP + 2 * q + 1) * D + j] = sd;
         }
         __syncthreads();
-        if (rg == 0) {
-          for (int q = 0; q < ng; ++q) {
-            float u = 0.f, dd = 0.f;
+        for (int q = rg; q < ng; q += RS) {  // pair q's sums for column j, one row group each
+          float u = 0.f, dd = 0.f;
 #pragma unroll
-            for (int g = 0; g < RS; ++g) {
-              u += part[(g * 2 * kGP + 2 * q) * D + j];
-              dd += part[(g * 2 * kGP + 2 * q + 1) * D + j];
-            }
-            const int s = slot(t - g0 - q);
-            const float cm = mb[s] * c.inv_n, cc = cm * eta_j;
-            const float r = ADD ? vb[s * D + j] : vb[s * D + j] - gam * u;
-            dl[(g0 + q) * D + j] = cc * r;
-            drs[(g0 + q) * D + j] = ADD ? 0.f : cc * dd;
-            gv[s * D + j] += cc * dd;
-            deta = fmaf(cm, r * dd, deta);
+          for (int gg = 0; gg < RS; ++gg) {
+            if (!ADD) u += part[(gg * 2 * kGP + 2 * q) * D + j];
+            dd += part[(gg * 2 * kGP + 2 * q + 1) * D + j];
           }
+          const int s = slot(t - g0 - q);
+          const float cm = mb[s] * c.inv_n, cc = cm * eta_j;
+          const float r = ADD ? vb[s * D + j] : vb[s * D + j] - gam * u;
+          dl[(g0 + q) * D + j] = cc * r;
+          drs[(g0 + q) * D + j] = ADD ? 0.f : cc * dd;
+          gv[s * D + j] += cc * dd;
+          deta = fmaf(cm, r * dd, deta);
         }
         __syncthreads();
         // column sums: dS delta_a - gamma S_{t-1} dr_a, and (first group) S_{t-1} do,
         // 16 rows at a time; lane l (l even) ends with row g + RS (16 hh + l / 2)
+#pragma unroll 2
         for (int q = 0; q < ng; ++q) {
           const float dj = dl[(g0 + q) * D + j], rj = drs[(g0 + q) * D + j];
 #pragma unroll
@@ -470,13 +503,13 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
       }
       // delta_a . do, and the step's sum for the gradient of eta
       for (int q = warp; q < W; q += NW) {
-        float s = 0.f;
-        for (int i = lane; i < D; i += 32) s = fmaf(dl[q * D + i], ds[i], s);
-        s = warp_total(s);
-        if (lane == 0) dots[q] = s;
+        float sdot = 0.f;
+        for (int i = lane; i < D; i += 32) sdot = fmaf(dl[q * D + i], dc[i], sdot);
+        sdot = warp_total(sdot);
+        if (lane == 0) dots[q] = sdot;
       }
       {
-        float rv = rg == 0 ? (PERCH ? deta * eta_j : deta) : 0.f;
+        float rv = PERCH ? deta * eta_j : deta;
         rv = warp_total(rv);
         if (lane == 0) red[warp] = rv;
       }
@@ -485,8 +518,8 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
 #pragma unroll
       for (int w = 0; w < NW; ++w) etot += red[w];
       // de = -<deta, eta> / (eps + e)
-      const float de = c.has ? -(PERCH ? etot : etot * c.eta) / c.den : 0.f;
-      if (PERCH) {
+      const float de = c.has ? -(PERCH ? etot : etot * eta_j) / c.den : 0.f;
+      if (PERCH) {  // a one-pair variant: row group 0 holds the column's deta
         if (rg == 0) a.dbeta[gidx(t) * D + j] = c.has ? deta / c.den : 0.f;
       } else if (tid == 0) {
         a.dbeta[gidx(t)] = c.has ? etot / c.den : 0.f;
@@ -510,22 +543,23 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
           for (int m = 0; m < EPT; ++m) dS[m] = fmaf(-xs[row(m)], rj, dS[m]);
         }
       }
-      float g = 0.f;
+      float gsum = 0.f;
 #pragma unroll
       for (int m = 0; m < EPT; ++m) {
-        g = fmaf(dS[m], Sp[m], g);
+        gsum = fmaf(dS[m], Sp[m], gsum);
         dS[m] *= gam;
       }
-      g = warp_total(g);
-      if (lane == 0) red[NW + warp] = g;
+      gsum = warp_total(gsum);
+      if (lane == 0) red[NW + warp] = gsum;
       __syncthreads();
       if (tid == 0) {
         float dg = 0.f;
         for (int w = 0; w < NW; ++w) dg += red[NW + w];
-        const float om = 1.f - lam_t;
+        const float om = 1.f - g.lam;
         a.dlam[gidx(t)] = (om >= a.eps_gamma && om <= 1.f) ? -dg : 0.f;
       }
-      // pair t is complete: its gradients leave, and pair t - W takes its slot
+      // pair t is complete (no later step reads it): its gradients leave and
+      // its accumulators clear for the pair that takes the slot
       for (int i = tid; i < D; i += NT) {
         const int s = slot(t);
         const float gk = gx[s * D + i], gvv = gv[s * D + i];
@@ -536,13 +570,9 @@ __global__ void __launch_bounds__(WinCfg<D>::NT, 1) falcon_bwd_win_kernel(WinArg
         gx[s * D + i] = 0.f;
         gv[s * D + i] = 0.f;
       }
-      if (warp == 0 && t >= 1) {
-        put_pair(t - W, bx, bv, bex, xb, vb, eb, mb);
-        fetch_pair(t - W - 1, bx, bv, bex);
-      }
-      __syncthreads();
     }
   }
+  __syncthreads();
   // the carried window ring's pairs -W+1 .. -1 (complete after step 0; zero when T = 0)
   if (W > 1 && a.dwin_x) {
     for (int idx = tid; idx < (W - 1) * D; idx += NT) {

@@ -112,7 +112,7 @@ def test_workspace_size_is_deterministic(F):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(variant=4, window=44, dk=128, dv=128), -2), (dict(variant=5, window=65), -2),
+    (dict(variant=4, window=42, dk=128, dv=128), -2), (dict(variant=5, window=65), -2),
     (dict(dk=32, dv=64), -2), (dict(dk=16, dv=16), -2), (dict(variant=9), -1), (dict(T=-1), -1),
 ])
 def test_backward_rejects_bad_params_on_host(F, kw, code):
@@ -127,7 +127,7 @@ def test_backward_rejects_bad_params_on_host(F, kw, code):
     assert F.falcon_backward_workspace_size(p) == 0
 
 
-@pytest.mark.parametrize("kw", [dict(variant=4, window=8), dict(variant=5, window=43, dk=128, dv=128),
+@pytest.mark.parametrize("kw", [dict(variant=4, window=8), dict(variant=5, window=41, dk=128, dv=128),
                                 dict(variant=4, window=64), dict(variant=1, dk=128, dv=128),
                                 dict(variant=2, dk=128, dv=128), dict(variant=4, window=1, dk=32, dv=32)])
 def test_backward_window_kernel_workspace(F, kw):
