@@ -322,7 +322,7 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
 static bool use_window_kernel(int variant, int d) { return variant_windowed(variant) || d == 128; }
 
 size_t backward_ws_bytes(int variant, int B, int T, int H, int d, int window) {
-  if (use_window_kernel(variant, d)) return backward_window_ws_bytes(B, T, H, d);
+  if (use_window_kernel(variant, d)) return backward_window_ws_bytes(B, T, H, d, effective_window(variant, window));
   if (backward_chunk_supported(variant, d, d, T)) return backward_chunk_ws_bytes(B, T, H);
   const size_t NB = (size_t)(T + kBB - 1) / kBB;
   return (size_t)B * H * (NB + kBB) * d * d * sizeof(float);

@@ -136,7 +136,7 @@ int launch_backward(const FwdArgs& f, const void* dO, const float* dS_final, voi
                     void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev, void* dwin_x,
                     void* dwin_v);
 bool backward_window_supported(int variant, int dk, int dv, int window);
-size_t backward_window_ws_bytes(int B, int T, int H, int d);
+size_t backward_window_ws_bytes(int B, int T, int H, int d, int window);
 int launch_backward_window(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk,
                            void* dv, float* dbeta, float* dlam, float* dS_in, void* dk_prev, void* dwin_x,
                            void* dwin_v);

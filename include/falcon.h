@@ -311,7 +311,7 @@ size_t falcon_backward_workspace_size(const falcon_params_t* p);
  * clamp passes the gradient where eps_gamma <= 1 - lambda <= 1.  The forward
  * is recomputed inside (states kept at every 64th step in the workspace), so
  * o need not be saved.  Covered: every variant, both pairings, bf16 or fp32,
- * d_k = d_v in {32, 64, 128}; Falcon-3/3A with W up to 64 (up to 41 at
+ * d_k = d_v in {32, 64, 128}; Falcon-3/3A with W up to 64 (up to 34 at
  * d = 128, the window kernel's shared memory); any T >= 0 (chunk and impl
  * are ignored).  Falcon-1/1A at d = 64 run a chunked kernel, Falcon-3/3A
  * and d = 128 a step-by-step kernel that carries the window's key and value

@@ -125,8 +125,8 @@ def test_backward_clamped_decay(F, variant):
 
 def test_backward_rejects_window_past_the_limit(F):
     """Falcon-3/3A are covered up to the window the window kernel's shared
-    memory holds (41 at d = 128); a wider one is refused on the host."""
-    w = wl(FALCON_3, d=128, T=10, window=42)
+    memory holds (34 at d = 128); a wider one is refused on the host."""
+    w = wl(FALCON_3, d=128, T=10, window=35)
     x = make_inputs(w, device="cuda")
     c = make_cotangents(w, 1, device="cuda")
     with pytest.raises(F.FalconError) as e:

@@ -114,7 +114,7 @@ def test_backward_d128_one_pair(F, variant, pairing):
     check(w, g, ref, names=ALL)
 
 
-@pytest.mark.parametrize("W,d", [(64, 64), (41, 128), (17, 32)])
+@pytest.mark.parametrize("W,d", [(64, 64), (34, 128), (17, 32)])
 def test_window_backward_wide_windows(F, W, d):
     """The widest windows the kernel takes (two or more reduction groups of
     eight pairs, and a group that is not full)."""

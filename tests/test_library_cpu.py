@@ -112,7 +112,7 @@ def test_workspace_size_is_deterministic(F):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(variant=4, window=42, dk=128, dv=128), -2), (dict(variant=5, window=65), -2),
+    (dict(variant=4, window=35, dk=128, dv=128), -2), (dict(variant=5, window=65), -2),
     (dict(dk=32, dv=64), -2), (dict(dk=16, dv=16), -2), (dict(variant=9), -1), (dict(T=-1), -1),
 ])
 def test_backward_rejects_bad_params_on_host(F, kw, code):
@@ -127,15 +127,20 @@ def test_backward_rejects_bad_params_on_host(F, kw, code):
     assert F.falcon_backward_workspace_size(p) == 0
 
 
-@pytest.mark.parametrize("kw", [dict(variant=4, window=8), dict(variant=5, window=41, dk=128, dv=128),
+@pytest.mark.parametrize("kw", [dict(variant=4, window=8), dict(variant=5, window=34, dk=128, dv=128),
                                 dict(variant=4, window=64), dict(variant=1, dk=128, dv=128),
                                 dict(variant=2, dk=128, dv=128), dict(variant=4, window=1, dk=32, dv=32)])
 def test_backward_window_kernel_workspace(F, kw):
     """Falcon-3/3A and d = 128 take the window kernel: the states at every
-    64th step plus one recomputed block of 64 states, fp32."""
+    64th step plus one recomputed block of 65 states, then per step and
+    16-column group the partial sums (W + 1 d-vectors and two scalars,
+    padded to 4 floats), and four scalars per step; all fp32."""
     p = _p(F, **kw)
-    d = p.dk
-    assert F.falcon_backward_workspace_size(p) == 2 * 3 * (2 + 64) * d * d * 4
+    d, W = p.dk, (p.window if p.variant in (4, 5) else 1)
+    kp = (W * d + d + 2 + 3) // 4 * 4
+    BH, T = 2 * 3, 100
+    want = BH * (2 + 64 + 1) * d * d + BH * T * (d // 16) * kp + BH * T * 4
+    assert F.falcon_backward_workspace_size(p) == want * 4
 
 
 def test_backward_workspace_and_overlap_checks(F):
