@@ -161,10 +161,15 @@ size_t falcon_workspace_size(const falcon_params_t* p) {
   return kernel_ws_bytes(p) + (p->prologue ? prologue_bytes(p, false) : 0);
 }
 
+// packed sequences' chunk map (B H NC items, their count and B + 1 sequence offsets, int32)
+static size_t varlen_map_bytes(const falcon_params_t* p) {
+  return align_up(((size_t)p->B * p->H * ((p->T + 63) / 64) + 1 + p->B + 1) * 4, 256);
+}
+
 size_t falcon_varlen_workspace_size(const falcon_params_t* p) {
   if (check_params(p, false) != FALCON_OK) return 0;
   if (pick_impl(p, make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr)) < 0) return 0;
-  return kernel_ws_bytes(p) + prologue_bytes(p, true);
+  return kernel_ws_bytes(p) + prologue_bytes(p, true) + varlen_map_bytes(p);
 }
 
 // The prologue runs inside the kernels on the pipelined d = 64 tensor-core
@@ -182,10 +187,33 @@ static bool prologue_fused(const falcon_params_t* p, const void* q = nullptr, co
          FALCON_IMPL_TC;
 }
 
+// The packed-sequence chunk map that the Falcon-1 / 1A d = 64 tensor-core
+// kernels take in place of the padded batch's every chunk.
+struct VarlenMap {
+  const int32_t* cu;
+  const int32_t* item_map;  // B H NC entries, then the count
+  int NC;
+};
+
+// The kernel family a chunk forward with these args runs: pick_impl, then
+// the portable kernel for rows off a 16-byte boundary; -1 if none.
+static int resolve_impl(const falcon_params_t* p, const FwdArgs& a) {
+  int impl = pick_impl(p, a);
+  if (impl < 0) return impl;
+  // the window recurrence's 16-byte async copies and the tensor-core
+  // kernels' TMA maps and 16-byte stores need rows on 16-byte boundaries
+  if ((impl == FALCON_IMPL_SCAN || impl == FALCON_IMPL_TC) && !aligned16(a)) {
+    if (p->impl == impl) return -2;
+    impl = FALCON_IMPL_GENERIC;
+  }
+  return impl;
+}
+
 static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k, const void* v,
                           const float* beta, const float* lambda, const falcon_carry_t* carry_in,
                           void* o, falcon_carry_t* carry_out, void* workspace,
-                          size_t workspace_bytes, void* stream, void* const* events, int n_events) {
+                          size_t workspace_bytes, void* stream, void* const* events, int n_events,
+                          const VarlenMap* vm = nullptr) {
   int st = check_params(p, false);
   if (st != FALCON_OK) return st;
   if (p->T > 0 && (!q || !k || !v || !beta || !lambda || !o)) return FALCON_ERR_INVALID_ARG;
@@ -234,13 +262,13 @@ static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k
   a.ws = workspace; a.ws_bytes = workspace_bytes;
   a.events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
   a.n_events = n_events;
-  int impl = pick_impl(p, a);
+  const int impl = resolve_impl(p, a);
+  if (impl == -2) return FALCON_ERR_INVALID_ARG;
   if (impl < 0) return FALCON_ERR_UNSUPPORTED;
-  // the window recurrence's 16-byte async copies and the tensor-core
-  // kernels' TMA maps and 16-byte stores need rows on 16-byte boundaries
-  if ((impl == FALCON_IMPL_SCAN || impl == FALCON_IMPL_TC) && !aligned16(a)) {
-    if (p->impl == impl) return FALCON_ERR_INVALID_ARG;
-    impl = FALCON_IMPL_GENERIC;
+  if (vm && impl == FALCON_IMPL_TC && tc_chunk_takes_map(a)) {
+    a.cu = vm->cu;
+    a.item_map = vm->item_map;
+    a.item_count = vm->item_map + (size_t)p->B * p->H * vm->NC;
   }
   if (impl == FALCON_IMPL_SCAN) {
     const size_t need = window_scan_ws_bytes(p->B, p->T, p->H, a.W);
@@ -306,21 +334,38 @@ int falcon_chunk_fwd_varlen(const falcon_params_t* p, const int32_t* cu_seqlens,
   if (total_tokens > 0 && (!q || !k || !v || !beta || !lambda || !o)) return FALCON_ERR_INVALID_ARG;
   if (pick_impl(p, make_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr)) < 0)
     return FALCON_ERR_UNSUPPORTED;
-  const size_t kws = kernel_ws_bytes(p);
-  if (!ws_ok(workspace, workspace_bytes, kws + prologue_bytes(p, true))) return FALCON_ERR_WORKSPACE;
+  const size_t kws = kernel_ws_bytes(p), pws = prologue_bytes(p, true);
+  if (!ws_ok(workspace, workspace_bytes, kws + pws + varlen_map_bytes(p))) return FALCON_ERR_WORKSPACE;
   ProArgs pa = pro_args(p, cu_seqlens, q, k, v, beta, lambda);
   void* o_pad = nullptr;
   prologue_carve(pa, reinterpret_cast<uint8_t*>(workspace) + kws, true, &o_pad);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = launch_prologue(pa, s);
-  if (st != FALCON_OK) return st;
   falcon_params_t p0 = *p;
   p0.prologue = 0;
   falcon_carry_t co_state;  // the dense pass gives the state; the rest depends on each length
   std::memset(&co_state, 0, sizeof(co_state));
   if (carry_out) co_state.S = carry_out->S;
+  // the Falcon-1 / 1A d = 64 tensor-core kernels take only the chunks that
+  // hold tokens (a map built here); the gather then leaves the rest unwritten
+  VarlenMap vm;
+  vm.cu = cu_seqlens;
+  vm.item_map = reinterpret_cast<const int32_t*>(reinterpret_cast<uint8_t*>(workspace) + kws + pws);
+  vm.NC = (p->T + 63) / 64;
+  FwdArgs ad = make_args(&p0, pa.qo, pa.ko, pa.vo, pa.bo, pa.lo, o_pad, stream);
+  if (carry_in) {
+    ad.S_in = carry_in->S; ad.kprev_in = carry_in->k_prev; ad.pos_in = carry_in->pos;
+    if (ad.W > 1) { ad.winx_in = carry_in->win_x; ad.winv_in = carry_in->win_v; }
+  }
+  const bool mapped = resolve_impl(&p0, ad) == FALCON_IMPL_TC && tc_chunk_takes_map(ad);
+  pa.skip_tail = mapped ? 1 : 0;
+  st = launch_prologue(pa, s);
+  if (st != FALCON_OK) return st;
+  if (mapped) {
+    st = launch_varlen_item_map(cu_seqlens, p->B, p->H, vm.NC, const_cast<int32_t*>(vm.item_map), s);
+    if (st != FALCON_OK) return st;
+  }
   st = chunk_fwd_impl(&p0, pa.qo, pa.ko, pa.vo, pa.bo, pa.lo, carry_in, o_pad, &co_state,
-                      kws ? workspace : nullptr, kws, stream, nullptr, 0);
+                      kws ? workspace : nullptr, kws, stream, nullptr, 0, mapped ? &vm : nullptr);
   if (st != FALCON_OK) return st;
   return launch_varlen_finish(pa, o_pad, o, effective_window(p->variant, p->window),
                               p->pairing == FALCON_PAIR_PREFIX ? 1 : 0, carry_in, carry_out, s);

@@ -67,6 +67,12 @@ struct FwdArgs {
   cudaEvent_t* events;      // optional: recorded before the first and after every kernel
   int n_events;
   int prologue;             // falcon_prologue_t flags applied inside the kernel (recurrent step)
+  // packed sequences laid out as a padded batch (varlen): sequence b holds
+  // rows 0 .. cu[b+1] - cu[b] - 1 of batch row b, and the Falcon-1 / 1A
+  // d = 64 tensor-core kernels skip the chunks past its last (NULL: dense)
+  const int32_t* cu;
+  const int32_t* item_map;  // the (b, h, chunk) items that hold tokens, as (b H + h) NC + chunk
+  const int32_t* item_count;
 };
 
 // Gates with the optional logit prologue: gamma = clamp(1 - lambda) or
@@ -93,12 +99,18 @@ struct ProArgs {
   void* vo;
   float* bo;
   float* lo;
+  int skip_tail;            // packed sequences: rows of the chunks past a sequence's last are not written
 };
 size_t prologue_ws_bytes(int B, int T, int H, int dk, int dv, int dtype, bool perch, bool with_o);
 void prologue_carve(ProArgs& a, void* base, bool with_o, void** o_pad);
 int launch_prologue(const ProArgs& a, cudaStream_t s);
 int launch_varlen_finish(const ProArgs& a, const void* o_pad, void* o, int W, int shift,
                          const falcon_carry_t* ci, falcon_carry_t* co, cudaStream_t s);
+// Whether launch_tc_chunk runs the Falcon-1 / 1A d = 64 kernels for these
+// args (the path that takes a packed-sequence chunk map), and the kernel that
+// builds that map (B H NC + B + 2 int32) from cu_seqlens.
+bool tc_chunk_takes_map(const FwdArgs& a);
+int launch_varlen_item_map(const int32_t* cu, int B, int H, int NC, int32_t* map, cudaStream_t s);
 
 // Record the caller's event i on the stream (no-op without events).
 inline void record_event(const FwdArgs& a, int i) {

@@ -7,7 +7,9 @@
 //    dense [B, T, H, .] batch.  For packed sequences (cu_seqlens) it also
 //    lays sequence b's tokens at rows (b, 0 .. len_b - 1) and fills the rest
 //    with beta = 0, lambda = 0 and zero q, k, v: such a step neither writes
-//    nor decays, so the state after T padded steps is the state after len_b.
+//    nor decays, so the state after T padded steps is the state after len_b
+//    (when the kernels after it skip the chunks past a sequence's last, only
+//    the padding inside its last chunk is written).
 //  - varlen_scatter_kernel: the outputs of the real rows back to the packed
 //    layout;
 //  - varlen_carry_kernel: the carry fields that depend on where a sequence
@@ -49,6 +51,10 @@ __global__ void __launch_bounds__(32 * kProWarps) prologue_kernel(ProArgs a) {
   Tin* ko = reinterpret_cast<Tin*>(a.ko);
   Tin* vo = reinterpret_cast<Tin*>(a.vo);
   const int nb = a.perch ? a.dv : 1;
+  if (sr < 0 && a.skip_tail) {  // a chunk past the sequence's last: read by no kernel
+    const int len = a.cu[b + 1] - a.cu[b];
+    if (t >= (len + 63) / 64 * 64) return;
+  }
   if (sr < 0) {  // padding: a step that neither writes nor decays
     for (int i = lane; i < a.dk; i += 32) {
       qo[dst * a.dk + i] = from_f32<Tin>(0.f);
@@ -110,6 +116,9 @@ __global__ void __launch_bounds__(32 * kProWarps) prologue_vec_kernel(ProArgs a,
   const long long bt = live ? row / a.H : 0;
   const int t = (int)(bt % a.T), b = (int)(bt / a.T);
   const long long sr = live ? src_row(a, b, t) : -1;
+  // a row of a chunk past the sequence's last is read by no kernel: not
+  // written (the lanes still join the shuffles below)
+  const bool put = live && !(sr < 0 && a.skip_tail && t >= (a.cu[b + 1] - a.cu[b] + 63) / 64 * 64);
   const size_t dst = (size_t)row, srow = (size_t)(sr < 0 ? 0 : sr) * a.H + h;
   const bool l2 = (a.flags & FALCON_PROLOGUE_L2NORM_QK) != 0;
   const bool logits = (a.flags & FALCON_PROLOGUE_GATE_LOGITS) != 0;
@@ -132,9 +141,9 @@ __global__ void __launch_bounds__(32 * kProWarps) prologue_vec_kernel(ProArgs a,
     Tin* oe = reinterpret_cast<Tin*>(&outv);
 #pragma unroll
     for (int i = 0; i < EC; ++i) oe[i] = from_f32<Tin>(x[i] * scale);
-    if (live) *reinterpret_cast<uint4*>(reinterpret_cast<Tin*>(which == 0 ? a.qo : a.ko) + dst * a.dk + sub * EC) = outv;
+    if (put) *reinterpret_cast<uint4*>(reinterpret_cast<Tin*>(which == 0 ? a.qo : a.ko) + dst * a.dk + sub * EC) = outv;
   }
-  if (!live) return;
+  if (!put) return;
   const int vc = a.dv / EC;  // 16-byte pieces per value row
   for (int c = sub; c < vc; c += LPR) {
     uint4 raw = make_uint4(0u, 0u, 0u, 0u);
@@ -150,6 +159,20 @@ __global__ void __launch_bounds__(32 * kProWarps) prologue_vec_kernel(ProArgs a,
     const float lv = sr >= 0 ? a.lam[srow] : 0.f;
     a.lo[dst] = (sr >= 0 && logits) ? sigmoidf(lv) : lv;
   }
+}
+
+// one thread per 16 bytes of a row (rows of both layouts on 16-byte boundaries)
+__global__ void __launch_bounds__(256) varlen_scatter16_kernel(ProArgs a, int pieces, const uint4* o_pad, uint4* o) {
+  const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (i >= (long long)a.B * a.T * a.H * pieces) return;
+  const long long row = i / pieces;
+  const int c = (int)(i % pieces);
+  const int h = (int)(row % a.H);
+  const long long bt = row / a.H;
+  const int t = (int)(bt % a.T), b = (int)(bt / a.T);
+  const long long sr = src_row(a, b, t);
+  if (sr < 0) return;
+  o[((size_t)sr * a.H + h) * pieces + c] = o_pad[(size_t)row * pieces + c];
 }
 
 template <typename Tin>
@@ -268,7 +291,14 @@ int launch_prologue(const ProArgs& a, cudaStream_t s) {
 
 int launch_varlen_finish(const ProArgs& a, const void* o_pad, void* o, int W, int shift,
                          const falcon_carry_t* ci, falcon_carry_t* co, cudaStream_t s) {
-  if ((long long)a.B * a.T * a.H > 0) {
+  const size_t row_bytes = (size_t)a.dv * (a.dtype == FALCON_BF16 ? 2 : 4);
+  const long long rows = (long long)a.B * a.T * a.H;
+  if (rows > 0 && row_bytes % 16 == 0 && ((reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(o_pad)) & 15) == 0) {
+    const int pieces = (int)(row_bytes / 16);
+    const long long n = rows * pieces;
+    varlen_scatter16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, pieces, reinterpret_cast<const uint4*>(o_pad),
+                                                                       reinterpret_cast<uint4*>(o));
+  } else if (rows > 0) {
     if (a.dtype == FALCON_BF16) varlen_scatter_kernel<__nv_bfloat16><<<rows_grid(a), 32 * kProWarps, 0, s>>>(a, o_pad, o);
     else varlen_scatter_kernel<float><<<rows_grid(a), 32 * kProWarps, 0, s>>>(a, o_pad, o);
   }

@@ -77,6 +77,12 @@ struct TcArgs {
   uint64_t wait_ns;   // limit of every bounded wait
   int stall;          // failure-detection test hook: the per-chunk kernel's first CTA waits on
                       // a barrier that nothing completes (the wait runs out, a timeout is recorded)
+  // packed sequences (d = 64 only): sequence b's length is cu[b+1] - cu[b];
+  // the per-chunk kernel takes the items of item_map[0 .. *item_count), the
+  // sequential kernel stops after the sequence's last chunk (NULL: dense)
+  const int32_t* cu;
+  const int32_t* item_map;
+  const int32_t* item_count;
 };
 
 // ======================================================================
@@ -100,7 +106,7 @@ struct WyuSmem {
   static constexpr size_t TOTAL = MISC + 16 + 1024;
 };
 
-template <bool SOLVE, int DK>
+template <bool SOLVE, int DK, bool MAP = false>  // MAP: the items of packed sequences' chunk map
 __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                     const __grid_constant__ CUtensorMap tm_v,
                                                                     TcArgs a) {
@@ -125,12 +131,15 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = a.NC * a.B * a.H;  // work item = (b, h, chunk), chunk fastest
   // launched overlapping the stream's previous grid: wait for it before any
   // read; then (every CTA of this persistent grid being resident) let the
   // sequential kernel launch and wait for this grid in hardware
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // work item = (b, h, chunk) as (b H + h) NC + chunk, chunk fastest: all of
+  // them, or for packed sequences the listed ones (those holding tokens)
+  const int n_items = MAP ? *a.item_count : a.NC * a.B * a.H;
+  auto real_item = [&](int item) { return MAP ? a.item_map[item] : item; };
   // the call's status word starts clear (the grid is resident as a whole,
   // so no CTA of it records a timeout a full wait limit before this runs)
   if (blockIdx.x == 0 && tid == 0) atomicExch(a.status, 0u);
@@ -165,7 +174,8 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   // first used two items later, so the loads stay in flight meanwhile)
   int issued = 0;  // tile loads issued (thread 0); item `it` waits for the it-th
   auto fetch_tiles = [&](int item) {
-    const int chunk = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
+    const int ri = real_item(item);
+    const int chunk = ri % a.NC, bh = ri / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
     if (tid == 0) {
       ++issued;
       mbar_arrive_expect_tx(&bar[0], kImg);
@@ -180,7 +190,8 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
     beta_r = 0.f;
     pos_r = 0;
     if (item >= n_items) return;
-    const int chunk = item % a.NC, bh = item / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
+    const int ri = real_item(item);
+    const int chunk = ri % a.NC, bh = ri / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
     const int t = t0 + tid;
     const bool step_ok = tid < 64 && t < a.T;
     const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
@@ -198,7 +209,8 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   }
   int it = 0;
   for (int item = first_item; item < n_items; item += gridDim.x, ++it) {
-  const int chunk = item % a.NC, bh = item / a.NC;
+  const int ri = real_item(item);
+  const int chunk = ri % a.NC, bh = ri / a.NC;
   const int next = item + gridDim.x;
   const int t_row = chunk * kC + tid;
   const bool step_ok = tid < 64 && t_row < a.T;
@@ -1011,7 +1023,9 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const bool upstream_failed = *reinterpret_cast<volatile uint32_t*>(a.status) != 0u;
   if (upstream_failed) *abort_flag = 1;
-  const int NC = upstream_failed ? 0 : a.NC;
+  // a packed sequence ends with its last chunk that holds tokens
+  const int NCb = a.cu ? min(a.NC, (a.cu[b + 1] - a.cu[b] + kC - 1) / kC) : a.NC;
+  const int NC = upstream_failed ? 0 : NCb;
   // chunk c into stage c % NST (one thread; the stage's previous chunk is done)
   auto load_chunk = [&](int c) {
     const int s = c % NST;
@@ -1384,7 +1398,7 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
     return FALCON_ERR_CUDA;
   if constexpr (DK == 64) {
     {  // per-chunk gates, W and U
-      auto k = tc_wyu_kernel<SOLVE, 64>;
+      auto k = ta.item_map ? tc_wyu_kernel<SOLVE, 64, true> : tc_wyu_kernel<SOLVE, 64, false>;
       const size_t smem = WyuSmem<64>::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
@@ -1475,9 +1489,68 @@ int launch_tc_chunk(const FwdArgs& fa) {
   ta.pro = fa.dk == 64 ? fa.prologue : 0;  // fused into the d = 64 kernels (else applied before)
   ta.wait_ns = wait_limit_ns();
   ta.stall = take_test_stall() ? 1 : 0;
+  ta.cu = fa.dk == 64 ? fa.cu : nullptr;
+  ta.item_map = ta.cu ? fa.item_map : nullptr;
+  ta.item_count = ta.cu ? fa.item_count : nullptr;
   const bool solve = fa.variant == FALCON_1;
   if (fa.dk == 64) return solve ? launch_t<64, 64, true>(fa, ta) : launch_t<64, 64, false>(fa, ta);
   return solve ? launch_t<128, 64, true>(fa, ta) : launch_t<128, 64, false>(fa, ta);
+}
+
+// The items of packed sequences, (b H + h) NC + chunk for every chunk that
+// holds tokens, in that order, then their count at map[B H NC] and the
+// sequences' item offsets at map[B H NC + 1 + b]: one block scans the chunk
+// counts 1024 sequences at a time, then every thread fills items, finding
+// an item's sequence by bisection over the offsets.
+__global__ void __launch_bounds__(1024) varlen_item_map_kernel(const int32_t* cu, int B, int H, int NC,
+                                                              int32_t* map) {
+  __shared__ int32_t scan[1024];
+  __shared__ int32_t base;
+  int32_t* off = map + (size_t)B * H * NC + 1;  // [B + 1]
+  const int tid = threadIdx.x;
+  if (tid == 0) base = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < B; b0 += 1024) {
+    const int b = b0 + tid;
+    const int n = b < B ? min(NC, max(0, (cu[b + 1] - cu[b] + kC - 1) / kC)) * H : 0;
+    scan[tid] = n;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {  // inclusive prefix sum
+      const int v = tid >= o ? scan[tid - o] : 0;
+      __syncthreads();
+      scan[tid] += v;
+      __syncthreads();
+    }
+    if (b < B) off[b] = base + scan[tid] - n;
+    __syncthreads();
+    if (tid == 1023) base += scan[1023];
+    __syncthreads();
+  }
+  const int total = base;
+  if (tid == 0) {
+    off[B] = total;
+    map[(size_t)B * H * NC] = total;
+  }
+  __syncthreads();
+  for (int i = tid; i < total; i += 1024) {
+    int lo = 0, hi = B - 1;  // the last b with off[b] <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    const int r = i - off[lo], nc = (off[lo + 1] - off[lo]) / H;
+    map[i] = (lo * H + r / nc) * NC + r % nc;
+  }
+}
+
+bool tc_chunk_takes_map(const FwdArgs& a) {
+  return !tc_f2_supported(a) && !tc_f3a_supported(a) && !tc_f3_supported(a) && a.dk == 64;
+}
+
+int launch_varlen_item_map(const int32_t* cu, int B, int H, int NC, int32_t* map, cudaStream_t s) {
+  varlen_item_map_kernel<<<1, 1024, 0, s>>>(cu, B, H, NC, map);
+  return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
 
 }  // namespace falcon
