@@ -193,6 +193,7 @@ struct VarlenMap {
   const int32_t* cu;
   const int32_t* item_map;  // B H NC entries, then the count
   int NC;
+  int64_t packed_total;     // > 0: the call's tensors are the packed rows themselves
 };
 
 // The kernel family a chunk forward with these args runs: pick_impl, then
@@ -269,6 +270,9 @@ static int chunk_fwd_impl(const falcon_params_t* p, const void* q, const void* k
     a.cu = vm->cu;
     a.item_map = vm->item_map;
     a.item_count = vm->item_map + (size_t)p->B * p->H * vm->NC;
+    a.packed_total = vm->packed_total;
+  } else if (vm && vm->packed_total > 0) {
+    return FALCON_ERR_UNSUPPORTED;  // packed rows are read in place by that path only
   }
   if (impl == FALCON_IMPL_SCAN) {
     const size_t need = window_scan_ws_bytes(p->B, p->T, p->H, a.W);
@@ -337,25 +341,44 @@ int falcon_chunk_fwd_varlen(const falcon_params_t* p, const int32_t* cu_seqlens,
   const size_t kws = kernel_ws_bytes(p), pws = prologue_bytes(p, true);
   if (!ws_ok(workspace, workspace_bytes, kws + pws + varlen_map_bytes(p))) return FALCON_ERR_WORKSPACE;
   ProArgs pa = pro_args(p, cu_seqlens, q, k, v, beta, lambda);
-  void* o_pad = nullptr;
-  prologue_carve(pa, reinterpret_cast<uint8_t*>(workspace) + kws, true, &o_pad);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  falcon_params_t p0 = *p;
-  p0.prologue = 0;
-  falcon_carry_t co_state;  // the dense pass gives the state; the rest depends on each length
+  falcon_carry_t co_state;  // the chunk pass gives the state; the rest depends on each length
   std::memset(&co_state, 0, sizeof(co_state));
   if (carry_out) co_state.S = carry_out->S;
+  const int W = effective_window(p->variant, p->window), shift = p->pairing == FALCON_PAIR_PREFIX ? 1 : 0;
   // the Falcon-1 / 1A d = 64 tensor-core kernels take only the chunks that
-  // hold tokens (a map built here); the gather then leaves the rest unwritten
+  // hold tokens (a map built here), and read the packed rows in place (the
+  // prologue inside them); every other path reads a padded batch gathered
+  // into the workspace
   VarlenMap vm;
   vm.cu = cu_seqlens;
   vm.item_map = reinterpret_cast<const int32_t*>(reinterpret_cast<uint8_t*>(workspace) + kws + pws);
   vm.NC = (p->T + 63) / 64;
-  FwdArgs ad = make_args(&p0, pa.qo, pa.ko, pa.vo, pa.bo, pa.lo, o_pad, stream);
-  if (carry_in) {
-    ad.S_in = carry_in->S; ad.kprev_in = carry_in->k_prev; ad.pos_in = carry_in->pos;
-    if (ad.W > 1) { ad.winx_in = carry_in->win_x; ad.winv_in = carry_in->win_v; }
+  vm.packed_total = 0;
+  auto with_carry = [&](FwdArgs x) {
+    if (carry_in) {
+      x.S_in = carry_in->S; x.kprev_in = carry_in->k_prev; x.pos_in = carry_in->pos;
+      if (x.W > 1) { x.winx_in = carry_in->win_x; x.winv_in = carry_in->win_v; }
+    }
+    return x;
+  };
+  const FwdArgs au = with_carry(make_args(p, q, k, v, beta, lambda, o, stream));
+  const bool in_place = total_tokens > 0 && W == 1 && resolve_impl(p, au) == FALCON_IMPL_TC &&
+                        tc_chunk_takes_map(au) && (!p->prologue || prologue_fused(p, q, k, v));
+  if (in_place) {
+    vm.packed_total = total_tokens;
+    st = launch_varlen_item_map(cu_seqlens, p->B, p->H, vm.NC, const_cast<int32_t*>(vm.item_map), s);
+    if (st != FALCON_OK) return st;
+    st = chunk_fwd_impl(p, q, k, v, beta, lambda, carry_in, o, &co_state, kws ? workspace : nullptr, kws,
+                        stream, nullptr, 0, &vm);
+    if (st != FALCON_OK) return st;
+    return launch_varlen_finish(pa, nullptr, o, W, shift, carry_in, carry_out, s);
   }
+  void* o_pad = nullptr;
+  prologue_carve(pa, reinterpret_cast<uint8_t*>(workspace) + kws, true, &o_pad);
+  falcon_params_t p0 = *p;
+  p0.prologue = 0;
+  const FwdArgs ad = with_carry(make_args(&p0, pa.qo, pa.ko, pa.vo, pa.bo, pa.lo, o_pad, stream));
   const bool mapped = resolve_impl(&p0, ad) == FALCON_IMPL_TC && tc_chunk_takes_map(ad);
   pa.skip_tail = mapped ? 1 : 0;
   st = launch_prologue(pa, s);
@@ -367,8 +390,7 @@ int falcon_chunk_fwd_varlen(const falcon_params_t* p, const int32_t* cu_seqlens,
   st = chunk_fwd_impl(&p0, pa.qo, pa.ko, pa.vo, pa.bo, pa.lo, carry_in, o_pad, &co_state,
                       kws ? workspace : nullptr, kws, stream, nullptr, 0, mapped ? &vm : nullptr);
   if (st != FALCON_OK) return st;
-  return launch_varlen_finish(pa, o_pad, o, effective_window(p->variant, p->window),
-                              p->pairing == FALCON_PAIR_PREFIX ? 1 : 0, carry_in, carry_out, s);
+  return launch_varlen_finish(pa, o_pad, o, W, shift, carry_in, carry_out, s);
 }
 
 int falcon_recurrent_step(const falcon_params_t* p, const void* q, const void* k, const void* v,

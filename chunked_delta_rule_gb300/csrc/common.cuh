@@ -67,12 +67,14 @@ struct FwdArgs {
   cudaEvent_t* events;      // optional: recorded before the first and after every kernel
   int n_events;
   int prologue;             // falcon_prologue_t flags applied inside the kernel (recurrent step)
-  // packed sequences laid out as a padded batch (varlen): sequence b holds
-  // rows 0 .. cu[b+1] - cu[b] - 1 of batch row b, and the Falcon-1 / 1A
-  // d = 64 tensor-core kernels skip the chunks past its last (NULL: dense)
+  // packed sequences (varlen): sequence b's tokens are rows 0 .. len_b - 1
+  // of batch row b of a padded batch, or (packed_total > 0) rows cu[b] ..
+  // cu[b+1] - 1 of the packed tensors; the Falcon-1 / 1A d = 64 tensor-core
+  // kernels skip the chunks past its last (NULL: dense)
   const int32_t* cu;
   const int32_t* item_map;  // the (b, h, chunk) items that hold tokens, as (b H + h) NC + chunk
   const int32_t* item_count;
+  int64_t packed_total;     // > 0: q, k, v, beta, lambda, o are the packed rows themselves (that many)
 };
 
 // Gates with the optional logit prologue: gamma = clamp(1 - lambda) or

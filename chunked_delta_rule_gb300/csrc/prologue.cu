@@ -190,23 +190,44 @@ __global__ void __launch_bounds__(32 * kProWarps) varlen_scatter_kernel(ProArgs 
   for (int i = lane; i < a.dv; i += 32) dst[i] = src[i];
 }
 
-// per (sequence, head): last key, token count and window ring after the call
+// per (sequence, head): last key, token count and window ring after the call,
+// from the padded batch of the gather or (packed) from the packed rows, whose
+// keys then still take phi here
 template <typename Tin>
-__global__ void __launch_bounds__(128) varlen_carry_kernel(ProArgs a, int W, int shift, const void* kprev_in,
-                                                           const void* winx_in, const void* winv_in,
-                                                           const int64_t* pos_in, void* kprev_out,
-                                                           void* winx_out, void* winv_out, int64_t* pos_out) {
+__global__ void __launch_bounds__(128) varlen_carry_kernel(ProArgs a, int packed, int W, int shift,
+                                                           const void* kprev_in, const void* winx_in,
+                                                           const void* winv_in, const int64_t* pos_in,
+                                                           void* kprev_out, void* winx_out, void* winv_out,
+                                                           int64_t* pos_out) {
+  __shared__ float red[4];
   const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H, tid = threadIdx.x;
   const int len = a.cu[b + 1] - a.cu[b];
   const int64_t pos = pos_in ? pos_in[bh] : 0;
-  const Tin* kpad = cptr<Tin>(a.ko);
-  const Tin* vpad = cptr<Tin>(a.vo);
-  auto pad_row = [&](int t) { return ((size_t)b * a.T + t) * a.H + h; };
+  const Tin* kpad = cptr<Tin>(packed ? a.k : a.ko);
+  const Tin* vpad = cptr<Tin>(packed ? a.v : a.vo);
+  auto pad_row = [&](int t) { return packed ? ((size_t)a.cu[b] + t) * a.H + h : ((size_t)b * a.T + t) * a.H + h; };
+  // phi's scale 1 / max(|x|, 1e-12) of key row t (1 unless the packed rows still need it); every thread calls it
+  auto key_scale = [&](int t) {
+    if (!packed || !(a.flags & FALCON_PROLOGUE_L2NORM_QK)) return 1.f;
+    float ss = 0.f;
+    for (int i = tid; i < a.dk; i += 128) {
+      const float x = to_f32(kpad[pad_row(t) * a.dk + i]);
+      ss = fmaf(x, x, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    const float tot = (red[0] + red[1]) + (red[2] + red[3]);
+    __syncthreads();
+    return 1.f / fmaxf(sqrtf(tot), 1e-12f);
+  };
   if (kprev_out) {
     Tin* kp = reinterpret_cast<Tin*>(kprev_out);
+    const float sc = len >= 1 ? key_scale(len - 1) : 1.f;
     for (int i = tid; i < a.dk; i += 128) {
       Tin x = from_f32<Tin>(0.f);
-      if (len >= 1) x = kpad[pad_row(len - 1) * a.dk + i];
+      if (len >= 1) x = from_f32<Tin>(to_f32(kpad[pad_row(len - 1) * a.dk + i]) * sc);
       else if (kprev_in) x = cptr<Tin>(kprev_in)[(size_t)bh * a.dk + i];
       kp[(size_t)bh * a.dk + i] = x;
     }
@@ -292,7 +313,8 @@ int launch_prologue(const ProArgs& a, cudaStream_t s) {
 int launch_varlen_finish(const ProArgs& a, const void* o_pad, void* o, int W, int shift,
                          const falcon_carry_t* ci, falcon_carry_t* co, cudaStream_t s) {
   const size_t row_bytes = (size_t)a.dv * (a.dtype == FALCON_BF16 ? 2 : 4);
-  const long long rows = (long long)a.B * a.T * a.H;
+  const long long rows = o_pad ? (long long)a.B * a.T * a.H : 0;  // no padded outputs: written in place
+  const int packed = o_pad ? 0 : 1;
   if (rows > 0 && row_bytes % 16 == 0 && ((reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(o_pad)) & 15) == 0) {
     const int pieces = (int)(row_bytes / 16);
     const long long n = rows * pieces;
@@ -310,9 +332,11 @@ int launch_varlen_finish(const ProArgs& a, const void* o_pad, void* o, int W, in
     void* wxo = W > 1 ? co->win_x : nullptr;
     void* wvo = W > 1 ? co->win_v : nullptr;
     if (a.dtype == FALCON_BF16)
-      varlen_carry_kernel<__nv_bfloat16><<<a.B * a.H, 128, 0, s>>>(a, W, shift, kpi, wxi, wvi, pi, co->k_prev, wxo, wvo, co->pos);
+      varlen_carry_kernel<__nv_bfloat16><<<a.B * a.H, 128, 0, s>>>(a, packed, W, shift, kpi, wxi, wvi, pi, co->k_prev,
+                                                                  wxo, wvo, co->pos);
     else
-      varlen_carry_kernel<float><<<a.B * a.H, 128, 0, s>>>(a, W, shift, kpi, wxi, wvi, pi, co->k_prev, wxo, wvo, co->pos);
+      varlen_carry_kernel<float><<<a.B * a.H, 128, 0, s>>>(a, packed, W, shift, kpi, wxi, wvi, pi, co->k_prev, wxo,
+                                                          wvo, co->pos);
   }
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }

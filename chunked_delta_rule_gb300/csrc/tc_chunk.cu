@@ -83,6 +83,9 @@ struct TcArgs {
   const int32_t* cu;
   const int32_t* item_map;
   const int32_t* item_count;
+  int packed;         // with cu: q, k, v, o are the packed [total, H, d] rows themselves, sequence b
+                      // at rows cu[b] .. cu[b+1] - 1 (else a padded [B, T] batch)
+  __nv_bfloat16* o;   // the output rows (packed: stored row by row, up to each sequence's end)
 };
 
 // ======================================================================
@@ -177,11 +180,13 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
     const int ri = real_item(item);
     const int chunk = ri % a.NC, bh = ri / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
     if (tid == 0) {
+      // packed rows: sequence b from row cu[b] of one [total, H, d] batch row
+      const int r0 = (MAP && a.packed) ? a.cu[b] + t0 : t0, bb = (MAP && a.packed) ? 0 : b;
       ++issued;
       mbar_arrive_expect_tx(&bar[0], kImg);
       for (int k = 0; k < kSl; ++k) {
-        tma_load_4d(Vs + k * 8192, &tm_v, &bar[0], 64 * k, h, t0, b);
-        tma_load_4d(Xs + k * 8192, &tm_k, &bar[0], 64 * k, h, t0 - a.shift, b);
+        tma_load_4d(Vs + k * 8192, &tm_v, &bar[0], 64 * k, h, r0, bb);
+        tma_load_4d(Xs + k * 8192, &tm_k, &bar[0], 64 * k, h, r0 - a.shift, bb);
       }
     }
   };
@@ -193,8 +198,12 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
     const int ri = real_item(item);
     const int chunk = ri % a.NC, bh = ri / a.NC, b = bh / a.H, h = bh % a.H, t0 = chunk * kC;
     const int t = t0 + tid;
-    const bool step_ok = tid < 64 && t < a.T;
-    const size_t gi = ((size_t)b * a.T + (step_ok ? t : 0)) * a.H + h;
+    // a step past the sequence's end neither writes nor decays (packed rows:
+    // those are the next sequence's)
+    const int len = MAP ? a.cu[b + 1] - a.cu[b] : a.T;
+    const bool step_ok = tid < 64 && t < len;
+    const size_t grow = (MAP && a.packed) ? (size_t)a.cu[b] + (step_ok ? t : 0) : (size_t)b * a.T + (step_ok ? t : 0);
+    const size_t gi = grow * a.H + h;
     lam_r = a.lam[gi];
     beta_r = a.beta[gi];
     pos_r = a.pos_in ? a.pos_in[bh] : 0;
@@ -213,7 +222,8 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   const int chunk = ri % a.NC, bh = ri / a.NC;
   const int next = item + gridDim.x;
   const int t_row = chunk * kC + tid;
-  const bool step_ok = tid < 64 && t_row < a.T;
+  const int len_b = MAP ? a.cu[bh / a.H + 1] - a.cu[bh / a.H] : a.T;
+  const bool step_ok = tid < 64 && t_row < len_b;
   // the clamped decay and the step size, from gate logits when the prologue asks
   const float ell = step_ok ? logf(gate_gamma(lam_n, a.eps_gamma, a.pro)) : 0.f;
   const float beta = (step_ok && pos_n + t_row >= a.shift) ? gate_beta(beta_n, a.pro) : 0.f;
@@ -243,6 +253,8 @@ __global__ void __launch_bounds__(128, DK == 64 ? 4 : 2) tc_wyu_kernel(const __g
   const bool carried = chunk == 0 && a.kprev_in && a.shift;  // x_0 = the carried key
   if (carried && tid < DK)
     *reinterpret_cast<__nv_bfloat16*>(Xs + (tid >> 6) * 8192 + sw128(0, tid & 63)) = a.kprev_in[(size_t)bh * DK + tid];
+  if (MAP && a.packed && chunk == 0 && a.shift && !a.kprev_in && tid < DK)  // not the previous sequence's key
+    *reinterpret_cast<__nv_bfloat16*>(Xs + (tid >> 6) * 8192 + sw128(0, tid & 63)) = __float2bfloat16_rn(0.f);
   if constexpr (DK == 64) {  // the prologue is fused into the d = 64 path only
     // phi(k) = k / max(|k|, 1e-12) per key row, in place (the carried key is
     // a feature already)
@@ -950,7 +962,7 @@ struct ChainSmem {
   static constexpr int G_SQ = 256, G_SX = 320;
 };
 
-template <bool SOLVE, bool L2N>
+template <bool SOLVE, bool L2N, bool PK = false>  // PK: packed sequences' rows read and written in place
 __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
     tc_fwd_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_o, TcArgs a) {
@@ -1032,8 +1044,9 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
     uint8_t* st = stage(s);
     const size_t ci = (size_t)bh * a.NC + c;
     mbar_arrive_expect_tx(&full[s], L::TX);
-    tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, c * kC - a.shift, b);
-    tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
+    const int r0 = PK ? a.cu[b] + c * kC : c * kC, bb = PK ? 0 : b;  // packed: one batch row
+    tma_load_4d(st + L::XO, &tm_k, &full[s], 0, h, r0 - a.shift, bb);
+    tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, r0, bb);
     if (SOLVE) bulk_load(st + L::WO, a.ws_T + ci * 16384, 8192, &full[s]);
     bulk_load(st + L::UO, a.ws_T + ci * 16384 + 8192, 8192, &full[s]);
     bulk_load(st + L::GO, a.ws_g + ci * kGateF, 1024, &full[s]);
@@ -1074,6 +1087,8 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
       const bool carried = c == 0 && a.kprev_in && a.shift;  // x_0 = the carried key
       if (carried && ftid < 64)
         *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = a.kprev_in[(size_t)bh * 64 + ftid];
+      if (PK && c == 0 && a.shift && !a.kprev_in && ftid < 64)  // not the previous sequence's key
+        *reinterpret_cast<__nv_bfloat16*>(st + L::XO + sw128(0, ftid)) = __float2bfloat16_rn(0.f);
       if constexpr (L2N) {  // row scales of the prologue's phi, 1 / max(|row|, 1e-12), of the query
                             // row and the key row r (the carried key is a feature already); the raw
                             // rows enter the products and the scales their epilogues
@@ -1349,15 +1364,23 @@ __global__ void __launch_bounds__(ChainSmem<SOLVE, L2N>::kThreads, 1)
             const int n = 8 * j + 2 * e;
             pk[e] = pack_bf16(__uint_as_float(ov[n >> 5][n & 31]), __uint_as_float(ov[(n + 1) >> 5][(n + 1) & 31]));
           }
-          *reinterpret_cast<uint4*>(Ost + sw128(t, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          if (PK) {  // the row itself, if it belongs to the sequence
+            if (c * kC + t < a.cu[b + 1] - a.cu[b])
+              *reinterpret_cast<uint4*>(a.o + (((size_t)a.cu[b] + c * kC + t) * a.H + h) * 64 + 8 * j) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          } else {
+            *reinterpret_cast<uint4*>(Ost + sw128(t, 8 * j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
         }
       }
       fence_proxy_async();
       named_bar(4, 64);
       if (tid == 64) {
         *out_read = c + 1;  // both output warps read this chunk's accumulator
-        tma_store_4d(&tm_o, Ost, 0, h, c * kC, b);
-        bulk_commit();
+        if (!PK) {
+          tma_store_4d(&tm_o, Ost, 0, h, c * kC, b);
+          bulk_commit();
+        }
       }
     }
     if (tid == 64) bulk_wait0();
@@ -1393,8 +1416,10 @@ template <int DK, int NV, bool SOLVE>
 int launch_t(const FwdArgs& fa, const TcArgs& ta) {
   const int BH = fa.B * fa.H;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, fa.q, fa.B, fa.T, fa.H, DK, 64) || !make_map(&mk, fa.k, fa.B, fa.T, fa.H, DK, 64) ||
-      !make_map(&mv, fa.v, fa.B, fa.T, fa.H, fa.dv, 64) || !make_map(&mo, fa.o, fa.B, fa.T, fa.H, fa.dv, 64))
+  // packed sequences read in place: the rows of all sequences as one batch row
+  const int mB = ta.packed ? 1 : fa.B, mT = ta.packed ? (int)fa.packed_total : fa.T;
+  if (!make_map(&mq, fa.q, mB, mT, fa.H, DK, 64) || !make_map(&mk, fa.k, mB, mT, fa.H, DK, 64) ||
+      !make_map(&mv, fa.v, mB, mT, fa.H, fa.dv, 64) || !make_map(&mo, fa.o, mB, mT, fa.H, fa.dv, 64))
     return FALCON_ERR_CUDA;
   if constexpr (DK == 64) {
     {  // per-chunk gates, W and U
@@ -1411,7 +1436,8 @@ int launch_t(const FwdArgs& fa, const TcArgs& ta) {
     }
     {  // transition form: producer warp, front warpgroup, chain and output warps
       const bool l2n = (ta.pro & FALCON_PROLOGUE_L2NORM_QK) != 0;
-      auto k = l2n ? tc_fwd_chain_kernel<SOLVE, true> : tc_fwd_chain_kernel<SOLVE, false>;
+      auto k = ta.packed ? (l2n ? tc_fwd_chain_kernel<SOLVE, true, true> : tc_fwd_chain_kernel<SOLVE, false, true>)
+                         : (l2n ? tc_fwd_chain_kernel<SOLVE, true, false> : tc_fwd_chain_kernel<SOLVE, false, false>);
       const size_t smem = l2n ? ChainSmem<SOLVE, true>::TOTAL : ChainSmem<SOLVE, false>::TOTAL;
       if (!set_smem_limit(reinterpret_cast<const void*>(k), smem))
         return FALCON_ERR_CUDA;
@@ -1492,6 +1518,8 @@ int launch_tc_chunk(const FwdArgs& fa) {
   ta.cu = fa.dk == 64 ? fa.cu : nullptr;
   ta.item_map = ta.cu ? fa.item_map : nullptr;
   ta.item_count = ta.cu ? fa.item_count : nullptr;
+  ta.packed = ta.cu && fa.packed_total > 0 ? 1 : 0;
+  ta.o = reinterpret_cast<__nv_bfloat16*>(fa.o);
   const bool solve = fa.variant == FALCON_1;
   if (fa.dk == 64) return solve ? launch_t<64, 64, true>(fa, ta) : launch_t<64, 64, false>(fa, ta);
   return solve ? launch_t<128, 64, true>(fa, ta) : launch_t<128, 64, false>(fa, ta);

@@ -233,3 +233,31 @@ def test_prologue_misaligned_rows(F):
     torch.cuda.synchronize()
     o_ref, c_ref = oracle_pro(w, x, BOTH)
     check(w, o, co["S"], o_ref, c_ref["S"])
+
+
+@pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])
+def test_varlen_in_place_carry_without_key(F, variant):
+    """Packed rows read in place: a sequence that continues (pos > 0) with no
+    carried key pairs its first value with a zero key, never with the
+    previous sequence's last key, which sits on the row before it."""
+    lengths = [70, 5, 131]
+    w = wl(variant, seed=1201)
+    T = max(lengths)
+    wfull = w.with_(B=len(lengths), T=T)
+    x = make_inputs(wfull, device="cpu")
+    packed, cu = pack_varlen(x, lengths, device="cuda")
+    p = params_for(F, wfull)
+    ci = make_carry(wfull, seed=78, pos=torch.tensor([3, 9, 1]).repeat_interleave(w.H), device="cuda")
+    del ci["k_prev"]
+    o, co = F.chunk_forward_varlen(p, cu, packed["q"], packed["k"], packed["v"], packed["beta"],
+                                   packed["lam"], ci)
+    torch.cuda.synchronize()
+    pn = to_np(packed)
+    cn = to_np(ci)
+    cin = [{n: a[i:i + 1] for n, a in cn.items()} for i in range(len(lengths))]
+    o_ref, cos = oracle.recurrent_varlen(pn["q"], pn["k"], pn["v"], pn["beta"], pn["lam"], cu.cpu().numpy(),
+                                         w.variant, w.window, w.eps, w.eps_gamma, carries=cin, pairing=w.pairing)
+    tol = TOL[w.dtype]
+    assert rel_err(o.float().cpu().numpy(), o_ref) <= tol
+    for i in range(len(lengths)):
+        assert rel_err(co["S"][i:i + 1].cpu().numpy(), cos[i]["S"]) <= tol, i
