@@ -237,14 +237,17 @@ size_t falcon_varlen_workspace_size(const falcon_params_t* p);
  * q, k [total_tokens, H, dk], v, o [total_tokens, H, dv], beta
  * [total_tokens, H] (or [total_tokens, H, dv]), lambda [total_tokens, H];
  * carry_in / carry_out are per sequence ([B, H, ...], as for
- * falcon_chunk_fwd; NULL carry_in = every sequence fresh).  The tokens are
- * laid out as a [B, p->T] batch in the workspace (applying p->prologue on
- * the way); positions past a sequence's end get beta = 0 and lambda = 0,
- * steps that neither write nor decay, so each sequence's state after p->T
- * steps is its state after its own length; the same kernel family as
- * falcon_chunk_fwd then runs, and the outputs go back to the packed layout.
- * carry_out's k_prev, pos and window ring are those after each sequence's
- * own last token.  Errors as falcon_chunk_fwd. */
+ * falcon_chunk_fwd; NULL carry_in = every sequence fresh).  On the
+ * Falcon-1 / 1A d = 64 tensor-core path (bf16, rows on 16-byte boundaries)
+ * the kernels read and write the packed rows in place and take only the
+ * chunks that hold tokens (p->prologue applied inside them).  Otherwise the
+ * tokens are laid out as a [B, p->T] batch in the workspace (applying
+ * p->prologue on the way); positions past a sequence's end get beta = 0 and
+ * lambda = 0, steps that neither write nor decay, so each sequence's state
+ * after p->T steps is its state after its own length; the same kernel
+ * family as falcon_chunk_fwd then runs, and the outputs go back to the
+ * packed layout.  carry_out's k_prev, pos and window ring are those after
+ * each sequence's own last token.  Errors as falcon_chunk_fwd. */
 int falcon_chunk_fwd_varlen(const falcon_params_t* p, const int32_t* cu_seqlens, int64_t total_tokens,
                             const void* q, const void* k, const void* v, const float* beta,
                             const float* lambda, const falcon_carry_t* carry_in, void* o,
