@@ -189,6 +189,28 @@ def test_recurrent_step_decode(F, variant, dtype):
                                   carry[key].cpu().numpy(), c_ref[key]), key
 
 
+@pytest.mark.parametrize("variant", [FALCON_1, FALCON_3, FALCON_3A])
+def test_recurrent_step_full_size(F, variant):
+    """256 x 12 heads, d = 64 (the decode workload the benchmark times): more
+    (b, h) items than the window variants' persistent kernel has CTAs, so its
+    CTAs walk several items through the double-buffered state; three
+    consecutive steps, every head against the oracle."""
+    from workloads import make_decode_inputs
+    x, carry, w = make_decode_inputs(variant, window=8, B=256, H=12, d=64, seed=17)
+    carry = {k: v.cuda() for k, v in carry.items()}
+    cref = {k: v.clone().cpu() for k, v in carry.items()}
+    p = params_for(F, w, T=1)
+    for step in range(3):
+        xs, _, _ = make_decode_inputs(variant, window=8, B=256, H=12, d=64, seed=100 + step)
+        xs = {k: v.cuda() for k, v in xs.items()}
+        o_ref, c_next = oracle_full(w, xs, {k: v.clone() for k, v in cref.items()})
+        o = torch.empty((w.B, 1, w.H, w.dv), dtype=xs["q"].dtype, device="cuda")
+        F.falcon_recurrent_step(p, xs["q"], xs["k"], xs["v"], xs["beta"], xs["lam"], carry, o)
+        torch.cuda.synchronize()
+        check(w, o, carry, o_ref, c_next, "decode")
+        cref = {k: torch.from_numpy(np.asarray(c)) for k, c in c_next.items()}  # the oracle's own carry, fp64
+
+
 @pytest.mark.parametrize("d", [16, 32, 128])
 def test_recurrent_step_dims(F, d):
     from workloads import make_decode_inputs
