@@ -110,7 +110,8 @@ def kernel_bytes(w, names) -> list:
     if names[0] == "window_prep_kernel":  # keys and gate inputs; then the whole forward
         return [th * w.dk * es + beta + th * 4, algorithmic_bytes(w)]
     if names[0] == "f3a_chunk_kernel":  # q, k, v and gate inputs; then q in, o and the state out
-        return [th * (2 * w.dk + w.dv) * es + beta + th * 4, th * (w.dk + w.dv) * es + state]
+        mid = [0] if len(names) == 3 else []  # the group totals read intermediates only
+        return [th * (2 * w.dk + w.dv) * es + beta + th * 4] + mid + [th * (w.dk + w.dv) * es + state]
     if names[0] == "f3_chunk_kernel":  # q, k, v and gate inputs; then o and the state out
         return [th * (2 * w.dk + w.dv) * es + beta + th * 4, th * w.dv * es + state]
     return [th * (w.dk + w.dv) * es + beta + th * 4, th * (2 * w.dk + w.dv) * es + state]
@@ -723,8 +724,9 @@ def main():
             names = ["generic_chunk_kernel"]
         elif w.per_channel:
             names = ["tc_f2_kernel"]
-        elif w.variant == 5:  # Falcon-3A
-            names = ["f3a_chunk_kernel", "f3a_chain_kernel"]
+        elif w.variant == 5:  # Falcon-3A (the chain in groups: their totals first)
+            names = (["f3a_chunk_kernel", "f3a_group_kernel", "f3a_chain_kernel"] if launches == 3
+                     else ["f3a_chunk_kernel", "f3a_chain_kernel"])
         elif w.variant == 4:  # Falcon-3
             names = ["f3_chunk_kernel", "f3_chain_kernel"]
         elif w.dk == 64:

@@ -134,6 +134,7 @@ int launch_tc_f2(const FwdArgs& a);
 bool tc_f3a_supported(const FwdArgs& a);
 int launch_tc_f3a(const FwdArgs& a);
 size_t tc_f3a_ws_bytes(int B, int T, int H);
+int tc_f3a_launches(const FwdArgs& a);  // 2, or 3 when the chain runs in groups
 bool tc_f3_supported(const FwdArgs& a);
 int launch_tc_f3(const FwdArgs& a);
 size_t tc_f3_ws_bytes(int B, int T, int H);

@@ -1482,7 +1482,10 @@ bool tc_chunk_supported(const FwdArgs& a) {
   return true;
 }
 
-int tc_chunk_launches(const FwdArgs& a) { return tc_f2_supported(a) ? 1 : 2; }
+int tc_chunk_launches(const FwdArgs& a) {
+  if (tc_f3a_supported(a)) return tc_f3a_launches(a);
+  return tc_f2_supported(a) ? 1 : 2;
+}
 
 size_t tc_chunk_ws_bytes(int B, int T, int H, int dk, int, int chunk, int variant) {
   if (variant == FALCON_2 || variant == FALCON_2A) return 256;  // status word only

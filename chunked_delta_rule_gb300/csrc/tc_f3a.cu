@@ -27,8 +27,13 @@
 //      fp32 state in registers (no product on the chain), and off it
 //      O = diag(Gamma) Q S0 + O0 with Q S0 one tcgen05 product per chunk
 //      (N = 32), the outputs stored by 32-byte rows; a producer warp streams
-//      Q, b, O0 and the gates six chunks ahead; two output warpgroups take
-//      alternate chunks.
+//      Q, its half of b and O0 (stored by halves) and the gates ahead; two
+//      output warpgroups take alternate chunks.  The chain's only coupling
+//      across chunks is the scalar decay, so when one chain per (b, h)
+//      would leave SMs idle the chunks split into G groups:
+//      f3a_group_kernel sums each group's b with its decays (from a zero
+//      state), and the chain CTAs of group g (lighter, two per SM) start
+//      from S_in carried through the earlier groups' totals.
 // Every wait is bounded; on timeout a kernel records an error in the
 // workspace status word and leaves its loop (the chain kernel computes
 // nothing when the first kernel recorded one).
@@ -74,10 +79,35 @@ struct F3aArgs {
   uint64_t wait_ns;   // limit of every bounded wait
   int stall;          // failure-detection test hook: the per-chunk kernel's first CTA waits on
                       // a barrier that nothing completes, and so records a timeout
+  // the chain in G groups of CPG chunks (G = 1: one group): group g of (b, h)
+  // starts from the state the groups before it leave, gdec[g'] S + gtot[g']
+  int G, CPG;
+  float* gtot;        // [B H][G][64][64] fp32: a group's state from a zero start
+  float* gdec;        // [B H][G]: the product of its chunks' Gamma_last
 };
 
-// per chunk in the workspace: b (bf16 tile) | Gamma (64 fp32) | O0 (bf16 tile)
+// per chunk in the workspace: b | Gamma (64 fp32) | O0, b and O0 bf16 by
+// halves of 32 value columns ([2][64 rows][32], 4 KB each, pieces placed by
+// half_off; only the chain's elementwise work reads them, so each chain CTA
+// loads its own half)
 constexpr size_t kF3aChunkWs = 8192 + 256 + 8192;
+constexpr size_t kF3aGam = 8192, kF3aO0 = 8192 + 256;
+
+// Byte offset of the 16-byte piece p (columns 8 p .. 8 p + 7) of row r in
+// one half of such a tile: the piece index XOR (r >> 1) & 3 puts eight
+// consecutive rows' pieces on different banks.
+__device__ __forceinline__ int half_off(int r, int p) { return r * 64 + 16 * (p ^ ((r >> 1) & 3)); }
+
+// a 64-value fp32 row as bf16 into a [2][64][32] half-major tile
+__device__ __forceinline__ void store_row_halves(uint8_t* tile, int r, const float* v) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pk[e] = pack_bf16(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+    *reinterpret_cast<uint4*>(tile + (j >> 2) * 4096 + half_off(r, j & 3)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
 
 struct F3aChunkSmem {
   // X (80 key rows, then X~) | P~^T (80 rows; then O0's staging) | V (80 rows) | Q | gates | b's staging
@@ -93,24 +123,30 @@ struct F3aChunkSmem {
   static constexpr uint32_t COL_PT = 0, COL_D = 64, NCOLS = 128;
 };
 
-struct F3aChainSmem {
+template <int NST_, int NB_>
+struct F3aChainSmemT {
   // stages in flight: each CTA streams ~25 KB per chunk, so the loads in
   // flight (NST stages) set its bandwidth at the memory latency
-  static constexpr int NST = 6;
-  // stage: Q | b | Gamma | O0
-  static constexpr size_t QO = 0, BO = 8192, GO = BO + 8192, OO = GO + 256, STAGE = 25600;
-  static constexpr int NB = 6;                     // S0 tiles and TMEM accumulators in flight
+  static constexpr int NST = NST_;
+  // stage: Q | this CTA's half of b | Gamma | its half of O0
+  static constexpr size_t QO = 0, BO = 8192, GO = BO + 4096, OO = GO + 256, STAGE = 17408;
+  static constexpr int NB = NB_;                   // S0 tiles and TMEM accumulators in flight
+  static constexpr uint32_t NCOLS = NB * 32 <= 128 ? 128 : 256;
   static constexpr size_t SB = NST * STAGE;        // S0 of chunk c in SB + (c % NB) 8192 (MN-major B,
                                                    // this CTA's 32 columns in columns 0..31)
   static constexpr size_t BAR = SB + NB * 8192;
   static constexpr size_t MISC = BAR + 256;
   static constexpr size_t TOTAL = MISC + 16 + 1024;
-  static constexpr uint32_t TX = 8192 + 8192 + 256 + 8192;
+  static constexpr uint32_t TX = 8192 + 4096 + 256 + 4096;
   static constexpr int kThreads = 384;  // outputs 0..3 and 8..11 (alternate chunks), chain 4..5,
                                         // producer 6, issuer 7
-  static_assert(OO + 8192 <= STAGE && STAGE % 1024 == 0, "stage layout");
+  static_assert(OO + 4096 <= STAGE && STAGE % 1024 == 0, "stage layout");
   static_assert(TOTAL <= 232448, "shared memory budget");
+  static_assert((2 * NST + 3 * NB) * 8 <= 256, "barriers");
 };
+// one chain CTA per SM for (b, h) over all chunks; two per SM for groups of chunks
+using F3aChainSmem = F3aChainSmemT<6, 6>;
+using F3aChainSmemG = F3aChainSmemT<4, 4>;
 
 // Key (x) and value of local pair j of (b, h): j >= 1 from the sequence,
 // j = 0 the carried key with the first value, j < 0 the carried window ring.
@@ -379,7 +415,7 @@ __global__ void __launch_bounds__(128, 4)
       float dv[64];
       tmem_ld64(tmem + lane_off + L::COL_D, dv);
       tmem_wait_ld();
-      store_row64(quad < 2 ? sm + L::BST : sm + L::PO, row & 63, dv);
+      store_row_halves(quad < 2 ? sm + L::BST : sm + L::PO, row & 63, dv);
       if (tid < 64) reinterpret_cast<float*>(sm + L::BST + 8192)[tid] = gt[L::G_GAM + tid];
     }
     fence_proxy_async();
@@ -410,9 +446,10 @@ __global__ void __launch_bounds__(128, 4)
 // ======================================================================
 // (b) the chain: S1 = Gamma_last S0 + b, O = diag(Gamma) Q S0 + O0
 // ======================================================================
-__global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
+template <int NST_, int NB_, int MINB>
+__global__ void __launch_bounds__(384, MINB)
     f3a_chain_kernel(const __grid_constant__ CUtensorMap tm_q, F3aArgs a) {
-  using L = F3aChainSmem;
+  using L = F3aChainSmemT<NST_, NB_>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   constexpr int NST = L::NST;
@@ -426,8 +463,12 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x >> 1, half = blockIdx.x & 1, b = bh / a.H, h = bh % a.H;
+  // CTA (g, b, h, half): group g of the chunks of (b, h), 32 value columns
+  const int BH = a.B * a.H;
+  const int bh = (blockIdx.x >> 1) % BH, g = (blockIdx.x >> 1) / BH, half = blockIdx.x & 1;
+  const int b = bh / a.H, h = bh % a.H;
   const int c0 = 32 * half;  // this CTA's value columns c0 .. c0 + 31
+  const bool last_group = g == a.G - 1;
   const int W = a.W;
   auto stage = [&](int s) { return sm + s * L::STAGE; };
   auto fail = [&]() {
@@ -448,7 +489,7 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, L::NCOLS);
     tmem_relinquish();
     tc_fence_before();
   }
@@ -461,7 +502,9 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const bool upstream_failed = *reinterpret_cast<volatile uint32_t*>(a.status) != 0u;
   if (upstream_failed) *abort_flag = 1;
-  const int NC = upstream_failed ? 0 : a.NC;
+  // this group's chunks cbase .. cbase + NC - 1 (local index c below)
+  const int cbase = g * a.CPG;
+  const int NC = upstream_failed ? 0 : max(0, min(a.NC - cbase, a.CPG));
   const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
 
   if (warp == 6) {
@@ -474,11 +517,12 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
         if (c >= NST && !mbar_wait(&empty[s], (uint32_t)(((c - NST) / NST) & 1), a.wait_ns)) { fail(); break; }
         if (*abort_flag) break;
         uint8_t* st = stage(s);
-        const uint8_t* src = a.ws_f3a + (size_t)(bh * a.NC + c) * kF3aChunkWs;
+        const uint8_t* src = a.ws_f3a + (size_t)(bh * a.NC + cbase + c) * kF3aChunkWs;
         mbar_arrive_expect_tx(&full[s], L::TX);
-        tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, c * kC, b);
-        bulk_load(st + L::BO, src, 8192 + 256, &full[s]);
-        bulk_load(st + L::OO, src + 8192 + 256, 8192, &full[s]);
+        tma_load_4d(st + L::QO, &tm_q, &full[s], 0, h, (cbase + c) * kC, b);
+        bulk_load(st + L::BO, src + half * 4096, 4096, &full[s]);
+        bulk_load(st + L::GO, src + kF3aGam, 256, &full[s]);
+        bulk_load(st + L::OO, src + kF3aO0 + half * 4096, 4096, &full[s]);
       }
       if (*abort_flag) {  // drain the loads still in flight
         for (int cc = (c > NST ? c - NST : 0); cc < c; ++cc)
@@ -519,6 +563,16 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
         sreg[n] = v4.x; sreg[n + 1] = v4.y; sreg[n + 2] = v4.z; sreg[n + 3] = v4.w;
       }
     }
+    for (int gg = 0; gg < g; ++gg) {  // through the groups before this one
+      const float dg = a.gdec[(size_t)bh * a.G + gg];
+      const float* tg = a.gtot + (((size_t)bh * a.G + gg) * 64 + r) * 64 + c0;
+#pragma unroll
+      for (int n = 0; n < 32; n += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(tg + n);
+        sreg[n] = fmaf(dg, sreg[n], v4.x); sreg[n + 1] = fmaf(dg, sreg[n + 1], v4.y);
+        sreg[n + 2] = fmaf(dg, sreg[n + 2], v4.z); sreg[n + 3] = fmaf(dg, sreg[n + 3], v4.w);
+      }
+    }
     auto store_s = [&](int buf) {  // row r, columns 0..31 of the tile
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -543,7 +597,7 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
       const float gl = reinterpret_cast<const float*>(st + L::GO)[63];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {  // S1 = Gamma_last S0 + b, row r, this CTA's columns
-        const uint4 raw = *reinterpret_cast<const uint4*>(st + L::BO + sw128(r, c0 + 8 * j));
+        const uint4 raw = *reinterpret_cast<const uint4*>(st + L::BO + half_off(r, j));
         const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -561,7 +615,7 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
         mbar_arrive(&sready[pn]);
       }
     }
-    if (!*abort_flag && a.S_out) {
+    if (!*abort_flag && a.S_out && last_group) {
       float* dst = a.S_out + ((size_t)bh * 64 + r) * 64 + c0;
 #pragma unroll
       for (int n = 0; n < 32; n += 4)
@@ -591,7 +645,7 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
       const int col = c0 + 16 * hf;  // this thread's 16 value columns
       uint4 o0[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) o0[j] = *reinterpret_cast<const uint4*>(st + L::OO + sw128(t, col + 8 * j));
+      for (int j = 0; j < 2; ++j) o0[j] = *reinterpret_cast<const uint4*>(st + L::OO + half_off(t, 2 * hf + j));
       mbar_arrive(&empty[s]);
       uint32_t pk[8];
 #pragma unroll
@@ -604,14 +658,14 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
           pk[4 * j + e] = pack_bf16(fmaf(gq, __uint_as_float(acc[n]), b2.x), fmaf(gq, __uint_as_float(acc[n + 1]), b2.y));
         }
       }
-      const int tg = c * kC + t;
+      const int tg = (cbase + c) * kC + t;
       if (tg < a.T) {
         uint4* dst = reinterpret_cast<uint4*>(a.o + (((size_t)b * a.T + tg) * a.H + h) * 64 + col);
         dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
     }
-    if (half == 0 && og == 0 && !*abort_flag) {  // carry: last key, the last W - 1 pairs, position
+    if (half == 0 && og == 0 && last_group && !*abort_flag) {  // carry: last key, the last W - 1 pairs, position
       if (a.kprev_out && otid < 64)
         a.kprev_out[(size_t)bh * 64 + otid] = a.k[(((size_t)b * a.T + (a.T - 1)) * a.H + h) * 64 + otid];
       const int Wr = W - 1;
@@ -634,7 +688,77 @@ __global__ void __launch_bounds__(F3aChainSmem::kThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, L::NCOLS);
+  }
+}
+
+// Group totals of the chain (every group but the last; G >= 2): from a zero
+// state, T = Gamma_last T + b over the group's chunks, and D = the product of
+// their Gamma_last.  Eight parts of 64 threads take an eighth of the chunks
+// each (thread r: row r, all 64 columns; the next chunk's row is loaded
+// before the current one is added), then the parts combine in order,
+// T = (..(T0 D1 + T1) D2 + ..) D7 + T7.
+constexpr int kGParts = 8;
+constexpr int kGLd = 68;  // padded row of the part totals (rows on different banks)
+__global__ void __launch_bounds__(64 * kGParts) f3a_group_kernel(F3aArgs a) {
+  extern __shared__ float gsm[];  // [kGParts][64][kGLd] part totals, then [kGParts] part decays
+  const int tid = threadIdx.x, r = tid & 63, part = tid >> 6;
+  const int g = blockIdx.x % (a.G - 1), bh = blockIdx.x / (a.G - 1);
+  const int cs = g * a.CPG, qp = (a.CPG + kGParts - 1) / kGParts;
+  const int p0 = cs + part * qp, p1 = min(cs + min(a.CPG, (part + 1) * qp), a.NC);
+  float t[64];
+#pragma unroll
+  for (int n = 0; n < 64; ++n) t[n] = 0.f;
+  float d = 1.f;
+  const bool failed = *reinterpret_cast<volatile uint32_t*>(a.status) != 0u;
+  auto rec = [&](int c) { return a.ws_f3a + (size_t)(bh * a.NC + c) * kF3aChunkWs; };
+  uint4 nx[8];
+  float gn = 1.f;
+  auto fetch = [&](int c) {  // row r of b and Gamma_last of chunk c
+#pragma unroll
+    for (int j = 0; j < 8; ++j) nx[j] = *reinterpret_cast<const uint4*>(rec(c) + (j >> 2) * 4096 + half_off(r, j & 3));
+    gn = reinterpret_cast<const float*>(rec(c) + kF3aGam)[63];
+  };
+  if (!failed && p0 < p1) fetch(p0);
+  for (int c = p0; c < p1 && !failed; ++c) {
+    uint4 cur[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cur[j] = nx[j];
+    const float gl = gn;
+    if (c + 1 < p1) fetch(c + 1);
+    d *= gl;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // eight 16-byte pieces of row r (four of each half)
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&cur[j]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 b2 = __bfloat1622float2(pb[e]);
+        t[8 * j + 2 * e] = fmaf(gl, t[8 * j + 2 * e], b2.x);
+        t[8 * j + 2 * e + 1] = fmaf(gl, t[8 * j + 2 * e + 1], b2.y);
+      }
+    }
+  }
+  float* mine = gsm + ((size_t)part * 64 + r) * kGLd;
+#pragma unroll
+  for (int n = 0; n < 64; n += 4) *reinterpret_cast<float4*>(mine + n) = make_float4(t[n], t[n + 1], t[n + 2], t[n + 3]);
+  if (r == 0) gsm[kGParts * 64 * kGLd + part] = d;
+  __syncthreads();
+  const float* dp = gsm + kGParts * 64 * kGLd;
+  constexpr int kCols = 64 / kGParts;
+  const int col0 = kCols * part;  // this thread combines row r, columns col0 .. col0 + kCols - 1
+  float* dst = a.gtot + (((size_t)bh * a.G + g) * 64 + r) * 64 + col0;
+#pragma unroll
+  for (int n = 0; n < kCols; ++n) {
+    float v = gsm[(size_t)r * kGLd + col0 + n];
+#pragma unroll
+    for (int q = 1; q < kGParts; ++q) v = fmaf(dp[q], v, gsm[((size_t)q * 64 + r) * kGLd + col0 + n]);
+    dst[n] = v;
+  }
+  if (tid == 0) {
+    float dd = 1.f;
+#pragma unroll
+    for (int q = 0; q < kGParts; ++q) dd *= dp[q];
+    a.gdec[(size_t)bh * a.G + g] = dd;
   }
 }
 
@@ -645,9 +769,25 @@ bool tc_f3a_supported(const FwdArgs& a) {
   return a.dk == 64 && a.dv == 64 && a.W >= 2 && a.W <= 16;
 }
 
+// the chain's group totals and decays: at most kMaxG groups
+constexpr int kMaxG = 16;
+static size_t f3a_records_bytes(int B, int T, int H) {
+  return 256 + (size_t)B * H * ((size_t)(T + kC - 1) / kC) * kF3aChunkWs;
+}
+
+// Groups of the chain: one, unless the chain CTAs of all (b, h) leave SMs
+// idle; then as many as two light CTAs per SM allow (at least 8 chunks each).
+static int f3a_groups(int BH, int NC) {
+  if (NC < 16) return 1;
+  return std::max(1, std::min({(2 * sm_count()) / (2 * BH), NC / 8, kMaxG}));
+}
+
+int tc_f3a_launches(const FwdArgs& a) {
+  return f3a_groups(a.B * a.H, (a.T + kC - 1) / kC) > 1 ? 3 : 2;
+}
+
 size_t tc_f3a_ws_bytes(int B, int T, int H) {
-  const size_t NC = (size_t)(T + kC - 1) / kC;
-  return 256 + (size_t)B * H * NC * kF3aChunkWs;
+  return f3a_records_bytes(B, T, H) + (size_t)B * H * kMaxG * (64 * 64 + 1) * 4;
 }
 
 int launch_tc_f3a(const FwdArgs& fa) {
@@ -686,15 +826,38 @@ int launch_tc_f3a(const FwdArgs& fa) {
     if (launch_overlapped(fa, k, grid, dim3(128), smem, mq, mk, mv, ta) != FALCON_OK) return FALCON_ERR_CUDA;
     record_event(fa, 1);
   }
-  {  // the chain and the outputs, two CTAs per (b, h) (32 value columns each)
-    auto k = f3a_chain_kernel;
+  // The chain and the outputs, two CTAs per (b, h) (32 value columns each).
+  // Long sequences with few heads leave SMs idle on one chain per (b, h):
+  // then the chunks split into G groups whose CTAs (lighter, two per SM) run
+  // side by side, each starting from the state that a pass over the earlier
+  // groups' totals gives it.
+  const int BH = fa.B * fa.H;
+  const int G = f3a_groups(BH, ta.NC);
+  ta.G = G;
+  ta.CPG = (ta.NC + G - 1) / G;
+  uint8_t* gbase = reinterpret_cast<uint8_t*>(fa.ws) + f3a_records_bytes(fa.B, fa.T, fa.H);
+  ta.gtot = reinterpret_cast<float*>(gbase);
+  ta.gdec = reinterpret_cast<float*>(gbase + (size_t)BH * kMaxG * 64 * 64 * 4);
+  if (G > 1) {
+    auto k = f3a_group_kernel;
+    const size_t smem = (kGParts * 64 * kGLd + kGParts) * 4;
+    if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
+    k<<<dim3(BH * (G - 1)), dim3(64 * kGParts), smem, fa.stream>>>(ta);
+    if (cudaGetLastError() != cudaSuccess) return FALCON_ERR_CUDA;
+    record_event(fa, 2);
+    auto kc = f3a_chain_kernel<F3aChainSmemG::NST, F3aChainSmemG::NB, 2>;
+    const size_t smc = F3aChainSmemG::TOTAL;
+    if (!set_smem_limit(reinterpret_cast<const void*>(kc), smc)) return FALCON_ERR_CUDA;
+    if (launch_overlapped(fa, kc, dim3(2 * BH * G), dim3(F3aChainSmemG::kThreads), smc, mq, ta) != FALCON_OK)
+      return FALCON_ERR_CUDA;
+  } else {
+    auto k = f3a_chain_kernel<F3aChainSmem::NST, F3aChainSmem::NB, 1>;
     const size_t smem = F3aChainSmem::TOTAL;
     if (!set_smem_limit(reinterpret_cast<const void*>(k), smem)) return FALCON_ERR_CUDA;
-    if (launch_overlapped(fa, k, dim3(2 * fa.B * fa.H), dim3(F3aChainSmem::kThreads), smem, mq, ta) !=
-        FALCON_OK)
+    if (launch_overlapped(fa, k, dim3(2 * BH), dim3(F3aChainSmem::kThreads), smem, mq, ta) != FALCON_OK)
       return FALCON_ERR_CUDA;
-    record_event(fa, 2);
   }
+  record_event(fa, G > 1 ? 3 : 2);
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
 

@@ -31,7 +31,7 @@ def test_f3a_tc_forced_matches_oracle(F, W):
     w = w_f3a(W)
     x = make_inputs(w, device="cuda")
     p = params_for(F, w, impl=F.FALCON_IMPL_TC)
-    assert F.falcon_chunk_fwd_plan(p) == (F.FALCON_IMPL_TC, 2)
+    assert F.falcon_chunk_fwd_plan(p) == (F.FALCON_IMPL_TC, 2)  # one chain group at this length
     o, co = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"])
     torch.cuda.synchronize()
     o_ref, c_ref = oracle_full(w, x)
@@ -88,6 +88,29 @@ def test_f3a_tc_clamped_runs(F):
     assert torch.isfinite(o.float()).all()
     assert rel_err(o.float().cpu().numpy(), o_ref) <= TOL["bf16"]
     assert rel_err(co["S"].cpu().numpy(), c_ref["S"]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("pairing", ["prefix", "same"])
+def test_f3a_tc_chain_in_groups(F, pairing):
+    """1 x 1650 x 3 heads (26 chunks, the last one ragged) with a carry: few
+    heads over many chunks, so the chain runs in groups (three here: 9, 9
+    and 8 chunks), each group starting from the state the earlier groups'
+    totals give it; every element against the oracle."""
+    w = Workload("tc_f3a_groups", FALCON_3A, 1, 1650, 3, 64, 64, chunk=64, window=8, seed=57,
+                 pairing=pairing)
+    x = make_inputs(w, device="cuda")
+    carry = make_carry(w, 59, torch.tensor([[0, 9, 300]]), device="cuda")
+    p = params_for(F, w)
+    assert F.falcon_chunk_fwd_plan(p) == (F.FALCON_IMPL_TC, 3)
+    o, co = F.chunk_forward(p, x["q"], x["k"], x["v"], x["beta"], x["lam"], carry)
+    torch.cuda.synchronize()
+    o_ref, c_ref = oracle_full(w, x, carry)
+    e_o = rel_err(o.float().cpu().numpy(), o_ref)
+    e_s = rel_err(co["S"].cpu().numpy(), c_ref["S"])
+    assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"], (e_o, e_s)
+    for n in ("k_prev", "win_x", "win_v"):
+        assert np.array_equal(co[n].cpu().double().numpy(), c_ref[n]), n
+    assert np.array_equal(co["pos"].cpu().numpy(), c_ref["pos"])
 
 
 def test_f3a_tc_full_size_sampled_heads(F):
