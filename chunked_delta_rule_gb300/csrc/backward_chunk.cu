@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tc_util.cuh"
 
 namespace falcon {
 
@@ -70,6 +71,8 @@ struct CbArgs {
   float* dS_in;
   void* dk_prev;
   float* ws;
+  uint32_t* status;   // the call's status word (a bounded wait that gave up)
+  uint64_t wait_ns;
 };
 
 __device__ __forceinline__ float* wsmat(const CbArgs& a, size_t cg, int which) {
@@ -354,6 +357,7 @@ __global__ void __launch_bounds__(kThr) bwdc_prep_kernel(CbArgs a) {
   float* M3 = Tm + kN * LDM;
   float* Wm = M3 + kN * LDM;
   GateSm& gs = *reinterpret_cast<GateSm*>(Wm + kN * LDM);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;  // each call starts with a clear status
   const size_t cg = blockIdx.x;
   const int c = (int)(cg % a.NC), bh = (int)(cg / a.NC), b = bh / a.H, h = bh % a.H, t0 = c * kN;
   const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
@@ -1037,6 +1041,497 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
     for (int cc = tid; cc < kN; cc += kThr) stx<Tin>(a.dk_prev, (size_t)bh * kN + cc, 0.f);
 }
 
+// ---------------------------------------------------------------- (d) on tcgen05
+// The gradient kernel for bf16 inputs, every 64 x 64 x 64 product a chain of
+// tcgen05 MMAs (kind::f16, M = N = 64, fp32 accumulators in TMEM).  An fp32
+// operand is split into bf16 hi = bf16(x) and lo = bf16(x - hi), 16
+// significant bits together, and a b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi
+// (the dropped terms are ~2^-16 of |a| |b|); keys, queries and output
+// gradients are exact in bf16 and take one image.  Each matrix sits in
+// shared memory once, as 64 rows of 64 bf16 with the 128-byte swizzle: the
+// same image is a K-major operand where its rows run along M (or N) and an
+// MN-major one where they run along K, so transposed products need no
+// transposed copy.  A thread owns one row and 16 columns of every 64 x 64
+// result (an M = 64 accumulator keeps row 16 q + l in TMEM lane 32 q + l),
+// so the element-wise work runs in registers and each result is written
+// back as images straight from them.
+namespace gtc {
+constexpr int kImg = 64 * 128;
+enum {
+  I_X = 0, I_Q, I_DO,           // exact inputs
+  I_S0, I_S0L, I_DS1, I_DS1L,   // start state, end-state gradient
+  I_W, I_WL,                    // W, then dDelta
+  I_T, I_TL, I_DL, I_DLL,       // T; Delta
+  I_PD, I_PDL,                  // P (.) D, then dR
+  I_DG, I_DGL, I_DP, I_DPL, kImgs
+};
+enum { A_0 = 0, A_XS0, A_QS0, A_QX, A_XDS1, A_G, A_DOS0, A_7, kAcc };  // 64 TMEM columns each
+enum { R_DGO = 0, R_EDE, R_DE, R_DGR, R_DEA, R_ROWM, R_SD, kRed };     // row sums, by column half
+struct Tail {
+  GateSm gs;
+  float red[kRed][2][kN];
+  float colM[4][kN];  // column sums of M by row quarter
+  uint64_t bar;
+  uint32_t tmem;
+  int pad;
+};
+constexpr size_t kSmem = 1024 + (size_t)kImgs * kImg + sizeof(Tail);
+static_assert(kAcc * 64 == 512, "the accumulators fill the TMEM of one CTA");
+
+// D (+)= op(A) op(B) over K = 64: the hi x hi term, then hi x lo and lo x hi
+// where that operand has a low part.  amn / bmn: the image's rows run along K.
+__device__ __forceinline__ void terms(uint32_t d, uint32_t ahi, uint32_t alo, bool asp, bool amn, uint32_t bhi,
+                                      uint32_t blo, bool bsp, bool bmn, bool accumulate) {
+  const uint32_t id = tc::idesc_bf16(64, 64, amn, bmn);
+  auto dsc = [](uint32_t s, bool mn, int ks) { return mn ? tcu::mndesc(s, ks) : tcu::kdesc<64>(s, ks); };
+  uint32_t on = accumulate ? 1u : 0u;
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks, on = 1u) tc::umma_bf16(d, dsc(ahi, amn, ks), dsc(bhi, bmn, ks), id, on);
+  if (bsp)
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) tc::umma_bf16(d, dsc(ahi, amn, ks), dsc(blo, bmn, ks), id, 1u);
+  if (asp)
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) tc::umma_bf16(d, dsc(alo, amn, ks), dsc(bhi, bmn, ks), id, 1u);
+}
+
+// 16 fp32 values of row r, columns c0 .. c0 + 15, into the hi and lo images
+__device__ __forceinline__ void put_split(uint8_t* hi, uint8_t* lo, int r, int c0, const float (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint32_t ph[4], pl[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = v[8 * j + 2 * e], x1 = v[8 * j + 2 * e + 1];
+      const __nv_bfloat162 hv = __floats2bfloat162_rn(x0, x1);
+      const float2 hf = __bfloat1622float2(hv);
+      const __nv_bfloat162 lv = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+      ph[e] = *reinterpret_cast<const uint32_t*>(&hv);
+      pl[e] = *reinterpret_cast<const uint32_t*>(&lv);
+    }
+    const uint32_t off = tcu::sw128(r, c0 + 8 * j);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+  }
+}
+// 16 values of an exact image's row r from column c0
+__device__ __forceinline__ void get_row(float (&v)[16], const uint8_t* im, int r, int c0) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint4 p = *reinterpret_cast<const uint4*>(im + tcu::sw128(r, c0 + 8 * j));
+    const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&p);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(e[q]);
+      v[8 * j + 2 * q] = f.x;
+      v[8 * j + 2 * q + 1] = f.y;
+    }
+  }
+}
+__device__ __forceinline__ void ld16(float (&v)[16], const float* p) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 f = reinterpret_cast<const float4*>(p)[k];
+    v[4 * k] = f.x; v[4 * k + 1] = f.y; v[4 * k + 2] = f.z; v[4 * k + 3] = f.w;
+  }
+}
+}  // namespace gtc
+
+__global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
+  using namespace gtc;
+  extern __shared__ uint8_t gtc_raw[];
+  uint8_t* base = tcu::align1024(gtc_raw);
+  auto img = [&](int i) { return base + (size_t)i * kImg; };
+  auto sa = [&](int i) { return tc::smem_u32(base + (size_t)i * kImg); };
+  Tail& tl = *reinterpret_cast<Tail*>(base + (size_t)kImgs * kImg);
+  GateSm& gs = tl.gs;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int R = 16 * quad + (lane & 15), C0 = 32 * half + 16 * (lane >> 4);  // this thread's row and columns
+  const size_t cg = blockIdx.x;
+  const int c = (int)(cg % a.NC), bh = (int)(cg / a.NC), b = bh / a.H, h = bh % a.H, t0 = c * kN;
+  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+  const bool reg = !a.additive;
+  const int t = t0 + R;
+  using Tin = __nv_bfloat16;
+
+  if (warp == 0) {
+    tc::tmem_alloc(&tl.tmem, 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 32) {
+    tc::mbar_init(&tl.bar, 1);
+    tc::fence_mbar_init();
+  }
+  // row sums: the two threads of a row in this warp, then one entry per column half
+  auto row_part = [&](int which, float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    if (lane < 16) tl.red[which][half][R] = v;
+  };
+  auto row_sum = [&](int which, int r) { return tl.red[which][0][r] + tl.red[which][1][r]; };
+
+  // ---- loads: gates; keys, queries, output gradients as images; S0, dS1, W
+  if (tid < (int)(sizeof(GateSm) / 16)) cp16(reinterpret_cast<float*>(&gs) + 4 * tid, wsgate(a, cg) + 4 * tid);
+  cp_commit();
+  {
+    uint4 px[2], pq[2], pd[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = tid + kThr * k, r = i >> 3, ch = i & 7, tr = t0 + r;
+      const Tin* row = nullptr;
+      if (tr < a.T && pos + tr >= a.shift) {
+        if (tr - a.shift >= 0) row = reinterpret_cast<const Tin*>(a.k) + (((size_t)b * a.T + (tr - a.shift)) * a.H + h) * kN;
+        else if (a.kprev_in) row = reinterpret_cast<const Tin*>(a.kprev_in) + (size_t)bh * kN;
+      }
+      const size_t gi = (((size_t)b * a.T + tr) * a.H + h) * kN + 8 * ch;
+      px[k] = row ? *reinterpret_cast<const uint4*>(row + 8 * ch) : make_uint4(0u, 0u, 0u, 0u);
+      pq[k] = tr < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(a.q) + gi) : make_uint4(0u, 0u, 0u, 0u);
+      pd[k] = tr < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(a.dO) + gi) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = tid + kThr * k, r = i >> 3, ch = i & 7;
+      const uint32_t off = (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
+      *reinterpret_cast<uint4*>(img(I_X) + off) = px[k];
+      *reinterpret_cast<uint4*>(img(I_Q) + off) = pq[k];
+      *reinterpret_cast<uint4*>(img(I_DO) + off) = pd[k];
+    }
+  }
+  {
+    float s0[16], ds[16];
+    ld16(s0, wsmat(a, cg, M_S0) + R * kN + C0);
+    ld16(ds, wsmat(a, cg, M_DS1) + R * kN + C0);
+    put_split(img(I_S0), img(I_S0L), R, C0, s0);
+    put_split(img(I_DS1), img(I_DS1L), R, C0, ds);
+    float sd = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sd = fmaf(s0[e], ds[e], sd);
+    row_part(R_SD, sd);
+    if (reg) {
+      float w[16];
+      ld16(w, wsmat(a, cg, M_W) + R * kN + C0);
+      put_split(img(I_W), img(I_WL), R, C0, w);
+    }
+  }
+  cp_wait0();
+  tc::fence_proxy_async();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tl.tmem;
+  const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+  auto acc = [&](int s) { return tmem + (uint32_t)(64 * s); };
+  auto tld = [&](int s, float (&v)[16]) {
+    uint32_t r[16];
+    tc::tmem_ld16x2_16(tmem + lane_off + (uint32_t)(64 * s + 32 * half), r);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+  };
+  uint32_t phase = 0;
+  bool ok = true;
+  // every thread waits for the step's MMAs; all agree on the outcome
+  auto wait_step = [&]() {
+    const bool mine = tc::mbar_wait(&tl.bar, phase, a.wait_ns);
+    phase ^= 1u;
+    tc::tc_fence_after();
+    ok = !__syncthreads_or(!mine);
+    return ok;
+  };
+  // the images written since the last step are visible to the MMAs, and
+  // every accumulator read so far is done
+  auto step_barrier = [&]() {
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+  };
+  const float etaR = gs.eta[R], GamR = gs.Gam[R], ER = gs.E[R], gR = gs.g[R];
+
+  do {
+    // ---- step 1: W S0, X S0, Q S0, Q X^T, X dS1, X X^T, dO S0^T
+    if (tid == 0) {
+      if (reg) {
+        terms(acc(A_0), sa(I_W), sa(I_WL), true, false, sa(I_S0), sa(I_S0L), true, true, false);
+        terms(acc(A_XS0), sa(I_X), 0, false, false, sa(I_S0), sa(I_S0L), true, true, false);
+        terms(acc(A_G), sa(I_X), 0, false, false, sa(I_X), 0, false, false, false);
+      }
+      terms(acc(A_QS0), sa(I_Q), 0, false, false, sa(I_S0), sa(I_S0L), true, true, false);
+      terms(acc(A_QX), sa(I_Q), 0, false, false, sa(I_X), 0, false, false, false);
+      terms(acc(A_XDS1), sa(I_X), 0, false, false, sa(I_DS1), sa(I_DS1L), true, true, false);
+      terms(acc(A_DOS0), sa(I_DO), 0, false, false, sa(I_S0), sa(I_S0L), true, false, false);
+      tc::umma_commit(&tl.bar);
+    }
+    // meanwhile: T as images, this thread's U and V
+    float u[16], vv[16];
+    if (reg) {
+      float tt[16];
+      ld16(tt, wsmat(a, cg, M_T) + R * kN + C0);
+      put_split(img(I_T), img(I_TL), R, C0, tt);
+      ld16(u, wsmat(a, cg, M_U) + R * kN + C0);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint4 p = t < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(a.v) +
+                                                              (((size_t)b * a.T + t) * a.H + h) * kN + C0 + 8 * j)
+                              : make_uint4(0u, 0u, 0u, 0u);
+      const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&p);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(e2[q]);
+        vv[8 * j + 2 * q] = f.x;
+        vv[8 * j + 2 * q + 1] = f.y;
+      }
+    }
+    if (!wait_step()) break;
+
+    // ---- E1: Delta; dGamma through the output term; P (.) D; E dE
+    float dl[16], pv[16];
+    if (reg) {
+      tld(A_0, pv);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) dl[e] = u[e] - pv[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) dl[e] = etaR * vv[e];
+    }
+    put_split(img(I_DL), img(I_DLL), R, C0, dl);
+    {
+      float dov[16], s = 0.f;
+      get_row(dov, img(I_DO), R, C0);
+      tld(A_QS0, pv);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s = fmaf(dov[e], pv[e], s);
+      row_part(R_DGO, s);
+    }
+    {
+      float pd[16];
+      tld(A_QX, pv);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int cc = C0 + e;
+        pd[e] = cc <= R ? __expf(gR - gs.g[cc]) * pv[e] : 0.f;
+      }
+      put_split(img(I_PD), img(I_PDL), R, C0, pd);
+    }
+    {
+      float s = 0.f;
+      tld(A_XDS1, pv);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s = fmaf(pv[e], dl[e], s);
+      row_part(R_EDE, s);
+    }
+    step_barrier();
+
+    // ---- step 2: (P (.) D)^T dO
+    if (tid == 0) {
+      terms(acc(A_7), sa(I_PD), sa(I_PDL), true, true, sa(I_DO), 0, false, true, false);
+      tc::umma_commit(&tl.bar);
+    }
+    if (!wait_step()) break;
+    // ---- E2: dDelta = (P (.) D)^T dO + diag(E) X dS1
+    float dd[16];
+    {
+      float p2[16];
+      tld(A_7, pv);
+      tld(A_XDS1, p2);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) dd[e] = pv[e] + ER * p2[e];
+    }
+    if (reg) {
+      put_split(img(I_W), img(I_WL), R, C0, dd);
+      step_barrier();
+      // ---- step 3: dR = T^T dDelta
+      if (tid == 0) {
+        terms(acc(A_0), sa(I_T), sa(I_TL), true, true, sa(I_W), sa(I_WL), true, true, false);
+        tc::umma_commit(&tl.bar);
+      }
+      if (!wait_step()) break;
+      tld(A_0, dd);
+    }
+    // ---- E3 (dd holds dR): dV, d eta and dGamma through the residual
+    if (t < a.T) {
+      float v8[8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v8[e] = etaR * dd[8 * j + e];
+        stx8<Tin>(a.dv, (((size_t)b * a.T + t) * a.H + h) * kN + C0 + 8 * j, v8);
+      }
+    }
+    {
+      float de = 0.f, dgr = 0.f;
+      if (reg) {
+        tld(A_XS0, pv);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          de = fmaf(dd[e], vv[e] - GamR * pv[e], de);
+          dgr = fmaf(dd[e], pv[e], dgr);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) de = fmaf(dd[e], vv[e], de);
+      }
+      row_part(R_DE, de);
+      row_part(R_DGR, dgr);
+    }
+    put_split(img(I_PD), img(I_PDL), R, C0, dd);  // dR
+    step_barrier();
+
+    // ---- step 4: dR Delta^T, dO Delta^T, dR S0^T
+    if (tid == 0) {
+      if (reg) {
+        terms(acc(A_0), sa(I_PD), sa(I_PDL), true, false, sa(I_DL), sa(I_DLL), true, false, false);
+        terms(acc(A_XDS1), sa(I_PD), sa(I_PDL), true, false, sa(I_S0), sa(I_S0L), true, false, false);
+      }
+      terms(acc(A_QS0), sa(I_DO), 0, false, false, sa(I_DL), sa(I_DLL), true, false, false);
+      tc::umma_commit(&tl.bar);
+    }
+    if (!wait_step()) break;
+    // ---- E4: dG (A = diag(eta) L), M = D (.) dD, dP
+    {
+      float dod[16], qx[16], dra[16], gg[16], m[16], dp[16], dg[16];
+      tld(A_QS0, dod);
+      tld(A_QX, qx);
+      if (reg) {
+        tld(A_0, dra);
+        tld(A_G, gg);
+      }
+      float dea = 0.f, rm = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int cc = C0 + e;
+        const float D = cc <= R ? __expf(gR - gs.g[cc]) : 0.f;
+        float me = dod[e] * D * qx[e];  // (dO Delta^T) (.) (P (.) D)
+        dp[e] = D * dod[e];
+        dg[e] = 0.f;
+        if (reg && cc < R) {
+          const float dA = -dra[e];
+          dea = fmaf(dA * D, gg[e], dea);  // d eta through A = diag(eta) L
+          const float dL = etaR * dA;
+          dg[e] = dL * D;
+          me = fmaf(D * dL, gg[e], me);
+        }
+        m[e] = me;
+        rm += me;
+      }
+      row_part(R_DEA, dea);
+      row_part(R_ROWM, rm);
+      // column sums over this quadrant's 16 rows: a reduce-scatter over the
+      // half-warp leaves lane l the sum of column C0 + (l & 15)
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+          const float send = up ? m[i] : m[i + o];
+          const float keep = up ? m[i + o] : m[i];
+          m[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      tl.colM[quad][C0 + (lane & 15)] = m[0];
+      if (reg) put_split(img(I_DG), img(I_DGL), R, C0, dg);
+      put_split(img(I_DP), img(I_DPL), R, C0, dp);
+    }
+    step_barrier();
+
+    // ---- step 5: dX = (dG + dG^T) X + dP^T Q (- and + terms below); dP X; Delta dS1^T
+    if (tid == 0) {
+      terms(acc(A_7), sa(I_DP), sa(I_DPL), true, true, sa(I_Q), 0, false, true, false);
+      if (reg) {
+        terms(acc(A_7), sa(I_DG), sa(I_DGL), true, false, sa(I_X), 0, false, true, true);
+        terms(acc(A_7), sa(I_DG), sa(I_DGL), true, true, sa(I_X), 0, false, true, true);
+      }
+      terms(acc(A_QX), sa(I_DP), sa(I_DPL), true, false, sa(I_X), 0, false, true, false);
+      terms(acc(A_G), sa(I_DL), sa(I_DLL), true, false, sa(I_DS1), sa(I_DS1L), true, false, false);
+      tc::umma_commit(&tl.bar);
+    }
+    if (!wait_step()) break;
+    // ---- E5: dq, dk (the TMEM loads are warp-wide: every lane takes them,
+    // only the stores are limited to the call's rows)
+    {
+      float p1[16], p2[16];
+      tld(A_DOS0, p1);
+      tld(A_QX, p2);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) p1[e] = GamR * p1[e] + p2[e];
+      if (t < a.T) {
+        stx8<Tin>(a.dq, (((size_t)b * a.T + t) * a.H + h) * kN + C0, *reinterpret_cast<float(*)[8]>(&p1[0]));
+        stx8<Tin>(a.dq, (((size_t)b * a.T + t) * a.H + h) * kN + C0 + 8, *reinterpret_cast<float(*)[8]>(&p1[8]));
+      }
+    }
+    {
+      const float deta = row_sum(R_DE, R) + row_sum(R_DEA, R);
+      const float dn = gs.ex[R] != 0.f ? -deta * etaR / (a.eps + gs.nrm[R]) : 0.f;
+      float xr[16], p3[16], p4[16], p5[16];
+      get_row(xr, img(I_X), R, C0);
+      tld(A_7, p3);
+      tld(A_G, p4);
+      if (reg) tld(A_XDS1, p5);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float x = p3[e] + ER * p4[e] + 2.f * dn * xr[e];
+        if (reg) x -= etaR * GamR * p5[e];
+        p3[e] = x;
+      }
+      if (t < a.T) {
+        Tin* dst = nullptr;
+        if (t - a.shift >= 0) dst = reinterpret_cast<Tin*>(a.dk) + (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN;
+        else if (a.dk_prev) dst = reinterpret_cast<Tin*>(a.dk_prev) + (size_t)bh * kN;
+        if (dst) {
+          stx8<Tin>(dst, C0, *reinterpret_cast<float(*)[8]>(&p3[0]));
+          stx8<Tin>(dst, C0 + 8, *reinterpret_cast<float(*)[8]>(&p3[8]));
+        }
+      }
+    }
+    if (tid < 32) {  // gate gradients: dg_r, then the reverse cumulative sum over the chunk
+      float sdS = row_sum(R_SD, tid) + row_sum(R_SD, tid + 32);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sdS += __shfl_xor_sync(0xffffffffu, sdS, o);
+      float ede[2];
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) ede[hlf] = gs.E[tid + 32 * hlf] * row_sum(R_EDE, tid + 32 * hlf);
+      float sE = ede[0] + ede[1];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sE += __shfl_xor_sync(0xffffffffu, sE, o);
+      float d[2];
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int r = tid + 32 * hlf;
+        const float dGr = reg ? -gs.eta[r] * row_sum(R_DGR, r) : 0.f;
+        const float colM = tl.colM[0][r] + tl.colM[1][r] + tl.colM[2][r] + tl.colM[3][r];
+        const float dG = row_sum(R_DGO, r) + dGr + (r == kN - 1 ? sdS : 0.f);
+        d[hlf] = gs.Gam[r] * dG + row_sum(R_ROWM, r) - colM - ede[hlf] + (r == kN - 1 ? sE : 0.f);
+      }
+      float v1 = d[1], v0 = d[0];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float n1 = __shfl_down_sync(0xffffffffu, v1, o), n0 = __shfl_down_sync(0xffffffffu, v0, o);
+        if (tid + o < 32) { v1 += n1; v0 += n0; }
+      }
+      v0 += __shfl_sync(0xffffffffu, v1, 0);
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int r = tid + 32 * hlf, tr = t0 + r;
+        if (tr >= a.T) continue;
+        const size_t gi = ((size_t)b * a.T + tr) * a.H + h;
+        const float dl_ = hlf ? v1 : v0;
+        const float om = 1.f - a.lam[gi];
+        a.dlam[gi] = (om >= a.eps_gamma && om <= 1.f) ? -dl_ / gs.gam[r] : 0.f;
+        a.dbeta[gi] = gs.ex[r] != 0.f ? (row_sum(R_DE, r) + row_sum(R_DEA, r)) / (a.eps + gs.nrm[r]) : 0.f;
+      }
+    }
+    if (a.shift == 1 && c == a.NC - 1)  // the last key is the x of no pair of this call
+      for (int cc = tid; cc < kN; cc += kThr) stx<Tin>(a.dk, (((size_t)b * a.T + (a.T - 1)) * a.H + h) * kN + cc, 0.f);
+    if (c == 0 && a.dk_prev && a.shift == 0)
+      for (int cc = tid; cc < kN; cc += kThr) stx<Tin>(a.dk_prev, (size_t)bh * kN + cc, 0.f);
+  } while (false);
+  if (!ok && tid == 0) atomicExch(a.status, tcu::kStatusTimeout);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tl.tmem, 512);
+}
+
 constexpr size_t prep_smem() { return 8 * kN * LDM * sizeof(float) + sizeof(GateSm) + 4 * kN * sizeof(float); }
 constexpr size_t grad_smem() { return 12 * kN * LDM * sizeof(float) + sizeof(GateSm) + 8 * kN * sizeof(float); }
 
@@ -1055,9 +1550,9 @@ template <typename Tin>
 int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
   const unsigned nch = (unsigned)(a.B * a.H * a.NC);
   auto prep = bwdc_prep_kernel<Tin>;
-  auto grad = bwdc_grad_kernel<Tin>;
+  auto grad = bwdc_grad_kernel<float>;
   if (!set_smem_limit(reinterpret_cast<const void*>(prep), prep_smem())) return FALCON_ERR_CUDA;
-  if (!set_smem_limit(reinterpret_cast<const void*>(grad), grad_smem())) return FALCON_ERR_CUDA;
+  if (sizeof(Tin) == 4 && !set_smem_limit(reinterpret_cast<const void*>(grad), grad_smem())) return FALCON_ERR_CUDA;
   prep<<<nch, kThr, prep_smem(), s>>>(a);
   // 16-column chain slices when their CTAs fit one wave at two per SM, else 32
   int dev = 0, sms = 0;
@@ -1066,7 +1561,12 @@ int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
     return FALCON_ERR_CUDA;
   const int st = (long)a.B * a.H * (kN / 16) <= 2L * sms ? launch_chains<16>(a, s) : launch_chains<32>(a, s);
   if (st != FALCON_OK) return st;
-  grad<<<nch, kThr, grad_smem(), s>>>(a);
+  if constexpr (sizeof(Tin) == 2) {  // bf16 inputs: the tensor-core gradient kernel
+    if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_grad_tc_kernel), gtc::kSmem)) return FALCON_ERR_CUDA;
+    bwdc_grad_tc_kernel<<<nch, kThr, gtc::kSmem, s>>>(a);
+  } else {
+    grad<<<nch, kThr, grad_smem(), s>>>(a);
+  }
   return cudaGetLastError() == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA;
 }
 
@@ -1076,9 +1576,10 @@ bool backward_chunk_supported(int variant, int dk, int dv, int T) {
   return (variant == FALCON_1 || variant == FALCON_1A) && dk == 64 && dv == 64 && T >= 1;
 }
 
+// a 256-byte block with the status word, then per chunk the matrices, then the gate rows
 size_t backward_chunk_ws_bytes(int B, int T, int H) {
   const size_t NC = (size_t)(T + kN - 1) / kN;
-  return (size_t)B * H * NC * (kMats * kMat + kGateVecs * kN) * sizeof(float);
+  return 256 + (size_t)B * H * NC * (kMats * kMat + kGateVecs * kN) * sizeof(float);
 }
 
 int launch_backward_chunk(const FwdArgs& f, const void* dO, const float* dS_final, void* dq, void* dk, void* dv,
@@ -1090,7 +1591,9 @@ int launch_backward_chunk(const FwdArgs& f, const void* dO, const float* dS_fina
   a.q = f.q; a.k = f.k; a.v = f.v; a.dO = dO; a.beta = f.beta; a.lam = f.lam;
   a.S_in = f.S_in; a.kprev_in = f.kprev_in; a.pos_in = f.pos_in; a.dS_final = dS_final;
   a.dq = dq; a.dk = dk; a.dv = dv; a.dbeta = dbeta; a.dlam = dlam; a.dS_in = dS_in; a.dk_prev = dk_prev;
-  a.ws = reinterpret_cast<float*>(f.ws);
+  a.status = reinterpret_cast<uint32_t*>(f.ws);
+  a.ws = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(f.ws) + 256);
+  a.wait_ns = wait_limit_ns();
   return f.dtype == FALCON_BF16 ? launch_bwdc_t<__nv_bfloat16>(a, f.stream) : launch_bwdc_t<float>(a, f.stream);
 }
 

@@ -319,7 +319,10 @@ size_t falcon_backward_workspace_size(const falcon_params_t* p);
  * are ignored).  Falcon-1/1A at d = 64 run a chunked kernel, Falcon-3/3A
  * and d = 128 a step-by-step kernel that carries the window's key and value
  * gradients in a ring, the rest a step-by-step one-pair kernel.  Gradients
- * must not overlap inputs or one another.
+ * must not overlap inputs or one another.  The chunked kernel with bf16
+ * inputs runs its products on the tensor cores with bounded waits: a wait
+ * that runs out is recorded in the workspace's status word and read with
+ * falcon_workspace_status, as for the chunk forward.
  * Errors: FALCON_ERR_INVALID_ARG, FALCON_ERR_UNSUPPORTED (other dims, the
  * prologue, a window past the limit), FALCON_ERR_WORKSPACE, FALCON_ERR_CUDA. */
 int falcon_backward_carry(const falcon_params_t* p, const void* q, const void* k, const void* v,
@@ -351,16 +354,17 @@ int falcon_backward(const falcon_params_t* p, const void* q, const void* k, cons
  * The function synchronises `stream` (the call's stream), reads the word
  * and clears it.  Returns FALCON_OK, FALCON_ERR_TIMEOUT (the outputs and
  * carry of that call are incomplete), FALCON_ERR_WORKSPACE (workspace not
- * 256-byte aligned) or FALCON_ERR_CUDA.  Other kernel families have no
- * device-side waits and do not write the word. */
+ * 256-byte aligned) or FALCON_ERR_CUDA.  The chunked backward (Falcon-1 /
+ * 1A, d = 64) keeps its word in the same place.  Other kernel families have
+ * no device-side waits and do not write the word. */
 int falcon_workspace_status(const void* workspace, void* stream);
 
 /* Test hook of the failure-detection path (no counterpart on the pages; not
  * for production use).  wait_limit_ns > 0 sets the limit of the bounded
  * device-side waits of the Falcon-1 / 1A, 3 and 3A tensor-core kernels
- * launched from now on in this process (0 restores 2 s; the Falcon-2 kernel
- * keeps 2 s).  stall != 0 makes the next such
- * call's per-chunk kernel wait once, before it loads anything, on a barrier
+ * and of the chunked backward launched from now on in this process (0
+ * restores 2 s; the Falcon-2 kernel keeps 2 s).  stall != 0 makes the next
+ * forward call's per-chunk kernel wait once, before it loads anything, on a barrier
  * that nothing completes: that wait runs out after the limit, the timeout is
  * recorded as described at falcon_workspace_status and the call's later
  * kernels skip their work.  No fault, trap or unbounded wait is involved;

@@ -27,12 +27,16 @@ def F():
 
 @pytest.mark.parametrize("w", [LM_F1.with_(B=1, T=300, H=2), LONG_F1.with_(B=1, T=200, H=2,
                                                                              force_zero_gamma=0.0),
-                               WINDOW_F3.with_(B=1, T=300, H=2), WINDOW_F3A.with_(B=1, T=300, H=2)],
-                         ids=["d64", "d128", "falcon3", "falcon3a"])
+                               WINDOW_F3.with_(B=1, T=300, H=2), WINDOW_F3A.with_(B=1, T=300, H=2),
+                               WINDOW_F3A.with_(B=1, T=1650, H=2)],
+                         ids=["d64", "d128", "falcon3", "falcon3a", "falcon3a_groups"])
 def test_stalled_wait_is_reported_and_the_context_survives(F, w):
     x = make_inputs(w, device="cuda")
     p = params_for(F, w)
-    assert F.falcon_chunk_fwd_plan(p)[0] == F.FALCON_IMPL_TC
+    impl, launches = F.falcon_chunk_fwd_plan(p)
+    assert impl == F.FALCON_IMPL_TC
+    if w.T == 1650:
+        assert launches == 3   # Falcon-3A's chain in groups: the group-total kernel runs between
     n = F.falcon_workspace_size(p)
     ws = F.alloc_workspace(n)
     ws.fill_(0xFF)   # garbage in the status word: each call clears it when it starts
