@@ -1135,6 +1135,57 @@ __device__ __forceinline__ void ld16(float (&v)[16], const float* p) {
     v[4 * k] = f.x; v[4 * k + 1] = f.y; v[4 * k + 2] = f.z; v[4 * k + 3] = f.w;
   }
 }
+// keys (with the pairing's shift and the carried key), queries and output
+// gradients of the chunk as exact bf16 images
+__device__ __forceinline__ void load_xqdo(const CbArgs& a, uint8_t* ix, uint8_t* iq, uint8_t* ido, int b, int h,
+                                          int t0, int64_t pos, int bh) {
+  using Tin = __nv_bfloat16;
+  uint4 px[2], pq[2], pd[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i >> 3, ch = i & 7, tr = t0 + r;
+    const Tin* row = nullptr;
+    if (tr < a.T && pos + tr >= a.shift) {
+      if (tr - a.shift >= 0) row = reinterpret_cast<const Tin*>(a.k) + (((size_t)b * a.T + (tr - a.shift)) * a.H + h) * kN;
+      else if (a.kprev_in) row = reinterpret_cast<const Tin*>(a.kprev_in) + (size_t)bh * kN;
+    }
+    const size_t gi = (((size_t)b * a.T + tr) * a.H + h) * kN + 8 * ch;
+    px[k] = row ? *reinterpret_cast<const uint4*>(row + 8 * ch) : make_uint4(0u, 0u, 0u, 0u);
+    pq[k] = tr < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(a.q) + gi) : make_uint4(0u, 0u, 0u, 0u);
+    pd[k] = tr < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(a.dO) + gi) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i >> 3, ch = i & 7;
+    const uint32_t off = (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
+    *reinterpret_cast<uint4*>(ix + off) = px[k];
+    *reinterpret_cast<uint4*>(iq + off) = pq[k];
+    *reinterpret_cast<uint4*>(ido + off) = pd[k];
+  }
+}
+// 16 values of row t of a [B, T, H, 64] bf16 tensor from column c0 (zero past T)
+__device__ __forceinline__ void load_row16(float (&v)[16], const void* src, const CbArgs& a, int b, int h, int t,
+                                           int c0) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint4 p = t < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(src) +
+                                                            (((size_t)b * a.T + t) * a.H + h) * kN + c0 + 8 * j)
+                            : make_uint4(0u, 0u, 0u, 0u);
+    const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&p);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(e2[q]);
+      v[8 * j + 2 * q] = f.x;
+      v[8 * j + 2 * q + 1] = f.y;
+    }
+  }
+}
+__device__ __forceinline__ void st16(float* p, const float (&v)[16]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    reinterpret_cast<float4*>(p)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
+
 }  // namespace gtc
 
 __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
@@ -1173,30 +1224,7 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
   // ---- loads: gates; keys, queries, output gradients as images; S0, dS1, W
   if (tid < (int)(sizeof(GateSm) / 16)) cp16(reinterpret_cast<float*>(&gs) + 4 * tid, wsgate(a, cg) + 4 * tid);
   cp_commit();
-  {
-    uint4 px[2], pq[2], pd[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = tid + kThr * k, r = i >> 3, ch = i & 7, tr = t0 + r;
-      const Tin* row = nullptr;
-      if (tr < a.T && pos + tr >= a.shift) {
-        if (tr - a.shift >= 0) row = reinterpret_cast<const Tin*>(a.k) + (((size_t)b * a.T + (tr - a.shift)) * a.H + h) * kN;
-        else if (a.kprev_in) row = reinterpret_cast<const Tin*>(a.kprev_in) + (size_t)bh * kN;
-      }
-      const size_t gi = (((size_t)b * a.T + tr) * a.H + h) * kN + 8 * ch;
-      px[k] = row ? *reinterpret_cast<const uint4*>(row + 8 * ch) : make_uint4(0u, 0u, 0u, 0u);
-      pq[k] = tr < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(a.q) + gi) : make_uint4(0u, 0u, 0u, 0u);
-      pd[k] = tr < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(a.dO) + gi) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = tid + kThr * k, r = i >> 3, ch = i & 7;
-      const uint32_t off = (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
-      *reinterpret_cast<uint4*>(img(I_X) + off) = px[k];
-      *reinterpret_cast<uint4*>(img(I_Q) + off) = pq[k];
-      *reinterpret_cast<uint4*>(img(I_DO) + off) = pd[k];
-    }
-  }
+  load_xqdo(a, img(I_X), img(I_Q), img(I_DO), b, h, t0, pos, bh);
   {
     float s0[16], ds[16];
     ld16(s0, wsmat(a, cg, M_S0) + R * kN + C0);
@@ -1270,19 +1298,7 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
       put_split(img(I_T), img(I_TL), R, C0, tt);
       ld16(u, wsmat(a, cg, M_U) + R * kN + C0);
     }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint4 p = t < a.T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(a.v) +
-                                                              (((size_t)b * a.T + t) * a.H + h) * kN + C0 + 8 * j)
-                              : make_uint4(0u, 0u, 0u, 0u);
-      const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&p);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(e2[q]);
-        vv[8 * j + 2 * q] = f.x;
-        vv[8 * j + 2 * q + 1] = f.y;
-      }
-    }
+    load_row16(vv, a.v, a, b, h, t, C0);
     if (!wait_step()) break;
 
     // ---- E1: Delta; dGamma through the output term; P (.) D; E dE
@@ -1532,6 +1548,276 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
   if (warp == 0) tc::tmem_dealloc(tl.tmem, 512);
 }
 
+// ---------------------------------------------------------------- (a) on tcgen05
+// The per-chunk preparation for bf16 inputs with its products on the tensor
+// cores, in the images and thread layout of the gradient kernel above:
+// A = diag(eta) (D (.) X X^T) and P (.) D from one step of MMAs; T = (I +
+// A)^{-1} by forward substitution (a column per thread, as before); then
+// W = T diag(eta Gamma) X, U = T diag(eta) V, Q^T diag(Gamma) dO and
+// Z = (P (.) D)^T dO in one step, and W^T Z in a last one.  Thirteen images
+// and 256 TMEM columns: two CTAs share an SM.
+namespace ptc {
+enum {
+  I_X = 0, I_Q, I_DO,
+  I_PD, I_PDL,      // P (.) D
+  I_M3, I_M3L,      // diag(Gamma) dO
+  I_M1, I_M1L,      // diag(eta) V, then W
+  I_MX, I_MXL,      // diag(eta Gamma) X, then Z
+  I_T, I_TL,        // A as fp32 rows, then T
+  kImgs
+};
+struct Tail {
+  GateSm gs;
+  float red[2][kN];
+  uint64_t bar;
+  uint32_t tmem;
+  int pad;
+};
+constexpr size_t kSmem = 1024 + (size_t)kImgs * gtc::kImg + sizeof(Tail);
+static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
+}  // namespace ptc
+
+__global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
+  using namespace ptc;
+  extern __shared__ uint8_t ptc_raw[];
+  uint8_t* base = tcu::align1024(ptc_raw);
+  auto img = [&](int i) { return base + (size_t)i * gtc::kImg; };
+  auto sa = [&](int i) { return tc::smem_u32(base + (size_t)i * gtc::kImg); };
+  Tail& tl = *reinterpret_cast<Tail*>(base + (size_t)kImgs * gtc::kImg);
+  GateSm& gs = tl.gs;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int R = 16 * quad + (lane & 15), C0 = 32 * half + 16 * (lane >> 4);
+  const size_t cg = blockIdx.x;
+  const int c = (int)(cg % a.NC), bh = (int)(cg / a.NC), b = bh / a.H, h = bh % a.H, t0 = c * kN;
+  const int64_t pos = a.pos_in ? a.pos_in[bh] : 0;
+  const bool reg = !a.additive;
+  if (blockIdx.x == 0 && tid == 0) *a.status = 0u;  // each call starts with a clear status
+
+  if (warp == 0) {
+    tc::tmem_alloc(&tl.tmem, 256);
+    tc::tmem_relinquish();
+  }
+  if (tid == 32) {
+    tc::mbar_init(&tl.bar, 1);
+    tc::fence_mbar_init();
+  }
+  gtc::load_xqdo(a, img(I_X), img(I_Q), img(I_DO), b, h, t0, pos, bh);
+  float vv[16];
+  gtc::load_row16(vv, a.v, a, b, h, t0 + R, C0);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tl.tmem;
+  const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+  auto acc = [&](int s) { return tmem + (uint32_t)(64 * s); };
+  auto tld = [&](int s, float (&v)[16]) {
+    uint32_t r[16];
+    tc::tmem_ld16x2_16(tmem + lane_off + (uint32_t)(64 * s + 32 * half), r);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+  };
+  // gates: |x_r|^2 from this thread's 16 columns, summed over the row's four threads
+  float xr[16];
+  gtc::get_row(xr, img(I_X), R, C0);
+  {
+    float n = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) n = fmaf(xr[e], xr[e], n);
+    n += __shfl_xor_sync(0xffffffffu, n, 16);
+    if (lane < 16) tl.red[half][R] = n;
+  }
+  __syncthreads();
+  if (tid < kN) {
+    const int r = tid, t = t0 + r;
+    const float n = tl.red[0][r] + tl.red[1][r];
+    const bool live = t < a.T, ex = live && pos + t >= a.shift;
+    const size_t gi = ((size_t)b * a.T + (live ? t : 0)) * a.H + h;
+    gs.nrm[r] = n;
+    gs.ex[r] = ex ? 1.f : 0.f;
+    gs.eta[r] = ex ? a.beta[gi] / (a.eps + n) : 0.f;
+    const float gm = live ? fminf(fmaxf(1.f - a.lam[gi], a.eps_gamma), 1.f) : 1.f;
+    gs.gam[r] = gm;
+    gs.g[r] = live ? logf(gm) : 0.f;
+  }
+  __syncthreads();
+  if (tid < 32) {  // inclusive prefix sum over the 64 rows
+    float v0 = gs.g[tid], v1 = gs.g[tid + 32];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n0 = __shfl_up_sync(0xffffffffu, v0, o), n1 = __shfl_up_sync(0xffffffffu, v1, o);
+      if (tid >= o) { v0 += n0; v1 += n1; }
+    }
+    v1 += __shfl_sync(0xffffffffu, v0, 31);
+    gs.g[tid] = v0;
+    gs.g[tid + 32] = v1;
+  }
+  __syncthreads();
+  if (tid < kN) {
+    gs.Gam[tid] = __expf(gs.g[tid]);
+    gs.E[tid] = __expf(gs.g[kN - 1] - gs.g[tid]);
+  }
+  __syncthreads();
+  const float etaR = gs.eta[R], GamR = gs.Gam[R], ER = gs.E[R], gR = gs.g[R];
+  uint32_t phase = 0;
+  bool ok = true;
+  auto wait_step = [&]() {
+    const bool mine = tc::mbar_wait(&tl.bar, phase, a.wait_ns);
+    phase ^= 1u;
+    tc::tc_fence_after();
+    ok = !__syncthreads_or(!mine);
+    return ok;
+  };
+  auto step_barrier = [&]() {
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+  };
+
+  do {
+    // ---- step 1: X X^T, P = Q X^T
+    if (tid == 0) {
+      if (reg) gtc::terms(acc(0), sa(I_X), 0, false, false, sa(I_X), 0, false, false, false);
+      gtc::terms(acc(1), sa(I_Q), 0, false, false, sa(I_X), 0, false, false, false);
+      tc::umma_commit(&tl.bar);
+    }
+    {  // meanwhile: the scaled operands of step 2, diag(E) X, U (additive) and the gates into the workspace
+      float dov[16], m[16];
+      gtc::get_row(dov, img(I_DO), R, C0);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) m[e] = GamR * dov[e];
+      gtc::put_split(img(I_M3), img(I_M3L), R, C0, m);
+      if (reg) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m[e] = etaR * vv[e];
+        gtc::put_split(img(I_M1), img(I_M1L), R, C0, m);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m[e] = etaR * GamR * xr[e];
+        gtc::put_split(img(I_MX), img(I_MXL), R, C0, m);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m[e] = etaR * vv[e];
+        gtc::st16(wsmat(a, cg, M_U) + R * kN + C0, m);
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) m[e] = ER * xr[e];
+      gtc::st16(wsmat(a, cg, M_XT) + R * kN + C0, m);
+      float* gv = wsgate(a, cg);
+      if (tid < kN) {
+        gv[tid] = gs.g[tid];
+        gv[kN + tid] = gs.Gam[tid];
+        gv[2 * kN + tid] = gs.E[tid];
+        gv[3 * kN + tid] = gs.eta[tid];
+        gv[4 * kN + tid] = gs.nrm[tid];
+        gv[5 * kN + tid] = gs.ex[tid];
+        gv[6 * kN + tid] = gs.gam[tid];
+      }
+    }
+    if (!wait_step()) break;
+    // ---- E1: P (.) D as images; A = diag(eta) (D (.) X X^T) (strictly lower) as fp32 rows
+    {
+      float p[16];
+      tld(1, p);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int cc = C0 + e;
+        p[e] = cc <= R ? __expf(gR - gs.g[cc]) * p[e] : 0.f;
+      }
+      gtc::put_split(img(I_PD), img(I_PDL), R, C0, p);
+      if (reg) {
+        tld(0, p);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int cc = C0 + e;
+          p[e] = cc < R ? etaR * __expf(gR - gs.g[cc]) * p[e] : 0.f;
+        }
+        gtc::st16(reinterpret_cast<float*>(img(I_T)) + R * kN + C0, p);
+      }
+    }
+    step_barrier();
+    if (reg) {
+      // T = (I + A)^{-1}: thread j < 64 solves column j by forward
+      // substitution, the column in registers, A's rows read as broadcasts;
+      // then (A read by all 64) the column into the T images and the workspace
+      if (tid < kN) {
+        const float* Am = reinterpret_cast<const float*>(img(I_T));
+        const int j = tid;
+        float tcol[kN];
+#pragma unroll
+        for (int r = 0; r < kN; ++r) {
+          float s0 = (r == j) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < r; i += 2) {
+            s0 = fmaf(-Am[r * kN + i], tcol[i], s0);
+            if (i + 1 < r) s1 = fmaf(-Am[r * kN + i + 1], tcol[i + 1], s1);
+          }
+          tcol[r] = s0 + s1;
+        }
+        tcu::named_bar(1, kN);
+        float* wT = wsmat(a, cg, M_T);
+        uint8_t* th = img(I_T);
+        uint8_t* tlo = img(I_TL);
+#pragma unroll
+        for (int r = 0; r < kN; ++r) {
+          const __nv_bfloat16 hv = __float2bfloat16_rn(tcol[r]);
+          const __nv_bfloat16 lv = __float2bfloat16_rn(tcol[r] - __bfloat162float(hv));
+          *reinterpret_cast<__nv_bfloat16*>(th + tcu::sw128(r, j)) = hv;
+          *reinterpret_cast<__nv_bfloat16*>(tlo + tcu::sw128(r, j)) = lv;
+          wT[r * kN + j] = tcol[r];
+        }
+      }
+      step_barrier();
+    }
+    // ---- step 2: W = T diag(eta Gamma) X, U = T diag(eta) V, Q^T diag(Gamma) dO, Z = (P (.) D)^T dO
+    if (tid == 0) {
+      if (reg) {
+        gtc::terms(acc(0), sa(I_T), sa(I_TL), true, false, sa(I_MX), sa(I_MXL), true, true, false);
+        gtc::terms(acc(1), sa(I_T), sa(I_TL), true, false, sa(I_M1), sa(I_M1L), true, true, false);
+        gtc::terms(acc(3), sa(I_PD), sa(I_PDL), true, true, sa(I_DO), 0, false, true, false);
+      }
+      gtc::terms(acc(2), sa(I_Q), 0, false, true, sa(I_M3), sa(I_M3L), true, true, false);
+      tc::umma_commit(&tl.bar);
+    }
+    if (!wait_step()) break;
+    if (reg) {
+      // ---- E2: W and U into the workspace, W and Z as images
+      float p[16];
+      tld(0, p);
+      gtc::st16(wsmat(a, cg, M_W) + R * kN + C0, p);
+      gtc::put_split(img(I_M1), img(I_M1L), R, C0, p);
+      tld(1, p);
+      gtc::st16(wsmat(a, cg, M_U) + R * kN + C0, p);
+      tld(3, p);
+      gtc::put_split(img(I_MX), img(I_MXL), R, C0, p);
+      step_barrier();
+      // ---- step 3: W^T Z
+      if (tid == 0) {
+        gtc::terms(acc(0), sa(I_M1), sa(I_M1L), true, true, sa(I_MX), sa(I_MXL), true, true, false);
+        tc::umma_commit(&tl.bar);
+      }
+      if (!wait_step()) break;
+    }
+    // ---- E3: Y = Q^T diag(Gamma) dO - W^T (P (.) D)^T dO
+    {
+      float y[16];
+      tld(2, y);
+      if (reg) {
+        float p[16];
+        tld(0, p);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) y[e] -= p[e];
+      }
+      gtc::st16(wsmat(a, cg, M_Y) + R * kN + C0, y);
+    }
+  } while (false);
+  if (!ok && tid == 0) atomicExch(a.status, tcu::kStatusTimeout);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tl.tmem, 256);
+}
+
 constexpr size_t prep_smem() { return 8 * kN * LDM * sizeof(float) + sizeof(GateSm) + 4 * kN * sizeof(float); }
 constexpr size_t grad_smem() { return 12 * kN * LDM * sizeof(float) + sizeof(GateSm) + 8 * kN * sizeof(float); }
 
@@ -1549,11 +1835,17 @@ int launch_chains(const CbArgs& a, cudaStream_t s) {
 template <typename Tin>
 int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
   const unsigned nch = (unsigned)(a.B * a.H * a.NC);
-  auto prep = bwdc_prep_kernel<Tin>;
+  auto prep = bwdc_prep_kernel<float>;
   auto grad = bwdc_grad_kernel<float>;
-  if (!set_smem_limit(reinterpret_cast<const void*>(prep), prep_smem())) return FALCON_ERR_CUDA;
-  if (sizeof(Tin) == 4 && !set_smem_limit(reinterpret_cast<const void*>(grad), grad_smem())) return FALCON_ERR_CUDA;
-  prep<<<nch, kThr, prep_smem(), s>>>(a);
+  if constexpr (sizeof(Tin) == 2) {  // bf16 inputs: the tensor-core kernels
+    if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_prep_tc_kernel), ptc::kSmem)) return FALCON_ERR_CUDA;
+    bwdc_prep_tc_kernel<<<nch, kThr, ptc::kSmem, s>>>(a);
+  } else {
+    if (!set_smem_limit(reinterpret_cast<const void*>(prep), prep_smem()) ||
+        !set_smem_limit(reinterpret_cast<const void*>(grad), grad_smem()))
+      return FALCON_ERR_CUDA;
+    prep<<<nch, kThr, prep_smem(), s>>>(a);
+  }
   // 16-column chain slices when their CTAs fit one wave at two per SM, else 32
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1561,7 +1853,7 @@ int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
     return FALCON_ERR_CUDA;
   const int st = (long)a.B * a.H * (kN / 16) <= 2L * sms ? launch_chains<16>(a, s) : launch_chains<32>(a, s);
   if (st != FALCON_OK) return st;
-  if constexpr (sizeof(Tin) == 2) {  // bf16 inputs: the tensor-core gradient kernel
+  if constexpr (sizeof(Tin) == 2) {
     if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_grad_tc_kernel), gtc::kSmem)) return FALCON_ERR_CUDA;
     bwdc_grad_tc_kernel<<<nch, kThr, gtc::kSmem, s>>>(a);
   } else {
