@@ -46,7 +46,10 @@ static_assert(kRows * (kThr / 16) == kN && (kRows == 2 || kRows == 4), "product 
 static_assert(kRowT * kN == kThr && (kN % kRowT) == 0, "row sums must cover 64 rows");
 constexpr int kThrC = 256;    // chain kernels
 constexpr size_t kMat = (size_t)kN * kN;
-enum { M_T = 0, M_W, M_U, M_XT, M_Y, M_S0, M_DS1, kMats };
+// per chunk: T, W, U, diag(E) X (fp32 inputs) or the chain offset b (bf16
+// inputs), Y, the start state, the end-state gradient, and (bf16 inputs) the
+// chain transition A as hi | lo bf16 images
+enum { M_T = 0, M_W, M_U, M_XT, M_Y, M_S0, M_DS1, M_AC, kMats };
 constexpr int kGateVecs = 8;  // per chunk: g, Gamma, E, eta, nrm, exists, (2 spare)
 constexpr int NN = 0, TN = 1, NT = 2;
 
@@ -1078,11 +1081,12 @@ struct Tail {
 constexpr size_t kSmem = 1024 + (size_t)kImgs * kImg + sizeof(Tail);
 static_assert(kAcc * 64 == 512, "the accumulators fill the TMEM of one CTA");
 
-// D (+)= op(A) op(B) over K = 64: the hi x hi term, then hi x lo and lo x hi
-// where that operand has a low part.  amn / bmn: the image's rows run along K.
+// D (+)= op(A) op(B) over K = 64 (M = 64, N columns): the hi x hi term, then
+// hi x lo and lo x hi where that operand has a low part.  amn / bmn: the
+// image's rows run along K.
 __device__ __forceinline__ void terms(uint32_t d, uint32_t ahi, uint32_t alo, bool asp, bool amn, uint32_t bhi,
-                                      uint32_t blo, bool bsp, bool bmn, bool accumulate) {
-  const uint32_t id = tc::idesc_bf16(64, 64, amn, bmn);
+                                      uint32_t blo, bool bsp, bool bmn, bool accumulate, int N = 64) {
+  const uint32_t id = tc::idesc_bf16(64, N, amn, bmn);
   auto dsc = [](uint32_t s, bool mn, int ks) { return mn ? tcu::mndesc(s, ks) : tcu::kdesc<64>(s, ks); };
   uint32_t on = accumulate ? 1u : 0u;
 #pragma unroll
@@ -1554,8 +1558,11 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
 // A = diag(eta) (D (.) X X^T) and P (.) D from one step of MMAs; T = (I +
 // A)^{-1} by forward substitution (a column per thread, as before); then
 // W = T diag(eta Gamma) X, U = T diag(eta) V, Q^T diag(Gamma) dO and
-// Z = (P (.) D)^T dO in one step, and W^T Z in a last one.  Thirteen images
-// and 256 TMEM columns: two CTAs share an SM.
+// Z = (P (.) D)^T dO in one step, and in a last one W^T Z with the chain's
+// transition A = Gamma_63 I - (diag(E) X)^T W (stored as hi | lo images) and
+// offset b = (diag(E) X)^T U, so that a chain step is one product (additive:
+// A = Gamma_63 I, no product).  Thirteen images and 256 TMEM columns: two
+// CTAs share an SM.
 namespace ptc {
 enum {
   I_X = 0, I_Q, I_DO,
@@ -1696,14 +1703,7 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) m[e] = etaR * GamR * xr[e];
         gtc::put_split(img(I_MX), img(I_MXL), R, C0, m);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) m[e] = etaR * vv[e];
-        gtc::st16(wsmat(a, cg, M_U) + R * kN + C0, m);
       }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) m[e] = ER * xr[e];
-      gtc::st16(wsmat(a, cg, M_XT) + R * kN + C0, m);
       float* gv = wsgate(a, cg);
       if (tid < kN) {
         gv[tid] = gs.g[tid];
@@ -1781,41 +1781,189 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
       tc::umma_commit(&tl.bar);
     }
     if (!wait_step()) break;
-    if (reg) {
-      // ---- E2: W and U into the workspace, W and Z as images
-      float p[16];
-      tld(0, p);
-      gtc::st16(wsmat(a, cg, M_W) + R * kN + C0, p);
-      gtc::put_split(img(I_M1), img(I_M1L), R, C0, p);
-      tld(1, p);
-      gtc::st16(wsmat(a, cg, M_U) + R * kN + C0, p);
-      tld(3, p);
-      gtc::put_split(img(I_MX), img(I_MXL), R, C0, p);
-      step_barrier();
-      // ---- step 3: W^T Z
-      if (tid == 0) {
-        gtc::terms(acc(0), sa(I_M1), sa(I_M1L), true, true, sa(I_MX), sa(I_MXL), true, true, false);
-        tc::umma_commit(&tl.bar);
-      }
-      if (!wait_step()) break;
-    }
-    // ---- E3: Y = Q^T diag(Gamma) dO - W^T (P (.) D)^T dO
+    // ---- E2: W and U into the workspace; W, U, Z and diag(E) X as images
     {
-      float y[16];
+      float p[16];
+      if (reg) {
+        tld(0, p);
+        gtc::st16(wsmat(a, cg, M_W) + R * kN + C0, p);
+        gtc::put_split(img(I_M1), img(I_M1L), R, C0, p);
+        tld(1, p);
+        gtc::st16(wsmat(a, cg, M_U) + R * kN + C0, p);
+        gtc::put_split(img(I_M3), img(I_M3L), R, C0, p);
+        tld(3, p);
+        gtc::put_split(img(I_MX), img(I_MXL), R, C0, p);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) p[e] = etaR * vv[e];
+        gtc::put_split(img(I_M3), img(I_M3L), R, C0, p);
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) p[e] = ER * xr[e];
+      gtc::put_split(img(I_T), img(I_TL), R, C0, p);
+    }
+    step_barrier();
+    // ---- step 3: W^T Z, (diag(E) X)^T W, (diag(E) X)^T U
+    if (tid == 0) {
+      if (reg) {
+        gtc::terms(acc(0), sa(I_M1), sa(I_M1L), true, true, sa(I_MX), sa(I_MXL), true, true, false);
+        gtc::terms(acc(1), sa(I_T), sa(I_TL), true, true, sa(I_M1), sa(I_M1L), true, true, false);
+      }
+      gtc::terms(acc(3), sa(I_T), sa(I_TL), true, true, sa(I_M3), sa(I_M3L), true, true, false);
+      tc::umma_commit(&tl.bar);
+    }
+    if (!wait_step()) break;
+    // ---- E3: Y = Q^T diag(Gamma) dO - W^T (P (.) D)^T dO; the chain's offset
+    // b = (diag(E) X)^T U and transition A = Gamma_63 I - (diag(E) X)^T W
+    {
+      float y[16], p[16];
       tld(2, y);
       if (reg) {
-        float p[16];
         tld(0, p);
 #pragma unroll
         for (int e = 0; e < 16; ++e) y[e] -= p[e];
       }
       gtc::st16(wsmat(a, cg, M_Y) + R * kN + C0, y);
+      tld(3, p);
+      gtc::st16(wsmat(a, cg, M_XT) + R * kN + C0, p);
+      if (reg) {
+        tld(1, p);
+        const float g63 = gs.Gam[kN - 1];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) p[e] = (C0 + e == R ? g63 : 0.f) - p[e];
+        uint8_t* ac = reinterpret_cast<uint8_t*>(wsmat(a, cg, M_AC));
+        gtc::put_split(ac, ac + gtc::kImg, R, C0, p);
+      }
     }
   } while (false);
   if (!ok && tid == 0) atomicExch(a.status, tcu::kStatusTimeout);
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tl.tmem, 256);
+}
+
+
+// ---------------------------------------------------------------- (b), (c) on tcgen05
+// The chains for bf16 inputs, one product per chunk step with the transition
+// and offset formed by the preparation:
+//   forward   S_{c+1} = A_c S_c + b_c       (S_c out: the chunk's start state),
+//   backward  dS_c = A_c^T dS_{c+1} + Y_c   (dS_{c+1} out: its end-state gradient),
+// the backward reading the same images MN-major; additive: A_c = Gamma_63 I.
+// One CTA of 128 threads per (b, h, 32 value columns); a thread keeps a row
+// and 16 columns of the slice in registers (the M = 64 accumulator layout);
+// the next chunks' images arrive by bulk copies into a ring of stages.
+namespace ctc {
+constexpr int kSC = 32, kThr = 128, kNST = 3;
+struct Smem {
+  uint8_t A[kNST][2 * gtc::kImg];  // hi | lo images of A_c
+  uint8_t S[2 * gtc::kImg];        // hi | lo images of the slice (32 of each row's 64 columns)
+  uint64_t full[kNST];
+  uint64_t done;
+  uint32_t tmem;
+  int pad;
+};
+constexpr size_t kSmem = 1024 + sizeof(Smem);
+}  // namespace ctc
+
+template <bool BWD>
+__global__ void __launch_bounds__(ctc::kThr) bwdc_chain_tc_kernel(CbArgs a) {
+  using namespace ctc;
+  extern __shared__ uint8_t ctc_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(tcu::align1024(ctc_raw));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x, c0 = blockIdx.y * kSC;
+  const int R = 16 * warp + (lane & 15), Cl = 16 * (lane >> 4), C = c0 + Cl;  // row, first column
+  const bool reg = !a.additive;
+  const size_t base = (size_t)bh * a.NC;
+  auto chunk = [&](int n) { return BWD ? a.NC - 1 - n : n; };  // the chunk of step n
+  if (warp == 0) {
+    tc::tmem_alloc(&sm.tmem, 32);
+    tc::tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < kNST; ++s) tc::mbar_init(&sm.full[s], 1);
+    tc::mbar_init(&sm.done, 1);
+    tc::fence_mbar_init();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  int issued = 0;  // thread 0: transitions requested
+  auto issue = [&]() {
+    const int s = issued % kNST;
+    tc::mbar_arrive_expect_tx(&sm.full[s], 2 * gtc::kImg);
+    tc::bulk_load(sm.A[s], wsmat(a, base + chunk(issued), M_AC), 2 * gtc::kImg, &sm.full[s]);
+    ++issued;
+  };
+  if (reg && tid == 0)
+    while (issued < kNST && issued < a.NC) issue();
+  const int OFF = BWD ? M_Y : M_XT;
+  float S[16], off[16];
+  const float* init = BWD ? a.dS_final : a.S_in;
+  if (init) gtc::ld16(S, init + ((size_t)bh * kN + R) * kN + C);
+  else
+#pragma unroll
+    for (int e = 0; e < 16; ++e) S[e] = 0.f;
+  if (a.NC > 0) gtc::ld16(off, wsmat(a, base + chunk(0), OFF) + R * kN + C);
+  uint32_t dphase = 0;
+  bool ok = true;
+  for (int n = 0; n < a.NC; ++n) {
+    const size_t cg = base + chunk(n);
+    gtc::st16(wsmat(a, cg, BWD ? M_DS1 : M_S0) + R * kN + C, S);
+    float nxt[16];
+    if (n + 1 < a.NC) gtc::ld16(nxt, wsmat(a, base + chunk(n + 1), OFF) + R * kN + C);
+    if (reg) {
+      gtc::put_split(sm.S, sm.S + gtc::kImg, R, Cl, S);
+      tc::fence_proxy_async();
+      tc::tc_fence_before();
+      __syncthreads();  // the slice's images are written, the last step's TMEM reads are done
+      tc::tc_fence_after();
+      bool mine = true;
+      if (tid == 0) {
+        const int s = n % kNST;
+        mine = tc::mbar_wait(&sm.full[s], (uint32_t)((n / kNST) & 1), a.wait_ns);
+        if (mine) {
+          tc::tc_fence_after();
+          const uint32_t ah = tc::smem_u32(sm.A[s]), sh = tc::smem_u32(sm.S);
+          gtc::terms(tmem, ah, ah + gtc::kImg, true, BWD, sh, sh + gtc::kImg, true, true, false, kSC);
+          tc::umma_commit(&sm.done);
+        } else {
+          tcu::mbar_arrive(&sm.done);  // release the others; the step is abandoned
+        }
+      }
+      mine = tc::mbar_wait(&sm.done, dphase, a.wait_ns) && mine;
+      dphase ^= 1u;
+      tc::tc_fence_after();
+      if (__syncthreads_or(!mine)) {
+        ok = false;
+        break;
+      }
+      if (tid == 0 && issued < a.NC) issue();  // the stage read by this step's product is free
+      uint32_t r[16];
+      tc::tmem_ld16x2_16(tmem + ((uint32_t)(32 * warp) << 16), r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) S[e] = __uint_as_float(r[e]) + off[e];
+    } else {
+      const float g63 = wsgate(a, cg)[2 * kN - 1];  // Gamma of the chunk's last row
+#pragma unroll
+      for (int e = 0; e < 16; ++e) S[e] = fmaf(g63, S[e], off[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) off[e] = nxt[e];
+  }
+  if (ok && BWD && a.dS_in) gtc::st16(a.dS_in + ((size_t)bh * kN + R) * kN + C, S);
+  if (!ok && tid == 0) {
+    atomicExch(a.status, tcu::kStatusTimeout);
+    // the copies still in flight land before the CTA leaves (bounded): the
+    // last use of each stage
+    for (int m = issued - kNST > 0 ? issued - kNST : 0; m < issued; ++m)
+      tc::mbar_wait(&sm.full[m % kNST], (uint32_t)((m / kNST) & 1), a.wait_ns);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, 32);
 }
 
 constexpr size_t prep_smem() { return 8 * kN * LDM * sizeof(float) + sizeof(GateSm) + 4 * kN * sizeof(float); }
@@ -1851,8 +1999,16 @@ int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FALCON_ERR_CUDA;
-  const int st = (long)a.B * a.H * (kN / 16) <= 2L * sms ? launch_chains<16>(a, s) : launch_chains<32>(a, s);
-  if (st != FALCON_OK) return st;
+  if constexpr (sizeof(Tin) == 2) {
+    if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_chain_tc_kernel<false>), ctc::kSmem) ||
+        !set_smem_limit(reinterpret_cast<const void*>(bwdc_chain_tc_kernel<true>), ctc::kSmem))
+      return FALCON_ERR_CUDA;
+    bwdc_chain_tc_kernel<false><<<dim3(a.B * a.H, kN / ctc::kSC), ctc::kThr, ctc::kSmem, s>>>(a);
+    bwdc_chain_tc_kernel<true><<<dim3(a.B * a.H, kN / ctc::kSC), ctc::kThr, ctc::kSmem, s>>>(a);
+  } else {
+    const int st = (long)a.B * a.H * (kN / 16) <= 2L * sms ? launch_chains<16>(a, s) : launch_chains<32>(a, s);
+    if (st != FALCON_OK) return st;
+  }
   if constexpr (sizeof(Tin) == 2) {
     if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_grad_tc_kernel), gtc::kSmem)) return FALCON_ERR_CUDA;
     bwdc_grad_tc_kernel<<<nch, kThr, gtc::kSmem, s>>>(a);

@@ -146,9 +146,9 @@ def test_backward_window_kernel_workspace(F, kw):
 def test_backward_workspace_and_overlap_checks(F):
     p = _p(F, B=2, T=100, H=3)
     n = F.falcon_backward_workspace_size(p)
-    # chunked form (Falcon-1, d = 64): the status block, then per chunk seven 64 x 64 fp32
-    # matrices and 8 gate rows
-    assert n == 256 + 2 * 3 * 2 * (7 * 64 * 64 + 8 * 64) * 4
+    # chunked form (Falcon-1, d = 64): the status block, then per chunk eight 64 x 64 fp32
+    # matrices (the chain transition's bf16 images take one) and 8 gate rows
+    assert n == 256 + 2 * 3 * 2 * (8 * 64 * 64 + 8 * 64) * 4
     # recurrent form (d = 32, or an empty call): states at every 64th step + one block
     assert F.falcon_backward_workspace_size(_p(F, dk=32, dv=32)) == 2 * 3 * (2 + 64) * 32 * 32 * 4
     assert F.falcon_backward_workspace_size(_p(F, T=0)) == 2 * 3 * 64 * 64 * 64 * 4
