@@ -1118,6 +1118,25 @@ __device__ __forceinline__ void put_split(uint8_t* hi, uint8_t* lo, int r, int c
     *reinterpret_cast<uint4*>(lo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
   }
 }
+// A 64 x 64 fp32 workspace matrix into 16 KB of shared memory by cp.async
+// (no wait): row r's 16-byte piece q at piece q ^ (r & 7) of the row, so that
+// eight consecutive rows read at one column are free of bank conflicts.
+__device__ __forceinline__ void cp_mat_sw(uint8_t* dst, const float* src) {
+#pragma unroll
+  for (int k = 0; k < kN * kN / 4 / kThr; ++k) {
+    const int i = threadIdx.x + kThr * k, r = i >> 4, q = i & 15;
+    cp16(dst + (r * 16 + (q ^ (r & 7))) * 16, src + r * kN + q * 4);
+  }
+}
+// 16 values of row r of such a matrix from column c0 (a multiple of 16)
+__device__ __forceinline__ void ld_sw16(float (&v)[16], const uint8_t* m, int r, int c0) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int q = (c0 >> 2) + k;
+    const float4 f = *reinterpret_cast<const float4*>(m + (r * 16 + (q ^ (r & 7))) * 16);
+    v[4 * k] = f.x; v[4 * k + 1] = f.y; v[4 * k + 2] = f.z; v[4 * k + 3] = f.w;
+  }
+}
 // 16 values of an exact image's row r from column c0
 __device__ __forceinline__ void get_row(float (&v)[16], const uint8_t* im, int r, int c0) {
 #pragma unroll
@@ -1225,14 +1244,28 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
   };
   auto row_sum = [&](int which, int r) { return tl.red[which][0][r] + tl.red[which][1][r]; };
 
-  // ---- loads: gates; keys, queries, output gradients as images; S0, dS1, W
+  // ---- loads, one round: the gates and the workspace's fp32 matrices by
+  // cp.async (into image slots that are free until later: S0 into Delta's,
+  // dS1 into P (.) D's, W into dG's, T into dP's, U into T's), keys, queries,
+  // output gradients as images, this thread's values
   if (tid < (int)(sizeof(GateSm) / 16)) cp16(reinterpret_cast<float*>(&gs) + 4 * tid, wsgate(a, cg) + 4 * tid);
+  cp_mat_sw(img(I_DL), wsmat(a, cg, M_S0));
+  cp_mat_sw(img(I_PD), wsmat(a, cg, M_DS1));
+  if (reg) {
+    cp_mat_sw(img(I_DG), wsmat(a, cg, M_W));
+    cp_mat_sw(img(I_DP), wsmat(a, cg, M_T));
+    cp_mat_sw(img(I_T), wsmat(a, cg, M_U));
+  }
   cp_commit();
   load_xqdo(a, img(I_X), img(I_Q), img(I_DO), b, h, t0, pos, bh);
-  {
+  float vv[16];
+  load_row16(vv, a.v, a, b, h, t, C0);
+  cp_wait0();
+  __syncthreads();
+  {  // S0, dS1 and W as images
     float s0[16], ds[16];
-    ld16(s0, wsmat(a, cg, M_S0) + R * kN + C0);
-    ld16(ds, wsmat(a, cg, M_DS1) + R * kN + C0);
+    ld_sw16(s0, img(I_DL), R, C0);
+    ld_sw16(ds, img(I_PD), R, C0);
     put_split(img(I_S0), img(I_S0L), R, C0, s0);
     put_split(img(I_DS1), img(I_DS1L), R, C0, ds);
     float sd = 0.f;
@@ -1241,7 +1274,7 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
     row_part(R_SD, sd);
     if (reg) {
       float w[16];
-      ld16(w, wsmat(a, cg, M_W) + R * kN + C0);
+      ld_sw16(w, img(I_DG), R, C0);
       put_split(img(I_W), img(I_WL), R, C0, w);
     }
   }
@@ -1294,15 +1327,8 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
       terms(acc(A_DOS0), sa(I_DO), 0, false, false, sa(I_S0), sa(I_S0L), true, false, false);
       tc::umma_commit(&tl.bar);
     }
-    // meanwhile: T as images, this thread's U and V
-    float u[16], vv[16];
-    if (reg) {
-      float tt[16];
-      ld16(tt, wsmat(a, cg, M_T) + R * kN + C0);
-      put_split(img(I_T), img(I_TL), R, C0, tt);
-      ld16(u, wsmat(a, cg, M_U) + R * kN + C0);
-    }
-    load_row16(vv, a.v, a, b, h, t, C0);
+    float u[16];  // meanwhile: this thread's U (staged in T's slots)
+    if (reg) ld_sw16(u, img(I_T), R, C0);
     if (!wait_step()) break;
 
     // ---- E1: Delta; dGamma through the output term; P (.) D; E dE
@@ -1360,6 +1386,11 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
     }
     if (reg) {
       put_split(img(I_W), img(I_WL), R, C0, dd);
+      {  // T as images (its slots held U until every thread read it, before E1's barrier)
+        float tt[16];
+        ld_sw16(tt, img(I_DP), R, C0);
+        put_split(img(I_T), img(I_TL), R, C0, tt);
+      }
       step_barrier();
       // ---- step 3: dR = T^T dDelta
       if (tid == 0) {
@@ -1690,20 +1721,12 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
       gtc::terms(acc(1), sa(I_Q), 0, false, false, sa(I_X), 0, false, false, false);
       tc::umma_commit(&tl.bar);
     }
-    {  // meanwhile: the scaled operands of step 2, diag(E) X, U (additive) and the gates into the workspace
+    {  // meanwhile: diag(Gamma) dO as images, the gates into the workspace
       float dov[16], m[16];
       gtc::get_row(dov, img(I_DO), R, C0);
 #pragma unroll
       for (int e = 0; e < 16; ++e) m[e] = GamR * dov[e];
       gtc::put_split(img(I_M3), img(I_M3L), R, C0, m);
-      if (reg) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) m[e] = etaR * vv[e];
-        gtc::put_split(img(I_M1), img(I_M1L), R, C0, m);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) m[e] = etaR * GamR * xr[e];
-        gtc::put_split(img(I_MX), img(I_MXL), R, C0, m);
-      }
       float* gv = wsgate(a, cg);
       if (tid < kN) {
         gv[tid] = gs.g[tid];
@@ -1733,40 +1756,79 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
           const int cc = C0 + e;
           p[e] = cc < R ? etaR * __expf(gR - gs.g[cc]) * p[e] : 0.f;
         }
-        gtc::st16(reinterpret_cast<float*>(img(I_T)) + R * kN + C0, p);
+        gtc::st16(reinterpret_cast<float*>(img(I_M1)) + R * kN + C0, p);  // A, fp32 rows
       }
     }
     step_barrier();
     if (reg) {
-      // T = (I + A)^{-1}: thread j < 64 solves column j by forward
-      // substitution, the column in registers, A's rows read as broadcasts;
-      // then (A read by all 64) the column into the T images and the workspace
+      // T = (I + A)^{-1} by 16 x 16 blocks (A in the slots of diag(eta) V's
+      // images, T in those of diag(eta Gamma) X's, both fp32 rows, the images
+      // written after): the diagonal blocks by forward substitution (a thread
+      // per column), then block diagonal by block diagonal
+      //   T_ij = -T_ii G_ij,  G_ij = sum_{k=j}^{i-1} A_ik T_kj  (i > j),
+      // the G blocks kept in T's upper blocks, which are zeroed at the end.
+      const float* Am = reinterpret_cast<const float*>(img(I_M1));
+      float* Tm = reinterpret_cast<float*>(img(I_MX));
       if (tid < kN) {
-        const float* Am = reinterpret_cast<const float*>(img(I_T));
-        const int j = tid;
-        float tcol[kN];
+        const int o = 16 * (tid >> 4), jj = tid & 15;
+        float x[16];
 #pragma unroll
-        for (int r = 0; r < kN; ++r) {
-          float s0 = (r == j) ? 1.f : 0.f, s1 = 0.f;
+        for (int r = 0; r < 16; ++r) {
+          float sv = r == jj ? 1.f : 0.f;
 #pragma unroll
-          for (int i = 0; i < r; i += 2) {
-            s0 = fmaf(-Am[r * kN + i], tcol[i], s0);
-            if (i + 1 < r) s1 = fmaf(-Am[r * kN + i + 1], tcol[i + 1], s1);
-          }
-          tcol[r] = s0 + s1;
+          for (int i = 0; i < r; ++i) sv = fmaf(-Am[(o + r) * kN + o + i], x[i], sv);
+          x[r] = sv;
         }
-        tcu::named_bar(1, kN);
-        float* wT = wsmat(a, cg, M_T);
-        uint8_t* th = img(I_T);
-        uint8_t* tlo = img(I_TL);
 #pragma unroll
-        for (int r = 0; r < kN; ++r) {
-          const __nv_bfloat16 hv = __float2bfloat16_rn(tcol[r]);
-          const __nv_bfloat16 lv = __float2bfloat16_rn(tcol[r] - __bfloat162float(hv));
-          *reinterpret_cast<__nv_bfloat16*>(th + tcu::sw128(r, j)) = hv;
-          *reinterpret_cast<__nv_bfloat16*>(tlo + tcu::sw128(r, j)) = lv;
-          wT[r * kN + j] = tcol[r];
+        for (int r = 0; r < 16; ++r) Tm[(o + r) * kN + o + jj] = x[r];
+      }
+      __syncthreads();
+      for (int d = 1; d < 4; ++d) {
+        const int nb = 4 - d;
+        for (int e = tid; e < nb * 256; e += kThr) {
+          const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15, j = blk, i = j + d;
+          float g = 0.f;
+          for (int k = j; k < i; ++k)
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+              g = fmaf(Am[(16 * i + rr) * kN + 16 * k + m], Tm[(16 * k + m) * kN + 16 * j + cc], g);
+          Tm[rr * kN + 16 * (1 + blk) + cc] = g;  // G_ij in upper block (0, 1 + blk)
         }
+        __syncthreads();
+        for (int e = tid; e < nb * 256; e += kThr) {
+          const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = blk + d;
+          float tv = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            tv = fmaf(Tm[(16 * i + rr) * kN + 16 * i + m], Tm[m * kN + 16 * (1 + blk) + cc], tv);
+          Tm[(16 * i + rr) * kN + 16 * blk + cc] = -tv;
+        }
+        __syncthreads();
+      }
+      for (int e = tid; e < 6 * 256; e += kThr) {  // the upper blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        const int ub = e >> 8, bi = ub < 3 ? 0 : (ub < 5 ? 1 : 2), bj = ub < 3 ? ub + 1 : (ub < 5 ? ub - 1 : 3);
+        Tm[(16 * bi + ((e >> 4) & 15)) * kN + 16 * bj + (e & 15)] = 0.f;
+      }
+      __syncthreads();
+      {  // T as images and into the workspace
+        float tt[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 f = reinterpret_cast<const float4*>(Tm + R * kN + C0)[k];
+          tt[4 * k] = f.x; tt[4 * k + 1] = f.y; tt[4 * k + 2] = f.z; tt[4 * k + 3] = f.w;
+        }
+        gtc::put_split(img(I_T), img(I_TL), R, C0, tt);
+        gtc::st16(wsmat(a, cg, M_T) + R * kN + C0, tt);
+      }
+      __syncthreads();  // A and T read: their slots take the scaled operands of step 2
+      {
+        float m[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m[e] = etaR * vv[e];
+        gtc::put_split(img(I_M1), img(I_M1L), R, C0, m);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m[e] = etaR * GamR * xr[e];
+        gtc::put_split(img(I_MX), img(I_MXL), R, C0, m);
       }
       step_barrier();
     }
