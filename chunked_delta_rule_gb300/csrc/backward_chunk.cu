@@ -1118,6 +1118,12 @@ __device__ __forceinline__ void put_split(uint8_t* hi, uint8_t* lo, int r, int c
     *reinterpret_cast<uint4*>(lo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
   }
 }
+// The first 1024-byte boundary of a dynamic shared-memory array, as an
+// offset from the array itself, so that the compiler keeps the pointers in
+// the shared space (shared loads and stores, not generic ones).
+__device__ __forceinline__ uint8_t* shared_align1024(uint8_t* raw) {
+  return raw + ((1024u - (tc::smem_u32(raw) & 1023u)) & 1023u);
+}
 // A 64 x 64 fp32 workspace matrix into 16 KB of shared memory by cp.async
 // (no wait): row r's 16-byte piece q at piece q ^ (r & 7) of the row, so that
 // eight consecutive rows read at one column are free of bank conflicts.
@@ -1214,7 +1220,7 @@ __device__ __forceinline__ void st16(float* p, const float (&v)[16]) {
 __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
   using namespace gtc;
   extern __shared__ uint8_t gtc_raw[];
-  uint8_t* base = tcu::align1024(gtc_raw);
+  uint8_t* base = shared_align1024(gtc_raw);
   auto img = [&](int i) { return base + (size_t)i * kImg; };
   auto sa = [&](int i) { return tc::smem_u32(base + (size_t)i * kImg); };
   Tail& tl = *reinterpret_cast<Tail*>(base + (size_t)kImgs * kImg);
@@ -1618,7 +1624,7 @@ static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
   using namespace ptc;
   extern __shared__ uint8_t ptc_raw[];
-  uint8_t* base = tcu::align1024(ptc_raw);
+  uint8_t* base = gtc::shared_align1024(ptc_raw);
   auto img = [&](int i) { return base + (size_t)i * gtc::kImg; };
   auto sa = [&](int i) { return tc::smem_u32(base + (size_t)i * gtc::kImg); };
   Tail& tl = *reinterpret_cast<Tail*>(base + (size_t)kImgs * gtc::kImg);
@@ -1639,6 +1645,12 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
   if (tid == 32) {
     tc::mbar_init(&tl.bar, 1);
     tc::fence_mbar_init();
+  }
+  float beta_r = 0.f, lam_r = 0.f;  // this row's gates (threads < 64), fetched with the inputs
+  if (tid < kN && t0 + tid < a.T) {
+    const size_t gi = ((size_t)b * a.T + t0 + tid) * a.H + h;
+    beta_r = a.beta[gi];
+    lam_r = a.lam[gi];
   }
   gtc::load_xqdo(a, img(I_X), img(I_Q), img(I_DO), b, h, t0, pos, bh);
   float vv[16];
@@ -1671,11 +1683,10 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
     const int r = tid, t = t0 + r;
     const float n = tl.red[0][r] + tl.red[1][r];
     const bool live = t < a.T, ex = live && pos + t >= a.shift;
-    const size_t gi = ((size_t)b * a.T + (live ? t : 0)) * a.H + h;
     gs.nrm[r] = n;
     gs.ex[r] = ex ? 1.f : 0.f;
-    gs.eta[r] = ex ? a.beta[gi] / (a.eps + n) : 0.f;
-    const float gm = live ? fminf(fmaxf(1.f - a.lam[gi], a.eps_gamma), 1.f) : 1.f;
+    gs.eta[r] = ex ? beta_r / (a.eps + n) : 0.f;
+    const float gm = live ? fminf(fmaxf(1.f - lam_r, a.eps_gamma), 1.f) : 1.f;
     gs.gam[r] = gm;
     gs.g[r] = live ? logf(gm) : 0.f;
   }
@@ -1774,10 +1785,12 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float sv = r == jj ? 1.f : 0.f;
+          float ar[16], sv[4] = {r == jj ? 1.f : 0.f, 0.f, 0.f, 0.f};  // the row's loads first, four chains
 #pragma unroll
-          for (int i = 0; i < r; ++i) sv = fmaf(-Am[(o + r) * kN + o + i], x[i], sv);
-          x[r] = sv;
+          for (int i = 0; i < r; ++i) ar[i] = Am[(o + r) * kN + o + i];
+#pragma unroll
+          for (int i = 0; i < r; ++i) sv[i & 3] = fmaf(-ar[i], x[i], sv[i & 3]);
+          x[r] = (sv[0] + sv[1]) + (sv[2] + sv[3]);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tm[(o + r) * kN + o + jj] = x[r];
@@ -1787,21 +1800,31 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
         const int nb = 4 - d;
         for (int e = tid; e < nb * 256; e += kThr) {
           const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15, j = blk, i = j + d;
-          float g = 0.f;
-          for (int k = j; k < i; ++k)
+          float g[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int k = j; k < i; ++k) {
+            float av[16], tv[16];
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-              g = fmaf(Am[(16 * i + rr) * kN + 16 * k + m], Tm[(16 * k + m) * kN + 16 * j + cc], g);
-          Tm[rr * kN + 16 * (1 + blk) + cc] = g;  // G_ij in upper block (0, 1 + blk)
+            for (int m = 0; m < 16; ++m) {
+              av[m] = Am[(16 * i + rr) * kN + 16 * k + m];
+              tv[m] = Tm[(16 * k + m) * kN + 16 * j + cc];
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) g[m & 3] = fmaf(av[m], tv[m], g[m & 3]);
+          }
+          Tm[rr * kN + 16 * (1 + blk) + cc] = (g[0] + g[1]) + (g[2] + g[3]);  // G_ij in upper block (0, 1 + blk)
         }
         __syncthreads();
         for (int e = tid; e < nb * 256; e += kThr) {
           const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = blk + d;
-          float tv = 0.f;
+          float av[16], gv[16], tv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int m = 0; m < 16; ++m)
-            tv = fmaf(Tm[(16 * i + rr) * kN + 16 * i + m], Tm[m * kN + 16 * (1 + blk) + cc], tv);
-          Tm[(16 * i + rr) * kN + 16 * blk + cc] = -tv;
+          for (int m = 0; m < 16; ++m) {
+            av[m] = Tm[(16 * i + rr) * kN + 16 * i + m];
+            gv[m] = Tm[m * kN + 16 * (1 + blk) + cc];
+          }
+#pragma unroll
+          for (int m = 0; m < 16; ++m) tv[m & 3] = fmaf(av[m], gv[m], tv[m & 3]);
+          Tm[(16 * i + rr) * kN + 16 * blk + cc] = -((tv[0] + tv[1]) + (tv[2] + tv[3]));
         }
         __syncthreads();
       }
@@ -1931,7 +1954,7 @@ template <bool BWD>
 __global__ void __launch_bounds__(ctc::kThr) bwdc_chain_tc_kernel(CbArgs a) {
   using namespace ctc;
   extern __shared__ uint8_t ctc_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(tcu::align1024(ctc_raw));
+  Smem& sm = *reinterpret_cast<Smem*>(gtc::shared_align1024(ctc_raw));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, c0 = blockIdx.y * kSC;
   const int R = 16 * warp + (lane & 15), Cl = 16 * (lane >> 4), C = c0 + Cl;  // row, first column
