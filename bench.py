@@ -420,8 +420,10 @@ def run_backward(args, w):
                  dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32,
                  pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX)
     chunked = w.variant in (0, 1) and w.dk == 64 and w.dv == 64
-    grad_k = "bwdc_grad_tc_kernel" if w.dtype == "bf16" else "bwdc_grad_kernel"
-    kernel = (f"bwdc_prep_kernel + bwdc_fwd_chain_kernel + bwdc_bwd_chain_kernel + {grad_k} (whole call)"
+    chunk_k = ("bwdc_prep_tc_kernel + bwdc_chain_tc_kernel<0> + bwdc_chain_tc_kernel<1> + bwdc_grad_tc_kernel"
+               if w.dtype == "bf16" else
+               "bwdc_prep_kernel + bwdc_fwd_chain_kernel + bwdc_bwd_chain_kernel + bwdc_grad_kernel")
+    kernel = (f"{chunk_k} (whole call)"
               if chunked else "falcon_bwd_win_kernel" if (w.variant in (4, 5) or w.dk == 128)
               else "falcon_bwd_kernel")
     sets = []
