@@ -1061,25 +1061,25 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
 namespace gtc {
 constexpr int kImg = 64 * 128;
 enum {
-  I_X = 0, I_Q, I_DO,           // exact inputs
-  I_S0, I_S0L, I_DS1, I_DS1L,   // start state, end-state gradient
-  I_W, I_WL,                    // W, then dDelta
-  I_T, I_TL, I_DL, I_DLL,       // T; Delta
-  I_PD, I_PDL,                  // P (.) D, then dR
-  I_DG, I_DGL, I_DP, I_DPL, kImgs
+  I_X = 0, I_Q, I_DO,       // exact inputs
+  I_DL, I_S0, I_DS1,        // hi images: Delta (then diag(E) Delta), the start state, the end-state gradient
+  I_DLL, I_S0L, I_DS1L,     // their lo images
+  I_W, I_WL,                // W; then P (.) D; then dDelta; then dG | dP (one image each)
+  I_T, I_TL,                // T; then dR (then -diag(eta Gamma) dR)
+  kImgs
 };
-enum { A_0 = 0, A_XS0, A_QS0, A_QX, A_XDS1, A_G, A_DOS0, A_7, kAcc };  // 64 TMEM columns each
-enum { R_DGO = 0, R_EDE, R_DE, R_DGR, R_DEA, R_ROWM, R_SD, kRed };     // row sums, by column half
+enum { R_DGO = 0, R_EDE, R_DE, R_DGR, R_DEA, R_ROWM, R_SD, kRed };  // row sums, by column half
 struct Tail {
   GateSm gs;
   float red[kRed][2][kN];
   float colM[4][kN];  // column sums of M by row quarter
-  uint64_t bar;
+  uint64_t bar;       // the MMA steps
+  uint64_t ld;        // the bulk copies of the workspace's images
   uint32_t tmem;
   int pad;
 };
 constexpr size_t kSmem = 1024 + (size_t)kImgs * kImg + sizeof(Tail);
-static_assert(kAcc * 64 == 512, "the accumulators fill the TMEM of one CTA");
+static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
 // D (+)= op(A) op(B) over K = 64 (M = 64, N columns): the hi x hi term, then
 // hi x lo and lo x hi where that operand has a low part.  amn / bmn: the
@@ -1124,23 +1124,14 @@ __device__ __forceinline__ void put_split(uint8_t* hi, uint8_t* lo, int r, int c
 __device__ __forceinline__ uint8_t* shared_align1024(uint8_t* raw) {
   return raw + ((1024u - (tc::smem_u32(raw) & 1023u)) & 1023u);
 }
-// A 64 x 64 fp32 workspace matrix into 16 KB of shared memory by cp.async
-// (no wait): row r's 16-byte piece q at piece q ^ (r & 7) of the row, so that
-// eight consecutive rows read at one column are free of bank conflicts.
-__device__ __forceinline__ void cp_mat_sw(uint8_t* dst, const float* src) {
+// 16 fp32 values of row r, columns c0 .. c0 + 15, into one bf16 image
+__device__ __forceinline__ void put_one(uint8_t* im, int r, int c0, const float (&v)[16]) {
 #pragma unroll
-  for (int k = 0; k < kN * kN / 4 / kThr; ++k) {
-    const int i = threadIdx.x + kThr * k, r = i >> 4, q = i & 15;
-    cp16(dst + (r * 16 + (q ^ (r & 7))) * 16, src + r * kN + q * 4);
-  }
-}
-// 16 values of row r of such a matrix from column c0 (a multiple of 16)
-__device__ __forceinline__ void ld_sw16(float (&v)[16], const uint8_t* m, int r, int c0) {
+  for (int j = 0; j < 2; ++j) {
+    uint32_t ph[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int q = (c0 >> 2) + k;
-    const float4 f = *reinterpret_cast<const float4*>(m + (r * 16 + (q ^ (r & 7))) * 16);
-    v[4 * k] = f.x; v[4 * k + 1] = f.y; v[4 * k + 2] = f.z; v[4 * k + 3] = f.w;
+    for (int e = 0; e < 4; ++e) ph[e] = tcu::pack_bf16(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+    *reinterpret_cast<uint4*>(im + tcu::sw128(r, c0 + 8 * j)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
   }
 }
 // 16 values of an exact image's row r from column c0
@@ -1217,7 +1208,7 @@ __device__ __forceinline__ void st16(float* p, const float (&v)[16]) {
 
 }  // namespace gtc
 
-__global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
+__global__ void __launch_bounds__(kThr, 2) bwdc_grad_tc_kernel(CbArgs a) {
   using namespace gtc;
   extern __shared__ uint8_t gtc_raw[];
   uint8_t* base = shared_align1024(gtc_raw);
@@ -1236,55 +1227,40 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
   using Tin = __nv_bfloat16;
 
   if (warp == 0) {
-    tc::tmem_alloc(&tl.tmem, 512);
+    tc::tmem_alloc(&tl.tmem, 256);
     tc::tmem_relinquish();
   }
   if (tid == 32) {
     tc::mbar_init(&tl.bar, 1);
+    tc::mbar_init(&tl.ld, 1);
     tc::fence_mbar_init();
   }
-  // row sums: the two threads of a row in this warp, then one entry per column half
-  auto row_part = [&](int which, float v) {
-    v += __shfl_xor_sync(0xffffffffu, v, 16);
-    if (lane < 16) tl.red[which][half][R] = v;
-  };
-  auto row_sum = [&](int which, int r) { return tl.red[which][0][r] + tl.red[which][1][r]; };
-
-  // ---- loads, one round: the gates and the workspace's fp32 matrices by
-  // cp.async (into image slots that are free until later: S0 into Delta's,
-  // dS1 into P (.) D's, W into dG's, T into dP's, U into T's), keys, queries,
-  // output gradients as images, this thread's values
-  if (tid < (int)(sizeof(GateSm) / 16)) cp16(reinterpret_cast<float*>(&gs) + 4 * tid, wsgate(a, cg) + 4 * tid);
-  cp_mat_sw(img(I_DL), wsmat(a, cg, M_S0));
-  cp_mat_sw(img(I_PD), wsmat(a, cg, M_DS1));
-  if (reg) {
-    cp_mat_sw(img(I_DG), wsmat(a, cg, M_W));
-    cp_mat_sw(img(I_DP), wsmat(a, cg, M_T));
-    cp_mat_sw(img(I_T), wsmat(a, cg, M_U));
-  }
-  cp_commit();
-  load_xqdo(a, img(I_X), img(I_Q), img(I_DO), b, h, t0, pos, bh);
-  float vv[16];
-  load_row16(vv, a.v, a, b, h, t, C0);
-  cp_wait0();
-  __syncthreads();
-  {  // S0, dS1 and W as images
-    float s0[16], ds[16];
-    ld_sw16(s0, img(I_DL), R, C0);
-    ld_sw16(ds, img(I_PD), R, C0);
-    put_split(img(I_S0), img(I_S0L), R, C0, s0);
-    put_split(img(I_DS1), img(I_DS1L), R, C0, ds);
-    float sd = 0.f;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) sd = fmaf(s0[e], ds[e], sd);
-    row_part(R_SD, sd);
+  __syncthreads();  // the barriers are initialised
+  // ---- loads, one round: the workspace's images of S0, dS1, W and T by bulk
+  // copies, the gates by cp.async, keys, queries, output gradients as
+  // images, this thread's U and V
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&tl.ld, (reg ? 4u : 2u) * 2u * kImg);
+    const uint8_t* s0 = reinterpret_cast<const uint8_t*>(wsmat(a, cg, M_S0));
+    const uint8_t* ds = reinterpret_cast<const uint8_t*>(wsmat(a, cg, M_DS1));
+    tc::bulk_load(img(I_S0), s0, kImg, &tl.ld);
+    tc::bulk_load(img(I_S0L), s0 + kImg, kImg, &tl.ld);
+    tc::bulk_load(img(I_DS1), ds, kImg, &tl.ld);
+    tc::bulk_load(img(I_DS1L), ds + kImg, kImg, &tl.ld);
     if (reg) {
-      float w[16];
-      ld_sw16(w, img(I_DG), R, C0);
-      put_split(img(I_W), img(I_WL), R, C0, w);
+      tc::bulk_load(img(I_W), wsmat(a, cg, M_W), 2 * kImg, &tl.ld);
+      tc::bulk_load(img(I_T), wsmat(a, cg, M_T), 2 * kImg, &tl.ld);
     }
   }
+  if (tid < (int)(sizeof(GateSm) / 16)) cp16(reinterpret_cast<float*>(&gs) + 4 * tid, wsgate(a, cg) + 4 * tid);
+  cp_commit();
+  load_xqdo(a, img(I_X), img(I_Q), img(I_DO), b, h, t0, pos, bh);
+  float vv[16], u[16];
+  load_row16(vv, a.v, a, b, h, t, C0);
+  if (reg) ld16(u, wsmat(a, cg, M_U) + R * kN + C0);
   cp_wait0();
+  bool ok = tc::mbar_wait(&tl.ld, 0, a.wait_ns);
+  ok = !__syncthreads_or(!ok);
   tc::fence_proxy_async();
   tc::tc_fence_before();
   __syncthreads();
@@ -1299,8 +1275,21 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
   };
+  // row sums: the two threads of a row in this warp, then one entry per column half
+  auto row_part = [&](int which, float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    if (lane < 16) tl.red[which][half][R] = v;
+  };
+  auto row_sum = [&](int which, int r) { return tl.red[which][0][r] + tl.red[which][1][r]; };
+  // a row block of a split image pair, back in fp32 (hi + lo)
+  auto get_split = [&](float (&v)[16], int hi, int lo) {
+    float l[16];
+    get_row(v, img(hi), R, C0);
+    get_row(l, img(lo), R, C0);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] += l[e];
+  };
   uint32_t phase = 0;
-  bool ok = true;
   // every thread waits for the step's MMAs; all agree on the outcome
   auto wait_step = [&]() {
     const bool mine = tc::mbar_wait(&tl.bar, phase, a.wait_ns);
@@ -1320,27 +1309,29 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
   const float etaR = gs.eta[R], GamR = gs.Gam[R], ER = gs.E[R], gR = gs.g[R];
 
   do {
-    // ---- step 1: W S0, X S0, Q S0, Q X^T, X dS1, X X^T, dO S0^T
+    if (!ok) break;
+    {  // <S0, dS1> by rows
+      float s0[16], ds[16], sd = 0.f;
+      get_split(s0, I_S0, I_S0L);
+      get_split(ds, I_DS1, I_DS1L);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) sd = fmaf(s0[e], ds[e], sd);
+      row_part(R_SD, sd);
+    }
+    // ---- step 1: W S0, Q S0, Q X^T, X dS1
     if (tid == 0) {
-      if (reg) {
-        terms(acc(A_0), sa(I_W), sa(I_WL), true, false, sa(I_S0), sa(I_S0L), true, true, false);
-        terms(acc(A_XS0), sa(I_X), 0, false, false, sa(I_S0), sa(I_S0L), true, true, false);
-        terms(acc(A_G), sa(I_X), 0, false, false, sa(I_X), 0, false, false, false);
-      }
-      terms(acc(A_QS0), sa(I_Q), 0, false, false, sa(I_S0), sa(I_S0L), true, true, false);
-      terms(acc(A_QX), sa(I_Q), 0, false, false, sa(I_X), 0, false, false, false);
-      terms(acc(A_XDS1), sa(I_X), 0, false, false, sa(I_DS1), sa(I_DS1L), true, true, false);
-      terms(acc(A_DOS0), sa(I_DO), 0, false, false, sa(I_S0), sa(I_S0L), true, false, false);
+      if (reg) terms(acc(0), sa(I_W), sa(I_WL), true, false, sa(I_S0), sa(I_S0L), true, true, false);
+      terms(acc(1), sa(I_Q), 0, false, false, sa(I_S0), sa(I_S0L), true, true, false);
+      terms(acc(2), sa(I_Q), 0, false, false, sa(I_X), 0, false, false, false);
+      terms(acc(3), sa(I_X), 0, false, false, sa(I_DS1), sa(I_DS1L), true, true, false);
       tc::umma_commit(&tl.bar);
     }
-    float u[16];  // meanwhile: this thread's U (staged in T's slots)
-    if (reg) ld_sw16(u, img(I_T), R, C0);
     if (!wait_step()) break;
 
-    // ---- E1: Delta; dGamma through the output term; P (.) D; E dE
+    // ---- E1: Delta; dGamma through the output term; P (.) D (into W's slots); E dE
     float dl[16], pv[16];
     if (reg) {
-      tld(A_0, pv);
+      tld(0, pv);
 #pragma unroll
       for (int e = 0; e < 16; ++e) dl[e] = u[e] - pv[e];
     } else {
@@ -1351,33 +1342,34 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
     {
       float dov[16], s = 0.f;
       get_row(dov, img(I_DO), R, C0);
-      tld(A_QS0, pv);
+      tld(1, pv);
 #pragma unroll
       for (int e = 0; e < 16; ++e) s = fmaf(dov[e], pv[e], s);
       row_part(R_DGO, s);
     }
     {
       float pd[16];
-      tld(A_QX, pv);
+      tld(2, pv);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int cc = C0 + e;
         pd[e] = cc <= R ? __expf(gR - gs.g[cc]) * pv[e] : 0.f;
       }
-      put_split(img(I_PD), img(I_PDL), R, C0, pd);
+      put_split(img(I_W), img(I_WL), R, C0, pd);
     }
     {
       float s = 0.f;
-      tld(A_XDS1, pv);
+      tld(3, pv);
 #pragma unroll
       for (int e = 0; e < 16; ++e) s = fmaf(pv[e], dl[e], s);
       row_part(R_EDE, s);
     }
     step_barrier();
 
-    // ---- step 2: (P (.) D)^T dO
+    // ---- step 2: (P (.) D)^T dO, X S0
     if (tid == 0) {
-      terms(acc(A_7), sa(I_PD), sa(I_PDL), true, true, sa(I_DO), 0, false, true, false);
+      terms(acc(0), sa(I_W), sa(I_WL), true, true, sa(I_DO), 0, false, true, false);
+      if (reg) terms(acc(1), sa(I_X), 0, false, false, sa(I_S0), sa(I_S0L), true, true, false);
       tc::umma_commit(&tl.bar);
     }
     if (!wait_step()) break;
@@ -1385,28 +1377,24 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
     float dd[16];
     {
       float p2[16];
-      tld(A_7, pv);
-      tld(A_XDS1, p2);
+      tld(0, pv);
+      tld(3, p2);
 #pragma unroll
       for (int e = 0; e < 16; ++e) dd[e] = pv[e] + ER * p2[e];
     }
     if (reg) {
-      put_split(img(I_W), img(I_WL), R, C0, dd);
-      {  // T as images (its slots held U until every thread read it, before E1's barrier)
-        float tt[16];
-        ld_sw16(tt, img(I_DP), R, C0);
-        put_split(img(I_T), img(I_TL), R, C0, tt);
-      }
+      put_split(img(I_W), img(I_WL), R, C0, dd);  // dDelta (P (.) D is consumed)
       step_barrier();
-      // ---- step 3: dR = T^T dDelta
+      // ---- step 3: dR = T^T dDelta; G = X X^T
       if (tid == 0) {
-        terms(acc(A_0), sa(I_T), sa(I_TL), true, true, sa(I_W), sa(I_WL), true, true, false);
+        terms(acc(0), sa(I_T), sa(I_TL), true, true, sa(I_W), sa(I_WL), true, true, false);
+        terms(acc(3), sa(I_X), 0, false, false, sa(I_X), 0, false, false, false);
         tc::umma_commit(&tl.bar);
       }
       if (!wait_step()) break;
-      tld(A_0, dd);
+      tld(0, dd);
     }
-    // ---- E3 (dd holds dR): dV, d eta and dGamma through the residual
+    // ---- E3 (dd holds dR): dV, d eta and dGamma through the residual; dR into T's slots
     if (t < a.T) {
       float v8[8];
 #pragma unroll
@@ -1419,7 +1407,7 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
     {
       float de = 0.f, dgr = 0.f;
       if (reg) {
-        tld(A_XS0, pv);
+        tld(1, pv);  // X S0
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           de = fmaf(dd[e], vv[e] - GamR * pv[e], de);
@@ -1432,27 +1420,25 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
       row_part(R_DE, de);
       row_part(R_DGR, dgr);
     }
-    put_split(img(I_PD), img(I_PDL), R, C0, dd);  // dR
+    put_split(img(I_T), img(I_TL), R, C0, dd);
     step_barrier();
 
-    // ---- step 4: dR Delta^T, dO Delta^T, dR S0^T
+    // ---- step 4: dR Delta^T, dO Delta^T
     if (tid == 0) {
-      if (reg) {
-        terms(acc(A_0), sa(I_PD), sa(I_PDL), true, false, sa(I_DL), sa(I_DLL), true, false, false);
-        terms(acc(A_XDS1), sa(I_PD), sa(I_PDL), true, false, sa(I_S0), sa(I_S0L), true, false, false);
-      }
-      terms(acc(A_QS0), sa(I_DO), 0, false, false, sa(I_DL), sa(I_DLL), true, false, false);
+      if (reg) terms(acc(0), sa(I_T), sa(I_TL), true, false, sa(I_DL), sa(I_DLL), true, false, false);
+      terms(acc(1), sa(I_DO), 0, false, false, sa(I_DL), sa(I_DLL), true, false, false);
       tc::umma_commit(&tl.bar);
     }
     if (!wait_step()) break;
-    // ---- E4: dG (A = diag(eta) L), M = D (.) dD, dP
+    // ---- E4: dG (A = diag(eta) L), M = D (.) dD, dP; the row scales of
+    // step 5's last terms applied to the Delta and dR images in place
     {
       float dod[16], qx[16], dra[16], gg[16], m[16], dp[16], dg[16];
-      tld(A_QS0, dod);
-      tld(A_QX, qx);
+      tld(1, dod);
+      tld(2, qx);
       if (reg) {
-        tld(A_0, dra);
-        tld(A_G, gg);
+        tld(0, dra);
+        tld(3, gg);
       }
       float dea = 0.f, rm = 0.f;
 #pragma unroll
@@ -1487,20 +1473,38 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
         }
       }
       tl.colM[quad][C0 + (lane & 15)] = m[0];
-      if (reg) put_split(img(I_DG), img(I_DGL), R, C0, dg);
-      put_split(img(I_DP), img(I_DPL), R, C0, dp);
+      // dG and dP feed only dq and dk (bf16 results): one bf16 image each
+      put_one(img(I_W), R, C0, dg);
+      put_one(img(I_WL), R, C0, dp);
+    }
+    {
+      float v[16];
+      get_split(v, I_DL, I_DLL);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] *= ER;
+      put_split(img(I_DL), img(I_DLL), R, C0, v);  // diag(E) Delta
+      if (reg) {
+        get_split(v, I_T, I_TL);
+        const float s = -etaR * GamR;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] *= s;
+        put_split(img(I_T), img(I_TL), R, C0, v);  // -diag(eta Gamma) dR
+      }
     }
     step_barrier();
 
-    // ---- step 5: dX = (dG + dG^T) X + dP^T Q (- and + terms below); dP X; Delta dS1^T
+    // ---- step 5: dX = dP^T Q + (dG + dG^T) X + diag(E) Delta dS1^T - diag(eta Gamma) dR S0^T;
+    // dP X; dO S0^T
     if (tid == 0) {
-      terms(acc(A_7), sa(I_DP), sa(I_DPL), true, true, sa(I_Q), 0, false, true, false);
+      terms(acc(0), sa(I_WL), 0, false, true, sa(I_Q), 0, false, true, false);
       if (reg) {
-        terms(acc(A_7), sa(I_DG), sa(I_DGL), true, false, sa(I_X), 0, false, true, true);
-        terms(acc(A_7), sa(I_DG), sa(I_DGL), true, true, sa(I_X), 0, false, true, true);
+        terms(acc(0), sa(I_W), 0, false, false, sa(I_X), 0, false, true, true);
+        terms(acc(0), sa(I_W), 0, false, true, sa(I_X), 0, false, true, true);
+        terms(acc(0), sa(I_T), sa(I_TL), true, false, sa(I_S0), sa(I_S0L), true, false, true);
       }
-      terms(acc(A_QX), sa(I_DP), sa(I_DPL), true, false, sa(I_X), 0, false, true, false);
-      terms(acc(A_G), sa(I_DL), sa(I_DLL), true, false, sa(I_DS1), sa(I_DS1L), true, false, false);
+      terms(acc(0), sa(I_DL), sa(I_DLL), true, false, sa(I_DS1), sa(I_DS1L), true, false, true);
+      terms(acc(1), sa(I_WL), 0, false, false, sa(I_X), 0, false, true, false);
+      terms(acc(2), sa(I_DO), 0, false, false, sa(I_S0), sa(I_S0L), true, false, false);
       tc::umma_commit(&tl.bar);
     }
     if (!wait_step()) break;
@@ -1508,8 +1512,8 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
     // only the stores are limited to the call's rows)
     {
       float p1[16], p2[16];
-      tld(A_DOS0, p1);
-      tld(A_QX, p2);
+      tld(2, p1);
+      tld(1, p2);
 #pragma unroll
       for (int e = 0; e < 16; ++e) p1[e] = GamR * p1[e] + p2[e];
       if (t < a.T) {
@@ -1520,17 +1524,11 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
     {
       const float deta = row_sum(R_DE, R) + row_sum(R_DEA, R);
       const float dn = gs.ex[R] != 0.f ? -deta * etaR / (a.eps + gs.nrm[R]) : 0.f;
-      float xr[16], p3[16], p4[16], p5[16];
+      float xr[16], p3[16];
       get_row(xr, img(I_X), R, C0);
-      tld(A_7, p3);
-      tld(A_G, p4);
-      if (reg) tld(A_XDS1, p5);
+      tld(0, p3);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float x = p3[e] + ER * p4[e] + 2.f * dn * xr[e];
-        if (reg) x -= etaR * GamR * p5[e];
-        p3[e] = x;
-      }
+      for (int e = 0; e < 16; ++e) p3[e] = fmaf(2.f * dn, xr[e], p3[e]);
       if (t < a.T) {
         Tin* dst = nullptr;
         if (t - a.shift >= 0) dst = reinterpret_cast<Tin*>(a.dk) + (((size_t)b * a.T + (t - a.shift)) * a.H + h) * kN;
@@ -1586,7 +1584,7 @@ __global__ void __launch_bounds__(kThr, 1) bwdc_grad_tc_kernel(CbArgs a) {
   if (!ok && tid == 0) atomicExch(a.status, tcu::kStatusTimeout);
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tl.tmem, 512);
+  if (warp == 0) tc::tmem_dealloc(tl.tmem, 256);
 }
 
 // ---------------------------------------------------------------- (a) on tcgen05
@@ -1841,7 +1839,8 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
           tt[4 * k] = f.x; tt[4 * k + 1] = f.y; tt[4 * k + 2] = f.z; tt[4 * k + 3] = f.w;
         }
         gtc::put_split(img(I_T), img(I_TL), R, C0, tt);
-        gtc::st16(wsmat(a, cg, M_T) + R * kN + C0, tt);
+        uint8_t* gt = reinterpret_cast<uint8_t*>(wsmat(a, cg, M_T));
+        gtc::put_split(gt, gt + gtc::kImg, R, C0, tt);
       }
       __syncthreads();  // A and T read: their slots take the scaled operands of step 2
       {
@@ -1871,7 +1870,10 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
       float p[16];
       if (reg) {
         tld(0, p);
-        gtc::st16(wsmat(a, cg, M_W) + R * kN + C0, p);
+        {
+          uint8_t* gw = reinterpret_cast<uint8_t*>(wsmat(a, cg, M_W));
+          gtc::put_split(gw, gw + gtc::kImg, R, C0, p);
+        }
         gtc::put_split(img(I_M1), img(I_M1L), R, C0, p);
         tld(1, p);
         gtc::st16(wsmat(a, cg, M_U) + R * kN + C0, p);
@@ -1995,7 +1997,10 @@ __global__ void __launch_bounds__(ctc::kThr) bwdc_chain_tc_kernel(CbArgs a) {
   bool ok = true;
   for (int n = 0; n < a.NC; ++n) {
     const size_t cg = base + chunk(n);
-    gtc::st16(wsmat(a, cg, BWD ? M_DS1 : M_S0) + R * kN + C, S);
+    {  // the chunk's state out, as hi | lo images
+      uint8_t* gi = reinterpret_cast<uint8_t*>(wsmat(a, cg, BWD ? M_DS1 : M_S0));
+      gtc::put_split(gi, gi + gtc::kImg, R, C, S);
+    }
     float nxt[16];
     if (n + 1 < a.NC) gtc::ld16(nxt, wsmat(a, base + chunk(n + 1), OFF) + R * kN + C);
     if (reg) {
