@@ -1206,6 +1206,15 @@ __device__ __forceinline__ void st16(float* p, const float (&v)[16]) {
     reinterpret_cast<float4*>(p)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
 }
 
+// Element (r, c) of a 64 x 64 fp32 matrix in shared memory whose 16-byte
+// pieces are permuted within each row (piece q at q ^ (r & 7)): eight
+// consecutive rows read or written at one column hit different banks.
+__device__ __forceinline__ int swz(int r, int c) { return r * kN + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
+// the four values (r, c .. c + 3), c a multiple of 4
+__device__ __forceinline__ float4 ld4s(const float* m, int r, int c) {
+  return *reinterpret_cast<const float4*>(m + swz(r, c));
+}
+__device__ __forceinline__ void st4s(float* m, int r, int c, float4 v) { *reinterpret_cast<float4*>(m + swz(r, c)) = v; }
 }  // namespace gtc
 
 __global__ void __launch_bounds__(kThr, 2) bwdc_grad_tc_kernel(CbArgs a) {
@@ -1748,24 +1757,28 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
       }
     }
     if (!wait_step()) break;
-    // ---- E1: P (.) D as images; A = diag(eta) (D (.) X X^T) (strictly lower) as fp32 rows
+    // ---- E1: P (.) D as images; A = diag(eta) (D (.) X X^T) (strictly lower)
+    // as fp32 rows (16-byte pieces permuted, gtc::swz); both accumulators in
+    // one TMEM round trip, the decay mask formed once
     {
-      float p[16];
-      tld(1, p);
+      uint32_t rp[16], rg[16];
+      tc::tmem_ld16x2_16(tmem + lane_off + (uint32_t)(64 * 1 + 32 * half), rp);
+      if (reg) tc::tmem_ld16x2_16(tmem + lane_off + (uint32_t)(64 * 0 + 32 * half), rg);
+      tc::tmem_wait_ld();
+      float p[16], am[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int cc = C0 + e;
-        p[e] = cc <= R ? __expf(gR - gs.g[cc]) * p[e] : 0.f;
+        const float D = cc <= R ? __expf(gR - gs.g[cc]) : 0.f;
+        p[e] = D * __uint_as_float(rp[e]);
+        am[e] = cc < R ? etaR * D * __uint_as_float(rg[e]) : 0.f;
       }
       gtc::put_split(img(I_PD), img(I_PDL), R, C0, p);
       if (reg) {
-        tld(0, p);
+        float* Aw = reinterpret_cast<float*>(img(I_M1));
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int cc = C0 + e;
-          p[e] = cc < R ? etaR * __expf(gR - gs.g[cc]) * p[e] : 0.f;
-        }
-        gtc::st16(reinterpret_cast<float*>(img(I_M1)) + R * kN + C0, p);  // A, fp32 rows
+        for (int k = 0; k < 4; ++k)
+          gtc::st4s(Aw, R, C0 + 4 * k, make_float4(am[4 * k], am[4 * k + 1], am[4 * k + 2], am[4 * k + 3]));
       }
     }
     step_barrier();
@@ -1778,6 +1791,7 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
       // the G blocks kept in T's upper blocks, which are zeroed at the end.
       const float* Am = reinterpret_cast<const float*>(img(I_M1));
       float* Tm = reinterpret_cast<float*>(img(I_MX));
+      using gtc::swz;
       if (tid < kN) {
         const int o = 16 * (tid >> 4), jj = tid & 15;
         float x[16];
@@ -1785,57 +1799,70 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
         for (int r = 0; r < 16; ++r) {
           float ar[16], sv[4] = {r == jj ? 1.f : 0.f, 0.f, 0.f, 0.f};  // the row's loads first, four chains
 #pragma unroll
-          for (int i = 0; i < r; ++i) ar[i] = Am[(o + r) * kN + o + i];
+          for (int i = 0; i < r; ++i) ar[i] = Am[swz(o + r, o + i)];
 #pragma unroll
           for (int i = 0; i < r; ++i) sv[i & 3] = fmaf(-ar[i], x[i], sv[i & 3]);
           x[r] = (sv[0] + sv[1]) + (sv[2] + sv[3]);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tm[(o + r) * kN + o + jj] = x[r];
+        for (int r = 0; r < 16; ++r) Tm[swz(o + r, o + jj)] = x[r];
       }
       __syncthreads();
+      // levels: a thread takes row rr and columns 4 cq .. 4 cq + 3 of a block
       for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;
-        for (int e = tid; e < nb * 256; e += kThr) {
-          const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15, j = blk, i = j + d;
+        const int blk = tid >> 6, rr = (tid >> 2) & 15, cq = tid & 3;
+        if (blk < nb) {
+          const int j = blk, i = j + d;
           float g[4] = {0.f, 0.f, 0.f, 0.f};
           for (int k = j; k < i; ++k) {
-            float av[16], tv[16];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-              av[m] = Am[(16 * i + rr) * kN + 16 * k + m];
-              tv[m] = Tm[(16 * k + m) * kN + 16 * j + cc];
+            for (int m4 = 0; m4 < 4; ++m4) {
+              const float4 a4 = gtc::ld4s(Am, 16 * i + rr, 16 * k + 4 * m4);
+              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+              for (int mm = 0; mm < 4; ++mm) {
+                const float4 t4 = gtc::ld4s(Tm, 16 * k + 4 * m4 + mm, 16 * j + 4 * cq);
+                g[0] = fmaf(av[mm], t4.x, g[0]);
+                g[1] = fmaf(av[mm], t4.y, g[1]);
+                g[2] = fmaf(av[mm], t4.z, g[2]);
+                g[3] = fmaf(av[mm], t4.w, g[3]);
+              }
             }
-#pragma unroll
-            for (int m = 0; m < 16; ++m) g[m & 3] = fmaf(av[m], tv[m], g[m & 3]);
           }
-          Tm[rr * kN + 16 * (1 + blk) + cc] = (g[0] + g[1]) + (g[2] + g[3]);  // G_ij in upper block (0, 1 + blk)
+          gtc::st4s(Tm, rr, 16 * (1 + blk) + 4 * cq, make_float4(g[0], g[1], g[2], g[3]));  // G_ij in upper block (0, 1 + blk)
         }
         __syncthreads();
-        for (int e = tid; e < nb * 256; e += kThr) {
-          const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = blk + d;
-          float av[16], gv[16], tv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (blk < nb) {
+          const int i = blk + d;
+          float tv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            av[m] = Tm[(16 * i + rr) * kN + 16 * i + m];
-            gv[m] = Tm[m * kN + 16 * (1 + blk) + cc];
+          for (int m4 = 0; m4 < 4; ++m4) {
+            const float4 a4 = gtc::ld4s(Tm, 16 * i + rr, 16 * i + 4 * m4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+              const float4 g4 = gtc::ld4s(Tm, 4 * m4 + mm, 16 * (1 + blk) + 4 * cq);
+              tv[0] = fmaf(av[mm], g4.x, tv[0]);
+              tv[1] = fmaf(av[mm], g4.y, tv[1]);
+              tv[2] = fmaf(av[mm], g4.z, tv[2]);
+              tv[3] = fmaf(av[mm], g4.w, tv[3]);
+            }
           }
-#pragma unroll
-          for (int m = 0; m < 16; ++m) tv[m & 3] = fmaf(av[m], gv[m], tv[m & 3]);
-          Tm[(16 * i + rr) * kN + 16 * blk + cc] = -((tv[0] + tv[1]) + (tv[2] + tv[3]));
+          gtc::st4s(Tm, 16 * i + rr, 16 * blk + 4 * cq, make_float4(-tv[0], -tv[1], -tv[2], -tv[3]));
         }
         __syncthreads();
       }
       for (int e = tid; e < 6 * 256; e += kThr) {  // the upper blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
         const int ub = e >> 8, bi = ub < 3 ? 0 : (ub < 5 ? 1 : 2), bj = ub < 3 ? ub + 1 : (ub < 5 ? ub - 1 : 3);
-        Tm[(16 * bi + ((e >> 4) & 15)) * kN + 16 * bj + (e & 15)] = 0.f;
+        Tm[swz(16 * bi + ((e >> 4) & 15), 16 * bj + (e & 15))] = 0.f;
       }
       __syncthreads();
       {  // T as images and into the workspace
         float tt[16];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float4 f = reinterpret_cast<const float4*>(Tm + R * kN + C0)[k];
+          const float4 f = gtc::ld4s(Tm, R, C0 + 4 * k);
           tt[4 * k] = f.x; tt[4 * k + 1] = f.y; tt[4 * k + 2] = f.z; tt[4 * k + 3] = f.w;
         }
         gtc::put_split(img(I_T), img(I_TL), R, C0, tt);
