@@ -420,7 +420,7 @@ def run_backward(args, w):
                  dtype=F.FALCON_BF16 if w.dtype == "bf16" else F.FALCON_F32,
                  pairing=F.FALCON_PAIR_SAME_STEP if w.pairing == "same" else F.FALCON_PAIR_PREFIX)
     chunked = w.variant in (0, 1) and w.dk == 64 and w.dv == 64
-    chunk_k = ("bwdc_prep_tc_kernel + bwdc_chain_tc_kernel<0> + bwdc_chain_tc_kernel<1> + bwdc_grad_tc_kernel"
+    chunk_k = ("bwdc_prep_tc_kernel + bwdc_chain_tc_kernel (both chains) + bwdc_grad_tc_kernel"
                if w.dtype == "bf16" else
                "bwdc_prep_kernel + bwdc_fwd_chain_kernel + bwdc_bwd_chain_kernel + bwdc_grad_kernel")
     kernel = (f"{chunk_k} (whole call)"

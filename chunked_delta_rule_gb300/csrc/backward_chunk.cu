@@ -1958,8 +1958,9 @@ __global__ void __launch_bounds__(kThr, 2) bwdc_prep_tc_kernel(CbArgs a) {
 
 
 // ---------------------------------------------------------------- (b), (c) on tcgen05
-// The chains for bf16 inputs, one product per chunk step with the transition
-// and offset formed by the preparation:
+// The chains for bf16 inputs (one launch, blockIdx.z the direction: the two
+// read only the preparation's results), one product per chunk step with the
+// transition and offset formed by the preparation:
 //   forward   S_{c+1} = A_c S_c + b_c       (S_c out: the chunk's start state),
 //   backward  dS_c = A_c^T dS_{c+1} + Y_c   (dS_{c+1} out: its end-state gradient),
 // the backward reading the same images MN-major; additive: A_c = Gamma_63 I.
@@ -1979,9 +1980,9 @@ struct Smem {
 constexpr size_t kSmem = 1024 + sizeof(Smem);
 }  // namespace ctc
 
-template <bool BWD>
 __global__ void __launch_bounds__(ctc::kThr) bwdc_chain_tc_kernel(CbArgs a) {
   using namespace ctc;
+  const bool BWD = blockIdx.z != 0;  // the two chains are independent: one launch runs both
   extern __shared__ uint8_t ctc_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(gtc::shared_align1024(ctc_raw));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -2117,11 +2118,8 @@ int launch_bwdc_t(const CbArgs& a, cudaStream_t s) {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FALCON_ERR_CUDA;
   if constexpr (sizeof(Tin) == 2) {
-    if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_chain_tc_kernel<false>), ctc::kSmem) ||
-        !set_smem_limit(reinterpret_cast<const void*>(bwdc_chain_tc_kernel<true>), ctc::kSmem))
-      return FALCON_ERR_CUDA;
-    bwdc_chain_tc_kernel<false><<<dim3(a.B * a.H, kN / ctc::kSC), ctc::kThr, ctc::kSmem, s>>>(a);
-    bwdc_chain_tc_kernel<true><<<dim3(a.B * a.H, kN / ctc::kSC), ctc::kThr, ctc::kSmem, s>>>(a);
+    if (!set_smem_limit(reinterpret_cast<const void*>(bwdc_chain_tc_kernel), ctc::kSmem)) return FALCON_ERR_CUDA;
+    bwdc_chain_tc_kernel<<<dim3(a.B * a.H, kN / ctc::kSC, 2), ctc::kThr, ctc::kSmem, s>>>(a);
   } else {
     const int st = (long)a.B * a.H * (kN / 16) <= 2L * sms ? launch_chains<16>(a, s) : launch_chains<32>(a, s);
     if (st != FALCON_OK) return st;
