@@ -18,16 +18,22 @@
 //   dX = (dG + dG^T) X - diag(eta Gamma) dR S0^T + dP^T Q + diag(E) Delta dS1^T + 2 dn x,
 //   dG = -(diag(eta) dR Delta^T) (.) D (i < r),
 // and the log-decay gradients from Gamma, E and D (row minus column sums of
-// D (.) dD), summed back over the chunk's steps.  Four kernels:
-//  (a) bwdc_prep_kernel, per chunk: gates, T, W, U, diag(E) X and the chain's
-//      constant Y = Q^T diag(Gamma) dO - W^T (P (.) D)^T dO, into the workspace;
-//  (b) bwdc_fwd_chain_kernel, per (b, h, 16 or 32 value columns): chunk start states;
-//  (c) bwdc_bwd_chain_kernel, per (b, h, 16 or 32 value columns): dS at chunk ends;
-//  (d) bwdc_grad_kernel, per chunk: every gradient.
-// The 64 x 64 products read fp32 operands from shared memory and run on the
-// tensor cores as warp-level m16n8k8 tf32 products with the three-term split
-// of each operand (hi + lo), which keeps their error at the level of fp32
-// accumulation; the element-wise work and the reductions stay in fp32.
+// D (.) dD), summed back over the chunk's steps.  With the chunk transition
+// A = Gamma_63 I - (diag(E) X)^T W and offset b = (diag(E) X)^T U both chains
+// are one product a step: S1 = A S0 + b, dS0 = A^T dS1 + Y.
+//
+// bf16 inputs, every product on tcgen05 (the sections "on tcgen05" below):
+//  (a) bwdc_prep_tc_kernel, per chunk: gates, T, W, U, Y, b, and A as images;
+//  (b, c) bwdc_chain_tc_kernel, per (b, h, 32 value columns) and direction
+//      (both chains in one launch): chunk start states, end-state gradients;
+//  (d) bwdc_grad_tc_kernel, per chunk: every gradient.
+// fp32 inputs (tolerance 1e-3, operands not exact in bf16) keep the first
+// forms: bwdc_prep_kernel, bwdc_fwd_chain_kernel / bwdc_bwd_chain_kernel
+// (two products a step, from W and diag(E) X), bwdc_grad_kernel, whose
+// 64 x 64 products read fp32 operands from shared memory and run as
+// warp-level m16n8k8 tf32 MMAs with the three-term split of each operand
+// (hi + lo), which keeps their error at the level of fp32 accumulation.
+// The element-wise work and the reductions stay in fp32 in both forms.
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -1057,7 +1063,8 @@ __global__ void __launch_bounds__(kThr) bwdc_grad_kernel(CbArgs a) {
 // transposed copy.  A thread owns one row and 16 columns of every 64 x 64
 // result (an M = 64 accumulator keeps row 16 q + l in TMEM lane 32 q + l),
 // so the element-wise work runs in registers and each result is written
-// back as images straight from them.
+// back as images straight from them.  Thirteen image slots, reused as their
+// images die, and four 64-column accumulators: two CTAs share an SM.
 namespace gtc {
 constexpr int kImg = 64 * 128;
 enum {
