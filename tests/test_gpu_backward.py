@@ -4,7 +4,8 @@ and d = 128 are in test_gpu_backward_window.py): every gradient
 element by element, for Falcon-1/1A/2/2A, both pairings, bf16 and fp32,
 d = 32 and 64, carried state / key / positions, clamped decays, the empty
 and one-step sequences, block boundaries (64 steps) and a ragged tail; and,
-at the full 8 x 2048 x 12 d64 size, sampled heads computed one by one."""
+at the full 8 x 2048 x 12 d64 size and over 16384 steps (256 chunks), sampled
+heads computed one by one."""
 
 from __future__ import annotations
 
@@ -132,6 +133,29 @@ def test_backward_rejects_window_past_the_limit(F):
     with pytest.raises(F.FalconError) as e:
         F.backward(params_for(F, w), x["q"], x["k"], x["v"], x["beta"], x["lam"], c["dO"], None)
     assert e.value.code == -2
+
+
+def test_backward_long_sequence_sampled_head(F):
+    """Falcon-1, 1 x 16384 x 2 heads, d = 64, bf16: 256 chunks, so the chains
+    carry their products of split-bf16 operands (transition and state) through
+    256 steps; one head is recomputed by the oracle, the gradient of the
+    (zero) start state included."""
+    w = wl(FALCON_1, T=16384, B=1, H=2, seed=811)
+    x = make_inputs(w, device="cuda")
+    c = make_cotangents(w, 11, device="cuda")
+    g = F.backward(params_for(F, w), x["q"], x["k"], x["v"], x["beta"], x["lam"], c["dO"],
+                   c["dS_final"])
+    torch.cuda.synchronize()
+    xn = to_np(x)
+    cn = to_np(c)
+    h = 1
+    sl = lambda a: a[:, :, h:h + 1]
+    ref = oracle.recurrent_vjp(sl(xn["q"]), sl(xn["k"]), sl(xn["v"]), sl(xn["beta"]), sl(xn["lam"]),
+                               w.variant, sl(cn["dO"]), cn["dS_final"][:, h:h + 1], w.eps, w.eps_gamma,
+                               carry={"S": np.zeros((1, 1, w.dk, w.dv))})
+    gs = {n: g[n][:, :, h:h + 1] for n in ("dq", "dk", "dv", "dbeta", "dlam")}
+    gs["dS_in"] = g["dS_in"][:, h:h + 1]
+    check(w, gs, ref, names=("dq", "dk", "dv", "dbeta", "dlam", "dS_in"))
 
 
 @pytest.mark.parametrize("variant", [FALCON_1, FALCON_1A])
