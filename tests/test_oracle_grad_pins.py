@@ -11,6 +11,9 @@ G3  a clamped decay passes no gradient to lambda, and a step whose pair does
 G4  the window variants (Falcon-3/3A): G1 and G2 with a carried window ring
     whose slots hold existing and missing pairs (the gradient of every ring
     entry included), and W = 1 gives Falcon-1's / 1A's gradients
+G5  closed forms: Falcon-1A without decay and with same-step pairs is causal
+    linear attention weighted by eta, o_t = sum_{s<=t} eta_s (q_t . k_s) v_s,
+    whose value, query and beta gradients are written out with a causal mask
 """
 
 import numpy as np
@@ -179,3 +182,32 @@ def test_g4_window_one_is_the_one_pair_gradient(pair):
     g1 = O.recurrent_vjp(**x, variant=pair[1], do=do, carry=carry)
     for n in ("dq", "dk", "dv", "dbeta", "dlam", "dS_in", "dk_prev"):
         assert np.abs(g3[n] - g1[n]).max() <= 1e-13 * max(1.0, np.abs(g1[n]).max()), n
+
+
+def test_g5_linear_attention_closed_forms():
+    """lambda = 0 gives gamma = 1 (no decay), and Falcon-1A's additive write
+    with same-step pairs accumulates S_t = sum_{s<=t} eta_s k_s v_s^T, so
+    o_t = S_t^T q_t = sum_{s<=t} eta_s (q_t . k_s) v_s with eta_s =
+    beta_s / (eps + |k_s|^2) [FW Falcon 家族; JC Falcon家族六个变体各管一段].
+    For L = <o, dO>, with A_ts = (q_t . k_s) for s <= t (else 0):
+      dv_s = eta_s sum_t A_ts do_t,          dq_t = sum_{s<=t} eta_s (do_t . v_s) k_s,
+      dbeta_s = sum_t A_ts (v_s . do_t) / (eps + |k_s|^2)."""
+    rng = np.random.default_rng(71)
+    B, T, H, d = 1, 12, 2, 5
+    x = inputs(rng, B, T, H, d, d, False)
+    x["lam"] = np.zeros((B, T, H))
+    do = rng.standard_normal((B, T, H, d))
+    eps = 1e-6
+    g = O.recurrent_vjp(x["q"], x["k"], x["v"], x["beta"], x["lam"], O.FALCON_1A, do, None, eps, 1e-3,
+                        pairing="same")
+    for h in range(H):
+        q, k, v, dO = (a[0, :, h] for a in (x["q"], x["k"], x["v"], do))
+        den = eps + (k * k).sum(-1)
+        eta = x["beta"][0, :, h] / den
+        A = np.tril(q @ k.T)                       # A[t, s] = q_t . k_s, s <= t
+        dv = eta[:, None] * (A.T @ dO)
+        dq = np.tril(dO @ v.T) @ (eta[:, None] * k)
+        dbeta = (A * (dO @ v.T)).sum(0) / den
+        assert np.allclose(g["dv"][0, :, h], dv, rtol=1e-10, atol=1e-12)
+        assert np.allclose(g["dq"][0, :, h], dq, rtol=1e-10, atol=1e-12)
+        assert np.allclose(g["dbeta"][0, :, h], dbeta, rtol=1e-10, atol=1e-12)
