@@ -13,7 +13,8 @@ G4  the window variants (Falcon-3/3A): G1 and G2 with a carried window ring
     entry included), and W = 1 gives Falcon-1's / 1A's gradients
 G5  closed forms: Falcon-1A without decay and with same-step pairs is causal
     linear attention weighted by eta, o_t = sum_{s<=t} eta_s (q_t . k_s) v_s,
-    whose value, query and beta gradients are written out with a causal mask
+    whose value, query, beta, key, carried-state and decay gradients are
+    written out with causal masks
 """
 
 import numpy as np
@@ -211,3 +212,43 @@ def test_g5_linear_attention_closed_forms():
         assert np.allclose(g["dv"][0, :, h], dv, rtol=1e-10, atol=1e-12)
         assert np.allclose(g["dq"][0, :, h], dq, rtol=1e-10, atol=1e-12)
         assert np.allclose(g["dbeta"][0, :, h], dbeta, rtol=1e-10, atol=1e-12)
+
+
+def test_g5_linear_attention_closed_forms_keys_state_decay():
+    """The same case with a carried state S_in (o_t gains S_in^T q_t) and an
+    end-state cotangent dS_final (S_T = S_in + sum_s eta_s k_s v_s^T): the key
+    gradient, with the eta term,
+      dk_s = eta_s (sum_t (v_s . do_t) q_t + dS_final v_s)
+             - 2 beta_s k_s / (eps + |k_s|^2)^2 (sum_t A_ts (v_s . do_t) + k_s^T dS_final v_s),
+    the carried state's gradient is dS_in = sum_t q_t do_t^T + dS_final, and
+    the decay gradient at gamma = 1 (inside the clamp) is dlambda_t = -dgamma_t,
+      dgamma_t = <sum_{u>=t} q_u do_u^T + dS_final, S_{t-1}>,
+      S_{t-1} = S_in + sum_{s<t} eta_s k_s v_s^T."""
+    rng = np.random.default_rng(72)
+    B, T, H, d = 1, 10, 1, 4
+    x = inputs(rng, B, T, H, d, d, False)
+    x["lam"] = np.zeros((B, T, H))
+    do = rng.standard_normal((B, T, H, d))
+    dSf = rng.standard_normal((B, H, d, d))
+    S_in = 0.5 * rng.standard_normal((B, H, d, d))
+    eps = 1e-6
+    g = O.recurrent_vjp(x["q"], x["k"], x["v"], x["beta"], x["lam"], O.FALCON_1A, do, dSf, eps, 1e-3,
+                        carry={"S": S_in}, pairing="same")
+    q, k, v, dO = (a[0, :, 0] for a in (x["q"], x["k"], x["v"], do))
+    beta = x["beta"][0, :, 0]
+    den = eps + (k * k).sum(-1)
+    eta = beta / den
+    A = np.tril(q @ k.T)
+    VD = dO @ v.T                                   # VD[t, s] = do_t . v_s
+    Sv = v @ dSf[0, 0].T                             # Sv[s] = dS_final v_s
+    kSv = (k * Sv).sum(-1)                           # k_s^T dS_final v_s
+    dk = (eta[:, None] * (np.tril(VD).T @ q + Sv)
+          - (2 * beta / den ** 2)[:, None] * k * ((A * VD).sum(0) + kSv)[:, None])
+    assert np.allclose(g["dk"][0, :, 0], dk, rtol=1e-9, atol=1e-11)
+    assert np.allclose(g["dS_in"][0, 0], q.T @ dO + dSf[0, 0], rtol=1e-10, atol=1e-12)
+    dgam = np.zeros(T)
+    for t in range(T):
+        S_prev = S_in[0, 0] + sum(eta[s] * np.outer(k[s], v[s]) for s in range(t))
+        dS_t = q[t:].T @ dO[t:] + dSf[0, 0]
+        dgam[t] = (dS_t * S_prev).sum()
+    assert np.allclose(g["dlam"][0, :, 0], -dgam, rtol=1e-9, atol=1e-11)
