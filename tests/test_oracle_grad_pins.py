@@ -14,7 +14,8 @@ G4  the window variants (Falcon-3/3A): G1 and G2 with a carried window ring
 G5  closed forms: Falcon-1A without decay and with same-step pairs is causal
     linear attention weighted by eta, o_t = sum_{s<=t} eta_s (q_t . k_s) v_s,
     whose value, query, beta, key, carried-state and decay gradients are
-    written out with causal masks
+    written out with causal masks; and one Falcon-1 (regression) step from a
+    carried state, every gradient derived by hand
 """
 
 import numpy as np
@@ -252,3 +253,46 @@ def test_g5_linear_attention_closed_forms_keys_state_decay():
         dS_t = q[t:].T @ dO[t:] + dSf[0, 0]
         dgam[t] = (dS_t * S_prev).sum()
     assert np.allclose(g["dlam"][0, :, 0], -dgam, rtol=1e-9, atol=1e-11)
+
+
+def test_g5_one_regression_step_closed_forms():
+    """One Falcon-1 step from a carried state, same-step pair x = k_0 [FW
+    Falcon 家族; JC Falcon家族六个变体各管一段]: with gamma the clamped decay,
+    eta = beta / (eps + |x|^2), r = v - gamma S0^T x,
+      S1 = gamma S0 + eta x r^T = gamma (I - eta x x^T) S0 + eta x v^T,  o = S1^T q,
+    and G = dS1 = q do^T + dS_final, the gradients written out by hand:
+      dq = S1 do,  dv = eta G^T x,  dS0 = gamma (I - eta x x^T) G,
+      dgamma = <G, (I - eta x x^T) S0>  (dlambda = -dgamma inside the clamp),
+      dbeta = x^T G r / (eps + |x|^2),
+      dk = eta G v - eta gamma (G S0^T x + S0 G^T x) - 2 beta x (x^T G r) / (eps + |x|^2)^2."""
+    rng = np.random.default_rng(73)
+    d = 5
+    x = inputs(rng, 1, 1, 1, d, d, False)
+    do = rng.standard_normal((1, 1, 1, d))
+    dSf = rng.standard_normal((1, 1, d, d))
+    S0 = 0.5 * rng.standard_normal((1, 1, d, d))
+    eps, eps_g = 1e-6, 1e-3
+    g = O.recurrent_vjp(x["q"], x["k"], x["v"], x["beta"], x["lam"], O.FALCON_1, do, dSf, eps, eps_g,
+                        carry={"S": S0}, pairing="same")
+    q, k, v, dO = (a[0, 0, 0] for a in (x["q"], x["k"], x["v"], do))
+    beta, lam, S, Gf = x["beta"][0, 0, 0], x["lam"][0, 0, 0], S0[0, 0], dSf[0, 0]
+    gamma = min(max(1.0 - lam, eps_g), 1.0)
+    assert eps_g < 1.0 - lam < 1.0   # inside the clamp: the gradient passes
+    den = eps + k @ k
+    eta = beta / den
+    r = v - gamma * (S.T @ k)
+    P = np.eye(d) - eta * np.outer(k, k)
+    S1 = gamma * S + eta * np.outer(k, r)
+    G = np.outer(q, dO) + Gf
+    want = {
+        "dq": S1 @ dO,
+        "dv": eta * (G.T @ k),
+        "dS_in": gamma * (P @ G),
+        "dlam": -np.sum(G * (P @ S)),
+        "dbeta": (k @ G @ r) / den,
+        "dk": eta * (G @ v) - eta * gamma * (G @ S.T @ k + S @ G.T @ k) - 2 * beta * k * (k @ G @ r) / den ** 2,
+    }
+    got = {"dq": g["dq"][0, 0, 0], "dv": g["dv"][0, 0, 0], "dS_in": g["dS_in"][0, 0], "dlam": g["dlam"][0, 0, 0],
+           "dbeta": g["dbeta"][0, 0, 0], "dk": g["dk"][0, 0, 0]}
+    for n, w_ in want.items():
+        assert np.allclose(got[n], w_, rtol=1e-10, atol=1e-12), n
