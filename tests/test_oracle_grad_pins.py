@@ -14,8 +14,9 @@ G4  the window variants (Falcon-3/3A): G1 and G2 with a carried window ring
 G5  closed forms: Falcon-1A without decay and with same-step pairs is causal
     linear attention weighted by eta, o_t = sum_{s<=t} eta_s (q_t . k_s) v_s,
     whose value, query, beta, key, carried-state and decay gradients are
-    written out with causal masks; and one Falcon-1 (regression) step from a
-    carried state, every gradient derived by hand
+    written out with causal masks; and one Falcon-1 (regression) step and one
+    Falcon-2 (per-channel) step from a carried state, every gradient derived
+    by hand
 """
 
 import numpy as np
@@ -291,6 +292,49 @@ def test_g5_one_regression_step_closed_forms():
         "dlam": -np.sum(G * (P @ S)),
         "dbeta": (k @ G @ r) / den,
         "dk": eta * (G @ v) - eta * gamma * (G @ S.T @ k + S @ G.T @ k) - 2 * beta * k * (k @ G @ r) / den ** 2,
+    }
+    got = {"dq": g["dq"][0, 0, 0], "dv": g["dv"][0, 0, 0], "dS_in": g["dS_in"][0, 0], "dlam": g["dlam"][0, 0, 0],
+           "dbeta": g["dbeta"][0, 0, 0], "dk": g["dk"][0, 0, 0]}
+    for n, w_ in want.items():
+        assert np.allclose(got[n], w_, rtol=1e-10, atol=1e-12), n
+
+
+def test_g5_one_per_channel_step_closed_forms():
+    """One Falcon-2 step (per-channel step size, eta_j = beta_j / (eps + |x|^2)
+    for value channel j) from a carried state, same-step pair x = k_0:
+      S1 = gamma S0 + x (eta (.) (v - gamma S0^T x))^T = gamma (S0 - x x^T S0 D) + x v^T D,
+    D = diag(eta), G = q do^T + dS_final, r = v - gamma S0^T x:
+      dq = S1 do,  dv = D G^T x,  dS0 = gamma (G - x x^T G D),
+      dgamma = <G, S0 - x x^T S0 D>,  d eta_j = (G^T x)_j r_j,  dbeta_j = d eta_j / (eps + |x|^2),
+      dk = G D v - gamma (G D S0^T x + S0 D G^T x) - 2 x (sum_j d eta_j beta_j) / (eps + |x|^2)^2."""
+    rng = np.random.default_rng(74)
+    d = 5
+    x = inputs(rng, 1, 1, 1, d, d, True)
+    do = rng.standard_normal((1, 1, 1, d))
+    dSf = rng.standard_normal((1, 1, d, d))
+    S0 = 0.5 * rng.standard_normal((1, 1, d, d))
+    eps, eps_g = 1e-6, 1e-3
+    g = O.recurrent_vjp(x["q"], x["k"], x["v"], x["beta"], x["lam"], O.FALCON_2, do, dSf, eps, eps_g,
+                        carry={"S": S0}, pairing="same")
+    q, k, v, dO = (a[0, 0, 0] for a in (x["q"], x["k"], x["v"], do))
+    beta, lam, S, Gf = x["beta"][0, 0, 0], x["lam"][0, 0, 0], S0[0, 0], dSf[0, 0]
+    gamma = min(max(1.0 - lam, eps_g), 1.0)
+    assert eps_g < 1.0 - lam < 1.0
+    den = eps + k @ k
+    eta = beta / den
+    D = np.diag(eta)
+    r = v - gamma * (S.T @ k)
+    S1 = gamma * S + np.outer(k, eta * r)
+    G = np.outer(q, dO) + Gf
+    deta = (G.T @ k) * r
+    xx = np.outer(k, k)
+    want = {
+        "dq": S1 @ dO,
+        "dv": D @ G.T @ k,
+        "dS_in": gamma * (G - xx @ G @ D),
+        "dlam": -np.sum(G * (S - xx @ S @ D)),
+        "dbeta": deta / den,
+        "dk": G @ D @ v - gamma * (G @ D @ S.T @ k + S @ D @ G.T @ k) - 2 * k * (deta @ beta) / den ** 2,
     }
     got = {"dq": g["dq"][0, 0, 0], "dv": g["dv"][0, 0, 0], "dS_in": g["dS_in"][0, 0], "dlam": g["dlam"][0, 0, 0],
            "dbeta": g["dbeta"][0, 0, 0], "dk": g["dk"][0, 0, 0]}
