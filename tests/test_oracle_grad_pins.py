@@ -14,9 +14,10 @@ G4  the window variants (Falcon-3/3A): G1 and G2 with a carried window ring
 G5  closed forms: Falcon-1A without decay and with same-step pairs is causal
     linear attention weighted by eta, o_t = sum_{s<=t} eta_s (q_t . k_s) v_s,
     whose value, query, beta, key, carried-state and decay gradients are
-    written out with causal masks; and one Falcon-1 (regression) step and one
-    Falcon-2 (per-channel) step from a carried state, every gradient derived
-    by hand
+    written out with causal masks; and one Falcon-1 (regression) step, one
+    Falcon-2 (per-channel) step and one Falcon-3 (window of two pairs, one of
+    them from the carried ring) step from a carried state, every gradient
+    derived by hand
 """
 
 import numpy as np
@@ -340,3 +341,61 @@ def test_g5_one_per_channel_step_closed_forms():
            "dbeta": g["dbeta"][0, 0, 0], "dk": g["dk"][0, 0, 0]}
     for n, w_ in want.items():
         assert np.allclose(got[n], w_, rtol=1e-10, atol=1e-12), n
+
+
+def test_g5_one_window_step_closed_forms():
+    """One Falcon-3 step with W = 2 and same-step pairs [FW Falcon 家族; JC
+    Falcon家族六个变体各管一段]: the window holds the carried ring pair a
+    (x_a, v_a) and the step's own pair b (k_0, v_0), both existing (pos = 3),
+    n = 2, e = (|x_a|^2 + |x_b|^2) / 2, eta = beta / (eps + e), c = eta / n,
+    r_i = v_i - gamma S0^T x_i, and
+      S1 = gamma S0 + c sum_i x_i r_i^T = gamma (I - c X) S0 + c sum_i x_i v_i^T,  X = sum_i x_i x_i^T.
+    With G = q do^T + dS_final and dc = sum_i x_i^T G r_i:
+      dq = S1 do,  dv_i = c G^T x_i,  dS0 = gamma (I - c X) G,
+      dgamma = <G, (I - c X) S0>,  dbeta = dc / (n (eps + e)),
+      dx_i = c (G r_i - gamma S0 G^T x_i) - (dc / n) eta / (eps + e) (2 x_i / n),
+    dk_0 = dx_b and the ring entry's gradients dx_a, dv_a."""
+    rng = np.random.default_rng(75)
+    d, W = 4, 2
+    x = inputs(rng, 1, 1, 1, d, d, False)
+    do = rng.standard_normal((1, 1, 1, d))
+    dSf = rng.standard_normal((1, 1, d, d))
+    S0 = 0.5 * rng.standard_normal((1, 1, d, d))
+    xa = rng.standard_normal((1, 1, W - 1, d)) / np.sqrt(d)
+    va = rng.standard_normal((1, 1, W - 1, d))
+    eps, eps_g = 1e-6, 1e-3
+    carry = {"S": S0, "pos": np.array([[3]], dtype=np.int64), "win_x": xa, "win_v": va}
+    g = O.recurrent_vjp(x["q"], x["k"], x["v"], x["beta"], x["lam"], O.FALCON_3, do, dSf, eps, eps_g,
+                        carry=carry, pairing="same", window=W)
+    q, kb, vb, dO = (a[0, 0, 0] for a in (x["q"], x["k"], x["v"], do))
+    beta, lam, S, Gf = x["beta"][0, 0, 0], x["lam"][0, 0, 0], S0[0, 0], dSf[0, 0]
+    pa, qa = xa[0, 0, 0], va[0, 0, 0]
+    gamma = min(max(1.0 - lam, eps_g), 1.0)
+    assert eps_g < 1.0 - lam < 1.0
+    n = 2.0
+    e = (pa @ pa + kb @ kb) / n
+    eta = beta / (eps + e)
+    c = eta / n
+    X = np.outer(pa, pa) + np.outer(kb, kb)
+    I = np.eye(d)
+    ra, rb = qa - gamma * (S.T @ pa), vb - gamma * (S.T @ kb)
+    S1 = gamma * (I - c * X) @ S + c * (np.outer(pa, qa) + np.outer(kb, vb))
+    G = np.outer(q, dO) + Gf
+    dc = pa @ G @ ra + kb @ G @ rb
+    de = -(dc / n) * eta / (eps + e)
+    dx = lambda xi, ri: c * (G @ ri - gamma * S @ G.T @ xi) + de * 2 * xi / n
+    want = {
+        "dq": S1 @ dO,
+        "dv": c * (G.T @ kb),
+        "dS_in": gamma * (I - c * X) @ G,
+        "dlam": -np.sum(G * ((I - c * X) @ S)),
+        "dbeta": dc / (n * (eps + e)),
+        "dk": dx(kb, rb),
+        "dwin_x": dx(pa, ra),
+        "dwin_v": c * (G.T @ pa),
+    }
+    got = {"dq": g["dq"][0, 0, 0], "dv": g["dv"][0, 0, 0], "dS_in": g["dS_in"][0, 0], "dlam": g["dlam"][0, 0, 0],
+           "dbeta": g["dbeta"][0, 0, 0], "dk": g["dk"][0, 0, 0], "dwin_x": g["dwin_x"][0, 0, 0],
+           "dwin_v": g["dwin_v"][0, 0, 0]}
+    for nme, w_ in want.items():
+        assert np.allclose(got[nme], w_, rtol=1e-10, atol=1e-12), nme
