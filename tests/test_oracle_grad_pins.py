@@ -343,7 +343,8 @@ def test_g5_one_per_channel_step_closed_forms():
         assert np.allclose(got[n], w_, rtol=1e-10, atol=1e-12), n
 
 
-def test_g5_one_window_step_closed_forms():
+@pytest.mark.parametrize("variant", [O.FALCON_3, O.FALCON_3A])
+def test_g5_one_window_step_closed_forms(variant):
     """One Falcon-3 step with W = 2 and same-step pairs [FW Falcon 家族; JC
     Falcon家族六个变体各管一段]: the window holds the carried ring pair a
     (x_a, v_a) and the step's own pair b (k_0, v_0), both existing (pos = 3),
@@ -354,7 +355,9 @@ def test_g5_one_window_step_closed_forms():
       dq = S1 do,  dv_i = c G^T x_i,  dS0 = gamma (I - c X) G,
       dgamma = <G, (I - c X) S0>,  dbeta = dc / (n (eps + e)),
       dx_i = c (G r_i - gamma S0 G^T x_i) - (dc / n) eta / (eps + e) (2 x_i / n),
-    dk_0 = dx_b and the ring entry's gradients dx_a, dv_a."""
+    dk_0 = dx_b and the ring entry's gradients dx_a, dv_a.  Falcon-3A writes
+    additively: r_i = v_i, so the gamma S0^T x_i terms drop (dS0 = gamma G,
+    dgamma = <G, S0>, dx_i = c G v_i + the e term)."""
     rng = np.random.default_rng(75)
     d, W = 4, 2
     x = inputs(rng, 1, 1, 1, d, d, False)
@@ -365,8 +368,9 @@ def test_g5_one_window_step_closed_forms():
     va = rng.standard_normal((1, 1, W - 1, d))
     eps, eps_g = 1e-6, 1e-3
     carry = {"S": S0, "pos": np.array([[3]], dtype=np.int64), "win_x": xa, "win_v": va}
-    g = O.recurrent_vjp(x["q"], x["k"], x["v"], x["beta"], x["lam"], O.FALCON_3, do, dSf, eps, eps_g,
+    g = O.recurrent_vjp(x["q"], x["k"], x["v"], x["beta"], x["lam"], variant, do, dSf, eps, eps_g,
                         carry=carry, pairing="same", window=W)
+    add = variant == O.FALCON_3A
     q, kb, vb, dO = (a[0, 0, 0] for a in (x["q"], x["k"], x["v"], do))
     beta, lam, S, Gf = x["beta"][0, 0, 0], x["lam"][0, 0, 0], S0[0, 0], dSf[0, 0]
     pa, qa = xa[0, 0, 0], va[0, 0, 0]
@@ -376,14 +380,15 @@ def test_g5_one_window_step_closed_forms():
     e = (pa @ pa + kb @ kb) / n
     eta = beta / (eps + e)
     c = eta / n
-    X = np.outer(pa, pa) + np.outer(kb, kb)
+    X = np.zeros((d, d)) if add else np.outer(pa, pa) + np.outer(kb, kb)  # the residual's S0 term
     I = np.eye(d)
-    ra, rb = qa - gamma * (S.T @ pa), vb - gamma * (S.T @ kb)
+    sg = 0.0 if add else gamma
+    ra, rb = qa - sg * (S.T @ pa), vb - sg * (S.T @ kb)
     S1 = gamma * (I - c * X) @ S + c * (np.outer(pa, qa) + np.outer(kb, vb))
     G = np.outer(q, dO) + Gf
     dc = pa @ G @ ra + kb @ G @ rb
     de = -(dc / n) * eta / (eps + e)
-    dx = lambda xi, ri: c * (G @ ri - gamma * S @ G.T @ xi) + de * 2 * xi / n
+    dx = lambda xi, ri: c * (G @ ri - sg * S @ G.T @ xi) + de * 2 * xi / n
     want = {
         "dq": S1 @ dO,
         "dv": c * (G.T @ kb),
